@@ -1,0 +1,284 @@
+"""Plain float64 CPU oracle for the RidgeFill upper-layer KV fill, its calibration
+statistics and closed-form ridge solve, and the cross-model per-head ridge mapper.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports, calls or links this
+module: only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+use it. It shares no code with the CUDA library (no kernels, headers, tables or
+helpers); the two meet only through the seeded input generators in ``synth/``.
+
+Every function restates one definition from the pages, in float64, with numpy's
+matmul, ``linalg.solve`` and elementwise math as the only library steps. There is no
+blocking, fusion or reordering beyond what the definition states. Inputs arrive as
+the same bf16 bit patterns the GPU receives and are decoded exactly.
+
+Sources (cited by page and section):
+  [RF] RidgeFill review, jaehun.me, English edition ("Paper: RidgeFill" review of
+       arXiv 2611.09709). Sections "Two numbers set the skip range", "Ridge map:
+       predict the input, and the original projection runs unchanged", Table 2
+       (notation), Table 3 (the four arms), the worked example "A small example:
+       how one row lands in the cache".
+  [XM] "Cross-Model KV Cache Transfer in LLM Families: A Closed-Form Linear Mapping
+       for Prefill Reuse" (digest, seosoyoung.eiaserinnys.me). Sections "헤드별 리지
+       회귀" (per-head ridge regression), "층 교차 소스 선택" (cross-layer source
+       selection), "RoPE를 제거한 내용 공간 매핑" (content-space mapping, equation
+       for K̂_t).
+
+Readings where the pages leave a step open (each is listed in the design doc):
+  * x_S is the residual stream entering layer S; one map per layer l in [S, L).
+  * RMSNorm is y = g * x / sqrt(mean(x^2) + eps); K/V projections have no bias.
+  * RoPE is the rotate-half form: pair (i, i + hd/2), inv_freq_i = theta^(-2i/hd),
+    angle = position * inv_freq_i, position = row index + pos_offset.
+  * Calibration sums are raw one-pass sums; they are centred at solve time.
+  * alpha = lambda * tr(Gc) / d_in by default ("trace" mode), or alpha = lambda.
+  * The cross-model bias is b = mu_Y - W mu_X (centred-ridge identity).
+
+Parity status: every public function here is pinned by tests/test_oracle_pins.py
+against closed forms, invariants, textbook routines or brute force; none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "bf16_bits_to_f64", "rope_inv_freq", "rope", "rms_norm", "prefix_partition",
+    "map_predict", "fill_rows", "fill_kv", "calib_stats", "centre_stats",
+    "ridge_alpha", "ridge_solve", "xmodel_features", "xmodel_map_layer",
+    "fill_flops_per_row_layer",
+]
+
+
+# --------------------------------------------------------------------------- #
+# Number format
+# --------------------------------------------------------------------------- #
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Decode bfloat16 bit patterns (uint16 / int16 arrays) exactly to float64.
+
+    A bf16 value is the upper 16 bits of an IEEE binary32, so widening the bit
+    pattern by 16 zero bits and reinterpreting as float32 is exact.
+    """
+    u = np.asarray(bits).view(np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------- #
+# RoPE and RMSNorm: the layer's own operations that run unchanged on the
+# predicted input ([RF] "Ridge map ... the original projection runs unchanged").
+# --------------------------------------------------------------------------- #
+def rope_inv_freq(head_dim: int, theta: float) -> np.ndarray:
+    """Rotary inverse frequencies theta^(-2i/hd), i = 0 .. hd/2 - 1 (float64)."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return np.power(np.float64(theta), -2.0 * i / head_dim)
+
+
+def rope(x: np.ndarray, positions, theta: float, inverse: bool = False) -> np.ndarray:
+    """Rotate-half RoPE over the last axis of ``x`` (length hd).
+
+    Pair (i, i + hd/2) is rotated by angle pos * inv_freq_i. ``positions`` must
+    broadcast against ``x.shape[:-1]``. ``inverse=True`` applies R^-1 (the
+    "unrope" of [XM] content-space mapping).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    hd = x.shape[-1]
+    half = hd // 2
+    pos = np.asarray(positions, dtype=np.float64)[..., None]
+    ang = pos * rope_inv_freq(hd, theta)
+    c, s = np.cos(ang), np.sin(ang)
+    if inverse:
+        s = -s
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def rms_norm(x: np.ndarray, gain: np.ndarray, eps: float) -> np.ndarray:
+    """y = g * x / sqrt(mean(x^2) + eps) over the last axis."""
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return np.asarray(gain, dtype=np.float64) * x / np.sqrt(ms + eps)
+
+
+# --------------------------------------------------------------------------- #
+# Bookkeeping: which rows are filled ([RF] "Two numbers set the skip range")
+# --------------------------------------------------------------------------- #
+def prefix_partition(N: int, T: int, exact_mask=None) -> np.ndarray:
+    """Rows filled by the map: prefix rows t < N - T that are not exact rows.
+
+    Layers < S run for every row, the last T rows run every layer, and an exact
+    prefix row runs every layer; the rest of the prefix is filled. Returned in
+    ascending order (int64).
+    """
+    n_prefix = N - T
+    if exact_mask is None:
+        return np.arange(n_prefix, dtype=np.int64)
+    m = np.asarray(exact_mask).astype(bool)
+    assert m.shape == (n_prefix,)
+    return np.nonzero(~m)[0].astype(np.int64)
+
+
+# --------------------------------------------------------------------------- #
+# The fill ([RF] "Ridge map", equation x̂_l = A_l x_S + b_l, and Fig. 2)
+# --------------------------------------------------------------------------- #
+def map_predict(x_S: np.ndarray, A_l: np.ndarray, b_l: np.ndarray) -> np.ndarray:
+    """x̂_l = A_l x_S + b_l for each row of ``x_S`` ([n, d_in] -> [n, d_out])."""
+    return np.asarray(x_S, np.float64) @ np.asarray(A_l, np.float64).T + np.asarray(b_l, np.float64)
+
+
+def fill_rows(x_S_rows, positions, A, b, gain, Wk, Wv, n_kv_heads, head_dim,
+              rope_theta, rms_eps):
+    """Filled keys and values for a set of rows and every upper layer.
+
+    For each row t and upper layer l (index p = l - S):
+        x̂ = A_p x_S[t] + b_p
+        y  = g_p * x̂ / sqrt(mean(x̂^2) + eps)
+        k  = Wk_p y,  v = Wv_p y          (the layer's own projections)
+        k_h <- RoPE(k_h, position_t)      (per KV head)
+
+    Shapes: x_S_rows [n, d]; positions [n]; A [P, d, d]; b [P, d]; gain [P, d];
+    Wk, Wv [P, H*hd, d]. Returns K, V as [P, n, H, hd] float64.
+    """
+    x = np.asarray(x_S_rows, np.float64)
+    n = x.shape[0]
+    P = A.shape[0]
+    K = np.empty((P, n, n_kv_heads, head_dim))
+    V = np.empty((P, n, n_kv_heads, head_dim))
+    pos = np.asarray(positions, np.float64)
+    for p in range(P):
+        xhat = map_predict(x, A[p], b[p])
+        y = rms_norm(xhat, gain[p], rms_eps)
+        k = (y @ np.asarray(Wk[p], np.float64).T).reshape(n, n_kv_heads, head_dim)
+        v = (y @ np.asarray(Wv[p], np.float64).T).reshape(n, n_kv_heads, head_dim)
+        K[p] = rope(k, pos[:, None], rope_theta)
+        V[p] = v
+    return K, V
+
+
+def fill_kv(k_cache, v_cache, x_S, exact_mask, A, b, gain, Wk, Wv, *, L, S, N, T,
+            n_kv_heads, head_dim, rope_theta, rms_eps, pos_offset=0):
+    """Whole-cache fill: returns (new_k_cache, new_v_cache, fill_idx).
+
+    Caches are [L, N_cap, H, hd] arrays (float64 copies of the input caches).
+    Only cache[l][t] for l in [S, L) and t in fill_idx is replaced; every other
+    entry keeps its input value ([RF] Table 3: exact rows and the tail run the
+    real layers, the no-fill arm writes nothing).
+    """
+    assert A.shape[0] == L - S
+    idx = prefix_partition(N, T, exact_mask)
+    kc = np.array(k_cache, dtype=np.float64, copy=True)
+    vc = np.array(v_cache, dtype=np.float64, copy=True)
+    if idx.size and L > S:
+        K, V = fill_rows(np.asarray(x_S, np.float64)[idx], idx + pos_offset, A, b, gain,
+                         Wk, Wv, n_kv_heads, head_dim, rope_theta, rms_eps)
+        for p in range(L - S):
+            kc[S + p][idx] = K[p]
+            vc[S + p][idx] = V[p]
+    return kc, vc, idx
+
+
+def fill_flops_per_row_layer(d: int, n_kv_heads: int, head_dim: int) -> int:
+    """Algorithmic flops for one filled (row, layer): the map (2 d^2) plus the
+    K and V projections (2 * d * 2 * H * hd). Norm, RoPE and bias are O(d)."""
+    kv = n_kv_heads * head_dim
+    return 2 * d * d + 2 * d * (2 * kv)
+
+
+# --------------------------------------------------------------------------- #
+# Calibration and the closed-form ridge solve ([RF] "Ridge map": objective,
+# closed form, alpha = lambda tr(XᵀX)/d_in, one-pass statistics)
+# --------------------------------------------------------------------------- #
+def calib_stats(X, Ys) -> dict:
+    """Raw one-pass sums over the rows of X [n, d_in] and Ys [P, n, d_out].
+
+    G = Σ_t x_t x_tᵀ,  C_p = Σ_t x_t y_{p,t}ᵀ,  sx = Σ_t x_t,  sy_p = Σ_t y_{p,t},  n.
+    """
+    X = np.asarray(X, np.float64)
+    Ys = np.asarray(Ys, np.float64)
+    return {
+        "G": X.T @ X,
+        "C": np.stack([X.T @ Ys[p] for p in range(Ys.shape[0])]),
+        "sx": X.sum(axis=0),
+        "sy": Ys.sum(axis=1),
+        "n": int(X.shape[0]),
+    }
+
+
+def add_stats(a: dict, b: dict) -> dict:
+    """Sum of two sets of raw statistics (calibration is resumable by adding)."""
+    return {k: a[k] + b[k] for k in ("G", "C", "sx", "sy", "n")}
+
+
+def centre_stats(st: dict):
+    """Centred Gram and cross terms from raw sums.
+
+    mu_x = sx/n, mu_p = sy_p/n, Gc = G - n mu_x mu_xᵀ, Cc_p = C_p - n mu_x mu_pᵀ.
+    These equal Σ (x - mu_x)(x - mu_x)ᵀ and Σ (x - mu_x)(y_p - mu_p)ᵀ.
+    """
+    n = float(st["n"])
+    mu_x = st["sx"] / n
+    mu_y = st["sy"] / n
+    Gc = st["G"] - n * np.outer(mu_x, mu_x)
+    Cc = st["C"] - n * np.einsum("i,pj->pij", mu_x, mu_y)
+    return Gc, Cc, mu_x, mu_y
+
+
+def ridge_alpha(Gc: np.ndarray, lam: float, mode: str = "trace") -> float:
+    """alpha = lambda * tr(XᵀX)/d_in (centred X) in "trace" mode, else alpha = lambda."""
+    if mode == "trace":
+        return float(lam) * float(np.trace(Gc)) / Gc.shape[0]
+    if mode == "absolute":
+        return float(lam)
+    raise ValueError(mode)
+
+
+def ridge_solve(st: dict, lam: float, alpha_mode: str = "trace"):
+    """A_p = Y_pᵀX (XᵀX + alpha I)^-1 and b_p = mu_p - A_p mu_x for every map p.
+
+    With centred data, Y_pᵀX = Cc_pᵀ and XᵀX = Gc, so A_pᵀ solves
+    (Gc + alpha I) A_pᵀ = Cc_p. Returns A [P, d_out, d_in], b [P, d_out], alpha.
+    """
+    Gc, Cc, mu_x, mu_y = centre_stats(st)
+    alpha = ridge_alpha(Gc, lam, alpha_mode)
+    H = Gc + alpha * np.eye(Gc.shape[0])
+    P = Cc.shape[0]
+    A = np.empty((P, Cc.shape[2], Cc.shape[1]))
+    b = np.empty((P, Cc.shape[2]))
+    for p in range(P):
+        A[p] = np.linalg.solve(H, Cc[p]).T
+        b[p] = mu_y[p] - A[p] @ mu_x
+    return A, b, alpha
+
+
+# --------------------------------------------------------------------------- #
+# Cross-model mapper ([XM] content-space mapping K̂_t = (K_s R_s^-1(t) W_K + b_K) R_t(t);
+# V is mapped without RoPE; source layers of a target layer are concatenated)
+# --------------------------------------------------------------------------- #
+def xmodel_features(src_cache, src_layers, positions, theta_src=None):
+    """Concatenated features of the selected source layers for each row.
+
+    ``src_cache`` is [L_src, n, H, hd]. With ``theta_src`` given (keys), each
+    selected layer is un-roped at the row's position first; with None (values)
+    the cache is used as is. Feature order: selected layer j, then head h, then
+    dim c. Returns [n, k*H*hd].
+    """
+    parts = []
+    for s in src_layers:
+        blk = np.asarray(src_cache[s], np.float64)
+        if theta_src is not None:
+            blk = rope(blk, np.asarray(positions, np.float64)[:, None], theta_src, inverse=True)
+        parts.append(blk.reshape(blk.shape[0], -1))
+    return np.concatenate(parts, axis=1)
+
+
+def xmodel_map_layer(k_src, v_src, src_layers, Wk, bk, Wv, bv, positions,
+                     theta_src, theta_tgt, n_kv_heads, head_dim):
+    """One target layer of the cross-model mapper.
+
+    K̂ = RoPE_tgt(F_K Wkᵀ + bk) with F_K the un-roped source keys; V̂ = F_V Wvᵀ + bv.
+    Wk, Wv are [H*hd, k*H*hd] (output x input). Returns K̂, V̂ as [n, H, hd].
+    """
+    FK = xmodel_features(k_src, src_layers, positions, theta_src)
+    FV = xmodel_features(v_src, src_layers, positions, None)
+    n = FK.shape[0]
+    kc = (FK @ np.asarray(Wk, np.float64).T + np.asarray(bk, np.float64)).reshape(n, n_kv_heads, head_dim)
+    vh = (FV @ np.asarray(Wv, np.float64).T + np.asarray(bv, np.float64)).reshape(n, n_kv_heads, head_dim)
+    kh = rope(kc, np.asarray(positions, np.float64)[:, None], theta_tgt)
+    return kh, vh

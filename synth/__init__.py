@@ -1,0 +1,255 @@
+"""Seeded synthetic inputs shaped like the pages' deployments.
+
+This module holds workload shapes and random-number recipes only; it contains
+none of the method's arithmetic (no map, norm, projection, RoPE or solve). Both
+the fp64 oracle and the CUDA library receive the bf16 tensors made here, so the
+two sides see identical bit patterns.
+
+Recipe (one per workload):
+  * x_S ~ N(0, 1); maps A = I + N(0, 0.02^2/d) and offsets b ~ N(0, 0.1^2), one
+    per upper layer; RMSNorm gains 1 + 0.1 N(0, 1); W_k, W_v ~ N(0, 1/d); all cast
+    to bf16 (b stays fp32).
+  * calibration rows: x ~ N(0, 1), y_l = A_true,l x + b_true,l + 0.05 N(0, 1).
+  * exact-row masks: the toy's rows {4, 5, 6, 7}; "uniform 10%": exactly
+    round(0.10 (N - T)) rows by a seeded permutation; "blocks of 16, 5%":
+    round(0.05 (N - T)/16) aligned 16-row blocks chosen without replacement.
+  * cross-model: source K, V ~ N(0, 1), W ~ N(0, 1/(k H hd)), b ~ N(0, 0.1^2);
+    target layer j reads the k consecutive source layers starting at
+    clamp(round(j (L_src - 1)/(L_tgt - 1)) - k/2 + 1, 0, L_src - k).
+Seeds: base = 20261202 + workload index; one sub-seed per named tensor.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+BASE_SEED = 20261202
+
+
+@dataclasses.dataclass(frozen=True)
+class FillConfig:
+    name: str
+    index: int
+    d: int
+    L: int
+    S: int
+    N: int
+    T: int
+    H: int
+    hd: int
+    rope_theta: float
+    exact: object            # tuple of rows, "uniform10", "blocks16_5", or None
+    lam: float
+    calib_n: int
+    rms_eps: float = 1e-5
+    pos_offset: int = 0
+
+    @property
+    def P(self) -> int:
+        return self.L - self.S
+
+    @property
+    def KV(self) -> int:
+        return self.H * self.hd
+
+    def with_layers(self, n_upper: int) -> "FillConfig":
+        """Same shapes with only the top ``n_upper`` layers filled (S = L - n_upper)."""
+        return dataclasses.replace(self, S=self.L - n_upper)
+
+    def with_rows(self, N: int, T: int) -> "FillConfig":
+        return dataclasses.replace(self, N=N, T=T)
+
+
+@dataclasses.dataclass(frozen=True)
+class XModelConfig:
+    name: str
+    index: int
+    L_src: int
+    L_tgt: int
+    k: int
+    H: int
+    hd: int
+    N: int
+    theta_src: float
+    theta_tgt: float
+    calib_n: int
+    lam: float
+    pos_offset: int = 0
+
+    @property
+    def KV(self) -> int:
+        return self.H * self.hd
+
+    @property
+    def d_in(self) -> int:
+        return self.k * self.H * self.hd
+
+
+TOY = FillConfig("toy-8layer d256", 0, d=256, L=8, S=4, N=12, T=3, H=2, hd=64,
+                 rope_theta=5.0e5, exact=(4, 5, 6, 7), lam=0.03, calib_n=2048)
+LLAMA8B = FillConfig("llama3.1-8b-shaped d4096 L32 S12 N16384 T4096", 1, d=4096, L=32, S=12,
+                     N=16384, T=4096, H=8, hd=128, rope_theta=5.0e5, exact="uniform10",
+                     lam=0.03, calib_n=8192)
+QWEN3_8B = FillConfig("qwen3-8b-shaped d4096 L36 S13 N32768 T4096", 2, d=4096, L=36, S=13,
+                      N=32768, T=4096, H=8, hd=128, rope_theta=1.0e6, exact=None,
+                      lam=0.01, calib_n=8192)
+DENSE27B = FillConfig("27b-shaped d5120 L64 S16 N32768 T4096", 3, d=5120, L=64, S=16,
+                      N=32768, T=4096, H=8, hd=128, rope_theta=1.0e6, exact="blocks16_5",
+                      lam=0.03, calib_n=16384)
+XMODEL = XModelConfig("xmodel 40->64 layers 8x128 k8 N32768", 4, L_src=40, L_tgt=64, k=8,
+                      H=8, hd=128, N=32768, theta_src=1.0e6, theta_tgt=1.0e6,
+                      calib_n=131072, lam=0.01)
+
+FILL_CONFIGS = {"toy": TOY, "llama8b": LLAMA8B, "qwen3_8b": QWEN3_8B, "dense27b": DENSE27B}
+
+_TENSOR_IDS = {name: i for i, name in enumerate(
+    ["x_S", "mask", "A", "b", "gain", "Wk", "Wv", "calib_X", "calib_Atrue", "calib_btrue",
+     "calib_noise", "k_src", "v_src", "xWk", "xWv", "xbk", "xbv", "cache", "extra"])}
+
+
+def sub_seed(index: int, tensor: str, salt: int = 0) -> int:
+    return (BASE_SEED + index) * 1009 + _TENSOR_IDS[tensor] * 101 + salt
+
+
+def _gen(device, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _randn(shape, seed, device, std=1.0, mean=0.0, dtype=torch.bfloat16, chunk_rows=None):
+    """N(mean, std^2) in float32, then cast to ``dtype``; generated in slabs along
+    dim 0 so that large tensors never need a full float32 copy."""
+    shape = tuple(int(s) for s in shape)
+    out = torch.empty(shape, dtype=dtype, device=device)
+    g = _gen(device, seed)
+    if len(shape) == 0 or shape[0] == 0:
+        return out
+    per = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+    step = chunk_rows or max(1, (1 << 26) // max(per, 1))
+    for i in range(0, shape[0], step):
+        j = min(shape[0], i + step)
+        t = torch.randn((j - i,) + shape[1:], generator=g, device=device, dtype=torch.float32)
+        if std != 1.0:
+            t.mul_(std)
+        if mean != 0.0:
+            t.add_(mean)
+        out[i:j] = t.to(dtype)
+    return out
+
+
+def exact_mask(cfg: FillConfig, device="cpu", seed: Optional[int] = None) -> Optional[torch.Tensor]:
+    """uint8 [N - T] mask, 1 = exact prefix row (never filled); None = no exact rows."""
+    n_prefix = cfg.N - cfg.T
+    if cfg.exact is None:
+        return None
+    m = torch.zeros(n_prefix, dtype=torch.uint8)
+    seed = sub_seed(cfg.index, "mask") if seed is None else seed
+    g = _gen("cpu", seed)
+    if isinstance(cfg.exact, (tuple, list)):
+        rows = [r for r in cfg.exact if r < n_prefix]
+        m[list(rows)] = 1
+    elif cfg.exact == "uniform10":
+        k = int(round(0.10 * n_prefix))
+        m[torch.randperm(n_prefix, generator=g)[:k]] = 1
+    elif cfg.exact == "blocks16_5":
+        nb = n_prefix // 16
+        k = int(round(0.05 * nb))
+        for blk in torch.randperm(nb, generator=g)[:k].tolist():
+            m[blk * 16:(blk + 1) * 16] = 1
+    else:
+        raise ValueError(cfg.exact)
+    return m.to(device)
+
+
+def fill_inputs(cfg: FillConfig, device="cpu", with_mask=True) -> dict:
+    """Inputs of one fill: x_S [N, d], mask [N-T] (or None), maps A [P, d, d],
+    offsets b [P, d] (fp32), gains [P, d], W_k and W_v [P, H*hd, d]."""
+    P, d, KV = cfg.P, cfg.d, cfg.KV
+    ix = cfg.index
+    A = _randn((P, d, d), sub_seed(ix, "A"), device, std=0.02 / math.sqrt(d))
+    eye = torch.eye(d, dtype=torch.float32, device=device)
+    for p in range(P):
+        A[p] = (A[p].float() + eye).to(torch.bfloat16)
+    return {
+        "x_S": _randn((cfg.N, d), sub_seed(ix, "x_S"), device),
+        "mask": exact_mask(cfg, device) if with_mask else None,
+        "A": A,
+        "b": _randn((P, d), sub_seed(ix, "b"), device, std=0.1, dtype=torch.float32),
+        "gain": _randn((P, d), sub_seed(ix, "gain"), device, std=0.1, mean=1.0),
+        "Wk": _randn((P, KV, d), sub_seed(ix, "Wk"), device, std=1.0 / math.sqrt(d)),
+        "Wv": _randn((P, KV, d), sub_seed(ix, "Wv"), device, std=1.0 / math.sqrt(d)),
+    }
+
+
+def calib_inputs(d_in: int, d_out: int, n_maps: int, n_rows: int, index: int, device="cpu",
+                 noise: float = 0.05, salt: int = 0) -> dict:
+    """Planted calibration rows: X [n, d_in] ~ N(0,1); Y [P, n, d_out] with
+    y_p = A_true,p x + b_true,p + noise * N(0,1), everything rounded to bf16."""
+    X = _randn((n_rows, d_in), sub_seed(index, "calib_X", salt), device)
+    At = _randn((n_maps, d_out, d_in), sub_seed(index, "calib_Atrue", salt), device,
+                std=0.02 / math.sqrt(d_in), dtype=torch.float32)
+    for p in range(n_maps):
+        if d_out == d_in:
+            At[p].diagonal().add_(1.0)
+    bt = _randn((n_maps, d_out), sub_seed(index, "calib_btrue", salt), device, std=0.1,
+                dtype=torch.float32)
+    Y = torch.empty((n_maps, n_rows, d_out), dtype=torch.bfloat16, device=device)
+    gn = _gen(device, sub_seed(index, "calib_noise", salt))
+    Xf = X.float()
+    for p in range(n_maps):
+        e = torch.randn((n_rows, d_out), generator=gn, device=device, dtype=torch.float32)
+        Y[p] = (Xf @ At[p].T + bt[p] + noise * e).to(torch.bfloat16)
+    return {"X": X, "Y": Y, "A_true": At, "b_true": bt}
+
+
+def source_table(L_src: int, L_tgt: int, k: int) -> np.ndarray:
+    """int32 [L_tgt, k]: the k consecutive source layers each target layer reads."""
+    tab = np.empty((L_tgt, k), dtype=np.int32)
+    for j in range(L_tgt):
+        c = int(round(j * (L_src - 1) / max(L_tgt - 1, 1)))
+        s0 = min(max(c - k // 2 + 1, 0), L_src - k)
+        tab[j] = np.arange(s0, s0 + k, dtype=np.int32)
+    return tab
+
+
+def xmodel_inputs(cfg: XModelConfig, device="cpu", L_tgt: Optional[int] = None,
+                  N: Optional[int] = None) -> dict:
+    """Source caches [L_src, N, H, hd], mapper weights [L_tgt, KV, k*KV], biases."""
+    L_t = cfg.L_tgt if L_tgt is None else L_tgt
+    n = cfg.N if N is None else N
+    KV, din, ix = cfg.KV, cfg.d_in, cfg.index
+    return {
+        "k_src": _randn((cfg.L_src, n, cfg.H, cfg.hd), sub_seed(ix, "k_src"), device),
+        "v_src": _randn((cfg.L_src, n, cfg.H, cfg.hd), sub_seed(ix, "v_src"), device),
+        "Wk": _randn((L_t, KV, din), sub_seed(ix, "xWk"), device, std=1.0 / math.sqrt(din)),
+        "Wv": _randn((L_t, KV, din), sub_seed(ix, "xWv"), device, std=1.0 / math.sqrt(din)),
+        "bk": _randn((L_t, KV), sub_seed(ix, "xbk"), device, std=0.1, dtype=torch.float32),
+        "bv": _randn((L_t, KV), sub_seed(ix, "xbv"), device, std=0.1, dtype=torch.float32),
+        "src": source_table(cfg.L_src, cfg.L_tgt, cfg.k)[:L_t].copy(),
+    }
+
+
+def canary_cache(L: int, N_cap: int, H: int, hd: int, kind: int, device="cpu") -> torch.Tensor:
+    """bf16 cache filled with NaN canaries whose payload encodes (kind, l, t, h, c)
+    modulo the 6 free mantissa bits, so any stray write is visible bit for bit."""
+    l = torch.arange(L, dtype=torch.int32).view(L, 1, 1, 1)
+    t = torch.arange(N_cap, dtype=torch.int32).view(1, N_cap, 1, 1)
+    h = torch.arange(H, dtype=torch.int32).view(1, 1, H, 1)
+    c = torch.arange(hd, dtype=torch.int32).view(1, 1, 1, hd)
+    payload = (kind * 31 + l * 7 + t * 13 + h * 5 + c) % 63 + 1     # 1..63, never 0
+    bits = (0x7F80 | payload).to(torch.int16)                       # quiet-bit clear NaNs
+    return bits.view(torch.bfloat16).to(device)
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """Host numpy uint16 view of a bf16 tensor's bit patterns (no arithmetic)."""
+    return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu").contiguous().numpy()
