@@ -1,0 +1,238 @@
+/*
+ * rf.h — C ABI of librf.so: the RidgeFill upper-layer KV fill, its calibration
+ * statistics and closed-form ridge solve, and the cross-model per-head ridge
+ * mapper, for one NVIDIA GB300 (sm_103a).
+ *
+ * Sources cited below:
+ *   [RF] RidgeFill review (jaehun.me, English edition of the review of arXiv
+ *        2611.09709): "Two numbers set the skip range", "Ridge map: predict the
+ *        input, and the original projection runs unchanged", Table 3.
+ *   [XM] "Cross-Model KV Cache Transfer in LLM Families: A Closed-Form Linear
+ *        Mapping for Prefill Reuse" (digest): per-head ridge regression,
+ *        cross-layer source selection, content-space mapping equation.
+ *
+ * Conventions shared by every call
+ *   - Tensor arguments are DEVICE pointers owned by the caller, unless a comment
+ *     says "host". bf16 values are passed as their 16-bit patterns (rf_bf16).
+ *   - Every call is asynchronous on the caller's stream (a cudaStream_t passed
+ *     as rf_stream_t; NULL is the legacy default stream). No call synchronises
+ *     the host unless its comment says so.
+ *   - The library allocates no device memory. Calls that need scratch memory
+ *     take a caller workspace of at least rf_*_workspace_bytes(...) bytes,
+ *     256-byte aligned; its contents are undefined after the call. Calls that
+ *     share one workspace must be ordered on one stream.
+ *   - Argument errors are detected on the host before any launch and return a
+ *     status other than RF_OK; nothing is written then. rf_last_error() gives a
+ *     thread-local text for the last failing call on the calling thread.
+ *   - Errors found on the device (a bounded wait that gave up, a non-positive
+ *     Cholesky pivot) are written to the optional device int32 *dev_status
+ *     (first error wins; the caller zeroes it). A kernel that gives up returns
+ *     without touching the outputs it had not written yet.
+ *   - Functions are thread-safe; no call aborts the process or throws.
+ *   - Rows of every matrix are contiguous; "ld" arguments are row strides in
+ *     elements. Pointers must be 16-byte aligned and row/layer strides multiples
+ *     of 8 elements, else RF_ERR_ALIGN.
+ */
+#ifndef RIDGE_MAP_KV_RF_H
+#define RIDGE_MAP_KV_RF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rf_status {
+  RF_OK = 0,
+  RF_ERR_INVALID_ARG = 1,  /* null pointer, negative size, unknown mode        */
+  RF_ERR_SHAPE = 2,        /* sizes the kernels do not support                */
+  RF_ERR_ALIGN = 3,        /* pointer or stride alignment                      */
+  RF_ERR_CUDA = 4,         /* CUDA runtime error; text in rf_last_error()      */
+  RF_ERR_NOT_SPD = 5,      /* device status: Cholesky pivot <= 0               */
+  RF_ERR_TIMEOUT = 6,      /* device status: a bounded device wait gave up      */
+  RF_ERR_UNSUPPORTED = 7,  /* current device is not sm_100-family (tcgen05)    */
+  RF_ERR_WORKSPACE = 8     /* workspace missing, too small or misaligned       */
+} rf_status;
+
+typedef uint16_t rf_bf16;   /* bfloat16 bit pattern                             */
+typedef void* rf_stream_t;  /* cudaStream_t                                     */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int rf_version(void);
+/* Static text for a status code (never NULL). */
+const char* rf_status_string(int status);
+/* Thread-local text describing the last failing call on this thread ("" if none). */
+const char* rf_last_error(void);
+/* 1 if `device` has tcgen05 tensor cores (compute capability 10.x), else 0. */
+int rf_device_supported(int device);
+/* Bounded device waits give up after this many milliseconds (default 4000). Host
+ * setting, read at each launch; values < 1 restore the default. */
+void rf_set_wait_timeout_ms(int64_t ms);
+
+/* ===================================================================== *
+ * Fill  ([RF] "Two numbers set the skip range"; "Ridge map", first equation
+ * x̂_l = A_l x_S + b_l; the layer's own norm and K/V projections and RoPE)
+ * ===================================================================== */
+typedef struct rf_fill_desc {
+  int64_t d;           /* hidden size: map input and output width, projection input  */
+  int64_t L;           /* number of layers                                          */
+  int64_t S;           /* split layer: maps exist for layers S .. L-1 (P = L - S)    */
+  int64_t N;           /* prompt rows                                               */
+  int64_t T;           /* tail rows: rows N-T .. N-1 are never filled (0 <= T <= N)  */
+  int64_t n_kv_heads;  /* H                                                         */
+  int64_t head_dim;    /* hd; KV = H*hd                                              */
+  double rope_theta;   /* RoPE base (rotate-half pairs (i, i+hd/2), θ^(-2i/hd))      */
+  double rms_eps;      /* RMSNorm ε: y = g ⊙ x / sqrt(mean(x²) + ε)                   */
+  int64_t pos_offset;  /* RoPE position of row 0                                     */
+} rf_fill_desc;
+
+/* Supported fill shapes: d % 256 == 0, head_dim in {64, 128}, KV % 128 == 0,
+ * 1 <= N - T <= 2^30 when anything is filled. */
+
+/* Workspace bytes rf_fill_kv needs for `desc` (0 on invalid desc). */
+size_t rf_fill_workspace_bytes(const rf_fill_desc* desc);
+
+/* One-time weight preparation for rf_fill_kv: folds each layer's RMSNorm gain into
+ * its K and V projections and stacks them,
+ *   Wkv[p][j][i]      = bf16(Wk[p][j][i] * gain[p][i])   j <  KV
+ *   Wkv[p][KV + j][i] = bf16(Wv[p][j][i] * gain[p][i])   j <  KV
+ * gain [P][d], Wk and Wv [P][KV][d] (row = output channel), Wkv [P][2*KV][d]. */
+rf_status rf_fold_kv_weights(const rf_fill_desc* desc, const rf_bf16* gain,
+                             const rf_bf16* Wk, const rf_bf16* Wv, rf_bf16* Wkv,
+                             rf_stream_t stream);
+
+/* The fill. For every filled row t (t < N-T, exact_mask[t] == 0, ascending) and
+ * every layer l = S + p:
+ *   x̂ = A_p x_S[t] + b_p;  r = (mean(x̂²) + ε)^-1/2;  [k | v] = r · Wkv_p x̂;
+ *   k_h <- RoPE(k_h, t + pos_offset) per head;
+ *   k_cache[l][t][h][:] = bf16(k_h),  v_cache[l][t][h][:] = bf16(v_h).
+ * Nothing else in the caches is written: not the tail, not exact rows, not
+ * layers < S ([RF] Table 3). x̂ is rounded to bf16 before the projection.
+ *   x_S        [N][ld_x] bf16, the residual stream entering layer S
+ *   exact_mask [N-T] uint8, nonzero = exact row (never filled); NULL = none
+ *   A          [P][d][d] bf16, A_p[o][i] (row = output)
+ *   b          [P][d] fp32
+ *   Wkv        [P][2*KV][d] bf16 from rf_fold_kv_weights
+ *   k_cache, v_cache: element (l, t, h, c) at l*layer_stride + t*row_stride + h*hd + c
+ *   n_fill_out device int32 (may be NULL): number of filled rows
+ * Kernels: row compaction + gather, one tcgen05 GEMM for all maps (bias, bf16 x̂
+ * and per-row sum-of-squares in its epilogue), one tcgen05 GEMM for all K/V
+ * projections (RMS scale, RoPE and cache scatter in its epilogue). */
+rf_status rf_fill_kv(const rf_fill_desc* desc,
+                     const rf_bf16* x_S, int64_t ld_x,
+                     const uint8_t* exact_mask,
+                     const rf_bf16* A, const float* b, const rf_bf16* Wkv,
+                     rf_bf16* k_cache, rf_bf16* v_cache,
+                     int64_t layer_stride, int64_t row_stride,
+                     int32_t* n_fill_out, int32_t* dev_status,
+                     void* workspace, size_t workspace_bytes, rf_stream_t stream);
+
+/* ===================================================================== *
+ * Calibration statistics ([RF] "Ridge map": only XᵀX, XᵀY_l and the two means
+ * are accumulated in one pass; [XM]: XᵀX is the dominant fitting cost)
+ * ===================================================================== */
+typedef struct rf_calib_desc {
+  int64_t d_in;    /* width of x (map input)        */
+  int64_t d_out;   /* width of each y_p (map output) */
+  int64_t n_maps;  /* P                              */
+} rf_calib_desc;
+
+/* Raw one-pass sums, all device fp64 (n as int64), caller-owned.
+ *   G  [d_in][d_in]         Σ x xᵀ   (both triangles)
+ *   C  [n_maps][d_in][d_out] Σ x y_pᵀ
+ *   sx [d_in]               Σ x
+ *   sy [n_maps][d_out]      Σ y_p
+ *   n  [1]                  rows seen
+ * Zero them to start; saved and reloaded sums resume accumulation. */
+typedef struct rf_calib_stats {
+  double* G;
+  double* C;
+  double* sx;
+  double* sy;
+  int64_t* n;
+} rf_calib_stats;
+
+/* Supported: d_in % 128 == 0, d_out % 256 == 0 (or n_maps == 0), n_rows % 8 == 0. */
+size_t rf_calib_workspace_bytes(const rf_calib_desc* desc, int64_t n_rows);
+
+/* Adds one batch of rows: G += XᵀX, C_p += XᵀY_p, sx += Σx, sy_p += Σy_p, n += n_rows.
+ *   X [n_rows][ld_x] bf16; Y_p at Y + p*y_map_stride, [n_rows][ld_y] bf16.
+ * Products are exact in fp32, summed in fp32 over chunks of rows on the tensor
+ * cores and added to the fp64 totals. */
+rf_status rf_calib_accumulate(const rf_calib_desc* desc,
+                              const rf_bf16* X, int64_t ld_x,
+                              const rf_bf16* Y, int64_t ld_y, int64_t y_map_stride,
+                              int64_t n_rows, const rf_calib_stats* stats,
+                              int32_t* dev_status,
+                              void* workspace, size_t workspace_bytes, rf_stream_t stream);
+
+/* ===================================================================== *
+ * Ridge solve ([RF] "Ridge map": A_l = Y_lᵀX (XᵀX + αI)^-1, b_l = μ_l − A_l μ_S,
+ * α = λ·tr(XᵀX)/d_in on centred X; a new λ only needs a re-solve)
+ * ===================================================================== */
+enum { RF_ALPHA_TRACE = 0, RF_ALPHA_ABSOLUTE = 1 };
+
+size_t rf_solve_workspace_bytes(const rf_calib_desc* desc);
+
+/* Solves every map from the statistics (read only, so re-solving at another λ
+ * is legal):
+ *   Gc = G − n μ_x μ_xᵀ, Cc_p = C_p − n μ_x μ_pᵀ, α = λ tr(Gc)/d_in (TRACE) or λ,
+ *   Gc + αI = L Lᵀ (fp32 Cholesky), A_p = Cc_pᵀ (Gc + αI)^-1 (fp32), then
+ *   `refine_iters` sweeps of A_p += (Cc_pᵀ − A_p (Gc + αI)) (Gc + αI)^-1 with the
+ *   residual in fp64; b_p = μ_p − A_p μ_x (fp64 → fp32).
+ *   A [n_maps][d_out][d_in] fp32, b [n_maps][d_out] fp32,
+ *   A_bf16 (may be NULL) bf16 copy of A for rf_fill_kv, alpha_out (device, may be NULL).
+ * A non-positive pivot sets RF_ERR_NOT_SPD in *dev_status. */
+rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* stats,
+                   double lambda, int alpha_mode, int refine_iters,
+                   float* A, float* b, rf_bf16* A_bf16, double* alpha_out,
+                   int32_t* dev_status,
+                   void* workspace, size_t workspace_bytes, rf_stream_t stream);
+
+/* ===================================================================== *
+ * Cross-model mapper ([XM] content-space mapping
+ *   K̂_t = (K_s R_s^-1(t) W_K + b_K) R_t(t), V mapped without RoPE;
+ * the k source layers chosen for a target layer are concatenated, all heads)
+ * ===================================================================== */
+typedef struct rf_xmodel_desc {
+  int64_t L_src;       /* source layers                                  */
+  int64_t L_tgt;       /* target layers                                  */
+  int64_t k;           /* source layers concatenated per target layer     */
+  int64_t n_kv_heads;  /* H (same on both sides: KV-matched pair)         */
+  int64_t head_dim;    /* hd                                             */
+  int64_t N;           /* rows (tokens)                                  */
+  double theta_src;    /* source RoPE base                                */
+  double theta_tgt;    /* target RoPE base                                */
+  int64_t pos_offset;  /* position of row 0                               */
+} rf_xmodel_desc;
+
+/* Supported: head_dim in {64, 128}, KV % 256 == 0, N >= 1. */
+size_t rf_xmodel_workspace_bytes(const rf_xmodel_desc* desc);
+
+/* For every target layer l and row t:
+ *   F_K = [RoPE_src^-1(k_src[s_j][t]) for j < k] (feature order: j, head, dim),
+ *   F_V = [v_src[s_j][t] for j < k],  s_j = src_layers[l*k + j],
+ *   k_tgt[l][t] = bf16(RoPE_tgt(F_K Wk_lᵀ + bk_l)),  v_tgt[l][t] = bf16(F_V Wv_lᵀ + bv_l).
+ *   src_layers  HOST int32 [L_tgt][k], each in [0, L_src) (copied before return)
+ *   k_src, v_src [L_src][N][KV] bf16;  k_tgt, v_tgt [L_tgt][N][KV] bf16
+ *   Wk, Wv [L_tgt][KV][k*KV] bf16 (row = output);  bk, bv [L_tgt][KV] fp32 */
+rf_status rf_xmodel_map(const rf_xmodel_desc* desc, const int32_t* src_layers,
+                        const rf_bf16* k_src, const rf_bf16* v_src,
+                        const rf_bf16* Wk, const float* bk,
+                        const rf_bf16* Wv, const float* bv,
+                        rf_bf16* k_tgt, rf_bf16* v_tgt, int32_t* dev_status,
+                        void* workspace, size_t workspace_bytes, rf_stream_t stream);
+
+/* RoPE (inverse = 0) or its inverse (inverse = 1) on rows of heads, out of place
+ * or in place: out[t][h][:] = R^{±1}(t + pos_offset) in[t][h][:].
+ * in, out [n_rows][ld] bf16 with H*hd <= ld. Used to build cross-model
+ * calibration features (un-roped keys). [XM] content-space mapping. */
+rf_status rf_rope_rows(const rf_bf16* in, rf_bf16* out, int64_t n_rows, int64_t ld,
+                       int64_t n_heads, int64_t head_dim, double theta,
+                       int64_t pos_offset, int inverse, rf_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RIDGE_MAP_KV_RF_H */

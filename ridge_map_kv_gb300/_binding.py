@@ -1,0 +1,206 @@
+"""ctypes binding of librf.so (include/rf.h). Argument marshalling only.
+
+Functions keep the C names and argument order. Tensor arguments may be torch
+tensors (their data_ptr() is passed), plain integers (device addresses) or None
+(NULL). ``stream=None`` means torch's current CUDA stream. A status other than
+RF_OK raises RFError carrying the status and the library's error text. There is
+no fallback: if librf.so has not been built, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_double, c_int, c_int32, c_int64, c_size_t, c_void_p
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "librf.so")
+
+RF_OK = 0
+RF_ERR_INVALID_ARG = 1
+RF_ERR_SHAPE = 2
+RF_ERR_ALIGN = 3
+RF_ERR_CUDA = 4
+RF_ERR_NOT_SPD = 5
+RF_ERR_TIMEOUT = 6
+RF_ERR_UNSUPPORTED = 7
+RF_ERR_WORKSPACE = 8
+RF_ALPHA_TRACE = 0
+RF_ALPHA_ABSOLUTE = 1
+
+
+class RFError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+class rf_fill_desc(ctypes.Structure):
+    _fields_ = [("d", c_int64), ("L", c_int64), ("S", c_int64), ("N", c_int64), ("T", c_int64),
+                ("n_kv_heads", c_int64), ("head_dim", c_int64), ("rope_theta", c_double),
+                ("rms_eps", c_double), ("pos_offset", c_int64)]
+
+
+class rf_calib_desc(ctypes.Structure):
+    _fields_ = [("d_in", c_int64), ("d_out", c_int64), ("n_maps", c_int64)]
+
+
+class rf_calib_stats(ctypes.Structure):
+    _fields_ = [("G", c_void_p), ("C", c_void_p), ("sx", c_void_p), ("sy", c_void_p), ("n", c_void_p)]
+
+
+class rf_xmodel_desc(ctypes.Structure):
+    _fields_ = [("L_src", c_int64), ("L_tgt", c_int64), ("k", c_int64), ("n_kv_heads", c_int64),
+                ("head_dim", c_int64), ("N", c_int64), ("theta_src", c_double), ("theta_tgt", c_double),
+                ("pos_offset", c_int64)]
+
+
+_SIGS = {
+    "rf_version": (c_int, []),
+    "rf_status_string": (c_char_p, [c_int]),
+    "rf_last_error": (c_char_p, []),
+    "rf_device_supported": (c_int, [c_int]),
+    "rf_set_wait_timeout_ms": (None, [c_int64]),
+    "rf_fill_workspace_bytes": (c_size_t, [POINTER(rf_fill_desc)]),
+    "rf_fold_kv_weights": (c_int, [POINTER(rf_fill_desc), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "rf_fill_kv": (c_int, [POINTER(rf_fill_desc), c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p,
+                           c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p, c_size_t,
+                           c_void_p]),
+    "rf_calib_workspace_bytes": (c_size_t, [POINTER(rf_calib_desc), c_int64]),
+    "rf_calib_accumulate": (c_int, [POINTER(rf_calib_desc), c_void_p, c_int64, c_void_p, c_int64, c_int64,
+                                    c_int64, POINTER(rf_calib_stats), c_void_p, c_void_p, c_size_t, c_void_p]),
+    "rf_solve_workspace_bytes": (c_size_t, [POINTER(rf_calib_desc)]),
+    "rf_solve": (c_int, [POINTER(rf_calib_desc), POINTER(rf_calib_stats), c_double, c_int, c_int, c_void_p,
+                         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "rf_xmodel_workspace_bytes": (c_size_t, [POINTER(rf_xmodel_desc)]),
+    "rf_xmodel_map": (c_int, [POINTER(rf_xmodel_desc), POINTER(c_int32), c_void_p, c_void_p, c_void_p, c_void_p,
+                              c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "rf_rope_rows": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_double, c_int64, c_int,
+                             c_void_p]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Loads librf.so once. Raises if it is missing or lacks a declared symbol."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"librf.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name, None)
+            if f is None:
+                continue
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _p(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _s(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st: int, fn: str):
+    if st != RF_OK:
+        L = lib()
+        raise RFError(st, f"{fn}: {L.rf_status_string(st).decode()}: {L.rf_last_error().decode()}")
+
+
+# ---------------------------------------------------------------- library-wide
+def rf_version() -> int:
+    return lib().rf_version()
+
+
+def rf_status_string(status: int) -> str:
+    return lib().rf_status_string(status).decode()
+
+
+def rf_last_error() -> str:
+    return lib().rf_last_error().decode()
+
+
+def rf_device_supported(device: int = 0) -> bool:
+    return bool(lib().rf_device_supported(device))
+
+
+def rf_set_wait_timeout_ms(ms: int) -> None:
+    lib().rf_set_wait_timeout_ms(int(ms))
+
+
+# ------------------------------------------------------------------------ fill
+def rf_fill_workspace_bytes(desc: rf_fill_desc) -> int:
+    return int(lib().rf_fill_workspace_bytes(ctypes.byref(desc)))
+
+
+def rf_fold_kv_weights(desc, gain, Wk, Wv, Wkv, stream=None):
+    _check(lib().rf_fold_kv_weights(ctypes.byref(desc), _p(gain), _p(Wk), _p(Wv), _p(Wkv), _s(stream)),
+           "rf_fold_kv_weights")
+
+
+def rf_fill_kv(desc, x_S, ld_x, exact_mask, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride,
+               n_fill_out=None, dev_status=None, workspace=None, workspace_bytes=0, stream=None):
+    _check(lib().rf_fill_kv(ctypes.byref(desc), _p(x_S), int(ld_x), _p(exact_mask), _p(A), _p(b), _p(Wkv),
+                            _p(k_cache), _p(v_cache), int(layer_stride), int(row_stride), _p(n_fill_out),
+                            _p(dev_status), _p(workspace), int(workspace_bytes), _s(stream)), "rf_fill_kv")
+
+
+# ----------------------------------------------------------------- calibration
+def rf_calib_workspace_bytes(desc: rf_calib_desc, n_rows: int) -> int:
+    return int(lib().rf_calib_workspace_bytes(ctypes.byref(desc), int(n_rows)))
+
+
+def calib_stats_struct(G, C, sx, sy, n) -> rf_calib_stats:
+    return rf_calib_stats(_p(G), _p(C), _p(sx), _p(sy), _p(n))
+
+
+def rf_calib_accumulate(desc, X, ld_x, Y, ld_y, y_map_stride, n_rows, stats, dev_status=None,
+                        workspace=None, workspace_bytes=0, stream=None):
+    _check(lib().rf_calib_accumulate(ctypes.byref(desc), _p(X), int(ld_x), _p(Y), int(ld_y), int(y_map_stride),
+                                     int(n_rows), ctypes.byref(stats), _p(dev_status), _p(workspace),
+                                     int(workspace_bytes), _s(stream)), "rf_calib_accumulate")
+
+
+# ----------------------------------------------------------------------- solve
+def rf_solve_workspace_bytes(desc: rf_calib_desc) -> int:
+    return int(lib().rf_solve_workspace_bytes(ctypes.byref(desc)))
+
+
+def rf_solve(desc, stats, lam, alpha_mode, refine_iters, A, b, A_bf16=None, alpha_out=None, dev_status=None,
+             workspace=None, workspace_bytes=0, stream=None):
+    _check(lib().rf_solve(ctypes.byref(desc), ctypes.byref(stats), float(lam), int(alpha_mode), int(refine_iters),
+                          _p(A), _p(b), _p(A_bf16), _p(alpha_out), _p(dev_status), _p(workspace),
+                          int(workspace_bytes), _s(stream)), "rf_solve")
+
+
+# ------------------------------------------------------------------ cross-model
+def rf_xmodel_workspace_bytes(desc: rf_xmodel_desc) -> int:
+    return int(lib().rf_xmodel_workspace_bytes(ctypes.byref(desc)))
+
+
+def rf_xmodel_map(desc, src_layers, k_src, v_src, Wk, bk, Wv, bv, k_tgt, v_tgt, dev_status=None,
+                  workspace=None, workspace_bytes=0, stream=None):
+    """``src_layers``: host int32 array-like [L_tgt][k]."""
+    import numpy as np
+    tab = np.ascontiguousarray(np.asarray(src_layers, dtype=np.int32).reshape(-1))
+    _check(lib().rf_xmodel_map(ctypes.byref(desc), tab.ctypes.data_as(POINTER(c_int32)), _p(k_src), _p(v_src),
+                               _p(Wk), _p(bk), _p(Wv), _p(bv), _p(k_tgt), _p(v_tgt), _p(dev_status),
+                               _p(workspace), int(workspace_bytes), _s(stream)), "rf_xmodel_map")
+
+
+def rf_rope_rows(inp, out, n_rows, ld, n_heads, head_dim, theta, pos_offset=0, inverse=False, stream=None):
+    _check(lib().rf_rope_rows(_p(inp), _p(out), int(n_rows), int(ld), int(n_heads), int(head_dim), float(theta),
+                              int(pos_offset), 1 if inverse else 0, _s(stream)), "rf_rope_rows")

@@ -1,0 +1,61 @@
+// Host-side helpers shared by the entry points: error text, argument checks,
+// workspace carving, TMA descriptor encoding and device queries.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstddef>
+#include <cstdint>
+
+#include "rf.h"
+
+namespace rf {
+
+// Records a thread-local error text and returns `st`.
+rf_status fail(rf_status st, const char* fmt, ...);
+void clear_error();
+
+// Maps a CUDA error to RF_ERR_CUDA with its text (RF_OK on success).
+rf_status cuda_check(cudaError_t e, const char* what);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Current device: SM count and whether it is sm_100-family; RF_ERR_* on failure.
+rf_status current_device(int* sm_count);
+
+// Wait limit for bounded device waits, in ns.
+uint64_t wait_timeout_ns();
+
+// Builds a 2-D bf16 TMA descriptor with 128-byte swizzle and zero fill out of
+// bounds: dims {inner, outer}, row stride in elements, box {box_inner, box_outer}.
+rf_status make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
+                            uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer);
+
+// 3-D variant: dims {inner, mid, outer}, strides (elements) of mid and outer,
+// box {box_inner, box_mid, 1}.
+rf_status make_tmap_bf16_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
+                            uint64_t mid_stride_elems, uint64_t outer_stride_elems, uint32_t box_inner,
+                            uint32_t box_mid);
+
+// Bump allocator over the caller workspace (256-byte aligned regions).
+struct Carve {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carve(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <class T>
+  T* take(size_t count) {
+    off = (off + 255) & ~size_t(255);
+    T* p = reinterpret_cast<T*>(base ? base + off : nullptr);
+    off += count * sizeof(T);
+    return p;
+  }
+  size_t bytes() const { return (off + 255) & ~size_t(255); }
+};
+
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Sets the dynamic shared-memory limit of a kernel once per process and device.
+rf_status set_smem_attr(const void* kernel, size_t bytes, uint64_t* done_mask);
+
+}  // namespace rf

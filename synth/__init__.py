@@ -237,13 +237,14 @@ def xmodel_inputs(cfg: XModelConfig, device="cpu", L_tgt: Optional[int] = None,
 def canary_cache(L: int, N_cap: int, H: int, hd: int, kind: int, device="cpu") -> torch.Tensor:
     """bf16 cache filled with NaN canaries whose payload encodes (kind, l, t, h, c)
     modulo the 6 free mantissa bits, so any stray write is visible bit for bit."""
-    l = torch.arange(L, dtype=torch.int32).view(L, 1, 1, 1)
-    t = torch.arange(N_cap, dtype=torch.int32).view(1, N_cap, 1, 1)
-    h = torch.arange(H, dtype=torch.int32).view(1, 1, H, 1)
-    c = torch.arange(hd, dtype=torch.int32).view(1, 1, 1, hd)
-    payload = (kind * 31 + l * 7 + t * 13 + h * 5 + c) % 63 + 1     # 1..63, never 0
-    bits = (0x7F80 | payload).to(torch.int16)                       # quiet-bit clear NaNs
-    return bits.view(torch.bfloat16).to(device)
+    out = torch.empty((L, N_cap, H, hd), dtype=torch.int16, device=device)
+    t = torch.arange(N_cap, dtype=torch.int32, device=device).view(N_cap, 1, 1)
+    h = torch.arange(H, dtype=torch.int32, device=device).view(1, H, 1)
+    c = torch.arange(hd, dtype=torch.int32, device=device).view(1, 1, hd)
+    for l in range(L):
+        payload = (kind * 31 + l * 7 + t * 13 + h * 5 + c) % 63 + 1     # 1..63, never 0
+        out[l] = (0x7F80 | payload).to(torch.int16)                     # NaN bit patterns
+    return out.view(torch.bfloat16)
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

@@ -1,0 +1,117 @@
+"""GPU parity of rf_fill_kv against the fp64 oracle (through the C ABI).
+
+Small cases compare every filled entry and check the whole cache bit for bit
+against NaN canaries. They span several M/N tiles, ragged tails and the
+degenerate arms. Full-size cases use the workloads' own shapes: bookkeeping on
+the whole cache, values on sampled rows (first, last, neighbours of exact blocks,
+the last prefix row and seeded random rows).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from fillcheck import assert_bookkeeping, assert_values, run_fill
+
+pytestmark = pytest.mark.gpu
+
+
+def _small(name, **kw):
+    base = dict(name=name, index=90, d=512, L=5, S=2, N=400, T=37, H=2, hd=128, rope_theta=5e5,
+                exact="uniform10", lam=0.03, calib_n=0)
+    base.update(kw)
+    return synth.FillConfig(**base)
+
+
+def _mask_np(inp):
+    return None if inp["mask"] is None else inp["mask"].cpu().numpy()
+
+
+def test_toy_fill_matches_oracle_everywhere():
+    cfg = synth.TOY
+    inp = synth.fill_inputs(cfg)
+    res = run_fill(cfg, inp)
+    assert res["status"] == 0
+    idx = O.prefix_partition(cfg.N, cfg.T, _mask_np(inp))
+    assert idx.tolist() == [0, 1, 2, 3, 8]
+    assert res["n_fill"] == 5
+    assert_bookkeeping(cfg, res, _mask_np(inp))
+    assert_values(cfg, inp, res, idx)
+
+
+@pytest.mark.parametrize("cfg", [
+    _small("ragged 3 M-tiles, 2 N-tiles, hd128"),
+    _small("hd64, 4 heads, 2 layers", d=768, L=4, S=2, N=300, T=20, H=4, hd=64, exact="blocks16_5"),
+    _small("one layer, no exact rows", d=256, L=3, S=2, N=129, T=0, H=1, hd=128, exact=None),
+    _small("position offset", d=256, L=4, S=1, N=200, T=8, H=2, hd=64, exact="uniform10", pos_offset=1000),
+], ids=lambda c: c.name)
+def test_fill_small_shapes_match_oracle(cfg):
+    inp = synth.fill_inputs(cfg)
+    res = run_fill(cfg, inp)
+    assert res["status"] == 0
+    idx = O.prefix_partition(cfg.N, cfg.T, _mask_np(inp))
+    assert res["n_fill"] == len(idx)
+    assert_bookkeeping(cfg, res, _mask_np(inp))
+    assert_values(cfg, inp, res, idx)
+
+
+@pytest.mark.parametrize("case", ["all_exact", "tail_is_everything", "no_upper_layers", "one_row", "two_tiles_plus_one"])
+def test_fill_degenerate_arms(case):
+    cfg = _small(case, d=256, L=4, S=2, N=140, T=10, H=2, hd=64, exact=None)
+    mask = None
+    if case == "all_exact":
+        mask = torch.ones(cfg.N - cfg.T, dtype=torch.uint8)
+    elif case == "tail_is_everything":
+        cfg = dataclasses.replace(cfg, T=cfg.N)
+    elif case == "no_upper_layers":
+        cfg = dataclasses.replace(cfg, S=cfg.L)
+    elif case == "one_row":
+        mask = torch.ones(cfg.N - cfg.T, dtype=torch.uint8)
+        mask[77] = 0
+    elif case == "two_tiles_plus_one":
+        cfg = dataclasses.replace(cfg, N=267, T=10)
+    inp = synth.fill_inputs(cfg)
+    inp["mask"] = mask
+    res = run_fill(cfg, inp)
+    assert res["status"] == 0
+    mnp = None if mask is None else mask.numpy()
+    idx = O.prefix_partition(cfg.N, cfg.T, mnp)
+    assert res["n_fill"] == len(idx)
+    assert_bookkeeping(cfg, res, mnp)
+    if len(idx) and cfg.P > 0:
+        assert_values(cfg, inp, res, idx)
+
+
+def _sample_rows(idx: np.ndarray, mask_np, n_prefix: int, n_random=192, seed=1):
+    rng = np.random.default_rng(seed)
+    pick = {int(idx[0]), int(idx[-1])}
+    if n_prefix - 1 in set(idx.tolist()):
+        pick.add(n_prefix - 1)
+    if mask_np is not None:
+        ex = np.nonzero(mask_np)[0]
+        fill = set(idx.tolist())
+        for t in np.concatenate([ex - 1, ex + 1]):
+            if 0 <= t < n_prefix and int(t) in fill:
+                pick.add(int(t))
+    pick = sorted(pick)
+    rest = rng.choice(idx, size=min(n_random, len(idx)), replace=False)
+    rows = np.unique(np.concatenate([rng.permutation(np.array(pick))[:64], rest]))
+    return rows.astype(np.int64)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["llama8b", "dense27b"])
+def test_fill_full_size_sampled(name):
+    cfg = synth.FILL_CONFIGS[name]
+    inp = synth.fill_inputs(cfg, device="cuda")
+    res = run_fill(cfg, inp)
+    assert res["status"] == 0
+    mnp = _mask_np(inp)
+    idx = O.prefix_partition(cfg.N, cfg.T, mnp)
+    assert res["n_fill"] == len(idx)
+    assert_bookkeeping(cfg, res, mnp)
+    rows = _sample_rows(idx, mnp, cfg.N - cfg.T)
+    assert_values(cfg, inp, res, rows)
