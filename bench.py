@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Benchmark of the RidgeFill upper-layer KV fill on GB300 (librf.so, C ABI).
+
+One step = one rf_fill_kv call over the Llama-3.1-8B-shaped workload
+(d=4096, L=32, S=12, N=16384, T=4096, 8 KV heads x 128, 10% of prefix rows exact):
+row compaction, gather, RoPE table, the map GEMM for all 20 upper layers and the
+K/V GEMM with norm scale, RoPE and cache scatter. Inputs are seeded synthetic
+tensors resident in HBM. They are larger than L2 (1.1 GB of maps, weights and x_S
+are read per step), so no L2 flush is needed. Timing uses CUDA events on the
+launching stream, bracketed by a barrier and a device synchronize.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 (under torchrun): every rank runs an independent fill on its own GPU (weak
+scaling; no data-path collective). value = all ranks' row-layers / max rank time.
+--impl reference times the fp64 CPU oracle on the host cores over a bounded row
+sample of the same workload, and prints the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "filled rows×layers/s and fill TFLOP/s vs GB300 bf16 dense peak (1 GPU)"
+UNIT = "row-layers/s"
+WORKLOAD = "llama8b"
+KERNELS_PER_FILL = 5
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=1024, help="oracle row sample for the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", choices=sorted(workloads()), default=WORKLOAD,
+                    help="llama8b (default, the metric's workload); others for profiling and parity runs")
+    return ap.parse_args(argv)
+
+
+def workloads():
+    import dataclasses
+    import synth
+    w = dict(synth.FILL_CONFIGS)
+    # ncu-sized case: 8B shapes, 8 upper layers, 4096 prefix rows (maps 268 MB > L2, ~1.5 GB on device)
+    w["small"] = dataclasses.replace(synth.LLAMA8B, name="llama3.1-8b-shaped d4096 L20 S12 N4608 T512",
+                                     L=20, S=12, N=4608, T=512)
+    return w
+
+
+# --------------------------------------------------------------------------- #
+# Distributed plumbing (one process per GPU; timing reduction only)
+# --------------------------------------------------------------------------- #
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return ws, rank, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29511")
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- #
+# Clock sampling during the timed region
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="rf_clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 10:
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        load = [r for r in rows if (num(r[4]) or 0) >= 50] or rows
+        sm = [num(r[1]) for r in load if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i in range(4) if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(load[0][2]), "reasons": reasons, "samples": len(load),
+                "power_w_max": max((num(r[3]) or 0) for r in load)}
+
+
+# --------------------------------------------------------------------------- #
+# Helpers
+# --------------------------------------------------------------------------- #
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j.get("hbm_gbs"), "bf16_tflops": j.get("bf16_tflops"),
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ridge_map_kv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    s = re.search(r"source_sha:\s*([0-9a-f]+)", txt)
+    if not m or not s or s.group(1) != kernel_source_sha():
+        return None
+    return float(m.group(1))
+
+
+def fill_units(cfg, mask):
+    n_prefix = cfg.N - cfg.T
+    n_fill = n_prefix - (int(mask.sum().item()) if mask is not None else 0)
+    return n_fill, n_fill * cfg.P
+
+
+class OracleInputs:
+    """The workload's tensors decoded once to float64 (bf16 decoding is exact and
+    is input marshalling, not the oracle's arithmetic)."""
+
+    def __init__(self, cfg, inp):
+        import numpy as np
+        import oracle as O
+        import synth
+        f64 = O.bf16_bits_to_f64
+        self.cfg = cfg
+        mask = None if inp["mask"] is None else inp["mask"].cpu().numpy()
+        self.idx = O.prefix_partition(cfg.N, cfg.T, mask)
+        self.x = f64(synth.bits(inp["x_S"]))
+        self.A = [f64(synth.bits(inp["A"][p:p + 1])) for p in range(cfg.P)]
+        self.b = [synth.f32(inp["b"][p:p + 1]).astype(np.float64) for p in range(cfg.P)]
+        self.g = [f64(synth.bits(inp["gain"][p:p + 1])) for p in range(cfg.P)]
+        self.Wk = [f64(synth.bits(inp["Wk"][p:p + 1])) for p in range(cfg.P)]
+        self.Wv = [f64(synth.bits(inp["Wv"][p:p + 1])) for p in range(cfg.P)]
+
+
+def cpu_oracle_rate(oi: "OracleInputs", n_rows: int, seed: int = 7):
+    """Times the fp64 oracle (fill_rows, all upper layers) on ``n_rows`` filled rows."""
+    import numpy as np
+    import oracle as O
+    cfg = oi.cfg
+    rows = np.sort(np.random.default_rng(seed).choice(oi.idx, size=min(n_rows, len(oi.idx)), replace=False))
+    t0 = time.perf_counter()
+    x = oi.x[rows]
+    for p in range(cfg.P):
+        O.fill_rows(x, rows + cfg.pos_offset, oi.A[p], oi.b[p], oi.g[p], oi.Wk[p], oi.Wv[p],
+                    cfg.H, cfg.hd, cfg.rope_theta, cfg.rms_eps)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return len(rows) * cfg.P / dt, dt, len(rows), cores
+
+
+# --------------------------------------------------------------------------- #
+# Our arm
+# --------------------------------------------------------------------------- #
+def run_ours(args):
+    import torch
+
+    import ridge_map_kv_gb300 as rf
+    import synth
+
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    dev = torch.device("cuda", local)
+    cfg = workloads()[args.workload]
+    inp = synth.fill_inputs(cfg, device=dev)
+    n_fill, units = fill_units(cfg, inp["mask"])
+    P, d, KV = cfg.P, cfg.d, cfg.KV
+    desc = rf.rf_fill_desc(d=d, L=cfg.L, S=cfg.S, N=cfg.N, T=cfg.T, n_kv_heads=cfg.H, head_dim=cfg.hd,
+                           rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, pos_offset=0)
+    Wkv = torch.empty((P, 2 * KV, d), dtype=torch.bfloat16, device=dev)
+    kc = torch.zeros((cfg.L, cfg.N, cfg.H, cfg.hd), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    ws_bytes = rf.rf_fill_workspace_bytes(desc)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    nfill = torch.zeros(1, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # one-time weight preparation (reported separately)
+    rf.rf_profile_start(4)
+    rf.rf_fold_kv_weights(desc, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
+    fold_ms = sum(ms for _, ms in rf.rf_profile_stop())
+
+    def step():
+        rf.rf_fill_kv(desc, inp["x_S"], d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc, cfg.N * KV, KV,
+                      nfill, status, ws, ws_bytes)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    assert int(nfill.item()) == n_fill
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.4)                      # let the sampler start before the timed region
+    rf.rf_profile_start(args.steps * KERNELS_PER_FILL + 8)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    prof = rf.rf_profile_stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    assert int(status.item()) == 0
+    t_max = reduce_max(elapsed_ms, dev)
+    total_units = reduce_sum(float(units * args.steps), dev)
+    value = total_units / (t_max / 1e3)
+    ms_per_step = t_max / args.steps
+
+    stage_ms = {}
+    for name, ms in prof:
+        stage_ms.setdefault(name, []).append(ms)
+    stage_avg = {k: sum(v) / len(v) for k, v in stage_ms.items()}
+    launches = len(prof)
+
+    map_flops = 2.0 * n_fill * P * d * d
+    kv_flops = 2.0 * n_fill * P * d * 2 * KV
+    fill_flops = map_flops + kv_flops
+    peaks = measured_peaks()
+    map_ms = stage_avg.get("map_gemm")
+    achieved = map_flops / (map_ms / 1e3) / 1e12 if map_ms else None
+    peak = peaks["bf16_tflops"]
+    roofline = {"kernel": "map_gemm (tc_gemm<MapProb>)", "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": (achieved / peak) if achieved else None,
+                "traffic": profiled_traffic("map_gemm", args.workload),
+                "peak_source": f"{peaks['source']} burst bf16 (MEASURED_PEAKS.json)",
+                "algorithmic_flops_per_launch": map_flops,
+                "algorithmic_bytes_per_launch": n_fill * d * 2 + P * d * d * 2 + n_fill * P * d * 2
+                + n_fill * P * (d // 256) * 4 + P * d * 4}
+
+    # End to end through the C ABI from pinned host buffers: x_S and the mask go
+    # host->device, n_fill and the status word come back, every step.
+    e2e = None
+    if not args.no_e2e:
+        xh = inp["x_S"].cpu().pin_memory()
+        has_mask = inp["mask"] is not None
+        mh = inp["mask"].cpu().pin_memory() if has_mask else torch.zeros(0, dtype=torch.uint8)
+        xd = torch.empty_like(inp["x_S"])
+        md = torch.empty_like(inp["mask"]) if has_mask else None
+        outh = torch.zeros(2, dtype=torch.int32).pin_memory()
+        outd = torch.zeros(2, dtype=torch.int32, device=dev)
+
+        def step_e2e():
+            xd.copy_(xh, non_blocking=True)
+            if has_mask:
+                md.copy_(mh, non_blocking=True)
+            rf.rf_fill_kv(desc, xd, d, md, inp["A"], inp["b"], Wkv, kc, vc, cfg.N * KV, KV, outd[0:1],
+                          outd[1:2], ws, ws_bytes)
+            outh.copy_(outd, non_blocking=True)
+        for _ in range(3):
+            step_e2e()
+        torch.cuda.synchronize()
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step_e2e()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        assert int(outh[0]) == n_fill and int(outh[1]) == 0
+        t_e2e = reduce_max(e0.elapsed_time(e1), dev)
+        e2e = {"value": total_units / (t_e2e / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": xh.numel() * 2 + mh.numel(), "d2h_bytes_per_step": 8,
+               "ms_per_step": t_e2e / args.steps}
+
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        rate, dt, nrows, cores = cpu_oracle_rate(OracleInputs(cfg, inp), args.cpu_rows)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{nrows} filled rows x {P} upper layers of the same workload, fp64 numpy, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name + " 8x128 KV heads, 10% exact prefix rows", "n_fill": n_fill,
+                       "upper_layers": P, "row_layers_per_step": units, "parallelism": f"independent fills x{ws_n}",
+                       "l2": "no flush: inputs larger than L2 (1.1 GB of maps, weights and x_S read per step)"},
+            "tflops": fill_flops * args.steps * ws_n / (t_max / 1e3) / 1e12,
+            "frac_of_bf16_peak": fill_flops * args.steps * ws_n / (t_max / 1e3) / 1e12 / peak,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clk,
+            "stages_ms": stage_avg, "fold_once_ms": fold_ms,
+        }
+        print(json.dumps(line))
+
+
+# --------------------------------------------------------------------------- #
+# Reference arm: the fp64 oracle on the host cores
+# --------------------------------------------------------------------------- #
+def run_reference(args):
+    import synth
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cfg = workloads()[args.workload]
+    inp = synth.fill_inputs(cfg, device="cpu")
+    n_fill, units = fill_units(cfg, inp["mask"])
+    rows_per_step = 64
+    oi = OracleInputs(cfg, inp)
+    for _ in range(max(args.warmup, 3)):
+        cpu_oracle_rate(oi, 8, seed=0)
+    t = 0.0
+    done = 0
+    for k in range(args.steps):
+        _, dt, n, cores = cpu_oracle_rate(oi, rows_per_step, seed=100 + k)
+        t += dt
+        done += n * cfg.P
+    value = done / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": cfg.name + " 8x128 KV heads, 10% exact prefix rows", "n_fill": n_fill,
+                       "upper_layers": cfg.P, "sample_rows_per_step": rows_per_step},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{rows_per_step} filled rows x {cfg.P} upper layers per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

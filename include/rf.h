@@ -70,6 +70,30 @@ int rf_device_supported(int device);
  * setting, read at each launch; values < 1 restore the default. */
 void rf_set_wait_timeout_ms(int64_t ms);
 
+/* Optional per-kernel timing. Between rf_profile_start and rf_profile_stop every
+ * kernel the library launches (on any thread) is bracketed by two CUDA events
+ * recorded on its launching stream, up to `max_records` kernels; later launches
+ * are not recorded. rf_profile_stop waits for the recorded events, writes up to
+ * `capacity` (stage id, milliseconds) pairs in launch order (host arrays) and
+ * returns how many it wrote (-1 on a CUDA error). Recording adds two event
+ * records per launch and no synchronisation. */
+enum rf_stage {
+  RF_STAGE_COMPACT = 1,      /* exact-row mask -> fill_idx                    */
+  RF_STAGE_GATHER = 2,       /* x_S rows -> dense operand                      */
+  RF_STAGE_ROPE_TABLE = 3,   /* cos/sin table                                  */
+  RF_STAGE_MAP_GEMM = 4,     /* x̂ = x_S A_lᵀ + b_l, all upper layers           */
+  RF_STAGE_KV_GEMM = 5,      /* K/V projection + norm scale + RoPE + scatter   */
+  RF_STAGE_FOLD = 6,         /* gain fold into W_k / W_v                       */
+  RF_STAGE_CALIB_GEMM = 7,   /* XᵀX and XᵀY_l                                  */
+  RF_STAGE_COLSUM = 8,       /* Σx, Σy, n                                      */
+  RF_STAGE_SOLVE = 9,        /* kernels of the ridge solve                     */
+  RF_STAGE_UNROPE = 10,      /* RoPE / inverse RoPE on cache rows              */
+  RF_STAGE_XMODEL_GEMM = 11  /* cross-model mapper GEMM                        */
+};
+rf_status rf_profile_start(int max_records);
+int rf_profile_stop(int32_t* stage_ids, float* ms, int capacity);
+const char* rf_stage_name(int stage_id);
+
 /* ===================================================================== *
  * Fill  ([RF] "Two numbers set the skip range"; "Ridge map", first equation
  * x̂_l = A_l x_S + b_l; the layer's own norm and K/V projections and RoPE)

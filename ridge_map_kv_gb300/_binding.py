@@ -59,6 +59,9 @@ _SIGS = {
     "rf_last_error": (c_char_p, []),
     "rf_device_supported": (c_int, [c_int]),
     "rf_set_wait_timeout_ms": (None, [c_int64]),
+    "rf_profile_start": (c_int, [c_int]),
+    "rf_profile_stop": (c_int, [POINTER(c_int32), POINTER(ctypes.c_float), c_int]),
+    "rf_stage_name": (c_char_p, [c_int]),
     "rf_fill_workspace_bytes": (c_size_t, [POINTER(rf_fill_desc)]),
     "rf_fold_kv_weights": (c_int, [POINTER(rf_fill_desc), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "rf_fill_kv": (c_int, [POINTER(rf_fill_desc), c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -139,6 +142,25 @@ def rf_device_supported(device: int = 0) -> bool:
 
 def rf_set_wait_timeout_ms(ms: int) -> None:
     lib().rf_set_wait_timeout_ms(int(ms))
+
+
+def rf_profile_start(max_records: int) -> None:
+    _check(lib().rf_profile_start(int(max_records)), "rf_profile_start")
+
+
+def rf_profile_stop(capacity: int = 1 << 16):
+    """Returns a list of (stage name, milliseconds) in launch order."""
+    ids = (c_int32 * capacity)()
+    ms = (ctypes.c_float * capacity)()
+    n = lib().rf_profile_stop(ids, ms, capacity)
+    if n < 0:
+        raise RFError(RF_ERR_CUDA, "rf_profile_stop: CUDA error while reading events")
+    L = lib()
+    return [(L.rf_stage_name(ids[i]).decode(), float(ms[i])) for i in range(n)]
+
+
+def rf_stage_name(stage_id: int) -> str:
+    return lib().rf_stage_name(int(stage_id)).decode()
 
 
 # ------------------------------------------------------------------------ fill

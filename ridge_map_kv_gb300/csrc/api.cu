@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "rf_host.h"
 
@@ -107,9 +108,99 @@ rf_status set_smem_attr(const void* kernel, size_t bytes, uint64_t* done_mask) {
   return RF_OK;
 }
 
+// ----------------------------------------------------------------- profiler
+struct ProfRecord {
+  cudaEvent_t start = nullptr, stop = nullptr;
+  int stage = 0;
+};
+static std::mutex g_prof_mu;
+static std::vector<ProfRecord> g_prof;
+static int g_prof_used = 0;
+static bool g_prof_on = false;
+
+ProfScope::ProfScope(cudaStream_t s, int stage) : stream(s), slot(-1) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  if (!g_prof_on || g_prof_used >= static_cast<int>(g_prof.size())) return;
+  slot = g_prof_used++;
+  g_prof[slot].stage = stage;
+  cudaEventRecord(g_prof[slot].start, stream);
+}
+
+ProfScope::~ProfScope() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  if (slot < static_cast<int>(g_prof.size())) cudaEventRecord(g_prof[slot].stop, stream);
+}
+
+static void prof_release() {
+  for (auto& r : g_prof) {
+    if (r.start) cudaEventDestroy(r.start);
+    if (r.stop) cudaEventDestroy(r.stop);
+  }
+  g_prof.clear();
+  g_prof_used = 0;
+  g_prof_on = false;
+}
+
 }  // namespace rf
 
 extern "C" {
+
+rf_status rf_profile_start(int max_records) {
+  using namespace rf;
+  clear_error();
+  if (max_records <= 0) return fail(RF_ERR_INVALID_ARG, "max_records must be > 0");
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  prof_release();
+  g_prof.resize(max_records);
+  for (auto& r : g_prof) {
+    if (cudaEventCreate(&r.start) != cudaSuccess || cudaEventCreate(&r.stop) != cudaSuccess) {
+      prof_release();
+      return cuda_check(cudaGetLastError(), "cudaEventCreate");
+    }
+  }
+  g_prof_on = true;
+  return RF_OK;
+}
+
+int rf_profile_stop(int32_t* stage_ids, float* ms, int capacity) {
+  using namespace rf;
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  int n = 0;
+  bool err = false;
+  for (int i = 0; i < g_prof_used; ++i) {
+    float t = 0.f;
+    if (cudaEventSynchronize(g_prof[i].stop) != cudaSuccess ||
+        cudaEventElapsedTime(&t, g_prof[i].start, g_prof[i].stop) != cudaSuccess) {
+      err = true;
+      break;
+    }
+    if (n < capacity) {
+      if (stage_ids) stage_ids[n] = g_prof[i].stage;
+      if (ms) ms[n] = t;
+      ++n;
+    }
+  }
+  prof_release();
+  return err ? -1 : n;
+}
+
+const char* rf_stage_name(int s) {
+  switch (s) {
+    case RF_STAGE_COMPACT: return "compact";
+    case RF_STAGE_GATHER: return "gather";
+    case RF_STAGE_ROPE_TABLE: return "rope_table";
+    case RF_STAGE_MAP_GEMM: return "map_gemm";
+    case RF_STAGE_KV_GEMM: return "kv_gemm";
+    case RF_STAGE_FOLD: return "fold";
+    case RF_STAGE_CALIB_GEMM: return "calib_gemm";
+    case RF_STAGE_COLSUM: return "colsum";
+    case RF_STAGE_SOLVE: return "solve";
+    case RF_STAGE_UNROPE: return "unrope";
+    case RF_STAGE_XMODEL_GEMM: return "xmodel_gemm";
+    default: return "unknown";
+  }
+}
 
 int rf_version(void) { return 100; }
 

@@ -1,0 +1,212 @@
+// Calibration statistics (rf_calib_accumulate).
+//
+// [RF] RidgeFill review, "Ridge map": calibration only accumulates XᵀX, XᵀY_l and
+// the two means in one pass, so a new λ needs only a re-solve. [XM] per-head
+// ridge regression: computing XᵀX is the dominant fitting cost.
+//
+//   tc_gemm<GramProb>  G += XᵀX and C_p += XᵀY_p on the tensor cores. X and Y are
+//                      row-major (samples x features), so both operands are
+//                      MN-major tiles of the same rows. Each output tile's K-loop
+//                      (the rows) is cut into chunks of kCalibChunk rows; a chunk
+//                      is summed in fp32 in TMEM and added to the fp64 totals by
+//                      the epilogue, so fp32 sums never run over more than
+//                      kCalibChunk rows.
+//   k_colsum           Σx, Σy_p (fp32 over 64 rows, fp64 across) and n += rows.
+#include <algorithm>
+
+#include "rf_host.h"
+#include "tc_gemm.cuh"
+
+namespace rf {
+
+constexpr int kCalibChunk = 1024;  // rows summed in fp32 before the fp64 add
+
+struct GramProb {
+  CUtensorMap tmX;  // X  {d_in, n_rows}, box {64, 64}
+  CUtensorMap tmY;  // Y  {d_out, n_rows, P}, box {64, 64, 1}
+  double* G;        // [d_in][d_in]
+  double* C;        // [P][d_in][d_out]
+  int d_in, d_out, P, n_rows, n_chunks;
+  int g_mt, g_nt, c_nt, g_units;
+  int32_t* dev_status;
+  uint64_t timeout_ns;
+  static constexpr bool kAMN = true;
+  static constexpr bool kBMN = true;
+
+  __device__ void prefetch() const {
+    tma_prefetch_desc(&tmX);
+    if (P > 0) tma_prefetch_desc(&tmY);
+  }
+  __device__ int num_units() const { return g_units + P * g_mt * c_nt; }
+  __device__ int num_subtiles(int) const { return n_chunks; }
+  __device__ int num_kb(int, int sb) const {
+    const int rows = min(kCalibChunk, n_rows - sb * kCalibChunk);
+    return (rows + kBK - 1) / kBK;
+  }
+  // Unit order: the Gram tiles, then for every map p its N-tiles with the
+  // M-tiles fastest, so the CTAs in flight share one strip of Y_p.
+  __device__ void decode(int u, bool& is_g, int& p, int& mt, int& nt) const {
+    if (u < g_units) {
+      is_g = true;
+      p = 0;
+      nt = u / g_mt;
+      mt = u - nt * g_mt;
+    } else {
+      is_g = false;
+      u -= g_units;
+      const int per = g_mt * c_nt;
+      p = u / per;
+      const int r = u - p * per;
+      nt = r / g_mt;
+      mt = r - nt * g_mt;
+    }
+  }
+  __device__ void issue_loads(int u, int sb, int kb, uint8_t* sa, uint8_t* sbuf, uint64_t* bar) const {
+    bool is_g;
+    int p, mt, nt;
+    decode(u, is_g, p, mt, nt);
+    const int row0 = sb * kCalibChunk + kb * kBK;
+    load_operand<kBM, true>(sa, &tmX, bar, row0, mt * kBM);
+    if (is_g) {
+      load_operand<kBN, true>(sbuf, &tmX, bar, row0, nt * kBN);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kBN / 64; ++j) tma_load_3d(sbuf + j * (64 * kBK * 2), &tmY, bar, nt * kBN + 64 * j, row0, p);
+    }
+  }
+  __device__ void epilogue(int u, int, uint32_t tacc, int row) const {
+    bool is_g;
+    int p, mt, nt;
+    decode(u, is_g, p, mt, nt);
+    const size_t i = static_cast<size_t>(mt) * kBM + row;
+    double* o = is_g ? G + i * d_in + static_cast<size_t>(nt) * kBN
+                     : C + (static_cast<size_t>(p) * d_in + i) * d_out + static_cast<size_t>(nt) * kBN;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(tacc + ch * 32, v);
+      tmem_wait_ld32(v);
+      double2* o2 = reinterpret_cast<double2*>(o + ch * 32);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        double2 a = o2[q];
+        a.x += static_cast<double>(u2f(v[2 * q]));
+        a.y += static_cast<double>(u2f(v[2 * q + 1]));
+        o2[q] = a;
+      }
+    }
+  }
+};
+
+// Column sums of `n_maps` row-major bf16 matrices [n_rows][ld] (map p at
+// base + p*map_stride): out[p][c] += Σ_t M_p[t][c]. One thread per column, 512
+// rows per block; fp32 over 64 rows, then fp64, then one fp64 atomic per block.
+__global__ void __launch_bounds__(256) k_colsum(const __nv_bfloat16* __restrict__ M, long long ld, long long map_stride,
+                                                int n_rows, int n_cols, double* __restrict__ out,
+                                                int64_t* __restrict__ n_counter, long long add_n) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const int r0 = blockIdx.y * 512;
+  const int p = blockIdx.z;
+  if (n_counter != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+    atomicAdd(reinterpret_cast<unsigned long long*>(n_counter), static_cast<unsigned long long>(add_n));
+  if (c >= n_cols) return;
+  const __nv_bfloat16* col = M + static_cast<long long>(p) * map_stride + c;
+  const int r1 = min(r0 + 512, n_rows);
+  double acc = 0.0;
+  for (int r = r0; r < r1; r += 64) {
+    float s = 0.f;
+    const int re = min(r + 64, r1);
+    for (int t = r; t < re; ++t) s += __bfloat162float(col[static_cast<long long>(t) * ld]);
+    acc += static_cast<double>(s);
+  }
+  atomicAdd(out + static_cast<size_t>(p) * n_cols + c, acc);
+}
+
+static uint64_t g_gram_attr = 0;
+
+}  // namespace rf
+
+using namespace rf;
+
+static rf_status check_calib_desc(const rf_calib_desc* d) {
+  if (d == nullptr) return fail(RF_ERR_INVALID_ARG, "desc is NULL");
+  if (d->d_in <= 0 || d->n_maps < 0 || (d->n_maps > 0 && d->d_out <= 0))
+    return fail(RF_ERR_INVALID_ARG, "need d_in > 0, n_maps >= 0, d_out > 0");
+  if (d->d_in % kBN != 0) return fail(RF_ERR_SHAPE, "d_in = %lld must be a multiple of 256", (long long)d->d_in);
+  if (d->n_maps > 0 && d->d_out % kBN != 0)
+    return fail(RF_ERR_SHAPE, "d_out = %lld must be a multiple of 256", (long long)d->d_out);
+  if (d->n_maps > 65535) return fail(RF_ERR_SHAPE, "n_maps must be <= 65535");
+  return RF_OK;
+}
+
+extern "C" size_t rf_calib_workspace_bytes(const rf_calib_desc* desc, int64_t) {
+  if (check_calib_desc(desc) != RF_OK) return 0;
+  return 0;  // the accumulation needs no scratch memory
+}
+
+extern "C" rf_status rf_calib_accumulate(const rf_calib_desc* desc, const rf_bf16* X, int64_t ld_x, const rf_bf16* Y,
+                                         int64_t ld_y, int64_t y_map_stride, int64_t n_rows,
+                                         const rf_calib_stats* st, int32_t* dev_status, void*, size_t,
+                                         rf_stream_t stream) {
+  clear_error();
+  rf_status s = check_calib_desc(desc);
+  if (s != RF_OK) return s;
+  if (st == nullptr || !st->G || !st->sx || !st->n || (desc->n_maps > 0 && (!st->C || !st->sy)))
+    return fail(RF_ERR_INVALID_ARG, "stats pointers must be non-NULL (C and sy when n_maps > 0)");
+  if (n_rows < 0 || n_rows > (int64_t(1) << 30)) return fail(RF_ERR_INVALID_ARG, "n_rows must be in [0, 2^30]");
+  if (n_rows == 0) return RF_OK;
+  const int64_t d_in = desc->d_in, d_out = desc->d_out, P = desc->n_maps;
+  if (!X || (P > 0 && !Y)) return fail(RF_ERR_INVALID_ARG, "X (and Y when n_maps > 0) must be non-NULL");
+  if (!aligned16(X) || (P > 0 && !aligned16(Y)) || !aligned16(st->G) || (P > 0 && !aligned16(st->C)))
+    return fail(RF_ERR_ALIGN, "X, Y, G and C must be 16-byte aligned");
+  if (ld_x < d_in || ld_x % 8 != 0) return fail(RF_ERR_ALIGN, "ld_x must be >= d_in and a multiple of 8");
+  if (P > 0 && (ld_y < d_out || ld_y % 8 != 0 || y_map_stride % 8 != 0 || (P > 1 && y_map_stride < ld_y * n_rows)))
+    return fail(RF_ERR_ALIGN, "ld_y must be >= d_out and a multiple of 8; y_map_stride a multiple of 8 "
+                              "covering n_rows rows");
+  int sms = 0;
+  if ((s = current_device(&sms)) != RF_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+  {
+    ProfScope prof(cs, RF_STAGE_COLSUM);
+    dim3 gx(static_cast<unsigned>((d_in + 255) / 256), static_cast<unsigned>((n_rows + 511) / 512), 1);
+    k_colsum<<<gx, 256, 0, cs>>>(reinterpret_cast<const __nv_bfloat16*>(X), ld_x, 0, static_cast<int>(n_rows),
+                                 static_cast<int>(d_in), st->sx, st->n, n_rows);
+    if (P > 0) {
+      dim3 gy(static_cast<unsigned>((d_out + 255) / 256), static_cast<unsigned>((n_rows + 511) / 512),
+              static_cast<unsigned>(P));
+      k_colsum<<<gy, 256, 0, cs>>>(reinterpret_cast<const __nv_bfloat16*>(Y), ld_y, y_map_stride,
+                                   static_cast<int>(n_rows), static_cast<int>(d_out), st->sy, nullptr, 0);
+    }
+  }
+  if ((s = cuda_check(cudaGetLastError(), "k_colsum launch")) != RF_OK) return s;
+
+  if ((s = set_smem_attr(reinterpret_cast<const void*>(&tc_gemm_kernel<GramProb>), kGemmSmemBytes, &g_gram_attr)) != RF_OK)
+    return s;
+  GramProb pr;
+  if ((s = make_tmap_bf16_2d(&pr.tmX, X, d_in, n_rows, ld_x, 64, kBK)) != RF_OK) return s;
+  if (P > 0) {
+    if ((s = make_tmap_bf16_3d(&pr.tmY, Y, d_out, n_rows, P, ld_y, P > 1 ? y_map_stride : ld_y * n_rows, 64, kBK)) != RF_OK)
+      return s;
+  } else {
+    pr.tmY = pr.tmX;
+  }
+  pr.G = st->G;
+  pr.C = st->C;
+  pr.d_in = static_cast<int>(d_in);
+  pr.d_out = static_cast<int>(P > 0 ? d_out : 0);
+  pr.P = static_cast<int>(P);
+  pr.n_rows = static_cast<int>(n_rows);
+  pr.n_chunks = static_cast<int>((n_rows + kCalibChunk - 1) / kCalibChunk);
+  pr.g_mt = static_cast<int>(d_in / kBM);
+  pr.g_nt = static_cast<int>(d_in / kBN);
+  pr.c_nt = static_cast<int>(P > 0 ? d_out / kBN : 0);
+  pr.g_units = pr.g_mt * pr.g_nt;
+  pr.dev_status = dev_status;
+  pr.timeout_ns = wait_timeout_ns();
+  const int64_t units = pr.g_units + P * pr.g_mt * pr.c_nt;
+  const int grid = static_cast<int>(std::min<int64_t>(units, sms));
+  ProfScope prof(cs, RF_STAGE_CALIB_GEMM);
+  tc_gemm_kernel<GramProb><<<grid, kGemmThreads, kGemmSmemBytes, cs>>>(pr);
+  return cuda_check(cudaGetLastError(), "calibration GEMM launch");
+}

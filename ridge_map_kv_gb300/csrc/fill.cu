@@ -17,6 +17,7 @@
 #include <algorithm>
 
 #include "rf_host.h"
+#include "epilogue.cuh"
 #include "tc_gemm.cuh"
 
 namespace rf {
@@ -281,58 +282,7 @@ struct KVProb {
       const bool is_k = col0 < KV;
       const int h = (is_k ? col0 : col0 - KV) / hd;
       __nv_bfloat16* dst = (is_k ? kc : vc) + row_off + static_cast<size_t>(h) * hd;
-      const uint32_t tcol = tacc + hh * hd;
-      if (is_k) {
-#pragma unroll 1
-        for (int i0 = 0; i0 < half; i0 += 16) {
-          uint32_t a[16], b[16];
-          tmem_ld16(tcol + i0, a);
-          tmem_ld16(tcol + half + i0, b);
-          tmem_wait_ld16(a);
-          tmem_wait_ld16(b);
-          uint32_t o1[8], o2[8];
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const float4 c4 = *reinterpret_cast<const float4*>(cs + i0 + i);
-            const float4 s4 = *reinterpret_cast<const float4*>(sn + i0 + i);
-            const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-            const float ssn[4] = {s4.x, s4.y, s4.z, s4.w};
-            float r1[4], r2[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float x1 = u2f(a[i + q]) * rs;
-              const float x2 = u2f(b[i + q]) * rs;
-              r1[q] = x1 * cc[q] - x2 * ssn[q];
-              r2[q] = x2 * cc[q] + x1 * ssn[q];
-            }
-            o1[i / 2] = pack_bf16x2(r1[0], r1[1]);
-            o1[i / 2 + 1] = pack_bf16x2(r1[2], r1[3]);
-            o2[i / 2] = pack_bf16x2(r2[0], r2[1]);
-            o2[i / 2 + 1] = pack_bf16x2(r2[2], r2[3]);
-          }
-          if (valid) {
-            st_global_v4(dst + i0, o1[0], o1[1], o1[2], o1[3]);
-            st_global_v4(dst + i0 + 8, o1[4], o1[5], o1[6], o1[7]);
-            st_global_v4(dst + half + i0, o2[0], o2[1], o2[2], o2[3]);
-            st_global_v4(dst + half + i0 + 8, o2[4], o2[5], o2[6], o2[7]);
-          }
-        }
-      } else {
-#pragma unroll 1
-        for (int i0 = 0; i0 < hd; i0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tcol + i0, v);
-          tmem_wait_ld32(v);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) pk[i / 2] = pack_bf16x2(u2f(v[i]) * rs, u2f(v[i + 1]) * rs);
-          if (valid) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              st_global_v4(dst + i0 + 8 * q, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-          }
-        }
-      }
+      emit_head(tacc + hh * hd, hd, rs, nullptr, is_k, cs, sn, dst, valid);
     }
   }
 };
@@ -409,6 +359,7 @@ extern "C" rf_status rf_fold_kv_weights(const rf_fill_desc* desc, const rf_bf16*
   const int d_vec = static_cast<int>(desc->d / 8);
   const long long total = P * 2LL * KV * d_vec;
   const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 8LL * sms));
+  ProfScope prof(static_cast<cudaStream_t>(stream), RF_STAGE_FOLD);
   k_fold_gain<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(gain), reinterpret_cast<const uint4*>(Wk), reinterpret_cast<const uint4*>(Wv),
       reinterpret_cast<uint4*>(Wkv), static_cast<int>(P), KV, d_vec);
@@ -451,18 +402,27 @@ extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, in
     if (n_fill_out) return cuda_check(cudaMemsetAsync(n_fill_out, 0, sizeof(int32_t), s), "memset n_fill_out");
     return RF_OK;
   }
-  k_compact<<<1, 1024, 0, s>>>(exact_mask, static_cast<int>(n_prefix), lay.fill_idx, lay.n_fill, n_fill_out);
+  {
+    ProfScope prof(s, RF_STAGE_COMPACT);
+    k_compact<<<1, 1024, 0, s>>>(exact_mask, static_cast<int>(n_prefix), lay.fill_idx, lay.n_fill, n_fill_out);
+  }
   if ((st = cuda_check(cudaGetLastError(), "k_compact launch")) != RF_OK) return st;
   if (P == 0) return RF_OK;
 
   const int64_t M_pad = round_up(n_prefix, kBM);
-  k_gather_rows<<<static_cast<unsigned>(M_pad), 128, 0, s>>>(reinterpret_cast<const uint4*>(x_S), ld_x / 8, lay.fill_idx,
-                                                            lay.n_fill, reinterpret_cast<uint4*>(lay.xf),
-                                                            static_cast<int>(d / 8), static_cast<int>(M_pad));
+  {
+    ProfScope prof(s, RF_STAGE_GATHER);
+    k_gather_rows<<<static_cast<unsigned>(M_pad), 128, 0, s>>>(reinterpret_cast<const uint4*>(x_S), ld_x / 8,
+                                                              lay.fill_idx, lay.n_fill, reinterpret_cast<uint4*>(lay.xf),
+                                                              static_cast<int>(d / 8), static_cast<int>(M_pad));
+  }
   const int half = static_cast<int>(desc->head_dim / 2);
   const int rope_blocks = static_cast<int>(std::min<int64_t>((n_prefix * half + 255) / 256, 4LL * sms));
-  k_rope_table<<<rope_blocks, 256, 0, s>>>(lay.rope_cos, lay.rope_sin, static_cast<int>(n_prefix), half,
-                                           desc->rope_theta, static_cast<long long>(desc->pos_offset));
+  {
+    ProfScope prof(s, RF_STAGE_ROPE_TABLE);
+    k_rope_table<<<rope_blocks, 256, 0, s>>>(lay.rope_cos, lay.rope_sin, static_cast<int>(n_prefix), half,
+                                             desc->rope_theta, static_cast<long long>(desc->pos_offset));
+  }
   if ((st = cuda_check(cudaGetLastError(), "gather / rope launch")) != RF_OK) return st;
 
   static uint64_t map_attr = 0, kv_attr = 0;
@@ -487,6 +447,7 @@ extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, in
     pr.timeout_ns = tmo;
     const int64_t units = m_tiles_max * pr.n_ntiles;
     const int grid = static_cast<int>(std::min<int64_t>(units, sms));
+    ProfScope prof(s, RF_STAGE_MAP_GEMM);
     tc_gemm_kernel<MapProb><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(pr);
     if ((st = cuda_check(cudaGetLastError(), "map GEMM launch")) != RF_OK) return st;
   }
@@ -517,6 +478,7 @@ extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, in
     pr.timeout_ns = tmo;
     const int64_t units = P * m_tiles_max * pr.n_ntiles;
     const int grid = static_cast<int>(std::min<int64_t>(units, sms));
+    ProfScope prof(s, RF_STAGE_KV_GEMM);
     tc_gemm_kernel<KVProb><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(pr);
     if ((st = cuda_check(cudaGetLastError(), "K/V GEMM launch")) != RF_OK) return st;
   }
