@@ -152,6 +152,32 @@ rf_status rf_fill_kv(const rf_fill_desc* desc,
                      int32_t* n_fill_out, int32_t* dev_status,
                      void* workspace, size_t workspace_bytes, rf_stream_t stream);
 
+/* Fill for callers that cannot allocate device memory (the pages have no
+ * counterpart; this is a library convenience). Some callers have no way to get
+ * scratch memory on the GPU: a plugin inside a serving engine whose device memory
+ * all belongs to the engine's own pool, or a latency-critical path where a
+ * cudaMalloc would synchronise the device. This call computes exactly what
+ * rf_fill_kv computes, with the same arguments minus the workspace: its scratch
+ * is a fixed 256-byte aligned array of RF_STATIC_SCRATCH_BYTES inside the
+ * library's device code, which every GPU that loads the library keeps until the
+ * process exits. It makes no allocating call.
+ *   - Fills whose rf_fill_workspace_bytes(desc) exceeds RF_STATIC_SCRATCH_BYTES
+ *     are rejected with RF_ERR_WORKSPACE before anything runs.
+ *   - The first call on each device looks up the array's device address (and may
+ *     load the library's device code there); make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the array, which keeps the previous call's
+ *     contents; nothing in it needs clearing between calls. Calls that overlap
+ *     on the GPU race on it: order them on one stream. */
+#define RF_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)
+rf_status rf_fill_kv_static(const rf_fill_desc* desc,
+                            const rf_bf16* x_S, int64_t ld_x,
+                            const uint8_t* exact_mask,
+                            const rf_bf16* A, const float* b, const rf_bf16* Wkv,
+                            rf_bf16* k_cache, rf_bf16* v_cache,
+                            int64_t layer_stride, int64_t row_stride,
+                            int32_t* n_fill_out, int32_t* dev_status, rf_stream_t stream);
+
 /* ===================================================================== *
  * Calibration statistics ([RF] "Ridge map": only XᵀX, XᵀY_l and the two means
  * are accumulated in one pass; [XM]: XᵀX is the dominant fitting cost)

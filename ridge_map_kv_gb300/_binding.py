@@ -67,6 +67,8 @@ _SIGS = {
     "rf_fill_kv": (c_int, [POINTER(rf_fill_desc), c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p,
                            c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p, c_size_t,
                            c_void_p]),
+    "rf_fill_kv_static": (c_int, [POINTER(rf_fill_desc), c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
+                                  c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p]),
     "rf_calib_workspace_bytes": (c_size_t, [POINTER(rf_calib_desc), c_int64]),
     "rf_calib_accumulate": (c_int, [POINTER(rf_calib_desc), c_void_p, c_int64, c_void_p, c_int64, c_int64,
                                     c_int64, POINTER(rf_calib_stats), c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -178,6 +180,18 @@ def rf_fill_kv(desc, x_S, ld_x, exact_mask, A, b, Wkv, k_cache, v_cache, layer_s
     _check(lib().rf_fill_kv(ctypes.byref(desc), _p(x_S), int(ld_x), _p(exact_mask), _p(A), _p(b), _p(Wkv),
                             _p(k_cache), _p(v_cache), int(layer_stride), int(row_stride), _p(n_fill_out),
                             _p(dev_status), _p(workspace), int(workspace_bytes), _s(stream)), "rf_fill_kv")
+
+
+RF_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def rf_fill_kv_static(desc, x_S, ld_x, exact_mask, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride,
+                      n_fill_out=None, dev_status=None, stream=None):
+    """rf_fill_kv for callers that cannot allocate device memory: the library's own
+    fixed 64 MiB device array serves as scratch (see include/rf.h)."""
+    _check(lib().rf_fill_kv_static(ctypes.byref(desc), _p(x_S), int(ld_x), _p(exact_mask), _p(A), _p(b), _p(Wkv),
+                                   _p(k_cache), _p(v_cache), int(layer_stride), int(row_stride), _p(n_fill_out),
+                                   _p(dev_status), _s(stream)), "rf_fill_kv_static")
 
 
 # ----------------------------------------------------------------- calibration

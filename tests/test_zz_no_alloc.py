@@ -1,0 +1,105 @@
+"""rf_fill_kv_static: the fill for callers that cannot allocate device memory.
+
+A plugin inside a serving engine that owns all device memory through its own
+pool, or a latency-critical path where a cudaMalloc would synchronise the device,
+cannot hand the library a workspace. rf_fill_kv_static keeps its scratch in a
+fixed array inside the library instead. These tests call it twice in a row
+through the C ABI, on two different fills, and check each result against
+rf_fill_kv run with a caller workspace on the same inputs; then they check that a
+fill too large for the fixed array is refused before anything runs.
+
+This file is collected last on purpose, and it needs nothing from the other
+tests: it passes alone in a fresh process and after the rest of the suite.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import ridge_map_kv_gb300 as rf
+import synth
+from fillcheck import TOL_MAX, TOL_MEAN, desc_of
+
+pytestmark = pytest.mark.gpu
+
+
+def _cfg(name, **kw):
+    base = dict(name=name, index=91, d=512, L=5, S=2, N=400, T=37, H=2, hd=128, rope_theta=5e5,
+                exact="uniform10", lam=0.03, calib_n=0)
+    base.update(kw)
+    return synth.FillConfig(**base)
+
+
+def _prepare(cfg):
+    dev = torch.device("cuda")
+    inp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in synth.fill_inputs(cfg).items()}
+    desc = desc_of(cfg)
+    Wkv = torch.empty((cfg.P, 2 * cfg.KV, cfg.d), dtype=torch.bfloat16, device=dev)
+    rf.rf_fold_kv_weights(desc, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
+    return desc, inp, Wkv
+
+
+def _caches(cfg):
+    return (synth.canary_cache(cfg.L, cfg.N, cfg.H, cfg.hd, 0, "cuda"),
+            synth.canary_cache(cfg.L, cfg.N, cfg.H, cfg.hd, 1, "cuda"))
+
+
+def _out():
+    return torch.full((1,), -1, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _compare(cfg, inp, got_k, got_v, ref_k, ref_v):
+    mask = None if inp["mask"] is None else inp["mask"].cpu().numpy()
+    idx = O.prefix_partition(cfg.N, cfg.T, mask)
+    written = np.zeros((cfg.L, cfg.N), bool)
+    written[cfg.S:, idx] = True
+    for got, ref in ((got_k, ref_k), (got_v, ref_v)):
+        gb, rb = synth.bits(got), synth.bits(ref)
+        assert np.array_equal(gb[~written], rb[~written]), "entries outside the filled set differ"
+        e = np.linalg.norm(O.bf16_bits_to_f64(gb[written]) - O.bf16_bits_to_f64(rb[written]), axis=-1)
+        e = e / np.maximum(np.linalg.norm(O.bf16_bits_to_f64(rb[written]), axis=-1), 1e-6)
+        assert np.all(np.isfinite(e)) and e.max() <= TOL_MAX and e.mean() <= TOL_MEAN, (e.max(), e.mean())
+
+
+def test_static_fill_matches_workspace_fill_on_two_calls_in_a_row():
+    cfgs = [_cfg("static fill A"),
+            _cfg("static fill B", index=92, d=768, L=4, S=2, N=300, T=20, H=4, hd=64, exact="blocks16_5")]
+    prepared = [_prepare(c) for c in cfgs]
+
+    # references through rf_fill_kv with a caller workspace
+    refs = []
+    for cfg, (desc, inp, Wkv) in zip(cfgs, prepared):
+        kc, vc = _caches(cfg)
+        nf, st = _out()
+        ws_bytes = rf.rf_fill_workspace_bytes(desc)
+        assert ws_bytes <= rf.RF_STATIC_SCRATCH_BYTES
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        rf.rf_fill_kv(desc, inp["x_S"], cfg.d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc, cfg.N * cfg.KV, cfg.KV,
+                      nf, st, ws, ws_bytes)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        refs.append((kc, vc, int(nf.item())))
+
+    # the two static-scratch calls, back to back on one stream
+    outs = []
+    for cfg, (desc, inp, Wkv) in zip(cfgs, prepared):
+        kc, vc = _caches(cfg)
+        nf, st = _out()
+        rf.rf_fill_kv_static(desc, inp["x_S"], cfg.d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
+                             cfg.N * cfg.KV, cfg.KV, nf, st)
+        outs.append((kc, vc, nf, st))
+    torch.cuda.synchronize()
+
+    for cfg, (desc, inp, Wkv), (rk, rv, rn), (kc, vc, nf, st) in zip(cfgs, prepared, refs, outs):
+        assert int(st.item()) == 0
+        assert int(nf.item()) == rn
+        _compare(cfg, inp, kc, vc, rk, rv)
+
+
+def test_static_fill_refuses_fills_larger_than_its_scratch():
+    desc = desc_of(synth.LLAMA8B)
+    assert rf.rf_fill_workspace_bytes(desc) > rf.RF_STATIC_SCRATCH_BYTES
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_fill_kv_static(desc, None, synth.LLAMA8B.d, None, None, None, None, None, None, 0, 0)
+    assert ei.value.status == rf.RF_ERR_WORKSPACE
+    assert "static scratch" in str(ei.value)
