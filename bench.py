@@ -108,6 +108,14 @@ def reduce_sum(x: float, device=None) -> float:
     return float(t.item())
 
 
+def aggregate_timing(units_per_step: float, steps: int, elapsed_ms: float, device=None):
+    """Whole-job throughput: every rank's units over the slowest rank's time.
+    Returns (value per second, ms per step, max elapsed ms)."""
+    t_max = reduce_max(elapsed_ms, device)
+    total = reduce_sum(float(units_per_step) * steps, device)
+    return total / (t_max / 1e3), t_max / steps, t_max
+
+
 # --------------------------------------------------------------------------- #
 # Clock sampling during the timed region
 # --------------------------------------------------------------------------- #
@@ -303,10 +311,7 @@ def run_ours(args):
     prof = rf.rf_profile_stop()
     elapsed_ms = e0.elapsed_time(e1)
     assert int(status.item()) == 0
-    t_max = reduce_max(elapsed_ms, dev)
-    total_units = reduce_sum(float(units * args.steps), dev)
-    value = total_units / (t_max / 1e3)
-    ms_per_step = t_max / args.steps
+    value, ms_per_step, t_max = aggregate_timing(units, args.steps, elapsed_ms, dev)
 
     stage_ms = {}
     for name, ms in prof:
@@ -359,10 +364,10 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier()
         assert int(outh[0]) == n_fill and int(outh[1]) == 0
-        t_e2e = reduce_max(e0.elapsed_time(e1), dev)
-        e2e = {"value": total_units / (t_e2e / 1e3), "unit": UNIT,
+        e2e_value, e2e_ms, _ = aggregate_timing(units, args.steps, e0.elapsed_time(e1), dev)
+        e2e = {"value": e2e_value, "unit": UNIT,
                "h2d_bytes_per_step": xh.numel() * 2 + mh.numel(), "d2h_bytes_per_step": 8,
-               "ms_per_step": t_e2e / args.steps}
+               "ms_per_step": e2e_ms}
 
     cpu = None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:

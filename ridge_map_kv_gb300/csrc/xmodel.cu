@@ -1,0 +1,304 @@
+// Cross-model per-head ridge mapper (rf_xmodel_map) and RoPE on cache rows
+// (rf_rope_rows).
+//
+// [XM] "Cross-Model KV Cache Transfer in LLM Families", content-space mapping:
+//   K̂_t = (K_s R_s^-1(t) W_K + b_K) R_t(t); V is mapped without RoPE. The k source
+// layers chosen for a target layer are concatenated (all heads), and mapper
+// inference is one batched matmul per target layer.
+//
+// Launch sequence on the caller's stream:
+//   1. k_rope_table x2   cos/sin tables for θ_src and θ_tgt (fp64 angles)
+//   2. k_rope_rows       un-rope every source layer's keys once into the workspace
+//   3. tc_gemm<XMProb>   for every target layer l, M-tile of rows and N-tile of
+//                        [K | V] columns: A = the selected source features (the
+//                        K-loop walks the k source layers, 64 features per step,
+//                        reading the table src[l][j]), B = W_K or W_V of layer l;
+//                        epilogue: + b, target RoPE on K, store into the target
+//                        caches (16-byte stores).
+#include <algorithm>
+#include <vector>
+
+#include "epilogue.cuh"
+#include "rf_host.h"
+#include "tc_gemm.cuh"
+
+namespace rf {
+
+__global__ void k_rope_table(float* cos_t, float* sin_t, int n_rows, int half, double theta, long long pos_offset);
+
+// out[row][h][:] = R^{sign}(pos) in[row][h][:], pos = row % rows_per_position + pos_offset.
+// With a table (cos_t, sin_t: [rows_per_position][hd/2]) the angle comes from it;
+// without, the angle is computed here (fp64 angle, fp64 reduction mod 2π, sincosf).
+// Each thread handles 8 rotation pairs of one head of one row.
+__global__ void __launch_bounds__(256) k_rope_rows(const __nv_bfloat16* __restrict__ in, __nv_bfloat16* out,
+                                                   long long n_rows, long long ld_in, long long ld_out, int n_heads,
+                                                   int hd, long long rows_per_position, long long pos_offset,
+                                                   const float* __restrict__ cos_t, const float* __restrict__ sin_t,
+                                                   double theta, float sign) {
+  const int half = hd >> 1;
+  const int chunks = half / 8;
+  const long long total = n_rows * n_heads * chunks;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int ch = static_cast<int>(idx % chunks);
+    const long long rh = idx / chunks;
+    const int h = static_cast<int>(rh % n_heads);
+    const long long row = rh / n_heads;
+    const long long t = row % rows_per_position;
+    const int i0 = ch * 8;
+    const __nv_bfloat16* src = in + row * ld_in + static_cast<long long>(h) * hd;
+    const uint4 a = *reinterpret_cast<const uint4*>(src + i0);
+    const uint4 b = *reinterpret_cast<const uint4*>(src + half + i0);
+    float c[8], s[8];
+    if (cos_t != nullptr) {
+      const float4* cp = reinterpret_cast<const float4*>(cos_t + t * half + i0);
+      const float4* sp = reinterpret_cast<const float4*>(sin_t + t * half + i0);
+      const float4 c0 = cp[0], c1 = cp[1], s0 = sp[0], s1 = sp[1];
+      c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w; c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+      s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w; s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
+    } else {
+      const double kInv2Pi = 0.15915494309189535, k2PiHi = 6.283185307179586, k2PiLo = 2.4492935982947064e-16;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const double ang = static_cast<double>(t + pos_offset) * pow(theta, -2.0 * (i0 + q) / hd);
+        const double k = rint(ang * kInv2Pi);
+        double r = fma(-k, k2PiHi, ang);
+        r = fma(-k, k2PiLo, r);
+        sincosf(static_cast<float>(r), &s[q], &c[q]);
+      }
+    }
+    const __nv_bfloat162* ah = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* bh = reinterpret_cast<const __nv_bfloat162*>(&b);
+    uint4 o1, o2;
+    uint32_t* u1 = reinterpret_cast<uint32_t*>(&o1);
+    uint32_t* u2 = reinterpret_cast<uint32_t*>(&o2);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 x1 = __bfloat1622float2(ah[q]);
+      const float2 x2 = __bfloat1622float2(bh[q]);
+      const float sa = sign * s[2 * q], sb = sign * s[2 * q + 1];
+      u1[q] = pack_bf16x2(x1.x * c[2 * q] - x2.x * sa, x1.y * c[2 * q + 1] - x2.y * sb);
+      u2[q] = pack_bf16x2(x2.x * c[2 * q] + x1.x * sa, x2.y * c[2 * q + 1] + x1.y * sb);
+    }
+    __nv_bfloat16* dst = out + row * ld_out + static_cast<long long>(h) * hd;
+    *reinterpret_cast<uint4*>(dst + i0) = o1;
+    *reinterpret_cast<uint4*>(dst + half + i0) = o2;
+  }
+}
+
+struct XMProb {
+  CUtensorMap tmKu;  // un-roped source keys   {KV, L_src*N}, box {64, 128}
+  CUtensorMap tmVs;  // source values          {KV, L_src*N}, box {64, 128}
+  CUtensorMap tmWk;  // W_K                    {k*KV, L_tgt*KV}, box {64, 256}
+  CUtensorMap tmWv;  // W_V
+  const int32_t* src;  // [L_tgt][k]
+  const float* bk;     // [L_tgt][KV]
+  const float* bv;
+  const float* cos_t;  // target table [N][hd/2]
+  const float* sin_t;
+  __nv_bfloat16* k_tgt;  // [L_tgt][N][KV]
+  __nv_bfloat16* v_tgt;
+  int N, KV, hd, k, L_tgt, m_tiles, n_half;
+  int32_t* dev_status;
+  uint64_t timeout_ns;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+
+  __device__ void prefetch() const {
+    tma_prefetch_desc(&tmKu);
+    tma_prefetch_desc(&tmVs);
+    tma_prefetch_desc(&tmWk);
+    tma_prefetch_desc(&tmWv);
+  }
+  __device__ int num_units() const { return L_tgt * m_tiles * 2 * n_half; }
+  __device__ int num_subtiles(int) const { return 1; }
+  __device__ int num_kb(int, int) const { return k * KV / kBK; }
+  // Unit order: target layer, M-tile, then the 2*n_half N-tiles (K then V), so
+  // the CTAs in flight reuse one strip of features and one layer's W from L2.
+  __device__ void decode(int u, int& l, int& mt, int& nt) const {
+    const int per_layer = m_tiles * 2 * n_half;
+    l = u / per_layer;
+    const int r = u - l * per_layer;
+    mt = r / (2 * n_half);
+    nt = r - mt * 2 * n_half;
+  }
+  __device__ void issue_loads(int u, int, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    int l, mt, nt;
+    decode(u, l, mt, nt);
+    const bool is_k = nt < n_half;
+    const int f0 = kb * kBK;
+    const int j = f0 / KV;
+    const int c = f0 - j * KV;
+    const int s = __ldg(src + l * k + j);
+    tma_load_2d(sa, is_k ? &tmKu : &tmVs, bar, c, s * N + mt * kBM);
+    tma_load_2d(sb, is_k ? &tmWk : &tmWv, bar, f0, l * KV + (is_k ? nt : nt - n_half) * kBN);
+  }
+  __device__ void epilogue(int u, int, uint32_t tacc, int row) const {
+    int l, mt, nt;
+    decode(u, l, mt, nt);
+    const bool is_k = nt < n_half;
+    const int col0 = (is_k ? nt : nt - n_half) * kBN;
+    const int t = mt * kBM + row;
+    const bool valid = t < N;
+    const int tt = valid ? t : 0;
+    const int half = hd >> 1;
+    const float* cs = cos_t + static_cast<size_t>(tt) * half;
+    const float* sn = sin_t + static_cast<size_t>(tt) * half;
+    const float* bias = (is_k ? bk : bv) + static_cast<size_t>(l) * KV + col0;
+    __nv_bfloat16* dst = (is_k ? k_tgt : v_tgt) + (static_cast<size_t>(l) * N + tt) * KV + col0;
+#pragma unroll 1
+    for (int hh = 0; hh < kBN / hd; ++hh)
+      emit_head(tacc + hh * hd, hd, 1.0f, bias + hh * hd, is_k, cs, sn, dst + hh * hd, valid);
+  }
+};
+
+static uint64_t g_xm_attr = 0;
+
+struct XLayout {
+  __nv_bfloat16* ku;
+  int32_t* src;
+  float* cos_s;
+  float* sin_s;
+  float* cos_t;
+  float* sin_t;
+  size_t bytes;
+};
+
+static XLayout xmodel_layout(const rf_xmodel_desc* d, void* ws) {
+  const int64_t KV = d->n_kv_heads * d->head_dim;
+  Carve c(ws);
+  XLayout l;
+  l.ku = c.take<__nv_bfloat16>(d->L_src * d->N * KV);
+  l.src = c.take<int32_t>(d->L_tgt * d->k);
+  l.cos_s = c.take<float>(d->N * (d->head_dim / 2));
+  l.sin_s = c.take<float>(d->N * (d->head_dim / 2));
+  l.cos_t = c.take<float>(d->N * (d->head_dim / 2));
+  l.sin_t = c.take<float>(d->N * (d->head_dim / 2));
+  l.bytes = c.bytes();
+  return l;
+}
+
+static rf_status check_xmodel_desc(const rf_xmodel_desc* d) {
+  if (d == nullptr) return fail(RF_ERR_INVALID_ARG, "desc is NULL");
+  if (d->L_src <= 0 || d->L_tgt <= 0 || d->k <= 0 || d->n_kv_heads <= 0 || d->head_dim <= 0 || d->N <= 0)
+    return fail(RF_ERR_INVALID_ARG, "need L_src, L_tgt, k, H, hd, N > 0");
+  if (!(d->theta_src > 0.0) || !(d->theta_tgt > 0.0)) return fail(RF_ERR_INVALID_ARG, "RoPE bases must be > 0");
+  if (d->head_dim != 64 && d->head_dim != 128) return fail(RF_ERR_SHAPE, "head_dim must be 64 or 128");
+  const int64_t KV = d->n_kv_heads * d->head_dim;
+  if (KV % kBN != 0) return fail(RF_ERR_SHAPE, "n_kv_heads * head_dim = %lld must be a multiple of 256", (long long)KV);
+  if (d->L_src * d->N >= (int64_t(1) << 31) || d->L_tgt * KV >= (int64_t(1) << 31) || d->k * KV >= (int64_t(1) << 31))
+    return fail(RF_ERR_SHAPE, "sizes exceed 2^31 rows or features");
+  if (d->N > (int64_t(1) << 30)) return fail(RF_ERR_SHAPE, "N must be <= 2^30");
+  return RF_OK;
+}
+
+}  // namespace rf
+
+using namespace rf;
+
+extern "C" size_t rf_xmodel_workspace_bytes(const rf_xmodel_desc* desc) {
+  if (check_xmodel_desc(desc) != RF_OK) return 0;
+  return xmodel_layout(desc, nullptr).bytes;
+}
+
+extern "C" rf_status rf_xmodel_map(const rf_xmodel_desc* desc, const int32_t* src_layers, const rf_bf16* k_src,
+                                   const rf_bf16* v_src, const rf_bf16* Wk, const float* bk, const rf_bf16* Wv,
+                                   const float* bv, rf_bf16* k_tgt, rf_bf16* v_tgt, int32_t* dev_status,
+                                   void* workspace, size_t workspace_bytes, rf_stream_t stream) {
+  clear_error();
+  rf_status st = check_xmodel_desc(desc);
+  if (st != RF_OK) return st;
+  if (src_layers == nullptr) return fail(RF_ERR_INVALID_ARG, "src_layers is NULL");
+  for (int64_t i = 0; i < desc->L_tgt * desc->k; ++i)
+    if (src_layers[i] < 0 || src_layers[i] >= desc->L_src)
+      return fail(RF_ERR_INVALID_ARG, "src_layers[%lld] = %d is outside [0, L_src)", (long long)i, src_layers[i]);
+  if (!k_src || !v_src || !Wk || !bk || !Wv || !bv || !k_tgt || !v_tgt)
+    return fail(RF_ERR_INVALID_ARG, "tensor pointers must be non-NULL");
+  if (!aligned16(k_src) || !aligned16(v_src) || !aligned16(Wk) || !aligned16(bk) || !aligned16(Wv) || !aligned16(bv) ||
+      !aligned16(k_tgt) || !aligned16(v_tgt))
+    return fail(RF_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
+  XLayout lay = xmodel_layout(desc, workspace);
+  if (workspace == nullptr || workspace_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", lay.bytes, workspace_bytes);
+  int sms = 0;
+  if ((st = current_device(&sms)) != RF_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t KV = desc->n_kv_heads * desc->head_dim, N = desc->N;
+  const int half = static_cast<int>(desc->head_dim / 2);
+
+  // the layer table is copied from host memory before this call returns
+  if ((st = cuda_check(cudaMemcpyAsync(lay.src, src_layers, sizeof(int32_t) * desc->L_tgt * desc->k,
+                                       cudaMemcpyHostToDevice, s), "copy src_layers")) != RF_OK)
+    return st;
+  {
+    ProfScope prof(s, RF_STAGE_ROPE_TABLE);
+    const int blocks = static_cast<int>(std::min<int64_t>((N * half + 255) / 256, 4LL * sms));
+    k_rope_table<<<blocks, 256, 0, s>>>(lay.cos_s, lay.sin_s, static_cast<int>(N), half, desc->theta_src,
+                                        static_cast<long long>(desc->pos_offset));
+    k_rope_table<<<blocks, 256, 0, s>>>(lay.cos_t, lay.sin_t, static_cast<int>(N), half, desc->theta_tgt,
+                                        static_cast<long long>(desc->pos_offset));
+  }
+  {
+    ProfScope prof(s, RF_STAGE_UNROPE);
+    const long long n_rows = desc->L_src * N;
+    const long long total = n_rows * desc->n_kv_heads * (half / 8);
+    const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 16LL * sms));
+    k_rope_rows<<<blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(k_src), lay.ku, n_rows, KV, KV,
+                                       static_cast<int>(desc->n_kv_heads), static_cast<int>(desc->head_dim), N, 0,
+                                       lay.cos_s, lay.sin_s, 0.0, -1.0f);
+  }
+  if ((st = cuda_check(cudaGetLastError(), "rope launches")) != RF_OK) return st;
+
+  if ((st = set_smem_attr(reinterpret_cast<const void*>(&tc_gemm_kernel<XMProb>), kGemmSmemBytes, &g_xm_attr)) != RF_OK)
+    return st;
+  XMProb pr;
+  const int64_t rows = desc->L_src * N;
+  if ((st = make_tmap_bf16_2d(&pr.tmKu, lay.ku, KV, rows, KV, kBK, kBM)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmVs, v_src, KV, rows, KV, kBK, kBM)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmWk, Wk, desc->k * KV, desc->L_tgt * KV, desc->k * KV, kBK, kBN)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmWv, Wv, desc->k * KV, desc->L_tgt * KV, desc->k * KV, kBK, kBN)) != RF_OK) return st;
+  pr.src = lay.src;
+  pr.bk = bk;
+  pr.bv = bv;
+  pr.cos_t = lay.cos_t;
+  pr.sin_t = lay.sin_t;
+  pr.k_tgt = reinterpret_cast<__nv_bfloat16*>(k_tgt);
+  pr.v_tgt = reinterpret_cast<__nv_bfloat16*>(v_tgt);
+  pr.N = static_cast<int>(N);
+  pr.KV = static_cast<int>(KV);
+  pr.hd = static_cast<int>(desc->head_dim);
+  pr.k = static_cast<int>(desc->k);
+  pr.L_tgt = static_cast<int>(desc->L_tgt);
+  pr.m_tiles = static_cast<int>((N + kBM - 1) / kBM);
+  pr.n_half = static_cast<int>(KV / kBN);
+  pr.dev_status = dev_status;
+  pr.timeout_ns = wait_timeout_ns();
+  const int64_t units = desc->L_tgt * pr.m_tiles * 2 * pr.n_half;
+  const int grid = static_cast<int>(std::min<int64_t>(units, sms));
+  ProfScope prof(s, RF_STAGE_XMODEL_GEMM);
+  tc_gemm_kernel<XMProb><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(pr);
+  return cuda_check(cudaGetLastError(), "cross-model GEMM launch");
+}
+
+extern "C" rf_status rf_rope_rows(const rf_bf16* in, rf_bf16* out, int64_t n_rows, int64_t ld, int64_t n_heads,
+                                  int64_t head_dim, double theta, int64_t pos_offset, int inverse,
+                                  rf_stream_t stream) {
+  clear_error();
+  if (n_rows < 0 || n_heads <= 0 || !(theta > 0.0)) return fail(RF_ERR_INVALID_ARG, "need n_rows >= 0, n_heads > 0, theta > 0");
+  if (head_dim != 64 && head_dim != 128) return fail(RF_ERR_SHAPE, "head_dim must be 64 or 128");
+  if (ld < n_heads * head_dim || ld % 8 != 0) return fail(RF_ERR_ALIGN, "ld must be >= n_heads*head_dim and a multiple of 8");
+  if (n_rows == 0) return RF_OK;
+  if (!in || !out) return fail(RF_ERR_INVALID_ARG, "in and out must be non-NULL");
+  if (!aligned16(in) || !aligned16(out)) return fail(RF_ERR_ALIGN, "in and out must be 16-byte aligned");
+  int sms = 0;
+  rf_status st = current_device(&sms);
+  if (st != RF_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long total = n_rows * n_heads * (head_dim / 16);
+  const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 16LL * sms));
+  ProfScope prof(s, RF_STAGE_UNROPE);
+  k_rope_rows<<<blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(in), reinterpret_cast<__nv_bfloat16*>(out),
+                                     n_rows, ld, ld, static_cast<int>(n_heads), static_cast<int>(head_dim), n_rows,
+                                     pos_offset, nullptr, nullptr, theta, inverse ? -1.0f : 1.0f);
+  return cuda_check(cudaGetLastError(), "k_rope_rows launch");
+}

@@ -1,0 +1,118 @@
+"""CPU-only checks of the C ABI: librf.so loads without a GPU, exports every
+function include/rf.h declares, and rejects bad arguments on the host (before any
+launch, so no GPU is touched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ridge_map_kv_gb300 as rf
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    if not os.path.exists(rf.LIB_PATH):
+        from ridge_map_kv_gb300 import build
+        build.build()
+    rf.lib()
+
+
+def _declared_functions():
+    txt = open(os.path.join(ROOT, "include", "rf.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(rf_[a-z0-9_]+)\s*\(", txt)))
+
+
+def test_library_exports_every_declared_function():
+    names = _declared_functions()
+    assert len(names) >= 19
+    L = ctypes.CDLL(rf.LIB_PATH)
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_function():
+    from ridge_map_kv_gb300 import _binding
+    assert set(_declared_functions()) <= set(_binding._SIGS)
+
+
+def test_status_strings_and_version():
+    assert rf.rf_version() >= 100
+    assert rf.rf_status_string(rf.RF_OK) == "ok"
+    assert "timed out" in rf.rf_status_string(rf.RF_ERR_TIMEOUT)
+    assert rf.rf_status_string(999) == "unknown status"
+    for s in ("compact", "map_gemm", "kv_gemm", "calib_gemm", "xmodel_gemm"):
+        assert s in [rf.rf_stage_name(i) for i in range(1, 12)]
+
+
+def _fill_desc(**kw):
+    c = synth.TOY
+    d = dict(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
+             rms_eps=c.rms_eps, pos_offset=0)
+    d.update(kw)
+    return rf.rf_fill_desc(**d)
+
+
+def test_fill_workspace_size_follows_the_layout():
+    desc = _fill_desc()
+    # fill_idx, n_fill, Xf [128 x d], x̂ [P x 128 x d], ss partials [P x d/256 x 128], cos/sin [n_prefix x hd/2]
+    r = lambda x: (x + 255) // 256 * 256
+    n_prefix, M, P, d, half = 9, 128, 4, 256, 32
+    want = r(n_prefix * 4) + r(4) + r(M * d * 2) + r(P * M * d * 2) + r(P * (d // 256) * M * 4) \
+        + r(n_prefix * half * 4) + r(n_prefix * half * 4)
+    assert rf.rf_fill_workspace_bytes(desc) == want
+
+
+@pytest.mark.parametrize("bad", [dict(d=100), dict(head_dim=96), dict(S=9), dict(T=13), dict(n_kv_heads=1),
+                                 dict(rope_theta=0.0)])
+def test_fill_rejects_bad_descriptors_on_the_host(bad):
+    desc = _fill_desc(**bad)
+    assert rf.rf_fill_workspace_bytes(desc) == 0
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_fill_kv(desc, 16, 256, None, 16, 16, 16, 16, 16, 0, 128, None, None, 256, 1 << 30, stream=0)
+    assert ei.value.status in (rf.RF_ERR_INVALID_ARG, rf.RF_ERR_SHAPE)
+
+
+def test_fill_rejects_null_and_misaligned_pointers_and_small_workspace():
+    desc = _fill_desc()
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_fill_kv(desc, 256, 256, None, None, 256, 256, 256, 256, 0, 128, None, None, 256, 1 << 30, stream=0)
+    assert ei.value.status == rf.RF_ERR_INVALID_ARG
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_fill_kv(desc, 258, 256, None, 256, 256, 256, 256, 256, 0, 128, None, None, 256, 1 << 30, stream=0)
+    assert ei.value.status == rf.RF_ERR_ALIGN
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_fill_kv(desc, 256, 256, None, 256, 256, 256, 256, 256, 0, 100, None, None, 256, 1 << 30, stream=0)
+    assert ei.value.status == rf.RF_ERR_ALIGN
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_fill_kv(desc, 256, 256, None, 256, 256, 256, 256, 256, 0, 128, None, None, 256, 1024, stream=0)
+    assert ei.value.status == rf.RF_ERR_WORKSPACE
+    assert "workspace" in rf.rf_last_error()
+
+
+def test_calib_and_xmodel_and_solve_validate_on_the_host():
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_calib_accumulate(rf.rf_calib_desc(d_in=100, d_out=256, n_maps=1), 256, 256, 256, 256, 0, 8,
+                               rf.calib_stats_struct(256, 256, 256, 256, 256), stream=0)
+    assert ei.value.status == rf.RF_ERR_SHAPE
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_solve(rf.rf_calib_desc(d_in=256, d_out=256, n_maps=1), rf.calib_stats_struct(256, 256, 256, 256, 256),
+                    0.03, 7, 0, 256, 256, workspace=256, workspace_bytes=1 << 30, stream=0)
+    assert ei.value.status == rf.RF_ERR_INVALID_ARG
+    xd = rf.rf_xmodel_desc(L_src=4, L_tgt=2, k=2, n_kv_heads=2, head_dim=128, N=64, theta_src=1e6, theta_tgt=1e6,
+                           pos_offset=0)
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_xmodel_map(xd, [[0, 1], [2, 9]], 256, 256, 256, 256, 256, 256, 256, 256, workspace=256,
+                         workspace_bytes=1 << 34, stream=0)
+    assert ei.value.status == rf.RF_ERR_INVALID_ARG
+    assert "src_layers" in rf.rf_last_error()
+
+
+def test_static_fill_scratch_constant_matches_header():
+    txt = open(os.path.join(ROOT, "include", "rf.h")).read()
+    assert "RF_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)" in txt
+    assert rf.RF_STATIC_SCRATCH_BYTES == 64 * 1024 * 1024

@@ -1,0 +1,193 @@
+"""GPU parity of rf_calib_accumulate and rf_solve against the fp64 oracle.
+
+Calibration sums: every entry on small cases (ragged batches and row chunks),
+sampled entries at full width (27B-shaped d=5120, and the cross-model Gram 8192^2
+over 131,072 rows). Tolerance: |ΔG_ij| <= 1e-5 sqrt(G_ii G_jj), the same scale for C
+with the y column's sum of squares.
+Solve: on the toy, the fp32 solve (with fp64 refinement) equals the oracle's A
+and b within 1e-5 relative (Frobenius per map); at full width d=4096, sampled
+rows of A match and satisfy the normal equations.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import ridge_map_kv_gb300 as rf
+import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _zeros_stats(d_in, d_out, P):
+    return {"G": torch.zeros((d_in, d_in), dtype=torch.float64, device=DEV),
+            "C": torch.zeros((max(P, 1), d_in, d_out), dtype=torch.float64, device=DEV),
+            "sx": torch.zeros(d_in, dtype=torch.float64, device=DEV),
+            "sy": torch.zeros((max(P, 1), d_out), dtype=torch.float64, device=DEV),
+            "n": torch.zeros(1, dtype=torch.int64, device=DEV)}
+
+
+def _struct(st):
+    return rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
+
+
+def _accumulate(X, Y, st, row_splits):
+    n, d_in = X.shape
+    P, _, d_out = Y.shape
+    desc = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    bounds = [0] + list(row_splits) + [n]
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        rf.rf_calib_accumulate(desc, X[a:], d_in, Y[:, a:], d_out, n * d_out, b - a, _struct(st), status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+
+def _f64(t):
+    return O.bf16_bits_to_f64(synth.bits(t))
+
+
+def _check_stats(st, ref, Yref_sq=None, rows=None, cols_x=None, cols_y=None):
+    G = st["G"].cpu().numpy()
+    C = st["C"].cpu().numpy()
+    if cols_x is not None:
+        G = G[np.ix_(cols_x, cols_x)]
+        C = C[:, cols_x][:, :, cols_y]
+    dg = np.sqrt(np.diag(ref["G"]))
+    tolG = 1e-5 * np.outer(dg, dg)
+    assert np.all(np.abs(G - ref["G"]) <= tolG), np.max(np.abs(G - ref["G"]) / tolG)
+    if ref["C"].shape[0] and C.size:
+        ysq = np.sqrt(Yref_sq)                                       # [P, d_out]
+        tolC = 1e-5 * dg[None, :, None] * ysq[:, None, :]
+        assert np.all(np.abs(C - ref["C"]) <= tolC), np.max(np.abs(C - ref["C"]) / tolC)
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 4, 2048, [1000]), (512, 768, 3, 3000, []), (256, 512, 1, 100, [40])],
+                         ids=["toy two batches", "3 chunks ragged", "tiny ragged batches"])
+def test_calib_sums_match_oracle(shape):
+    d_in, d_out, P, n, splits = shape
+    cal = synth.calib_inputs(d_in, d_out, P, n, index=0 if d_in == 256 and P == 4 else 93)
+    X, Y = cal["X"].to(DEV), cal["Y"].to(DEV)
+    st = _zeros_stats(d_in, d_out, P)
+    _accumulate(X, Y, st, splits)
+    Xf, Yf = _f64(cal["X"]), _f64(cal["Y"])
+    ref = O.calib_stats(Xf, Yf)
+    _check_stats(st, ref, (Yf ** 2).sum(axis=1))
+    assert int(st["n"].item()) == n
+    np.testing.assert_allclose(st["sx"].cpu().numpy(), ref["sx"], rtol=0, atol=1e-6 * np.abs(Xf).sum(0).max())
+    np.testing.assert_allclose(st["sy"].cpu().numpy(), ref["sy"], rtol=0, atol=1e-6 * np.abs(Yf).sum(1).max())
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("d_in,d_out,P,n", [(5120, 5120, 2, 16384), (8192, 256, 0, 131072)],
+                         ids=["27b-shaped XtX and XtY", "cross-model Gram 8192^2 x 131072 rows"])
+def test_calib_full_width_sampled(d_in, d_out, P, n):
+    cal = synth.calib_inputs(d_in, d_out, max(P, 1), n, index=3 if P else 4, device=DEV, noise=0.05)
+    X, Y = cal["X"], cal["Y"][:P] if P else cal["Y"][:0]
+    st = _zeros_stats(d_in, d_out, P)
+    desc = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rf.rf_calib_accumulate(desc, X, d_in, Y if P else None, d_out, n * d_out, n, _struct(st), status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rng = np.random.default_rng(5)
+    cx = np.sort(rng.choice(d_in, 96, replace=False))
+    cy = np.sort(rng.choice(d_out, 64, replace=False))
+    Xs = _f64(X[:, torch.as_tensor(cx, device=DEV)])
+    if P:
+        Ys = _f64(Y[:, :, torch.as_tensor(cy, device=DEV)])
+        ref = O.calib_stats(Xs, Ys)
+    else:  # Gram only: the oracle's sums of X, with its C (of a dummy Y) left unused
+        ref = O.calib_stats(Xs, np.zeros((1, n, 1)))
+        ref["C"] = np.zeros((0, len(cx), len(cy)))
+    _check_stats(st, ref, (Ys ** 2).sum(axis=1) if P else None, cols_x=cx, cols_y=cy)
+
+
+# --------------------------------------------------------------------------- #
+# Solve
+# --------------------------------------------------------------------------- #
+def _upload_stats(ref):
+    P = ref["C"].shape[0]
+    return {"G": torch.as_tensor(ref["G"], device=DEV), "C": torch.as_tensor(ref["C"], device=DEV),
+            "sx": torch.as_tensor(ref["sx"], device=DEV), "sy": torch.as_tensor(ref["sy"], device=DEV),
+            "n": torch.tensor([ref["n"]], dtype=torch.int64, device=DEV)}
+
+
+def _solve(st, d_in, d_out, P, lam, mode=rf.RF_ALPHA_TRACE, refine=1):
+    desc = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P)
+    A = torch.empty((P, d_out, d_in), dtype=torch.float32, device=DEV)
+    b = torch.empty((P, d_out), dtype=torch.float32, device=DEV)
+    Ab = torch.empty((P, d_out, d_in), dtype=torch.bfloat16, device=DEV)
+    alpha = torch.zeros(1, dtype=torch.float64, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    wsb = rf.rf_solve_workspace_bytes(desc)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    rf.rf_solve(desc, _struct(st), lam, mode, refine, A, b, Ab, alpha, status, ws, wsb)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return A.cpu().numpy().astype(np.float64), b.cpu().numpy().astype(np.float64), Ab, float(alpha.item())
+
+
+def _rel(a, r, axis=None):
+    return np.linalg.norm(a - r, axis=axis) / np.linalg.norm(r, axis=axis)
+
+
+@pytest.mark.parametrize("mode,lam,refine", [(rf.RF_ALPHA_TRACE, 0.03, 1), (rf.RF_ALPHA_TRACE, 0.03, 0),
+                                             (rf.RF_ALPHA_ABSOLUTE, 5.0, 1), (rf.RF_ALPHA_TRACE, 1.0, 2)])
+def test_solve_toy_matches_oracle(mode, lam, refine):
+    cal = synth.calib_inputs(256, 256, 4, 2048, index=0)
+    ref = O.calib_stats(_f64(cal["X"]), _f64(cal["Y"]))
+    A, b, Ab, alpha = _solve(_upload_stats(ref), 256, 256, 4, lam, mode, refine)
+    Ar, br, alr = O.ridge_solve(ref, lam, "trace" if mode == rf.RF_ALPHA_TRACE else "absolute")
+    assert abs(alpha - alr) <= 1e-12 * alr
+    for p in range(4):
+        assert _rel(A[p], Ar[p]) <= 1e-5, _rel(A[p], Ar[p])
+        assert _rel(b[p], br[p]) <= 1e-5
+    # the bf16 copy is the rounding of the fp32 maps
+    np.testing.assert_array_equal(synth.bits(Ab), synth.bits(torch.as_tensor(A, dtype=torch.float32).to(torch.bfloat16)))
+
+
+def test_solve_resolve_at_new_lambda_equals_fresh_solve():
+    cal = synth.calib_inputs(256, 256, 2, 2048, index=0, salt=1)
+    ref = O.calib_stats(_f64(cal["X"]), _f64(cal["Y"]))
+    st = _upload_stats(ref)
+    _solve(st, 256, 256, 2, 1.0)
+    A1, b1, _, _ = _solve(st, 256, 256, 2, 0.01)
+    A2, b2, _, _ = _solve(_upload_stats(ref), 256, 256, 2, 0.01)
+    np.testing.assert_array_equal(A1, A2)
+    np.testing.assert_array_equal(b1, b2)
+
+
+def test_gpu_calibration_then_solve_recovers_planted_maps():
+    """Planted toy: GPU accumulate + GPU solve gives the oracle's maps (from exact
+    fp64 sums) within 1e-4, and both are near A_true at the noise level."""
+    cal = synth.calib_inputs(256, 256, 4, 2048, index=0)
+    st = _zeros_stats(256, 256, 4)
+    _accumulate(cal["X"].to(DEV), cal["Y"].to(DEV), st, [777])
+    A, b, _, _ = _solve(st, 256, 256, 4, 0.03)
+    Ar, br, _ = O.ridge_solve(O.calib_stats(_f64(cal["X"]), _f64(cal["Y"])), 0.03)
+    At = cal["A_true"].numpy().astype(np.float64)
+    for p in range(4):
+        assert _rel(A[p], Ar[p]) <= 1e-4
+        assert _rel(A[p], At[p]) <= 0.05
+
+
+@pytest.mark.slow
+def test_solve_full_width_sampled_rows():
+    d, P, n = 4096, 2, 8192
+    cal = synth.calib_inputs(d, d, P, n, index=1, device=DEV)
+    Xf, Yf = _f64(cal["X"]), _f64(cal["Y"])
+    ref = O.calib_stats(Xf, Yf)
+    A, b, _, alpha = _solve(_upload_stats(ref), d, d, P, 0.03)
+    Gc, Cc, mx, my = O.centre_stats(ref)
+    H = Gc + O.ridge_alpha(Gc, 0.03) * np.eye(d)
+    rows = np.sort(np.random.default_rng(2).choice(d, 64, replace=False))
+    for p in range(P):
+        Ar = np.linalg.solve(H, Cc[p][:, rows]).T        # oracle rows of A_p
+        assert _rel(A[p][rows], Ar) <= 1e-5, _rel(A[p][rows], Ar)
+        ne = _rel(A[p][rows] @ H, Cc[p][:, rows].T)      # normal equations
+        assert ne <= 1e-5, ne
+        assert _rel(b[p][rows], my[p][rows] - Ar @ mx) <= 1e-5

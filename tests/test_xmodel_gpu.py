@@ -1,0 +1,121 @@
+"""GPU parity of rf_xmodel_map and rf_rope_rows against the fp64 oracle.
+
+Small cases compare every mapped head; the full 40 -> 64 layer, N = 32768 case
+compares sampled rows of sampled target layers. Tolerance: per-head relative
+error max <= 2e-2, mean <= 3e-3.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import ridge_map_kv_gb300 as rf
+import synth
+from fillcheck import TOL_MAX, TOL_MEAN, head_errors
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _run(cfg, inp, L_tgt, N):
+    desc = rf.rf_xmodel_desc(L_src=cfg.L_src, L_tgt=L_tgt, k=cfg.k, n_kv_heads=cfg.H, head_dim=cfg.hd, N=N,
+                             theta_src=cfg.theta_src, theta_tgt=cfg.theta_tgt, pos_offset=cfg.pos_offset)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    kt = torch.full((L_tgt, N, cfg.H, cfg.hd), float("nan"), dtype=torch.bfloat16, device=DEV)
+    vt = torch.full_like(kt, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    wsb = rf.rf_xmodel_workspace_bytes(desc)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    rf.rf_xmodel_map(desc, g["src"], g["k_src"], g["v_src"], g["Wk"], g["bk"], g["Wv"], g["bv"], kt, vt, status,
+                     ws, wsb)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return kt, vt
+
+
+def _oracle_layer(cfg, inp, l, rows):
+    f64 = O.bf16_bits_to_f64
+    rt = torch.as_tensor(rows, device=inp["k_src"].device)
+    ks = f64(synth.bits(inp["k_src"].index_select(1, rt)))
+    vs = f64(synth.bits(inp["v_src"].index_select(1, rt)))
+    return O.xmodel_map_layer(ks, vs, list(inp["src"][l]), f64(synth.bits(inp["Wk"][l])),
+                              synth.f32(inp["bk"][l]).astype(np.float64), f64(synth.bits(inp["Wv"][l])),
+                              synth.f32(inp["bv"][l]).astype(np.float64), rows + cfg.pos_offset, cfg.theta_src,
+                              cfg.theta_tgt, cfg.H, cfg.hd)
+
+
+def _check(cfg, inp, kt, vt, layers, rows):
+    errs = []
+    rt = torch.as_tensor(rows, device=kt.device)
+    for l in layers:
+        K, V = _oracle_layer(cfg, inp, l, rows)
+        errs.append(head_errors(synth.bits(kt[l].index_select(0, rt)), K).ravel())
+        errs.append(head_errors(synth.bits(vt[l].index_select(0, rt)), V).ravel())
+    e = np.concatenate(errs)
+    assert np.all(np.isfinite(e)) and e.max() <= TOL_MAX and e.mean() <= TOL_MEAN, (e.max(), e.mean())
+
+
+SMALL = synth.XModelConfig("xmodel small", 94, L_src=5, L_tgt=3, k=2, H=2, hd=128, N=300, theta_src=1.0e6,
+                           theta_tgt=5.0e5, calib_n=0, lam=0.01)
+
+
+@pytest.mark.parametrize("cfg", [SMALL,
+                                 dataclasses.replace(SMALL, name="hd64 4 heads offset", H=4, hd=64, k=3, N=131,
+                                                     pos_offset=700, theta_tgt=1.0e6)],
+                         ids=lambda c: c.name)
+def test_xmodel_small_matches_oracle(cfg):
+    inp = synth.xmodel_inputs(cfg)
+    rng = np.random.default_rng(4)
+    inp["src"] = rng.integers(0, cfg.L_src, size=(cfg.L_tgt, cfg.k)).astype(np.int32)
+    kt, vt = _run(cfg, inp, cfg.L_tgt, cfg.N)
+    _check(cfg, inp, kt, vt, range(cfg.L_tgt), np.arange(cfg.N))
+
+
+def test_xmodel_identity_on_one_source_layer():
+    cfg = dataclasses.replace(SMALL, theta_tgt=SMALL.theta_src)
+    inp = synth.xmodel_inputs(cfg)
+    KV = cfg.KV
+    for l in range(cfg.L_tgt):
+        j = l % cfg.k
+        W = torch.zeros((KV, cfg.k * KV))
+        W[:, j * KV:(j + 1) * KV] = torch.eye(KV)
+        inp["Wk"][l] = W.to(torch.bfloat16)
+        inp["Wv"][l] = W.to(torch.bfloat16)
+    inp["bk"].zero_()
+    inp["bv"].zero_()
+    kt, vt = _run(cfg, inp, cfg.L_tgt, cfg.N)
+    for l in range(cfg.L_tgt):
+        s = int(inp["src"][l][l % cfg.k])
+        assert torch.equal(vt[l].cpu(), inp["v_src"][s])             # V: exact copy
+        e = head_errors(synth.bits(kt[l]), O.bf16_bits_to_f64(synth.bits(inp["k_src"][s])))
+        assert e.max() <= 1e-2 and e.mean() <= 3e-3                  # K: unrope, bf16, re-rope
+
+
+@pytest.mark.slow
+def test_xmodel_full_size_sampled():
+    cfg = synth.XMODEL
+    inp = synth.xmodel_inputs(cfg, device=DEV)
+    kt, vt = _run(cfg, inp, cfg.L_tgt, cfg.N)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, cfg.N - 1],
+                                     np.random.default_rng(3).choice(cfg.N, 59, replace=False)]))
+    _check(cfg, inp, kt, vt, [0, 21, 40, 63], rows)
+
+
+@pytest.mark.parametrize("hd,theta,off", [(128, 1.0e6, 0), (64, 5.0e5, 12345)])
+def test_rope_rows_matches_oracle_and_inverts(hd, theta, off):
+    n, H = 513, 3
+    ld = H * hd + 8
+    x = synth._randn((n, ld), 77, DEV)
+    y = torch.empty_like(x)
+    rf.rf_rope_rows(x, y, n, ld, H, hd, theta, off, False)
+    z = torch.empty_like(x)
+    rf.rf_rope_rows(y, z, n, ld, H, hd, theta, off, True)
+    torch.cuda.synchronize()
+    xs = O.bf16_bits_to_f64(synth.bits(x[:, :H * hd])).reshape(n, H, hd)
+    ref = O.rope(xs, (np.arange(n) + off)[:, None], theta)
+    e = head_errors(synth.bits(y[:, :H * hd]).reshape(n, H, hd), ref)
+    assert e.max() <= 1e-2 and e.mean() <= 2e-3
+    e2 = head_errors(synth.bits(z[:, :H * hd]).reshape(n, H, hd), xs)
+    assert e2.max() <= 1e-2 and e2.mean() <= 3e-3
