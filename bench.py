@@ -47,6 +47,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=1024, help="oracle row sample for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip timing the calibration, solve and cross-model rows")
     ap.add_argument("--workload", choices=sorted(workloads()), default=WORKLOAD,
                     help="llama8b (default, the metric's workload); others for profiling and parity runs")
     return ap.parse_args(argv)
@@ -375,21 +376,136 @@ def run_ours(args):
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{nrows} filled rows x {P} upper layers of the same workload, fp64 numpy, {dt:.1f} s"}
 
+    extras = None
+    if rank == 0 and ws_n == 1 and not args.no_extras:
+        del ws, kc, vc, inp, Wkv
+        torch.cuda.empty_cache()
+        extras = run_extras(dev, peak)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": cfg.name + " 8x128 KV heads, 10% exact prefix rows", "n_fill": n_fill,
+            "config": {"workload": workload_label(cfg), "n_fill": n_fill,
                        "upper_layers": P, "row_layers_per_step": units, "parallelism": f"independent fills x{ws_n}",
                        "l2": "no flush: inputs larger than L2 (1.1 GB of maps, weights and x_S read per step)"},
             "tflops": fill_flops * args.steps * ws_n / (t_max / 1e3) / 1e12,
             "frac_of_bf16_peak": fill_flops * args.steps * ws_n / (t_max / 1e3) / 1e12 / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clk,
-            "stages_ms": stage_avg, "fold_once_ms": fold_ms,
+            "stages_ms": stage_avg, "fold_once_ms": fold_ms, "extras": extras,
         }
         print(json.dumps(line))
+
+
+def workload_label(cfg) -> str:
+    exact = {None: "no exact prefix rows", "uniform10": "10% exact prefix rows (uniform)",
+             "blocks16_5": "5% exact prefix rows in blocks of 16"}.get(cfg.exact, f"exact rows {cfg.exact}")
+    return f"{cfg.name}, {cfg.H}x{cfg.hd} KV heads, {exact}"
+
+
+# --------------------------------------------------------------------------- #
+# The other rows of the path, timed once each at their workloads' sizes
+# --------------------------------------------------------------------------- #
+def _timed(fn, reps, stream):
+    import torch
+    import ridge_map_kv_gb300 as rf
+    fn()
+    torch.cuda.synchronize()
+    rf.rf_profile_start(4096)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    stages = {}
+    for name, ms in rf.rf_profile_stop():
+        stages[name] = stages.get(name, 0.0) + ms / reps
+    return e0.elapsed_time(e1) / reps, stages
+
+
+def _zero_stats(d_in, d_out, P, dev):
+    import torch
+    return {"G": torch.zeros((d_in, d_in), dtype=torch.float64, device=dev),
+            "C": torch.zeros((P, d_in, d_out), dtype=torch.float64, device=dev),
+            "sx": torch.zeros(d_in, dtype=torch.float64, device=dev),
+            "sy": torch.zeros((P, d_out), dtype=torch.float64, device=dev),
+            "n": torch.zeros(1, dtype=torch.int64, device=dev)}
+
+
+def run_extras(dev, peak_tflops):
+    """Calibration (27B shape), ridge solve (8B shape, 20 maps) and the cross-model
+    mapper (40 -> 64 layers, N = 32768), each timed with CUDA events."""
+    import torch
+
+    import ridge_map_kv_gb300 as rf
+    import synth
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+
+    # a5: calibration statistics, 27B-shaped: XᵀX and XᵀY_l for 48 maps over 16,384 rows
+    c = synth.DENSE27B
+    d, P, n = c.d, c.P, c.calib_n
+    cal = synth.calib_inputs(d, d, P, n, index=c.index, device=dev)
+    st = _zero_stats(d, d, P, dev)
+    cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
+    cd = rf.rf_calib_desc(d_in=d, d_out=d, n_maps=P)
+    ms, stages = _timed(lambda: rf.rf_calib_accumulate(cd, cal["X"], d, cal["Y"], d, n * d, n, cs), 3, stream)
+    flops = 2.0 * n * d * (d + P * d)
+    gm = stages.get("calib_gemm", ms)
+    out["a5_calibration"] = {
+        "workload": f"27b-shaped XᵀX + XᵀY, d={d}, {P} maps, {n} rows per call",
+        "ms_per_call": ms, "tflops": flops / (ms / 1e3) / 1e12, "gemm_ms": gm,
+        "gemm_frac_of_bf16_peak": flops / (gm / 1e3) / 1e12 / peak_tflops, "stages_ms": stages}
+    del cal, st, cs
+    torch.cuda.empty_cache()
+
+    # a6: ridge solve, 8B-shaped (d = 4096, 20 maps) from 8192 calibration rows
+    c = synth.LLAMA8B
+    d, P, n = c.d, c.P, c.calib_n
+    cal = synth.calib_inputs(d, d, P, n, index=c.index, device=dev)
+    st = _zero_stats(d, d, P, dev)
+    cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
+    cd = rf.rf_calib_desc(d_in=d, d_out=d, n_maps=P)
+    rf.rf_calib_accumulate(cd, cal["X"], d, cal["Y"], d, n * d, n, cs)
+    del cal
+    A = torch.empty((P, d, d), dtype=torch.float32, device=dev)
+    b = torch.empty((P, d), dtype=torch.float32, device=dev)
+    Ab = torch.empty((P, d, d), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    wsb = rf.rf_solve_workspace_bytes(cd)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    sol = {}
+    for refine in (0, 1):
+        ms, stages = _timed(lambda: rf.rf_solve(cd, cs, c.lam, rf.RF_ALPHA_TRACE, refine, A, b, Ab, None, status,
+                                               ws, wsb), 1, stream)
+        sol[f"refine_{refine}_ms"] = ms
+    assert int(status.item()) == 0
+    out["a6_solve"] = {"workload": f"8b-shaped ridge solve, d={d}, {P} maps, lambda={c.lam}", **sol}
+    del st, cs, A, b, Ab, ws
+    torch.cuda.empty_cache()
+
+    # a7: cross-model mapper, 40 -> 64 layers, k = 8, 8 x 128 heads, N = 32768
+    x = synth.XMODEL
+    inp = synth.xmodel_inputs(x, device=dev)
+    xd = rf.rf_xmodel_desc(L_src=x.L_src, L_tgt=x.L_tgt, k=x.k, n_kv_heads=x.H, head_dim=x.hd, N=x.N,
+                           theta_src=x.theta_src, theta_tgt=x.theta_tgt, pos_offset=0)
+    kt = torch.empty((x.L_tgt, x.N, x.KV), dtype=torch.bfloat16, device=dev)
+    vt = torch.empty_like(kt)
+    wsb = rf.rf_xmodel_workspace_bytes(xd)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    ms, stages = _timed(lambda: rf.rf_xmodel_map(xd, inp["src"], inp["k_src"], inp["v_src"], inp["Wk"], inp["bk"],
+                                                 inp["Wv"], inp["bv"], kt, vt, None, ws, wsb), 3, stream)
+    flops = 2.0 * x.N * x.d_in * 2 * x.KV * x.L_tgt
+    gm = stages.get("xmodel_gemm", ms)
+    out["a7_xmodel"] = {"workload": x.name, "ms_per_call": ms, "tflops": flops / (ms / 1e3) / 1e12,
+                        "gemm_ms": gm, "gemm_frac_of_bf16_peak": flops / (gm / 1e3) / 1e12 / peak_tflops,
+                        "stages_ms": stages,
+                        "pages_context": "277.6 ms for a 40->64 layer pair at 32K on unstated hardware (context only)"}
+    return out
 
 
 # --------------------------------------------------------------------------- #
@@ -418,7 +534,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": 1e3 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": cfg.name + " 8x128 KV heads, 10% exact prefix rows", "n_fill": n_fill,
+            "config": {"workload": workload_label(cfg), "n_fill": n_fill,
                        "upper_layers": cfg.P, "sample_rows_per_step": rows_per_step},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"{rows_per_step} filled rows x {cfg.P} upper layers per step"},
