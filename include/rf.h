@@ -109,7 +109,16 @@ typedef struct rf_fill_desc {
   double rope_theta;   /* RoPE base (rotate-half pairs (i, i+hd/2), θ^(-2i/hd))      */
   double rms_eps;      /* RMSNorm ε: y = g ⊙ x / sqrt(mean(x²) + ε)                   */
   int64_t pos_offset;  /* RoPE position of row 0                                     */
+  uint64_t flags;      /* RF_FLAG_* (0 = defaults)                                   */
 } rf_fill_desc;
+
+/* Flags of rf_fill_desc, rf_calib_desc and rf_xmodel_desc: which tensor-core GEMM
+ * kernel runs. RF_FLAG_SINGLE_CTA: one CTA per 128 x 256 output tile
+ * (cta_group::1). RF_FLAG_CTA_PAIR: a CTA pair per 256 x 256 tile (cta_group::2,
+ * each CTA holding half of B). 0 selects the library's default (single CTA).
+ * Results agree up to the order of fp32 additions. */
+#define RF_FLAG_SINGLE_CTA 1u
+#define RF_FLAG_CTA_PAIR 2u
 
 /* Supported fill shapes: d % 256 == 0, head_dim in {64, 128}, KV % 128 == 0,
  * 1 <= N - T <= 2^30 when anything is filled. */
@@ -186,6 +195,7 @@ typedef struct rf_calib_desc {
   int64_t d_in;    /* width of x (map input)        */
   int64_t d_out;   /* width of each y_p (map output) */
   int64_t n_maps;  /* P                              */
+  uint64_t flags;  /* RF_FLAG_* (0 = defaults)       */
 } rf_calib_desc;
 
 /* Raw one-pass sums, all device fp64 (n as int64), caller-owned.
@@ -255,6 +265,7 @@ typedef struct rf_xmodel_desc {
   double theta_src;    /* source RoPE base                                */
   double theta_tgt;    /* target RoPE base                                */
   int64_t pos_offset;  /* position of row 0                               */
+  uint64_t flags;      /* RF_FLAG_* (0 = defaults)                        */
 } rf_xmodel_desc;
 
 /* Supported: head_dim in {64, 128}, KV % 256 == 0, N >= 1. */

@@ -33,14 +33,18 @@ class RFError(RuntimeError):
         self.status = status
 
 
+RF_FLAG_SINGLE_CTA = 1
+RF_FLAG_CTA_PAIR = 2
+
+
 class rf_fill_desc(ctypes.Structure):
     _fields_ = [("d", c_int64), ("L", c_int64), ("S", c_int64), ("N", c_int64), ("T", c_int64),
                 ("n_kv_heads", c_int64), ("head_dim", c_int64), ("rope_theta", c_double),
-                ("rms_eps", c_double), ("pos_offset", c_int64)]
+                ("rms_eps", c_double), ("pos_offset", c_int64), ("flags", ctypes.c_uint64)]
 
 
 class rf_calib_desc(ctypes.Structure):
-    _fields_ = [("d_in", c_int64), ("d_out", c_int64), ("n_maps", c_int64)]
+    _fields_ = [("d_in", c_int64), ("d_out", c_int64), ("n_maps", c_int64), ("flags", ctypes.c_uint64)]
 
 
 class rf_calib_stats(ctypes.Structure):
@@ -50,7 +54,7 @@ class rf_calib_stats(ctypes.Structure):
 class rf_xmodel_desc(ctypes.Structure):
     _fields_ = [("L_src", c_int64), ("L_tgt", c_int64), ("k", c_int64), ("n_kv_heads", c_int64),
                 ("head_dim", c_int64), ("N", c_int64), ("theta_src", c_double), ("theta_tgt", c_double),
-                ("pos_offset", c_int64)]
+                ("pos_offset", c_int64), ("flags", ctypes.c_uint64)]
 
 
 _SIGS = {

@@ -29,6 +29,7 @@ namespace rf {
 constexpr int kCalibChunk = RF_CALIB_CHUNK;
 static_assert(kCalibChunk % 64 == 0, "calibration chunk must be a multiple of the K block");
 
+template <bool kPair_>
 struct GramProb {
   CUtensorMap tmX;  // X  {d_in, n_rows}, box {64, 64}
   CUtensorMap tmY;  // Y  {d_out, n_rows, P}, box {64, 64, 1}
@@ -40,6 +41,8 @@ struct GramProb {
   uint64_t timeout_ns;
   static constexpr bool kAMN = true;
   static constexpr bool kBMN = true;
+  static constexpr bool kPair = kPair_;
+  using Cfg = GemmCfg<kPair_>;
 
   __device__ void prefetch() const {
     tma_prefetch_desc(&tmX);
@@ -69,24 +72,26 @@ struct GramProb {
       mt = r - nt * g_mt;
     }
   }
-  __device__ void issue_loads(int u, int sb, int kb, uint8_t* sa, uint8_t* sbuf, uint64_t* bar) const {
+  __device__ void issue_loads(int u, int sb, int kb, uint8_t* sa, uint8_t* sbuf, uint32_t bar, uint32_t rank) const {
     bool is_g;
     int p, mt, nt;
     decode(u, is_g, p, mt, nt);
     const int row0 = sb * kCalibChunk + kb * kBK;
-    load_operand<kBM, true>(sa, &tmX, bar, row0, mt * kBM);
+    const int n0 = nt * kBN + static_cast<int>(rank) * Cfg::kBRows;
+    load_operand<kBM, true, kPair>(sa, &tmX, bar, row0, mt * Cfg::kUnitM + rank * kBM);
     if (is_g) {
-      load_operand<kBN, true>(sbuf, &tmX, bar, row0, nt * kBN);
+      load_operand<Cfg::kBRows, true, kPair>(sbuf, &tmX, bar, row0, n0);
     } else {
 #pragma unroll
-      for (int j = 0; j < kBN / 64; ++j) tma_load_3d(sbuf + j * (64 * kBK * 2), &tmY, bar, nt * kBN + 64 * j, row0, p);
+      for (int j = 0; j < Cfg::kBRows / 64; ++j)
+        tma3<kPair>(sbuf + j * (64 * kBK * 2), &tmY, bar, n0 + 64 * j, row0, p);
     }
   }
-  __device__ void epilogue(int u, int, uint32_t tacc, int row) const {
+  __device__ void epilogue(int u, int, uint32_t tacc, int row, uint32_t rank) const {
     bool is_g;
     int p, mt, nt;
     decode(u, is_g, p, mt, nt);
-    const size_t i = static_cast<size_t>(mt) * kBM + row;
+    const size_t i = static_cast<size_t>(mt) * Cfg::kUnitM + rank * kBM + row;
     double* o = is_g ? G + i * d_in + static_cast<size_t>(nt) * kBN
                      : C + (static_cast<size_t>(p) * d_in + i) * d_out + static_cast<size_t>(nt) * kBN;
 #pragma unroll 1
@@ -130,7 +135,38 @@ __global__ void __launch_bounds__(256) k_colsum(const __nv_bfloat16* __restrict_
   atomicAdd(out + static_cast<size_t>(p) * n_cols + c, acc);
 }
 
-static uint64_t g_gram_attr = 0;
+template <bool kPair>
+rf_status calib_gemm(const rf_calib_desc* desc, const rf_bf16* X, int64_t ld_x, const rf_bf16* Y, int64_t ld_y,
+                     int64_t y_map_stride, int64_t n_rows, const rf_calib_stats* st, int32_t* dev_status, int sms,
+                     cudaStream_t cs) {
+  using Cfg = GemmCfg<kPair>;
+  const int64_t d_in = desc->d_in, d_out = desc->d_out, P = desc->n_maps;
+  rf_status s;
+  GramProb<kPair> pr;
+  if ((s = make_tmap_bf16_2d(&pr.tmX, X, d_in, n_rows, ld_x, 64, kBK)) != RF_OK) return s;
+  if (P > 0) {
+    if ((s = make_tmap_bf16_3d(&pr.tmY, Y, d_out, n_rows, P, ld_y, P > 1 ? y_map_stride : ld_y * n_rows, 64, kBK)) !=
+        RF_OK)
+      return s;
+  } else {
+    pr.tmY = pr.tmX;
+  }
+  pr.G = st->G;
+  pr.C = st->C;
+  pr.d_in = static_cast<int>(d_in);
+  pr.d_out = static_cast<int>(P > 0 ? d_out : 0);
+  pr.P = static_cast<int>(P);
+  pr.n_rows = static_cast<int>(n_rows);
+  pr.n_chunks = static_cast<int>((n_rows + kCalibChunk - 1) / kCalibChunk);
+  pr.g_mt = static_cast<int>(d_in / Cfg::kUnitM);
+  pr.g_nt = static_cast<int>(d_in / kBN);
+  pr.c_nt = static_cast<int>(P > 0 ? d_out / kBN : 0);
+  pr.g_units = pr.g_mt * pr.g_nt;
+  pr.dev_status = dev_status;
+  pr.timeout_ns = wait_timeout_ns();
+  ProfScope prof(cs, RF_STAGE_CALIB_GEMM);
+  return launch_gemm(pr, pr.g_units + P * pr.g_mt * pr.c_nt, sms, cs, "calibration GEMM launch");
+}
 
 }  // namespace rf
 
@@ -189,32 +225,7 @@ extern "C" rf_status rf_calib_accumulate(const rf_calib_desc* desc, const rf_bf1
   }
   if ((s = cuda_check(cudaGetLastError(), "k_colsum launch")) != RF_OK) return s;
 
-  if ((s = set_smem_attr(reinterpret_cast<const void*>(&tc_gemm_kernel<GramProb>), kGemmSmemBytes, &g_gram_attr)) != RF_OK)
-    return s;
-  GramProb pr;
-  if ((s = make_tmap_bf16_2d(&pr.tmX, X, d_in, n_rows, ld_x, 64, kBK)) != RF_OK) return s;
-  if (P > 0) {
-    if ((s = make_tmap_bf16_3d(&pr.tmY, Y, d_out, n_rows, P, ld_y, P > 1 ? y_map_stride : ld_y * n_rows, 64, kBK)) != RF_OK)
-      return s;
-  } else {
-    pr.tmY = pr.tmX;
-  }
-  pr.G = st->G;
-  pr.C = st->C;
-  pr.d_in = static_cast<int>(d_in);
-  pr.d_out = static_cast<int>(P > 0 ? d_out : 0);
-  pr.P = static_cast<int>(P);
-  pr.n_rows = static_cast<int>(n_rows);
-  pr.n_chunks = static_cast<int>((n_rows + kCalibChunk - 1) / kCalibChunk);
-  pr.g_mt = static_cast<int>(d_in / kBM);
-  pr.g_nt = static_cast<int>(d_in / kBN);
-  pr.c_nt = static_cast<int>(P > 0 ? d_out / kBN : 0);
-  pr.g_units = pr.g_mt * pr.g_nt;
-  pr.dev_status = dev_status;
-  pr.timeout_ns = wait_timeout_ns();
-  const int64_t units = pr.g_units + P * pr.g_mt * pr.c_nt;
-  const int grid = static_cast<int>(std::min<int64_t>(units, sms));
-  ProfScope prof(cs, RF_STAGE_CALIB_GEMM);
-  tc_gemm_kernel<GramProb><<<grid, kGemmThreads, kGemmSmemBytes, cs>>>(pr);
-  return cuda_check(cudaGetLastError(), "calibration GEMM launch");
+  if (use_pair(desc->flags))
+    return calib_gemm<true>(desc, X, ld_x, Y, ld_y, y_map_stride, n_rows, st, dev_status, sms, cs);
+  return calib_gemm<false>(desc, X, ld_x, Y, ld_y, y_map_stride, n_rows, st, dev_status, sms, cs);
 }

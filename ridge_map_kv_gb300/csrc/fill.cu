@@ -22,6 +22,10 @@
 
 namespace rf {
 
+// Filled rows are padded to whole 256-row units (the M of a CTA-pair tile) in
+// the gathered operand, the x̂ buffer and the sum-of-squares partials.
+constexpr int kFillRowAlign = 256;
+
 // --------------------------------------------------------------------------
 // 1. Row compaction: one CTA, each thread scans a contiguous chunk of the mask.
 // --------------------------------------------------------------------------
@@ -73,7 +77,7 @@ __global__ void __launch_bounds__(128) k_gather_rows(const uint4* __restrict__ x
                                                      int row_vecs, int max_rows) {
   const int m = blockIdx.x;
   const int nf = *n_fill;
-  const int pad_end = min((nf + kBM - 1) / kBM * kBM, max_rows);
+  const int pad_end = min((nf + kFillRowAlign - 1) / kFillRowAlign * kFillRowAlign, max_rows);
   if (m >= pad_end) return;
   uint4* dst = xf + static_cast<size_t>(m) * row_vecs;
   if (m < nf) {
@@ -147,6 +151,7 @@ __global__ void k_fold_gain(const uint4* __restrict__ gain, const uint4* __restr
 //    Unit u: N-tile nt = u / m_tiles, M-tile mt = u % m_tiles (M fastest, so the
 //    CTAs in flight share the same map tiles through L2).
 // --------------------------------------------------------------------------
+template <bool kPair_>
 struct MapProb {
   CUtensorMap tmA;
   CUtensorMap tmB;
@@ -159,29 +164,31 @@ struct MapProb {
   uint64_t timeout_ns;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
+  static constexpr bool kPair = kPair_;
+  using Cfg = GemmCfg<kPair_>;
 
   __device__ void prefetch() const {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  __device__ int m_tiles() const { return (*n_fill + kBM - 1) / kBM; }
+  __device__ int m_tiles() const { return (*n_fill + Cfg::kUnitM - 1) / Cfg::kUnitM; }
   __device__ int num_units() const { return m_tiles() * n_ntiles; }
   __device__ int num_subtiles(int) const { return 1; }
   __device__ int num_kb(int, int) const { return d / kBK; }
-  __device__ void issue_loads(int u, int, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+  __device__ void issue_loads(int u, int, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar, uint32_t rank) const {
     const int mtc = m_tiles();
     const int nt = u / mtc, mt = u - nt * mtc;
-    load_operand<kBM, false>(sa, &tmA, bar, kb * kBK, mt * kBM);
-    load_operand<kBN, false>(sb, &tmB, bar, kb * kBK, nt * kBN);
+    load_operand<kBM, false, kPair>(sa, &tmA, bar, kb * kBK, mt * Cfg::kUnitM + rank * kBM);
+    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, kb * kBK, nt * kBN + rank * Cfg::kBRows);
   }
-  __device__ void epilogue(int u, int, uint32_t tacc, int row) const {
+  __device__ void epilogue(int u, int, uint32_t tacc, int row, uint32_t rank) const {
     const int nf = *n_fill;
-    const int mtc = (nf + kBM - 1) / kBM;
+    const int mtc = (nf + Cfg::kUnitM - 1) / Cfg::kUnitM;
     const int nt = u / mtc, mt = u - nt * mtc;
     const int n0 = nt * kBN;
     const int p = n0 / d;
     const int c0 = n0 - p * d;
-    const int m = mt * kBM + row;
+    const int m = mt * Cfg::kUnitM + static_cast<int>(rank) * kBM + row;
     const bool valid = m < nf;
     const float* bp = bias + static_cast<size_t>(p) * d + c0;
     __nv_bfloat16* dst = xhat + (static_cast<size_t>(p) * M_pad + m) * d + c0;
@@ -218,6 +225,7 @@ struct MapProb {
 //    Unit u: layer p, M-tile mt, N-tile nt (N fastest: the A tile is reused by
 //    the CTAs in flight, and a layer's 2KV x d weights stay in L2).
 // --------------------------------------------------------------------------
+template <bool kPair_>
 struct KVProb {
   CUtensorMap tmA;
   CUtensorMap tmB;
@@ -235,12 +243,14 @@ struct KVProb {
   uint64_t timeout_ns;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
+  static constexpr bool kPair = kPair_;
+  using Cfg = GemmCfg<kPair_>;
 
   __device__ void prefetch() const {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  __device__ int m_tiles() const { return (*n_fill + kBM - 1) / kBM; }
+  __device__ int m_tiles() const { return (*n_fill + Cfg::kUnitM - 1) / Cfg::kUnitM; }
   __device__ int num_units() const { return P * m_tiles() * n_ntiles; }
   __device__ int num_subtiles(int) const { return 1; }
   __device__ int num_kb(int, int) const { return d / kBK; }
@@ -251,17 +261,17 @@ struct KVProb {
     mt = r / n_ntiles;
     nt = r - mt * n_ntiles;
   }
-  __device__ void issue_loads(int u, int, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+  __device__ void issue_loads(int u, int, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar, uint32_t rank) const {
     int p, mt, nt;
     decode(u, m_tiles(), p, mt, nt);
-    load_operand<kBM, false>(sa, &tmA, bar, kb * kBK, p * M_pad + mt * kBM);
-    load_operand<kBN, false>(sb, &tmB, bar, kb * kBK, p * 2 * KV + nt * kBN);
+    load_operand<kBM, false, kPair>(sa, &tmA, bar, kb * kBK, p * M_pad + mt * Cfg::kUnitM + rank * kBM);
+    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, kb * kBK, p * 2 * KV + nt * kBN + rank * Cfg::kBRows);
   }
-  __device__ void epilogue(int u, int, uint32_t tacc, int row) const {
+  __device__ void epilogue(int u, int, uint32_t tacc, int row, uint32_t rank) const {
     const int nf = *n_fill;
     int p, mt, nt;
-    decode(u, (nf + kBM - 1) / kBM, p, mt, nt);
-    const int m = mt * kBM + row;
+    decode(u, (nf + Cfg::kUnitM - 1) / Cfg::kUnitM, p, mt, nt);
+    const int m = mt * Cfg::kUnitM + static_cast<int>(rank) * kBM + row;
     const bool valid = m < nf;
     int t = 0;
     float rs = 0.f;
@@ -319,7 +329,7 @@ static rf_status check_fill_desc(const rf_fill_desc* d) {
 
 static FillLayout fill_layout(const rf_fill_desc* d, void* ws) {
   const int64_t n_prefix = d->N - d->T;
-  const int64_t M_pad = round_up(std::max<int64_t>(n_prefix, 1), kBM);
+  const int64_t M_pad = round_up(std::max<int64_t>(n_prefix, 1), kFillRowAlign);
   const int64_t P = d->L - d->S;
   Carve c(ws);
   FillLayout l;
@@ -332,6 +342,65 @@ static FillLayout fill_layout(const rf_fill_desc* d, void* ws) {
   l.rope_sin = c.take<float>(std::max<int64_t>(n_prefix, 1) * (d->head_dim / 2));
   l.bytes = c.bytes();
   return l;
+}
+
+// The two fill GEMMs, on CTA pairs (kPair) or single CTAs.
+template <bool kPair>
+rf_status fill_gemms(const rf_fill_desc* desc, const FillLayout& lay, const rf_bf16* A, const float* b,
+                     const rf_bf16* Wkv, rf_bf16* k_cache, rf_bf16* v_cache, int64_t layer_stride, int64_t row_stride,
+                     int32_t* dev_status, int sms, cudaStream_t s) {
+  using Cfg = GemmCfg<kPair>;
+  rf_status st;
+  const int64_t d = desc->d, P = desc->L - desc->S, KV = desc->n_kv_heads * desc->head_dim;
+  const int64_t M_pad = round_up(desc->N - desc->T, kFillRowAlign);
+  const int64_t m_tiles_max = M_pad / Cfg::kUnitM;
+  const uint64_t tmo = wait_timeout_ns();
+  {
+    MapProb<kPair> pr;
+    if ((st = make_tmap_bf16_2d(&pr.tmA, lay.xf, d, M_pad, d, kBK, kBM)) != RF_OK) return st;
+    if ((st = make_tmap_bf16_2d(&pr.tmB, A, d, P * d, d, kBK, Cfg::kBRows)) != RF_OK) return st;
+    pr.n_fill = lay.n_fill;
+    pr.bias = b;
+    pr.xhat = lay.xhat;
+    pr.ssp = lay.ssp;
+    pr.d = static_cast<int>(d);
+    pr.P = static_cast<int>(P);
+    pr.M_pad = static_cast<int>(M_pad);
+    pr.n_ntiles = static_cast<int>(P * d / kBN);
+    pr.dev_status = dev_status;
+    pr.timeout_ns = tmo;
+    ProfScope prof(s, RF_STAGE_MAP_GEMM);
+    if ((st = launch_gemm(pr, m_tiles_max * pr.n_ntiles, sms, s, "map GEMM launch")) != RF_OK) return st;
+  }
+  {
+    KVProb<kPair> pr;
+    if ((st = make_tmap_bf16_2d(&pr.tmA, lay.xhat, d, P * M_pad, d, kBK, kBM)) != RF_OK) return st;
+    if ((st = make_tmap_bf16_2d(&pr.tmB, Wkv, d, P * 2 * KV, d, kBK, Cfg::kBRows)) != RF_OK) return st;
+    pr.n_fill = lay.n_fill;
+    pr.fill_idx = lay.fill_idx;
+    pr.ssp = lay.ssp;
+    pr.rope_cos = lay.rope_cos;
+    pr.rope_sin = lay.rope_sin;
+    pr.kc = reinterpret_cast<__nv_bfloat16*>(k_cache);
+    pr.vc = reinterpret_cast<__nv_bfloat16*>(v_cache);
+    pr.layer_stride = layer_stride;
+    pr.row_stride = row_stride;
+    pr.d = static_cast<int>(d);
+    pr.P = static_cast<int>(P);
+    pr.S = static_cast<int>(desc->S);
+    pr.M_pad = static_cast<int>(M_pad);
+    pr.KV = static_cast<int>(KV);
+    pr.hd = static_cast<int>(desc->head_dim);
+    pr.n_ntiles = static_cast<int>(2 * KV / kBN);
+    pr.n_ss = static_cast<int>(d / kBN);
+    pr.inv_d = 1.0f / static_cast<float>(d);
+    pr.eps = static_cast<float>(desc->rms_eps);
+    pr.dev_status = dev_status;
+    pr.timeout_ns = tmo;
+    ProfScope prof(s, RF_STAGE_KV_GEMM);
+    if ((st = launch_gemm(pr, P * m_tiles_max * pr.n_ntiles, sms, s, "K/V GEMM launch")) != RF_OK) return st;
+  }
+  return RF_OK;
 }
 
 }  // namespace rf
@@ -409,7 +478,7 @@ extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, in
   if ((st = cuda_check(cudaGetLastError(), "k_compact launch")) != RF_OK) return st;
   if (P == 0) return RF_OK;
 
-  const int64_t M_pad = round_up(n_prefix, kBM);
+  const int64_t M_pad = round_up(n_prefix, kFillRowAlign);
   {
     ProfScope prof(s, RF_STAGE_GATHER);
     k_gather_rows<<<static_cast<unsigned>(M_pad), 128, 0, s>>>(reinterpret_cast<const uint4*>(x_S), ld_x / 8,
@@ -425,62 +494,7 @@ extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, in
   }
   if ((st = cuda_check(cudaGetLastError(), "gather / rope launch")) != RF_OK) return st;
 
-  static uint64_t map_attr = 0, kv_attr = 0;
-  if ((st = set_smem_attr(reinterpret_cast<const void*>(&tc_gemm_kernel<MapProb>), kGemmSmemBytes, &map_attr)) != RF_OK) return st;
-  if ((st = set_smem_attr(reinterpret_cast<const void*>(&tc_gemm_kernel<KVProb>), kGemmSmemBytes, &kv_attr)) != RF_OK) return st;
-
-  const int64_t m_tiles_max = M_pad / kBM;
-  const uint64_t tmo = wait_timeout_ns();
-  {
-    MapProb pr;
-    if ((st = make_tmap_bf16_2d(&pr.tmA, lay.xf, d, M_pad, d, kBK, kBM)) != RF_OK) return st;
-    if ((st = make_tmap_bf16_2d(&pr.tmB, A, d, P * d, d, kBK, kBN)) != RF_OK) return st;
-    pr.n_fill = lay.n_fill;
-    pr.bias = b;
-    pr.xhat = lay.xhat;
-    pr.ssp = lay.ssp;
-    pr.d = static_cast<int>(d);
-    pr.P = static_cast<int>(P);
-    pr.M_pad = static_cast<int>(M_pad);
-    pr.n_ntiles = static_cast<int>(P * d / kBN);
-    pr.dev_status = dev_status;
-    pr.timeout_ns = tmo;
-    const int64_t units = m_tiles_max * pr.n_ntiles;
-    const int grid = static_cast<int>(std::min<int64_t>(units, sms));
-    ProfScope prof(s, RF_STAGE_MAP_GEMM);
-    tc_gemm_kernel<MapProb><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(pr);
-    if ((st = cuda_check(cudaGetLastError(), "map GEMM launch")) != RF_OK) return st;
-  }
-  {
-    KVProb pr;
-    if ((st = make_tmap_bf16_2d(&pr.tmA, lay.xhat, d, P * M_pad, d, kBK, kBM)) != RF_OK) return st;
-    if ((st = make_tmap_bf16_2d(&pr.tmB, Wkv, d, P * 2 * KV, d, kBK, kBN)) != RF_OK) return st;
-    pr.n_fill = lay.n_fill;
-    pr.fill_idx = lay.fill_idx;
-    pr.ssp = lay.ssp;
-    pr.rope_cos = lay.rope_cos;
-    pr.rope_sin = lay.rope_sin;
-    pr.kc = reinterpret_cast<__nv_bfloat16*>(k_cache);
-    pr.vc = reinterpret_cast<__nv_bfloat16*>(v_cache);
-    pr.layer_stride = layer_stride;
-    pr.row_stride = row_stride;
-    pr.d = static_cast<int>(d);
-    pr.P = static_cast<int>(P);
-    pr.S = static_cast<int>(desc->S);
-    pr.M_pad = static_cast<int>(M_pad);
-    pr.KV = static_cast<int>(KV);
-    pr.hd = static_cast<int>(desc->head_dim);
-    pr.n_ntiles = static_cast<int>(2 * KV / kBN);
-    pr.n_ss = static_cast<int>(d / kBN);
-    pr.inv_d = 1.0f / static_cast<float>(d);
-    pr.eps = static_cast<float>(desc->rms_eps);
-    pr.dev_status = dev_status;
-    pr.timeout_ns = tmo;
-    const int64_t units = P * m_tiles_max * pr.n_ntiles;
-    const int grid = static_cast<int>(std::min<int64_t>(units, sms));
-    ProfScope prof(s, RF_STAGE_KV_GEMM);
-    tc_gemm_kernel<KVProb><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(pr);
-    if ((st = cuda_check(cudaGetLastError(), "K/V GEMM launch")) != RF_OK) return st;
-  }
-  return RF_OK;
+  if (use_pair(desc->flags))
+    return fill_gemms<true>(desc, lay, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride, dev_status, sms, s);
+  return fill_gemms<false>(desc, lay, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride, dev_status, sms, s);
 }

@@ -1,43 +1,64 @@
-// Persistent, warp-specialised tcgen05 GEMM core for sm_103a.
+// Persistent, warp-specialised tcgen05 GEMM cores for sm_103a.
 //
-//   D[128 x 256] (fp32, TMEM) = Σ_k A[128 x 64] · B[256 x 64]ᵀ   (bf16 operands)
+// Two kernels share one problem interface:
 //
-// Roles (192 threads, one CTA per SM):
-//   warp 0      one thread issues TMA loads into a kStages-deep ring of
-//               128-byte-swizzled shared-memory tiles (full/empty mbarriers);
-//   warp 1      allocates 512 TMEM columns (two 256-column accumulators) and one
-//               thread issues tcgen05.mma (M=128, N=256, K=16) and commits;
-//   warps 2..5  the epilogue warpgroup: tcgen05.ld 32 rows each from the finished
-//               accumulator while the MMA warp fills the other one.
+//   tc_gemm_kernel       one CTA per unit of 128 x 256 outputs. Per k-block of 64,
+//                        the CTA loads A (128 rows) and B (256 rows) and issues
+//                        tcgen05.mma M=128 N=256 K=16 (cta_group::1).
+//   tc_gemm_pair_kernel  a CTA pair (cluster of 2) per unit of 256 x 256 outputs.
+//                        Each CTA loads its 128 rows of A and its 128 rows of B;
+//                        one thread of the even CTA issues tcgen05.mma M=256 N=256
+//                        (cta_group::2), which reads B from both CTAs. Per CTA this
+//                        moves 32 KB per k-block instead of 48 KB for the same
+//                        flops, which relieves shared-memory bandwidth.
 //
-// The problem type `Prob` decides the work: how many work units there are, how
-// many independent accumulations ("sub-tiles") a unit holds, the K-blocks of each,
-// which TMA boxes to load for a K-block, and what the epilogue does with a
-// finished 128 x 256 fp32 tile. Units are dealt round-robin over the CTAs.
+// D (fp32) lives in TMEM: 512 columns = two 256-column accumulators, so the
+// epilogue of one unit overlaps the MMAs of the next.
 //
-// Operands may be K-major (rows of K contiguous: box {64, rows}) or MN-major
-// (rows of M/N contiguous: 64-wide boxes {64, 64 k-rows}, one per 64 M/N).
-// All waits are bounded (see rf_device.cuh); on a timeout every role stops,
-// outstanding TMA copies and MMAs are drained, and TMEM is freed.
+// Roles (192 threads per CTA, one CTA per SM):
+//   warp 0      one thread issues TMA loads into the shared-memory stage ring
+//               (full/empty mbarriers);
+//   warp 1      allocates TMEM; in the single kernel and in the even CTA of a
+//               pair, one thread issues the MMAs and commits;
+//   warps 2..5  epilogue: tcgen05.ld 32 TMEM lanes (rows) each.
+//
+// The problem type `Prob` decides the work: how many units there are, how many
+// independent accumulations ("sub-tiles") a unit holds, the K-blocks of each,
+// which TMA boxes a CTA loads for a K-block, and what the epilogue does with a
+// finished 128-row x 256-column fp32 block. Units are dealt round-robin over
+// CTAs (pairs). Operands may be K-major (box {64, rows}) or MN-major (boxes
+// {64, 64} per 64 rows of M or N).
+//
+// All waits are bounded (rf_device.cuh); on a timeout every role stops,
+// outstanding copies and MMAs are drained, and TMEM is freed.
 #pragma once
+#include <algorithm>
+
 #include "rf_device.cuh"
+#include "rf_host.h"
 
 namespace rf {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
-constexpr int kBK = 64;
-constexpr int kStages = 4;
-constexpr int kTileABytes = kBM * kBK * 2;
-constexpr int kTileBBytes = kBN * kBK * 2;
-constexpr int kStageBytes = kTileABytes + kTileBBytes;
+constexpr int kBM = 128;  // accumulator rows per CTA (TMEM lanes)
+constexpr int kBN = 256;  // accumulator columns (N of a unit)
+constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kGemmThreads = 192;
 constexpr int kEpiThreads = 128;
+constexpr int kTileABytes = kBM * kBK * 2;
+
+template <bool kPair>
+struct GemmCfg {
+  static constexpr int kBRows = kPair ? 128 : 256;  // B rows this CTA loads per stage
+  static constexpr int kUnitM = kPair ? 256 : 128;  // output rows of a unit
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kTileBBytes = kBRows * kBK * 2;
+  static constexpr int kStageBytes = kTileABytes + kTileBBytes;
+};
 
 struct GemmShared {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[8];
+  uint64_t empty[8];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t mma_done;
@@ -45,18 +66,32 @@ struct GemmShared {
   int abort;
 };
 
-constexpr size_t kGemmSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(GemmShared);
+template <bool kPair>
+constexpr size_t gemm_smem_bytes() {
+  return 1024 + static_cast<size_t>(GemmCfg<kPair>::kStages) * GemmCfg<kPair>::kStageBytes + sizeof(GemmShared);
+}
 
-// Issue the TMA loads of one operand tile.
-//   K-major: one box {64 (k), rows}; the shared tile is rows x 128 B.
-//   MN-major: rows/64 boxes {64 (m or n), 64 (k)}; chunk j lands at j * 8 KB.
-template <int kRows, bool kMN>
-__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar, int k0, int r0) {
+template <bool kPair>
+__device__ __forceinline__ void tma2(void* dst, const CUtensorMap* tm, uint32_t bar, int32_t x, int32_t y) {
+  if constexpr (kPair) tma_load_2d_pair(dst, tm, bar, x, y);
+  else tma_load_2d_u32(dst, tm, bar, x, y);
+}
+template <bool kPair>
+__device__ __forceinline__ void tma3(void* dst, const CUtensorMap* tm, uint32_t bar, int32_t x, int32_t y, int32_t z) {
+  if constexpr (kPair) tma_load_3d_pair(dst, tm, bar, x, y, z);
+  else tma_load_3d_u32(dst, tm, bar, x, y, z);
+}
+
+// Loads one operand tile of kRows rows x 64 K.
+//   K-major: one box {64 (k), kRows}; the shared tile is kRows x 128 B.
+//   MN-major: kRows/64 boxes {64 (m or n), 64 (k)}; chunk j lands at j * 8 KB.
+template <int kRows, bool kMN, bool kPair>
+__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* tm, uint32_t bar, int k0, int r0) {
   if constexpr (!kMN) {
-    tma_load_2d(dst, tm, bar, k0, r0);
+    tma2<kPair>(dst, tm, bar, k0, r0);
   } else {
 #pragma unroll
-    for (int j = 0; j < kRows / 64; ++j) tma_load_2d(dst + j * (64 * kBK * 2), tm, bar, r0 + 64 * j, k0);
+    for (int j = 0; j < kRows / 64; ++j) tma2<kPair>(dst + j * (64 * kBK * 2), tm, bar, r0 + 64 * j, k0);
   }
 }
 
@@ -70,18 +105,27 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int k) {
   }
 }
 
+__device__ __forceinline__ uint8_t* gemm_smem_base(uint8_t* raw) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+}
+
+// --------------------------------------------------------------------------
+// Single-CTA kernel
+// --------------------------------------------------------------------------
 template <class Prob>
 __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ Prob prob) {
+  static_assert(!Prob::kPair, "pair problems run on tc_gemm_pair_kernel");
+  using Cfg = GemmCfg<false>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  GemmShared* sh = reinterpret_cast<GemmShared*>(smem + kStages * kStageBytes);
+  uint8_t* smem = gemm_smem_base(smem_raw);
+  GemmShared* sh = reinterpret_cast<GemmShared*>(smem + Cfg::kStages * Cfg::kStageBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = &sh->abort;
   const uint64_t timeout = prob.timeout_ns;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < Cfg::kStages; ++s) {
       mbar_init(&sh->full[s], 1);
       mbar_init(&sh->empty[s], 1);
     }
@@ -106,7 +150,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------------------------------------------------- producer
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
@@ -116,11 +159,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           const int nkb = prob.num_kb(u, sb);
           for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort_flag, timeout)) goto producer_done;
-            mbar_arrive_expect_tx(&sh->full[stage], kStageBytes);
-            uint8_t* sa = smem + stage * kStageBytes;
-            prob.issue_loads(u, sb, kb, sa, sa + kTileABytes, &sh->full[stage]);
+            mbar_arrive_expect_tx(&sh->full[stage], Cfg::kStageBytes);
+            uint8_t* sa = smem + stage * Cfg::kStageBytes;
+            prob.issue_loads(u, sb, kb, sa, sa + kTileABytes, smem_u32(&sh->full[stage]), 0u);
             ++issued;
-            if (++stage == kStages) {
+            if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
             }
@@ -129,16 +172,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       }
     producer_done:
       // Drain: every issued copy must land before the CTA may exit.
-      for (long long i = (issued > kStages ? issued - kStages : 0); i < issued; ++i) {
-        const int s = static_cast<int>(i % kStages);
-        const uint32_t ph = static_cast<uint32_t>((i / kStages) & 1);
+      for (long long i = (issued > Cfg::kStages ? issued - Cfg::kStages : 0); i < issued; ++i) {
         int dummy = 0;
-        mbar_wait(&sh->full[s], ph, &dummy, timeout);
+        mbar_wait(&sh->full[i % Cfg::kStages], static_cast<uint32_t>((i / Cfg::kStages) & 1), &dummy, timeout);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // --------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = make_idesc_bf16(kBM, kBN, Prob::kAMN ? 1 : 0, Prob::kBMN ? 1 : 0);
       int stage = 0;
       uint32_t phase = 0;
@@ -147,23 +187,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         const int nsub = prob.num_subtiles(u);
         for (int sb = 0; sb < nsub; ++sb, ++it) {
           const uint32_t acc = it & 1u;
-          const uint32_t acc_phase = (it >> 1) & 1u;
-          if (!mbar_wait(&sh->tmem_empty[acc], acc_phase ^ 1u, abort_flag, timeout)) goto mma_done;
+          if (!mbar_wait(&sh->tmem_empty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, timeout)) goto mma_done;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * kBN;
           const int nkb = prob.num_kb(u, sb);
           for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&sh->full[stage], phase, abort_flag, timeout)) goto mma_done;
             tc_fence_after();
-            const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+            const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
             const uint32_t sbb = sa + kTileABytes;
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
+            for (int k = 0; k < kBK / 16; ++k)
               tc_mma_bf16(d_tmem, operand_desc<Prob::kAMN>(sa, k), operand_desc<Prob::kBMN>(sbb, k), idesc,
                           (kb | k) != 0 ? 1u : 0u);
-            }
             tc_commit(&sh->empty[stage]);
-            if (++stage == kStages) {
+            if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
             }
@@ -179,7 +217,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
     uint32_t it = 0;
@@ -187,12 +224,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       const int nsub = prob.num_subtiles(u);
       for (int sb = 0; sb < nsub; ++sb, ++it) {
         const uint32_t acc = it & 1u;
-        const uint32_t acc_phase = (it >> 1) & 1u;
-        bool ok = mbar_wait(&sh->tmem_full[acc], acc_phase, abort_flag, timeout);
+        bool ok = mbar_wait(&sh->tmem_full[acc], (it >> 1) & 1u, abort_flag, timeout);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) goto epi_done;
         tc_fence_after();
-        prob.epilogue(u, sb, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN, row);
+        prob.epilogue(u, sb, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN, row, 0u);
         tc_fence_before();
         mbar_arrive(&sh->tmem_empty[acc]);
       }
@@ -208,6 +244,188 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+}
+
+// --------------------------------------------------------------------------
+// CTA-pair kernel (cluster of 2; rank 0 issues the MMAs)
+//   full[s]       rank 0's only: its producer expects both CTAs' bytes, and both
+//                 CTAs' TMA loads complete on it;
+//   empty[s]      in each CTA: the pair commit arrives on both;
+//   tmem_full[a]  in each CTA: the pair commit arrives on both;
+//   tmem_empty[a] rank 0's only: the 4 epilogue warps of both CTAs arrive.
+// Waits use cluster-scope acquire, since peer arrivals release at cluster scope.
+// --------------------------------------------------------------------------
+template <class Prob>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ Prob prob) {
+  static_assert(Prob::kPair, "single-CTA problems run on tc_gemm_kernel");
+  using Cfg = GemmCfg<true>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = gemm_smem_base(smem_raw);
+  GemmShared* sh = reinterpret_cast<GemmShared*>(smem + Cfg::kStages * Cfg::kStageBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int n_pairs = gridDim.x >> 1;
+  volatile int* abort_flag = &sh->abort;
+  const uint64_t timeout = prob.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sh->tmem_full[a], 1);
+      mbar_init(&sh->tmem_empty[a], 2 * (kEpiThreads / 32));
+    }
+    mbar_init(&sh->mma_done, 1);
+    sh->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) prob.prefetch();
+  __syncwarp();
+  if (warp == 1) {
+    tmem_alloc_pair(&sh->tmem_base, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+  const int n_units = prob.num_units();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      for (int u = pair; u < n_units; u += n_pairs) {
+        const int nsub = prob.num_subtiles(u);
+        for (int sb = 0; sb < nsub; ++sb) {
+          const int nkb = prob.num_kb(u, sb);
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait<true>(&sh->empty[stage], phase ^ 1u, abort_flag, timeout)) goto producer_done;
+            if (rank == 0) mbar_arrive_expect_tx(&sh->full[stage], 2 * Cfg::kStageBytes);
+            uint8_t* sa = smem + stage * Cfg::kStageBytes;
+            prob.issue_loads(u, sb, kb, sa, sa + kTileABytes, mapa_shared(smem_u32(&sh->full[stage]), 0), rank);
+            ++issued;
+            if (++stage == Cfg::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+    producer_done:
+      // Both CTAs' copies complete on rank 0's full barriers: rank 0 drains them
+      // before the closing cluster barrier, which neither CTA passes alone.
+      if (rank == 0) {
+        for (long long i = (issued > Cfg::kStages ? issued - Cfg::kStages : 0); i < issued; ++i) {
+          int dummy = 0;
+          mbar_wait<true>(&sh->full[i % Cfg::kStages], static_cast<uint32_t>((i / Cfg::kStages) & 1), &dummy,
+                          timeout);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16(2 * kBM, kBN, Prob::kAMN ? 1 : 0, Prob::kBMN ? 1 : 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t it = 0;
+      for (int u = pair; u < n_units; u += n_pairs) {
+        const int nsub = prob.num_subtiles(u);
+        for (int sb = 0; sb < nsub; ++sb, ++it) {
+          const uint32_t acc = it & 1u;
+          if (!mbar_wait<true>(&sh->tmem_empty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, timeout)) goto mma_done;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * kBN;
+          const int nkb = prob.num_kb(u, sb);
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait<true>(&sh->full[stage], phase, abort_flag, timeout)) goto mma_done;
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
+            const uint32_t sbb = sa + kTileABytes;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              tc_mma_bf16_pair(d_tmem, operand_desc<Prob::kAMN>(sa, k), operand_desc<Prob::kBMN>(sbb, k), idesc,
+                               (kb | k) != 0 ? 1u : 0u);
+            tc_commit_pair_multicast(&sh->empty[stage], 0x3);
+            if (++stage == Cfg::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          tc_commit_pair_multicast(&sh->tmem_full[acc], 0x3);
+        }
+      }
+    mma_done:
+      tc_commit_pair(&sh->mma_done);
+      int dummy = 0;
+      mbar_wait<true>(&sh->mma_done, 0, &dummy, timeout);
+    }
+    __syncwarp();
+  } else {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    uint32_t it = 0;
+    for (int u = pair; u < n_units; u += n_pairs) {
+      const int nsub = prob.num_subtiles(u);
+      for (int sb = 0; sb < nsub; ++sb, ++it) {
+        const uint32_t acc = it & 1u;
+        bool ok = mbar_wait<true>(&sh->tmem_full[acc], (it >> 1) & 1u, abort_flag, timeout);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) goto epi_done;
+        tc_fence_after();
+        prob.epilogue(u, sb, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN, row, rank);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sh->tmem_empty[acc]), 0));
+      }
+    }
+  epi_done:;
+  }
+
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();
+  if (threadIdx.x == 0 && sh->abort) record_status(prob.dev_status, RF_ERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+// Host launcher: persistent grid of min(units, SMs) CTAs, or min(units, SMs/2)
+// CTA pairs, with the kernel's dynamic shared memory opted in once per device.
+template <class Prob>
+rf_status launch_gemm(const Prob& pr, int64_t max_units, int sms, cudaStream_t s, const char* what) {
+  static uint64_t attr_mask = 0;
+  constexpr bool kPair = Prob::kPair;
+  const void* fn;
+  if constexpr (kPair) fn = reinterpret_cast<const void*>(&tc_gemm_pair_kernel<Prob>);
+  else fn = reinterpret_cast<const void*>(&tc_gemm_kernel<Prob>);
+  rf_status st = set_smem_attr(fn, gemm_smem_bytes<kPair>(), &attr_mask);
+  if (st != RF_OK) return st;
+  if (max_units <= 0) max_units = 1;
+  if constexpr (kPair) {
+    const int pairs = static_cast<int>(std::min<int64_t>(max_units, std::max(sms / 2, 1)));
+    tc_gemm_pair_kernel<Prob><<<2 * pairs, kGemmThreads, gemm_smem_bytes<true>(), s>>>(pr);
+  } else {
+    const int grid = static_cast<int>(std::min<int64_t>(max_units, sms));
+    tc_gemm_kernel<Prob><<<grid, kGemmThreads, gemm_smem_bytes<false>(), s>>>(pr);
+  }
+  return cuda_check(cudaGetLastError(), what);
+}
+
+// Chooses CTA pairs or single CTAs from RF_FLAG_* bits. The single-CTA kernels are
+// the default; RF_FLAG_CTA_PAIR selects the pair kernels.
+inline bool use_pair(uint64_t flags) {
+  if (flags & RF_FLAG_SINGLE_CTA) return false;
+  return (flags & RF_FLAG_CTA_PAIR) != 0;
 }
 
 }  // namespace rf

@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(256) k_rope_rows(const __nv_bfloat16* __restri
   }
 }
 
+template <bool kPair_>
 struct XMProb {
   CUtensorMap tmKu;  // un-roped source keys   {KV, L_src*N}, box {64, 128}
   CUtensorMap tmVs;  // source values          {KV, L_src*N}, box {64, 128}
@@ -103,6 +104,8 @@ struct XMProb {
   uint64_t timeout_ns;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
+  static constexpr bool kPair = kPair_;
+  using Cfg = GemmCfg<kPair_>;
 
   __device__ void prefetch() const {
     tma_prefetch_desc(&tmKu);
@@ -122,7 +125,7 @@ struct XMProb {
     mt = r / (2 * n_half);
     nt = r - mt * 2 * n_half;
   }
-  __device__ void issue_loads(int u, int, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+  __device__ void issue_loads(int u, int, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar, uint32_t rank) const {
     int l, mt, nt;
     decode(u, l, mt, nt);
     const bool is_k = nt < n_half;
@@ -130,15 +133,16 @@ struct XMProb {
     const int j = f0 / KV;
     const int c = f0 - j * KV;
     const int s = __ldg(src + l * k + j);
-    tma_load_2d(sa, is_k ? &tmKu : &tmVs, bar, c, s * N + mt * kBM);
-    tma_load_2d(sb, is_k ? &tmWk : &tmWv, bar, f0, l * KV + (is_k ? nt : nt - n_half) * kBN);
+    tma2<kPair>(sa, is_k ? &tmKu : &tmVs, bar, c, s * N + mt * Cfg::kUnitM + rank * kBM);
+    tma2<kPair>(sb, is_k ? &tmWk : &tmWv, bar, f0,
+                l * KV + (is_k ? nt : nt - n_half) * kBN + static_cast<int>(rank) * Cfg::kBRows);
   }
-  __device__ void epilogue(int u, int, uint32_t tacc, int row) const {
+  __device__ void epilogue(int u, int, uint32_t tacc, int row, uint32_t rank) const {
     int l, mt, nt;
     decode(u, l, mt, nt);
     const bool is_k = nt < n_half;
     const int col0 = (is_k ? nt : nt - n_half) * kBN;
-    const int t = mt * kBM + row;
+    const int t = mt * Cfg::kUnitM + static_cast<int>(rank) * kBM + row;
     const bool valid = t < N;
     const int tt = valid ? t : 0;
     const int half = hd >> 1;
@@ -152,7 +156,6 @@ struct XMProb {
   }
 };
 
-static uint64_t g_xm_attr = 0;
 
 struct XLayout {
   __nv_bfloat16* ku;
@@ -190,6 +193,41 @@ static rf_status check_xmodel_desc(const rf_xmodel_desc* d) {
     return fail(RF_ERR_SHAPE, "sizes exceed 2^31 rows or features");
   if (d->N > (int64_t(1) << 30)) return fail(RF_ERR_SHAPE, "N must be <= 2^30");
   return RF_OK;
+}
+
+template <bool kPair>
+rf_status xmodel_gemm(const rf_xmodel_desc* desc, const XLayout& lay, const rf_bf16* v_src, const rf_bf16* Wk,
+                      const float* bk, const rf_bf16* Wv, const float* bv, rf_bf16* k_tgt, rf_bf16* v_tgt,
+                      int32_t* dev_status, int sms, cudaStream_t s) {
+  using Cfg = GemmCfg<kPair>;
+  rf_status st;
+  const int64_t KV = desc->n_kv_heads * desc->head_dim, N = desc->N;
+  XMProb<kPair> pr;
+  const int64_t rows = desc->L_src * N;
+  if ((st = make_tmap_bf16_2d(&pr.tmKu, lay.ku, KV, rows, KV, kBK, kBM)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmVs, v_src, KV, rows, KV, kBK, kBM)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmWk, Wk, desc->k * KV, desc->L_tgt * KV, desc->k * KV, kBK, Cfg::kBRows)) != RF_OK)
+    return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmWv, Wv, desc->k * KV, desc->L_tgt * KV, desc->k * KV, kBK, Cfg::kBRows)) != RF_OK)
+    return st;
+  pr.src = lay.src;
+  pr.bk = bk;
+  pr.bv = bv;
+  pr.cos_t = lay.cos_t;
+  pr.sin_t = lay.sin_t;
+  pr.k_tgt = reinterpret_cast<__nv_bfloat16*>(k_tgt);
+  pr.v_tgt = reinterpret_cast<__nv_bfloat16*>(v_tgt);
+  pr.N = static_cast<int>(N);
+  pr.KV = static_cast<int>(KV);
+  pr.hd = static_cast<int>(desc->head_dim);
+  pr.k = static_cast<int>(desc->k);
+  pr.L_tgt = static_cast<int>(desc->L_tgt);
+  pr.m_tiles = static_cast<int>((N + Cfg::kUnitM - 1) / Cfg::kUnitM);
+  pr.n_half = static_cast<int>(KV / kBN);
+  pr.dev_status = dev_status;
+  pr.timeout_ns = wait_timeout_ns();
+  ProfScope prof(s, RF_STAGE_XMODEL_GEMM);
+  return launch_gemm(pr, desc->L_tgt * pr.m_tiles * 2 * pr.n_half, sms, s, "cross-model GEMM launch");
 }
 
 }  // namespace rf
@@ -249,35 +287,9 @@ extern "C" rf_status rf_xmodel_map(const rf_xmodel_desc* desc, const int32_t* sr
   }
   if ((st = cuda_check(cudaGetLastError(), "rope launches")) != RF_OK) return st;
 
-  if ((st = set_smem_attr(reinterpret_cast<const void*>(&tc_gemm_kernel<XMProb>), kGemmSmemBytes, &g_xm_attr)) != RF_OK)
-    return st;
-  XMProb pr;
-  const int64_t rows = desc->L_src * N;
-  if ((st = make_tmap_bf16_2d(&pr.tmKu, lay.ku, KV, rows, KV, kBK, kBM)) != RF_OK) return st;
-  if ((st = make_tmap_bf16_2d(&pr.tmVs, v_src, KV, rows, KV, kBK, kBM)) != RF_OK) return st;
-  if ((st = make_tmap_bf16_2d(&pr.tmWk, Wk, desc->k * KV, desc->L_tgt * KV, desc->k * KV, kBK, kBN)) != RF_OK) return st;
-  if ((st = make_tmap_bf16_2d(&pr.tmWv, Wv, desc->k * KV, desc->L_tgt * KV, desc->k * KV, kBK, kBN)) != RF_OK) return st;
-  pr.src = lay.src;
-  pr.bk = bk;
-  pr.bv = bv;
-  pr.cos_t = lay.cos_t;
-  pr.sin_t = lay.sin_t;
-  pr.k_tgt = reinterpret_cast<__nv_bfloat16*>(k_tgt);
-  pr.v_tgt = reinterpret_cast<__nv_bfloat16*>(v_tgt);
-  pr.N = static_cast<int>(N);
-  pr.KV = static_cast<int>(KV);
-  pr.hd = static_cast<int>(desc->head_dim);
-  pr.k = static_cast<int>(desc->k);
-  pr.L_tgt = static_cast<int>(desc->L_tgt);
-  pr.m_tiles = static_cast<int>((N + kBM - 1) / kBM);
-  pr.n_half = static_cast<int>(KV / kBN);
-  pr.dev_status = dev_status;
-  pr.timeout_ns = wait_timeout_ns();
-  const int64_t units = desc->L_tgt * pr.m_tiles * 2 * pr.n_half;
-  const int grid = static_cast<int>(std::min<int64_t>(units, sms));
-  ProfScope prof(s, RF_STAGE_XMODEL_GEMM);
-  tc_gemm_kernel<XMProb><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(pr);
-  return cuda_check(cudaGetLastError(), "cross-model GEMM launch");
+  if (use_pair(desc->flags))
+    return xmodel_gemm<true>(desc, lay, v_src, Wk, bk, Wv, bv, k_tgt, v_tgt, dev_status, sms, s);
+  return xmodel_gemm<false>(desc, lay, v_src, Wk, bk, Wv, bv, k_tgt, v_tgt, dev_status, sms, s);
 }
 
 extern "C" rf_status rf_rope_rows(const rf_bf16* in, rf_bf16* out, int64_t n_rows, int64_t ld, int64_t n_heads,

@@ -13,16 +13,17 @@ TOL_MAX = 2e-2     # max over (layer, row, head, K|V) of ||gpu - ref|| / ||ref||
 TOL_MEAN = 3e-3    # mean of the same
 
 
-def desc_of(cfg) -> rf.rf_fill_desc:
+def desc_of(cfg, flags: int = 0) -> rf.rf_fill_desc:
     return rf.rf_fill_desc(d=cfg.d, L=cfg.L, S=cfg.S, N=cfg.N, T=cfg.T, n_kv_heads=cfg.H, head_dim=cfg.hd,
-                           rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, pos_offset=cfg.pos_offset)
+                           rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, pos_offset=cfg.pos_offset, flags=flags)
 
 
-def run_fill(cfg, inp: dict, dev="cuda", mask="inp", canary=True):
+def run_fill(cfg, inp: dict, dev="cuda", mask="inp", canary=True, flags: int = 0):
     """Runs fold + fill on device copies of ``inp``. Returns a dict with the
-    caches before/after, n_fill and the device status."""
+    caches before/after, n_fill and the device status. ``flags`` selects the GEMM
+    kernels (rf.RF_FLAG_SINGLE_CTA or rf.RF_FLAG_CTA_PAIR; 0 = library default)."""
     dev = torch.device(dev)
-    desc = desc_of(cfg)
+    desc = desc_of(cfg, flags)
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     m = g["mask"] if mask == "inp" else (mask.to(dev) if mask is not None else None)
     P, KV, d = cfg.P, cfg.KV, cfg.d

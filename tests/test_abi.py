@@ -59,9 +59,10 @@ def _fill_desc(**kw):
 
 def test_fill_workspace_size_follows_the_layout():
     desc = _fill_desc()
-    # fill_idx, n_fill, Xf [128 x d], x̂ [P x 128 x d], ss partials [P x d/256 x 128], cos/sin [n_prefix x hd/2]
+    # fill_idx, n_fill, Xf [M x d], x̂ [P x M x d], ss partials [P x d/256 x M], cos/sin [n_prefix x hd/2],
+    # with M = the prefix rows padded to a whole 256-row unit
     r = lambda x: (x + 255) // 256 * 256
-    n_prefix, M, P, d, half = 9, 128, 4, 256, 32
+    n_prefix, M, P, d, half = 9, 256, 4, 256, 32
     want = r(n_prefix * 4) + r(4) + r(M * d * 2) + r(P * M * d * 2) + r(P * (d // 256) * M * 4) \
         + r(n_prefix * half * 4) + r(n_prefix * half * 4)
     assert rf.rf_fill_workspace_bytes(desc) == want

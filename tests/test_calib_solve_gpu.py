@@ -34,10 +34,10 @@ def _struct(st):
     return rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
 
 
-def _accumulate(X, Y, st, row_splits):
+def _accumulate(X, Y, st, row_splits, flags=0):
     n, d_in = X.shape
     P, _, d_out = Y.shape
-    desc = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P)
+    desc = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P, flags=flags)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     bounds = [0] + list(row_splits) + [n]
     for a, b in zip(bounds[:-1], bounds[1:]):
@@ -67,12 +67,13 @@ def _check_stats(st, ref, Yref_sq=None, rows=None, cols_x=None, cols_y=None):
 
 @pytest.mark.parametrize("shape", [(256, 256, 4, 2048, [1000]), (512, 768, 3, 3000, []), (256, 512, 1, 100, [40])],
                          ids=["toy two batches", "3 chunks ragged", "tiny ragged batches"])
-def test_calib_sums_match_oracle(shape):
+@pytest.mark.parametrize("flags", [rf.RF_FLAG_SINGLE_CTA, rf.RF_FLAG_CTA_PAIR], ids=["single-cta", "cta-pair"])
+def test_calib_sums_match_oracle(shape, flags):
     d_in, d_out, P, n, splits = shape
     cal = synth.calib_inputs(d_in, d_out, P, n, index=0 if d_in == 256 and P == 4 else 93)
     X, Y = cal["X"].to(DEV), cal["Y"].to(DEV)
     st = _zeros_stats(d_in, d_out, P)
-    _accumulate(X, Y, st, splits)
+    _accumulate(X, Y, st, splits, flags)
     Xf, Yf = _f64(cal["X"]), _f64(cal["Y"])
     ref = O.calib_stats(Xf, Yf)
     _check_stats(st, ref, (Yf ** 2).sum(axis=1))
@@ -84,11 +85,12 @@ def test_calib_sums_match_oracle(shape):
 @pytest.mark.slow
 @pytest.mark.parametrize("d_in,d_out,P,n", [(5120, 5120, 2, 16384), (8192, 256, 0, 131072)],
                          ids=["27b-shaped XtX and XtY", "cross-model Gram 8192^2 x 131072 rows"])
-def test_calib_full_width_sampled(d_in, d_out, P, n):
+@pytest.mark.parametrize("flags", [rf.RF_FLAG_SINGLE_CTA, rf.RF_FLAG_CTA_PAIR], ids=["single-cta", "cta-pair"])
+def test_calib_full_width_sampled(d_in, d_out, P, n, flags):
     cal = synth.calib_inputs(d_in, d_out, max(P, 1), n, index=3 if P else 4, device=DEV, noise=0.05)
     X, Y = cal["X"], cal["Y"][:P] if P else cal["Y"][:0]
     st = _zeros_stats(d_in, d_out, P)
-    desc = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P)
+    desc = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P, flags=flags)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     rf.rf_calib_accumulate(desc, X, d_in, Y if P else None, d_out, n * d_out, n, _struct(st), status)
     torch.cuda.synchronize()

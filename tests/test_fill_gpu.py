@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import oracle as O
+import ridge_map_kv_gb300 as rf
 import synth
 from fillcheck import assert_bookkeeping, assert_values, run_fill
 
@@ -30,10 +31,14 @@ def _mask_np(inp):
     return None if inp["mask"] is None else inp["mask"].cpu().numpy()
 
 
-def test_toy_fill_matches_oracle_everywhere():
+KERNELS = pytest.mark.parametrize("flags", [rf.RF_FLAG_SINGLE_CTA, rf.RF_FLAG_CTA_PAIR], ids=["single-cta", "cta-pair"])
+
+
+@KERNELS
+def test_toy_fill_matches_oracle_everywhere(flags):
     cfg = synth.TOY
     inp = synth.fill_inputs(cfg)
-    res = run_fill(cfg, inp)
+    res = run_fill(cfg, inp, flags=flags)
     assert res["status"] == 0
     idx = O.prefix_partition(cfg.N, cfg.T, _mask_np(inp))
     assert idx.tolist() == [0, 1, 2, 3, 8]
@@ -48,9 +53,10 @@ def test_toy_fill_matches_oracle_everywhere():
     _small("one layer, no exact rows", d=256, L=3, S=2, N=129, T=0, H=1, hd=128, exact=None),
     _small("position offset", d=256, L=4, S=1, N=200, T=8, H=2, hd=64, exact="uniform10", pos_offset=1000),
 ], ids=lambda c: c.name)
-def test_fill_small_shapes_match_oracle(cfg):
+@KERNELS
+def test_fill_small_shapes_match_oracle(cfg, flags):
     inp = synth.fill_inputs(cfg)
-    res = run_fill(cfg, inp)
+    res = run_fill(cfg, inp, flags=flags)
     assert res["status"] == 0
     idx = O.prefix_partition(cfg.N, cfg.T, _mask_np(inp))
     assert res["n_fill"] == len(idx)
@@ -104,10 +110,11 @@ def _sample_rows(idx: np.ndarray, mask_np, n_prefix: int, n_random=192, seed=1):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["llama8b", "dense27b"])
-def test_fill_full_size_sampled(name):
+@KERNELS
+def test_fill_full_size_sampled(name, flags):
     cfg = synth.FILL_CONFIGS[name]
     inp = synth.fill_inputs(cfg, device="cuda")
-    res = run_fill(cfg, inp)
+    res = run_fill(cfg, inp, flags=flags)
     assert res["status"] == 0
     mnp = _mask_np(inp)
     idx = O.prefix_partition(cfg.N, cfg.T, mnp)

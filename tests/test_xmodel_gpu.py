@@ -19,9 +19,10 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _run(cfg, inp, L_tgt, N):
+def _run(cfg, inp, L_tgt, N, flags=0):
     desc = rf.rf_xmodel_desc(L_src=cfg.L_src, L_tgt=L_tgt, k=cfg.k, n_kv_heads=cfg.H, head_dim=cfg.hd, N=N,
-                             theta_src=cfg.theta_src, theta_tgt=cfg.theta_tgt, pos_offset=cfg.pos_offset)
+                             theta_src=cfg.theta_src, theta_tgt=cfg.theta_tgt, pos_offset=cfg.pos_offset,
+                             flags=flags)
     g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     kt = torch.full((L_tgt, N, cfg.H, cfg.hd), float("nan"), dtype=torch.bfloat16, device=DEV)
     vt = torch.full_like(kt, float("nan"))
@@ -65,11 +66,12 @@ SMALL = synth.XModelConfig("xmodel small", 94, L_src=5, L_tgt=3, k=2, H=2, hd=12
                                  dataclasses.replace(SMALL, name="hd64 4 heads offset", H=4, hd=64, k=3, N=131,
                                                      pos_offset=700, theta_tgt=1.0e6)],
                          ids=lambda c: c.name)
-def test_xmodel_small_matches_oracle(cfg):
+@pytest.mark.parametrize("flags", [rf.RF_FLAG_SINGLE_CTA, rf.RF_FLAG_CTA_PAIR], ids=["single-cta", "cta-pair"])
+def test_xmodel_small_matches_oracle(cfg, flags):
     inp = synth.xmodel_inputs(cfg)
     rng = np.random.default_rng(4)
     inp["src"] = rng.integers(0, cfg.L_src, size=(cfg.L_tgt, cfg.k)).astype(np.int32)
-    kt, vt = _run(cfg, inp, cfg.L_tgt, cfg.N)
+    kt, vt = _run(cfg, inp, cfg.L_tgt, cfg.N, flags)
     _check(cfg, inp, kt, vt, range(cfg.L_tgt), np.arange(cfg.N))
 
 
@@ -94,10 +96,11 @@ def test_xmodel_identity_on_one_source_layer():
 
 
 @pytest.mark.slow
-def test_xmodel_full_size_sampled():
+@pytest.mark.parametrize("flags", [rf.RF_FLAG_SINGLE_CTA, rf.RF_FLAG_CTA_PAIR], ids=["single-cta", "cta-pair"])
+def test_xmodel_full_size_sampled(flags):
     cfg = synth.XMODEL
     inp = synth.xmodel_inputs(cfg, device=DEV)
-    kt, vt = _run(cfg, inp, cfg.L_tgt, cfg.N)
+    kt, vt = _run(cfg, inp, cfg.L_tgt, cfg.N, flags)
     rows = np.unique(np.concatenate([[0, 1, 127, 128, cfg.N - 1],
                                      np.random.default_rng(3).choice(cfg.N, 59, replace=False)]))
     _check(cfg, inp, kt, vt, [0, 21, 40, 63], rows)
