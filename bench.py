@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the calibration, solve and cross-model rows")
+    ap.add_argument("--gemm", choices=["default", "single", "pair"], default="default",
+                    help="tensor-core GEMM kernel: one CTA per 128x256 tile, or a CTA pair per 256x256 tile")
     ap.add_argument("--workload", choices=sorted(workloads()), default=WORKLOAD,
                     help="llama8b (default, the metric's workload); others for profiling and parity runs")
     return ap.parse_args(argv)
@@ -251,6 +253,11 @@ def cpu_oracle_rate(oi: "OracleInputs", n_rows: int, seed: int = 7):
     return len(rows) * cfg.P / dt, dt, len(rows), cores
 
 
+def gemm_flags(name):
+    """RF_FLAG_* bits for the --gemm choice (0 = the library's default kernel)."""
+    return {"default": 0, "single": 1, "pair": 2}[name]
+
+
 # --------------------------------------------------------------------------- #
 # Our arm
 # --------------------------------------------------------------------------- #
@@ -269,7 +276,8 @@ def run_ours(args):
     n_fill, units = fill_units(cfg, inp["mask"])
     P, d, KV = cfg.P, cfg.d, cfg.KV
     desc = rf.rf_fill_desc(d=d, L=cfg.L, S=cfg.S, N=cfg.N, T=cfg.T, n_kv_heads=cfg.H, head_dim=cfg.hd,
-                           rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, pos_offset=0)
+                           rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, pos_offset=0,
+                           flags=gemm_flags(args.gemm))
     Wkv = torch.empty((P, 2 * KV, d), dtype=torch.bfloat16, device=dev)
     kc = torch.zeros((cfg.L, cfg.N, cfg.H, cfg.hd), dtype=torch.bfloat16, device=dev)
     vc = torch.zeros_like(kc)
@@ -380,7 +388,7 @@ def run_ours(args):
     if rank == 0 and ws_n == 1 and not args.no_extras:
         del ws, kc, vc, inp, Wkv
         torch.cuda.empty_cache()
-        extras = run_extras(dev, peak)
+        extras = run_extras(dev, peak, gemm_flags(args.gemm))
 
     if rank == 0:
         line = {
@@ -389,6 +397,7 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": workload_label(cfg), "n_fill": n_fill,
                        "upper_layers": P, "row_layers_per_step": units, "parallelism": f"independent fills x{ws_n}",
+                       "gemm": args.gemm,
                        "l2": "no flush: inputs larger than L2 (1.1 GB of maps, weights and x_S read per step)"},
             "tflops": fill_flops * args.steps * ws_n / (t_max / 1e3) / 1e12,
             "frac_of_bf16_peak": fill_flops * args.steps * ws_n / (t_max / 1e3) / 1e12 / peak,
@@ -436,7 +445,7 @@ def _zero_stats(d_in, d_out, P, dev):
             "n": torch.zeros(1, dtype=torch.int64, device=dev)}
 
 
-def run_extras(dev, peak_tflops):
+def run_extras(dev, peak_tflops, flags=0):
     """Calibration (27B shape), ridge solve (8B shape, 20 maps) and the cross-model
     mapper (40 -> 64 layers, N = 32768), each timed with CUDA events."""
     import torch
@@ -452,7 +461,7 @@ def run_extras(dev, peak_tflops):
     cal = synth.calib_inputs(d, d, P, n, index=c.index, device=dev)
     st = _zero_stats(d, d, P, dev)
     cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
-    cd = rf.rf_calib_desc(d_in=d, d_out=d, n_maps=P)
+    cd = rf.rf_calib_desc(d_in=d, d_out=d, n_maps=P, flags=flags)
     ms, stages = _timed(lambda: rf.rf_calib_accumulate(cd, cal["X"], d, cal["Y"], d, n * d, n, cs), 3, stream)
     flops = 2.0 * n * d * (d + P * d)
     gm = stages.get("calib_gemm", ms)
@@ -469,7 +478,7 @@ def run_extras(dev, peak_tflops):
     cal = synth.calib_inputs(d, d, P, n, index=c.index, device=dev)
     st = _zero_stats(d, d, P, dev)
     cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
-    cd = rf.rf_calib_desc(d_in=d, d_out=d, n_maps=P)
+    cd = rf.rf_calib_desc(d_in=d, d_out=d, n_maps=P, flags=flags)
     rf.rf_calib_accumulate(cd, cal["X"], d, cal["Y"], d, n * d, n, cs)
     del cal
     A = torch.empty((P, d, d), dtype=torch.float32, device=dev)
@@ -492,7 +501,7 @@ def run_extras(dev, peak_tflops):
     x = synth.XMODEL
     inp = synth.xmodel_inputs(x, device=dev)
     xd = rf.rf_xmodel_desc(L_src=x.L_src, L_tgt=x.L_tgt, k=x.k, n_kv_heads=x.H, head_dim=x.hd, N=x.N,
-                           theta_src=x.theta_src, theta_tgt=x.theta_tgt, pos_offset=0)
+                           theta_src=x.theta_src, theta_tgt=x.theta_tgt, pos_offset=0, flags=flags)
     kt = torch.empty((x.L_tgt, x.N, x.KV), dtype=torch.bfloat16, device=dev)
     vt = torch.empty_like(kt)
     wsb = rf.rf_xmodel_workspace_bytes(xd)

@@ -108,6 +108,39 @@ rf_status set_smem_attr(const void* kernel, size_t bytes, uint64_t* done_mask) {
   return RF_OK;
 }
 
+// How many clusters of 2 CTAs of `kernel` (kGemmThreads threads, `smem_bytes` of
+// dynamic shared memory) fit on the device at once. A persistent pair grid larger
+// than this would run its last pairs after the others finish. Cached per device.
+int max_active_pairs(const void* kernel, size_t smem_bytes, int threads, int sms, int* cache) {
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return std::max(sms / 2, 1);
+  }
+  std::lock_guard<std::mutex> g(mu);
+  int& c = cache[dev & 63];
+  if (c > 0) return c;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * std::max(sms / 2, 1));
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = std::max(sms / 2, 1);
+  }
+  c = std::min(n, std::max(sms / 2, 1));
+  return c;
+}
+
 // ----------------------------------------------------------------- profiler
 struct ProfRecord {
   cudaEvent_t start = nullptr, stop = nullptr;

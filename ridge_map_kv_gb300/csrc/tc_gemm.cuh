@@ -399,11 +399,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-// Host launcher: persistent grid of min(units, SMs) CTAs, or min(units, SMs/2)
-// CTA pairs, with the kernel's dynamic shared memory opted in once per device.
+// Host launcher: persistent grid of min(units, SMs) CTAs, or of min(units,
+// co-resident clusters) CTA pairs, with the kernel's dynamic shared memory opted in once per device.
 template <class Prob>
 rf_status launch_gemm(const Prob& pr, int64_t max_units, int sms, cudaStream_t s, const char* what) {
   static uint64_t attr_mask = 0;
+  static int pair_cap[64] = {};
   constexpr bool kPair = Prob::kPair;
   const void* fn;
   if constexpr (kPair) fn = reinterpret_cast<const void*>(&tc_gemm_pair_kernel<Prob>);
@@ -412,7 +413,8 @@ rf_status launch_gemm(const Prob& pr, int64_t max_units, int sms, cudaStream_t s
   if (st != RF_OK) return st;
   if (max_units <= 0) max_units = 1;
   if constexpr (kPair) {
-    const int pairs = static_cast<int>(std::min<int64_t>(max_units, std::max(sms / 2, 1)));
+    const int cap = max_active_pairs(fn, gemm_smem_bytes<true>(), kGemmThreads, sms, pair_cap);
+    const int pairs = static_cast<int>(std::min<int64_t>(max_units, cap));
     tc_gemm_pair_kernel<Prob><<<2 * pairs, kGemmThreads, gemm_smem_bytes<true>(), s>>>(pr);
   } else {
     const int grid = static_cast<int>(std::min<int64_t>(max_units, sms));
