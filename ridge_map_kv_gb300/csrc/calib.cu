@@ -225,7 +225,7 @@ extern "C" rf_status rf_calib_accumulate(const rf_calib_desc* desc, const rf_bf1
   }
   if ((s = cuda_check(cudaGetLastError(), "k_colsum launch")) != RF_OK) return s;
 
-  if (use_pair(desc->flags))
+  if (use_pair(desc->flags, true))
     return calib_gemm<true>(desc, X, ld_x, Y, ld_y, y_map_stride, n_rows, st, dev_status, sms, cs);
   return calib_gemm<false>(desc, X, ld_x, Y, ld_y, y_map_stride, n_rows, st, dev_status, sms, cs);
 }

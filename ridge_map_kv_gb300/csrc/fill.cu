@@ -494,7 +494,7 @@ extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, in
   }
   if ((st = cuda_check(cudaGetLastError(), "gather / rope launch")) != RF_OK) return st;
 
-  if (use_pair(desc->flags))
+  if (use_pair(desc->flags, true))
     return fill_gemms<true>(desc, lay, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride, dev_status, sms, s);
   return fill_gemms<false>(desc, lay, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride, dev_status, sms, s);
 }

@@ -253,7 +253,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
 //   empty[s]      in each CTA: the pair commit arrives on both;
 //   tmem_full[a]  in each CTA: the pair commit arrives on both;
 //   tmem_empty[a] rank 0's only: the 4 epilogue warps of both CTAs arrive.
-// Waits use cluster-scope acquire, since peer arrivals release at cluster scope.
+// full, empty and tmem_full complete through the async proxy (TMA complete_tx,
+// tcgen05.commit) and guard async-proxy accesses (MMA reads, TMA writes, TMEM
+// loads after a tcgen05 fence), so CTA-scope waits suffice there. tmem_empty
+// orders the peer's generic-proxy threads and uses cluster-scope release/acquire;
+// it is waited on once per accumulator, not per k-block.
 // --------------------------------------------------------------------------
 template <class Prob>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
@@ -307,7 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         for (int sb = 0; sb < nsub; ++sb) {
           const int nkb = prob.num_kb(u, sb);
           for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait<true>(&sh->empty[stage], phase ^ 1u, abort_flag, timeout)) goto producer_done;
+            if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort_flag, timeout)) goto producer_done;
             if (rank == 0) mbar_arrive_expect_tx(&sh->full[stage], 2 * Cfg::kStageBytes);
             uint8_t* sa = smem + stage * Cfg::kStageBytes;
             prob.issue_loads(u, sb, kb, sa, sa + kTileABytes, mapa_shared(smem_u32(&sh->full[stage]), 0), rank);
@@ -325,8 +329,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (rank == 0) {
         for (long long i = (issued > Cfg::kStages ? issued - Cfg::kStages : 0); i < issued; ++i) {
           int dummy = 0;
-          mbar_wait<true>(&sh->full[i % Cfg::kStages], static_cast<uint32_t>((i / Cfg::kStages) & 1), &dummy,
-                          timeout);
+          mbar_wait(&sh->full[i % Cfg::kStages], static_cast<uint32_t>((i / Cfg::kStages) & 1), &dummy, timeout);
         }
       }
     }
@@ -345,7 +348,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const uint32_t d_tmem = tmem_base + acc * kBN;
           const int nkb = prob.num_kb(u, sb);
           for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait<true>(&sh->full[stage], phase, abort_flag, timeout)) goto mma_done;
+            if (!mbar_wait(&sh->full[stage], phase, abort_flag, timeout)) goto mma_done;
             tc_fence_after();
             const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
             const uint32_t sbb = sa + kTileABytes;
@@ -365,7 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     mma_done:
       tc_commit_pair(&sh->mma_done);
       int dummy = 0;
-      mbar_wait<true>(&sh->mma_done, 0, &dummy, timeout);
+      mbar_wait(&sh->mma_done, 0, &dummy, timeout);
     }
     __syncwarp();
   } else {
@@ -376,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const int nsub = prob.num_subtiles(u);
       for (int sb = 0; sb < nsub; ++sb, ++it) {
         const uint32_t acc = it & 1u;
-        bool ok = mbar_wait<true>(&sh->tmem_full[acc], (it >> 1) & 1u, abort_flag, timeout);
+        bool ok = mbar_wait(&sh->tmem_full[acc], (it >> 1) & 1u, abort_flag, timeout);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) goto epi_done;
         tc_fence_after();
@@ -423,11 +426,12 @@ rf_status launch_gemm(const Prob& pr, int64_t max_units, int sms, cudaStream_t s
   return cuda_check(cudaGetLastError(), what);
 }
 
-// Chooses CTA pairs or single CTAs from RF_FLAG_* bits. The single-CTA kernels are
-// the default; RF_FLAG_CTA_PAIR selects the pair kernels.
-inline bool use_pair(uint64_t flags) {
+// Chooses CTA pairs or single CTAs from RF_FLAG_* bits; with neither bit set,
+// the operation's own default `pair_by_default` applies.
+inline bool use_pair(uint64_t flags, bool pair_by_default) {
   if (flags & RF_FLAG_SINGLE_CTA) return false;
-  return (flags & RF_FLAG_CTA_PAIR) != 0;
+  if (flags & RF_FLAG_CTA_PAIR) return true;
+  return pair_by_default;
 }
 
 }  // namespace rf
