@@ -26,6 +26,12 @@ namespace rf {
 // the gathered operand, the x̂ buffer and the sum-of-squares partials.
 constexpr int kFillRowAlign = 256;
 
+// Bytes of gathered rows Xf that one band of the map GEMM keeps in L2.
+#ifndef RF_MAP_BAND_BYTES
+#define RF_MAP_BAND_BYTES (32ll << 20)
+#endif
+constexpr long long kMapBandBytes = RF_MAP_BAND_BYTES;
+
 // --------------------------------------------------------------------------
 // 1. Row compaction: one CTA, each thread scans a contiguous chunk of the mask.
 // --------------------------------------------------------------------------
@@ -148,8 +154,12 @@ __global__ void k_fold_gain(const uint4* __restrict__ gain, const uint4* __restr
 
 // --------------------------------------------------------------------------
 // 4. Map GEMM: A operand Xf [M_pad][d], B operand maps [P*d][d] (both K-major).
-//    Unit u: N-tile nt = u / m_tiles, M-tile mt = u % m_tiles (M fastest, so the
-//    CTAs in flight share the same map tiles through L2).
+//    Units run in bands of m_band M-tiles; within a band, N-tiles outer and the
+//    band's M-tiles inner. The CTAs in flight share one map tile through L2,
+//    and the band's rows of Xf (about kMapBandBytes) stay in L2 for every N-tile
+//    of the band; the maps are read once per band. Without bands, the whole Xf
+//    is re-read per N-tile and, once it outgrows the share of L2 left beside the
+//    streaming maps and outputs, LRU evicts exactly the rows needed next.
 // --------------------------------------------------------------------------
 template <bool kPair_>
 struct MapProb {
@@ -159,7 +169,7 @@ struct MapProb {
   const float* bias;       // [P][d]
   __nv_bfloat16* xhat;     // [P][M_pad][d]
   float* ssp;              // [P][d/256][M_pad]
-  int d, P, M_pad, n_ntiles;
+  int d, P, M_pad, n_ntiles, m_band;
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = false;
@@ -172,19 +182,29 @@ struct MapProb {
     tma_prefetch_desc(&tmB);
   }
   __device__ int m_tiles() const { return (*n_fill + Cfg::kUnitM - 1) / Cfg::kUnitM; }
+  // Unit -> (M-tile, N-tile): band b holds M-tiles [b*m_band, b*m_band + gb),
+  // gb = m_band except in the last band.
+  __device__ void decode(int u, int mtc, int& mt, int& nt) const {
+    const int per_band = m_band * n_ntiles;
+    const int b = u / per_band;
+    const int r = u - b * per_band;
+    const int gb = min(m_band, mtc - b * m_band);
+    nt = r / gb;
+    mt = b * m_band + (r - nt * gb);
+  }
   __device__ int num_units() const { return m_tiles() * n_ntiles; }
   __device__ int num_subtiles(int) const { return 1; }
   __device__ int num_kb(int, int) const { return d / kBK; }
   __device__ void issue_loads(int u, int, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar, uint32_t rank) const {
-    const int mtc = m_tiles();
-    const int nt = u / mtc, mt = u - nt * mtc;
+    int mt, nt;
+    decode(u, m_tiles(), mt, nt);
     load_operand<kBM, false, kPair>(sa, &tmA, bar, kb * kBK, mt * Cfg::kUnitM + rank * kBM);
     load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, kb * kBK, nt * kBN + rank * Cfg::kBRows);
   }
   __device__ void epilogue(int u, int, uint32_t tacc, int row, uint32_t rank) const {
     const int nf = *n_fill;
-    const int mtc = (nf + Cfg::kUnitM - 1) / Cfg::kUnitM;
-    const int nt = u / mtc, mt = u - nt * mtc;
+    int mt, nt;
+    decode(u, (nf + Cfg::kUnitM - 1) / Cfg::kUnitM, mt, nt);
     const int n0 = nt * kBN;
     const int p = n0 / d;
     const int c0 = n0 - p * d;
@@ -367,6 +387,8 @@ rf_status fill_gemms(const rf_fill_desc* desc, const FillLayout& lay, const rf_b
     pr.P = static_cast<int>(P);
     pr.M_pad = static_cast<int>(M_pad);
     pr.n_ntiles = static_cast<int>(P * d / kBN);
+    pr.m_band = static_cast<int>(
+        std::max<long long>(1, std::min<long long>(m_tiles_max, kMapBandBytes / (Cfg::kUnitM * d * 2))));
     pr.dev_status = dev_status;
     pr.timeout_ns = tmo;
     ProfScope prof(s, RF_STAGE_MAP_GEMM);
