@@ -72,19 +72,28 @@ struct GramProb {
       mt = r - nt * g_mt;
     }
   }
-  __device__ void issue_loads(int u, int sb, int kb, uint8_t* sa, uint8_t* sbuf, uint32_t bar, uint32_t rank) const {
+  struct Coords {
     bool is_g;
-    int p, mt, nt;
-    decode(u, is_g, p, mt, nt);
-    const int row0 = sb * kCalibChunk + kb * kBK;
-    const int n0 = nt * kBN + static_cast<int>(rank) * Cfg::kBRows;
-    load_operand<kBM, true, kPair>(sa, &tmX, bar, row0, mt * Cfg::kUnitM + rank * kBM);
-    if (is_g) {
-      load_operand<Cfg::kBRows, true, kPair>(sbuf, &tmX, bar, row0, n0);
+    int p, m0, n0, row0;
+  };
+  __device__ Coords coords(int u, int sb, uint32_t rank) const {
+    Coords c;
+    int mt, nt;
+    decode(u, c.is_g, c.p, mt, nt);
+    c.m0 = mt * Cfg::kUnitM + static_cast<int>(rank) * kBM;
+    c.n0 = nt * kBN + static_cast<int>(rank) * Cfg::kBRows;
+    c.row0 = sb * kCalibChunk;
+    return c;
+  }
+  __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sbuf, uint32_t bar) const {
+    const int row = c.row0 + kb * kBK;
+    load_operand<kBM, true, kPair>(sa, &tmX, bar, row, c.m0);
+    if (c.is_g) {
+      load_operand<Cfg::kBRows, true, kPair>(sbuf, &tmX, bar, row, c.n0);
     } else {
 #pragma unroll
       for (int j = 0; j < Cfg::kBRows / 64; ++j)
-        tma3<kPair>(sbuf + j * (64 * kBK * 2), &tmY, bar, n0 + 64 * j, row0, p);
+        tma3<kPair>(sbuf + j * (64 * kBK * 2), &tmY, bar, c.n0 + 64 * j, row, c.p);
     }
   }
   __device__ void epilogue(int u, int, uint32_t tacc, int row, uint32_t rank) const {

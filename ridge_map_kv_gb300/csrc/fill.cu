@@ -195,11 +195,17 @@ struct MapProb {
   __device__ int num_units() const { return m_tiles() * n_ntiles; }
   __device__ int num_subtiles(int) const { return 1; }
   __device__ int num_kb(int, int) const { return d / kBK; }
-  __device__ void issue_loads(int u, int, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar, uint32_t rank) const {
+  struct Coords {
+    int a_row, b_row;
+  };
+  __device__ Coords coords(int u, int, uint32_t rank) const {
     int mt, nt;
     decode(u, m_tiles(), mt, nt);
-    load_operand<kBM, false, kPair>(sa, &tmA, bar, kb * kBK, mt * Cfg::kUnitM + rank * kBM);
-    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, kb * kBK, nt * kBN + rank * Cfg::kBRows);
+    return {mt * Cfg::kUnitM + static_cast<int>(rank) * kBM, nt * kBN + static_cast<int>(rank) * Cfg::kBRows};
+  }
+  __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    load_operand<kBM, false, kPair>(sa, &tmA, bar, kb * kBK, c.a_row);
+    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, kb * kBK, c.b_row);
   }
   __device__ void epilogue(int u, int, uint32_t tacc, int row, uint32_t rank) const {
     const int nf = *n_fill;
@@ -281,11 +287,18 @@ struct KVProb {
     mt = r / n_ntiles;
     nt = r - mt * n_ntiles;
   }
-  __device__ void issue_loads(int u, int, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar, uint32_t rank) const {
+  struct Coords {
+    int a_row, b_row;
+  };
+  __device__ Coords coords(int u, int, uint32_t rank) const {
     int p, mt, nt;
     decode(u, m_tiles(), p, mt, nt);
-    load_operand<kBM, false, kPair>(sa, &tmA, bar, kb * kBK, p * M_pad + mt * Cfg::kUnitM + rank * kBM);
-    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, kb * kBK, p * 2 * KV + nt * kBN + rank * Cfg::kBRows);
+    return {p * M_pad + mt * Cfg::kUnitM + static_cast<int>(rank) * kBM,
+            p * 2 * KV + nt * kBN + static_cast<int>(rank) * Cfg::kBRows};
+  }
+  __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    load_operand<kBM, false, kPair>(sa, &tmA, bar, kb * kBK, c.a_row);
+    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, kb * kBK, c.b_row);
   }
   __device__ void epilogue(int u, int, uint32_t tacc, int row, uint32_t rank) const {
     const int nf = *n_fill;

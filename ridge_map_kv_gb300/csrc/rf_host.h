@@ -55,8 +55,10 @@ struct Carve {
 
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-// Sets the dynamic shared-memory limit of a kernel once per process and device.
+// Clusters of 2 CTAs of `kernel` that fit on the device at once (cached per device).
 int max_active_pairs(const void* kernel, size_t smem_bytes, int threads, int sms, int* cache);
+
+// Sets the dynamic shared-memory limit of a kernel once per process and device.
 rf_status set_smem_attr(const void* kernel, size_t bytes, uint64_t* done_mask);
 
 // Brackets one kernel launch with profiling events when rf_profile_start is active.

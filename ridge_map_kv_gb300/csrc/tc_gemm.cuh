@@ -25,7 +25,11 @@
 // The problem type `Prob` decides the work: how many units there are, how many
 // independent accumulations ("sub-tiles") a unit holds, the K-blocks of each,
 // which TMA boxes a CTA loads for a K-block, and what the epilogue does with a
-// finished 128-row x 256-column fp32 block. Units are dealt round-robin over
+// finished 128-row x 256-column fp32 block. The producer asks the problem once
+// per (unit, sub-tile) for its `Coords` (`coords(u, sb)`), and per K-block only
+// issues the loads from them (`issue_loads(c, kb, ...)`): one thread issues every
+// copy of the CTA, so any per-K-block arithmetic or memory read there would
+// throttle the whole pipeline. Units are dealt round-robin over
 // CTAs (pairs). Operands may be K-major (box {64, rows}) or MN-major (boxes
 // {64, 64} per 64 rows of M or N).
 //
@@ -157,11 +161,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         const int nsub = prob.num_subtiles(u);
         for (int sb = 0; sb < nsub; ++sb) {
           const int nkb = prob.num_kb(u, sb);
+          typename Prob::Coords c = prob.coords(u, sb, 0u);
           for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort_flag, timeout)) goto producer_done;
             mbar_arrive_expect_tx(&sh->full[stage], Cfg::kStageBytes);
             uint8_t* sa = smem + stage * Cfg::kStageBytes;
-            prob.issue_loads(u, sb, kb, sa, sa + kTileABytes, smem_u32(&sh->full[stage]), 0u);
+            prob.issue_loads(c, kb, sa, sa + kTileABytes, smem_u32(&sh->full[stage]));
             ++issued;
             if (++stage == Cfg::kStages) {
               stage = 0;
@@ -180,6 +185,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc_bf16(kBM, kBN, Prob::kAMN ? 1 : 0, Prob::kBMN ? 1 : 0);
+      // Stage-0 descriptors of the four K=16 slices; stage s adds its byte offset
+      // / 16 to the start-address field (shared addresses stay below 256 KB).
+      uint64_t adesc[kBK / 16], bdesc[kBK / 16];
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k) {
+        adesc[k] = operand_desc<Prob::kAMN>(smem_u32(smem), k);
+        bdesc[k] = operand_desc<Prob::kBMN>(smem_u32(smem) + kTileABytes, k);
+      }
       int stage = 0;
       uint32_t phase = 0;
       uint32_t it = 0;
@@ -194,12 +207,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&sh->full[stage], phase, abort_flag, timeout)) goto mma_done;
             tc_fence_after();
-            const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
-            const uint32_t sbb = sa + kTileABytes;
+            const uint64_t soff = static_cast<uint64_t>((stage * Cfg::kStageBytes) >> 4);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-              tc_mma_bf16(d_tmem, operand_desc<Prob::kAMN>(sa, k), operand_desc<Prob::kBMN>(sbb, k), idesc,
-                          (kb | k) != 0 ? 1u : 0u);
+              tc_mma_bf16(d_tmem, adesc[k] + soff, bdesc[k] + soff, idesc, (kb | k) != 0 ? 1u : 0u);
             tc_commit(&sh->empty[stage]);
             if (++stage == Cfg::kStages) {
               stage = 0;
@@ -306,15 +317,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
+      // rank 0's full barriers, as shared::cluster addresses (8 bytes apart)
+      const uint32_t full_leader = mapa_shared(smem_u32(&sh->full[0]), 0);
       for (int u = pair; u < n_units; u += n_pairs) {
         const int nsub = prob.num_subtiles(u);
         for (int sb = 0; sb < nsub; ++sb) {
           const int nkb = prob.num_kb(u, sb);
+          typename Prob::Coords c = prob.coords(u, sb, rank);
           for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort_flag, timeout)) goto producer_done;
             if (rank == 0) mbar_arrive_expect_tx(&sh->full[stage], 2 * Cfg::kStageBytes);
             uint8_t* sa = smem + stage * Cfg::kStageBytes;
-            prob.issue_loads(u, sb, kb, sa, sa + kTileABytes, mapa_shared(smem_u32(&sh->full[stage]), 0), rank);
+            prob.issue_loads(c, kb, sa, sa + kTileABytes, full_leader + stage * 8u);
             ++issued;
             if (++stage == Cfg::kStages) {
               stage = 0;
@@ -336,6 +350,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       constexpr uint32_t idesc = make_idesc_bf16(2 * kBM, kBN, Prob::kAMN ? 1 : 0, Prob::kBMN ? 1 : 0);
+      uint64_t adesc[kBK / 16], bdesc[kBK / 16];
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k) {
+        adesc[k] = operand_desc<Prob::kAMN>(smem_u32(smem), k);
+        bdesc[k] = operand_desc<Prob::kBMN>(smem_u32(smem) + kTileABytes, k);
+      }
       int stage = 0;
       uint32_t phase = 0;
       uint32_t it = 0;
@@ -350,12 +370,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&sh->full[stage], phase, abort_flag, timeout)) goto mma_done;
             tc_fence_after();
-            const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
-            const uint32_t sbb = sa + kTileABytes;
+            const uint64_t soff = static_cast<uint64_t>((stage * Cfg::kStageBytes) >> 4);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-              tc_mma_bf16_pair(d_tmem, operand_desc<Prob::kAMN>(sa, k), operand_desc<Prob::kBMN>(sbb, k), idesc,
-                               (kb | k) != 0 ? 1u : 0u);
+              tc_mma_bf16_pair(d_tmem, adesc[k] + soff, bdesc[k] + soff, idesc, (kb | k) != 0 ? 1u : 0u);
             tc_commit_pair_multicast(&sh->empty[stage], 0x3);
             if (++stage == Cfg::kStages) {
               stage = 0;

@@ -125,17 +125,37 @@ struct XMProb {
     mt = r / (2 * n_half);
     nt = r - mt * 2 * n_half;
   }
-  __device__ void issue_loads(int u, int, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar, uint32_t rank) const {
+  // K-blocks run in order 0, 1, ...; the feature column c walks through one
+  // source layer's KV columns, then the next source layer (row base a_src).
+  struct Coords {
+    const CUtensorMap* ta;
+    const CUtensorMap* tb;
+    const int32_t* srcs;  // this target layer's k source layers
+    int a_row, b_row, a_src, c, j;
+  };
+  __device__ Coords coords(int u, int, uint32_t rank) const {
     int l, mt, nt;
     decode(u, l, mt, nt);
     const bool is_k = nt < n_half;
-    const int f0 = kb * kBK;
-    const int j = f0 / KV;
-    const int c = f0 - j * KV;
-    const int s = __ldg(src + l * k + j);
-    tma2<kPair>(sa, is_k ? &tmKu : &tmVs, bar, c, s * N + mt * Cfg::kUnitM + rank * kBM);
-    tma2<kPair>(sb, is_k ? &tmWk : &tmWv, bar, f0,
-                l * KV + (is_k ? nt : nt - n_half) * kBN + static_cast<int>(rank) * Cfg::kBRows);
+    Coords c;
+    c.ta = is_k ? &tmKu : &tmVs;
+    c.tb = is_k ? &tmWk : &tmWv;
+    c.srcs = src + l * k;
+    c.a_row = mt * Cfg::kUnitM + static_cast<int>(rank) * kBM;
+    c.b_row = l * KV + (is_k ? nt : nt - n_half) * kBN + static_cast<int>(rank) * Cfg::kBRows;
+    c.j = 0;
+    c.c = 0;
+    c.a_src = __ldg(c.srcs) * N;
+    return c;
+  }
+  __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    if (c.c == KV) {
+      c.c = 0;
+      c.a_src = __ldg(c.srcs + ++c.j) * N;
+    }
+    tma2<kPair>(sa, c.ta, bar, c.c, c.a_src + c.a_row);
+    tma2<kPair>(sb, c.tb, bar, kb * kBK, c.b_row);
+    c.c += kBK;
   }
   __device__ void epilogue(int u, int, uint32_t tacc, int row, uint32_t rank) const {
     int l, mt, nt;
