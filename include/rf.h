@@ -115,10 +115,9 @@ typedef struct rf_fill_desc {
 /* Flags of rf_fill_desc, rf_calib_desc and rf_xmodel_desc: which tensor-core GEMM
  * kernel runs. RF_FLAG_SINGLE_CTA: one CTA per 128 x 256 output tile
  * (cta_group::1). RF_FLAG_CTA_PAIR: a CTA pair per 256 x 256 tile (cta_group::2,
- * each CTA holding half of B). With neither bit set each operation takes its
- * measured-faster default: CTA pairs for rf_fill_kv, rf_fill_kv_static and
- * rf_calib_accumulate, single CTAs for rf_xmodel_map. Results agree up to the
- * order of fp32 additions. */
+ * each CTA holding half of B). With neither bit set every operation runs on
+ * CTA pairs, the measured-faster kernel. Results agree up to the order of fp32
+ * additions. */
 #define RF_FLAG_SINGLE_CTA 1u
 #define RF_FLAG_CTA_PAIR 2u
 

@@ -49,14 +49,21 @@ constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kGemmThreads = 192;
 constexpr int kEpiThreads = 128;
-constexpr int kTileABytes = kBM * kBK * 2;
+constexpr int kAtomABytes = kBM * kBK * 2;
 
+// A stage holds kAtoms consecutive K-blocks of 64 ("atoms") of A, then of B;
+// each atom has the layout of a single 64-wide tile. The pair kernel takes two
+// atoms per stage, which halves the barrier traffic per unit of K for its one
+// producer thread and one MMA thread.
 template <bool kPair>
 struct GemmCfg {
   static constexpr int kBRows = kPair ? 128 : 256;  // B rows this CTA loads per stage
   static constexpr int kUnitM = kPair ? 256 : 128;  // output rows of a unit
-  static constexpr int kStages = kPair ? 6 : 4;
-  static constexpr int kTileBBytes = kBRows * kBK * 2;
+  static constexpr int kAtoms = kPair ? 2 : 1;
+  static constexpr int kStages = kPair ? 3 : 4;
+  static constexpr int kAtomBBytes = kBRows * kBK * 2;
+  static constexpr int kTileABytes = kAtoms * kAtomABytes;
+  static constexpr int kTileBBytes = kAtoms * kAtomBBytes;
   static constexpr int kStageBytes = kTileABytes + kTileBBytes;
 };
 
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort_flag, timeout)) goto producer_done;
             mbar_arrive_expect_tx(&sh->full[stage], Cfg::kStageBytes);
             uint8_t* sa = smem + stage * Cfg::kStageBytes;
-            prob.issue_loads(c, kb, sa, sa + kTileABytes, smem_u32(&sh->full[stage]));
+            prob.issue_loads(c, kb, sa, sa + Cfg::kTileABytes, smem_u32(&sh->full[stage]));
             ++issued;
             if (++stage == Cfg::kStages) {
               stage = 0;
@@ -191,7 +198,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
 #pragma unroll
       for (int k = 0; k < kBK / 16; ++k) {
         adesc[k] = operand_desc<Prob::kAMN>(smem_u32(smem), k);
-        bdesc[k] = operand_desc<Prob::kBMN>(smem_u32(smem) + kTileABytes, k);
+        bdesc[k] = operand_desc<Prob::kBMN>(smem_u32(smem) + Cfg::kTileABytes, k);
       }
       int stage = 0;
       uint32_t phase = 0;
@@ -322,13 +329,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       for (int u = pair; u < n_units; u += n_pairs) {
         const int nsub = prob.num_subtiles(u);
         for (int sb = 0; sb < nsub; ++sb) {
-          const int nkb = prob.num_kb(u, sb);
+          // K-blocks rounded up to whole stages: a missing last atom is read past
+          // the operand's end, where TMA fills zeros (only the ragged last row
+          // chunk of the calibration sums has an odd count).
+          const int nst = (prob.num_kb(u, sb) + Cfg::kAtoms - 1) / Cfg::kAtoms;
           typename Prob::Coords c = prob.coords(u, sb, rank);
-          for (int kb = 0; kb < nkb; ++kb) {
+          for (int st = 0; st < nst; ++st) {
             if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort_flag, timeout)) goto producer_done;
             if (rank == 0) mbar_arrive_expect_tx(&sh->full[stage], 2 * Cfg::kStageBytes);
             uint8_t* sa = smem + stage * Cfg::kStageBytes;
-            prob.issue_loads(c, kb, sa, sa + kTileABytes, full_leader + stage * 8u);
+#pragma unroll
+            for (int a = 0; a < Cfg::kAtoms; ++a)
+              prob.issue_loads(c, st * Cfg::kAtoms + a, sa + a * kAtomABytes,
+                               sa + Cfg::kTileABytes + a * Cfg::kAtomBBytes, full_leader + stage * 8u);
             ++issued;
             if (++stage == Cfg::kStages) {
               stage = 0;
@@ -350,11 +363,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       constexpr uint32_t idesc = make_idesc_bf16(2 * kBM, kBN, Prob::kAMN ? 1 : 0, Prob::kBMN ? 1 : 0);
-      uint64_t adesc[kBK / 16], bdesc[kBK / 16];
+      constexpr int kSlices = Cfg::kAtoms * kBK / 16;
+      uint64_t adesc[kSlices], bdesc[kSlices];
 #pragma unroll
-      for (int k = 0; k < kBK / 16; ++k) {
-        adesc[k] = operand_desc<Prob::kAMN>(smem_u32(smem), k);
-        bdesc[k] = operand_desc<Prob::kBMN>(smem_u32(smem) + kTileABytes, k);
+      for (int k = 0; k < kSlices; ++k) {
+        const int a = k / (kBK / 16), kk = k % (kBK / 16);
+        adesc[k] = operand_desc<Prob::kAMN>(smem_u32(smem) + a * kAtomABytes, kk);
+        bdesc[k] = operand_desc<Prob::kBMN>(smem_u32(smem) + Cfg::kTileABytes + a * Cfg::kAtomBBytes, kk);
       }
       int stage = 0;
       uint32_t phase = 0;
@@ -366,14 +381,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           if (!mbar_wait<true>(&sh->tmem_empty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, timeout)) goto mma_done;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * kBN;
-          const int nkb = prob.num_kb(u, sb);
-          for (int kb = 0; kb < nkb; ++kb) {
+          const int nst = (prob.num_kb(u, sb) + Cfg::kAtoms - 1) / Cfg::kAtoms;
+          for (int st = 0; st < nst; ++st) {
             if (!mbar_wait(&sh->full[stage], phase, abort_flag, timeout)) goto mma_done;
             tc_fence_after();
             const uint64_t soff = static_cast<uint64_t>((stage * Cfg::kStageBytes) >> 4);
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              tc_mma_bf16_pair(d_tmem, adesc[k] + soff, bdesc[k] + soff, idesc, (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kSlices; ++k)
+              tc_mma_bf16_pair(d_tmem, adesc[k] + soff, bdesc[k] + soff, idesc, (st | k) != 0 ? 1u : 0u);
             tc_commit_pair_multicast(&sh->empty[stage], 0x3);
             if (++stage == Cfg::kStages) {
               stage = 0;

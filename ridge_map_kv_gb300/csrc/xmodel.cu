@@ -307,7 +307,7 @@ extern "C" rf_status rf_xmodel_map(const rf_xmodel_desc* desc, const int32_t* sr
   }
   if ((st = cuda_check(cudaGetLastError(), "rope launches")) != RF_OK) return st;
 
-  if (use_pair(desc->flags, false))
+  if (use_pair(desc->flags, true))
     return xmodel_gemm<true>(desc, lay, v_src, Wk, bk, Wv, bv, k_tgt, v_tgt, dev_status, sms, s);
   return xmodel_gemm<false>(desc, lay, v_src, Wk, bk, Wv, bv, k_tgt, v_tgt, dev_status, sms, s);
 }
