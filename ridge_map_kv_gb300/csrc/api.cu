@@ -108,7 +108,7 @@ rf_status set_smem_attr(const void* kernel, size_t bytes, uint64_t* done_mask) {
   return RF_OK;
 }
 
-// How many clusters of 2 CTAs of `kernel` (kGemmThreads threads, `smem_bytes` of
+// How many clusters of 2 CTAs of `kernel` (`threads` threads, `smem_bytes` of
 // dynamic shared memory) fit on the device at once. A persistent pair grid larger
 // than this would run its last pairs after the others finish. Cached per device.
 int max_active_pairs(const void* kernel, size_t smem_bytes, int threads, int sms, int* cache) {

@@ -175,6 +175,8 @@ struct MapProb {
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
   static constexpr bool kPair = kPair_;
+  static constexpr int kEpiWarps = 4;
+  struct EpiState {};
   using Cfg = GemmCfg<kPair_>;
 
   __device__ void prefetch() const {
@@ -207,7 +209,7 @@ struct MapProb {
     load_operand<kBM, false, kPair>(sa, &tmA, bar, kb * kBK, c.a_row);
     load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, kb * kBK, c.b_row);
   }
-  __device__ void epilogue(int u, int, uint32_t tacc, int row, uint32_t rank) const {
+  __device__ void epilogue(EpiState&, int u, int, int, uint32_t tacc, int row, int, uint32_t rank) const {
     const int nf = *n_fill;
     int mt, nt;
     decode(u, (nf + Cfg::kUnitM - 1) / Cfg::kUnitM, mt, nt);
@@ -270,6 +272,8 @@ struct KVProb {
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
   static constexpr bool kPair = kPair_;
+  static constexpr int kEpiWarps = 4;
+  struct EpiState {};
   using Cfg = GemmCfg<kPair_>;
 
   __device__ void prefetch() const {
@@ -300,7 +304,7 @@ struct KVProb {
     load_operand<kBM, false, kPair>(sa, &tmA, bar, kb * kBK, c.a_row);
     load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, kb * kBK, c.b_row);
   }
-  __device__ void epilogue(int u, int, uint32_t tacc, int row, uint32_t rank) const {
+  __device__ void epilogue(EpiState&, int u, int, int, uint32_t tacc, int row, int, uint32_t rank) const {
     const int nf = *n_fill;
     int p, mt, nt;
     decode(u, (nf + Cfg::kUnitM - 1) / Cfg::kUnitM, p, mt, nt);

@@ -15,12 +15,16 @@
 // D (fp32) lives in TMEM: 512 columns = two 256-column accumulators, so the
 // epilogue of one unit overlaps the MMAs of the next.
 //
-// Roles (192 threads per CTA, one CTA per SM):
+// Roles (64 + 32 * Prob::kEpiWarps threads per CTA, one CTA per SM):
 //   warp 0      one thread issues TMA loads into the shared-memory stage ring
 //               (full/empty mbarriers);
 //   warp 1      allocates TMEM; in the single kernel and in the even CTA of a
 //               pair, one thread issues the MMAs and commits;
-//   warps 2..5  epilogue: tcgen05.ld 32 TMEM lanes (rows) each.
+//   warps 2..   epilogue, 4 or 8 warps. A warp may only read the TMEM lanes
+//               32*(warp % 4) .. +31, so warp w takes rows 32*(w % 4) + lane;
+//               with 8 warps the second four take the upper 128 columns.
+//               The epilogue keeps a per-thread `Prob::EpiState` across the
+//               sub-tiles of a unit (e.g. register running sums).
 //
 // The problem type `Prob` decides the work: how many units there are, how many
 // independent accumulations ("sub-tiles") a unit holds, the K-blocks of each,
@@ -47,8 +51,10 @@ constexpr int kBM = 128;  // accumulator rows per CTA (TMEM lanes)
 constexpr int kBN = 256;  // accumulator columns (N of a unit)
 constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int kTmemCols = 2 * kBN;
-constexpr int kGemmThreads = 192;
-constexpr int kEpiThreads = 128;
+template <class Prob>
+constexpr int gemm_threads() {
+  return 64 + 32 * Prob::kEpiWarps;
+}
 constexpr int kAtomABytes = kBM * kBK * 2;
 
 // A stage holds kAtoms consecutive K-blocks of 64 ("atoms") of A, then of B;
@@ -124,7 +130,7 @@ __device__ __forceinline__ uint8_t* gemm_smem_base(uint8_t* raw) {
 // Single-CTA kernel
 // --------------------------------------------------------------------------
 template <class Prob>
-__global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ Prob prob) {
+__global__ void __launch_bounds__(gemm_threads<Prob>(), 1) tc_gemm_kernel(const __grid_constant__ Prob prob) {
   static_assert(!Prob::kPair, "pair problems run on tc_gemm_pair_kernel");
   using Cfg = GemmCfg<false>;
   extern __shared__ uint8_t smem_raw[];
@@ -142,7 +148,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh->tmem_full[a], 1);
-      mbar_init(&sh->tmem_empty[a], kEpiThreads);
+      mbar_init(&sh->tmem_empty[a], 32 * Prob::kEpiWarps);
     }
     mbar_init(&sh->mma_done, 1);
     sh->abort = 0;
@@ -237,6 +243,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   } else {
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
+    const int col0 = ((warp - 2) >> 2) * (kBN * 4 / Prob::kEpiWarps);
+    typename Prob::EpiState es{};
     uint32_t it = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       const int nsub = prob.num_subtiles(u);
@@ -246,7 +254,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) goto epi_done;
         tc_fence_after();
-        prob.epilogue(u, sb, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN, row, 0u);
+        prob.epilogue(es, u, sb, nsub,
+                      tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN + static_cast<uint32_t>(col0),
+                      row, col0, 0u);
         tc_fence_before();
         mbar_arrive(&sh->tmem_empty[acc]);
       }
@@ -278,7 +288,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
 // it is waited on once per accumulator, not per k-block.
 // --------------------------------------------------------------------------
 template <class Prob>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>(), 1)
     tc_gemm_pair_kernel(const __grid_constant__ Prob prob) {
   static_assert(Prob::kPair, "single-CTA problems run on tc_gemm_kernel");
   using Cfg = GemmCfg<true>;
@@ -300,7 +310,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh->tmem_full[a], 1);
-      mbar_init(&sh->tmem_empty[a], 2 * (kEpiThreads / 32));
+      mbar_init(&sh->tmem_empty[a], 2 * Prob::kEpiWarps);
     }
     mbar_init(&sh->mma_done, 1);
     sh->abort = 0;
@@ -407,6 +417,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   } else {
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
+    const int col0 = ((warp - 2) >> 2) * (kBN * 4 / Prob::kEpiWarps);
+    typename Prob::EpiState es{};
     uint32_t it = 0;
     for (int u = pair; u < n_units; u += n_pairs) {
       const int nsub = prob.num_subtiles(u);
@@ -416,7 +428,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) goto epi_done;
         tc_fence_after();
-        prob.epilogue(u, sb, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN, row, rank);
+        prob.epilogue(es, u, sb, nsub,
+                      tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN + static_cast<uint32_t>(col0),
+                      row, col0, rank);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sh->tmem_empty[acc]), 0));
@@ -449,12 +463,12 @@ rf_status launch_gemm(const Prob& pr, int64_t max_units, int sms, cudaStream_t s
   if (st != RF_OK) return st;
   if (max_units <= 0) max_units = 1;
   if constexpr (kPair) {
-    const int cap = max_active_pairs(fn, gemm_smem_bytes<true>(), kGemmThreads, sms, pair_cap);
+    const int cap = max_active_pairs(fn, gemm_smem_bytes<true>(), gemm_threads<Prob>(), sms, pair_cap);
     const int pairs = static_cast<int>(std::min<int64_t>(max_units, cap));
-    tc_gemm_pair_kernel<Prob><<<2 * pairs, kGemmThreads, gemm_smem_bytes<true>(), s>>>(pr);
+    tc_gemm_pair_kernel<Prob><<<2 * pairs, gemm_threads<Prob>(), gemm_smem_bytes<true>(), s>>>(pr);
   } else {
     const int grid = static_cast<int>(std::min<int64_t>(max_units, sms));
-    tc_gemm_kernel<Prob><<<grid, kGemmThreads, gemm_smem_bytes<false>(), s>>>(pr);
+    tc_gemm_kernel<Prob><<<grid, gemm_threads<Prob>(), gemm_smem_bytes<false>(), s>>>(pr);
   }
   return cuda_check(cudaGetLastError(), what);
 }

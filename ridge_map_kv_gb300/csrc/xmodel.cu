@@ -105,6 +105,8 @@ struct XMProb {
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
   static constexpr bool kPair = kPair_;
+  static constexpr int kEpiWarps = 4;
+  struct EpiState {};
   using Cfg = GemmCfg<kPair_>;
 
   __device__ void prefetch() const {
@@ -157,7 +159,7 @@ struct XMProb {
     tma2<kPair>(sb, c.tb, bar, kb * kBK, c.b_row);
     c.c += kBK;
   }
-  __device__ void epilogue(int u, int, uint32_t tacc, int row, uint32_t rank) const {
+  __device__ void epilogue(EpiState&, int u, int, int, uint32_t tacc, int row, int, uint32_t rank) const {
     int l, mt, nt;
     decode(u, l, mt, nt);
     const bool is_k = nt < n_half;
