@@ -334,11 +334,17 @@ def run_ours(args):
     peaks = measured_peaks()
     map_ms = stage_avg.get("map_gemm")
     achieved = map_flops / (map_ms / 1e3) / 1e12 if map_ms else None
-    peak = peaks["bf16_tflops"]
+    # The map GEMM is timed inside the whole run of K steps: a run of 0.2 s or
+    # more is a sustained load (the 1.4 kW power cap engages within it), so its
+    # denominator is the sustained bf16 figure; a shorter run takes the burst one.
+    sustained = t_max >= 200.0 and peaks.get("bf16_tflops_sustained")
+    peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     roofline = {"kernel": "map_gemm (tc_gemm<MapProb>)", "bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": (achieved / peak) if achieved else None,
                 "traffic": profiled_traffic("map_gemm", args.workload),
-                "peak_source": f"{peaks['source']} burst bf16 (MEASURED_PEAKS.json)",
+                "peak_source": f"{peaks['source']} {'sustained' if sustained else 'burst'} bf16 (MEASURED_PEAKS.json)"
+                               f"; timed region {t_max:.0f} ms",
+                "peak_burst": peaks["bf16_tflops"], "peak_sustained": peaks.get("bf16_tflops_sustained"),
                 "algorithmic_flops_per_launch": map_flops,
                 "algorithmic_bytes_per_launch": n_fill * d * 2 + P * d * d * 2 + n_fill * P * d * 2
                 + n_fill * P * (d // 256) * 4 + P * d * 4}
@@ -388,7 +394,7 @@ def run_ours(args):
     if rank == 0 and ws_n == 1 and not args.no_extras:
         del ws, kc, vc, inp, Wkv
         torch.cuda.empty_cache()
-        extras = run_extras(dev, peak, gemm_flags(args.gemm))
+        extras = run_extras(dev, peaks["bf16_tflops"], gemm_flags(args.gemm))
 
     if rank == 0:
         line = {
