@@ -109,8 +109,7 @@ struct GramProb {
   // sums in memory. The fp32 running sum over at most 16 chunk partials adds a
   // relative error of at most 16 * 2^-24 (about 1e-6) of sqrt(G_ii G_jj), and
   // the read-modify-write traffic on G and C falls 16-fold against a flush per chunk.
-  __device__ void epilogue(EpiState& es, int u, int sb, int nsub, uint32_t tacc, int row, int col0,
-                           uint32_t rank) const {
+  __device__ void epilogue(EpiState& es, int, int sb, int, uint32_t tacc, int, int, uint32_t) const {
     const bool first = (sb % kFlushChunks) == 0;
 #pragma unroll
     for (int ch = 0; ch < kCols / 32; ++ch) {
@@ -120,6 +119,10 @@ struct GramProb {
 #pragma unroll
       for (int q = 0; q < 32; ++q) es.rs[ch * 32 + q] = first ? u2f(v[q]) : es.rs[ch * 32 + q] + u2f(v[q]);
     }
+  }
+  // The flush runs after the accumulator is handed back, overlapping the MMAs of
+  // the next chunk.
+  __device__ void epilogue_after(EpiState& es, int u, int sb, int nsub, int row, int col0, uint32_t rank) const {
     if ((sb % kFlushChunks) != kFlushChunks - 1 && sb != nsub - 1) return;
     bool is_g;
     int p, mt, nt;

@@ -24,7 +24,10 @@
 //               32*(warp % 4) .. +31, so warp w takes rows 32*(w % 4) + lane;
 //               with 8 warps the second four take the upper 128 columns.
 //               The epilogue keeps a per-thread `Prob::EpiState` across the
-//               sub-tiles of a unit (e.g. register running sums).
+//               sub-tiles of a unit (e.g. register running sums). It reads the
+//               accumulator in `epilogue`, hands the accumulator back to the
+//               MMA thread, and may then finish in `epilogue_after` (work that
+//               needs no TMEM, such as a flush of running sums to memory).
 //
 // The problem type `Prob` decides the work: how many units there are, how many
 // independent accumulations ("sub-tiles") a unit holds, the K-blocks of each,
@@ -259,6 +262,7 @@ __global__ void __launch_bounds__(gemm_threads<Prob>(), 1) tc_gemm_kernel(const 
                       row, col0, 0u);
         tc_fence_before();
         mbar_arrive(&sh->tmem_empty[acc]);
+        prob.epilogue_after(es, u, sb, nsub, row, col0, 0u);
       }
     }
   epi_done:;
@@ -434,6 +438,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>()
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sh->tmem_empty[acc]), 0));
+        prob.epilogue_after(es, u, sb, nsub, row, col0, rank);
       }
     }
   epi_done:;

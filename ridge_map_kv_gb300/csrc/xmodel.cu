@@ -107,6 +107,7 @@ struct XMProb {
   static constexpr bool kPair = kPair_;
   static constexpr int kEpiWarps = 4;
   struct EpiState {};
+  __device__ void epilogue_after(EpiState&, int, int, int, int, int, uint32_t) const {}
   using Cfg = GemmCfg<kPair_>;
 
   __device__ void prefetch() const {
