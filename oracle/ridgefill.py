@@ -16,7 +16,8 @@ Sources (cited by page and section):
        arXiv 2611.09709). Sections "Two numbers set the skip range", "Ridge map:
        predict the input, and the original projection runs unchanged", Table 2
        (notation), Table 3 (the four arms), the worked example "A small example:
-       how one row lands in the cache".
+       how one row lands in the cache", and "Hybrid layers and two corrections"
+       (value rescale).
   [XM] "Cross-Model KV Cache Transfer in LLM Families: A Closed-Form Linear Mapping
        for Prefill Reuse" (digest, seosoyoung.eiaserinnys.me). Sections "헤드별 리지
        회귀" (per-head ridge regression), "층 교차 소스 선택" (cross-layer source
@@ -31,6 +32,10 @@ Readings where the pages leave a step open (each is listed in the design doc):
   * Calibration sums are raw one-pass sums; they are centred at solve time.
   * alpha = lambda * tr(Gc) / d_in by default ("trace" mode), or alpha = lambda.
   * The cross-model bias is b = mu_Y - W mu_X (centred-ridge identity).
+  * Value rescale: "the first c rows of the tail" are rows N-T .. N-T+c-1; the
+    value projection includes the layer's RMSNorm (the same path as the fill);
+    a head's "magnitude" is the L2 norm of its hd-vector; rows whose predicted
+    norm is 0 carry no ratio and are left out of the mean (scale 1 if none is left).
 
 Parity status: every public function here is pinned by tests/test_oracle_pins.py
 against closed forms, invariants, textbook routines or brute force; none is
@@ -44,7 +49,7 @@ __all__ = [
     "bf16_bits_to_f64", "rope_inv_freq", "rope", "rms_norm", "prefix_partition",
     "map_predict", "fill_rows", "fill_kv", "calib_stats", "centre_stats",
     "ridge_alpha", "ridge_solve", "xmodel_features", "xmodel_map_layer",
-    "fill_flops_per_row_layer",
+    "fill_flops_per_row_layer", "value_scale",
 ]
 
 
@@ -124,7 +129,7 @@ def map_predict(x_S: np.ndarray, A_l: np.ndarray, b_l: np.ndarray) -> np.ndarray
 
 
 def fill_rows(x_S_rows, positions, A, b, gain, Wk, Wv, n_kv_heads, head_dim,
-              rope_theta, rms_eps):
+              rope_theta, rms_eps, v_scale=None):
     """Filled keys and values for a set of rows and every upper layer.
 
     For each row t and upper layer l (index p = l - S):
@@ -135,6 +140,7 @@ def fill_rows(x_S_rows, positions, A, b, gain, Wk, Wv, n_kv_heads, head_dim,
 
     Shapes: x_S_rows [n, d]; positions [n]; A [P, d, d]; b [P, d]; gain [P, d];
     Wk, Wv [P, H*hd, d]. Returns K, V as [P, n, H, hd] float64.
+    With ``v_scale`` [P, H] (the value rescale), V_p[:, h] is multiplied by v_scale[p, h].
     """
     x = np.asarray(x_S_rows, np.float64)
     n = x.shape[0]
@@ -148,12 +154,12 @@ def fill_rows(x_S_rows, positions, A, b, gain, Wk, Wv, n_kv_heads, head_dim,
         k = (y @ np.asarray(Wk[p], np.float64).T).reshape(n, n_kv_heads, head_dim)
         v = (y @ np.asarray(Wv[p], np.float64).T).reshape(n, n_kv_heads, head_dim)
         K[p] = rope(k, pos[:, None], rope_theta)
-        V[p] = v
+        V[p] = v if v_scale is None else v * np.asarray(v_scale, np.float64)[p][None, :, None]
     return K, V
 
 
 def fill_kv(k_cache, v_cache, x_S, exact_mask, A, b, gain, Wk, Wv, *, L, S, N, T,
-            n_kv_heads, head_dim, rope_theta, rms_eps, pos_offset=0):
+            n_kv_heads, head_dim, rope_theta, rms_eps, pos_offset=0, v_scale=None):
     """Whole-cache fill: returns (new_k_cache, new_v_cache, fill_idx).
 
     Caches are [L, N_cap, H, hd] arrays (float64 copies of the input caches).
@@ -167,11 +173,43 @@ def fill_kv(k_cache, v_cache, x_S, exact_mask, A, b, gain, Wk, Wv, *, L, S, N, T
     vc = np.array(v_cache, dtype=np.float64, copy=True)
     if idx.size and L > S:
         K, V = fill_rows(np.asarray(x_S, np.float64)[idx], idx + pos_offset, A, b, gain,
-                         Wk, Wv, n_kv_heads, head_dim, rope_theta, rms_eps)
+                         Wk, Wv, n_kv_heads, head_dim, rope_theta, rms_eps, v_scale)
         for p in range(L - S):
             kc[S + p][idx] = K[p]
             vc[S + p][idx] = V[p]
     return kc, vc, idx
+
+
+def value_scale(x_S_tail, x_exact_tail, A, b, gain, Wv, n_kv_heads, head_dim, rms_eps):
+    """Value rescale ([RF] "Hybrid layers and two corrections", value rescale).
+
+    In each upper layer p, each of the first c tail rows passes through the
+    layer's value projection twice, with the exact input and with the map's
+    prediction:
+        v_pred  = Wv_p RMSNorm_g(A_p x_S[t] + b_p)
+        v_exact = Wv_p RMSNorm_g(x_exact[p, t])
+    and per KV head h the scale is the mean over the rows of
+    ||v_exact_h|| / ||v_pred_h|| (rows with ||v_pred_h|| = 0 left out; 1 if none).
+
+    Shapes: x_S_tail [c, d] (x_S at rows N-T .. N-T+c-1); x_exact_tail [P, c, d]
+    (the exact inputs of layers S .. L-1 at those rows); A [P, d, d]; b, gain [P, d];
+    Wv [P, H*hd, d]. Returns [P, H] float64.
+    """
+    x = np.asarray(x_S_tail, np.float64)
+    c = x.shape[0]
+    P = A.shape[0]
+    out = np.ones((P, n_kv_heads))
+    for p in range(P):
+        W = np.asarray(Wv[p], np.float64)
+        y_pred = rms_norm(map_predict(x, A[p], b[p]), gain[p], rms_eps)
+        y_exact = rms_norm(np.asarray(x_exact_tail[p], np.float64), gain[p], rms_eps)
+        n_pred = np.linalg.norm((y_pred @ W.T).reshape(c, n_kv_heads, head_dim), axis=-1)
+        n_exact = np.linalg.norm((y_exact @ W.T).reshape(c, n_kv_heads, head_dim), axis=-1)
+        for h in range(n_kv_heads):
+            ok = n_pred[:, h] > 0
+            if ok.any():
+                out[p, h] = np.mean(n_exact[ok, h] / n_pred[ok, h])
+    return out
 
 
 def fill_flops_per_row_layer(d: int, n_kv_heads: int, head_dim: int) -> int:

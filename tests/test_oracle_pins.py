@@ -466,3 +466,96 @@ def test_flops_per_row_layer():
     f = O.fill_flops_per_row_layer(4096, 8, 128)
     assert f == 2 * 4096 * 4096 + 2 * 4096 * 2048
     assert abs(f * 11059 * 20 / 1e12 - 11.13) < 0.01
+
+
+# --------------------------------------------------------------------------- #
+# Value rescale (RidgeFill review, "Hybrid layers and two corrections")
+# --------------------------------------------------------------------------- #
+def _rescale_problem(P=2, c=6, d=32, H=2, hd=8, seed=7):
+    rng = np.random.default_rng(seed)
+    KV = H * hd
+    return {"P": P, "c": c, "d": d, "H": H, "hd": hd,
+            "x": rng.normal(size=(c, d)), "A": np.eye(d)[None] + 0.1 * rng.normal(size=(P, d, d)),
+            "b": 0.1 * rng.normal(size=(P, d)), "g": 1.0 + 0.1 * rng.normal(size=(P, d)),
+            "Wv": rng.normal(size=(P, KV, d)) / math.sqrt(d)}
+
+
+def test_value_scale_is_one_when_the_map_predicts_exactly():
+    pr = _rescale_problem()
+    x_exact = np.stack([pr["x"] @ pr["A"][p].T + pr["b"][p] for p in range(pr["P"])])
+    s = O.value_scale(pr["x"], x_exact, pr["A"], pr["b"], pr["g"], pr["Wv"], pr["H"], pr["hd"], 1e-5)
+    assert s.shape == (pr["P"], pr["H"])
+    np.testing.assert_allclose(s, 1.0, rtol=0, atol=1e-12)
+
+
+def test_value_scale_closed_form_for_a_scaled_subspace():
+    """W_v reads only coordinates [0, k). If the exact input equals the prediction
+    with those coordinates multiplied by beta, every head's exact value is the
+    predicted one times beta * rms(x̂) / rms(x_exact), rms including eps, so the
+    scale is the row mean of that factor, the same for every head."""
+    pr = _rescale_problem(P=2, c=5, d=32, H=3, hd=8)
+    k, beta, eps = 12, 2.5, 1e-3
+    Wv = pr["Wv"].copy()
+    Wv[:, :, k:] = 0.0
+    xhat = np.stack([pr["x"] @ pr["A"][p].T + pr["b"][p] for p in range(pr["P"])])
+    x_exact = xhat.copy()
+    x_exact[:, :, :k] *= beta
+    s = O.value_scale(pr["x"], x_exact, pr["A"], pr["b"], pr["g"], Wv, pr["H"], pr["hd"], eps)
+    for p in range(pr["P"]):
+        rms_pred = np.sqrt((xhat[p] ** 2).mean(axis=1) + eps)
+        rms_exact = np.sqrt((x_exact[p] ** 2).mean(axis=1) + eps)
+        want = np.mean(beta * rms_pred / rms_exact)
+        np.testing.assert_allclose(s[p], want, rtol=1e-12)
+
+
+def test_value_scale_invariants_and_direction():
+    pr = _rescale_problem(P=1, c=7, d=24, H=2, hd=6, seed=11)
+    rng = np.random.default_rng(3)
+    x_exact = rng.normal(size=(1, pr["c"], pr["d"]))
+    args = (pr["A"], pr["b"], pr["g"])
+    s = O.value_scale(pr["x"], x_exact, *args, pr["Wv"], pr["H"], pr["hd"], 1e-5)
+    # order of the c rows does not matter
+    perm = rng.permutation(pr["c"])
+    s_perm = O.value_scale(pr["x"][perm], x_exact[:, perm], *args, pr["Wv"], pr["H"], pr["hd"], 1e-5)
+    np.testing.assert_allclose(s_perm, s, rtol=1e-12)
+    # a head's W_v rows scaled by any factor cancel in its ratio and leave the other head alone
+    W2 = pr["Wv"].copy()
+    W2[:, 0:pr["hd"]] *= 7.0
+    np.testing.assert_allclose(O.value_scale(pr["x"], x_exact, *args, W2, pr["H"], pr["hd"], 1e-5), s, rtol=1e-12)
+    # the ratio is exact over predicted: with one row, swapping the two inputs inverts it
+    xhat0 = pr["x"][:1] @ pr["A"][0].T + pr["b"][0]
+    eye = (np.eye(pr["d"])[None], np.zeros((1, pr["d"])))
+    s1 = O.value_scale(xhat0, x_exact[:, :1], *eye, pr["g"], pr["Wv"], pr["H"], pr["hd"], 1e-5)
+    s2 = O.value_scale(x_exact[0, :1], xhat0[None], *eye, pr["g"], pr["Wv"], pr["H"], pr["hd"], 1e-5)
+    np.testing.assert_allclose(s1 * s2, 1.0, rtol=1e-12)
+    assert not np.allclose(s1, 1.0)
+
+
+def test_value_scale_skips_rows_with_a_zero_prediction():
+    pr = _rescale_problem(P=1, c=4, d=16, H=2, hd=4, seed=5)
+    rng = np.random.default_rng(9)
+    x_exact = rng.normal(size=(1, 4, 16))
+    b = pr["b"].copy()
+    x = pr["x"].copy()
+    x[2] = 0.0
+    b[0] = 0.0            # row 2 predicts x̂ = 0, so every head's v_pred is 0 there
+    s_all = O.value_scale(x, x_exact, pr["A"], b, pr["g"], pr["Wv"], 2, 4, 1e-5)
+    keep = [0, 1, 3]
+    s_kept = O.value_scale(x[keep], x_exact[:, keep], pr["A"], b, pr["g"], pr["Wv"], 2, 4, 1e-5)
+    np.testing.assert_allclose(s_all, s_kept, rtol=1e-12)
+    only_zero = O.value_scale(x[2:3], x_exact[:, 2:3], pr["A"], b, pr["g"], pr["Wv"], 2, 4, 1e-5)
+    np.testing.assert_array_equal(only_zero, 1.0)
+
+
+def test_fill_rows_value_scale_multiplies_values_only():
+    pr = _rescale_problem(P=2, c=3, d=16, H=2, hd=4, seed=21)
+    rng = np.random.default_rng(1)
+    Wk = rng.normal(size=(2, 8, 16))
+    vs = np.array([[1.5, 0.25], [2.0, -1.0]])
+    pos = np.arange(3) + 10
+    K0, V0 = O.fill_rows(pr["x"], pos, pr["A"], pr["b"], pr["g"], Wk, pr["Wv"], 2, 4, 1e4, 1e-5)
+    K1, V1 = O.fill_rows(pr["x"], pos, pr["A"], pr["b"], pr["g"], Wk, pr["Wv"], 2, 4, 1e4, 1e-5, v_scale=vs)
+    np.testing.assert_array_equal(K1, K0)
+    for p in range(2):
+        for h in range(2):
+            np.testing.assert_allclose(V1[p, :, h], vs[p, h] * V0[p, :, h], rtol=1e-14)
