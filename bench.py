@@ -520,6 +520,43 @@ def run_extras(dev, peak_tflops, flags=0):
                         "gemm_ms": gm, "gemm_frac_of_bf16_peak": flops / (gm / 1e3) / 1e12 / peak_tflops,
                         "stages_ms": stages,
                         "pages_context": "277.6 ms for a 40->64 layer pair at 32K on unstated hardware (context only)"}
+    del inp, kt, vt, ws
+    torch.cuda.empty_cache()
+
+    # Value rescale (the 27B deployment, c = 512), then the 27B fill with the scale
+    c = synth.DENSE27B
+    n_tail = 512
+    inp = synth.fill_inputs(c, device=dev)
+    x_exact = synth.rescale_inputs(c, inp["x_S"], n_tail, device=dev)
+    fd = rf.rf_fill_desc(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
+                         rms_eps=c.rms_eps, pos_offset=0, flags=flags)
+    Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
+    rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
+    del inp["Wk"], inp["Wv"]
+    vs = torch.empty((c.P, c.H), dtype=torch.float32, device=dev)
+    wsb = rf.rf_value_scale_workspace_bytes(fd, n_tail)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    ms_scale, st_scale = _timed(lambda: rf.rf_value_scale(fd, n_tail, inp["x_S"], c.d, x_exact, c.d, inp["A"], inp["b"],
+                                                          Wkv, vs, None, ws, wsb), 3, stream)
+    del ws
+    fd.v_scale = vs.data_ptr()
+    kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    wsb = rf.rf_fill_workspace_bytes(fd)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    nf = torch.zeros(1, dtype=torch.int32, device=dev)
+    ms_fill, st_fill = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
+                                                    c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
+    n_fill = int(nf.item())
+    f_flops = 2.0 * n_fill * c.P * (c.d * c.d + c.d * 2 * c.KV)
+    s_flops = 2.0 * n_tail * c.P * (c.d * c.d + 2 * c.d * c.KV)
+    out["next1_value_rescale_27b"] = {
+        "workload": f"27b-shaped deployment: value rescale over c={n_tail} tail rows, then the fill with the scale "
+                    f"(d={c.d}, {c.P} upper layers, n_fill={n_fill})",
+        "rescale_ms": ms_scale, "rescale_tflops": s_flops / (ms_scale / 1e3) / 1e12, "rescale_stages_ms": st_scale,
+        "fill_ms": ms_fill, "fill_tflops": f_flops / (ms_fill / 1e3) / 1e12,
+        "fill_frac_of_bf16_peak": f_flops / (ms_fill / 1e3) / 1e12 / peak_tflops,
+        "fill_row_layers_per_s": n_fill * c.P / (ms_fill / 1e3), "fill_stages_ms": st_fill}
     return out
 
 

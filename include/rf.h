@@ -88,7 +88,8 @@ enum rf_stage {
   RF_STAGE_COLSUM = 8,       /* Σx, Σy, n                                      */
   RF_STAGE_SOLVE = 9,        /* kernels of the ridge solve                     */
   RF_STAGE_UNROPE = 10,      /* RoPE / inverse RoPE on cache rows              */
-  RF_STAGE_XMODEL_GEMM = 11  /* cross-model mapper GEMM                        */
+  RF_STAGE_XMODEL_GEMM = 11, /* cross-model mapper GEMM                        */
+  RF_STAGE_RESCALE = 12      /* value rescale: value norms and their ratios   */
 };
 rf_status rf_profile_start(int max_records);
 int rf_profile_stop(int32_t* stage_ids, float* ms, int capacity);
@@ -110,6 +111,9 @@ typedef struct rf_fill_desc {
   double rms_eps;      /* RMSNorm ε: y = g ⊙ x / sqrt(mean(x²) + ε)                   */
   int64_t pos_offset;  /* RoPE position of row 0                                     */
   uint64_t flags;      /* RF_FLAG_* (0 = defaults)                                   */
+  const float* v_scale;/* [P][H] device fp32 or NULL: the value rescale. Filled V of  */
+                       /* layer S+p, head h is multiplied by v_scale[p*H + h] before */
+                       /* rounding (see rf_value_scale). NULL = no rescale.         */
 } rf_fill_desc;
 
 /* Flags of rf_fill_desc, rf_calib_desc and rf_xmodel_desc: which tensor-core GEMM
@@ -187,6 +191,33 @@ rf_status rf_fill_kv_static(const rf_fill_desc* desc,
                             rf_bf16* k_cache, rf_bf16* v_cache,
                             int64_t layer_stride, int64_t row_stride,
                             int32_t* n_fill_out, int32_t* dev_status, rf_stream_t stream);
+
+/* Value rescale ([RF] "Hybrid layers and two corrections", value rescale; the
+ * 27B deployment uses it with c = 512, "Two numbers set the skip range"). For
+ * each upper layer l = S + p and KV head h:
+ *   v_scale[p*H + h] = mean over t in [0, c) of ||v_exact_h(t)|| / ||v_pred_h(t)||
+ *   v_pred(t)  = r(x̂) · Wv'_p x̂,  x̂ = bf16(A_p x_S[N-T+t] + b_p)   (as in the fill)
+ *   v_exact(t) = r(x)  · Wv'_p x,  x  = x_exact[p][t]
+ * where Wv'_p is the V half of Wkv (gain folded), r(x) = (mean(x²) + ε)^-1/2 and
+ * ||.|| is the L2 norm of the head's hd values. Rows whose predicted norm is 0 are
+ * left out of a head's mean (scale 1 if none is left). The result is meant for
+ * rf_fill_desc.v_scale.
+ *   c         number of tail rows used, 1 <= c <= T (rows N-T .. N-T+c-1)
+ *   x_S, ld_x as for rf_fill_kv (only rows N-T .. N-T+c-1 are read)
+ *   x_exact   [P][c][ld_e] bf16 (device): the exact inputs of layers S .. L-1
+ *             at those rows (the tail runs every layer exactly)
+ *   A, b, Wkv as for rf_fill_kv;  v_scale  [P][H] fp32 (device), written
+ * Requires d % 256 == 0, head_dim 64 or 128, KV % 128 == 0, S < L. Kernels: the
+ * fill's map GEMM on the c tail rows, one tcgen05 GEMM for the V projections of
+ * the predicted and the exact rows with per-head norms in its epilogue, and a
+ * small reduction. The workspace is rf_value_scale_workspace_bytes(desc, c). */
+size_t rf_value_scale_workspace_bytes(const rf_fill_desc* desc, int64_t c);
+rf_status rf_value_scale(const rf_fill_desc* desc, int64_t c,
+                         const rf_bf16* x_S, int64_t ld_x,
+                         const rf_bf16* x_exact, int64_t ld_e,
+                         const rf_bf16* A, const float* b, const rf_bf16* Wkv,
+                         float* v_scale, int32_t* dev_status,
+                         void* workspace, size_t workspace_bytes, rf_stream_t stream);
 
 /* ===================================================================== *
  * Calibration statistics ([RF] "Ridge map": only XᵀX, XᵀY_l and the two means

@@ -40,7 +40,8 @@ RF_FLAG_CTA_PAIR = 2
 class rf_fill_desc(ctypes.Structure):
     _fields_ = [("d", c_int64), ("L", c_int64), ("S", c_int64), ("N", c_int64), ("T", c_int64),
                 ("n_kv_heads", c_int64), ("head_dim", c_int64), ("rope_theta", c_double),
-                ("rms_eps", c_double), ("pos_offset", c_int64), ("flags", ctypes.c_uint64)]
+                ("rms_eps", c_double), ("pos_offset", c_int64), ("flags", ctypes.c_uint64),
+                ("v_scale", ctypes.c_void_p)]
 
 
 class rf_calib_desc(ctypes.Structure):
@@ -73,6 +74,9 @@ _SIGS = {
                            c_void_p]),
     "rf_fill_kv_static": (c_int, [POINTER(rf_fill_desc), c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p]),
+    "rf_value_scale_workspace_bytes": (c_size_t, [POINTER(rf_fill_desc), c_int64]),
+    "rf_value_scale": (c_int, [POINTER(rf_fill_desc), c_int64, c_void_p, c_int64, c_void_p, c_int64, c_void_p,
+                               c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "rf_calib_workspace_bytes": (c_size_t, [POINTER(rf_calib_desc), c_int64]),
     "rf_calib_accumulate": (c_int, [POINTER(rf_calib_desc), c_void_p, c_int64, c_void_p, c_int64, c_int64,
                                     c_int64, POINTER(rf_calib_stats), c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -196,6 +200,18 @@ def rf_fill_kv_static(desc, x_S, ld_x, exact_mask, A, b, Wkv, k_cache, v_cache, 
     _check(lib().rf_fill_kv_static(ctypes.byref(desc), _p(x_S), int(ld_x), _p(exact_mask), _p(A), _p(b), _p(Wkv),
                                    _p(k_cache), _p(v_cache), int(layer_stride), int(row_stride), _p(n_fill_out),
                                    _p(dev_status), _s(stream)), "rf_fill_kv_static")
+
+
+def rf_value_scale_workspace_bytes(desc: rf_fill_desc, c: int) -> int:
+    return int(lib().rf_value_scale_workspace_bytes(ctypes.byref(desc), int(c)))
+
+
+def rf_value_scale(desc, c, x_S, ld_x, x_exact, ld_e, A, b, Wkv, v_scale, dev_status=None, workspace=None,
+                   workspace_bytes=0, stream=None):
+    """Per-(layer, KV head) value-rescale factors into v_scale [P][H] fp32 (see include/rf.h)."""
+    _check(lib().rf_value_scale(ctypes.byref(desc), int(c), _p(x_S), int(ld_x), _p(x_exact), int(ld_e), _p(A), _p(b),
+                                _p(Wkv), _p(v_scale), _p(dev_status), _p(workspace), int(workspace_bytes),
+                                _s(stream)), "rf_value_scale")
 
 
 # ----------------------------------------------------------------- calibration

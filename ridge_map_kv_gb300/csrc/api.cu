@@ -231,6 +231,7 @@ const char* rf_stage_name(int s) {
     case RF_STAGE_SOLVE: return "solve";
     case RF_STAGE_UNROPE: return "unrope";
     case RF_STAGE_XMODEL_GEMM: return "xmodel_gemm";
+    case RF_STAGE_RESCALE: return "value_rescale";
     default: return "unknown";
   }
 }

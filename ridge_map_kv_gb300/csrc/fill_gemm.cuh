@@ -1,0 +1,228 @@
+// The two tensor-core GEMM problems of the fill (map GEMM, K/V GEMM), shared by
+// rf_fill_kv and the value rescale (rf_value_scale), which runs the same map
+// GEMM on the first tail rows.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "epilogue.cuh"
+#include "tc_gemm.cuh"
+
+namespace rf {
+
+// Filled rows are padded to whole 256-row units (the M of a CTA-pair tile) in
+// the gathered operand, the x̂ buffer and the sum-of-squares partials.
+constexpr int kFillRowAlign = 256;
+
+// Bytes of gathered rows Xf that one band of the map GEMM keeps in L2.
+#ifndef RF_MAP_BAND_BYTES
+#define RF_MAP_BAND_BYTES (32ll << 20)
+#endif
+constexpr long long kMapBandBytes = RF_MAP_BAND_BYTES;
+
+// --------------------------------------------------------------------------
+// 4. Map GEMM: A operand Xf [M_pad][d], B operand maps [P*d][d] (both K-major).
+//    Units run in bands of m_band M-tiles; within a band, N-tiles outer and the
+//    band's M-tiles inner. The CTAs in flight share one map tile through L2,
+//    and the band's rows of Xf (about kMapBandBytes) stay in L2 for every N-tile
+//    of the band; the maps are read once per band. Without bands, the whole Xf
+//    is re-read per N-tile and, once it outgrows the share of L2 left beside the
+//    streaming maps and outputs, LRU evicts exactly the rows needed next.
+// --------------------------------------------------------------------------
+template <bool kPair_>
+struct MapProb {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  const int32_t* n_fill;
+  const float* bias;       // [P][d]
+  __nv_bfloat16* xhat;     // [P][M_pad][d]
+  float* ssp;              // [P][d/256][M_pad]
+  int d, P, M_pad, n_ntiles, m_band;
+  int32_t* dev_status;
+  uint64_t timeout_ns;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kPair = kPair_;
+  static constexpr int kEpiWarps = 4;
+  struct EpiState {};
+  __device__ void epilogue_after(EpiState&, int, int, int, int, int, uint32_t) const {}
+  using Cfg = GemmCfg<kPair_>;
+
+  __device__ void prefetch() const {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  __device__ int m_tiles() const { return (*n_fill + Cfg::kUnitM - 1) / Cfg::kUnitM; }
+  // Unit -> (M-tile, N-tile): band b holds M-tiles [b*m_band, b*m_band + gb),
+  // gb = m_band except in the last band.
+  __device__ void decode(int u, int mtc, int& mt, int& nt) const {
+    const int per_band = m_band * n_ntiles;
+    const int b = u / per_band;
+    const int r = u - b * per_band;
+    const int gb = min(m_band, mtc - b * m_band);
+    nt = r / gb;
+    mt = b * m_band + (r - nt * gb);
+  }
+  __device__ int num_units() const { return m_tiles() * n_ntiles; }
+  __device__ int num_subtiles(int) const { return 1; }
+  __device__ int num_kb(int, int) const { return d / kBK; }
+  struct Coords {
+    int a_row, b_row;
+  };
+  __device__ Coords coords(int u, int, uint32_t rank) const {
+    int mt, nt;
+    decode(u, m_tiles(), mt, nt);
+    return {mt * Cfg::kUnitM + static_cast<int>(rank) * kBM, nt * kBN + static_cast<int>(rank) * Cfg::kBRows};
+  }
+  __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    load_operand<kBM, false, kPair>(sa, &tmA, bar, kb * kBK, c.a_row);
+    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, kb * kBK, c.b_row);
+  }
+  __device__ void epilogue(EpiState&, int u, int, int, uint32_t tacc, int row, int, uint32_t rank) const {
+    const int nf = *n_fill;
+    int mt, nt;
+    decode(u, (nf + Cfg::kUnitM - 1) / Cfg::kUnitM, mt, nt);
+    const int n0 = nt * kBN;
+    const int p = n0 / d;
+    const int c0 = n0 - p * d;
+    const int m = mt * Cfg::kUnitM + static_cast<int>(rank) * kBM + row;
+    const bool valid = m < nf;
+    const float* bp = bias + static_cast<size_t>(p) * d + c0;
+    __nv_bfloat16* dst = xhat + (static_cast<size_t>(p) * M_pad + m) * d + c0;
+    float ss = 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(tacc + ch * 32, v);
+      tmem_wait_ld32(v);
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 bb = __ldg(reinterpret_cast<const float4*>(bp + ch * 32 + i));
+        const float x0 = u2f(v[i]) + bb.x, x1 = u2f(v[i + 1]) + bb.y;
+        const float x2 = u2f(v[i + 2]) + bb.z, x3 = u2f(v[i + 3]) + bb.w;
+        ss = fmaf(x0, x0, ss);
+        ss = fmaf(x1, x1, ss);
+        ss = fmaf(x2, x2, ss);
+        ss = fmaf(x3, x3, ss);
+        pk[i / 2] = pack_bf16x2(x0, x1);
+        pk[i / 2 + 1] = pack_bf16x2(x2, x3);
+      }
+      if (valid) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_global_v4(dst + ch * 32 + 8 * q, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+    }
+    if (valid) ssp[(static_cast<size_t>(p) * (d / kBN) + c0 / kBN) * M_pad + m] = ss;
+  }
+};
+
+// --------------------------------------------------------------------------
+// 5. K/V GEMM: A operand x̂ [P*M_pad][d], B operand Wkv [P*2KV][d] (K-major).
+//    Unit u: layer p, M-tile mt, N-tile nt (N fastest: the A tile is reused by
+//    the CTAs in flight, and a layer's 2KV x d weights stay in L2).
+// --------------------------------------------------------------------------
+template <bool kPair_>
+struct KVProb {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  const int32_t* n_fill;
+  const int32_t* fill_idx;
+  const float* ssp;        // [P][d/256][M_pad]
+  const float* rope_cos;   // [n_prefix][hd/2]
+  const float* rope_sin;
+  __nv_bfloat16* kc;
+  __nv_bfloat16* vc;
+  const float* v_scale;    // [P][H] or nullptr (value rescale)
+  long long layer_stride, row_stride;
+  int d, P, S, M_pad, KV, hd, n_ntiles, n_ss;
+  float inv_d, eps;
+  int32_t* dev_status;
+  uint64_t timeout_ns;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kPair = kPair_;
+  static constexpr int kEpiWarps = 4;
+  struct EpiState {};
+  __device__ void epilogue_after(EpiState&, int, int, int, int, int, uint32_t) const {}
+  using Cfg = GemmCfg<kPair_>;
+
+  __device__ void prefetch() const {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  __device__ int m_tiles() const { return (*n_fill + Cfg::kUnitM - 1) / Cfg::kUnitM; }
+  __device__ int num_units() const { return P * m_tiles() * n_ntiles; }
+  __device__ int num_subtiles(int) const { return 1; }
+  __device__ int num_kb(int, int) const { return d / kBK; }
+  __device__ void decode(int u, int mtc, int& p, int& mt, int& nt) const {
+    const int per_layer = mtc * n_ntiles;
+    p = u / per_layer;
+    const int r = u - p * per_layer;
+    mt = r / n_ntiles;
+    nt = r - mt * n_ntiles;
+  }
+  struct Coords {
+    int a_row, b_row;
+  };
+  __device__ Coords coords(int u, int, uint32_t rank) const {
+    int p, mt, nt;
+    decode(u, m_tiles(), p, mt, nt);
+    return {p * M_pad + mt * Cfg::kUnitM + static_cast<int>(rank) * kBM,
+            p * 2 * KV + nt * kBN + static_cast<int>(rank) * Cfg::kBRows};
+  }
+  __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    load_operand<kBM, false, kPair>(sa, &tmA, bar, kb * kBK, c.a_row);
+    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, kb * kBK, c.b_row);
+  }
+  __device__ void epilogue(EpiState&, int u, int, int, uint32_t tacc, int row, int, uint32_t rank) const {
+    const int nf = *n_fill;
+    int p, mt, nt;
+    decode(u, (nf + Cfg::kUnitM - 1) / Cfg::kUnitM, p, mt, nt);
+    const int m = mt * Cfg::kUnitM + static_cast<int>(rank) * kBM + row;
+    const bool valid = m < nf;
+    int t = 0;
+    float rs = 0.f;
+    if (valid) {
+      t = fill_idx[m];
+      const float* sp = ssp + static_cast<size_t>(p) * n_ss * M_pad + m;
+      float s = 0.f;
+      for (int j = 0; j < n_ss; ++j) s += sp[static_cast<size_t>(j) * M_pad];
+      rs = rsqrtf(fmaf(s, inv_d, eps));
+    }
+    const size_t row_off = static_cast<size_t>(S + p) * layer_stride + static_cast<size_t>(t) * row_stride;
+    const int half = hd >> 1;
+    const float* cs = rope_cos + static_cast<size_t>(t) * half;
+    const float* sn = rope_sin + static_cast<size_t>(t) * half;
+#pragma unroll 1
+    for (int hh = 0; hh < kBN / hd; ++hh) {
+      const int col0 = nt * kBN + hh * hd;
+      const bool is_k = col0 < KV;
+      const int h = (is_k ? col0 : col0 - KV) / hd;
+      __nv_bfloat16* dst = (is_k ? kc : vc) + row_off + static_cast<size_t>(h) * hd;
+      const float sc = (!is_k && v_scale != nullptr) ? rs * __ldg(v_scale + p * (KV / hd) + h) : rs;
+      emit_head(tacc + hh * hd, hd, sc, nullptr, is_k, cs, sn, dst, valid);
+    }
+  }
+};
+
+// The map GEMM (x̂ = x_rows · A_pᵀ + b_p for all P maps, bf16 x̂ and Σx̂²
+// partials), launched from fill.cu only, so that its kernels exist in one
+// translation unit (a kernel instantiated in two units would have two device
+// copies, and per-kernel launch attributes would be set on only one of them).
+//   x_rows      [n_rows_max][ld_x] bf16; rows >= *n_rows are not computed
+//   n_rows      device int32: rows to compute (<= n_rows_max <= M_pad)
+//   xhat        [P][M_pad][d] bf16, ssp [P][d/256][M_pad] fp32
+struct MapGemmArgs {
+  const void* x_rows;
+  int64_t ld_x, n_rows_max;
+  const int32_t* n_rows;
+  const void* A;
+  const float* b;
+  __nv_bfloat16* xhat;
+  float* ssp;
+  int64_t d, P, M_pad;
+  int32_t* dev_status;
+};
+rf_status map_gemm(bool pair, const MapGemmArgs& a, int sms, cudaStream_t s);
+
+}  // namespace rf

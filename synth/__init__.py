@@ -108,7 +108,8 @@ FILL_CONFIGS = {"toy": TOY, "llama8b": LLAMA8B, "qwen3_8b": QWEN3_8B, "dense27b"
 
 _TENSOR_IDS = {name: i for i, name in enumerate(
     ["x_S", "mask", "A", "b", "gain", "Wk", "Wv", "calib_X", "calib_Atrue", "calib_btrue",
-     "calib_noise", "k_src", "v_src", "xWk", "xWv", "xbk", "xbv", "cache", "extra"])}
+     "calib_noise", "k_src", "v_src", "xWk", "xWv", "xbk", "xbv", "cache", "extra",
+     "rescale_scale", "rescale_noise"])}
 
 
 def sub_seed(index: int, tensor: str, salt: int = 0) -> int:
@@ -184,6 +185,22 @@ def fill_inputs(cfg: FillConfig, device="cpu", with_mask=True) -> dict:
         "Wk": _randn((P, KV, d), sub_seed(ix, "Wk"), device, std=1.0 / math.sqrt(d)),
         "Wv": _randn((P, KV, d), sub_seed(ix, "Wv"), device, std=1.0 / math.sqrt(d)),
     }
+
+
+def rescale_inputs(cfg: FillConfig, x_S: torch.Tensor, c: int, device="cpu") -> torch.Tensor:
+    """Exact inputs of the upper layers at the first c tail rows, x_exact [P, c, d]
+    (bf16): per layer, the tail's residual stream with the first d/2 channels
+    scaled by about 0.5 and the others by about 1.5 (each factor times U[0.9, 1.1]),
+    plus 0.1 * N(0, 1). With value weights that read both halves alike the norm
+    ratio stays near 1 (the layer norm removes the overall magnitude); weights
+    that favour one half move it well away from 1."""
+    P, d = cfg.P, cfg.d
+    g = _gen(device, sub_seed(cfg.index, "rescale_scale"))
+    half = torch.cat([torch.full((d // 2,), 0.5), torch.full((d - d // 2,), 1.5)]).to(device)
+    s = half.view(1, 1, d) * (0.9 + 0.2 * torch.rand((P, 1, d), generator=g, device=device, dtype=torch.float32))
+    tail = x_S[cfg.N - cfg.T: cfg.N - cfg.T + c].to(device).float()
+    noise = _randn((P, c, d), sub_seed(cfg.index, "rescale_noise"), device, std=0.1, dtype=torch.float32)
+    return (s * tail[None] + noise).to(torch.bfloat16)
 
 
 def calib_inputs(d_in: int, d_out: int, n_maps: int, n_rows: int, index: int, device="cpu",

@@ -13,17 +13,18 @@ TOL_MAX = 2e-2     # max over (layer, row, head, K|V) of ||gpu - ref|| / ||ref||
 TOL_MEAN = 3e-3    # mean of the same
 
 
-def desc_of(cfg, flags: int = 0) -> rf.rf_fill_desc:
+def desc_of(cfg, flags: int = 0, v_scale=None) -> rf.rf_fill_desc:
     return rf.rf_fill_desc(d=cfg.d, L=cfg.L, S=cfg.S, N=cfg.N, T=cfg.T, n_kv_heads=cfg.H, head_dim=cfg.hd,
-                           rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, pos_offset=cfg.pos_offset, flags=flags)
+                           rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, pos_offset=cfg.pos_offset, flags=flags,
+                           v_scale=None if v_scale is None else v_scale.data_ptr())
 
 
-def run_fill(cfg, inp: dict, dev="cuda", mask="inp", canary=True, flags: int = 0):
+def run_fill(cfg, inp: dict, dev="cuda", mask="inp", canary=True, flags: int = 0, v_scale=None):
     """Runs fold + fill on device copies of ``inp``. Returns a dict with the
     caches before/after, n_fill and the device status. ``flags`` selects the GEMM
     kernels (rf.RF_FLAG_SINGLE_CTA or rf.RF_FLAG_CTA_PAIR; 0 = library default)."""
     dev = torch.device(dev)
-    desc = desc_of(cfg, flags)
+    desc = desc_of(cfg, flags, v_scale)
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     m = g["mask"] if mask == "inp" else (mask.to(dev) if mask is not None else None)
     P, KV, d = cfg.P, cfg.KV, cfg.d
@@ -48,8 +49,9 @@ def run_fill(cfg, inp: dict, dev="cuda", mask="inp", canary=True, flags: int = 0
             "status": int(status.item()), "ws": ws, "Wkv": Wkv}
 
 
-def oracle_rows(cfg, inp: dict, rows: np.ndarray):
-    """fp64 oracle K, V [P, n, H, hd] for the given filled rows."""
+def oracle_rows(cfg, inp: dict, rows: np.ndarray, v_scale=None):
+    """fp64 oracle K, V [P, n, H, hd] for the given filled rows (V scaled by
+    v_scale [P, H] when given)."""
     f64 = O.bf16_bits_to_f64
     x = f64(synth.bits(inp["x_S"][torch.as_tensor(rows, device=inp["x_S"].device)]))
     Ks, Vs = [], []
@@ -57,7 +59,8 @@ def oracle_rows(cfg, inp: dict, rows: np.ndarray):
         K, V = O.fill_rows(x, rows + cfg.pos_offset, f64(synth.bits(inp["A"][p:p + 1])),
                            synth.f32(inp["b"][p:p + 1]).astype(np.float64), f64(synth.bits(inp["gain"][p:p + 1])),
                            f64(synth.bits(inp["Wk"][p:p + 1])), f64(synth.bits(inp["Wv"][p:p + 1])),
-                           cfg.H, cfg.hd, cfg.rope_theta, cfg.rms_eps)
+                           cfg.H, cfg.hd, cfg.rope_theta, cfg.rms_eps,
+                           None if v_scale is None else np.asarray(v_scale, np.float64)[p:p + 1])
         Ks.append(K[0])
         Vs.append(V[0])
     return np.stack(Ks), np.stack(Vs)
@@ -68,9 +71,9 @@ def head_errors(got_bits: np.ndarray, ref: np.ndarray) -> np.ndarray:
     return np.linalg.norm(got - ref, axis=-1) / np.maximum(np.linalg.norm(ref, axis=-1), 1e-6)
 
 
-def check_values(cfg, inp, res, rows: np.ndarray):
+def check_values(cfg, inp, res, rows: np.ndarray, v_scale=None):
     """Per-head relative errors of the filled K and V at ``rows`` (all layers)."""
-    K, V = oracle_rows(cfg, inp, rows)
+    K, V = oracle_rows(cfg, inp, rows, v_scale)
     rt = torch.as_tensor(rows, device=res["kc"].device)
     kb = synth.bits(res["kc"][cfg.S:].index_select(1, rt))
     vb = synth.bits(res["vc"][cfg.S:].index_select(1, rt))
@@ -80,8 +83,8 @@ def check_values(cfg, inp, res, rows: np.ndarray):
     return e
 
 
-def assert_values(cfg, inp, res, rows):
-    e = check_values(cfg, inp, res, rows)
+def assert_values(cfg, inp, res, rows, v_scale=None):
+    e = check_values(cfg, inp, res, rows, v_scale)
     assert np.all(np.isfinite(e)), "non-finite filled values"
     assert e.max() <= TOL_MAX and e.mean() <= TOL_MEAN, f"max {e.max():.3e} mean {e.mean():.3e}"
     return e

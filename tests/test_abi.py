@@ -46,7 +46,8 @@ def test_status_strings_and_version():
     assert "timed out" in rf.rf_status_string(rf.RF_ERR_TIMEOUT)
     assert rf.rf_status_string(999) == "unknown status"
     for s in ("compact", "map_gemm", "kv_gemm", "calib_gemm", "xmodel_gemm"):
-        assert s in [rf.rf_stage_name(i) for i in range(1, 12)]
+        assert s in [rf.rf_stage_name(i) for i in range(1, 13)]
+    assert rf.rf_stage_name(12) == "value_rescale"
 
 
 def _fill_desc(**kw):
@@ -111,6 +112,26 @@ def test_calib_and_xmodel_and_solve_validate_on_the_host():
                          workspace_bytes=1 << 34, stream=0)
     assert ei.value.status == rf.RF_ERR_INVALID_ARG
     assert "src_layers" in rf.rf_last_error()
+
+
+def test_value_scale_validates_on_the_host():
+    desc = _fill_desc()                       # toy: T = 3
+    assert rf.rf_value_scale_workspace_bytes(desc, 0) == 0
+    assert rf.rf_value_scale_workspace_bytes(desc, 4) == 0
+    assert rf.rf_value_scale_workspace_bytes(desc, 3) > 0
+    for c in (0, 4):
+        with pytest.raises(rf.RFError) as ei:
+            rf.rf_value_scale(desc, c, 256, 256, 256, 256, 256, 256, 256, 256, workspace=256,
+                              workspace_bytes=1 << 30, stream=0)
+        assert ei.value.status == rf.RF_ERR_INVALID_ARG
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_value_scale(desc, 2, 256, 256, None, 256, 256, 256, 256, 256, workspace=256,
+                          workspace_bytes=1 << 30, stream=0)
+    assert ei.value.status == rf.RF_ERR_INVALID_ARG
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_value_scale(desc, 2, 256, 256, 256, 256, 256, 256, 256, 256, workspace=256, workspace_bytes=64,
+                          stream=0)
+    assert ei.value.status == rf.RF_ERR_WORKSPACE
 
 
 def test_static_fill_scratch_constant_matches_header():
