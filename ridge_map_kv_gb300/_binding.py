@@ -74,6 +74,7 @@ _SIGS = {
                            c_void_p]),
     "rf_fill_kv_static": (c_int, [POINTER(rf_fill_desc), c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p]),
+    "rf_selftest_wait_timeout": (c_int, [c_int, c_void_p, c_void_p]),
     "rf_value_scale_workspace_bytes": (c_size_t, [POINTER(rf_fill_desc), c_int64]),
     "rf_value_scale": (c_int, [POINTER(rf_fill_desc), c_int64, c_void_p, c_int64, c_void_p, c_int64, c_void_p,
                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -200,6 +201,12 @@ def rf_fill_kv_static(desc, x_S, ld_x, exact_mask, A, b, Wkv, k_cache, v_cache, 
     _check(lib().rf_fill_kv_static(ctypes.byref(desc), _p(x_S), int(ld_x), _p(exact_mask), _p(A), _p(b), _p(Wkv),
                                    _p(k_cache), _p(v_cache), int(layer_stride), int(row_stride), _p(n_fill_out),
                                    _p(dev_status), _s(stream)), "rf_fill_kv_static")
+
+
+def rf_selftest_wait_timeout(cta_pair, dev_status, stream=None):
+    """Runs the GEMM core on a problem whose copies never arrive: *dev_status becomes
+    RF_ERR_TIMEOUT after the wait limit (see include/rf.h)."""
+    _check(lib().rf_selftest_wait_timeout(int(bool(cta_pair)), _p(dev_status), _s(stream)), "rf_selftest_wait_timeout")
 
 
 def rf_value_scale_workspace_bytes(desc: rf_fill_desc, c: int) -> int:
