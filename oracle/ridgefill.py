@@ -36,6 +36,10 @@ Readings where the pages leave a step open (each is listed in the design doc):
     value projection includes the layer's RMSNorm (the same path as the fill);
     a head's "magnitude" is the L2 norm of its hd-vector; rows whose predicted
     norm is 0 carry no ratio and are left out of the mean (scale 1 if none is left).
+  * Key normalisation ("Qwen models normalize keys", same section): an RMSNorm of
+    each key head over its hd values, k_h <- g_k * k_h / sqrt(mean(k_h^2) + eps)
+    with one gain vector g_k of length hd per layer and the layer's eps, applied
+    after the K projection and before RoPE.
 
 Parity status: every public function here is pinned by tests/test_oracle_pins.py
 against closed forms, invariants, textbook routines or brute force; none is
@@ -129,7 +133,7 @@ def map_predict(x_S: np.ndarray, A_l: np.ndarray, b_l: np.ndarray) -> np.ndarray
 
 
 def fill_rows(x_S_rows, positions, A, b, gain, Wk, Wv, n_kv_heads, head_dim,
-              rope_theta, rms_eps, v_scale=None):
+              rope_theta, rms_eps, v_scale=None, k_norm_gain=None):
     """Filled keys and values for a set of rows and every upper layer.
 
     For each row t and upper layer l (index p = l - S):
@@ -141,6 +145,8 @@ def fill_rows(x_S_rows, positions, A, b, gain, Wk, Wv, n_kv_heads, head_dim,
     Shapes: x_S_rows [n, d]; positions [n]; A [P, d, d]; b [P, d]; gain [P, d];
     Wk, Wv [P, H*hd, d]. Returns K, V as [P, n, H, hd] float64.
     With ``v_scale`` [P, H] (the value rescale), V_p[:, h] is multiplied by v_scale[p, h].
+    With ``k_norm_gain`` [P, hd] (key normalisation), each key head is RMS-normalised
+    with that layer's gain before RoPE.
     """
     x = np.asarray(x_S_rows, np.float64)
     n = x.shape[0]
@@ -153,13 +159,15 @@ def fill_rows(x_S_rows, positions, A, b, gain, Wk, Wv, n_kv_heads, head_dim,
         y = rms_norm(xhat, gain[p], rms_eps)
         k = (y @ np.asarray(Wk[p], np.float64).T).reshape(n, n_kv_heads, head_dim)
         v = (y @ np.asarray(Wv[p], np.float64).T).reshape(n, n_kv_heads, head_dim)
+        if k_norm_gain is not None:
+            k = rms_norm(k, np.asarray(k_norm_gain, np.float64)[p], rms_eps)
         K[p] = rope(k, pos[:, None], rope_theta)
         V[p] = v if v_scale is None else v * np.asarray(v_scale, np.float64)[p][None, :, None]
     return K, V
 
 
 def fill_kv(k_cache, v_cache, x_S, exact_mask, A, b, gain, Wk, Wv, *, L, S, N, T,
-            n_kv_heads, head_dim, rope_theta, rms_eps, pos_offset=0, v_scale=None):
+            n_kv_heads, head_dim, rope_theta, rms_eps, pos_offset=0, v_scale=None, k_norm_gain=None):
     """Whole-cache fill: returns (new_k_cache, new_v_cache, fill_idx).
 
     Caches are [L, N_cap, H, hd] arrays (float64 copies of the input caches).
@@ -173,7 +181,7 @@ def fill_kv(k_cache, v_cache, x_S, exact_mask, A, b, gain, Wk, Wv, *, L, S, N, T
     vc = np.array(v_cache, dtype=np.float64, copy=True)
     if idx.size and L > S:
         K, V = fill_rows(np.asarray(x_S, np.float64)[idx], idx + pos_offset, A, b, gain,
-                         Wk, Wv, n_kv_heads, head_dim, rope_theta, rms_eps, v_scale)
+                         Wk, Wv, n_kv_heads, head_dim, rope_theta, rms_eps, v_scale, k_norm_gain)
         for p in range(L - S):
             kc[S + p][idx] = K[p]
             vc[S + p][idx] = V[p]

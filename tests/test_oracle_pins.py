@@ -559,3 +559,62 @@ def test_fill_rows_value_scale_multiplies_values_only():
     for p in range(2):
         for h in range(2):
             np.testing.assert_allclose(V1[p, :, h], vs[p, h] * V0[p, :, h], rtol=1e-14)
+
+
+# --------------------------------------------------------------------------- #
+# Key normalisation ("Qwen models normalize keys")
+# --------------------------------------------------------------------------- #
+def _knorm_args(pr, gk, eps=0.0, Wk=None):
+    return (pr["x"], pr["pos"], pr["A"], pr["b"], pr["g"], pr["Wk"] if Wk is None else Wk, pr["Wv"],
+            pr["H"], pr["hd"], 1.0e4, eps)
+
+
+def test_key_norm_fixes_every_key_magnitude():
+    """eps = 0 and g_k = 1: each key head has RMS 1 before RoPE, and RoPE keeps
+    norms, so every filled key head has norm sqrt(hd) exactly; with a general g_k
+    the un-rotated key divided by g_k has RMS 1."""
+    pr = _tiny_fill_problem()
+    P, hd = pr["P"], pr["hd"]
+    K, V = O.fill_rows(*_knorm_args(pr, None), k_norm_gain=np.ones((P, hd)))
+    np.testing.assert_allclose(np.linalg.norm(K, axis=-1), math.sqrt(hd), rtol=1e-12)
+    gk = 1.0 + 0.5 * RNG.uniform(size=(P, hd))
+    K2, V2 = O.fill_rows(*_knorm_args(pr, None), k_norm_gain=gk)
+    for p in range(P):
+        raw = O.rope(K2[p], np.asarray(pr["pos"], np.float64)[:, None], 1.0e4, inverse=True) / gk[p]
+        np.testing.assert_allclose(np.sqrt(np.mean(raw ** 2, axis=-1)), 1.0, rtol=1e-12)
+    _, V0 = O.fill_rows(*_knorm_args(pr, None))
+    np.testing.assert_array_equal(V, V0)      # values are not normalised
+
+
+def test_key_norm_removes_the_key_projection_scale():
+    pr = _tiny_fill_problem()
+    gk = 1.0 + 0.1 * RNG.normal(size=(pr["P"], pr["hd"]))
+    K1, _ = O.fill_rows(*_knorm_args(pr, None), k_norm_gain=gk)
+    K2, _ = O.fill_rows(*_knorm_args(pr, None, Wk=3.5 * np.asarray(pr["Wk"])), k_norm_gain=gk)
+    np.testing.assert_allclose(K2, K1, rtol=1e-12, atol=1e-12)
+    K3, _ = O.fill_rows(*_knorm_args(pr, None, Wk=3.5 * np.asarray(pr["Wk"])))
+    K4, _ = O.fill_rows(*_knorm_args(pr, None))
+    np.testing.assert_allclose(K3, 3.5 * K4, rtol=1e-12)   # without the norm the scale stays
+
+
+def test_key_norm_brute_force_scalar_loops():
+    pr = _tiny_fill_problem()
+    theta, eps = 1.0e4, 1e-3
+    gk = 1.0 + 0.2 * RNG.normal(size=(pr["P"], pr["hd"]))
+    K, _ = O.fill_rows(pr["x"], pr["pos"], pr["A"], pr["b"], pr["g"], pr["Wk"], pr["Wv"], pr["H"], pr["hd"],
+                       theta, eps, k_norm_gain=gk)
+    d, H, hd = pr["d"], pr["H"], pr["hd"]
+    for p in range(pr["P"]):
+        for r in range(pr["n"]):
+            xh = [sum(pr["A"][p][o][i] * pr["x"][r][i] for i in range(d)) + pr["b"][p][o] for o in range(d)]
+            ms = sum(v * v for v in xh) / d
+            y = [pr["g"][p][i] * xh[i] / math.sqrt(ms + eps) for i in range(d)]
+            for h in range(H):
+                kk = [sum(pr["Wk"][p][h * hd + c][i] * y[i] for i in range(d)) for c in range(hd)]
+                km = sum(v * v for v in kk) / hd
+                kn = [gk[p][c] * kk[c] / math.sqrt(km + eps) for c in range(hd)]
+                for c in range(hd // 2):
+                    ang = pr["pos"][r] * theta ** (-2.0 * c / hd)
+                    k1, k2 = kn[c], kn[c + hd // 2]
+                    assert abs(K[p, r, h, c] - (k1 * math.cos(ang) - k2 * math.sin(ang))) < 1e-10
+                    assert abs(K[p, r, h, c + hd // 2] - (k2 * math.cos(ang) + k1 * math.sin(ang))) < 1e-10
