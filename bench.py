@@ -523,6 +523,34 @@ def run_extras(dev, peak_tflops, flags=0):
     del inp, kt, vt, ws
     torch.cuda.empty_cache()
 
+    # Key normalisation: the Qwen3-8B-shaped fill without and with per-head K norm
+    c = synth.QWEN3_8B
+    inp = synth.fill_inputs(c, device=dev)
+    kg = synth.key_norm_gain(c, device=dev)
+    fd = rf.rf_fill_desc(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
+                         rms_eps=c.rms_eps, pos_offset=0, flags=flags)
+    Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
+    rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
+    del inp["Wk"], inp["Wv"]
+    kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    wsb = rf.rf_fill_workspace_bytes(fd)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    nf = torch.zeros(1, dtype=torch.int32, device=dev)
+    row = {"workload": f"qwen3-8b-shaped fill (d={c.d}, {c.P} upper layers, N={c.N}, T={c.T}, no exact rows)"}
+    for key, gain_ptr in (("plain", None), ("key_norm", kg.data_ptr())):
+        fd.k_norm_gain = gain_ptr
+        ms, st = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
+                                              c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
+        n_fill = int(nf.item())
+        f_flops = 2.0 * n_fill * c.P * (c.d * c.d + c.d * 2 * c.KV)
+        row[f"{key}_ms"] = ms
+        row[f"{key}_tflops"] = f_flops / (ms / 1e3) / 1e12
+        row[f"{key}_kv_gemm_ms"] = st.get("kv_gemm")
+    out["next2_key_norm_qwen3"] = row
+    del inp, kc, vc, ws, Wkv
+    torch.cuda.empty_cache()
+
     # Value rescale (the 27B deployment, c = 512), then the 27B fill with the scale
     c = synth.DENSE27B
     n_tail = 512

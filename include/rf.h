@@ -122,6 +122,9 @@ typedef struct rf_fill_desc {
   const float* v_scale;/* [P][H] device fp32 or NULL: the value rescale. Filled V of  */
                        /* layer S+p, head h is multiplied by v_scale[p*H + h] before */
                        /* rounding (see rf_value_scale). NULL = no rescale.         */
+  const rf_bf16* k_norm_gain; /* [P][hd] device bf16 or NULL: key normalisation.      */
+                       /* Each key head becomes g_p * k_h / sqrt(mean(k_h²) + ε)      */
+                       /* (ε = rms_eps) before RoPE ("Qwen models normalize keys").  */
 } rf_fill_desc;
 
 /* Flags of rf_fill_desc, rf_calib_desc and rf_xmodel_desc: which tensor-core GEMM

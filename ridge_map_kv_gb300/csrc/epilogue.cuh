@@ -10,10 +10,15 @@
 namespace rf {
 
 // acc column c (0 <= c < hd) of this thread's row lives at TMEM column tcol + c.
-// out[c] = bf16(f(acc[c] * scale + bias[c])), with f = RoPE at the table row
-// (cs, sn) when `rope`, else the identity. bias may be nullptr.
+// out[c] = bf16(f((acc[c] * scale + bias[c]) * gain[c])), with f = RoPE at the
+// table row (cs, sn) when `rope`, else the identity. bias and gain may be nullptr.
+__device__ __forceinline__ float gain_at(const __nv_bfloat16* __restrict__ gain, int c) {
+  return gain != nullptr ? __bfloat162float(gain[c]) : 1.0f;
+}
+
 __device__ __forceinline__ void emit_head(uint32_t tcol, int hd, float scale, const float* __restrict__ bias,
-                                          bool rope, const float* __restrict__ cs, const float* __restrict__ sn,
+                                          const __nv_bfloat16* __restrict__ gain, bool rope,
+                                          const float* __restrict__ cs, const float* __restrict__ sn,
                                           __nv_bfloat16* dst, bool valid) {
   const int half = hd >> 1;
   if (rope) {
@@ -41,8 +46,8 @@ __device__ __forceinline__ void emit_head(uint32_t tcol, int hd, float scale, co
         float r1[4], r2[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float x1 = fmaf(u2f(a[i + q]), scale, bb1[q]);
-          const float x2 = fmaf(u2f(b[i + q]), scale, bb2[q]);
+          const float x1 = fmaf(u2f(a[i + q]), scale, bb1[q]) * gain_at(gain, i0 + i + q);
+          const float x2 = fmaf(u2f(b[i + q]), scale, bb2[q]) * gain_at(gain, half + i0 + i + q);
           r1[q] = x1 * cc[q] - x2 * ssn[q];
           r2[q] = x2 * cc[q] + x1 * ssn[q];
         }
@@ -69,8 +74,11 @@ __device__ __forceinline__ void emit_head(uint32_t tcol, int hd, float scale, co
       for (int i = 0; i < 32; i += 4) {
         float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
         if (bias != nullptr) bb = __ldg(reinterpret_cast<const float4*>(bias + i0 + i));
-        pk[i / 2] = pack_bf16x2(fmaf(u2f(v[i]), scale, bb.x), fmaf(u2f(v[i + 1]), scale, bb.y));
-        pk[i / 2 + 1] = pack_bf16x2(fmaf(u2f(v[i + 2]), scale, bb.z), fmaf(u2f(v[i + 3]), scale, bb.w));
+        const int c = i0 + i;
+        pk[i / 2] = pack_bf16x2(fmaf(u2f(v[i]), scale, bb.x) * gain_at(gain, c),
+                                fmaf(u2f(v[i + 1]), scale, bb.y) * gain_at(gain, c + 1));
+        pk[i / 2 + 1] = pack_bf16x2(fmaf(u2f(v[i + 2]), scale, bb.z) * gain_at(gain, c + 2),
+                                    fmaf(u2f(v[i + 3]), scale, bb.w) * gain_at(gain, c + 3));
       }
       if (valid) {
 #pragma unroll

@@ -215,6 +215,7 @@ rf_status fill_gemms(const rf_fill_desc* desc, const FillLayout& lay, const rf_b
     pr.kc = reinterpret_cast<__nv_bfloat16*>(k_cache);
     pr.vc = reinterpret_cast<__nv_bfloat16*>(v_cache);
     pr.v_scale = desc->v_scale;
+    pr.k_gain = reinterpret_cast<const __nv_bfloat16*>(desc->k_norm_gain);
     pr.layer_stride = layer_stride;
     pr.row_stride = row_stride;
     pr.d = static_cast<int>(d);

@@ -133,6 +133,7 @@ struct KVProb {
   __nv_bfloat16* kc;
   __nv_bfloat16* vc;
   const float* v_scale;    // [P][H] or nullptr (value rescale)
+  const __nv_bfloat16* k_gain;  // [P][hd] or nullptr (key normalisation)
   long long layer_stride, row_stride;
   int d, P, S, M_pad, KV, hd, n_ntiles, n_ss;
   float inv_d, eps;
@@ -199,8 +200,25 @@ struct KVProb {
       const bool is_k = col0 < KV;
       const int h = (is_k ? col0 : col0 - KV) / hd;
       __nv_bfloat16* dst = (is_k ? kc : vc) + row_off + static_cast<size_t>(h) * hd;
-      const float sc = (!is_k && v_scale != nullptr) ? rs * __ldg(v_scale + p * (KV / hd) + h) : rs;
-      emit_head(tacc + hh * hd, hd, sc, nullptr, is_k, cs, sn, dst, valid);
+      float sc = rs;
+      const __nv_bfloat16* g = nullptr;
+      if (!is_k && v_scale != nullptr) sc = rs * __ldg(v_scale + p * (KV / hd) + h);
+      if (is_k && k_gain != nullptr) {
+        // Key normalisation: RMS of the head's rs-scaled values, then its gain (the
+        // TMEM loads are warp-collective; the branch is uniform across the warp).
+        float q = 0.f;
+#pragma unroll 1
+        for (int i0 = 0; i0 < hd; i0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tacc + hh * hd + i0, v);
+          tmem_wait_ld32(v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) q = fmaf(u2f(v[i]), u2f(v[i]), q);
+        }
+        sc = rs * rsqrtf(fmaf(rs * rs, q / static_cast<float>(hd), eps));
+        g = k_gain + static_cast<size_t>(p) * hd;
+      }
+      emit_head(tacc + hh * hd, hd, sc, nullptr, g, is_k, cs, sn, dst, valid);
     }
   }
 };

@@ -175,7 +175,7 @@ struct XMProb {
     __nv_bfloat16* dst = (is_k ? k_tgt : v_tgt) + (static_cast<size_t>(l) * N + tt) * KV + col0;
 #pragma unroll 1
     for (int hh = 0; hh < kBN / hd; ++hh)
-      emit_head(tacc + hh * hd, hd, 1.0f, bias + hh * hd, is_k, cs, sn, dst + hh * hd, valid);
+      emit_head(tacc + hh * hd, hd, 1.0f, bias + hh * hd, nullptr, is_k, cs, sn, dst + hh * hd, valid);
   }
 };
 

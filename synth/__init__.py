@@ -109,7 +109,7 @@ FILL_CONFIGS = {"toy": TOY, "llama8b": LLAMA8B, "qwen3_8b": QWEN3_8B, "dense27b"
 _TENSOR_IDS = {name: i for i, name in enumerate(
     ["x_S", "mask", "A", "b", "gain", "Wk", "Wv", "calib_X", "calib_Atrue", "calib_btrue",
      "calib_noise", "k_src", "v_src", "xWk", "xWv", "xbk", "xbv", "cache", "extra",
-     "rescale_scale", "rescale_noise"])}
+     "rescale_scale", "rescale_noise", "key_norm_gain"])}
 
 
 def sub_seed(index: int, tensor: str, salt: int = 0) -> int:
@@ -185,6 +185,11 @@ def fill_inputs(cfg: FillConfig, device="cpu", with_mask=True) -> dict:
         "Wk": _randn((P, KV, d), sub_seed(ix, "Wk"), device, std=1.0 / math.sqrt(d)),
         "Wv": _randn((P, KV, d), sub_seed(ix, "Wv"), device, std=1.0 / math.sqrt(d)),
     }
+
+
+def key_norm_gain(cfg: FillConfig, device="cpu") -> torch.Tensor:
+    """Per-layer key-normalisation gains [P, hd] (bf16), 1 + 0.1 * N(0, 1)."""
+    return _randn((cfg.P, cfg.hd), sub_seed(cfg.index, "key_norm_gain"), device, std=0.1, mean=1.0)
 
 
 def rescale_inputs(cfg: FillConfig, x_S: torch.Tensor, c: int, device="cpu") -> torch.Tensor:

@@ -13,18 +13,21 @@ TOL_MAX = 2e-2     # max over (layer, row, head, K|V) of ||gpu - ref|| / ||ref||
 TOL_MEAN = 3e-3    # mean of the same
 
 
-def desc_of(cfg, flags: int = 0, v_scale=None) -> rf.rf_fill_desc:
+def desc_of(cfg, flags: int = 0, v_scale=None, k_norm_gain=None) -> rf.rf_fill_desc:
     return rf.rf_fill_desc(d=cfg.d, L=cfg.L, S=cfg.S, N=cfg.N, T=cfg.T, n_kv_heads=cfg.H, head_dim=cfg.hd,
                            rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, pos_offset=cfg.pos_offset, flags=flags,
-                           v_scale=None if v_scale is None else v_scale.data_ptr())
+                           v_scale=None if v_scale is None else v_scale.data_ptr(),
+                           k_norm_gain=None if k_norm_gain is None else k_norm_gain.data_ptr())
 
 
-def run_fill(cfg, inp: dict, dev="cuda", mask="inp", canary=True, flags: int = 0, v_scale=None):
+def run_fill(cfg, inp: dict, dev="cuda", mask="inp", canary=True, flags: int = 0, v_scale=None,
+             k_norm_gain=None):
     """Runs fold + fill on device copies of ``inp``. Returns a dict with the
     caches before/after, n_fill and the device status. ``flags`` selects the GEMM
     kernels (rf.RF_FLAG_SINGLE_CTA or rf.RF_FLAG_CTA_PAIR; 0 = library default)."""
     dev = torch.device(dev)
-    desc = desc_of(cfg, flags, v_scale)
+    kng = None if k_norm_gain is None else k_norm_gain.to(dev)   # alive until the fill is done
+    desc = desc_of(cfg, flags, v_scale, kng)
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     m = g["mask"] if mask == "inp" else (mask.to(dev) if mask is not None else None)
     P, KV, d = cfg.P, cfg.KV, cfg.d
@@ -49,7 +52,7 @@ def run_fill(cfg, inp: dict, dev="cuda", mask="inp", canary=True, flags: int = 0
             "status": int(status.item()), "ws": ws, "Wkv": Wkv}
 
 
-def oracle_rows(cfg, inp: dict, rows: np.ndarray, v_scale=None):
+def oracle_rows(cfg, inp: dict, rows: np.ndarray, v_scale=None, k_norm_gain=None):
     """fp64 oracle K, V [P, n, H, hd] for the given filled rows (V scaled by
     v_scale [P, H] when given)."""
     f64 = O.bf16_bits_to_f64
@@ -60,7 +63,8 @@ def oracle_rows(cfg, inp: dict, rows: np.ndarray, v_scale=None):
                            synth.f32(inp["b"][p:p + 1]).astype(np.float64), f64(synth.bits(inp["gain"][p:p + 1])),
                            f64(synth.bits(inp["Wk"][p:p + 1])), f64(synth.bits(inp["Wv"][p:p + 1])),
                            cfg.H, cfg.hd, cfg.rope_theta, cfg.rms_eps,
-                           None if v_scale is None else np.asarray(v_scale, np.float64)[p:p + 1])
+                           None if v_scale is None else np.asarray(v_scale, np.float64)[p:p + 1],
+                           None if k_norm_gain is None else f64(synth.bits(k_norm_gain[p:p + 1])))
         Ks.append(K[0])
         Vs.append(V[0])
     return np.stack(Ks), np.stack(Vs)
@@ -71,9 +75,9 @@ def head_errors(got_bits: np.ndarray, ref: np.ndarray) -> np.ndarray:
     return np.linalg.norm(got - ref, axis=-1) / np.maximum(np.linalg.norm(ref, axis=-1), 1e-6)
 
 
-def check_values(cfg, inp, res, rows: np.ndarray, v_scale=None):
+def check_values(cfg, inp, res, rows: np.ndarray, v_scale=None, k_norm_gain=None):
     """Per-head relative errors of the filled K and V at ``rows`` (all layers)."""
-    K, V = oracle_rows(cfg, inp, rows, v_scale)
+    K, V = oracle_rows(cfg, inp, rows, v_scale, k_norm_gain)
     rt = torch.as_tensor(rows, device=res["kc"].device)
     kb = synth.bits(res["kc"][cfg.S:].index_select(1, rt))
     vb = synth.bits(res["vc"][cfg.S:].index_select(1, rt))
@@ -83,8 +87,8 @@ def check_values(cfg, inp, res, rows: np.ndarray, v_scale=None):
     return e
 
 
-def assert_values(cfg, inp, res, rows, v_scale=None):
-    e = check_values(cfg, inp, res, rows, v_scale)
+def assert_values(cfg, inp, res, rows, v_scale=None, k_norm_gain=None):
+    e = check_values(cfg, inp, res, rows, v_scale, k_norm_gain)
     assert np.all(np.isfinite(e)), "non-finite filled values"
     assert e.max() <= TOL_MAX and e.mean() <= TOL_MEAN, f"max {e.max():.3e} mean {e.mean():.3e}"
     return e

@@ -122,3 +122,38 @@ def test_fill_full_size_sampled(name, flags):
     assert_bookkeeping(cfg, res, mnp)
     rows = _sample_rows(idx, mnp, cfg.N - cfg.T)
     assert_values(cfg, inp, res, rows)
+
+
+# --------------------------------------------------------------------------- #
+# Key normalisation (per-head RMSNorm of K before RoPE, "Qwen models normalize keys")
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("cfg", [
+    _small("key norm, hd128, ragged 3 M-tiles"),
+    _small("key norm, hd64, 4 heads", d=768, L=4, S=2, N=300, T=20, H=4, hd=64, exact="blocks16_5"),
+], ids=lambda c: c.name)
+@KERNELS
+def test_fill_with_key_norm_matches_oracle(cfg, flags):
+    inp = synth.fill_inputs(cfg)
+    kg = synth.key_norm_gain(cfg)
+    res = run_fill(cfg, inp, flags=flags, k_norm_gain=kg)
+    assert res["status"] == 0
+    mnp = _mask_np(inp)
+    idx = O.prefix_partition(cfg.N, cfg.T, mnp)
+    assert_bookkeeping(cfg, res, mnp)
+    assert_values(cfg, inp, res, idx, k_norm_gain=kg)
+
+
+@pytest.mark.slow
+def test_fill_with_key_norm_qwen3_shape_sampled():
+    """Qwen3-8B shape (d=4096, 23 upper layers, N=32768, no exact rows) with key
+    normalisation: bookkeeping on the whole cache, values on sampled rows."""
+    cfg = synth.FILL_CONFIGS["qwen3_8b"]
+    inp = synth.fill_inputs(cfg, device="cuda")
+    kg = synth.key_norm_gain(cfg, device="cuda")
+    res = run_fill(cfg, inp, k_norm_gain=kg)
+    assert res["status"] == 0
+    mnp = _mask_np(inp)
+    idx = O.prefix_partition(cfg.N, cfg.T, mnp)
+    assert res["n_fill"] == len(idx)
+    assert_bookkeeping(cfg, res, mnp)
+    assert_values(cfg, inp, res, _sample_rows(idx, mnp, cfg.N - cfg.T), k_norm_gain=kg)
