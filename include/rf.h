@@ -108,7 +108,8 @@ const char* rf_stage_name(int stage_id);
  * x̂_l = A_l x_S + b_l; the layer's own norm and K/V projections and RoPE)
  * ===================================================================== */
 typedef struct rf_fill_desc {
-  int64_t d;           /* hidden size: map input and output width, projection input  */
+  int64_t d;           /* hidden size: map output width, projection input; also the */
+                       /* map input width unless d_in is set                        */
   int64_t L;           /* number of layers                                          */
   int64_t S;           /* split layer: maps exist for layers S .. L-1 (P = L - S)    */
   int64_t N;           /* prompt rows                                               */
@@ -125,6 +126,10 @@ typedef struct rf_fill_desc {
   const rf_bf16* k_norm_gain; /* [P][hd] device bf16 or NULL: key normalisation.      */
                        /* Each key head becomes g_p * k_h / sqrt(mean(k_h²) + ε)      */
                        /* (ε = rms_eps) before RoPE ("Qwen models normalize keys").  */
+  int64_t d_in;        /* width of x_S rows and of the maps' input; 0 = d (square).  */
+                       /* Non-square maps A_p [d][d_in] read a wider split state,    */
+                       /* e.g. parallel residual streams ([RF] "Ridge map": 10,240 */
+                       /* -> 2,560 for Flash-Next). Must be a multiple of 256.       */
 } rf_fill_desc;
 
 /* Flags of rf_fill_desc, rf_calib_desc and rf_xmodel_desc: which tensor-core GEMM
@@ -158,9 +163,9 @@ rf_status rf_fold_kv_weights(const rf_fill_desc* desc, const rf_bf16* gain,
  *   k_cache[l][t][h][:] = bf16(k_h),  v_cache[l][t][h][:] = bf16(v_h).
  * Nothing else in the caches is written: not the tail, not exact rows, not
  * layers < S ([RF] Table 3). x̂ is rounded to bf16 before the projection.
- *   x_S        [N][ld_x] bf16, the residual stream entering layer S
+ *   x_S        [N][ld_x] bf16 rows of width d_in (d if d_in = 0), the state entering layer S
  *   exact_mask [N-T] uint8, nonzero = exact row (never filled); NULL = none
- *   A          [P][d][d] bf16, A_p[o][i] (row = output)
+ *   A          [P][d][d_in] bf16, A_p[o][i] (row = output)
  *   b          [P][d] fp32
  *   Wkv        [P][2*KV][d] bf16 from rf_fold_kv_weights
  *   k_cache, v_cache: element (l, t, h, c) at l*layer_stride + t*row_stride + h*hd + c

@@ -41,7 +41,7 @@ class rf_fill_desc(ctypes.Structure):
     _fields_ = [("d", c_int64), ("L", c_int64), ("S", c_int64), ("N", c_int64), ("T", c_int64),
                 ("n_kv_heads", c_int64), ("head_dim", c_int64), ("rope_theta", c_double),
                 ("rms_eps", c_double), ("pos_offset", c_int64), ("flags", ctypes.c_uint64),
-                ("v_scale", ctypes.c_void_p), ("k_norm_gain", ctypes.c_void_p)]
+                ("v_scale", ctypes.c_void_p), ("k_norm_gain", ctypes.c_void_p), ("d_in", c_int64)]
 
 
 class rf_calib_desc(ctypes.Structure):

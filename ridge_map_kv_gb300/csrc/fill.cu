@@ -155,6 +155,9 @@ struct FillLayout {
   size_t bytes;
 };
 
+// Width of x_S rows and of the maps' input (d_in = 0 means square maps).
+static int64_t fill_din(const rf_fill_desc* d) { return d->d_in > 0 ? d->d_in : d->d; }
+
 static rf_status check_fill_desc(const rf_fill_desc* d) {
   if (d == nullptr) return fail(RF_ERR_INVALID_ARG, "desc is NULL");
   if (d->d <= 0 || d->L <= 0 || d->S < 0 || d->S > d->L || d->N < 0 || d->T < 0 || d->T > d->N ||
@@ -162,6 +165,9 @@ static rf_status check_fill_desc(const rf_fill_desc* d) {
     return fail(RF_ERR_INVALID_ARG, "need d > 0, L > 0, 0 <= S <= L, 0 <= T <= N, H > 0, hd > 0");
   if (!(d->rope_theta > 0.0) || !(d->rms_eps >= 0.0)) return fail(RF_ERR_INVALID_ARG, "need rope_theta > 0, rms_eps >= 0");
   if (d->d % kBN != 0) return fail(RF_ERR_SHAPE, "d = %lld must be a multiple of 256", (long long)d->d);
+  if (d->d_in < 0 || fill_din(d) % kBN != 0)
+    return fail(RF_ERR_SHAPE, "d_in = %lld must be 0 (square maps) or a multiple of 256", (long long)d->d_in);
+  if (fill_din(d) > (int64_t(1) << 20)) return fail(RF_ERR_SHAPE, "d_in must be <= 2^20");
   if (d->head_dim != 64 && d->head_dim != 128) return fail(RF_ERR_SHAPE, "head_dim must be 64 or 128");
   const int64_t KV = d->n_kv_heads * d->head_dim;
   if (KV % 128 != 0) return fail(RF_ERR_SHAPE, "n_kv_heads * head_dim = %lld must be a multiple of 128", (long long)KV);
@@ -179,7 +185,7 @@ static FillLayout fill_layout(const rf_fill_desc* d, void* ws) {
   FillLayout l;
   l.fill_idx = c.take<int32_t>(std::max<int64_t>(n_prefix, 1));
   l.n_fill = c.take<int32_t>(1);
-  l.xf = c.take<__nv_bfloat16>(M_pad * d->d);
+  l.xf = c.take<__nv_bfloat16>(M_pad * fill_din(d));
   l.xhat = c.take<__nv_bfloat16>(P * M_pad * d->d);
   l.ssp = c.take<float>(P * (d->d / kBN) * M_pad);
   l.rope_cos = c.take<float>(std::max<int64_t>(n_prefix, 1) * (d->head_dim / 2));
@@ -200,7 +206,8 @@ rf_status fill_gemms(const rf_fill_desc* desc, const FillLayout& lay, const rf_b
   const int64_t m_tiles_max = M_pad / Cfg::kUnitM;
   const uint64_t tmo = wait_timeout_ns();
   {
-    MapGemmArgs ma{lay.xf, d, M_pad, lay.n_fill, A, b, lay.xhat, lay.ssp, d, P, M_pad, dev_status};
+    const int64_t d_in = fill_din(desc);
+    MapGemmArgs ma{lay.xf, d_in, M_pad, lay.n_fill, A, b, lay.xhat, lay.ssp, d, d_in, P, M_pad, dev_status};
     if ((st = map_gemm(kPair, ma, sms, s)) != RF_OK) return st;
   }
   {
@@ -241,19 +248,20 @@ static rf_status map_gemm_t(const MapGemmArgs& a, int sms, cudaStream_t s) {
   using Cfg = GemmCfg<kPair>;
   rf_status st;
   MapProb<kPair> pr;
-  if ((st = make_tmap_bf16_2d(&pr.tmA, a.x_rows, a.d, a.n_rows_max, a.ld_x, kBK, kBM)) != RF_OK) return st;
-  if ((st = make_tmap_bf16_2d(&pr.tmB, a.A, a.d, a.P * a.d, a.d, kBK, Cfg::kBRows)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmA, a.x_rows, a.d_in, a.n_rows_max, a.ld_x, kBK, kBM)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmB, a.A, a.d_in, a.P * a.d, a.d_in, kBK, Cfg::kBRows)) != RF_OK) return st;
   const int64_t m_tiles_max = a.M_pad / Cfg::kUnitM;
   pr.n_fill = a.n_rows;
   pr.bias = a.b;
   pr.xhat = a.xhat;
   pr.ssp = a.ssp;
   pr.d = static_cast<int>(a.d);
+  pr.k_in = static_cast<int>(a.d_in);
   pr.P = static_cast<int>(a.P);
   pr.M_pad = static_cast<int>(a.M_pad);
   pr.n_ntiles = static_cast<int>(a.P * a.d / kBN);
   pr.m_band = static_cast<int>(
-      std::max<long long>(1, std::min<long long>(m_tiles_max, kMapBandBytes / (Cfg::kUnitM * a.d * 2))));
+      std::max<long long>(1, std::min<long long>(m_tiles_max, kMapBandBytes / (Cfg::kUnitM * a.d_in * 2))));
   pr.dev_status = a.dev_status;
   pr.timeout_ns = wait_timeout_ns();
   ProfScope prof(s, RF_STAGE_MAP_GEMM);
@@ -316,7 +324,8 @@ extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, in
     if (!A || !b || !Wkv || !k_cache || !v_cache) return fail(RF_ERR_INVALID_ARG, "A, b, Wkv, k_cache, v_cache must be non-NULL");
     if (!aligned16(x_S) || !aligned16(A) || !aligned16(b) || !aligned16(Wkv) || !aligned16(k_cache) || !aligned16(v_cache))
       return fail(RF_ERR_ALIGN, "x_S, A, b, Wkv and the caches must be 16-byte aligned");
-    if (ld_x < d || ld_x % 8 != 0) return fail(RF_ERR_ALIGN, "ld_x must be >= d and a multiple of 8");
+    if (ld_x < fill_din(desc) || ld_x % 8 != 0)
+      return fail(RF_ERR_ALIGN, "ld_x must be >= d_in (d for square maps) and a multiple of 8");
     if (row_stride < KV || row_stride % 8 != 0 || layer_stride < 0 || layer_stride % 8 != 0)
       return fail(RF_ERR_ALIGN, "row_stride must be >= H*hd and a multiple of 8; layer_stride a multiple of 8");
   }
@@ -344,7 +353,8 @@ extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, in
     ProfScope prof(s, RF_STAGE_GATHER);
     k_gather_rows<<<static_cast<unsigned>(M_pad), 128, 0, s>>>(reinterpret_cast<const uint4*>(x_S), ld_x / 8,
                                                               lay.fill_idx, lay.n_fill, reinterpret_cast<uint4*>(lay.xf),
-                                                              static_cast<int>(d / 8), static_cast<int>(M_pad));
+                                                              static_cast<int>(fill_din(desc) / 8),
+                                                              static_cast<int>(M_pad));
   }
   const int half = static_cast<int>(desc->head_dim / 2);
   const int rope_blocks = static_cast<int>(std::min<int64_t>((n_prefix * half + 255) / 256, 4LL * sms));

@@ -36,7 +36,7 @@ struct MapProb {
   const float* bias;       // [P][d]
   __nv_bfloat16* xhat;     // [P][M_pad][d]
   float* ssp;              // [P][d/256][M_pad]
-  int d, P, M_pad, n_ntiles, m_band;
+  int d, k_in, P, M_pad, n_ntiles, m_band;  // d: map output width; k_in: map input width
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = false;
@@ -64,7 +64,7 @@ struct MapProb {
   }
   __device__ int num_units() const { return m_tiles() * n_ntiles; }
   __device__ int num_subtiles(int) const { return 1; }
-  __device__ int num_kb(int, int) const { return d / kBK; }
+  __device__ int num_kb(int, int) const { return k_in / kBK; }
   struct Coords {
     int a_row, b_row;
   };
@@ -227,8 +227,9 @@ struct KVProb {
 // partials), launched from fill.cu only, so that its kernels exist in one
 // translation unit (a kernel instantiated in two units would have two device
 // copies, and per-kernel launch attributes would be set on only one of them).
-//   x_rows      [n_rows_max][ld_x] bf16; rows >= *n_rows are not computed
+//   x_rows      [n_rows_max][ld_x] bf16 rows of width d_in; rows >= *n_rows are not computed
 //   n_rows      device int32: rows to compute (<= n_rows_max <= M_pad)
+//   A           [P][d][d_in] bf16, b [P][d] fp32
 //   xhat        [P][M_pad][d] bf16, ssp [P][d/256][M_pad] fp32
 struct MapGemmArgs {
   const void* x_rows;
@@ -238,7 +239,7 @@ struct MapGemmArgs {
   const float* b;
   __nv_bfloat16* xhat;
   float* ssp;
-  int64_t d, P, M_pad;
+  int64_t d, d_in, P, M_pad;
   int32_t* dev_status;
 };
 rf_status map_gemm(bool pair, const MapGemmArgs& a, int sms, cudaStream_t s);

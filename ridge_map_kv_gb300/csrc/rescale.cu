@@ -192,6 +192,8 @@ static rf_status check_rescale(const rf_fill_desc* d, int64_t c) {
       d->n_kv_heads <= 0 || (d->head_dim != 64 && d->head_dim != 128) || !(d->rms_eps >= 0.0))
     return fail(RF_ERR_INVALID_ARG, "need d > 0, 0 <= S < L, 0 <= T <= N, H > 0, head_dim 64 or 128, rms_eps >= 0");
   if (d->d % kBN != 0) return fail(RF_ERR_SHAPE, "d = %lld must be a multiple of 256", (long long)d->d);
+  if (d->d_in < 0 || d->d_in % kBN != 0 || d->d_in > (int64_t(1) << 20))
+    return fail(RF_ERR_SHAPE, "d_in = %lld must be 0 (square maps) or a multiple of 256", (long long)d->d_in);
   const int64_t KV = d->n_kv_heads * d->head_dim;
   if (KV % 128 != 0) return fail(RF_ERR_SHAPE, "n_kv_heads * head_dim = %lld must be a multiple of 128", (long long)KV);
   if (c < 1 || c > d->T) return fail(RF_ERR_INVALID_ARG, "need 1 <= c <= T (c = %lld, T = %lld)", (long long)c,
@@ -213,7 +215,8 @@ static rf_status rescale_gemms(const rf_fill_desc* desc, int64_t c, const Rescal
   const int64_t Mc = round_up(c, kFillRowAlign);
   const uint64_t tmo = wait_timeout_ns();
   {
-    MapGemmArgs ma{x_tail, ld_x, c, lay.n_c, A, b, lay.xhat, lay.ssp, d, P, Mc, dev_status};
+    const int64_t d_in = desc->d_in > 0 ? desc->d_in : d;
+    MapGemmArgs ma{x_tail, ld_x, c, lay.n_c, A, b, lay.xhat, lay.ssp, d, d_in, P, Mc, dev_status};
     if ((st = map_gemm(kPair, ma, sms, s)) != RF_OK) return st;
   }
   {
@@ -269,8 +272,9 @@ extern "C" rf_status rf_value_scale(const rf_fill_desc* desc, int64_t c, const r
   if (!x_S || !x_exact || !A || !b || !Wkv || !v_scale)
     return fail(RF_ERR_INVALID_ARG, "x_S, x_exact, A, b, Wkv and v_scale must be non-NULL");
   const int64_t d = desc->d;
-  if (ld_x < d || ld_x % 8 != 0 || ld_e < d || ld_e % 8 != 0)
-    return fail(RF_ERR_ALIGN, "ld_x and ld_e must be >= d and multiples of 8");
+  const int64_t d_in = desc->d_in > 0 ? desc->d_in : d;
+  if (ld_x < d_in || ld_x % 8 != 0 || ld_e < d || ld_e % 8 != 0)
+    return fail(RF_ERR_ALIGN, "ld_x must be >= d_in, ld_e >= d, both multiples of 8");
   const rf_bf16* x_tail = reinterpret_cast<const rf_bf16*>(reinterpret_cast<const __nv_bfloat16*>(x_S) +
                                                            (desc->N - desc->T) * ld_x);
   if (!aligned16(x_tail) || !aligned16(x_exact) || !aligned16(A) || !aligned16(b) || !aligned16(Wkv))

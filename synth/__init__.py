@@ -47,6 +47,11 @@ class FillConfig:
     calib_n: int
     rms_eps: float = 1e-5
     pos_offset: int = 0
+    d_in: int = 0            # width of x_S and of the maps' input; 0 = d (square maps)
+
+    @property
+    def D_in(self) -> int:
+        return self.d_in if self.d_in > 0 else self.d
 
     @property
     def P(self) -> int:
@@ -168,16 +173,22 @@ def exact_mask(cfg: FillConfig, device="cpu", seed: Optional[int] = None) -> Opt
 
 
 def fill_inputs(cfg: FillConfig, device="cpu", with_mask=True) -> dict:
-    """Inputs of one fill: x_S [N, d], mask [N-T] (or None), maps A [P, d, d],
+    """Inputs of one fill: x_S [N, d_in], mask [N-T] (or None), maps A [P, d, d_in],
     offsets b [P, d] (fp32), gains [P, d], W_k and W_v [P, H*hd, d]."""
-    P, d, KV = cfg.P, cfg.d, cfg.KV
+    P, d, KV, di = cfg.P, cfg.d, cfg.KV, cfg.D_in
     ix = cfg.index
-    A = _randn((P, d, d), sub_seed(ix, "A"), device, std=0.02 / math.sqrt(d))
+    A = _randn((P, d, di), sub_seed(ix, "A"), device, std=0.02 / math.sqrt(di))
+    # Square maps are I + noise. A wider input (di = s * d, s parallel streams of
+    # width d) maps to the mean of the streams + noise: [I ... I] / s.
     eye = torch.eye(d, dtype=torch.float32, device=device)
+    streams = di // d if di % d == 0 else 0
     for p in range(P):
-        A[p] = (A[p].float() + eye).to(torch.bfloat16)
+        if streams:
+            A[p] = (A[p].float() + eye.repeat(1, streams) / streams).to(torch.bfloat16)
+        elif di == d:
+            A[p] = (A[p].float() + eye).to(torch.bfloat16)
     return {
-        "x_S": _randn((cfg.N, d), sub_seed(ix, "x_S"), device),
+        "x_S": _randn((cfg.N, di), sub_seed(ix, "x_S"), device),
         "mask": exact_mask(cfg, device) if with_mask else None,
         "A": A,
         "b": _randn((P, d), sub_seed(ix, "b"), device, std=0.1, dtype=torch.float32),

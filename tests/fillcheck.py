@@ -16,6 +16,7 @@ TOL_MEAN = 3e-3    # mean of the same
 def desc_of(cfg, flags: int = 0, v_scale=None, k_norm_gain=None) -> rf.rf_fill_desc:
     return rf.rf_fill_desc(d=cfg.d, L=cfg.L, S=cfg.S, N=cfg.N, T=cfg.T, n_kv_heads=cfg.H, head_dim=cfg.hd,
                            rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, pos_offset=cfg.pos_offset, flags=flags,
+                           d_in=cfg.d_in,
                            v_scale=None if v_scale is None else v_scale.data_ptr(),
                            k_norm_gain=None if k_norm_gain is None else k_norm_gain.data_ptr())
 
@@ -45,7 +46,7 @@ def run_fill(cfg, inp: dict, dev="cuda", mask="inp", canary=True, flags: int = 0
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     nfill = torch.full((1,), -1, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    rf.rf_fill_kv(desc, g["x_S"], d, m, g["A"] if P > 0 else None, g["b"] if P > 0 else None,
+    rf.rf_fill_kv(desc, g["x_S"], cfg.D_in, m, g["A"] if P > 0 else None, g["b"] if P > 0 else None,
                   Wkv if P > 0 else None, kc, vc, cfg.N * KV, KV, nfill, status, ws, ws_bytes)
     torch.cuda.synchronize()
     return {"kc": kc, "vc": vc, "kc0": kc0, "vc0": vc0, "n_fill": int(nfill.item()),

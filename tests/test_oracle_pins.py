@@ -618,3 +618,42 @@ def test_key_norm_brute_force_scalar_loops():
                     k1, k2 = kn[c], kn[c + hd // 2]
                     assert abs(K[p, r, h, c] - (k1 * math.cos(ang) - k2 * math.sin(ang))) < 1e-10
                     assert abs(K[p, r, h, c + hd // 2] - (k2 * math.cos(ang) + k1 * math.sin(ang))) < 1e-10
+
+
+# --------------------------------------------------------------------------- #
+# Non-square maps (RidgeFill review, "Ridge map": 10,240 -> 2,560 for Flash-Next)
+# --------------------------------------------------------------------------- #
+def test_stream_mean_map_reduces_to_the_square_identity_fill():
+    """x_S made of 4 identical streams of width d, A = [I I I I] / 4, b = 0: x̂ = x,
+    so the fill equals the square identity fill of x."""
+    pr = _tiny_fill_problem()
+    d, P = pr["d"], pr["P"]
+    x4 = np.concatenate([pr["x"]] * 4, axis=1)
+    A4 = np.stack([np.concatenate([np.eye(d)] * 4, axis=1) / 4.0] * P)
+    b0 = np.zeros((P, d))
+    K1, V1 = O.fill_rows(x4, pr["pos"], A4, b0, pr["g"], pr["Wk"], pr["Wv"], pr["H"], pr["hd"], 1e4, 1e-5)
+    K2, V2 = O.fill_rows(pr["x"], pr["pos"], np.stack([np.eye(d)] * P), b0, pr["g"], pr["Wk"], pr["Wv"],
+                         pr["H"], pr["hd"], 1e4, 1e-5)
+    np.testing.assert_allclose(K1, K2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(V1, V2, rtol=1e-12, atol=1e-12)
+
+
+def test_rectangular_map_brute_force():
+    rng = np.random.default_rng(17)
+    d_in, d, H, hd, P, n = 6, 4, 1, 4, 2, 2
+    x = rng.standard_normal((n, d_in))
+    A = rng.standard_normal((P, d, d_in))
+    b = rng.standard_normal((P, d))
+    g = 1.0 + 0.1 * rng.standard_normal((P, d))
+    Wk = rng.standard_normal((P, H * hd, d))
+    Wv = rng.standard_normal((P, H * hd, d))
+    pos = np.array([2, 7])
+    K, V = O.fill_rows(x, pos, A, b, g, Wk, Wv, H, hd, 1e4, 1e-5)
+    for p in range(P):
+        for r in range(n):
+            xh = [sum(A[p][o][i] * x[r][i] for i in range(d_in)) + b[p][o] for o in range(d)]
+            ms = sum(v * v for v in xh) / d
+            y = [g[p][i] * xh[i] / math.sqrt(ms + 1e-5) for i in range(d)]
+            vv = [sum(Wv[p][c][i] * y[i] for i in range(d)) for c in range(hd)]
+            for c in range(hd):
+                assert abs(V[p, r, 0, c] - vv[c]) < 1e-10
