@@ -274,8 +274,8 @@ def run_ours(args):
     cfg = workloads()[args.workload]
     inp = synth.fill_inputs(cfg, device=dev)
     n_fill, units = fill_units(cfg, inp["mask"])
-    P, d, KV = cfg.P, cfg.d, cfg.KV
-    desc = rf.rf_fill_desc(d=d, L=cfg.L, S=cfg.S, N=cfg.N, T=cfg.T, n_kv_heads=cfg.H, head_dim=cfg.hd,
+    P, d, KV, di = cfg.P, cfg.d, cfg.KV, cfg.D_in
+    desc = rf.rf_fill_desc(d=d, d_in=cfg.d_in, L=cfg.L, S=cfg.S, N=cfg.N, T=cfg.T, n_kv_heads=cfg.H, head_dim=cfg.hd,
                            rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, pos_offset=0,
                            flags=gemm_flags(args.gemm))
     Wkv = torch.empty((P, 2 * KV, d), dtype=torch.bfloat16, device=dev)
@@ -293,7 +293,7 @@ def run_ours(args):
     fold_ms = sum(ms for _, ms in rf.rf_profile_stop())
 
     def step():
-        rf.rf_fill_kv(desc, inp["x_S"], d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc, cfg.N * KV, KV,
+        rf.rf_fill_kv(desc, inp["x_S"], di, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc, cfg.N * KV, KV,
                       nfill, status, ws, ws_bytes)
 
     for _ in range(max(args.warmup, 3)):
@@ -328,7 +328,7 @@ def run_ours(args):
     stage_avg = {k: sum(v) / len(v) for k, v in stage_ms.items()}
     launches = len(prof)
 
-    map_flops = 2.0 * n_fill * P * d * d
+    map_flops = 2.0 * n_fill * P * d * di
     kv_flops = 2.0 * n_fill * P * d * 2 * KV
     fill_flops = map_flops + kv_flops
     peaks = measured_peaks()
@@ -346,7 +346,7 @@ def run_ours(args):
                                f"; timed region {t_max:.0f} ms",
                 "peak_burst": peaks["bf16_tflops"], "peak_sustained": peaks.get("bf16_tflops_sustained"),
                 "algorithmic_flops_per_launch": map_flops,
-                "algorithmic_bytes_per_launch": n_fill * d * 2 + P * d * d * 2 + n_fill * P * d * 2
+                "algorithmic_bytes_per_launch": n_fill * di * 2 + P * d * di * 2 + n_fill * P * d * 2
                 + n_fill * P * (d // 256) * 4 + P * d * 4}
 
     # End to end through the C ABI from pinned host buffers: x_S and the mask go
@@ -365,7 +365,7 @@ def run_ours(args):
             xd.copy_(xh, non_blocking=True)
             if has_mask:
                 md.copy_(mh, non_blocking=True)
-            rf.rf_fill_kv(desc, xd, d, md, inp["A"], inp["b"], Wkv, kc, vc, cfg.N * KV, KV, outd[0:1],
+            rf.rf_fill_kv(desc, xd, di, md, inp["A"], inp["b"], Wkv, kc, vc, cfg.N * KV, KV, outd[0:1],
                           outd[1:2], ws, ws_bytes)
             outh.copy_(outd, non_blocking=True)
         for _ in range(3):
@@ -548,6 +548,31 @@ def run_extras(dev, peak_tflops, flags=0):
         row[f"{key}_tflops"] = f_flops / (ms / 1e3) / 1e12
         row[f"{key}_kv_gemm_ms"] = st.get("kv_gemm")
     out["next2_key_norm_qwen3"] = row
+    del inp, kc, vc, ws, Wkv
+    torch.cuda.empty_cache()
+
+    # Non-square maps: the Flash-Next-shaped fill (10,240 -> 2,560, 24 upper layers)
+    c = synth.FLASH_NEXT
+    inp = synth.fill_inputs(c, device=dev)
+    fd = rf.rf_fill_desc(d=c.d, d_in=c.d_in, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd,
+                         rope_theta=c.rope_theta, rms_eps=c.rms_eps, pos_offset=0, flags=flags)
+    Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
+    rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
+    kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    wsb = rf.rf_fill_workspace_bytes(fd)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    nf = torch.zeros(1, dtype=torch.int32, device=dev)
+    ms, st = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d_in, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
+                                          c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
+    n_fill = int(nf.item())
+    f_flops = 2.0 * n_fill * c.P * (c.d * c.d_in + c.d * 2 * c.KV)
+    mg = st.get("map_gemm")
+    out["next4_nonsquare_flash_next"] = {
+        "workload": c.name + f", n_fill={n_fill}", "fill_ms": ms, "fill_tflops": f_flops / (ms / 1e3) / 1e12,
+        "fill_frac_of_bf16_peak": f_flops / (ms / 1e3) / 1e12 / peak_tflops,
+        "map_gemm_ms": mg, "map_gemm_tflops": 2.0 * n_fill * c.P * c.d * c.d_in / (mg / 1e3) / 1e12 if mg else None,
+        "fill_row_layers_per_s": n_fill * c.P / (ms / 1e3), "stages_ms": st}
     del inp, kc, vc, ws, Wkv
     torch.cuda.empty_cache()
 

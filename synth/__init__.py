@@ -109,7 +109,15 @@ XMODEL = XModelConfig("xmodel 40->64 layers 8x128 k8 N32768", 4, L_src=40, L_tgt
                       H=8, hd=128, N=32768, theta_src=1.0e6, theta_tgt=1.0e6,
                       calib_n=131072, lam=0.01)
 
-FILL_CONFIGS = {"toy": TOY, "llama8b": LLAMA8B, "qwen3_8b": QWEN3_8B, "dense27b": DENSE27B}
+# Non-square maps shaped like the pages' Flash-Next deployment ([RF] "Ridge map":
+# four parallel residual streams of width 2,560 read through gates, so each map is
+# 10,240 -> 2,560; split 24/48, tail 2,048, "Two numbers set the skip range"). The
+# pages give neither its KV heads nor an exact-row rate: 2 x 128 heads, none exact.
+FLASH_NEXT = FillConfig("flash-next-shaped maps d_in10240 d2560 L48 S24 N32768 T2048", 5, d=2560, L=48, S=24,
+                        N=32768, T=2048, H=2, hd=128, rope_theta=1.0e6, exact=None, lam=0.03, calib_n=0,
+                        d_in=10240)
+FILL_CONFIGS = {"toy": TOY, "llama8b": LLAMA8B, "qwen3_8b": QWEN3_8B, "dense27b": DENSE27B,
+                "flash_next": FLASH_NEXT}
 
 _TENSOR_IDS = {name: i for i, name in enumerate(
     ["x_S", "mask", "A", "b", "gain", "Wk", "Wv", "calib_X", "calib_Atrue", "calib_btrue",
@@ -214,7 +222,7 @@ def rescale_inputs(cfg: FillConfig, x_S: torch.Tensor, c: int, device="cpu") -> 
     g = _gen(device, sub_seed(cfg.index, "rescale_scale"))
     half = torch.cat([torch.full((d // 2,), 0.5), torch.full((d - d // 2,), 1.5)]).to(device)
     s = half.view(1, 1, d) * (0.9 + 0.2 * torch.rand((P, 1, d), generator=g, device=device, dtype=torch.float32))
-    tail = x_S[cfg.N - cfg.T: cfg.N - cfg.T + c].to(device).float()
+    tail = x_S[cfg.N - cfg.T: cfg.N - cfg.T + c, :d].to(device).float()   # first d channels if d_in > d
     noise = _randn((P, c, d), sub_seed(cfg.index, "rescale_noise"), device, std=0.1, dtype=torch.float32)
     return (s * tail[None] + noise).to(torch.bfloat16)
 

@@ -157,3 +157,38 @@ def test_fill_with_key_norm_qwen3_shape_sampled():
     assert res["n_fill"] == len(idx)
     assert_bookkeeping(cfg, res, mnp)
     assert_values(cfg, inp, res, _sample_rows(idx, mnp, cfg.N - cfg.T), k_norm_gain=kg)
+
+
+# --------------------------------------------------------------------------- #
+# Non-square maps: x_S and the map input are d_in wide, x̂ and the projections d
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("cfg", [
+    _small("d_in 1024 -> d 256 (4 streams)", d=256, d_in=1024, L=4, S=2, N=300, T=20, H=2, hd=64),
+    _small("d_in 768 -> d 512, hd128, ragged", d=512, d_in=768),
+], ids=lambda c: c.name)
+@KERNELS
+def test_fill_with_non_square_maps_matches_oracle(cfg, flags):
+    inp = synth.fill_inputs(cfg)
+    assert inp["x_S"].shape[1] == cfg.d_in and inp["A"].shape[1:] == (cfg.d, cfg.d_in)
+    res = run_fill(cfg, inp, flags=flags)
+    assert res["status"] == 0
+    mnp = _mask_np(inp)
+    idx = O.prefix_partition(cfg.N, cfg.T, mnp)
+    assert res["n_fill"] == len(idx)
+    assert_bookkeeping(cfg, res, mnp)
+    assert_values(cfg, inp, res, idx)
+
+
+@pytest.mark.slow
+def test_fill_flash_next_shaped_maps_sampled():
+    """Flash-Next-shaped maps: 24 upper layers of 10,240 -> 2,560, N = 32,768,
+    T = 2,048 (KV heads 2 x 128: the pages do not give them)."""
+    cfg = synth.FILL_CONFIGS["flash_next"]
+    inp = synth.fill_inputs(cfg, device="cuda")
+    res = run_fill(cfg, inp)
+    assert res["status"] == 0
+    mnp = _mask_np(inp)
+    idx = O.prefix_partition(cfg.N, cfg.T, mnp)
+    assert res["n_fill"] == len(idx)
+    assert_bookkeeping(cfg, res, mnp)
+    assert_values(cfg, inp, res, _sample_rows(idx, mnp, cfg.N - cfg.T))

@@ -42,7 +42,7 @@ def _gpu_scale(cfg, inp, x_exact, c, flags=0):
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     wsb = rf.rf_value_scale_workspace_bytes(desc, c)
     ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
-    rf.rf_value_scale(desc, c, g["x_S"], cfg.d, x_exact.to(DEV), cfg.d, g["A"], g["b"], Wkv, vs, status, ws, wsb)
+    rf.rf_value_scale(desc, c, g["x_S"], cfg.D_in, x_exact.to(DEV), cfg.d, g["A"], g["b"], Wkv, vs, status, ws, wsb)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return vs
@@ -75,6 +75,7 @@ def _assert_scales(got, ref):
     (_small("hd128 2 heads, c = T (300 rows, 2 M-tiles)"), 300),
     (_small("hd64 2 heads (KV = 128), c = 1", hd=64), 1),
     (_small("hd64 4 heads, 4 layers, c = 37", d=768, L=6, S=2, H=4, hd=64, T=37), 37),
+    (_small("non-square maps d_in 1024 -> d 512, c = 100", d_in=1024), 100),
 ], ids=lambda x: x.name if hasattr(x, "name") else str(x))
 @KERNELS
 def test_value_scale_matches_oracle(cfg, c, flags):
