@@ -40,6 +40,11 @@ Readings where the pages leave a step open (each is listed in the design doc):
     each key head over its hd values, k_h <- g_k * k_h / sqrt(mean(k_h^2) + eps)
     with one gain vector g_k of length hd per layer and the layer's eps, applied
     after the K projection and before RoPE.
+  * int8 maps ([RF] "Ridge map": 27B's 48 maps "in int8 total 1.2 GiB"; the scheme
+    is unstated): symmetric per output row, s[o] = max_i |A[o][i]| / 127 and
+    q[o][i] = rint(A[o][i] / s[o]) (round half to even), both in float32 (the
+    precision that decides the integers); a zero row has s = 0, q = 0. The map
+    used is then A'[o][i] = s[o] q[o][i].
 
 Parity status: every public function here is pinned by tests/test_oracle_pins.py
 against closed forms, invariants, textbook routines or brute force; none is
@@ -53,7 +58,7 @@ __all__ = [
     "bf16_bits_to_f64", "rope_inv_freq", "rope", "rms_norm", "prefix_partition",
     "map_predict", "fill_rows", "fill_kv", "calib_stats", "centre_stats",
     "ridge_alpha", "ridge_solve", "xmodel_features", "xmodel_map_layer",
-    "fill_flops_per_row_layer", "value_scale",
+    "fill_flops_per_row_layer", "value_scale", "quantize_rows_int8", "dequantize_rows_int8",
 ]
 
 
@@ -218,6 +223,24 @@ def value_scale(x_S_tail, x_exact_tail, A, b, gain, Wv, n_kv_heads, head_dim, rm
             if ok.any():
                 out[p, h] = np.mean(n_exact[ok, h] / n_pred[ok, h])
     return out
+
+
+def quantize_rows_int8(A):
+    """Symmetric per-row int8 code of maps A [..., d_out, d_in] (see the module
+    header): returns (q int8 [..., d_out, d_in], s float32 [..., d_out]). The
+    scale and the rounding decisions are taken in float32."""
+    a = np.asarray(A, np.float32)
+    amax = np.max(np.abs(a), axis=-1)
+    s = (amax / np.float32(127.0)).astype(np.float32)
+    safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    q = np.rint((a / safe[..., None]).astype(np.float32))
+    q = np.where(s[..., None] > 0, q, np.float32(0.0))
+    return np.clip(q, -127, 127).astype(np.int8), s
+
+
+def dequantize_rows_int8(q, s) -> np.ndarray:
+    """A'[o][i] = s[o] q[o][i] in float64."""
+    return np.asarray(s, np.float64)[..., None] * np.asarray(q, np.float64)
 
 
 def fill_flops_per_row_layer(d: int, n_kv_heads: int, head_dim: int) -> int:

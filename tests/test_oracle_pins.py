@@ -657,3 +657,34 @@ def test_rectangular_map_brute_force():
             vv = [sum(Wv[p][c][i] * y[i] for i in range(d)) for c in range(hd)]
             for c in range(hd):
                 assert abs(V[p, r, 0, c] - vv[c]) < 1e-10
+
+
+# --------------------------------------------------------------------------- #
+# int8 maps (symmetric per output row)
+# --------------------------------------------------------------------------- #
+def test_int8_rows_hit_full_range_and_the_rounding_bound():
+    rng = np.random.default_rng(23)
+    A = (rng.standard_normal((3, 16, 40)) * rng.uniform(0.01, 3.0, size=(3, 16, 1))).astype(np.float32)
+    q, s = O.quantize_rows_int8(A)
+    assert q.dtype == np.int8 and s.dtype == np.float32
+    assert np.all(np.abs(q.astype(int)).max(axis=-1) == 127)            # every row uses the full range
+    err = np.abs(A.astype(np.float64) - O.dequantize_rows_int8(q, s))
+    assert np.all(err <= 0.5 * s.astype(np.float64)[..., None] * (1 + 1e-6))   # half a step, up to fp32 division
+    # exact for rows that are integers times a power of two
+    B = np.zeros((1, 2, 8), np.float32)
+    B[0, 0] = np.arange(-3, 5) * 0.25
+    B[0, 1] = np.array([127, -127, 0, 1, -1, 64, 2, 3]) * 2.0 ** -5
+    qb, sb = O.quantize_rows_int8(B)
+    np.testing.assert_array_equal(O.dequantize_rows_int8(qb, sb)[0, 1], B[0, 1].astype(np.float64))
+
+
+def test_int8_zero_row_power_of_two_scaling_and_half_even_ties():
+    A = np.zeros((2, 4), np.float32)
+    A[1] = [127.0, 0.5, 1.5, -2.5]                 # s = 1: ties at .5 go to the even neighbour
+    q, s = O.quantize_rows_int8(A)
+    np.testing.assert_array_equal(s, [0.0, 1.0])
+    np.testing.assert_array_equal(q[0], 0)
+    np.testing.assert_array_equal(q[1], [127, 0, 2, -2])
+    q2, s2 = O.quantize_rows_int8(A * np.float32(8.0))
+    np.testing.assert_array_equal(q2, q)
+    np.testing.assert_array_equal(s2, s * 8)
