@@ -89,7 +89,9 @@ enum rf_stage {
   RF_STAGE_SOLVE = 9,        /* kernels of the ridge solve                     */
   RF_STAGE_UNROPE = 10,      /* RoPE / inverse RoPE on cache rows              */
   RF_STAGE_XMODEL_GEMM = 11, /* cross-model mapper GEMM                        */
-  RF_STAGE_RESCALE = 12      /* value rescale: value norms and their ratios   */
+  RF_STAGE_RESCALE = 12,     /* value rescale: value norms and their ratios   */
+  RF_STAGE_EXPAND = 13,      /* int8 map codes -> bf16 before a layer's GEMM   */
+  RF_STAGE_QUANTIZE = 14     /* bf16 maps -> int8 codes and row scales         */
 };
 rf_status rf_profile_start(int max_records);
 /* Diagnostic: runs the tensor-core GEMM kernel (cta_pair != 0: the CTA-pair
@@ -234,6 +236,50 @@ rf_status rf_value_scale(const rf_fill_desc* desc, int64_t c,
                          const rf_bf16* A, const float* b, const rf_bf16* Wkv,
                          float* v_scale, int32_t* dev_status,
                          void* workspace, size_t workspace_bytes, rf_stream_t stream);
+
+/* ===================================================================== *
+ * Map storage ([RF] "Ridge map": the 27B maps "in int8 total 1.2 GiB"; "maps can
+ * be kept resident in GPU memory or streamed from host memory one layer at a time")
+ * ===================================================================== */
+/* int8 code of the maps, symmetric per output row (the pages give no scheme):
+ *   s[p][o] = max_i |A[p][o][i]| / 127,  q[p][o][i] = rint(A[p][o][i] / s[p][o])
+ * (ties to even; both in fp32; a zero row gives s = 0 and q = 0), so that
+ * A[p][o][i] ≈ s[p][o] q[p][o][i]. A [P][d][d_in] bf16, q [P][d][d_in] int8,
+ * s [P][d] fp32, all device. */
+rf_status rf_quantize_maps_int8(const rf_fill_desc* desc, const rf_bf16* A, int8_t* q, float* s,
+                                rf_stream_t stream);
+
+#define RF_MAPS_BF16 0 /* A is [P][d][d_in] bf16                                   */
+#define RF_MAPS_INT8 1 /* A is q [P][d][d_in] int8 with row_scale s [P][d] fp32    */
+typedef struct rf_map_source {
+  int32_t kind;           /* RF_MAPS_BF16 or RF_MAPS_INT8                               */
+  int32_t on_host;        /* nonzero: A is in host memory. Page-locked memory lets the */
+                          /* copy of layer p+1 overlap the GEMMs of layer p; pageable  */
+                          /* memory works but its copies may block the calling thread. */
+  const void* A;          /* the maps, layer after layer (p = 0 .. P-1)                 */
+  const float* row_scale; /* RF_MAPS_INT8: [P][d] fp32 on the device; else unused       */
+} rf_map_source;
+
+/* The fill of rf_fill_kv, one layer at a time: for p = 0 .. P-1 the map GEMM of
+ * layer S+p and then its K/V GEMM, so x̂ exists for one layer only (workspace
+ * M_pad*d instead of P*M_pad*d bf16). Maps on the host or in int8 pass through a
+ * two-slot bf16 ring in the workspace: the library's copy stream copies layer
+ * p+1 (and expands int8 codes to bf16, exact for |q| <= 127) while the caller's
+ * stream computes layer p; int8 row scales are applied to the map GEMM's output
+ * columns with the bias. Device bf16 maps are read in place. The results equal
+ * rf_fill_kv's bit for bit when the maps are the same bf16 values (same kernels,
+ * same summation order). Arguments as for rf_fill_kv, with `maps` replacing A;
+ * the workspace is rf_fill_layered_workspace_bytes(desc, maps). Everything is
+ * asynchronous on `stream`. */
+size_t rf_fill_layered_workspace_bytes(const rf_fill_desc* desc, const rf_map_source* maps);
+rf_status rf_fill_kv_layered(const rf_fill_desc* desc,
+                             const rf_bf16* x_S, int64_t ld_x,
+                             const uint8_t* exact_mask,
+                             const rf_map_source* maps, const float* b, const rf_bf16* Wkv,
+                             rf_bf16* k_cache, rf_bf16* v_cache,
+                             int64_t layer_stride, int64_t row_stride,
+                             int32_t* n_fill_out, int32_t* dev_status,
+                             void* workspace, size_t workspace_bytes, rf_stream_t stream);
 
 /* ===================================================================== *
  * Calibration statistics ([RF] "Ridge map": only XᵀX, XᵀY_l and the two means

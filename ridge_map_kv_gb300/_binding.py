@@ -37,6 +37,14 @@ RF_FLAG_SINGLE_CTA = 1
 RF_FLAG_CTA_PAIR = 2
 
 
+RF_MAPS_BF16 = 0
+RF_MAPS_INT8 = 1
+
+
+class rf_map_source(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("on_host", ctypes.c_int32), ("A", c_void_p), ("row_scale", c_void_p)]
+
+
 class rf_fill_desc(ctypes.Structure):
     _fields_ = [("d", c_int64), ("L", c_int64), ("S", c_int64), ("N", c_int64), ("T", c_int64),
                 ("n_kv_heads", c_int64), ("head_dim", c_int64), ("rope_theta", c_double),
@@ -75,6 +83,11 @@ _SIGS = {
     "rf_fill_kv_static": (c_int, [POINTER(rf_fill_desc), c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p]),
     "rf_selftest_wait_timeout": (c_int, [c_int, c_void_p, c_void_p]),
+    "rf_quantize_maps_int8": (c_int, [POINTER(rf_fill_desc), c_void_p, c_void_p, c_void_p, c_void_p]),
+    "rf_fill_layered_workspace_bytes": (c_size_t, [POINTER(rf_fill_desc), POINTER(rf_map_source)]),
+    "rf_fill_kv_layered": (c_int, [POINTER(rf_fill_desc), c_void_p, c_int64, c_void_p, POINTER(rf_map_source),
+                                   c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p,
+                                   c_void_p, c_size_t, c_void_p]),
     "rf_value_scale_workspace_bytes": (c_size_t, [POINTER(rf_fill_desc), c_int64]),
     "rf_value_scale": (c_int, [POINTER(rf_fill_desc), c_int64, c_void_p, c_int64, c_void_p, c_int64, c_void_p,
                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -207,6 +220,29 @@ def rf_selftest_wait_timeout(cta_pair, dev_status, stream=None):
     """Runs the GEMM core on a problem whose copies never arrive: *dev_status becomes
     RF_ERR_TIMEOUT after the wait limit (see include/rf.h)."""
     _check(lib().rf_selftest_wait_timeout(int(bool(cta_pair)), _p(dev_status), _s(stream)), "rf_selftest_wait_timeout")
+
+
+def rf_quantize_maps_int8(desc, A, q, s, stream=None):
+    """Symmetric per-row int8 code of the maps: q [P][d][d_in] int8, s [P][d] fp32."""
+    _check(lib().rf_quantize_maps_int8(ctypes.byref(desc), _p(A), _p(q), _p(s), _s(stream)), "rf_quantize_maps_int8")
+
+
+def map_source(kind, A, on_host=False, row_scale=None) -> rf_map_source:
+    """rf_map_source for maps A (a device or host tensor, or an address)."""
+    return rf_map_source(int(kind), int(bool(on_host)), _p(A), _p(row_scale))
+
+
+def rf_fill_layered_workspace_bytes(desc, maps) -> int:
+    return int(lib().rf_fill_layered_workspace_bytes(ctypes.byref(desc), ctypes.byref(maps)))
+
+
+def rf_fill_kv_layered(desc, x_S, ld_x, exact_mask, maps, b, Wkv, k_cache, v_cache, layer_stride, row_stride,
+                       n_fill_out=None, dev_status=None, workspace=None, workspace_bytes=0, stream=None):
+    """rf_fill_kv one layer at a time, maps from the device or the host, bf16 or int8 (see include/rf.h)."""
+    _check(lib().rf_fill_kv_layered(ctypes.byref(desc), _p(x_S), int(ld_x), _p(exact_mask), ctypes.byref(maps),
+                                    _p(b), _p(Wkv), _p(k_cache), _p(v_cache), int(layer_stride), int(row_stride),
+                                    _p(n_fill_out), _p(dev_status), _p(workspace), int(workspace_bytes),
+                                    _s(stream)), "rf_fill_kv_layered")
 
 
 def rf_value_scale_workspace_bytes(desc: rf_fill_desc, c: int) -> int:

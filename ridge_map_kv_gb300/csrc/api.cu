@@ -232,6 +232,8 @@ const char* rf_stage_name(int s) {
     case RF_STAGE_UNROPE: return "unrope";
     case RF_STAGE_XMODEL_GEMM: return "xmodel_gemm";
     case RF_STAGE_RESCALE: return "value_rescale";
+    case RF_STAGE_EXPAND: return "int8_expand";
+    case RF_STAGE_QUANTIZE: return "int8_quantize";
     default: return "unknown";
   }
 }

@@ -148,12 +148,17 @@ struct FillLayout {
   int32_t* fill_idx;
   int32_t* n_fill;
   __nv_bfloat16* xf;
-  __nv_bfloat16* xhat;
+  __nv_bfloat16* xhat;      // [P][M_pad][d], or one layer in the layered fill
   float* ssp;
   float* rope_cos;
   float* rope_sin;
+  __nv_bfloat16* slot[2];   // layered fill: bf16 map ring (when maps are copied or expanded)
+  int8_t* stage[2];         // layered fill: int8 landing slots for host int8 maps
   size_t bytes;
 };
+
+// Maps the layered fill reads in place (device bf16) need no ring.
+static bool maps_staged(const rf_map_source* m) { return !(m->kind == RF_MAPS_BF16 && !m->on_host); }
 
 // Width of x_S rows and of the maps' input (d_in = 0 means square maps).
 static int64_t fill_din(const rf_fill_desc* d) { return d->d_in > 0 ? d->d_in : d->d; }
@@ -177,70 +182,46 @@ static rf_status check_fill_desc(const rf_fill_desc* d) {
   return RF_OK;
 }
 
-static FillLayout fill_layout(const rf_fill_desc* d, void* ws) {
+// Workspace of the fill (maps == nullptr) or of the layered fill (x̂ for one
+// layer at a time, plus the map ring).
+static FillLayout fill_layout(const rf_fill_desc* d, void* ws, const rf_map_source* maps = nullptr) {
   const int64_t n_prefix = d->N - d->T;
   const int64_t M_pad = round_up(std::max<int64_t>(n_prefix, 1), kFillRowAlign);
   const int64_t P = d->L - d->S;
+  const int64_t xhat_layers = maps != nullptr ? std::min<int64_t>(P, 1) : P;
   Carve c(ws);
-  FillLayout l;
+  FillLayout l{};
   l.fill_idx = c.take<int32_t>(std::max<int64_t>(n_prefix, 1));
   l.n_fill = c.take<int32_t>(1);
   l.xf = c.take<__nv_bfloat16>(M_pad * fill_din(d));
-  l.xhat = c.take<__nv_bfloat16>(P * M_pad * d->d);
-  l.ssp = c.take<float>(P * (d->d / kBN) * M_pad);
+  l.xhat = c.take<__nv_bfloat16>(xhat_layers * M_pad * d->d);
+  l.ssp = c.take<float>(xhat_layers * (d->d / kBN) * M_pad);
   l.rope_cos = c.take<float>(std::max<int64_t>(n_prefix, 1) * (d->head_dim / 2));
   l.rope_sin = c.take<float>(std::max<int64_t>(n_prefix, 1) * (d->head_dim / 2));
+  if (maps != nullptr && maps_staged(maps)) {
+    const int64_t n = d->d * fill_din(d);
+    for (int i = 0; i < 2; ++i) l.slot[i] = c.take<__nv_bfloat16>(n);
+    if (maps->kind == RF_MAPS_INT8 && maps->on_host)
+      for (int i = 0; i < 2; ++i) l.stage[i] = c.take<int8_t>(n);
+  }
   l.bytes = c.bytes();
   return l;
 }
 
-// The two fill GEMMs, on CTA pairs (kPair) or single CTAs.
-template <bool kPair>
-rf_status fill_gemms(const rf_fill_desc* desc, const FillLayout& lay, const rf_bf16* A, const float* b,
-                     const rf_bf16* Wkv, rf_bf16* k_cache, rf_bf16* v_cache, int64_t layer_stride, int64_t row_stride,
-                     int32_t* dev_status, int sms, cudaStream_t s) {
-  using Cfg = GemmCfg<kPair>;
+// The two fill GEMMs, on CTA pairs or single CTAs.
+static rf_status fill_gemms(bool pair, const rf_fill_desc* desc, const FillLayout& lay, const rf_bf16* A,
+                            const float* b, const rf_bf16* Wkv, rf_bf16* k_cache, rf_bf16* v_cache,
+                            int64_t layer_stride, int64_t row_stride, int32_t* dev_status, int sms, cudaStream_t s) {
   rf_status st;
   const int64_t d = desc->d, P = desc->L - desc->S, KV = desc->n_kv_heads * desc->head_dim;
   const int64_t M_pad = round_up(desc->N - desc->T, kFillRowAlign);
-  const int64_t m_tiles_max = M_pad / Cfg::kUnitM;
-  const uint64_t tmo = wait_timeout_ns();
-  {
-    const int64_t d_in = fill_din(desc);
-    MapGemmArgs ma{lay.xf, d_in, M_pad, lay.n_fill, A, b, lay.xhat, lay.ssp, d, d_in, P, M_pad, dev_status};
-    if ((st = map_gemm(kPair, ma, sms, s)) != RF_OK) return st;
-  }
-  {
-    KVProb<kPair> pr;
-    if ((st = make_tmap_bf16_2d(&pr.tmA, lay.xhat, d, P * M_pad, d, kBK, kBM)) != RF_OK) return st;
-    if ((st = make_tmap_bf16_2d(&pr.tmB, Wkv, d, P * 2 * KV, d, kBK, Cfg::kBRows)) != RF_OK) return st;
-    pr.n_fill = lay.n_fill;
-    pr.fill_idx = lay.fill_idx;
-    pr.ssp = lay.ssp;
-    pr.rope_cos = lay.rope_cos;
-    pr.rope_sin = lay.rope_sin;
-    pr.kc = reinterpret_cast<__nv_bfloat16*>(k_cache);
-    pr.vc = reinterpret_cast<__nv_bfloat16*>(v_cache);
-    pr.v_scale = desc->v_scale;
-    pr.k_gain = reinterpret_cast<const __nv_bfloat16*>(desc->k_norm_gain);
-    pr.layer_stride = layer_stride;
-    pr.row_stride = row_stride;
-    pr.d = static_cast<int>(d);
-    pr.P = static_cast<int>(P);
-    pr.S = static_cast<int>(desc->S);
-    pr.M_pad = static_cast<int>(M_pad);
-    pr.KV = static_cast<int>(KV);
-    pr.hd = static_cast<int>(desc->head_dim);
-    pr.n_ntiles = static_cast<int>(2 * KV / kBN);
-    pr.n_ss = static_cast<int>(d / kBN);
-    pr.inv_d = 1.0f / static_cast<float>(d);
-    pr.eps = static_cast<float>(desc->rms_eps);
-    pr.dev_status = dev_status;
-    pr.timeout_ns = tmo;
-    ProfScope prof(s, RF_STAGE_KV_GEMM);
-    if ((st = launch_gemm(pr, P * m_tiles_max * pr.n_ntiles, sms, s, "K/V GEMM launch")) != RF_OK) return st;
-  }
-  return RF_OK;
+  const int64_t d_in = fill_din(desc);
+  MapGemmArgs ma{lay.xf, d_in, M_pad, lay.n_fill, A, b, nullptr, lay.xhat, lay.ssp, d, d_in, P, M_pad, dev_status};
+  if ((st = map_gemm(pair, ma, sms, s)) != RF_OK) return st;
+  KvGemmArgs ka{lay.xhat, lay.ssp, lay.n_fill, lay.fill_idx, lay.rope_cos, lay.rope_sin, Wkv, k_cache, v_cache,
+                desc->v_scale, desc->k_norm_gain, layer_stride, row_stride, d, P, desc->S, M_pad, KV,
+                desc->head_dim, desc->rms_eps, dev_status};
+  return kv_gemm(pair, ka, sms, s);
 }
 
 template <bool kPair>
@@ -253,6 +234,7 @@ static rf_status map_gemm_t(const MapGemmArgs& a, int sms, cudaStream_t s) {
   const int64_t m_tiles_max = a.M_pad / Cfg::kUnitM;
   pr.n_fill = a.n_rows;
   pr.bias = a.b;
+  pr.col_scale = a.col_scale;
   pr.xhat = a.xhat;
   pr.ssp = a.ssp;
   pr.d = static_cast<int>(a.d);
@@ -270,6 +252,45 @@ static rf_status map_gemm_t(const MapGemmArgs& a, int sms, cudaStream_t s) {
 
 rf_status map_gemm(bool pair, const MapGemmArgs& a, int sms, cudaStream_t s) {
   return pair ? map_gemm_t<true>(a, sms, s) : map_gemm_t<false>(a, sms, s);
+}
+
+template <bool kPair>
+static rf_status kv_gemm_t(const KvGemmArgs& a, int sms, cudaStream_t s) {
+  using Cfg = GemmCfg<kPair>;
+  rf_status st;
+  KVProb<kPair> pr;
+  if ((st = make_tmap_bf16_2d(&pr.tmA, a.xhat, a.d, a.P * a.M_pad, a.d, kBK, kBM)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmB, a.Wkv, a.d, a.P * 2 * a.KV, a.d, kBK, Cfg::kBRows)) != RF_OK) return st;
+  pr.n_fill = a.n_fill;
+  pr.fill_idx = a.fill_idx;
+  pr.ssp = a.ssp;
+  pr.rope_cos = a.rope_cos;
+  pr.rope_sin = a.rope_sin;
+  pr.kc = static_cast<__nv_bfloat16*>(a.k_cache);
+  pr.vc = static_cast<__nv_bfloat16*>(a.v_cache);
+  pr.v_scale = a.v_scale;
+  pr.k_gain = static_cast<const __nv_bfloat16*>(a.k_gain);
+  pr.layer_stride = a.layer_stride;
+  pr.row_stride = a.row_stride;
+  pr.d = static_cast<int>(a.d);
+  pr.P = static_cast<int>(a.P);
+  pr.S = static_cast<int>(a.S);
+  pr.M_pad = static_cast<int>(a.M_pad);
+  pr.KV = static_cast<int>(a.KV);
+  pr.hd = static_cast<int>(a.hd);
+  pr.n_ntiles = static_cast<int>(2 * a.KV / kBN);
+  pr.n_ss = static_cast<int>(a.d / kBN);
+  pr.inv_d = 1.0f / static_cast<float>(a.d);
+  pr.eps = static_cast<float>(a.eps);
+  pr.dev_status = a.dev_status;
+  pr.timeout_ns = wait_timeout_ns();
+  const int64_t m_tiles_max = a.M_pad / Cfg::kUnitM;
+  ProfScope prof(s, RF_STAGE_KV_GEMM);
+  return launch_gemm(pr, a.P * m_tiles_max * pr.n_ntiles, sms, s, "K/V GEMM launch");
+}
+
+rf_status kv_gemm(bool pair, const KvGemmArgs& a, int sms, cudaStream_t s) {
+  return pair ? kv_gemm_t<true>(a, sms, s) : kv_gemm_t<false>(a, sms, s);
 }
 
 }  // namespace rf
@@ -304,50 +325,45 @@ extern "C" rf_status rf_fold_kv_weights(const rf_fill_desc* desc, const rf_bf16*
   return cuda_check(cudaGetLastError(), "k_fold_gain launch");
 }
 
-extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, int64_t ld_x, const uint8_t* exact_mask,
-                                const rf_bf16* A, const float* b, const rf_bf16* Wkv, rf_bf16* k_cache,
-                                rf_bf16* v_cache, int64_t layer_stride, int64_t row_stride, int32_t* n_fill_out,
-                                int32_t* dev_status, void* workspace, size_t workspace_bytes, rf_stream_t stream) {
-  clear_error();
-  rf_status st = check_fill_desc(desc);
-  if (st != RF_OK) return st;
+// Argument checks shared by rf_fill_kv and rf_fill_kv_layered (the maps are
+// checked by the caller).
+static rf_status check_fill_args(const rf_fill_desc* desc, const rf_bf16* x_S, int64_t ld_x, const float* b,
+                                 const rf_bf16* Wkv, const rf_bf16* k_cache, const rf_bf16* v_cache,
+                                 int64_t layer_stride, int64_t row_stride) {
   const int64_t n_prefix = desc->N - desc->T;
   const int64_t P = desc->L - desc->S;
   const int64_t KV = desc->n_kv_heads * desc->head_dim;
-  const int64_t d = desc->d;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool any = n_prefix > 0 && P > 0;
-  if (n_prefix > 0) {
-    if (!x_S && any) return fail(RF_ERR_INVALID_ARG, "x_S is NULL");
-  }
-  if (any) {
-    if (!A || !b || !Wkv || !k_cache || !v_cache) return fail(RF_ERR_INVALID_ARG, "A, b, Wkv, k_cache, v_cache must be non-NULL");
-    if (!aligned16(x_S) || !aligned16(A) || !aligned16(b) || !aligned16(Wkv) || !aligned16(k_cache) || !aligned16(v_cache))
+  if (n_prefix > 0 && P > 0) {
+    if (!x_S) return fail(RF_ERR_INVALID_ARG, "x_S is NULL");
+    if (!b || !Wkv || !k_cache || !v_cache) return fail(RF_ERR_INVALID_ARG, "A, b, Wkv, k_cache, v_cache must be non-NULL");
+    if (!aligned16(x_S) || !aligned16(b) || !aligned16(Wkv) || !aligned16(k_cache) || !aligned16(v_cache))
       return fail(RF_ERR_ALIGN, "x_S, A, b, Wkv and the caches must be 16-byte aligned");
     if (ld_x < fill_din(desc) || ld_x % 8 != 0)
       return fail(RF_ERR_ALIGN, "ld_x must be >= d_in (d for square maps) and a multiple of 8");
     if (row_stride < KV || row_stride % 8 != 0 || layer_stride < 0 || layer_stride % 8 != 0)
       return fail(RF_ERR_ALIGN, "row_stride must be >= H*hd and a multiple of 8; layer_stride a multiple of 8");
   }
-  FillLayout lay = fill_layout(desc, workspace);
-  if (n_prefix > 0) {
-    if (workspace == nullptr || workspace_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-      return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", lay.bytes, workspace_bytes);
-  }
-  int sms = 0;
-  if ((st = current_device(&sms)) != RF_OK) return st;
+  return RF_OK;
+}
 
+// Row compaction, and when anything is filled the gather and the RoPE table, on
+// stream s. *work is false when there is nothing left to fill.
+static rf_status fill_prologue(const rf_fill_desc* desc, const rf_bf16* x_S, int64_t ld_x, const uint8_t* exact_mask,
+                               int32_t* n_fill_out, const FillLayout& lay, int sms, cudaStream_t s, bool* work) {
+  *work = false;
+  const int64_t n_prefix = desc->N - desc->T;
+  const int64_t P = desc->L - desc->S;
   if (n_prefix == 0) {
     if (n_fill_out) return cuda_check(cudaMemsetAsync(n_fill_out, 0, sizeof(int32_t), s), "memset n_fill_out");
     return RF_OK;
   }
+  rf_status st;
   {
     ProfScope prof(s, RF_STAGE_COMPACT);
     k_compact<<<1, 1024, 0, s>>>(exact_mask, static_cast<int>(n_prefix), lay.fill_idx, lay.n_fill, n_fill_out);
   }
   if ((st = cuda_check(cudaGetLastError(), "k_compact launch")) != RF_OK) return st;
   if (P == 0) return RF_OK;
-
   const int64_t M_pad = round_up(n_prefix, kFillRowAlign);
   {
     ProfScope prof(s, RF_STAGE_GATHER);
@@ -364,8 +380,146 @@ extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, in
                                              desc->rope_theta, static_cast<long long>(desc->pos_offset));
   }
   if ((st = cuda_check(cudaGetLastError(), "gather / rope launch")) != RF_OK) return st;
+  *work = true;
+  return RF_OK;
+}
 
-  if (use_pair(desc->flags, true))
-    return fill_gemms<true>(desc, lay, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride, dev_status, sms, s);
-  return fill_gemms<false>(desc, lay, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride, dev_status, sms, s);
+extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, int64_t ld_x, const uint8_t* exact_mask,
+                                const rf_bf16* A, const float* b, const rf_bf16* Wkv, rf_bf16* k_cache,
+                                rf_bf16* v_cache, int64_t layer_stride, int64_t row_stride, int32_t* n_fill_out,
+                                int32_t* dev_status, void* workspace, size_t workspace_bytes, rf_stream_t stream) {
+  clear_error();
+  rf_status st = check_fill_desc(desc);
+  if (st != RF_OK) return st;
+  if ((st = check_fill_args(desc, x_S, ld_x, b, Wkv, k_cache, v_cache, layer_stride, row_stride)) != RF_OK) return st;
+  const int64_t n_prefix = desc->N - desc->T;
+  if (n_prefix > 0 && desc->L > desc->S) {
+    if (!A) return fail(RF_ERR_INVALID_ARG, "A, b, Wkv, k_cache, v_cache must be non-NULL");
+    if (!aligned16(A)) return fail(RF_ERR_ALIGN, "x_S, A, b, Wkv and the caches must be 16-byte aligned");
+  }
+  FillLayout lay = fill_layout(desc, workspace);
+  if (n_prefix > 0) {
+    if (workspace == nullptr || workspace_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", lay.bytes, workspace_bytes);
+  }
+  int sms = 0;
+  if ((st = current_device(&sms)) != RF_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool work = false;
+  if ((st = fill_prologue(desc, x_S, ld_x, exact_mask, n_fill_out, lay, sms, s, &work)) != RF_OK || !work) return st;
+  return fill_gemms(use_pair(desc->flags, true), desc, lay, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride,
+                    dev_status, sms, s);
+}
+
+// --------------------------------------------------------------------------
+// Layer-by-layer fill (rf_fill_kv_layered): one map GEMM and one K/V GEMM per
+// layer, x̂ for one layer at a time. Maps that live on the host or in int8 pass
+// through a two-slot bf16 ring: the library's copy stream copies (and expands)
+// layer p+1 while the caller's stream computes layer p; events order slot reuse.
+// --------------------------------------------------------------------------
+struct EventSet {
+  cudaEvent_t e[5] = {};
+  int n = 0;
+  ~EventSet() {
+    for (int i = 0; i < n; ++i) cudaEventDestroy(e[i]);
+  }
+  rf_status create() {
+    for (; n < 5; ++n) {
+      cudaError_t err = cudaEventCreateWithFlags(&e[n], cudaEventDisableTiming);
+      if (err != cudaSuccess) return cuda_check(err, "cudaEventCreateWithFlags");
+    }
+    return RF_OK;
+  }
+};
+
+static rf_status check_maps(const rf_map_source* m) {
+  if (m == nullptr) return fail(RF_ERR_INVALID_ARG, "maps is NULL");
+  if (m->kind != RF_MAPS_BF16 && m->kind != RF_MAPS_INT8)
+    return fail(RF_ERR_INVALID_ARG, "maps->kind must be RF_MAPS_BF16 or RF_MAPS_INT8");
+  return RF_OK;
+}
+
+extern "C" size_t rf_fill_layered_workspace_bytes(const rf_fill_desc* desc, const rf_map_source* maps) {
+  if (check_fill_desc(desc) != RF_OK || check_maps(maps) != RF_OK) return 0;
+  return fill_layout(desc, nullptr, maps).bytes;
+}
+
+extern "C" rf_status rf_fill_kv_layered(const rf_fill_desc* desc, const rf_bf16* x_S, int64_t ld_x,
+                                        const uint8_t* exact_mask, const rf_map_source* maps, const float* b,
+                                        const rf_bf16* Wkv, rf_bf16* k_cache, rf_bf16* v_cache, int64_t layer_stride,
+                                        int64_t row_stride, int32_t* n_fill_out, int32_t* dev_status, void* workspace,
+                                        size_t workspace_bytes, rf_stream_t stream) {
+  clear_error();
+  rf_status st = check_fill_desc(desc);
+  if (st != RF_OK) return st;
+  if ((st = check_maps(maps)) != RF_OK) return st;
+  if ((st = check_fill_args(desc, x_S, ld_x, b, Wkv, k_cache, v_cache, layer_stride, row_stride)) != RF_OK) return st;
+  const int64_t n_prefix = desc->N - desc->T;
+  const int64_t P = desc->L - desc->S, d = desc->d, d_in = fill_din(desc), KV = desc->n_kv_heads * desc->head_dim;
+  const bool int8 = maps->kind == RF_MAPS_INT8;
+  if (n_prefix > 0 && P > 0) {
+    if (!maps->A || (int8 && !maps->row_scale))
+      return fail(RF_ERR_INVALID_ARG, "maps->A (and maps->row_scale for int8 maps) must be non-NULL");
+    if (!aligned16(maps->A) || (int8 && !aligned16(maps->row_scale)))
+      return fail(RF_ERR_ALIGN, "maps->A and maps->row_scale must be 16-byte aligned");
+  }
+  FillLayout lay = fill_layout(desc, workspace, maps);
+  if (n_prefix > 0) {
+    if (workspace == nullptr || workspace_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", lay.bytes, workspace_bytes);
+  }
+  int sms = 0;
+  if ((st = current_device(&sms)) != RF_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool work = false;
+  if ((st = fill_prologue(desc, x_S, ld_x, exact_mask, n_fill_out, lay, sms, s, &work)) != RF_OK || !work) return st;
+
+  const bool pair = use_pair(desc->flags, true);
+  const bool staged = maps_staged(maps);
+  const int64_t M_pad = round_up(n_prefix, kFillRowAlign);
+  const size_t map_elems = static_cast<size_t>(d) * static_cast<size_t>(d_in);
+  const size_t elem = int8 ? 1 : 2;
+  const int64_t H = desc->n_kv_heads;
+  cudaStream_t cs = nullptr;
+  EventSet ev;
+  cudaEvent_t* ready = ev.e + 1;
+  cudaEvent_t* freed = ev.e + 3;
+  if (staged) {
+    if ((st = copy_stream(&cs)) != RF_OK || (st = ev.create()) != RF_OK) return st;
+    // The ring lives in the caller's workspace: earlier work on `s` may still use it.
+    if ((st = cuda_check(cudaEventRecord(ev.e[0], s), "cudaEventRecord")) != RF_OK) return st;
+    if ((st = cuda_check(cudaStreamWaitEvent(cs, ev.e[0], 0), "cudaStreamWaitEvent")) != RF_OK) return st;
+  }
+  for (int64_t p = 0; p < P; ++p) {
+    const int r = static_cast<int>(p & 1);
+    const char* src = static_cast<const char*>(maps->A) + static_cast<size_t>(p) * map_elems * elem;
+    const void* Ap = src;
+    if (staged) {
+      if (p >= 2 && (st = cuda_check(cudaStreamWaitEvent(cs, freed[r], 0), "cudaStreamWaitEvent")) != RF_OK) return st;
+      if (!int8) {
+        st = cuda_check(cudaMemcpyAsync(lay.slot[r], src, map_elems * 2, cudaMemcpyHostToDevice, cs), "map copy");
+      } else if (maps->on_host) {
+        st = cuda_check(cudaMemcpyAsync(lay.stage[r], src, map_elems, cudaMemcpyHostToDevice, cs), "map copy");
+        if (st == RF_OK) st = expand_int8(lay.stage[r], lay.slot[r], map_elems, sms, cs);
+      } else {
+        st = expand_int8(reinterpret_cast<const int8_t*>(src), lay.slot[r], map_elems, sms, cs);
+      }
+      if (st != RF_OK) return st;
+      if ((st = cuda_check(cudaEventRecord(ready[r], cs), "cudaEventRecord")) != RF_OK) return st;
+      if ((st = cuda_check(cudaStreamWaitEvent(s, ready[r], 0), "cudaStreamWaitEvent")) != RF_OK) return st;
+      Ap = lay.slot[r];
+    }
+    MapGemmArgs ma{lay.xf, d_in, M_pad, lay.n_fill, Ap, b + p * d, int8 ? maps->row_scale + p * d : nullptr,
+                   lay.xhat, lay.ssp, d, d_in, 1, M_pad, dev_status};
+    if ((st = map_gemm(pair, ma, sms, s)) != RF_OK) return st;
+    if (staged && (st = cuda_check(cudaEventRecord(freed[r], s), "cudaEventRecord")) != RF_OK) return st;
+    KvGemmArgs ka{lay.xhat, lay.ssp, lay.n_fill, lay.fill_idx, lay.rope_cos, lay.rope_sin,
+                  reinterpret_cast<const __nv_bfloat16*>(Wkv) + static_cast<size_t>(p) * 2 * KV * d, k_cache, v_cache,
+                  desc->v_scale ? desc->v_scale + p * H : nullptr,
+                  desc->k_norm_gain ? reinterpret_cast<const __nv_bfloat16*>(desc->k_norm_gain) + p * desc->head_dim
+                                    : nullptr,
+                  layer_stride, row_stride, d, 1, desc->S + p, M_pad, KV, desc->head_dim, desc->rms_eps, dev_status};
+    if ((st = kv_gemm(pair, ka, sms, s)) != RF_OK) return st;
+  }
+  return RF_OK;
 }

@@ -34,6 +34,7 @@ struct MapProb {
   CUtensorMap tmB;
   const int32_t* n_fill;
   const float* bias;       // [P][d]
+  const float* col_scale;  // [P][d] or nullptr: per output column scale (int8 maps' row scales)
   __nv_bfloat16* xhat;     // [P][M_pad][d]
   float* ssp;              // [P][d/256][M_pad]
   int d, k_in, P, M_pad, n_ntiles, m_band;  // d: map output width; k_in: map input width
@@ -87,6 +88,7 @@ struct MapProb {
     const int m = mt * Cfg::kUnitM + static_cast<int>(rank) * kBM + row;
     const bool valid = m < nf;
     const float* bp = bias + static_cast<size_t>(p) * d + c0;
+    const float* sp = col_scale != nullptr ? col_scale + static_cast<size_t>(p) * d + c0 : nullptr;
     __nv_bfloat16* dst = xhat + (static_cast<size_t>(p) * M_pad + m) * d + c0;
     float ss = 0.f;
 #pragma unroll 1
@@ -98,8 +100,10 @@ struct MapProb {
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
         const float4 bb = __ldg(reinterpret_cast<const float4*>(bp + ch * 32 + i));
-        const float x0 = u2f(v[i]) + bb.x, x1 = u2f(v[i + 1]) + bb.y;
-        const float x2 = u2f(v[i + 2]) + bb.z, x3 = u2f(v[i + 3]) + bb.w;
+        const float4 cs = sp != nullptr ? __ldg(reinterpret_cast<const float4*>(sp + ch * 32 + i))
+                                        : make_float4(1.f, 1.f, 1.f, 1.f);
+        const float x0 = fmaf(u2f(v[i]), cs.x, bb.x), x1 = fmaf(u2f(v[i + 1]), cs.y, bb.y);
+        const float x2 = fmaf(u2f(v[i + 2]), cs.z, bb.z), x3 = fmaf(u2f(v[i + 3]), cs.w, bb.w);
         ss = fmaf(x0, x0, ss);
         ss = fmaf(x1, x1, ss);
         ss = fmaf(x2, x2, ss);
@@ -230,6 +234,7 @@ struct KVProb {
 //   x_rows      [n_rows_max][ld_x] bf16 rows of width d_in; rows >= *n_rows are not computed
 //   n_rows      device int32: rows to compute (<= n_rows_max <= M_pad)
 //   A           [P][d][d_in] bf16, b [P][d] fp32
+//   col_scale   [P][d] fp32 or nullptr: x̂[o] = col_scale[o] * (A x)[o] + b[o]
 //   xhat        [P][M_pad][d] bf16, ssp [P][d/256][M_pad] fp32
 struct MapGemmArgs {
   const void* x_rows;
@@ -237,11 +242,32 @@ struct MapGemmArgs {
   const int32_t* n_rows;
   const void* A;
   const float* b;
+  const float* col_scale;
   __nv_bfloat16* xhat;
   float* ssp;
   int64_t d, d_in, P, M_pad;
   int32_t* dev_status;
 };
 rf_status map_gemm(bool pair, const MapGemmArgs& a, int sms, cudaStream_t s);
+
+// The K/V GEMM (norm scale, optional key norm and value scale, RoPE, cache
+// scatter), also launched from fill.cu only. Layers S .. S+P-1 of the caches.
+struct KvGemmArgs {
+  const __nv_bfloat16* xhat;  // [P][M_pad][d]
+  const float* ssp;           // [P][d/256][M_pad]
+  const int32_t* n_fill;
+  const int32_t* fill_idx;
+  const float* rope_cos;
+  const float* rope_sin;
+  const void* Wkv;            // [P][2KV][d]
+  void* k_cache;
+  void* v_cache;
+  const float* v_scale;       // [P][H] or nullptr
+  const void* k_gain;         // [P][hd] bf16 or nullptr
+  int64_t layer_stride, row_stride, d, P, S, M_pad, KV, hd;
+  double eps;
+  int32_t* dev_status;
+};
+rf_status kv_gemm(bool pair, const KvGemmArgs& a, int sms, cudaStream_t s);
 
 }  // namespace rf

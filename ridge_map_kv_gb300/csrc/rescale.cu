@@ -216,7 +216,7 @@ static rf_status rescale_gemms(const rf_fill_desc* desc, int64_t c, const Rescal
   const uint64_t tmo = wait_timeout_ns();
   {
     const int64_t d_in = desc->d_in > 0 ? desc->d_in : d;
-    MapGemmArgs ma{x_tail, ld_x, c, lay.n_c, A, b, lay.xhat, lay.ssp, d, d_in, P, Mc, dev_status};
+    MapGemmArgs ma{x_tail, ld_x, c, lay.n_c, A, b, nullptr, lay.xhat, lay.ssp, d, d_in, P, Mc, dev_status};
     if ((st = map_gemm(kPair, ma, sms, s)) != RF_OK) return st;
   }
   {

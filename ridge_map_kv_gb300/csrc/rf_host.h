@@ -2,6 +2,7 @@
 // workspace carving, TMA descriptor encoding and device queries.
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -60,6 +61,11 @@ int max_active_pairs(const void* kernel, size_t smem_bytes, int threads, int sms
 
 // Sets the dynamic shared-memory limit of a kernel once per process and device.
 rf_status set_smem_attr(const void* kernel, size_t bytes, uint64_t* done_mask);
+
+// int8 map codes -> bf16 (exact), n % 16 == 0 (maps.cu).
+rf_status expand_int8(const int8_t* q, __nv_bfloat16* out, size_t n, int sms, cudaStream_t s);
+// The library's non-blocking copy stream for the current device (maps.cu).
+rf_status copy_stream(cudaStream_t* out);
 
 // Brackets one kernel launch with profiling events when rf_profile_start is active.
 struct ProfScope {

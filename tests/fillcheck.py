@@ -53,6 +53,13 @@ def run_fill(cfg, inp: dict, dev="cuda", mask="inp", canary=True, flags: int = 0
             "status": int(status.item()), "ws": ws, "Wkv": Wkv}
 
 
+def _f64_of(t) -> np.ndarray:
+    """float64 copy of a bf16 tensor (exact decode) or of a float tensor."""
+    if t.dtype == torch.bfloat16:
+        return O.bf16_bits_to_f64(synth.bits(t))
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
 def oracle_rows(cfg, inp: dict, rows: np.ndarray, v_scale=None, k_norm_gain=None):
     """fp64 oracle K, V [P, n, H, hd] for the given filled rows (V scaled by
     v_scale [P, H] when given)."""
@@ -60,7 +67,7 @@ def oracle_rows(cfg, inp: dict, rows: np.ndarray, v_scale=None, k_norm_gain=None
     x = f64(synth.bits(inp["x_S"][torch.as_tensor(rows, device=inp["x_S"].device)]))
     Ks, Vs = [], []
     for p in range(cfg.P):          # one layer at a time keeps the fp64 copies small
-        K, V = O.fill_rows(x, rows + cfg.pos_offset, f64(synth.bits(inp["A"][p:p + 1])),
+        K, V = O.fill_rows(x, rows + cfg.pos_offset, _f64_of(inp["A"][p:p + 1]),
                            synth.f32(inp["b"][p:p + 1]).astype(np.float64), f64(synth.bits(inp["gain"][p:p + 1])),
                            f64(synth.bits(inp["Wk"][p:p + 1])), f64(synth.bits(inp["Wv"][p:p + 1])),
                            cfg.H, cfg.hd, cfg.rope_theta, cfg.rms_eps,

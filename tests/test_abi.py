@@ -134,6 +134,25 @@ def test_value_scale_validates_on_the_host():
     assert ei.value.status == rf.RF_ERR_WORKSPACE
 
 
+def test_layered_fill_workspace_and_host_checks():
+    desc = _fill_desc()
+    bf = rf.map_source(rf.RF_MAPS_BF16, 256)
+    resident = rf.rf_fill_workspace_bytes(desc)
+    inplace = rf.rf_fill_layered_workspace_bytes(desc, bf)
+    staged = rf.rf_fill_layered_workspace_bytes(desc, rf.map_source(rf.RF_MAPS_BF16, 256, on_host=True))
+    int8_host = rf.rf_fill_layered_workspace_bytes(desc, rf.map_source(rf.RF_MAPS_INT8, 256, on_host=True,
+                                                                        row_scale=256))
+    assert 0 < inplace < resident                   # x̂ for one layer instead of P
+    r = lambda x: (x + 255) // 256 * 256
+    assert staged == inplace + 2 * r(256 * 256 * 2)  # two bf16 map slots
+    assert int8_host == staged + 2 * r(256 * 256)    # plus two int8 landing slots
+    assert rf.rf_fill_layered_workspace_bytes(desc, rf.map_source(7, 256)) == 0
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_fill_kv_layered(desc, 256, 256, None, rf.map_source(rf.RF_MAPS_INT8, 256), 256, 256, 256, 256, 0,
+                              128, workspace=256, workspace_bytes=1 << 30, stream=0)
+    assert ei.value.status == rf.RF_ERR_INVALID_ARG and "row_scale" in rf.rf_last_error()
+
+
 def test_static_fill_scratch_constant_matches_header():
     txt = open(os.path.join(ROOT, "include", "rf.h")).read()
     assert "RF_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)" in txt
