@@ -523,6 +523,48 @@ def run_extras(dev, peak_tflops, flags=0):
     del inp, kt, vt, ws
     torch.cuda.empty_cache()
 
+    # Map storage at the bench workload (8B shape): the resident fill against the
+    # layer-by-layer fill with maps on the device or the host, bf16 or int8
+    c = synth.LLAMA8B
+    inp = synth.fill_inputs(c, device=dev)
+    fd = rf.rf_fill_desc(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
+                         rms_eps=c.rms_eps, pos_offset=0, flags=flags)
+    Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
+    rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
+    del inp["Wk"], inp["Wv"]
+    q = torch.empty((c.P, c.d, c.d), dtype=torch.int8, device=dev)
+    qs = torch.empty((c.P, c.d), dtype=torch.float32, device=dev)
+    rf.rf_quantize_maps_int8(fd, inp["A"], q, qs)
+    A_host = inp["A"].cpu().pin_memory()
+    q_host = q.cpu().pin_memory()
+    kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    nf = torch.zeros(1, dtype=torch.int32, device=dev)
+    row = {"workload": workload_label(c), "map_bytes_bf16": c.P * c.d * c.d * 2, "map_bytes_int8": c.P * c.d * c.d}
+    wsb = rf.rf_fill_workspace_bytes(fd)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    row["resident_ms"], _ = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], Wkv, kc,
+                                                         vc, c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
+    row["resident_workspace_bytes"] = wsb
+    del ws
+    variants = {"layered_device_bf16": rf.map_source(rf.RF_MAPS_BF16, inp["A"]),
+                "layered_host_bf16": rf.map_source(rf.RF_MAPS_BF16, A_host, on_host=True),
+                "layered_device_int8": rf.map_source(rf.RF_MAPS_INT8, q, row_scale=qs),
+                "layered_host_int8": rf.map_source(rf.RF_MAPS_INT8, q_host, on_host=True, row_scale=qs)}
+    for key, ms_ in variants.items():
+        wsb = rf.rf_fill_layered_workspace_bytes(fd, ms_)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        row[f"{key}_ms"], st = _timed(lambda: rf.rf_fill_kv_layered(fd, inp["x_S"], c.d, inp["mask"], ms_, inp["b"],
+                                                                    Wkv, kc, vc, c.N * c.KV, c.KV, nf, None, ws,
+                                                                    wsb), 3, stream)
+        row[f"{key}_workspace_bytes"] = wsb
+        if "int8_expand" in st:
+            row[f"{key}_expand_ms"] = st["int8_expand"]
+        del ws
+    out["next3_map_storage_8b"] = row
+    del inp, kc, vc, Wkv, q, qs, A_host, q_host
+    torch.cuda.empty_cache()
+
     # Key normalisation: the Qwen3-8B-shaped fill without and with per-head K norm
     c = synth.QWEN3_8B
     inp = synth.fill_inputs(c, device=dev)
