@@ -349,6 +349,23 @@ def run_ours(args):
                 "algorithmic_bytes_per_launch": n_fill * di * 2 + P * d * di * 2 + n_fill * P * d * 2
                 + n_fill * P * (d // 256) * 4 + P * d * 4}
 
+    # HBM-bound kernels of the step against the measured copy bandwidth:
+    # gather = read n_fill rows of x_S + write Xf (n_fill rows, zero pad to the
+    # 256-row unit); rope table = write 2 * n_prefix * hd/2 fp32; compaction =
+    # read the mask + write fill_idx.
+    n_prefix = cfg.N - cfg.T
+    m_pad = -(-n_fill // 256) * 256
+    hbm_bytes = {"gather": n_fill * di * 2 + m_pad * di * 2,
+                 "rope_table": 2 * n_prefix * (cfg.hd // 2) * 4,
+                 "compact": n_prefix + n_fill * 4}
+    hbm_kernels = {}
+    for k, nbytes in hbm_bytes.items():
+        ms_k = stage_avg.get(k)
+        if ms_k:
+            gbs = nbytes / (ms_k / 1e3) / 1e9
+            hbm_kernels[k] = {"bytes": nbytes, "ms": ms_k, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"],
+                              "peak": peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy (MEASURED_PEAKS.json)"}
+
     # End to end through the C ABI from pinned host buffers: x_S and the mask go
     # host->device, n_fill and the status word come back, every step.
     e2e = None
@@ -407,7 +424,8 @@ def run_ours(args):
                        "l2": "no flush: inputs larger than L2 (1.1 GB of maps, weights and x_S read per step)"},
             "tflops": fill_flops * args.steps * ws_n / (t_max / 1e3) / 1e12,
             "frac_of_bf16_peak": fill_flops * args.steps * ws_n / (t_max / 1e3) / 1e12 / peak,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "roofline": roofline, "hbm_kernels": hbm_kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches,
             "clocks": clk,
             "stages_ms": stage_avg, "fold_once_ms": fold_ms, "extras": extras,
         }

@@ -260,12 +260,13 @@ typedef struct rf_map_source {
   const float* row_scale; /* RF_MAPS_INT8: [P][d] fp32 on the device; else unused       */
 } rf_map_source;
 
-/* The fill of rf_fill_kv, one layer at a time: for p = 0 .. P-1 the map GEMM of
- * layer S+p and then its K/V GEMM, so x̂ exists for one layer only (workspace
- * M_pad*d instead of P*M_pad*d bf16). Maps on the host or in int8 pass through a
- * two-slot bf16 ring in the workspace: the library's copy stream copies layer
- * p+1 (and expands int8 codes to bf16, exact for |q| <= 127) while the caller's
- * stream computes layer p; int8 row scales are applied to the map GEMM's output
+/* The fill of rf_fill_kv, a few layers at a time: for each step of up to 4
+ * layers the map GEMM of those layers and then their K/V GEMM, so x̂ exists for
+ * 4 layers only (workspace 4*M_pad*d instead of P*M_pad*d bf16). Maps on the host
+ * or in int8 pass through a two-slot bf16 ring in the workspace: the library's
+ * copy stream copies the next step's maps (and expands int8 codes to bf16, exact
+ * for |q| <= 127) while the caller's stream computes the current step; int8 row
+ * scales are applied to the map GEMM's output
  * columns with the bias. Device bf16 maps are read in place. The results equal
  * rf_fill_kv's bit for bit when the maps are the same bf16 values (same kernels,
  * same summation order). Arguments as for rf_fill_kv, with `maps` replacing A;

@@ -157,6 +157,12 @@ struct FillLayout {
   size_t bytes;
 };
 
+// The layered fill computes kLayerChunk layers per step (one map GEMM and one K/V
+// GEMM over them): one layer per launch leaves the last wave of 76 CTA pairs
+// mostly idle (an 8B layer is 704 map and 352 K/V units), four layers per step
+// keep that loss to a few percent while x̂ still exists for 4 layers, not P.
+constexpr int64_t kLayerChunk = 4;
+
 // Maps the layered fill reads in place (device bf16) need no ring.
 static bool maps_staged(const rf_map_source* m) { return !(m->kind == RF_MAPS_BF16 && !m->on_host); }
 
@@ -188,7 +194,7 @@ static FillLayout fill_layout(const rf_fill_desc* d, void* ws, const rf_map_sour
   const int64_t n_prefix = d->N - d->T;
   const int64_t M_pad = round_up(std::max<int64_t>(n_prefix, 1), kFillRowAlign);
   const int64_t P = d->L - d->S;
-  const int64_t xhat_layers = maps != nullptr ? std::min<int64_t>(P, 1) : P;
+  const int64_t xhat_layers = maps != nullptr ? std::min<int64_t>(P, kLayerChunk) : P;
   Carve c(ws);
   FillLayout l{};
   l.fill_idx = c.take<int32_t>(std::max<int64_t>(n_prefix, 1));
@@ -199,7 +205,7 @@ static FillLayout fill_layout(const rf_fill_desc* d, void* ws, const rf_map_sour
   l.rope_cos = c.take<float>(std::max<int64_t>(n_prefix, 1) * (d->head_dim / 2));
   l.rope_sin = c.take<float>(std::max<int64_t>(n_prefix, 1) * (d->head_dim / 2));
   if (maps != nullptr && maps_staged(maps)) {
-    const int64_t n = d->d * fill_din(d);
+    const int64_t n = xhat_layers * d->d * fill_din(d);
     for (int i = 0; i < 2; ++i) l.slot[i] = c.take<__nv_bfloat16>(n);
     if (maps->kind == RF_MAPS_INT8 && maps->on_host)
       for (int i = 0; i < 2; ++i) l.stage[i] = c.take<int8_t>(n);
@@ -413,9 +419,10 @@ extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, in
 
 // --------------------------------------------------------------------------
 // Layer-by-layer fill (rf_fill_kv_layered): one map GEMM and one K/V GEMM per
-// layer, x̂ for one layer at a time. Maps that live on the host or in int8 pass
-// through a two-slot bf16 ring: the library's copy stream copies (and expands)
-// layer p+1 while the caller's stream computes layer p; events order slot reuse.
+// step of kLayerChunk layers, x̂ for those layers only. Maps that live on the host
+// or in int8 pass through a two-slot bf16 ring: the library's copy stream copies
+// (and expands) the next step's layers while the caller's stream computes the
+// current ones; events order slot reuse.
 // --------------------------------------------------------------------------
 struct EventSet {
   cudaEvent_t e[5] = {};
@@ -490,35 +497,38 @@ extern "C" rf_status rf_fill_kv_layered(const rf_fill_desc* desc, const rf_bf16*
     if ((st = cuda_check(cudaEventRecord(ev.e[0], s), "cudaEventRecord")) != RF_OK) return st;
     if ((st = cuda_check(cudaStreamWaitEvent(cs, ev.e[0], 0), "cudaStreamWaitEvent")) != RF_OK) return st;
   }
-  for (int64_t p = 0; p < P; ++p) {
-    const int r = static_cast<int>(p & 1);
-    const char* src = static_cast<const char*>(maps->A) + static_cast<size_t>(p) * map_elems * elem;
+  for (int64_t c0 = 0, step = 0; c0 < P; c0 += kLayerChunk, ++step) {
+    const int64_t g = std::min<int64_t>(kLayerChunk, P - c0);  // layers S+c0 .. S+c0+g-1
+    const int r = static_cast<int>(step & 1);
+    const size_t n = static_cast<size_t>(g) * map_elems;
+    const char* src = static_cast<const char*>(maps->A) + static_cast<size_t>(c0) * map_elems * elem;
     const void* Ap = src;
     if (staged) {
-      if (p >= 2 && (st = cuda_check(cudaStreamWaitEvent(cs, freed[r], 0), "cudaStreamWaitEvent")) != RF_OK) return st;
+      if (step >= 2 && (st = cuda_check(cudaStreamWaitEvent(cs, freed[r], 0), "cudaStreamWaitEvent")) != RF_OK)
+        return st;
       if (!int8) {
-        st = cuda_check(cudaMemcpyAsync(lay.slot[r], src, map_elems * 2, cudaMemcpyHostToDevice, cs), "map copy");
+        st = cuda_check(cudaMemcpyAsync(lay.slot[r], src, n * 2, cudaMemcpyHostToDevice, cs), "map copy");
       } else if (maps->on_host) {
-        st = cuda_check(cudaMemcpyAsync(lay.stage[r], src, map_elems, cudaMemcpyHostToDevice, cs), "map copy");
-        if (st == RF_OK) st = expand_int8(lay.stage[r], lay.slot[r], map_elems, sms, cs);
+        st = cuda_check(cudaMemcpyAsync(lay.stage[r], src, n, cudaMemcpyHostToDevice, cs), "map copy");
+        if (st == RF_OK) st = expand_int8(lay.stage[r], lay.slot[r], n, sms, cs);
       } else {
-        st = expand_int8(reinterpret_cast<const int8_t*>(src), lay.slot[r], map_elems, sms, cs);
+        st = expand_int8(reinterpret_cast<const int8_t*>(src), lay.slot[r], n, sms, cs);
       }
       if (st != RF_OK) return st;
       if ((st = cuda_check(cudaEventRecord(ready[r], cs), "cudaEventRecord")) != RF_OK) return st;
       if ((st = cuda_check(cudaStreamWaitEvent(s, ready[r], 0), "cudaStreamWaitEvent")) != RF_OK) return st;
       Ap = lay.slot[r];
     }
-    MapGemmArgs ma{lay.xf, d_in, M_pad, lay.n_fill, Ap, b + p * d, int8 ? maps->row_scale + p * d : nullptr,
-                   lay.xhat, lay.ssp, d, d_in, 1, M_pad, dev_status};
+    MapGemmArgs ma{lay.xf, d_in, M_pad, lay.n_fill, Ap, b + c0 * d, int8 ? maps->row_scale + c0 * d : nullptr,
+                   lay.xhat, lay.ssp, d, d_in, g, M_pad, dev_status};
     if ((st = map_gemm(pair, ma, sms, s)) != RF_OK) return st;
     if (staged && (st = cuda_check(cudaEventRecord(freed[r], s), "cudaEventRecord")) != RF_OK) return st;
     KvGemmArgs ka{lay.xhat, lay.ssp, lay.n_fill, lay.fill_idx, lay.rope_cos, lay.rope_sin,
-                  reinterpret_cast<const __nv_bfloat16*>(Wkv) + static_cast<size_t>(p) * 2 * KV * d, k_cache, v_cache,
-                  desc->v_scale ? desc->v_scale + p * H : nullptr,
-                  desc->k_norm_gain ? reinterpret_cast<const __nv_bfloat16*>(desc->k_norm_gain) + p * desc->head_dim
+                  reinterpret_cast<const __nv_bfloat16*>(Wkv) + static_cast<size_t>(c0) * 2 * KV * d, k_cache, v_cache,
+                  desc->v_scale ? desc->v_scale + c0 * H : nullptr,
+                  desc->k_norm_gain ? reinterpret_cast<const __nv_bfloat16*>(desc->k_norm_gain) + c0 * desc->head_dim
                                     : nullptr,
-                  layer_stride, row_stride, d, 1, desc->S + p, M_pad, KV, desc->head_dim, desc->rms_eps, dev_status};
+                  layer_stride, row_stride, d, g, desc->S + c0, M_pad, KV, desc->head_dim, desc->rms_eps, dev_status};
     if ((st = kv_gemm(pair, ka, sms, s)) != RF_OK) return st;
   }
   return RF_OK;

@@ -135,17 +135,17 @@ def test_value_scale_validates_on_the_host():
 
 
 def test_layered_fill_workspace_and_host_checks():
-    desc = _fill_desc()
+    desc = _fill_desc(L=10)                         # 6 upper layers
     bf = rf.map_source(rf.RF_MAPS_BF16, 256)
     resident = rf.rf_fill_workspace_bytes(desc)
     inplace = rf.rf_fill_layered_workspace_bytes(desc, bf)
     staged = rf.rf_fill_layered_workspace_bytes(desc, rf.map_source(rf.RF_MAPS_BF16, 256, on_host=True))
     int8_host = rf.rf_fill_layered_workspace_bytes(desc, rf.map_source(rf.RF_MAPS_INT8, 256, on_host=True,
                                                                         row_scale=256))
-    assert 0 < inplace < resident                   # x̂ for one layer instead of P
+    assert 0 < inplace < resident                   # x̂ for 4 layers at a time instead of all 6
     r = lambda x: (x + 255) // 256 * 256
-    assert staged == inplace + 2 * r(256 * 256 * 2)  # two bf16 map slots
-    assert int8_host == staged + 2 * r(256 * 256)    # plus two int8 landing slots
+    assert staged == inplace + 2 * r(4 * 256 * 256 * 2)  # two bf16 map slots of 4 layers
+    assert int8_host == staged + 2 * r(4 * 256 * 256)    # plus two int8 landing slots
     assert rf.rf_fill_layered_workspace_bytes(desc, rf.map_source(7, 256)) == 0
     with pytest.raises(rf.RFError) as ei:
         rf.rf_fill_kv_layered(desc, 256, 256, None, rf.map_source(rf.RF_MAPS_INT8, 256), 256, 256, 256, 256, 0,
