@@ -86,12 +86,14 @@ enum rf_stage {
   RF_STAGE_FOLD = 6,         /* gain fold into W_k / W_v                       */
   RF_STAGE_CALIB_GEMM = 7,   /* XᵀX and XᵀY_l                                  */
   RF_STAGE_COLSUM = 8,       /* Σx, Σy, n                                      */
-  RF_STAGE_SOLVE = 9,        /* kernels of the ridge solve                     */
+  RF_STAGE_SOLVE = 9,        /* ridge solve: centring, Cholesky, H^-1          */
   RF_STAGE_UNROPE = 10,      /* RoPE / inverse RoPE on cache rows              */
   RF_STAGE_XMODEL_GEMM = 11, /* cross-model mapper GEMM                        */
   RF_STAGE_RESCALE = 12,     /* value rescale: value norms and their ratios   */
   RF_STAGE_EXPAND = 13,      /* int8 map codes -> bf16 before a layer's GEMM   */
-  RF_STAGE_QUANTIZE = 14     /* bf16 maps -> int8 codes and row scales         */
+  RF_STAGE_QUANTIZE = 14,    /* bf16 maps -> int8 codes and row scales         */
+  RF_STAGE_SOLVE_PRODUCT = 15, /* solve: A_p = Cc_pᵀ H^-1 (split tensor-core GEMM) */
+  RF_STAGE_SOLVE_REFINE = 16   /* solve: fp64 residual and correction, per sweep */
 };
 rf_status rf_profile_start(int max_records);
 /* Diagnostic: runs the tensor-core GEMM kernel (cta_pair != 0: the CTA-pair

@@ -234,6 +234,8 @@ const char* rf_stage_name(int s) {
     case RF_STAGE_RESCALE: return "value_rescale";
     case RF_STAGE_EXPAND: return "int8_expand";
     case RF_STAGE_QUANTIZE: return "int8_quantize";
+    case RF_STAGE_SOLVE_PRODUCT: return "solve_product";
+    case RF_STAGE_SOLVE_REFINE: return "solve_refine";
     default: return "unknown";
   }
 }

@@ -11,14 +11,22 @@
 //                           diagonal blocks; panels and trailing updates are fp32
 //                           GEMMs (k_sgemm) with the inverse of the diagonal block
 //   trinv_lower (recursive) L^-1 from one-CTA diagonal inverses and fp32 GEMMs
-//   k_sgemm                 H^-1 = L^-ᵀ L^-1, then A_p = Cc_pᵀ H^-1 for every map
+//   k_sgemm                 H^-1 = L^-ᵀ L^-1 (fp32 SIMT)
+//   split3 + tc_gemm<Split3Prob>  A_p = Cc_pᵀ H^-1 for every map on the tensor
+//                           cores: each fp32 operand is the sum of three bf16
+//                           planes (hi + mid + lo, exact to fp32 rounding), and
+//                           the six products that matter at fp32 precision
+//                           (hi·hi, mid·hi, hi·mid, lo·hi, mid·mid, hi·lo) are
+//                           summed over 1024-wide K chunks in TMEM, then in fp32
+//                           registers across chunks and terms
 //   refinement (optional)   R_p = Cc_pᵀ − A_p H with fp64 products (k_resid64),
-//                           A_p += R_p H^-1 (fp32)
+//                           A_p += R_p H^-1 (the same split tensor-core product)
 //   k_bias                  b_p = μ_p − A_p μ_x (fp64 accumulation)
 #include <algorithm>
 
 #include "rf_host.h"
 #include "rf_device.cuh"
+#include "tc_gemm.cuh"
 
 namespace rf {
 
@@ -141,15 +149,18 @@ constexpr size_t kBlkSmem = sizeof(float) * kSolveBlock * kBlkLd;
 
 // In-place lower Cholesky of the n x n block at A (n <= 128); zeroes the upper
 // triangle. A non-positive pivot records RF_ERR_NOT_SPD and continues with 1.
+// Column by column: the pivot, the column scale, then the trailing update with
+// two threads per row (no index divisions; the 129-float row pitch keeps both
+// the row and the column accesses free of bank conflicts).
 __global__ void __launch_bounds__(256) k_chol_base(float* A, int n, long long lda, int32_t* dev_status) {
   extern __shared__ float S[];
-  for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
-    const int i = e / n, j = e % n;
-    S[i * kBlkLd + j] = A[i * lda + j];
-  }
+  for (int i = threadIdx.y; i < n; i += blockDim.y)
+    for (int k = threadIdx.x; k < n; k += blockDim.x) S[i * kBlkLd + k] = A[i * lda + k];
+  const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+  const int nthr = blockDim.x * blockDim.y;
   __syncthreads();
   for (int j = 0; j < n; ++j) {
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
       float d = S[j * kBlkLd + j];
       if (!(d > 0.f)) {
         record_status(dev_status, RF_ERR_NOT_SPD);
@@ -159,47 +170,62 @@ __global__ void __launch_bounds__(256) k_chol_base(float* A, int n, long long ld
     }
     __syncthreads();
     const float inv = 1.f / S[j * kBlkLd + j];
-    for (int i = j + 1 + threadIdx.x; i < n; i += blockDim.x) S[i * kBlkLd + j] *= inv;
+    for (int i = j + 1 + tid; i < n; i += nthr) S[i * kBlkLd + j] *= inv;
     __syncthreads();
-    const int m = n - j - 1;
-    for (int e = threadIdx.x; e < m * m; e += blockDim.x) {
-      const int i = j + 1 + e / m, k = j + 1 + e % m;
-      if (k <= i) S[i * kBlkLd + k] -= S[i * kBlkLd + j] * S[k * kBlkLd + j];
+    for (int i = j + 1 + (tid >> 1); i < n; i += nthr >> 1) {
+      const float lij = S[i * kBlkLd + j];
+      for (int k = j + 1 + (tid & 1); k <= i; k += 2) S[i * kBlkLd + k] -= lij * S[k * kBlkLd + j];
     }
     __syncthreads();
   }
-  for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
-    const int i = e / n, j = e % n;
-    A[i * lda + j] = j <= i ? S[i * kBlkLd + j] : 0.f;
-  }
+  for (int i = threadIdx.y; i < n; i += blockDim.y)
+    for (int k = threadIdx.x; k < n; k += blockDim.x) A[i * lda + k] = k <= i ? S[i * kBlkLd + k] : 0.f;
 }
 
-// W = L^-1 for the lower n x n block L (n <= 128), by forward substitution of the
-// unit vectors, one column per thread; the upper triangle of W is zeroed.
-__global__ void __launch_bounds__(128) k_trinv_base(const float* L, int n, long long ldl, float* W, long long ldw) {
+// Diagonal blocks of one triangular inverse, inverted by one launch (one CTA each).
+constexpr int kMaxLeaves = 256;
+struct LeafBlocks {
+  int off[kMaxLeaves];
+  int size[kMaxLeaves];
+};
+
+// W = L^-1 for lower n x n diagonal blocks L (n <= 128), row by row in shared
+// memory: W[i][j] = (δ_ij − Σ_{j<=k<i} L[i][k] W[k][j]) / L[i][i], thread j
+// computing column j of row i once rows < i are done (four partial sums keep the
+// dependent chain short); the upper triangle of W is zero. CTA b inverts the
+// block at (off[b], off[b]) of size size[b].
+__global__ void __launch_bounds__(128) k_trinv_base(const float* L0, long long ldl, float* W0, long long ldw,
+                                                    const __grid_constant__ LeafBlocks lb) {
+  const int off = lb.off[blockIdx.x], n = lb.size[blockIdx.x];
+  const float* L = L0 + static_cast<long long>(off) * ldl + off;
+  float* W = W0 + static_cast<long long>(off) * ldw + off;
   extern __shared__ float S[];
-  for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
-    const int i = e / n, j = e % n;
-    S[i * kBlkLd + j] = L[i * ldl + j];
-  }
+  float* Wi = S + kSolveBlock * kBlkLd;
+  for (int i = 0; i < n; ++i)
+    for (int k = threadIdx.x; k < n; k += blockDim.x) S[i * kBlkLd + k] = L[i * ldl + k];
   __syncthreads();
   const int j = threadIdx.x;
-  if (j < n) {
-    float x[kSolveBlock];
-#pragma unroll 1
-    for (int i = 0; i < n; ++i) {
-      if (i < j) {
-        x[i] = 0.f;
-        continue;
+  for (int i = 0; i < n; ++i) {
+    if (j < n) {
+      float s = 0.f;
+      if (j <= i) {
+        float s0 = (i == j) ? 1.f : 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        int k = j;
+        for (; k + 3 < i; k += 4) {
+          s0 = fmaf(-S[i * kBlkLd + k], Wi[k * kBlkLd + j], s0);
+          s1 = fmaf(-S[i * kBlkLd + k + 1], Wi[(k + 1) * kBlkLd + j], s1);
+          s2 = fmaf(-S[i * kBlkLd + k + 2], Wi[(k + 2) * kBlkLd + j], s2);
+          s3 = fmaf(-S[i * kBlkLd + k + 3], Wi[(k + 3) * kBlkLd + j], s3);
+        }
+        for (; k < i; ++k) s0 = fmaf(-S[i * kBlkLd + k], Wi[k * kBlkLd + j], s0);
+        s = ((s0 + s1) + (s2 + s3)) / S[i * kBlkLd + i];
       }
-      float s = (i == j) ? 1.f : 0.f;
-#pragma unroll 1
-      for (int k = j; k < i; ++k) s -= S[i * kBlkLd + k] * x[k];
-      x[i] = s / S[i * kBlkLd + i];
+      Wi[i * kBlkLd + j] = s;
     }
-#pragma unroll 1
-    for (int i = 0; i < n; ++i) W[i * ldw + j] = x[i];
+    __syncthreads();
   }
+  for (int i = 0; i < n; ++i)
+    for (int k = threadIdx.x; k < n; k += blockDim.x) W[i * ldw + k] = Wi[i * kBlkLd + k];
 }
 
 // --------------------------------------------------------------------------
@@ -355,18 +381,205 @@ static rf_status sgemm(SolveCtx& c, bool ta, bool tb, int M, int N, int K, float
   return cuda_check(cudaGetLastError(), "k_sgemm launch");
 }
 
+// --------------------------------------------------------------------------
+// fp32 -> three bf16 planes: x = hi + mid + lo up to the last rounding (x - hi
+// and its remainder are exact in fp32). planes[j][p][r][c] for X_p [R][Cn], or
+// for X_p's transpose when `tr` (src then holds [P][Cn][R]).
+// --------------------------------------------------------------------------
+__device__ __forceinline__ void split3(float x, __nv_bfloat16& h, __nv_bfloat16& m, __nv_bfloat16& l) {
+  h = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(h);
+  m = __float2bfloat16_rn(r1);
+  l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+}
+
+// Row-major copy: 4 consecutive elements per thread-step.
+__global__ void __launch_bounds__(256) k_split3(const float* __restrict__ src, __nv_bfloat16* __restrict__ planes,
+                                                size_t n4, size_t plane) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(src) + i);
+    __nv_bfloat16 h[4], m[4], l[4];
+    split3(v.x, h[0], m[0], l[0]);
+    split3(v.y, h[1], m[1], l[1]);
+    split3(v.z, h[2], m[2], l[2]);
+    split3(v.w, h[3], m[3], l[3]);
+    *reinterpret_cast<uint2*>(planes + 4 * i) = *reinterpret_cast<const uint2*>(h);
+    *reinterpret_cast<uint2*>(planes + plane + 4 * i) = *reinterpret_cast<const uint2*>(m);
+    *reinterpret_cast<uint2*>(planes + 2 * plane + 4 * i) = *reinterpret_cast<const uint2*>(l);
+  }
+}
+
+// Transposed copy through a 32 x 32 shared tile: out rows r < R, columns c < Cn
+// of matrix p read src[p][c][r]. Grid (Cn/32, R/32, P), 32 x 8 threads.
+__global__ void __launch_bounds__(256) k_split3_t(const float* __restrict__ src, __nv_bfloat16* __restrict__ planes,
+                                                  int R, int Cn, size_t plane) {
+  __shared__ float t[32][33];
+  const int p = blockIdx.z;
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const float* s = src + static_cast<size_t>(p) * R * Cn;
+  for (int j = threadIdx.y; j < 32; j += 8) t[j][threadIdx.x] = s[static_cast<size_t>(c0 + j) * R + r0 + threadIdx.x];
+  __syncthreads();
+  __nv_bfloat16* out = planes + static_cast<size_t>(p) * R * Cn;
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    __nv_bfloat16 h, m, l;
+    split3(t[threadIdx.x][j], h, m, l);
+    const size_t o = static_cast<size_t>(r0 + j) * Cn + c0 + threadIdx.x;
+    out[o] = h;
+    out[plane + o] = m;
+    out[2 * plane + o] = l;
+  }
+}
+
+// --------------------------------------------------------------------------
+// out_p = alpha · A_p B + beta · out_p for p < P on the tensor cores, A_p [M][K]
+// and Bᵀ [N][K] given as three bf16 planes each (K-major): planes A [3][P][M][K],
+// B [3][N][K]. Unit: (p, M-tile, N-tile), N fastest so an A strip is reused at
+// once. Sub-tile sb: product term sb / n_chunks over the K chunk sb % n_chunks.
+// Eight epilogue warps keep fp32 running sums of their 128 columns across all
+// sub-tiles and write the tile once at the end.
+// --------------------------------------------------------------------------
+__constant__ int kTermA[6] = {0, 1, 0, 2, 1, 0};  // hi·hi, mid·hi, hi·mid, lo·hi, mid·mid, hi·lo
+__constant__ int kTermB[6] = {0, 0, 1, 0, 1, 2};
+constexpr int kSplitChunk = 1024;
+
+template <bool kPair_>
+struct Split3Prob {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  float* out;  // [P][M][N]
+  float alpha, beta;
+  int P, M, N, K, m_tiles, n_tiles, n_chunks;
+  int32_t* dev_status;
+  uint64_t timeout_ns;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kPair = kPair_;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kCols = kBN / 2;
+  struct EpiState {
+    float rs[kCols];
+  };
+  using Cfg = GemmCfg<kPair_>;
+
+  __device__ void prefetch() const {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  __device__ int num_units() const { return P * m_tiles * n_tiles; }
+  __device__ int num_subtiles(int) const { return 6 * n_chunks; }
+  __device__ int num_kb(int, int sb) const {
+    const int c = sb % n_chunks;
+    return (min(kSplitChunk, K - c * kSplitChunk) + kBK - 1) / kBK;
+  }
+  __device__ void decode(int u, int& p, int& mt, int& nt) const {
+    nt = u % n_tiles;
+    u /= n_tiles;
+    mt = u % m_tiles;
+    p = u / m_tiles;
+  }
+  struct Coords {
+    int a_row, b_row, k0;
+  };
+  __device__ Coords coords(int u, int sb, uint32_t rank) const {
+    int p, mt, nt;
+    decode(u, p, mt, nt);
+    const int t = sb / n_chunks, c = sb - t * n_chunks;
+    return {(kTermA[t] * P + p) * M + mt * Cfg::kUnitM + static_cast<int>(rank) * kBM,
+            kTermB[t] * N + nt * kBN + static_cast<int>(rank) * Cfg::kBRows, c * kSplitChunk};
+  }
+  __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    load_operand<kBM, false, kPair>(sa, &tmA, bar, c.k0 + kb * kBK, c.a_row);
+    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, c.k0 + kb * kBK, c.b_row);
+  }
+  __device__ void epilogue(EpiState& es, int, int sb, int, uint32_t tacc, int, int, uint32_t) const {
+#pragma unroll
+    for (int ch = 0; ch < kCols / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(tacc + ch * 32, v);
+      tmem_wait_ld32(v);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) es.rs[ch * 32 + q] = sb == 0 ? u2f(v[q]) : es.rs[ch * 32 + q] + u2f(v[q]);
+    }
+  }
+  __device__ void epilogue_after(EpiState& es, int u, int sb, int nsub, int row, int col0, uint32_t rank) const {
+    if (sb != nsub - 1) return;
+    int p, mt, nt;
+    decode(u, p, mt, nt);
+    const size_t m = static_cast<size_t>(mt) * Cfg::kUnitM + rank * kBM + row;
+    float4* o = reinterpret_cast<float4*>(out + (static_cast<size_t>(p) * M + m) * N + static_cast<size_t>(nt) * kBN +
+                                          col0);
+#pragma unroll
+    for (int q = 0; q < kCols / 4; ++q) {
+      float4 v = make_float4(alpha * es.rs[4 * q], alpha * es.rs[4 * q + 1], alpha * es.rs[4 * q + 2],
+                             alpha * es.rs[4 * q + 3]);
+      if (beta != 0.f) {
+        const float4 c = o[q];
+        v.x = fmaf(beta, c.x, v.x);
+        v.y = fmaf(beta, c.y, v.y);
+        v.z = fmaf(beta, c.z, v.z);
+        v.w = fmaf(beta, c.w, v.w);
+      }
+      o[q] = v;
+    }
+  }
+};
+
+// out_p = alpha A_p B + beta out_p with A_p [M][K] read from `a` ([P][M][K], or
+// its transpose [P][K][M] when a_tr) and B [K][N] symmetric (its rows serve as
+// Bᵀ), through the split planes in `planes_a` (3·P·M·K) and `planes_b` (3·N·K).
+static rf_status split_gemm(SolveCtx& c, const float* a, bool a_tr, const float* Bsym, int P, int M, int N, int K,
+                            float alpha, float beta, float* out, __nv_bfloat16* planes_a, __nv_bfloat16* planes_b) {
+  rf_status st;
+  const size_t pa = static_cast<size_t>(P) * M * K, pb = static_cast<size_t>(N) * K;
+  const unsigned eb = static_cast<unsigned>(8 * c.sms);
+  if (a_tr) {
+    k_split3_t<<<dim3(K / 32, M / 32, P), dim3(32, 8), 0, c.s>>>(a, planes_a, M, K, pa);
+  } else {
+    k_split3<<<eb, 256, 0, c.s>>>(a, planes_a, pa / 4, pa);
+  }
+  k_split3<<<eb, 256, 0, c.s>>>(Bsym, planes_b, pb / 4, pb);
+  if ((st = cuda_check(cudaGetLastError(), "split launches")) != RF_OK) return st;
+  Split3Prob<true> pr;
+  if ((st = make_tmap_bf16_2d(&pr.tmA, planes_a, K, 3LL * P * M, K, kBK, kBM)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmB, planes_b, K, 3LL * N, K, kBK, GemmCfg<true>::kBRows)) != RF_OK) return st;
+  pr.out = out;
+  pr.alpha = alpha;
+  pr.beta = beta;
+  pr.P = P;
+  pr.M = M;
+  pr.N = N;
+  pr.K = K;
+  pr.m_tiles = M / GemmCfg<true>::kUnitM;
+  pr.n_tiles = N / kBN;
+  pr.n_chunks = (K + kSplitChunk - 1) / kSplitChunk;
+  pr.dev_status = c.dev_status;
+  pr.timeout_ns = wait_timeout_ns();
+  return launch_gemm(pr, static_cast<int64_t>(P) * pr.m_tiles * pr.n_tiles, c.sms, c.s, "split GEMM launch");
+}
+
 static int split_point(int n) { return std::max(kSolveBlock, (n / 2) / kSolveBlock * kSolveBlock); }
 
 // W (n x n, ld ldw) = L^-1 for the lower-triangular L (n x n, ld ldl); n % 128 == 0.
-static rf_status trinv_lower(SolveCtx& c, const float* L, int n, long long ldl, float* W, long long ldw) {
+static void trinv_leaves(int off, int n, LeafBlocks& lb, int& count) {
   if (n <= kSolveBlock) {
-    k_trinv_base<<<1, kSolveBlock, kBlkSmem, c.s>>>(L, n, ldl, W, ldw);
-    return cuda_check(cudaGetLastError(), "k_trinv_base launch");
+    lb.off[count] = off;
+    lb.size[count] = n;
+    ++count;
+    return;
   }
+  const int n1 = split_point(n);
+  trinv_leaves(off, n1, lb, count);
+  trinv_leaves(off + n1, n - n1, lb, count);
+}
+
+// Combines the inverted diagonal blocks bottom-up: W21 = −W22 (L21 W11).
+static rf_status trinv_combine(SolveCtx& c, const float* L, int n, long long ldl, float* W, long long ldw) {
+  if (n <= kSolveBlock) return RF_OK;
   const int n1 = split_point(n), n2 = n - n1;
   rf_status st;
-  if ((st = trinv_lower(c, L, n1, ldl, W, ldw)) != RF_OK) return st;
-  if ((st = trinv_lower(c, L + n1 * ldl + n1, n2, ldl, W + n1 * ldw + n1, ldw)) != RF_OK) return st;
+  if ((st = trinv_combine(c, L, n1, ldl, W, ldw)) != RF_OK) return st;
+  if ((st = trinv_combine(c, L + n1 * ldl + n1, n2, ldl, W + n1 * ldw + n1, ldw)) != RF_OK) return st;
   // T = L21 W11 ;  W21 = −W22 T ;  W12 = 0
   if ((st = sgemm(c, false, false, n2, n1, n1, 1.f, L + n1 * ldl, ldl, 0, W, ldw, 0, 0.f, c.tmp2, n1, 0, 1)) != RF_OK)
     return st;
@@ -376,10 +589,22 @@ static rf_status trinv_lower(SolveCtx& c, const float* L, int n, long long ldl, 
   return cuda_check(cudaMemset2DAsync(W + n1, ldw * sizeof(float), 0, n2 * sizeof(float), n1, c.s), "zero W12");
 }
 
+// W = L^-1 for the lower n x n L: every diagonal block of the split tree in one
+// launch, then the products that join them.
+static rf_status trinv_lower(SolveCtx& c, const float* L, int n, long long ldl, float* W, long long ldw) {
+  LeafBlocks lb;
+  int count = 0;
+  trinv_leaves(0, n, lb, count);
+  k_trinv_base<<<count, kSolveBlock, 2 * kBlkSmem, c.s>>>(L, ldl, W, ldw, lb);
+  rf_status st = cuda_check(cudaGetLastError(), "k_trinv_base launch");
+  if (st != RF_OK) return st;
+  return trinv_combine(c, L, n, ldl, W, ldw);
+}
+
 // In-place lower Cholesky of the n x n matrix A (ld lda); n % 128 == 0.
 static rf_status chol_lower(SolveCtx& c, float* A, int n, long long lda, float* winv) {
   if (n <= kSolveBlock) {
-    k_chol_base<<<1, 256, kBlkSmem, c.s>>>(A, n, lda, c.dev_status);
+    k_chol_base<<<1, dim3(32, 8), kBlkSmem, c.s>>>(A, n, lda, c.dev_status);
     return cuda_check(cudaGetLastError(), "k_chol_base launch");
   }
   const int n1 = split_point(n), n2 = n - n1;
@@ -414,6 +639,8 @@ struct SolveLayout {
   float* tmp;
   float* tmp2;
   float* work;  // Cc (first solve) then R (refinement), [P][d_in][d_out] floats
+  __nv_bfloat16* planes_a;  // [3][P][d_out][d_in] bf16 split of Cc_pᵀ or R_p
+  __nv_bfloat16* planes_b;  // [3][d_in][d_in] bf16 split of H^-1
   size_t bytes;
 };
 
@@ -432,6 +659,8 @@ static SolveLayout solve_layout(const rf_calib_desc* d, void* ws) {
   l.tmp = c.take<float>(di * di);
   l.tmp2 = c.take<float>(di * di);
   l.work = c.take<float>(std::max<int64_t>(P * di * dout, 1));
+  l.planes_a = c.take<__nv_bfloat16>(3 * std::max<int64_t>(P * di * dout, 1));
+  l.planes_b = c.take<__nv_bfloat16>(3 * di * di);
   l.bytes = c.bytes();
   return l;
 }
@@ -442,6 +671,7 @@ static rf_status check_solve_desc(const rf_calib_desc* d) {
   if (d->d_in % 256 != 0 || d->d_out % 256 != 0)
     return fail(RF_ERR_SHAPE, "d_in and d_out must be multiples of 256");
   if (d->d_in > 32768 || d->n_maps > 65535) return fail(RF_ERR_SHAPE, "d_in must be <= 32768, n_maps <= 65535");
+  // (d_in <= 32768 keeps the triangular inverse's leaf blocks within kMaxLeaves.)
   return RF_OK;
 }
 
@@ -477,34 +707,41 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
   int sms = 0;
   if ((s = current_device(&sms)) != RF_OK) return s;
   if ((s = set_smem_attr(reinterpret_cast<const void*>(&k_chol_base), kBlkSmem, &g_chol_attr)) != RF_OK) return s;
-  if ((s = set_smem_attr(reinterpret_cast<const void*>(&k_trinv_base), kBlkSmem, &g_trinv_attr)) != RF_OK) return s;
+  if ((s = set_smem_attr(reinterpret_cast<const void*>(&k_trinv_base), 2 * kBlkSmem, &g_trinv_attr)) != RF_OK) return s;
 
   const int di = static_cast<int>(desc->d_in), dout = static_cast<int>(desc->d_out), P = static_cast<int>(desc->n_maps);
   SolveCtx c{static_cast<cudaStream_t>(stream), sms, lay.tmp, lay.tmp2, dev_status};
-  ProfScope prof(c.s, RF_STAGE_SOLVE);
   const int eb = 8 * sms;
-  k_means<<<eb, 256, 0, c.s>>>(st->sx, st->sy, st->n, di, static_cast<long long>(P) * dout, lay.mu_x, lay.mu_y, lay.n);
-  k_trace_alpha<<<1, 1024, 0, c.s>>>(st->G, lay.mu_x, lay.n, di, lambda, alpha_mode, lay.alpha, alpha_out);
-  k_build_h<<<eb, 256, 0, c.s>>>(st->G, lay.mu_x, lay.n, lay.alpha, di, lay.H64, lay.L);
-  const long long ctotal = static_cast<long long>(P) * di * dout;
-  k_centre_c<<<eb, 256, 0, c.s>>>(st->C, lay.mu_x, lay.mu_y, lay.n, di, dout, ctotal, lay.work);
-  if ((s = cuda_check(cudaGetLastError(), "solve set-up launches")) != RF_OK) return s;
+  {
+    ProfScope pf(c.s, RF_STAGE_SOLVE);
+    k_means<<<eb, 256, 0, c.s>>>(st->sx, st->sy, st->n, di, static_cast<long long>(P) * dout, lay.mu_x, lay.mu_y, lay.n);
+    k_trace_alpha<<<1, 1024, 0, c.s>>>(st->G, lay.mu_x, lay.n, di, lambda, alpha_mode, lay.alpha, alpha_out);
+    k_build_h<<<eb, 256, 0, c.s>>>(st->G, lay.mu_x, lay.n, lay.alpha, di, lay.H64, lay.L);
+    const long long ctotal = static_cast<long long>(P) * di * dout;
+    k_centre_c<<<eb, 256, 0, c.s>>>(st->C, lay.mu_x, lay.mu_y, lay.n, di, dout, ctotal, lay.work);
+    if ((s = cuda_check(cudaGetLastError(), "solve set-up launches")) != RF_OK) return s;
 
-  // H = L Lᵀ ; L^-1 ; H^-1 = L^-ᵀ L^-1
-  if ((s = chol_lower(c, lay.L, di, di, lay.Linv)) != RF_OK) return s;
-  if ((s = trinv_lower(c, lay.L, di, di, lay.Linv, di)) != RF_OK) return s;
-  if ((s = sgemm(c, true, false, di, di, di, 1.f, lay.Linv, di, 0, lay.Linv, di, 0, 0.f, lay.Hinv, di, 0, 1)) != RF_OK)
-    return s;
-  // A_p = Cc_pᵀ H^-1  (Cc_p stored [d_in][d_out])
-  if ((s = sgemm(c, true, false, dout, di, di, 1.f, lay.work, dout, static_cast<long long>(di) * dout, lay.Hinv, di, 0,
-                 0.f, A, di, static_cast<long long>(dout) * di, P)) != RF_OK)
-    return s;
+    // H = L Lᵀ ; L^-1 ; H^-1 = L^-ᵀ L^-1
+    if ((s = chol_lower(c, lay.L, di, di, lay.Linv)) != RF_OK) return s;
+    if ((s = trinv_lower(c, lay.L, di, di, lay.Linv, di)) != RF_OK) return s;
+    if ((s = sgemm(c, true, false, di, di, di, 1.f, lay.Linv, di, 0, lay.Linv, di, 0, 0.f, lay.Hinv, di, 0, 1)) != RF_OK)
+      return s;
+  }
+  // A_p = Cc_pᵀ H^-1  (Cc_p stored [d_in][d_out]); H^-1 is symmetric bit for bit
+  // (both triangles come from the same products in the same order).
+  {
+    ProfScope pp(c.s, RF_STAGE_SOLVE_PRODUCT);
+    if ((s = split_gemm(c, lay.work, true, lay.Hinv, P, dout, di, di, 1.f, 0.f, A, lay.planes_a, lay.planes_b)) !=
+        RF_OK)
+      return s;
+  }
   for (int it = 0; it < refine_iters; ++it) {
+    ProfScope pr(c.s, RF_STAGE_SOLVE_REFINE);
     dim3 g(di / 64, dout / 64, P);
     k_resid64<<<g, 256, 0, c.s>>>(dout, di, A, lay.H64, st->C, lay.mu_x, lay.mu_y, lay.n, lay.work);
     if ((s = cuda_check(cudaGetLastError(), "k_resid64 launch")) != RF_OK) return s;
-    if ((s = sgemm(c, false, false, dout, di, di, 1.f, lay.work, di, static_cast<long long>(dout) * di, lay.Hinv, di, 0,
-                   1.f, A, di, static_cast<long long>(dout) * di, P)) != RF_OK)
+    if ((s = split_gemm(c, lay.work, false, lay.Hinv, P, dout, di, di, 1.f, 1.f, A, lay.planes_a, lay.planes_b)) !=
+        RF_OK)
       return s;
   }
   const long long rows = static_cast<long long>(P) * dout;
