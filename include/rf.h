@@ -163,6 +163,8 @@ rf_status rf_fold_kv_weights(const rf_fill_desc* desc, const rf_bf16* gain,
 /* The fill. For every filled row t (t < N-T, exact_mask[t] == 0, ascending) and
  * every layer l = S + p:
  *   x̂ = A_p x_S[t] + b_p;  r = (mean(x̂²) + ε)^-1/2;  [k | v] = r · Wkv_p x̂;
+ *   k_h <- g_k,p ⊙ k_h / sqrt(mean(k_h²) + ε)   when desc->k_norm_gain is set;
+ *   v_h <- v_scale[p][h] · v_h                  when desc->v_scale is set;
  *   k_h <- RoPE(k_h, t + pos_offset) per head;
  *   k_cache[l][t][h][:] = bf16(k_h),  v_cache[l][t][h][:] = bf16(v_h).
  * Nothing else in the caches is written: not the tail, not exact rows, not
