@@ -187,13 +187,18 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# The sources the map GEMM is compiled from (its kernel is instantiated in fill.cu
+# only); a committed DRAM-traffic figure is valid while these hash the same.
+MAP_GEMM_SOURCES = ("api.cu", "epilogue.cuh", "fill.cu", "fill_gemm.cuh", "rf_device.cuh", "rf_host.h", "tc_gemm.cuh")
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ridge_map_kv_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in MAP_GEMM_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    h.update(b"rf.h\0" + open(os.path.join(ROOT, "include", "rf.h"), "rb").read())
     return h.hexdigest()[:16]
 
 
