@@ -357,12 +357,14 @@ def run_ours(args):
     # HBM-bound kernels of the step against the measured copy bandwidth:
     # gather = read n_fill rows of x_S + write Xf (n_fill rows, zero pad to the
     # 256-row unit); rope table = write 2 * n_prefix * hd/2 fp32; compaction =
-    # read the mask + write fill_idx.
+    # read the mask + write fill_idx; row_rms = read the map GEMM's d/256 partial
+    # sums per row and layer + write the row scale.
     n_prefix = cfg.N - cfg.T
     m_pad = -(-n_fill // 256) * 256
     hbm_bytes = {"gather": n_fill * di * 2 + m_pad * di * 2,
                  "rope_table": 2 * n_prefix * (cfg.hd // 2) * 4,
-                 "compact": n_prefix + n_fill * 4}
+                 "compact": n_prefix + n_fill * 4,
+                 "row_rms": P * (d // 256) * n_fill * 4 + P * n_fill * 4}
     hbm_kernels = {}
     for k, nbytes in hbm_bytes.items():
         ms_k = stage_avg.get(k)

@@ -93,7 +93,8 @@ enum rf_stage {
   RF_STAGE_EXPAND = 13,      /* int8 map codes -> bf16 before a layer's GEMM   */
   RF_STAGE_QUANTIZE = 14,    /* bf16 maps -> int8 codes and row scales         */
   RF_STAGE_SOLVE_PRODUCT = 15, /* solve: A_p = Cc_pᵀ H^-1 (split tensor-core GEMM) */
-  RF_STAGE_SOLVE_REFINE = 16   /* solve: fp64 residual and correction, per sweep */
+  RF_STAGE_SOLVE_REFINE = 16,  /* solve: fp64 residual and correction, per sweep */
+  RF_STAGE_ROW_RMS = 17        /* fill: per-row RMS scale from the map GEMM's sums */
 };
 rf_status rf_profile_start(int max_records);
 /* Diagnostic: runs the tensor-core GEMM kernel (cta_pair != 0: the CTA-pair

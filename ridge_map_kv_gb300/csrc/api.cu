@@ -236,6 +236,7 @@ const char* rf_stage_name(int s) {
     case RF_STAGE_QUANTIZE: return "int8_quantize";
     case RF_STAGE_SOLVE_PRODUCT: return "solve_product";
     case RF_STAGE_SOLVE_REFINE: return "solve_refine";
+    case RF_STAGE_ROW_RMS: return "row_rms";
     default: return "unknown";
   }
 }

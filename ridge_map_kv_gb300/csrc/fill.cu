@@ -260,6 +260,20 @@ rf_status map_gemm(bool pair, const MapGemmArgs& a, int sms, cudaStream_t s) {
   return pair ? map_gemm_t<true>(a, sms, s) : map_gemm_t<false>(a, sms, s);
 }
 
+// Row RMS scale from the map GEMM's partial sums of squares: for each filled row
+// m and layer p, r = (Σ_j ssp[p][j][m] / d + ε)^-1/2, summed in the order j = 0, 1,
+// ... and stored in place in slot j = 0 (each thread reads its own row's slots
+// before writing), so the K/V epilogue reads one float per row.
+__global__ void __launch_bounds__(256) k_row_rms(float* __restrict__ ssp, const int32_t* __restrict__ n_fill, int n_ss,
+                                                 int M_pad, float inv_d, float eps) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= *n_fill) return;
+  float* sp = ssp + static_cast<size_t>(blockIdx.y) * n_ss * M_pad + m;
+  float s = 0.f;
+  for (int j = 0; j < n_ss; ++j) s += sp[static_cast<size_t>(j) * M_pad];
+  sp[0] = rsqrtf(fmaf(s, inv_d, eps));
+}
+
 template <bool kPair>
 static rf_status kv_gemm_t(const KvGemmArgs& a, int sms, cudaStream_t s) {
   using Cfg = GemmCfg<kPair>;
@@ -291,6 +305,12 @@ static rf_status kv_gemm_t(const KvGemmArgs& a, int sms, cudaStream_t s) {
   pr.dev_status = a.dev_status;
   pr.timeout_ns = wait_timeout_ns();
   const int64_t m_tiles_max = a.M_pad / Cfg::kUnitM;
+  {
+    ProfScope prof(s, RF_STAGE_ROW_RMS);
+    k_row_rms<<<dim3(static_cast<unsigned>((a.M_pad + 255) / 256), static_cast<unsigned>(a.P)), 256, 0, s>>>(
+        a.ssp, a.n_fill, pr.n_ss, pr.M_pad, pr.inv_d, pr.eps);
+  }
+  if ((st = cuda_check(cudaGetLastError(), "k_row_rms launch")) != RF_OK) return st;
   ProfScope prof(s, RF_STAGE_KV_GEMM);
   return launch_gemm(pr, a.P * m_tiles_max * pr.n_ntiles, sms, s, "K/V GEMM launch");
 }

@@ -131,7 +131,7 @@ struct KVProb {
   CUtensorMap tmB;
   const int32_t* n_fill;
   const int32_t* fill_idx;
-  const float* ssp;        // [P][d/256][M_pad]
+  const float* ssp;        // [P][d/256][M_pad]; slot 0 holds the row scale r after k_row_rms
   const float* rope_cos;   // [n_prefix][hd/2]
   const float* rope_sin;
   __nv_bfloat16* kc;
@@ -189,10 +189,7 @@ struct KVProb {
     float rs = 0.f;
     if (valid) {
       t = fill_idx[m];
-      const float* sp = ssp + static_cast<size_t>(p) * n_ss * M_pad + m;
-      float s = 0.f;
-      for (int j = 0; j < n_ss; ++j) s += sp[static_cast<size_t>(j) * M_pad];
-      rs = rsqrtf(fmaf(s, inv_d, eps));
+      rs = ssp[static_cast<size_t>(p) * n_ss * M_pad + m];  // the row's RMS scale (k_row_rms)
     }
     const size_t row_off = static_cast<size_t>(S + p) * layer_stride + static_cast<size_t>(t) * row_stride;
     const int half = hd >> 1;
@@ -254,7 +251,7 @@ rf_status map_gemm(bool pair, const MapGemmArgs& a, int sms, cudaStream_t s);
 // scatter), also launched from fill.cu only. Layers S .. S+P-1 of the caches.
 struct KvGemmArgs {
   const __nv_bfloat16* xhat;  // [P][M_pad][d]
-  const float* ssp;           // [P][d/256][M_pad]
+  float* ssp;                 // [P][d/256][M_pad]; k_row_rms turns slot 0 into the row scale
   const int32_t* n_fill;
   const int32_t* fill_idx;
   const float* rope_cos;
