@@ -65,10 +65,17 @@ struct GramProb {
   // M-tiles fastest, so the CTAs in flight share one strip of Y_p.
   __device__ void decode(int u, bool& is_g, int& p, int& mt, int& nt) const {
     if (u < g_units) {
+      // Gram tiles on or above the diagonal only, column tile nt holding the
+      // (nt + 1) * r row tiles that reach it (r = 256 / kUnitM), M fastest:
+      // tiles before column nt number r * nt (nt + 1) / 2.
+      constexpr int rr = kBN / Cfg::kUnitM;
       is_g = true;
       p = 0;
-      nt = u / g_mt;
-      mt = u - nt * g_mt;
+      int c = static_cast<int>((sqrtf(8.0f * static_cast<float>(u) / rr + 1.0f) - 1.0f) * 0.5f);
+      while (rr * (c + 1) * (c + 2) / 2 <= u) ++c;
+      while (rr * c * (c + 1) / 2 > u) --c;
+      nt = c;
+      mt = u - rr * c * (c + 1) / 2;
     } else {
       is_g = false;
       u -= g_units;
@@ -141,6 +148,21 @@ struct GramProb {
   }
 };
 
+// G[i][j] = G[j][i] for i > j: the lower triangle from the upper one, through
+// 32 x 32 shared tiles (block (bx, by) writes rows by*32.., columns bx*32..).
+__global__ void __launch_bounds__(256) k_mirror_lower(double* __restrict__ G, int d) {
+  const int bx = blockIdx.x, by = blockIdx.y;
+  if (bx > by) return;
+  __shared__ double t[32][33];
+  for (int j = threadIdx.y; j < 32; j += 8)
+    t[j][threadIdx.x] = G[static_cast<size_t>(bx * 32 + j) * d + by * 32 + threadIdx.x];  // upper block (bx, by)
+  __syncthreads();
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int i = by * 32 + j, c = bx * 32 + threadIdx.x;
+    if (i > c) G[static_cast<size_t>(i) * d + c] = t[threadIdx.x][j];
+  }
+}
+
 // Column sums of `n_maps` row-major bf16 matrices [n_rows][ld] (map p at
 // base + p*map_stride): out[p][c] += Σ_t M_p[t][c]. One thread per column, 512
 // rows per block; fp32 over 64 rows, then fp64, then one fp64 atomic per block.
@@ -191,11 +213,16 @@ rf_status calib_gemm(const rf_calib_desc* desc, const rf_bf16* X, int64_t ld_x, 
   pr.g_mt = static_cast<int>(d_in / Cfg::kUnitM);
   pr.g_nt = static_cast<int>(d_in / kBN);
   pr.c_nt = static_cast<int>(P > 0 ? d_out / kBN : 0);
-  pr.g_units = pr.g_mt * pr.g_nt;
+  pr.g_units = (kBN / Cfg::kUnitM) * pr.g_nt * (pr.g_nt + 1) / 2;  // upper-triangle tiles
   pr.dev_status = dev_status;
   pr.timeout_ns = wait_timeout_ns();
   ProfScope prof(cs, RF_STAGE_CALIB_GEMM);
-  return launch_gemm(pr, pr.g_units + P * pr.g_mt * pr.c_nt, sms, cs, "calibration GEMM launch");
+  if ((s = launch_gemm(pr, pr.g_units + P * pr.g_mt * pr.c_nt, sms, cs, "calibration GEMM launch")) != RF_OK) return s;
+  // The GEMM accumulates G's tiles on and above the diagonal; the lower triangle
+  // becomes their mirror (the accumulated upper triangle is the whole sum).
+  k_mirror_lower<<<dim3(static_cast<unsigned>(d_in / 32), static_cast<unsigned>(d_in / 32)), dim3(32, 8), 0, cs>>>(
+      st->G, static_cast<int>(d_in));
+  return cuda_check(cudaGetLastError(), "k_mirror_lower launch");
 }
 
 }  // namespace rf
