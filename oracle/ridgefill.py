@@ -45,6 +45,14 @@ Readings where the pages leave a step open (each is listed in the design doc):
     q[o][i] = rint(A[o][i] / s[o]) (round half to even), both in float32 (the
     precision that decides the integers); a zero row has s = 0, q = 0. The map
     used is then A'[o][i] = s[o] q[o][i].
+  * Source selection ([XM] greedy forward selection by head-mean R²): a head's R²
+    is the share of its total centred variance (over its head_dim columns) that
+    the fit explains; the fit is the ridge regression with the mapper's lambda and
+    one alpha per kind from the Gram of all source features, and its explained
+    energy c_oᵀ(Gc_SS + alpha I)⁻¹c_o makes R² = 1 - (RSS + alpha|w|²)/TSS, the
+    least-squares R² at lambda = 0; keys and values share one set per target
+    layer, chosen by the mean of their head-mean R²; ties go to the lower layer
+    index; a head with zero variance has R² = 0.
 
 Parity status: every public function here is pinned by tests/test_oracle_pins.py
 against closed forms, invariants, textbook routines or brute force; none is
@@ -59,6 +67,7 @@ __all__ = [
     "map_predict", "fill_rows", "fill_kv", "calib_stats", "centre_stats",
     "ridge_alpha", "ridge_solve", "xmodel_features", "xmodel_map_layer",
     "fill_flops_per_row_layer", "value_scale", "quantize_rows_int8", "dequantize_rows_int8",
+    "selection_scores", "select_sources",
 ]
 
 
@@ -257,7 +266,8 @@ def fill_flops_per_row_layer(d: int, n_kv_heads: int, head_dim: int) -> int:
 def calib_stats(X, Ys) -> dict:
     """Raw one-pass sums over the rows of X [n, d_in] and Ys [P, n, d_out].
 
-    G = Σ_t x_t x_tᵀ,  C_p = Σ_t x_t y_{p,t}ᵀ,  sx = Σ_t x_t,  sy_p = Σ_t y_{p,t},  n.
+    G = Σ_t x_t x_tᵀ,  C_p = Σ_t x_t y_{p,t}ᵀ,  sx = Σ_t x_t,  sy_p = Σ_t y_{p,t},
+    syy_p = Σ_t y_{p,t}² (per column; the total sum of squares of R²),  n.
     """
     X = np.asarray(X, np.float64)
     Ys = np.asarray(Ys, np.float64)
@@ -266,13 +276,14 @@ def calib_stats(X, Ys) -> dict:
         "C": np.stack([X.T @ Ys[p] for p in range(Ys.shape[0])]),
         "sx": X.sum(axis=0),
         "sy": Ys.sum(axis=1),
+        "syy": (Ys * Ys).sum(axis=1),
         "n": int(X.shape[0]),
     }
 
 
 def add_stats(a: dict, b: dict) -> dict:
     """Sum of two sets of raw statistics (calibration is resumable by adding)."""
-    return {k: a[k] + b[k] for k in ("G", "C", "sx", "sy", "n")}
+    return {k: a[k] + b[k] for k in ("G", "C", "sx", "sy", "syy", "n") if k in a}
 
 
 def centre_stats(st: dict):
@@ -351,3 +362,98 @@ def xmodel_map_layer(k_src, v_src, src_layers, Wk, bk, Wv, bv, positions,
     vh = (FV @ np.asarray(Wv, np.float64).T + np.asarray(bv, np.float64)).reshape(n, n_kv_heads, head_dim)
     kh = rope(kc, np.asarray(positions, np.float64)[:, None], theta_tgt)
     return kh, vh
+
+
+# --------------------------------------------------------------------------- #
+# Cross-layer source selection ([XM] "소스 층은 몇 개가 필요한가": greedy forward
+# selection that adds, one at a time, the source layer raising the head-mean R²
+# most; "층 교차 소스 선택": the k layers are chosen per target layer by the
+# head-mean R² of the un-roped keys and of the values, and all heads of a target
+# layer share them; "헤드별 리지 회귀": the fit is the ridge regression of the
+# centred target on the concatenated features of the chosen layers)
+# --------------------------------------------------------------------------- #
+def _selection_system(st: dict, lam: float, alpha_mode: str):
+    """Centred Gram, cross terms and per-column total sums of squares of one kind.
+
+    TSS_p[o] = Σ_t (y_{p,t,o} - mu_p[o])² = syy_p[o] - n mu_p[o]²; alpha is taken
+    once from the Gram of ALL source features (reading: every candidate set of the
+    selection is scored under the same penalty).
+    """
+    Gc, Cc, _, mu_y = centre_stats(st)
+    tss = st["syy"] - float(st["n"]) * mu_y * mu_y
+    return Gc, Cc, tss, ridge_alpha(Gc, lam, alpha_mode)
+
+
+def _head_mean_r2(explained: np.ndarray, tss: np.ndarray, head_dim: int) -> float:
+    """Mean over heads of R²_h = Σ_{o in h} explained[o] / Σ_{o in h} TSS[o].
+
+    A head is its head_dim columns: its R² is the share of its total centred
+    variance that the fit explains. A head with zero variance counts as R²_h = 0.
+    """
+    e = explained.reshape(-1, head_dim).sum(axis=1)
+    t = tss.reshape(-1, head_dim).sum(axis=1)
+    r = np.where(t > 0, e / np.where(t > 0, t, 1.0), 0.0)
+    return float(r.mean())
+
+
+def selection_scores(stats, layers, F: int, head_dim: int, lam: float, alpha_mode: str = "trace"):
+    """Head-mean R² of every target map fitted on the features of ``layers``.
+
+    ``stats`` is one statistics dict per kind (keys, values), each with d_in = L_src*F
+    and n_maps target layers. For each kind and map p the fit is the ridge
+    regression on the columns of the chosen layers (in the listed order); with
+    H = Gc_SS + alpha I and c_o the cross terms of output column o, the explained
+    energy is c_oᵀ H⁻¹ c_o, so R² = 1 - (RSS + alpha |w|²) / TSS (the least-squares
+    R² when alpha = 0). Returns [n_kinds, n_maps].
+    """
+    idx = np.concatenate([np.arange(s * F, (s + 1) * F) for s in layers])
+    out = []
+    for st in stats:
+        Gc, Cc, tss, alpha = _selection_system(st, lam, alpha_mode)
+        H = Gc[np.ix_(idx, idx)] + alpha * np.eye(idx.size)
+        row = []
+        for p in range(Cc.shape[0]):
+            c = Cc[p][idx, :]
+            explained = (c * np.linalg.solve(H, c)).sum(axis=0)
+            row.append(_head_mean_r2(explained, tss[p], head_dim))
+        out.append(row)
+    return np.asarray(out)
+
+
+def select_sources(stats, L_src: int, F: int, head_dim: int, k: int, lam: float,
+                   alpha_mode: str = "trace", path=None):
+    """Greedy forward selection of k source layers for every target layer.
+
+    Step j scores every layer s not yet chosen by the head-mean R² of the fit on
+    the chosen layers plus s (``selection_scores``), for each kind; the joint score
+    is the mean over kinds, and the layer with the highest joint score is added
+    (the lowest index among equal scores). ``path`` [n_maps, k] replays given
+    choices instead, and the scores are then those along that path.
+
+    Returns (sel [n_maps, k] int, table [n_kinds, n_maps, k, L_src]) where table
+    holds each candidate's score at each step and NaN for layers already chosen.
+    """
+    systems = [_selection_system(st, lam, alpha_mode) for st in stats]
+    n_maps = systems[0][1].shape[0]
+    sel = np.zeros((n_maps, k), np.int64)
+    table = np.full((len(stats), n_maps, k, L_src), np.nan)
+    for p in range(n_maps):
+        chosen = []
+        for j in range(k):
+            for s in range(L_src):
+                if s in chosen:
+                    continue
+                idx = np.concatenate([np.arange(c * F, (c + 1) * F) for c in chosen + [s]])
+                for kind, (Gc, Cc, tss, alpha) in enumerate(systems):
+                    H = Gc[np.ix_(idx, idx)] + alpha * np.eye(idx.size)
+                    c = Cc[p][idx, :]
+                    explained = (c * np.linalg.solve(H, c)).sum(axis=0)
+                    table[kind, p, j, s] = _head_mean_r2(explained, tss[p], head_dim)
+            joint = table[:, p, j, :].mean(axis=0)      # NaN for layers already chosen
+            if path is None:
+                b = int(np.nanargmax(joint))
+            else:
+                b = int(path[p][j])
+            chosen.append(b)
+            sel[p, j] = b
+    return sel, table

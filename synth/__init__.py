@@ -16,6 +16,14 @@ Recipe (one per workload):
   * cross-model: source K, V ~ N(0, 1), W ~ N(0, 1/(k H hd)), b ~ N(0, 0.1^2);
     target layer j reads the k consecutive source layers starting at
     clamp(round(j (L_src - 1)/(L_tgt - 1)) - k/2 + 1, 0, L_src - k).
+  * source selection: a latent random walk over source depth, r_0 ~ N(0, I_R),
+    r_s = r_{s-1} + 0.5 N(0, I_R); source layer s's features (un-roped keys, or
+    values) are r_s P_s + 0.3 N(0, 1) + mu_x with P_s ~ N(0, 1/R); target layer t
+    at depth a = floor(t (L_src - 1)/(L_tgt - 1)) is r_a M_1 + 0.6 r_{a+1} M_2 +
+    0.3 r_c M_3 + 0.3 N(0, 1) + mu_y (c = a + L_src/2 mod L_src, M ~ N(0, 1/R)),
+    so nearby layers carry most of a target and far ones a little; keys and values
+    share the walk and draw their own loadings. Raw rows are drawn from this
+    model; the full-size case uses its exact population sums instead.
 Seeds: base = 20261202 + workload index; one sub-seed per named tensor.
 """
 from __future__ import annotations
@@ -116,13 +124,47 @@ XMODEL = XModelConfig("xmodel 40->64 layers 8x128 k8 N32768", 4, L_src=40, L_tgt
 FLASH_NEXT = FillConfig("flash-next-shaped maps d_in10240 d2560 L48 S24 N32768 T2048", 5, d=2560, L=48, S=24,
                         N=32768, T=2048, H=2, hd=128, rope_theta=1.0e6, exact=None, lam=0.03, calib_n=0,
                         d_in=10240)
+
+
+@dataclasses.dataclass(frozen=True)
+class SelectConfig:
+    """Greedy source-layer selection: L_src candidate layers of H x hd features,
+    L_tgt target layers of H x hd columns, k layers chosen per target."""
+    name: str
+    index: int
+    L_src: int
+    L_tgt: int
+    k: int
+    H: int
+    hd: int
+    n: int                   # calibration rows
+    R: int                   # latent width of the random walk
+    lam: float
+    sigma: float = 0.3
+
+    @property
+    def F(self) -> int:
+        return self.H * self.hd
+
+    @property
+    def D(self) -> int:
+        return self.L_src * self.F
+
+
+# Small case the oracle finishes in seconds; the pages' 40 -> 64 layer pair with
+# k = 8, 8 x 128 heads and ~128K calibration rows ([XM] calibration setup).
+SELECT_SMALL = SelectConfig("selection 6->4 layers 2x128 k3", 6, L_src=6, L_tgt=4, k=3, H=2, hd=128,
+                            n=4096, R=32, lam=0.01)
+SELECT_XMODEL = SelectConfig("selection 40->64 layers 8x128 k8 n131072", 7, L_src=40, L_tgt=64, k=8, H=8,
+                             hd=128, n=131072, R=64, lam=0.01)
 FILL_CONFIGS = {"toy": TOY, "llama8b": LLAMA8B, "qwen3_8b": QWEN3_8B, "dense27b": DENSE27B,
                 "flash_next": FLASH_NEXT}
 
 _TENSOR_IDS = {name: i for i, name in enumerate(
     ["x_S", "mask", "A", "b", "gain", "Wk", "Wv", "calib_X", "calib_Atrue", "calib_btrue",
      "calib_noise", "k_src", "v_src", "xWk", "xWv", "xbk", "xbv", "cache", "extra",
-     "rescale_scale", "rescale_noise", "key_norm_gain"])}
+     "rescale_scale", "rescale_noise", "key_norm_gain", "sel_P", "sel_M", "sel_mu", "sel_latent",
+     "sel_noise"])}
 
 
 def sub_seed(index: int, tensor: str, salt: int = 0) -> int:
@@ -295,3 +337,72 @@ def bits(t: torch.Tensor) -> np.ndarray:
 
 def f32(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu").contiguous().numpy()
+
+
+# --------------------------------------------------------------------------- #
+# Source selection inputs (latent random-walk model; see the recipe above)
+# --------------------------------------------------------------------------- #
+def _walk_scale(l: int) -> float:
+    return 1.0 if l == 0 else 0.5
+
+
+def selection_loadings(cfg: SelectConfig, kind: int, device="cpu") -> dict:
+    """Loadings of the model on the independent standard walk steps e_0..e_{L_src-1}
+    (r_s = sum_{l <= s} c_l e_l): Z [L_src R, D] for the source features and
+    W [L_tgt, L_src R, F] for the targets, plus the means (float32)."""
+    L, R, F = cfg.L_src, cfg.R, cfg.F
+    P = _randn((L, R, F), sub_seed(cfg.index, "sel_P", kind), device, std=1 / math.sqrt(R), dtype=torch.float32)
+    M = _randn((cfg.L_tgt, 3, R, F), sub_seed(cfg.index, "sel_M", kind), device, std=1 / math.sqrt(R),
+               dtype=torch.float32)
+    Z = torch.zeros((L * R, L * F), dtype=torch.float32, device=device)
+    for s in range(L):
+        for l in range(s + 1):
+            Z[l * R:(l + 1) * R, s * F:(s + 1) * F] = _walk_scale(l) * P[s]
+    W = torch.zeros((cfg.L_tgt, L * R, F), dtype=torch.float32, device=device)
+    for t in range(cfg.L_tgt):
+        a = (t * (L - 1)) // max(cfg.L_tgt - 1, 1)
+        for depth, m, wgt in ((a, 0, 1.0), (min(a + 1, L - 1), 1, 0.6), ((a + L // 2) % L, 2, 0.3)):
+            for l in range(depth + 1):
+                W[t, l * R:(l + 1) * R] += (wgt * _walk_scale(l)) * M[t, m]
+    mu = _randn((L * F + cfg.L_tgt * F,), sub_seed(cfg.index, "sel_mu", kind), device, std=0.1,
+                dtype=torch.float32)
+    return {"Z": Z, "W": W, "mu_x": mu[:L * F], "mu_y": mu[L * F:].view(cfg.L_tgt, F)}
+
+
+def selection_rows(cfg: SelectConfig, kind: int, rows: int, chunk: int = 0, device="cpu",
+                   loadings: Optional[dict] = None) -> dict:
+    """One chunk of calibration rows: X [rows, D] bf16 (all source layers side by
+    side) and Y [L_tgt, rows, F] bf16. The walk steps depend on the chunk only, so
+    keys (kind 0) and values (kind 1) of a chunk come from the same walk."""
+    ld = selection_loadings(cfg, kind, device) if loadings is None else loadings
+    e = _randn((rows, cfg.L_src * cfg.R), sub_seed(cfg.index, "sel_latent", chunk), device, dtype=torch.float32)
+    X = e @ ld["Z"]
+    X += _randn((rows, cfg.D), sub_seed(cfg.index, "sel_noise", 2 * chunk + 64 * kind), device,
+                std=cfg.sigma, dtype=torch.float32)
+    X += ld["mu_x"]
+    Y = torch.empty((cfg.L_tgt, rows, cfg.F), dtype=torch.bfloat16, device=device)
+    noise = _randn((cfg.L_tgt, rows, cfg.F), sub_seed(cfg.index, "sel_noise", 2 * chunk + 1 + 64 * kind), device,
+                   std=cfg.sigma, dtype=torch.float32)
+    for t in range(cfg.L_tgt):
+        Y[t] = (e @ ld["W"][t] + noise[t] + ld["mu_y"][t]).to(torch.bfloat16)
+    return {"X": X.to(torch.bfloat16), "Y": Y}
+
+
+def selection_population_stats(cfg: SelectConfig, kind: int, device="cpu", loadings: Optional[dict] = None) -> dict:
+    """The model's exact sums over cfg.n rows, as float64 tensors:
+    G = n (ZᵀZ + sigma² I + mu_x mu_xᵀ), C_t = n (Zᵀ W_t + mu_x mu_tᵀ), sx = n mu_x,
+    sy_t = n mu_t, syy_t = n (diag(W_tᵀW_t) + sigma² + mu_t²). Products in float32."""
+    ld = selection_loadings(cfg, kind, device) if loadings is None else loadings
+    n = float(cfg.n)
+    Z, W, mx, my = ld["Z"], ld["W"], ld["mu_x"], ld["mu_y"]
+    G = (Z.T @ Z).to(torch.float64)
+    G.diagonal().add_(cfg.sigma ** 2)
+    G += torch.outer(mx.double(), mx.double())
+    G *= n
+    C = torch.empty((cfg.L_tgt, cfg.D, cfg.F), dtype=torch.float64, device=device)
+    for t in range(cfg.L_tgt):
+        C[t] = (Z.T @ W[t]).double() + torch.outer(mx.double(), my[t].double())
+    C *= n
+    syy = ((W * W).sum(dim=1).double() + cfg.sigma ** 2 + my.double() ** 2) * n
+    return {"G": G, "C": C, "sx": mx.double() * n, "sy": my.double() * n, "syy": syy,
+            "n": torch.tensor([cfg.n], dtype=torch.int64, device=device)}

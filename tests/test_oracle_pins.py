@@ -688,3 +688,167 @@ def test_int8_zero_row_power_of_two_scaling_and_half_even_ties():
     q2, s2 = O.quantize_rows_int8(A * np.float32(8.0))
     np.testing.assert_array_equal(q2, q)
     np.testing.assert_array_equal(s2, s * 8)
+
+
+# --------------------------------------------------------------------------- #
+# Cross-layer source selection (greedy forward selection by head-mean R²)
+# --------------------------------------------------------------------------- #
+def _layered_rows(n, L_src, F, P, Ft, seed, noise=0.3):
+    """Tiny raw calibration rows: source features [n, L_src*F] from a random walk
+    over layers, targets [P, n, Ft] as noisy linear functions of two layers."""
+    rng = np.random.default_rng(seed)
+    R = 3
+    r = [rng.standard_normal((n, R))]
+    for _ in range(1, L_src):
+        r.append(r[-1] + 0.7 * rng.standard_normal((n, R)))
+    X = np.concatenate([r[s] @ rng.standard_normal((R, F)) + noise * rng.standard_normal((n, F))
+                        for s in range(L_src)], axis=1) + 0.5
+    Ys = np.stack([r[p % L_src] @ rng.standard_normal((R, Ft)) + r[(p + 2) % L_src] @ rng.standard_normal((R, Ft))
+                   + noise * rng.standard_normal((n, Ft)) - 1.0 for p in range(P)])
+    return X, Ys
+
+
+def _head_r2_from_fit(Y, Yhat, head_dim, penalty=None):
+    """Head-mean R² straight from rows: 1 - (‖Y_h - Ŷ_h‖² + penalty_h) / ‖Y_h - Ȳ_h‖²."""
+    res = ((Y - Yhat) ** 2).sum(axis=0)
+    if penalty is not None:
+        res = res + penalty
+    tot = ((Y - Y.mean(axis=0)) ** 2).sum(axis=0)
+    rh = 1.0 - res.reshape(-1, head_dim).sum(axis=1) / tot.reshape(-1, head_dim).sum(axis=1)
+    return rh.mean()
+
+
+def _cols(layers, F):
+    return np.concatenate([np.arange(s * F, (s + 1) * F) for s in layers])
+
+
+def test_selection_score_is_least_squares_r2_of_the_rows():
+    # lambda = 0: the score of a set is the head-mean R² of an ordinary least-squares
+    # fit with an intercept column, solved by lstsq from the raw rows.
+    n, L, F, P, Ft, hd = 300, 4, 3, 2, 4, 2
+    X, Ys = _layered_rows(n, L, F, P, Ft, seed=7)
+    st = O.calib_stats(X, Ys)
+    for layers in ([1], [3, 0], [2, 1, 3]):
+        got = O.selection_scores([st], layers, F, hd, 0.0, "absolute")[0]
+        Z = np.concatenate([X[:, _cols(layers, F)], np.ones((n, 1))], axis=1)
+        for p in range(P):
+            w, *_ = np.linalg.lstsq(Z, Ys[p], rcond=None)
+            assert abs(got[p] - _head_r2_from_fit(Ys[p], Z @ w, hd)) < 1e-10
+
+
+@pytest.mark.parametrize("mode", ["absolute", "trace"])
+def test_selection_score_is_one_minus_ridge_objective_over_tss(mode):
+    # lambda > 0: with alpha from the centred Gram of ALL source features (trace mode)
+    # or alpha = lambda, the score is 1 - (RSS + alpha |w|²)/TSS per head, w being the
+    # ridge solution of the centred rows, solved as the augmented least-squares
+    # problem [Xc; sqrt(alpha) I] w = [Yc; 0] (a textbook identity).
+    n, L, F, P, Ft, hd = 250, 4, 3, 2, 4, 2
+    X, Ys = _layered_rows(n, L, F, P, Ft, seed=8)
+    st = O.calib_stats(X, Ys)
+    lam = 0.3
+    Xc = X - X.mean(axis=0)
+    alpha = lam * np.trace(Xc.T @ Xc) / Xc.shape[1] if mode == "trace" else lam
+    layers = [2, 0]
+    got = O.selection_scores([st], layers, F, hd, lam, mode)[0]
+    Xs = Xc[:, _cols(layers, F)]
+    aug = np.concatenate([Xs, math.sqrt(alpha) * np.eye(Xs.shape[1])], axis=0)
+    for p in range(P):
+        Yc = Ys[p] - Ys[p].mean(axis=0)
+        w, *_ = np.linalg.lstsq(aug, np.concatenate([Yc, np.zeros((Xs.shape[1], Ft))]), rcond=None)
+        want = _head_r2_from_fit(Yc, Xs @ w, hd, penalty=alpha * (w ** 2).sum(axis=0))
+        assert abs(got[p] - want) < 1e-10
+
+
+def test_single_feature_score_is_squared_correlation():
+    # One feature per layer, one column per head, lambda = 0: R² = Pearson r².
+    rng = np.random.default_rng(9)
+    n = 500
+    X = rng.standard_normal((n, 3))
+    X[:, 1] += 0.8 * X[:, 0]
+    Y = (0.6 * X[:, 0] - 0.3 * X[:, 2] + rng.standard_normal(n))[None, :, None]
+    st = O.calib_stats(X, Y)
+    for s in range(3):
+        got = O.selection_scores([st], [s], 1, 1, 0.0, "absolute")[0, 0]
+        assert abs(got - np.corrcoef(X[:, s], Y[0, :, 0])[0, 1] ** 2) < 1e-12
+
+
+def test_greedy_path_is_the_argmax_of_least_squares_r2_at_every_step():
+    # Brute force: at every step, fit every remaining layer added to the chosen ones
+    # by lstsq from the rows; the oracle's table must hold those scores and its
+    # choice must be their argmax.
+    n, L, F, P, Ft, hd, k = 400, 5, 2, 3, 4, 2, 4
+    X, Ys = _layered_rows(n, L, F, P, Ft, seed=10)
+    st = O.calib_stats(X, Ys)
+    sel, table = O.select_sources([st], L, F, hd, k, 0.0, "absolute")
+    for p in range(P):
+        chosen = []
+        for j in range(k):
+            scores = np.full(L, -np.inf)
+            for s in range(L):
+                if s in chosen:
+                    assert np.isnan(table[0, p, j, s])
+                    continue
+                Z = np.concatenate([X[:, _cols(chosen + [s], F)], np.ones((n, 1))], axis=1)
+                w, *_ = np.linalg.lstsq(Z, Ys[p], rcond=None)
+                scores[s] = _head_r2_from_fit(Ys[p], Z @ w, hd)
+                assert abs(table[0, p, j, s] - scores[s]) < 1e-10
+            assert sel[p, j] == int(np.argmax(scores))
+            chosen.append(int(sel[p, j]))
+        assert sorted(chosen) == sorted(set(chosen))
+
+
+def test_planted_source_layers_are_found_and_explain_everything():
+    # A noise-free target built from layers 3 (larger weight) and 1 is explained
+    # exactly by them: the path starts [3, 1] and the step-2 score is 1.
+    rng = np.random.default_rng(11)
+    n, L, F = 600, 5, 4
+    X = rng.standard_normal((n, L * F))
+    Y = (3.0 * X[:, 12:16] @ rng.standard_normal((4, 4)) + X[:, 4:8] @ rng.standard_normal((4, 4)))[None]
+    st = O.calib_stats(X, Y)
+    sel, table = O.select_sources([st], L, F, 2, 3, 0.0, "absolute")
+    assert list(sel[0, :2]) == [3, 1]
+    assert abs(table[0, 0, 1, 1] - 1.0) < 1e-10
+    assert np.all(table[0, 0, 0, [0, 1, 2, 4]] < table[0, 0, 0, 3])
+
+
+def test_selection_is_equivariant_under_layer_permutation():
+    n, L, F, P, Ft, hd, k = 300, 5, 2, 2, 4, 2, 3
+    X, Ys = _layered_rows(n, L, F, P, Ft, seed=12)
+    perm = np.array([3, 0, 4, 1, 2])          # new layer i is old layer perm[i]
+    Xp = np.concatenate([X[:, perm[i] * F:(perm[i] + 1) * F] for i in range(L)], axis=1)
+    s0, t0 = O.select_sources([O.calib_stats(X, Ys)], L, F, hd, k, 0.05)
+    s1, t1 = O.select_sources([O.calib_stats(Xp, Ys)], L, F, hd, k, 0.05)
+    np.testing.assert_array_equal(perm[s1], s0)
+    np.testing.assert_allclose(t1, t0[..., perm], atol=1e-10)
+
+
+def test_joint_selection_averages_the_kinds():
+    # Two identical kinds select like one. With two different kinds, each kind's table
+    # entry is that kind's own score of the set, and each step takes the argmax of
+    # the mean of the two tables.
+    n, L, F, P, Ft, hd, k = 300, 4, 2, 2, 4, 2, 3
+    X, Ys = _layered_rows(n, L, F, P, Ft, seed=13)
+    X2, Ys2 = _layered_rows(n, L, F, P, Ft, seed=14)
+    a, b = O.calib_stats(X, Ys), O.calib_stats(X2, Ys2)
+    s1, t1 = O.select_sources([a], L, F, hd, k, 0.01)
+    s2, t2 = O.select_sources([a, a], L, F, hd, k, 0.01)
+    np.testing.assert_array_equal(s1, s2)
+    np.testing.assert_allclose(t2[1], t1[0], atol=0)
+    sj, tj = O.select_sources([a, b], L, F, hd, k, 0.01)
+    for p in range(P):
+        chosen = []
+        for j in range(k):
+            sa = O.selection_scores([a], chosen + [int(sj[p, j])], F, hd, 0.01)[0, p]
+            sb = O.selection_scores([b], chosen + [int(sj[p, j])], F, hd, 0.01)[0, p]
+            assert abs(tj[0, p, j, sj[p, j]] - sa) < 1e-12 and abs(tj[1, p, j, sj[p, j]] - sb) < 1e-12
+            assert sj[p, j] == int(np.nanargmax(tj[:, p, j].mean(axis=0)))
+            chosen.append(int(sj[p, j]))
+
+
+def test_calibration_sum_of_squares_gives_total_variance():
+    rng = np.random.default_rng(15)
+    X = rng.standard_normal((100, 4))
+    Y = rng.standard_normal((2, 100, 3)) * 2 + 1
+    st = O.add_stats(O.calib_stats(X[:60], Y[:, :60]), O.calib_stats(X[60:], Y[:, 60:]))
+    tss = st["syy"] - st["n"] * (st["sy"] / st["n"]) ** 2
+    np.testing.assert_allclose(tss, Y.var(axis=1) * 100, rtol=1e-12)
