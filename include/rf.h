@@ -94,7 +94,11 @@ enum rf_stage {
   RF_STAGE_QUANTIZE = 14,    /* bf16 maps -> int8 codes and row scales         */
   RF_STAGE_SOLVE_PRODUCT = 15, /* solve: A_p = Cc_pᵀ H^-1 (split tensor-core GEMM) */
   RF_STAGE_SOLVE_REFINE = 16,  /* solve: fp64 residual and correction, per sweep */
-  RF_STAGE_ROW_RMS = 17        /* fill: per-row RMS scale from the map GEMM's sums */
+  RF_STAGE_ROW_RMS = 17,       /* fill: per-row RMS scale from the map GEMM's sums */
+  RF_STAGE_SELECT_GEMM = 18,   /* source selection: split tensor-core products    */
+  RF_STAGE_SELECT_FACTOR = 19, /* source selection: batched Cholesky and inverse  */
+  RF_STAGE_SELECT_SCORE = 20,  /* source selection: set-up, scores, argmax, copies */
+  RF_STAGE_SELECT_SPLIT = 21   /* source selection: fp32 -> three bf16 planes      */
 };
 rf_status rf_profile_start(int max_records);
 /* Diagnostic: runs the tensor-core GEMM kernel (cta_pair != 0: the CTA-pair
@@ -299,11 +303,13 @@ typedef struct rf_calib_desc {
 } rf_calib_desc;
 
 /* Raw one-pass sums, all device fp64 (n as int64), caller-owned.
- *   G  [d_in][d_in]         Σ x xᵀ   (both triangles)
- *   C  [n_maps][d_in][d_out] Σ x y_pᵀ
- *   sx [d_in]               Σ x
- *   sy [n_maps][d_out]      Σ y_p
- *   n  [1]                  rows seen
+ *   G   [d_in][d_in]          Σ x xᵀ   (both triangles)
+ *   C   [n_maps][d_in][d_out] Σ x y_pᵀ
+ *   sx  [d_in]                Σ x
+ *   sy  [n_maps][d_out]       Σ y_p
+ *   n   [1]                   rows seen
+ *   syy [n_maps][d_out]       Σ y_p² per column (optional, NULL = not kept; the
+ *                             total sums of squares that rf_select_sources needs)
  * Zero them to start; saved and reloaded sums resume accumulation. */
 typedef struct rf_calib_stats {
   double* G;
@@ -311,12 +317,14 @@ typedef struct rf_calib_stats {
   double* sx;
   double* sy;
   int64_t* n;
+  double* syy;
 } rf_calib_stats;
 
 /* Supported: d_in % 128 == 0, d_out % 256 == 0 (or n_maps == 0), n_rows % 8 == 0. */
 size_t rf_calib_workspace_bytes(const rf_calib_desc* desc, int64_t n_rows);
 
-/* Adds one batch of rows: G += XᵀX, C_p += XᵀY_p, sx += Σx, sy_p += Σy_p, n += n_rows.
+/* Adds one batch of rows: G += XᵀX, C_p += XᵀY_p, sx += Σx, sy_p += Σy_p, n += n_rows
+ * (and syy_p += Σy_p² when stats->syy is set).
  *   X [n_rows][ld_x] bf16; Y_p at Y + p*y_map_stride, [n_rows][ld_y] bf16.
  * Products are exact in fp32, summed in fp32 over chunks of rows on the tensor
  * cores and added to the fp64 totals. */
@@ -392,6 +400,62 @@ rf_status rf_xmodel_map(const rf_xmodel_desc* desc, const int32_t* src_layers,
 rf_status rf_rope_rows(const rf_bf16* in, rf_bf16* out, int64_t n_rows, int64_t ld,
                        int64_t n_heads, int64_t head_dim, double theta,
                        int64_t pos_offset, int inverse, rf_stream_t stream);
+
+/* Side-by-side features of several layers, for cross-model calibration:
+ *   out[t][l*W + j] = f(src[l*layer_stride + t*ld_src + j]),  W = n_heads*head_dim,
+ *   f = inverse RoPE at position t + pos_offset with base theta (theta > 0: keys)
+ *   or the identity (theta == 0: values), for l < n_layers, t < n_rows, j < W.
+ * src, out bf16 device; ld_src >= W, ld_out >= n_layers*W, strides multiples of 8.
+ * [XM] "층 교차 소스 선택": a target layer's features are all heads of its source
+ * layers side by side; content-space mapping: keys are un-roped first. */
+rf_status rf_concat_layers(const rf_bf16* src, int64_t n_layers, int64_t layer_stride,
+                           int64_t n_rows, int64_t ld_src, int64_t n_heads, int64_t head_dim,
+                           double theta, int64_t pos_offset,
+                           rf_bf16* out, int64_t ld_out, rf_stream_t stream);
+
+/* ===================================================================== *
+ * Cross-layer source selection ([XM] "소스 층은 몇 개가 필요한가": greedy
+ * forward selection adding the source layer that raises the head-mean R² most;
+ * "층 교차 소스 선택": k layers per target layer, chosen by the head-mean R² of
+ * the un-roped keys and of the values, shared by all heads of the target layer)
+ * ===================================================================== */
+typedef struct rf_select_desc {
+  int64_t L_src;      /* candidate source layers                                       */
+  int64_t F;          /* features per source layer (the statistics' d_in = L_src * F)  */
+  int64_t n_targets;  /* target layers (the statistics' n_maps)                        */
+  int64_t d_out;      /* columns per target layer                                      */
+  int64_t head_dim;   /* columns per target head; R² is averaged over d_out/head_dim   */
+  int64_t k;          /* layers chosen per target layer, 1 <= k <= L_src               */
+  int64_t n_kinds;    /* statistics sets scored together: 1, or 2 (keys and values)    */
+  int64_t group;      /* target layers per pass, 0 = all; the workspace grows with it  */
+  uint64_t flags;     /* RF_FLAG_* (0 = defaults)                                      */
+} rf_select_desc;
+
+/* Supported: F % 256 == 0, d_out % 256 == 0, d_out % head_dim == 0,
+ * L_src * F <= 65536, n_targets <= 65535. */
+size_t rf_select_workspace_bytes(const rf_select_desc* desc);
+
+/* Greedy forward selection for every target layer t, from calibration sums
+ * (stats[kind], one set per kind, each with d_in = L_src*F, d_out, n_maps =
+ * n_targets and syy set):
+ *   per kind: Gc, Cc_t centred as in rf_solve, TSS_t[o] = syy_t[o] − n μ_t[o]²,
+ *   α = λ·tr(Gc)/(L_src*F) (RF_ALPHA_TRACE, over ALL source features) or λ;
+ *   the score of a layer set S for target t and kind: the mean over heads h of
+ *     R²_h = Σ_{o∈h} Cc_t[S,o]ᵀ (Gc[S,S] + αI)^-1 Cc_t[S,o] / Σ_{o∈h} TSS_t[o],
+ *   i.e. 1 − (RSS + α‖w‖²)/TSS of the ridge fit (the least-squares R² at λ = 0);
+ *   a head with TSS = 0 counts as R² = 0;
+ *   step j adds the layer s not yet chosen whose set S ∪ {s} has the highest mean
+ *   score over kinds (the lowest index among equal scores).
+ * Outputs (device): src_layers [n_targets][k] int32, the layer chosen at each step;
+ * r2 [n_kinds][n_targets][k][L_src] fp32 (may be NULL): each candidate's score at
+ * each step, NaN for layers already chosen (step 0 is the single-layer R² table).
+ * Arithmetic: the Gram and cross terms in fp32, products as fp32-accurate split
+ * bf16 tensor-core GEMMs, Schur blocks factored in fp32; scores in fp64.
+ * A non-positive pivot sets RF_ERR_NOT_SPD in *dev_status. */
+rf_status rf_select_sources(const rf_select_desc* desc, const rf_calib_stats* stats,
+                            double lambda, int alpha_mode,
+                            int32_t* src_layers, float* r2, int32_t* dev_status,
+                            void* workspace, size_t workspace_bytes, rf_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -57,7 +57,14 @@ class rf_calib_desc(ctypes.Structure):
 
 
 class rf_calib_stats(ctypes.Structure):
-    _fields_ = [("G", c_void_p), ("C", c_void_p), ("sx", c_void_p), ("sy", c_void_p), ("n", c_void_p)]
+    _fields_ = [("G", c_void_p), ("C", c_void_p), ("sx", c_void_p), ("sy", c_void_p), ("n", c_void_p),
+                ("syy", c_void_p)]
+
+
+class rf_select_desc(ctypes.Structure):
+    _fields_ = [("L_src", c_int64), ("F", c_int64), ("n_targets", c_int64), ("d_out", c_int64),
+                ("head_dim", c_int64), ("k", c_int64), ("n_kinds", c_int64), ("group", c_int64),
+                ("flags", ctypes.c_uint64)]
 
 
 class rf_xmodel_desc(ctypes.Structure):
@@ -102,6 +109,11 @@ _SIGS = {
                               c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "rf_rope_rows": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_double, c_int64, c_int,
                              c_void_p]),
+    "rf_concat_layers": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_int64, c_int64, c_int64, c_double,
+                                 c_int64, c_void_p, c_int64, c_void_p]),
+    "rf_select_workspace_bytes": (c_size_t, [POINTER(rf_select_desc)]),
+    "rf_select_sources": (c_int, [POINTER(rf_select_desc), POINTER(rf_calib_stats), c_double, c_int, c_void_p,
+                                  c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
 }
 
 _lib = None
@@ -262,8 +274,8 @@ def rf_calib_workspace_bytes(desc: rf_calib_desc, n_rows: int) -> int:
     return int(lib().rf_calib_workspace_bytes(ctypes.byref(desc), int(n_rows)))
 
 
-def calib_stats_struct(G, C, sx, sy, n) -> rf_calib_stats:
-    return rf_calib_stats(_p(G), _p(C), _p(sx), _p(sy), _p(n))
+def calib_stats_struct(G, C, sx, sy, n, syy=None) -> rf_calib_stats:
+    return rf_calib_stats(_p(G), _p(C), _p(sx), _p(sy), _p(n), _p(syy))
 
 
 def rf_calib_accumulate(desc, X, ld_x, Y, ld_y, y_map_stride, n_rows, stats, dev_status=None,
@@ -303,3 +315,24 @@ def rf_xmodel_map(desc, src_layers, k_src, v_src, Wk, bk, Wv, bv, k_tgt, v_tgt, 
 def rf_rope_rows(inp, out, n_rows, ld, n_heads, head_dim, theta, pos_offset=0, inverse=False, stream=None):
     _check(lib().rf_rope_rows(_p(inp), _p(out), int(n_rows), int(ld), int(n_heads), int(head_dim), float(theta),
                               int(pos_offset), 1 if inverse else 0, _s(stream)), "rf_rope_rows")
+
+
+def rf_concat_layers(src, n_layers, layer_stride, n_rows, ld_src, n_heads, head_dim, theta, pos_offset, out, ld_out,
+                     stream=None):
+    """out[t][l*W + j] = (inverse RoPE if theta > 0 else identity)(src[l][t][j]); see include/rf.h."""
+    _check(lib().rf_concat_layers(_p(src), int(n_layers), int(layer_stride), int(n_rows), int(ld_src), int(n_heads),
+                                  int(head_dim), float(theta), int(pos_offset), _p(out), int(ld_out), _s(stream)),
+           "rf_concat_layers")
+
+
+def rf_select_workspace_bytes(desc: rf_select_desc) -> int:
+    return int(lib().rf_select_workspace_bytes(ctypes.byref(desc)))
+
+
+def rf_select_sources(desc, stats, lam, alpha_mode, src_layers, r2=None, dev_status=None, workspace=None,
+                      workspace_bytes=0, stream=None):
+    """Greedy source-layer selection; ``stats`` is a sequence of n_kinds rf_calib_stats."""
+    arr = (rf_calib_stats * len(stats))(*stats)
+    _check(lib().rf_select_sources(ctypes.byref(desc), arr, float(lam), int(alpha_mode), _p(src_layers), _p(r2),
+                                   _p(dev_status), _p(workspace), int(workspace_bytes), _s(stream)),
+           "rf_select_sources")

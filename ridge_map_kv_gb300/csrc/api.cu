@@ -237,6 +237,10 @@ const char* rf_stage_name(int s) {
     case RF_STAGE_SOLVE_PRODUCT: return "solve_product";
     case RF_STAGE_SOLVE_REFINE: return "solve_refine";
     case RF_STAGE_ROW_RMS: return "row_rms";
+    case RF_STAGE_SELECT_GEMM: return "select_gemm";
+    case RF_STAGE_SELECT_FACTOR: return "select_factor";
+    case RF_STAGE_SELECT_SCORE: return "select_score";
+    case RF_STAGE_SELECT_SPLIT: return "select_split";
     default: return "unknown";
   }
 }

@@ -12,7 +12,8 @@
 //                      more than kCalibChunk rows. Eight epilogue warps add the
 //                      chunk blocks into fp32 running sums in registers and flush
 //                      them into the fp64 totals every 16 chunks.
-//   k_colsum           Σx, Σy_p (fp32 over 64 rows, fp64 across) and n += rows.
+//   k_colsum           Σx, Σy_p, optionally Σy_p² (fp32 over 64 rows, fp64 across)
+//                      and n += rows.
 #include <algorithm>
 
 #include "rf_host.h"
@@ -164,11 +165,13 @@ __global__ void __launch_bounds__(256) k_mirror_lower(double* __restrict__ G, in
 }
 
 // Column sums of `n_maps` row-major bf16 matrices [n_rows][ld] (map p at
-// base + p*map_stride): out[p][c] += Σ_t M_p[t][c]. One thread per column, 512
-// rows per block; fp32 over 64 rows, then fp64, then one fp64 atomic per block.
+// base + p*map_stride): out[p][c] += Σ_t M_p[t][c], and out_sq[p][c] += Σ_t M_p[t][c]²
+// when out_sq is set. One thread per column, 512 rows per block; fp32 over 64 rows
+// (a bf16 square is exact in fp32), then fp64, then one fp64 atomic per block.
 __global__ void __launch_bounds__(256) k_colsum(const __nv_bfloat16* __restrict__ M, long long ld, long long map_stride,
                                                 int n_rows, int n_cols, double* __restrict__ out,
-                                                int64_t* __restrict__ n_counter, long long add_n) {
+                                                double* __restrict__ out_sq, int64_t* __restrict__ n_counter,
+                                                long long add_n) {
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   const int r0 = blockIdx.y * 512;
   const int p = blockIdx.z;
@@ -177,14 +180,20 @@ __global__ void __launch_bounds__(256) k_colsum(const __nv_bfloat16* __restrict_
   if (c >= n_cols) return;
   const __nv_bfloat16* col = M + static_cast<long long>(p) * map_stride + c;
   const int r1 = min(r0 + 512, n_rows);
-  double acc = 0.0;
+  double acc = 0.0, acc_sq = 0.0;
   for (int r = r0; r < r1; r += 64) {
-    float s = 0.f;
+    float s = 0.f, q = 0.f;
     const int re = min(r + 64, r1);
-    for (int t = r; t < re; ++t) s += __bfloat162float(col[static_cast<long long>(t) * ld]);
+    for (int t = r; t < re; ++t) {
+      const float v = __bfloat162float(col[static_cast<long long>(t) * ld]);
+      s += v;
+      q = fmaf(v, v, q);
+    }
     acc += static_cast<double>(s);
+    acc_sq += static_cast<double>(q);
   }
   atomicAdd(out + static_cast<size_t>(p) * n_cols + c, acc);
+  if (out_sq != nullptr) atomicAdd(out_sq + static_cast<size_t>(p) * n_cols + c, acc_sq);
 }
 
 template <bool kPair>
@@ -272,12 +281,12 @@ extern "C" rf_status rf_calib_accumulate(const rf_calib_desc* desc, const rf_bf1
     ProfScope prof(cs, RF_STAGE_COLSUM);
     dim3 gx(static_cast<unsigned>((d_in + 255) / 256), static_cast<unsigned>((n_rows + 511) / 512), 1);
     k_colsum<<<gx, 256, 0, cs>>>(reinterpret_cast<const __nv_bfloat16*>(X), ld_x, 0, static_cast<int>(n_rows),
-                                 static_cast<int>(d_in), st->sx, st->n, n_rows);
+                                 static_cast<int>(d_in), st->sx, nullptr, st->n, n_rows);
     if (P > 0) {
       dim3 gy(static_cast<unsigned>((d_out + 255) / 256), static_cast<unsigned>((n_rows + 511) / 512),
               static_cast<unsigned>(P));
       k_colsum<<<gy, 256, 0, cs>>>(reinterpret_cast<const __nv_bfloat16*>(Y), ld_y, y_map_stride,
-                                   static_cast<int>(n_rows), static_cast<int>(d_out), st->sy, nullptr, 0);
+                                   static_cast<int>(n_rows), static_cast<int>(d_out), st->sy, st->syy, nullptr, 0);
     }
   }
   if ((s = cuda_check(cudaGetLastError(), "k_colsum launch")) != RF_OK) return s;

@@ -307,4 +307,14 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
                : "memory");
 }
 
+// fp32 -> three bf16 planes: x = hi + mid + lo up to the last rounding (x - hi
+// and its remainder are exact in fp32), so products of the planes summed in
+// fp32 give fp32-accurate products on the bf16 tensor cores.
+__device__ __forceinline__ void split3(float x, __nv_bfloat16& h, __nv_bfloat16& m, __nv_bfloat16& l) {
+  h = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(h);
+  m = __float2bfloat16_rn(r1);
+  l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+}
+
 }  // namespace rf

@@ -67,6 +67,19 @@ rf_status expand_int8(const int8_t* q, __nv_bfloat16* out, size_t n, int sms, cu
 // The library's non-blocking copy stream for the current device (maps.cu).
 rf_status copy_stream(cudaStream_t* out);
 
+// From raw sums (solve.cu): μ_x = sx/n, μ_y = sy/n (n_y entries), n as double,
+// α = λ tr(Gc)/d_in or λ, and H = Gc + αI in fp32 (and fp64 when H64 is set).
+rf_status centre_system(const double* G, const double* sx, const double* sy, const int64_t* n, int d_in, long long n_y,
+                        double lambda, int alpha_mode, double* mu_x, double* mu_y, double* n_out, double* alpha,
+                        double* alpha_out, double* H64, float* H32, int sms, cudaStream_t s);
+
+// For b < batch (solve.cu): the SPD n x n matrix A + b*stride (ld lda, n % 128 == 0)
+// is overwritten by its lower Cholesky factor L_b (blocks above the diagonal keep
+// stale values), and Linv + b*n*ldi receives L_b^-1 (lower, zero above). fp32.
+// tmp holds batch * 128 * n floats. A non-positive pivot records RF_ERR_NOT_SPD.
+rf_status chol_inv_batched(float* A, long long lda, long long stride, float* Linv, long long ldi, int n, int batch,
+                           float* tmp, int32_t* dev_status, int sms, cudaStream_t s);
+
 // Brackets one kernel launch with profiling events when rf_profile_start is active.
 struct ProfScope {
   cudaStream_t stream;

@@ -1,0 +1,705 @@
+// Cross-layer source selection (rf_select_sources).
+//
+// [XM] "소스 층은 몇 개가 필요한가": greedy forward selection adds, one at a time,
+// the source layer that raises the head-mean R² most; "층 교차 소스 선택": the
+// mapper takes, per target layer, the k source layers with the highest head-mean
+// R² of the un-roped keys and of the values, shared by all heads of that layer.
+//
+// The ridge fit of a target on the features of a layer set S explains
+// e_o = c_oᵀ (Gc_SS + αI)^-1 c_o of each output column o. Greedy selection over
+// layers is a block Cholesky factorisation of H = Gc + αI whose next pivot block
+// is the layer with the best score. With S chosen (m features) and L_S its factor,
+// every other layer s carries
+//   W_s   = H_{s,S} L_S^-ᵀ              (its would-be row of the factor)
+//   Σ_s   = H_ss − W_s W_sᵀ              (its Schur block given S)
+//   R_s   = Cc_s − W_s Z_S               (its residual cross terms; Z_S = L_S^-1 Cc_S)
+// and adding s explains z_s = L_s^-1 R_s more (Σ_s = L_s L_sᵀ): e(S ∪ s) =
+// e(S) + colsum(z_s²). After choosing b, every layer gets one more block column
+//   W_s ← [W_s, (H_{s,b} − W_s W_bᵀ) L_b^-ᵀ],   Σ_s −= w wᵀ,   R_s −= w z_b
+// (w the new block). Per pass over a group of target layers, for every kind and
+// target ("problem" q) at once, a step runs:
+//   k_sel_mask_identity      Σ of already-chosen layers := I (never scored)
+//   chol_inv_batched         L_s^-1 for every (q, s), factoring a copy of Σ (fp32 SIMT)
+//   SelGemm (sum of squares) z_sᵀ = R_sᵀ L_s^-ᵀ, only colsum(z_s²) is kept
+//   k_sel_score              scores, the joint argmax, the tables, e += gain
+//   SelGemm                  z_bᵀ;  H[:, b] − W W_bᵀ;  × L_b^-ᵀ;  Σ_s −= w wᵀ;
+//                            Rᵀ −= z_bᵀ wᵀ
+// Every product is fp32-accurate on the bf16 tensor cores: each fp32 operand is
+// split into three bf16 planes (k_split_rows) and the six plane products that
+// matter at fp32 precision are summed, 1024-wide K chunks in TMEM and in fp32
+// registers across chunks and terms. Operands are K-major rows of the planes;
+// which rows and columns a batch entry reads is linear in (term, problem, layer
+// slot, chosen layer), the chosen layer read on the device, so no step waits on
+// the host.
+#include <algorithm>
+#include <cmath>
+
+#include "rf_host.h"
+#include "rf_device.cuh"
+#include "tc_gemm.cuh"
+
+namespace rf {
+
+constexpr int kSelChunk = 1024;  // K rows summed in TMEM before the fp32 register sum
+constexpr int kSelMaxKinds = 2;
+
+// Six plane products: term t multiplies A plane sel_term_a(t) by B plane sel_term_b(t):
+// hi·hi, mid·hi, hi·mid, lo·hi, mid·mid, hi·lo.
+__device__ __forceinline__ int sel_term_a(int t) { return (0x012010 >> (4 * t)) & 3; }
+__device__ __forceinline__ int sel_term_b(int t) { return (0x210100 >> (4 * t)) & 3; }
+
+// Row and K coordinates of one operand in the 2-D view [3 * plane_rows][k_extent]
+// of its planes.
+struct SelOperand {
+  long long plane_rows;
+  long long q_rows, s_rows, b_rows;  // per problem, per layer slot, per chosen layer
+  long long k0, s_k, b_k;            // K offset: fixed, per layer slot, per chosen layer
+};
+
+template <bool kPair_>
+struct SelGemmProb {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  SelOperand a, b;
+  const int32_t* chosen;  // [Q] layer chosen this step by problem q, or nullptr
+  int Q, nS;              // batch entry p = q * nS + s
+  int M, N, K, m_tiles, n_tiles, n_chunks;
+  float alpha, beta;
+  // store: out[q*o_q + s*o_s + m*ldo + n] = alpha·acc + beta·C, C at
+  //        csrc + (q / q_per_kind)*c_kind + bq*c_b + q*c_q + s*c_s + m*ldc + n
+  float* out;
+  long long o_q, o_s, ldo;
+  const float* csrc;
+  long long c_kind, c_b, c_q, c_s, ldc;
+  int q_per_kind;
+  // sum of squares: part[(p*M + m)*2*n_tiles + 2*nt + half] = Σ (alpha·acc)² over 128 columns
+  float* part;
+  int32_t* dev_status;
+  uint64_t timeout_ns;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kPair = kPair_;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kCols = kBN / 2;
+  struct EpiState {
+    float rs[kCols];
+  };
+  using Cfg = GemmCfg<kPair_>;
+
+  __device__ void prefetch() const {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  __device__ int num_units() const { return Q * nS * m_tiles * n_tiles; }
+  __device__ int num_subtiles(int) const { return 6 * n_chunks; }
+  __device__ int num_kb(int, int sb) const {
+    const int c = sb % n_chunks;
+    return (min(kSelChunk, K - c * kSelChunk) + kBK - 1) / kBK;
+  }
+  __device__ void decode(int u, int& q, int& s, int& mt, int& nt) const {
+    nt = u % n_tiles;
+    u /= n_tiles;
+    mt = u % m_tiles;
+    const int p = u / m_tiles;
+    q = p / nS;
+    s = p - q * nS;
+  }
+  struct Coords {
+    int a_row, a_k, b_row, b_k;
+  };
+  __device__ Coords coords(int u, int sb, uint32_t rank) const {
+    int q, s, mt, nt;
+    decode(u, q, s, mt, nt);
+    const int t = sb / n_chunks, c = sb - t * n_chunks;
+    const long long bq = chosen != nullptr ? chosen[q] : 0;
+    Coords r;
+    r.a_row = static_cast<int>(sel_term_a(t) * a.plane_rows + q * a.q_rows + s * a.s_rows + bq * a.b_rows +
+                               static_cast<long long>(mt) * Cfg::kUnitM + rank * kBM);
+    r.a_k = static_cast<int>(a.k0 + s * a.s_k + bq * a.b_k + static_cast<long long>(c) * kSelChunk);
+    r.b_row = static_cast<int>(sel_term_b(t) * b.plane_rows + q * b.q_rows + s * b.s_rows + bq * b.b_rows +
+                               static_cast<long long>(nt) * kBN + rank * Cfg::kBRows);
+    r.b_k = static_cast<int>(b.k0 + s * b.s_k + bq * b.b_k + static_cast<long long>(c) * kSelChunk);
+    return r;
+  }
+  __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    load_operand<kBM, false, kPair>(sa, &tmA, bar, c.a_k + kb * kBK, c.a_row);
+    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, c.b_k + kb * kBK, c.b_row);
+  }
+  __device__ void epilogue(EpiState& es, int, int sb, int, uint32_t tacc, int, int, uint32_t) const {
+#pragma unroll
+    for (int ch = 0; ch < kCols / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(tacc + ch * 32, v);
+      tmem_wait_ld32(v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) es.rs[ch * 32 + i] = sb == 0 ? u2f(v[i]) : es.rs[ch * 32 + i] + u2f(v[i]);
+    }
+  }
+  __device__ void epilogue_after(EpiState& es, int u, int sb, int nsub, int row, int col0, uint32_t rank) const {
+    if (sb != nsub - 1) return;
+    int q, s, mt, nt;
+    decode(u, q, s, mt, nt);
+    const long long m = static_cast<long long>(mt) * Cfg::kUnitM + rank * kBM + row;
+    const long long n0 = static_cast<long long>(nt) * kBN + col0;
+    if (part != nullptr) {
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < kCols; ++i) {
+        const float v = alpha * es.rs[i];
+        ss = fmaf(v, v, ss);
+      }
+      const long long p = static_cast<long long>(q) * nS + s;
+      part[(p * M + m) * (2 * n_tiles) + 2 * nt + col0 / kCols] = ss;
+      return;
+    }
+    float4* o = reinterpret_cast<float4*>(out + q * o_q + s * o_s + m * ldo + n0);
+    const float4* cp = nullptr;
+    if (beta != 0.f) {
+      const long long bq = chosen != nullptr ? chosen[q] : 0;
+      cp = reinterpret_cast<const float4*>(csrc + (q / q_per_kind) * c_kind + bq * c_b + q * c_q + s * c_s + m * ldc +
+                                           n0);
+    }
+#pragma unroll
+    for (int i = 0; i < kCols / 4; ++i) {
+      float4 v = make_float4(alpha * es.rs[4 * i], alpha * es.rs[4 * i + 1], alpha * es.rs[4 * i + 2],
+                             alpha * es.rs[4 * i + 3]);
+      if (cp != nullptr) {
+        const float4 c = cp[i];
+        v.x = fmaf(beta, c.x, v.x);
+        v.y = fmaf(beta, c.y, v.y);
+        v.z = fmaf(beta, c.z, v.z);
+        v.w = fmaf(beta, c.w, v.w);
+      }
+      o[i] = v;
+    }
+  }
+};
+
+// fp32 rows -> three bf16 planes: dst[j][r][col_off + c] for r < rows, c < cols
+// (cols % 4 == 0); plane j at dst + j * plane_stride.
+__global__ void __launch_bounds__(256) k_split_rows(const float* __restrict__ src, long long ld_src,
+                                                    __nv_bfloat16* __restrict__ dst, long long ld_dst, long long col_off,
+                                                    long long plane_stride, long long rows, int cols) {
+  const int per = cols / 4;
+  const long long total = rows * per;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / per;
+    const int c = static_cast<int>(i - r * per) * 4;
+    const float4 v = __ldg(reinterpret_cast<const float4*>(src + r * ld_src + c));
+    __nv_bfloat16 h[4], m[4], l[4];
+    split3(v.x, h[0], m[0], l[0]);
+    split3(v.y, h[1], m[1], l[1]);
+    split3(v.z, h[2], m[2], l[2]);
+    split3(v.w, h[3], m[3], l[3]);
+    __nv_bfloat16* d = dst + r * ld_dst + col_off + c;
+    *reinterpret_cast<uint2*>(d) = *reinterpret_cast<const uint2*>(h);
+    *reinterpret_cast<uint2*>(d + plane_stride) = *reinterpret_cast<const uint2*>(m);
+    *reinterpret_cast<uint2*>(d + 2 * plane_stride) = *reinterpret_cast<const uint2*>(l);
+  }
+}
+
+// Per-kind inputs of one call.
+struct SelKinds {
+  const double* C[kSelMaxKinds];    // [n_targets][D][Ft] raw cross sums
+  const double* syy[kSelMaxKinds];  // [n_targets][Ft]
+  const double* mu_x[kSelMaxKinds];  // [D]   (workspace)
+  const double* mu_y[kSelMaxKinds];  // [n_targets][Ft]
+  const double* n[kSelMaxKinds];     // rows, as double
+};
+
+// Rᵀ of problem q = (kind, target t0 + g): RT[q][o][i] = C[t][i][o] − n μ_x[i] μ_t[o] in
+// fp32, through 32 x 32 shared tiles. Grid (D/32, Ft/32, Q), 32 x 8 threads.
+__global__ void __launch_bounds__(256) k_sel_init_rt(const __grid_constant__ SelKinds kinds, int t0, int G, int D,
+                                                     int Ft, float* __restrict__ RT) {
+  __shared__ float tile[32][33];
+  const int q = blockIdx.z, kind = q / G, t = t0 + q % G;
+  const int i0 = blockIdx.x * 32, o0 = blockIdx.y * 32;
+  const double* C = kinds.C[kind] + static_cast<size_t>(t) * D * Ft;
+  const double* mx = kinds.mu_x[kind];
+  const double* my = kinds.mu_y[kind] + static_cast<size_t>(t) * Ft;
+  const double nn = *kinds.n[kind];
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int i = i0 + j, o = o0 + threadIdx.x;
+    tile[j][threadIdx.x] = static_cast<float>(C[static_cast<size_t>(i) * Ft + o] - nn * mx[i] * my[o]);
+  }
+  __syncthreads();
+  float* out = RT + static_cast<size_t>(q) * Ft * D;
+  for (int j = threadIdx.y; j < 32; j += 8) out[static_cast<size_t>(o0 + j) * D + i0 + threadIdx.x] = tile[threadIdx.x][j];
+}
+
+// Σ[q][s] = H_kind[s block][s block] (F x F), and for every q its TSS and e = 0.
+__global__ void __launch_bounds__(256) k_sel_init_sigma(const float* __restrict__ H, int G, int Q, int Ls, int F,
+                                                        float* __restrict__ Sig) {
+  const long long D = static_cast<long long>(Ls) * F;
+  const long long per = static_cast<long long>(F) * F / 4;
+  const long long total = static_cast<long long>(Q) * Ls * per;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long qs = i / per;
+    const long long e = (i - qs * per) * 4;
+    const int q = static_cast<int>(qs / Ls), s = static_cast<int>(qs - static_cast<long long>(q) * Ls);
+    const long long r = e / F, c = e - r * F;
+    const float* src = H + static_cast<long long>(q / G) * D * D + (s * static_cast<long long>(F) + r) * D +
+                       s * static_cast<long long>(F) + c;
+    *reinterpret_cast<float4*>(Sig + qs * F * F + e) = *reinterpret_cast<const float4*>(src);
+  }
+}
+
+__global__ void __launch_bounds__(256) k_sel_init_tss(const __grid_constant__ SelKinds kinds, int t0, int G, int Q,
+                                                      int Ft, double* __restrict__ tss, double* __restrict__ expl) {
+  const long long total = static_cast<long long>(Q) * Ft;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int q = static_cast<int>(i / Ft), o = static_cast<int>(i - static_cast<long long>(q) * Ft);
+    const int kind = q / G, t = t0 + q % G;
+    const double mu = kinds.mu_y[kind][static_cast<size_t>(t) * Ft + o];
+    tss[i] = kinds.syy[kind][static_cast<size_t>(t) * Ft + o] - (*kinds.n[kind]) * mu * mu;
+    expl[i] = 0.0;
+  }
+}
+
+// Σ[q][s] := I for every layer s already chosen for problem q's target.
+__global__ void __launch_bounds__(256) k_sel_mask_identity(const uint8_t* __restrict__ mask, int G, int Ls, int F,
+                                                           float* __restrict__ Sig) {
+  const int q = blockIdx.y, s = blockIdx.x;
+  if (!mask[(q % G) * Ls + s]) return;
+  float* S = Sig + (static_cast<long long>(q) * Ls + s) * F * F;
+  for (long long e = threadIdx.x; e < static_cast<long long>(F) * F; e += blockDim.x) {
+    const long long r = e / F;
+    S[e] = (e - r * F == r) ? 1.f : 0.f;
+  }
+}
+
+// One CTA per target g: for every kind and layer not yet chosen, gain_o = Σ partials
+// of colsum(z_s²); score = mean_h (Σ_{o∈h}(e_o + gain_o)) / Σ_{o∈h} TSS_o (0 for a
+// head without variance); joint = mean over kinds; the first layer with the
+// highest joint score is chosen. Writes the tables, the choice, the mask and e.
+__global__ void __launch_bounds__(256) k_sel_score(const float* __restrict__ part, int n_part, int G, int n_kinds,
+                                                   int Ls, int Ft, int hd, int t0, int n_targets, int k, int j,
+                                                   const double* __restrict__ tss, double* __restrict__ expl,
+                                                   uint8_t* __restrict__ mask, int32_t* __restrict__ chosen,
+                                                   int32_t* __restrict__ sel, float* __restrict__ r2) {
+  extern __shared__ double sh[];  // [n_kinds][Ls] scores
+  const int g = blockIdx.x, t = t0 + g;
+  const int nh = Ft / hd;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const uint8_t* mk = mask + g * Ls;
+  // scores: one warp per (kind, layer); heads in turn, the warp summing a head's columns
+  for (int ks = warp; ks < n_kinds * Ls; ks += nwarps) {
+    const int kind = ks / Ls, s = ks - kind * Ls;
+    const int q = kind * G + g;
+    double score = 0.0;
+    if (!mk[s]) {
+      const float* pp = part + (static_cast<size_t>(q) * Ls + s) * Ft * n_part;
+      for (int h = 0; h < nh; ++h) {
+        double num = 0.0, den = 0.0;
+        for (int o = h * hd + lane; o < (h + 1) * hd; o += 32) {
+          double gsum = 0.0;
+          for (int i = 0; i < n_part; ++i) gsum += static_cast<double>(pp[static_cast<size_t>(o) * n_part + i]);
+          num += expl[static_cast<size_t>(q) * Ft + o] + gsum;
+          den += tss[static_cast<size_t>(q) * Ft + o];
+        }
+        for (int off = 16; off > 0; off >>= 1) {
+          num += __shfl_xor_sync(0xffffffffu, num, off);
+          den += __shfl_xor_sync(0xffffffffu, den, off);
+        }
+        score += den > 0.0 ? num / den : 0.0;
+      }
+      score /= nh;
+    }
+    if (lane == 0) {
+      sh[ks] = score;
+      if (r2 != nullptr)
+        r2[((static_cast<size_t>(kind) * n_targets + t) * k + j) * Ls + s] = mk[s] ? nanf("") : static_cast<float>(score);
+    }
+  }
+  __syncthreads();
+  __shared__ int best_s;
+  if (threadIdx.x == 0) {
+    int best = -1;
+    double bv = 0.0;
+    for (int s = 0; s < Ls; ++s) {
+      if (mk[s]) continue;
+      double v = 0.0;
+      for (int kind = 0; kind < n_kinds; ++kind) v += sh[kind * Ls + s];
+      v /= n_kinds;
+      if (best < 0 || v > bv) {
+        best = s;
+        bv = v;
+      }
+    }
+    best_s = best;
+    sel[static_cast<size_t>(t) * k + j] = best;
+    mask[g * Ls + best] = 1;
+    for (int kind = 0; kind < n_kinds; ++kind) chosen[kind * G + g] = best;
+  }
+  __syncthreads();
+  const int b = best_s;
+  for (int i = threadIdx.x; i < n_kinds * Ft; i += blockDim.x) {
+    const int kind = i / Ft, o = i - kind * Ft;
+    const int q = kind * G + g;
+    const float* pp = part + ((static_cast<size_t>(q) * Ls + b) * Ft + o) * n_part;
+    double gsum = 0.0;
+    for (int p = 0; p < n_part; ++p) gsum += static_cast<double>(pp[p]);
+    expl[static_cast<size_t>(q) * Ft + o] += gsum;
+  }
+}
+
+// X[q][i][f] = H_kind[i][b_q F + f]: the first block column of the factor's input.
+__global__ void __launch_bounds__(256) k_sel_copy_hcols(const float* __restrict__ H, const int32_t* __restrict__ chosen,
+                                                        int G, int Q, long long D, int F, float* __restrict__ X) {
+  const long long per = D * F / 4;
+  const long long total = per * Q;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int q = static_cast<int>(i / per);
+    const long long e = (i - q * per) * 4;
+    const long long r = e / F, c = e - r * F;
+    const float* src = H + static_cast<long long>(q / G) * D * D + r * D + static_cast<long long>(chosen[q]) * F + c;
+    *reinterpret_cast<float4*>(X + static_cast<long long>(q) * D * F + e) = *reinterpret_cast<const float4*>(src);
+  }
+}
+
+// --------------------------------------------------------------------------
+// Host side
+// --------------------------------------------------------------------------
+struct SelLayout {
+  float* H;         // [n_kinds][D][D]
+  double* mu_x;     // [n_kinds][D]
+  double* mu_y;     // [n_kinds][n_targets][Ft]
+  double* nn;       // [n_kinds]
+  double* alpha;    // [n_kinds]
+  __nv_bfloat16* Wp;  // [3][Qmax * D][m_max]
+  float* Sig;       // [Qmax * Ls][F][F]  Schur blocks, kept across steps
+  float* Lf;        // [Qmax * Ls][F][F]  their Cholesky factors (factored in place from a copy)
+  float* Linv;      // [Qmax * Ls][F][F]
+  __nv_bfloat16* Lp;  // [3][Qmax * Ls * F][F]
+  float* ctmp;      // [Qmax * Ls][128][F]
+  float* RT;        // [Qmax][Ft][D]
+  __nv_bfloat16* RTp;  // [3][Qmax * Ft][D]
+  float* part;      // [Qmax * Ls][Ft][2 F / 256]
+  float* zb;        // [Qmax][Ft][F]
+  __nv_bfloat16* zbp;  // [3][Qmax * Ft][F]
+  float* X;         // [Qmax][D][F]
+  __nv_bfloat16* Xp;  // [3][Qmax * D][F]
+  double* tss;      // [Qmax][Ft]
+  double* expl;     // [Qmax][Ft]
+  int32_t* chosen;  // [Qmax]
+  uint8_t* mask;    // [Gmax][Ls]
+  size_t bytes;
+};
+
+static int sel_group(const rf_select_desc* d) {
+  return static_cast<int>(d->group > 0 ? std::min(d->group, d->n_targets) : d->n_targets);
+}
+
+static SelLayout sel_layout(const rf_select_desc* d, void* ws) {
+  const long long Ls = d->L_src, F = d->F, D = Ls * F, Ft = d->d_out, NK = d->n_kinds;
+  const long long Gm = sel_group(d), Q = NK * Gm;
+  const long long m_max = (d->k - 1) * F;
+  Carve c(ws);
+  SelLayout l;
+  l.H = c.take<float>(NK * D * D);
+  l.mu_x = c.take<double>(NK * D);
+  l.mu_y = c.take<double>(NK * d->n_targets * Ft);
+  l.nn = c.take<double>(NK);
+  l.alpha = c.take<double>(NK);
+  l.Wp = c.take<__nv_bfloat16>(std::max<long long>(3 * Q * D * m_max, 1));
+  l.Sig = c.take<float>(Q * Ls * F * F);
+  l.Lf = c.take<float>(Q * Ls * F * F);
+  l.Linv = c.take<float>(Q * Ls * F * F);
+  l.Lp = c.take<__nv_bfloat16>(3 * Q * Ls * F * F);
+  l.ctmp = c.take<float>(Q * Ls * 128 * F);
+  l.RT = c.take<float>(Q * Ft * D);
+  l.RTp = c.take<__nv_bfloat16>(3 * Q * Ft * D);
+  l.part = c.take<float>(Q * Ls * Ft * 2 * (F / kBN));
+  l.zb = c.take<float>(Q * Ft * F);
+  l.zbp = c.take<__nv_bfloat16>(3 * Q * Ft * F);
+  l.X = c.take<float>(Q * D * F);
+  l.Xp = c.take<__nv_bfloat16>(3 * Q * D * F);
+  l.tss = c.take<double>(Q * Ft);
+  l.expl = c.take<double>(Q * Ft);
+  l.chosen = c.take<int32_t>(Q);
+  l.mask = c.take<uint8_t>(Gm * Ls);
+  l.bytes = c.bytes();
+  return l;
+}
+
+static rf_status check_select_desc(const rf_select_desc* d) {
+  if (d == nullptr) return fail(RF_ERR_INVALID_ARG, "desc is NULL");
+  if (d->L_src <= 0 || d->F <= 0 || d->n_targets <= 0 || d->d_out <= 0 || d->head_dim <= 0 || d->k <= 0 ||
+      d->group < 0)
+    return fail(RF_ERR_INVALID_ARG, "need L_src, F, n_targets, d_out, head_dim, k > 0 and group >= 0");
+  if (d->k > d->L_src) return fail(RF_ERR_INVALID_ARG, "k = %lld exceeds L_src = %lld", (long long)d->k,
+                                   (long long)d->L_src);
+  if (d->n_kinds != 1 && d->n_kinds != 2) return fail(RF_ERR_INVALID_ARG, "n_kinds must be 1 or 2");
+  if (d->F % kBN != 0 || d->d_out % kBN != 0) return fail(RF_ERR_SHAPE, "F and d_out must be multiples of 256");
+  if (d->d_out % d->head_dim != 0) return fail(RF_ERR_SHAPE, "d_out must be a multiple of head_dim");
+  if (d->L_src * d->F > 65536) return fail(RF_ERR_SHAPE, "L_src * F must be <= 65536");
+  if (d->n_targets > 65535) return fail(RF_ERR_SHAPE, "n_targets must be <= 65535");
+  return RF_OK;
+}
+
+struct SelCtx {
+  cudaStream_t s;
+  int sms;
+  int32_t* dev_status;
+  bool pair;
+};
+
+static rf_status split_rows(SelCtx& c, const float* src, long long ld_src, __nv_bfloat16* dst, long long ld_dst,
+                            long long col_off, long long plane_stride, long long rows, int cols) {
+  const long long total = rows * (cols / 4);
+  const unsigned blocks = static_cast<unsigned>(std::min<long long>((total + 255) / 256, 8LL * c.sms));
+  ProfScope prof(c.s, RF_STAGE_SELECT_SPLIT);
+  k_split_rows<<<blocks, 256, 0, c.s>>>(src, ld_src, dst, ld_dst, col_off, plane_stride, rows, cols);
+  return cuda_check(cudaGetLastError(), "k_split_rows launch");
+}
+
+// One split product: operands are the planes at pa ([3][a_rows][a_kext]) and
+// pb ([3][b_rows][b_kext]).
+struct SelGemm {
+  const __nv_bfloat16* pa;
+  long long a_rows, a_kext;
+  SelOperand a;
+  const __nv_bfloat16* pb;
+  long long b_rows, b_kext;
+  SelOperand b;
+  const int32_t* chosen = nullptr;
+  int Q = 1, nS = 1, M = 0, N = 0, K = 0;
+  float alpha = 1.f, beta = 0.f;
+  float* out = nullptr;
+  long long o_q = 0, o_s = 0, ldo = 0;
+  const float* csrc = nullptr;
+  long long c_kind = 0, c_b = 0, c_q = 0, c_s = 0, ldc = 0;
+  int q_per_kind = 1;
+  float* part = nullptr;
+};
+
+template <bool kPair>
+static rf_status run_sel_gemm(SelCtx& c, const SelGemm& g) {
+  using Cfg = GemmCfg<kPair>;
+  SelGemmProb<kPair> pr;
+  rf_status st;
+  if ((st = make_tmap_bf16_2d(&pr.tmA, g.pa, g.a_kext, 3 * g.a_rows, g.a_kext, kBK, kBM)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmB, g.pb, g.b_kext, 3 * g.b_rows, g.b_kext, kBK, Cfg::kBRows)) != RF_OK) return st;
+  pr.a = g.a;
+  pr.b = g.b;
+  pr.a.plane_rows = g.a_rows;
+  pr.b.plane_rows = g.b_rows;
+  pr.chosen = g.chosen;
+  pr.Q = g.Q;
+  pr.nS = g.nS;
+  pr.M = g.M;
+  pr.N = g.N;
+  pr.K = g.K;
+  pr.m_tiles = g.M / Cfg::kUnitM;
+  pr.n_tiles = g.N / kBN;
+  pr.n_chunks = (g.K + kSelChunk - 1) / kSelChunk;
+  pr.alpha = g.alpha;
+  pr.beta = g.beta;
+  pr.out = g.out;
+  pr.o_q = g.o_q;
+  pr.o_s = g.o_s;
+  pr.ldo = g.ldo;
+  pr.csrc = g.csrc;
+  pr.c_kind = g.c_kind;
+  pr.c_b = g.c_b;
+  pr.c_q = g.c_q;
+  pr.c_s = g.c_s;
+  pr.ldc = g.ldc;
+  pr.q_per_kind = g.q_per_kind;
+  pr.part = g.part;
+  pr.dev_status = c.dev_status;
+  pr.timeout_ns = wait_timeout_ns();
+  ProfScope prof(c.s, RF_STAGE_SELECT_GEMM);
+  return launch_gemm(pr, static_cast<int64_t>(g.Q) * g.nS * pr.m_tiles * pr.n_tiles, c.sms, c.s,
+                     "selection GEMM launch");
+}
+
+static rf_status sel_gemm(SelCtx& c, const SelGemm& g) {
+  return c.pair ? run_sel_gemm<true>(c, g) : run_sel_gemm<false>(c, g);
+}
+
+static SelOperand op(long long q_rows, long long s_rows, long long b_rows, long long k0, long long s_k,
+                     long long b_k) {
+  SelOperand o;
+  o.plane_rows = 0;
+  o.q_rows = q_rows;
+  o.s_rows = s_rows;
+  o.b_rows = b_rows;
+  o.k0 = k0;
+  o.s_k = s_k;
+  o.b_k = b_k;
+  return o;
+}
+
+}  // namespace rf
+
+using namespace rf;
+
+extern "C" size_t rf_select_workspace_bytes(const rf_select_desc* desc) {
+  if (check_select_desc(desc) != RF_OK) return 0;
+  return sel_layout(desc, nullptr).bytes;
+}
+
+extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_calib_stats* stats, double lambda,
+                                       int alpha_mode, int32_t* src_layers, float* r2, int32_t* dev_status,
+                                       void* workspace, size_t workspace_bytes, rf_stream_t stream) {
+  clear_error();
+  rf_status st = check_select_desc(desc);
+  if (st != RF_OK) return st;
+  if (alpha_mode != RF_ALPHA_TRACE && alpha_mode != RF_ALPHA_ABSOLUTE)
+    return fail(RF_ERR_INVALID_ARG, "alpha_mode must be RF_ALPHA_TRACE or RF_ALPHA_ABSOLUTE");
+  if (!(lambda >= 0.0)) return fail(RF_ERR_INVALID_ARG, "need lambda >= 0");
+  if (stats == nullptr || src_layers == nullptr) return fail(RF_ERR_INVALID_ARG, "stats and src_layers must be non-NULL");
+  for (int kind = 0; kind < desc->n_kinds; ++kind) {
+    const rf_calib_stats& k = stats[kind];
+    if (!k.G || !k.C || !k.sx || !k.sy || !k.n || !k.syy)
+      return fail(RF_ERR_INVALID_ARG, "stats[%d]: G, C, sx, sy, n and syy must be non-NULL", kind);
+  }
+  SelLayout lay = sel_layout(desc, workspace);
+  if (workspace == nullptr || workspace_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", lay.bytes, workspace_bytes);
+  int sms = 0;
+  if ((st = current_device(&sms)) != RF_OK) return st;
+  SelCtx c{static_cast<cudaStream_t>(stream), sms, dev_status, use_pair(desc->flags, true)};
+
+  const int Ls = static_cast<int>(desc->L_src), F = static_cast<int>(desc->F), Ft = static_cast<int>(desc->d_out);
+  const int NK = static_cast<int>(desc->n_kinds), T = static_cast<int>(desc->n_targets), K = static_cast<int>(desc->k);
+  const int hd = static_cast<int>(desc->head_dim);
+  const long long D = static_cast<long long>(Ls) * F;
+  const long long m_max = static_cast<long long>(K - 1) * F;
+  const int Gm = sel_group(desc);
+  const int n_part = 2 * (F / kBN);
+  const int eb = 8 * sms;
+
+  SelKinds kinds{};
+  {
+    ProfScope pf(c.s, RF_STAGE_SELECT_SCORE);
+    for (int kind = 0; kind < NK; ++kind) {
+      const rf_calib_stats& k = stats[kind];
+      if ((st = centre_system(k.G, k.sx, k.sy, k.n, static_cast<int>(D), static_cast<long long>(T) * Ft, lambda,
+                              alpha_mode, lay.mu_x + kind * D, lay.mu_y + static_cast<long long>(kind) * T * Ft,
+                              lay.nn + kind, lay.alpha + kind, nullptr, nullptr, lay.H + kind * D * D, sms, c.s)) !=
+          RF_OK)
+        return st;
+      kinds.C[kind] = k.C;
+      kinds.syy[kind] = k.syy;
+      kinds.mu_x[kind] = lay.mu_x + kind * D;
+      kinds.mu_y[kind] = lay.mu_y + static_cast<long long>(kind) * T * Ft;
+      kinds.n[kind] = lay.nn + kind;
+    }
+  }
+  const size_t score_smem = sizeof(double) * NK * Ls;
+
+  for (int t0 = 0; t0 < T; t0 += Gm) {
+    const int G = std::min(Gm, T - t0), Q = NK * G;
+    {
+      ProfScope pf(c.s, RF_STAGE_SELECT_SCORE);
+      k_sel_init_rt<<<dim3(static_cast<unsigned>(D / 32), static_cast<unsigned>(Ft / 32), Q), dim3(32, 8), 0, c.s>>>(
+          kinds, t0, G, static_cast<int>(D), Ft, lay.RT);
+      k_sel_init_sigma<<<eb, 256, 0, c.s>>>(lay.H, G, Q, Ls, F, lay.Sig);
+      k_sel_init_tss<<<eb, 256, 0, c.s>>>(kinds, t0, G, Q, Ft, lay.tss, lay.expl);
+      if ((st = cuda_check(cudaMemsetAsync(lay.mask, 0, static_cast<size_t>(G) * Ls, c.s), "mask reset")) != RF_OK)
+        return st;
+      if ((st = cuda_check(cudaGetLastError(), "selection set-up launches")) != RF_OK) return st;
+    }
+    const long long lrows = static_cast<long long>(Q) * Ls * F;  // rows of the L^-1 planes
+    const long long rtrows = static_cast<long long>(Q) * Ft;     // rows of the Rᵀ planes
+    const long long wrows = static_cast<long long>(Q) * D;       // rows of the W and X planes
+    for (int j = 0; j < K; ++j) {
+      const long long m = static_cast<long long>(j) * F;
+      {
+        ProfScope pf(c.s, RF_STAGE_SELECT_FACTOR);
+        if (j > 0) k_sel_mask_identity<<<dim3(Ls, Q), 256, 0, c.s>>>(lay.mask, G, Ls, F, lay.Sig);
+        if ((st = cuda_check(cudaMemcpyAsync(lay.Lf, lay.Sig, sizeof(float) * Q * Ls * F * F,
+                                             cudaMemcpyDeviceToDevice, c.s),
+                             "Schur block copy")) != RF_OK)
+          return st;
+        if ((st = chol_inv_batched(lay.Lf, F, static_cast<long long>(F) * F, lay.Linv, F, F, Q * Ls, lay.ctmp,
+                                   dev_status, sms, c.s)) != RF_OK)
+          return st;
+      }
+      if ((st = split_rows(c, lay.Linv, F, lay.Lp, F, 0, lrows * F, lrows, F)) != RF_OK) return st;
+      if ((st = split_rows(c, lay.RT, D, lay.RTp, D, 0, rtrows * D, rtrows, static_cast<int>(D))) != RF_OK) return st;
+      // colsum(z_s²) for every (q, s): z_sᵀ = R_sᵀ L_s^-ᵀ
+      {
+        SelGemm g{};
+        g.pa = lay.RTp, g.a_rows = rtrows, g.a_kext = D, g.a = op(Ft, 0, 0, 0, F, 0);
+        g.pb = lay.Lp, g.b_rows = lrows, g.b_kext = F, g.b = op(static_cast<long long>(Ls) * F, F, 0, 0, 0, 0);
+        g.Q = Q, g.nS = Ls, g.M = Ft, g.N = F, g.K = F;
+        g.part = lay.part;
+        if ((st = sel_gemm(c, g)) != RF_OK) return st;
+      }
+      {
+        ProfScope pf(c.s, RF_STAGE_SELECT_SCORE);
+        k_sel_score<<<G, 256, score_smem, c.s>>>(lay.part, n_part, G, NK, Ls, Ft, hd, t0, T, K, j, lay.tss, lay.expl,
+                                                 lay.mask, lay.chosen, src_layers, r2);
+        if ((st = cuda_check(cudaGetLastError(), "k_sel_score launch")) != RF_OK) return st;
+      }
+      if (j == K - 1) break;
+      // z_bᵀ = R_bᵀ L_b^-ᵀ
+      {
+        SelGemm g{};
+        g.pa = lay.RTp, g.a_rows = rtrows, g.a_kext = D, g.a = op(Ft, 0, 0, 0, 0, F);
+        g.pb = lay.Lp, g.b_rows = lrows, g.b_kext = F, g.b = op(static_cast<long long>(Ls) * F, 0, F, 0, 0, 0);
+        g.chosen = lay.chosen, g.Q = Q, g.M = Ft, g.N = F, g.K = F;
+        g.out = lay.zb, g.o_q = static_cast<long long>(Ft) * F, g.ldo = F;
+        if ((st = sel_gemm(c, g)) != RF_OK) return st;
+      }
+      if ((st = split_rows(c, lay.zb, F, lay.zbp, F, 0, rtrows * F, rtrows, F)) != RF_OK) return st;
+      // X = H[:, b] − W W_bᵀ
+      if (j == 0) {
+        ProfScope pf(c.s, RF_STAGE_SELECT_SCORE);
+        k_sel_copy_hcols<<<eb, 256, 0, c.s>>>(lay.H, lay.chosen, G, Q, D, F, lay.X);
+        if ((st = cuda_check(cudaGetLastError(), "k_sel_copy_hcols launch")) != RF_OK) return st;
+      } else {
+        SelGemm g{};
+        g.pa = lay.Wp, g.a_rows = wrows, g.a_kext = m_max, g.a = op(D, 0, 0, 0, 0, 0);
+        g.pb = lay.Wp, g.b_rows = wrows, g.b_kext = m_max, g.b = op(D, 0, F, 0, 0, 0);
+        g.chosen = lay.chosen, g.Q = Q, g.M = static_cast<int>(D), g.N = F, g.K = static_cast<int>(m);
+        g.alpha = -1.f, g.beta = 1.f;
+        g.out = lay.X, g.o_q = D * F, g.ldo = F;
+        g.csrc = lay.H, g.c_kind = D * D, g.c_b = F, g.ldc = D, g.q_per_kind = G;
+        if ((st = sel_gemm(c, g)) != RF_OK) return st;
+      }
+      if ((st = split_rows(c, lay.X, F, lay.Xp, F, 0, wrows * F, wrows, F)) != RF_OK) return st;
+      // w = X L_b^-ᵀ  (the new block column of every layer), then into the W planes
+      {
+        SelGemm g{};
+        g.pa = lay.Xp, g.a_rows = wrows, g.a_kext = F, g.a = op(D, 0, 0, 0, 0, 0);
+        g.pb = lay.Lp, g.b_rows = lrows, g.b_kext = F, g.b = op(static_cast<long long>(Ls) * F, 0, F, 0, 0, 0);
+        g.chosen = lay.chosen, g.Q = Q, g.M = static_cast<int>(D), g.N = F, g.K = F;
+        g.out = lay.X, g.o_q = D * F, g.ldo = F;
+        if ((st = sel_gemm(c, g)) != RF_OK) return st;
+      }
+      if ((st = split_rows(c, lay.X, F, lay.Wp, m_max, m, wrows * m_max, wrows, F)) != RF_OK) return st;
+      // Σ_s −= w_s w_sᵀ for every (q, s)
+      {
+        SelGemm g{};
+        g.pa = lay.Wp, g.a_rows = wrows, g.a_kext = m_max, g.a = op(D, F, 0, m, 0, 0);
+        g.pb = lay.Wp, g.b_rows = wrows, g.b_kext = m_max, g.b = op(D, F, 0, m, 0, 0);
+        g.Q = Q, g.nS = Ls, g.M = F, g.N = F, g.K = F;
+        g.alpha = -1.f, g.beta = 1.f;
+        g.out = lay.Sig, g.o_q = static_cast<long long>(Ls) * F * F, g.o_s = static_cast<long long>(F) * F, g.ldo = F;
+        g.csrc = lay.Sig, g.c_q = static_cast<long long>(Ls) * F * F, g.c_s = static_cast<long long>(F) * F,
+        g.ldc = F;
+        if ((st = sel_gemm(c, g)) != RF_OK) return st;
+      }
+      // Rᵀ −= z_bᵀ wᵀ
+      {
+        SelGemm g{};
+        g.pa = lay.zbp, g.a_rows = rtrows, g.a_kext = F, g.a = op(Ft, 0, 0, 0, 0, 0);
+        g.pb = lay.Wp, g.b_rows = wrows, g.b_kext = m_max, g.b = op(D, 0, 0, m, 0, 0);
+        g.Q = Q, g.M = Ft, g.N = static_cast<int>(D), g.K = F;
+        g.alpha = -1.f, g.beta = 1.f;
+        g.out = lay.RT, g.o_q = static_cast<long long>(Ft) * D, g.ldo = D;
+        g.csrc = lay.RT, g.c_q = static_cast<long long>(Ft) * D, g.ldc = D;
+        if ((st = sel_gemm(c, g)) != RF_OK) return st;
+      }
+    }
+  }
+  return RF_OK;
+}

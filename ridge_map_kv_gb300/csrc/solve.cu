@@ -151,9 +151,12 @@ constexpr size_t kBlkSmem = sizeof(float) * kSolveBlock * kBlkLd;
 // triangle. A non-positive pivot records RF_ERR_NOT_SPD and continues with 1.
 // Column by column: the pivot, the column scale, then the trailing update with
 // two threads per row (no index divisions; the 129-float row pitch keeps both
-// the row and the column accesses free of bank conflicts).
-__global__ void __launch_bounds__(256) k_chol_base(float* A, int n, long long lda, int32_t* dev_status) {
+// the row and the column accesses free of bank conflicts). CTA b works on the
+// block at A + b * stride.
+__global__ void __launch_bounds__(256) k_chol_base(float* A, int n, long long lda, long long stride,
+                                                   int32_t* dev_status) {
   extern __shared__ float S[];
+  A += blockIdx.x * stride;
   for (int i = threadIdx.y; i < n; i += blockDim.y)
     for (int k = threadIdx.x; k < n; k += blockDim.x) S[i * kBlkLd + k] = A[i * lda + k];
   const int tid = threadIdx.y * blockDim.x + threadIdx.x;
@@ -193,12 +196,13 @@ struct LeafBlocks {
 // memory: W[i][j] = (δ_ij − Σ_{j<=k<i} L[i][k] W[k][j]) / L[i][i], thread j
 // computing column j of row i once rows < i are done (four partial sums keep the
 // dependent chain short); the upper triangle of W is zero. CTA b inverts the
-// block at (off[b], off[b]) of size size[b].
-__global__ void __launch_bounds__(128) k_trinv_base(const float* L0, long long ldl, float* W0, long long ldw,
-                                                    const __grid_constant__ LeafBlocks lb) {
+// block at (off[b], off[b]) of size size[b], in matrix blockIdx.y (L0 + y * sL,
+// W0 + y * sW).
+__global__ void __launch_bounds__(128) k_trinv_base(const float* L0, long long ldl, long long sL, float* W0,
+                                                    long long ldw, long long sW, const __grid_constant__ LeafBlocks lb) {
   const int off = lb.off[blockIdx.x], n = lb.size[blockIdx.x];
-  const float* L = L0 + static_cast<long long>(off) * ldl + off;
-  float* W = W0 + static_cast<long long>(off) * ldw + off;
+  const float* L = L0 + blockIdx.y * sL + static_cast<long long>(off) * ldl + off;
+  float* W = W0 + blockIdx.y * sW + static_cast<long long>(off) * ldw + off;
   extern __shared__ float S[];
   float* Wi = S + kSolveBlock * kBlkLd;
   for (int i = 0; i < n; ++i)
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(1024) k_trace_alpha(const double* G, const dou
   }
 }
 
-// H = (G + Gᵀ)/2 − n μ_x μ_xᵀ + αI, stored in fp64 and fp32.
+// H = (G + Gᵀ)/2 − n μ_x μ_xᵀ + αI, stored in fp32 and (when H64 is set) fp64.
 __global__ void k_build_h(const double* G, const double* mu_x, const double* n, const double* alpha, int d_in,
                           double* H64, float* H32) {
   const long long total = static_cast<long long>(d_in) * d_in;
@@ -272,7 +276,7 @@ __global__ void k_build_h(const double* G, const double* mu_x, const double* n, 
     const int i = static_cast<int>(e / d_in), j = static_cast<int>(e % d_in);
     double h = 0.5 * (G[e] + G[static_cast<long long>(j) * d_in + i]) - (*n) * mu_x[i] * mu_x[j];
     if (i == j) h += *alpha;
-    H64[e] = h;
+    if (H64 != nullptr) H64[e] = h;
     H32[e] = static_cast<float>(h);
   }
 }
@@ -386,13 +390,6 @@ static rf_status sgemm(SolveCtx& c, bool ta, bool tb, int M, int N, int K, float
 // and its remainder are exact in fp32). planes[j][p][r][c] for X_p [R][Cn], or
 // for X_p's transpose when `tr` (src then holds [P][Cn][R]).
 // --------------------------------------------------------------------------
-__device__ __forceinline__ void split3(float x, __nv_bfloat16& h, __nv_bfloat16& m, __nv_bfloat16& l) {
-  h = __float2bfloat16_rn(x);
-  const float r1 = x - __bfloat162float(h);
-  m = __float2bfloat16_rn(r1);
-  l = __float2bfloat16_rn(r1 - __bfloat162float(m));
-}
-
 // Row-major copy: 4 consecutive elements per thread-step.
 __global__ void __launch_bounds__(256) k_split3(const float* __restrict__ src, __nv_bfloat16* __restrict__ planes,
                                                 size_t n4, size_t plane) {
@@ -595,7 +592,7 @@ static rf_status trinv_lower(SolveCtx& c, const float* L, int n, long long ldl, 
   LeafBlocks lb;
   int count = 0;
   trinv_leaves(0, n, lb, count);
-  k_trinv_base<<<count, kSolveBlock, 2 * kBlkSmem, c.s>>>(L, ldl, W, ldw, lb);
+  k_trinv_base<<<count, kSolveBlock, 2 * kBlkSmem, c.s>>>(L, ldl, 0, W, ldw, 0, lb);
   rf_status st = cuda_check(cudaGetLastError(), "k_trinv_base launch");
   if (st != RF_OK) return st;
   return trinv_combine(c, L, n, ldl, W, ldw);
@@ -604,7 +601,7 @@ static rf_status trinv_lower(SolveCtx& c, const float* L, int n, long long ldl, 
 // In-place lower Cholesky of the n x n matrix A (ld lda); n % 128 == 0.
 static rf_status chol_lower(SolveCtx& c, float* A, int n, long long lda, float* winv) {
   if (n <= kSolveBlock) {
-    k_chol_base<<<1, dim3(32, 8), kBlkSmem, c.s>>>(A, n, lda, c.dev_status);
+    k_chol_base<<<1, dim3(32, 8), kBlkSmem, c.s>>>(A, n, lda, 0, c.dev_status);
     return cuda_check(cudaGetLastError(), "k_chol_base launch");
   }
   const int n1 = split_point(n), n2 = n - n1;
@@ -677,6 +674,71 @@ static rf_status check_solve_desc(const rf_calib_desc* d) {
 
 static uint64_t g_chol_attr = 0, g_trinv_attr = 0;
 
+static rf_status solve_kernel_attrs() {
+  rf_status s = set_smem_attr(reinterpret_cast<const void*>(&k_chol_base), kBlkSmem, &g_chol_attr);
+  if (s != RF_OK) return s;
+  return set_smem_attr(reinterpret_cast<const void*>(&k_trinv_base), 2 * kBlkSmem, &g_trinv_attr);
+}
+
+rf_status centre_system(const double* G, const double* sx, const double* sy, const int64_t* n, int d_in, long long n_y,
+                        double lambda, int alpha_mode, double* mu_x, double* mu_y, double* n_out, double* alpha,
+                        double* alpha_out, double* H64, float* H32, int sms, cudaStream_t s) {
+  const int eb = 8 * sms;
+  k_means<<<eb, 256, 0, s>>>(sx, sy, n, d_in, n_y, mu_x, mu_y, n_out);
+  k_trace_alpha<<<1, 1024, 0, s>>>(G, mu_x, n_out, d_in, lambda, alpha_mode, alpha, alpha_out);
+  k_build_h<<<eb, 256, 0, s>>>(G, mu_x, n_out, alpha, d_in, H64, H32);
+  return cuda_check(cudaGetLastError(), "centring launches");
+}
+
+// Right-looking blocked factorisation over the batch, one 128-wide column block
+// at a time: the diagonal block (one CTA per matrix), its inverse (the diagonal
+// block of L^-1), the panel below it times that inverse's transpose, then the
+// trailing update. The panel product runs in place: with a single 128-wide
+// output column tile, each CTA reads and then writes only its own 128 rows.
+// L^-1's off-diagonal row blocks follow bottom-up from
+//   (L^-1)[i][0:i] = −(L^-1)[i][i] · (L[i][0:i] · (L^-1)[0:i][0:i]).
+rf_status chol_inv_batched(float* A, long long lda, long long stride, float* Linv, long long ldi, int n, int batch,
+                           float* tmp, int32_t* dev_status, int sms, cudaStream_t s) {
+  rf_status st = solve_kernel_attrs();
+  if (st != RF_OK) return st;
+  const long long stride_inv = static_cast<long long>(n) * ldi;
+  SolveCtx c{s, sms, nullptr, nullptr, dev_status};
+  if ((st = cuda_check(cudaMemsetAsync(Linv, 0, sizeof(float) * stride_inv * batch, s), "zero L^-1")) != RF_OK)
+    return st;
+  LeafBlocks one;
+  one.off[0] = 0;
+  one.size[0] = kSolveBlock;
+  const int nb = n / kSolveBlock;
+  for (int kb = 0; kb < nb; ++kb) {
+    const long long o = static_cast<long long>(kb) * kSolveBlock;
+    const int r = n - static_cast<int>(o) - kSolveBlock;
+    float* Akk = A + o * lda + o;
+    k_chol_base<<<batch, dim3(32, 8), kBlkSmem, s>>>(Akk, kSolveBlock, lda, stride, dev_status);
+    k_trinv_base<<<dim3(1, batch), kSolveBlock, 2 * kBlkSmem, s>>>(Akk, lda, stride, Linv + o * ldi + o, ldi,
+                                                                   stride_inv, one);
+    if ((st = cuda_check(cudaGetLastError(), "batched diagonal block launches")) != RF_OK) return st;
+    if (r == 0) break;
+    float* A21 = A + (o + kSolveBlock) * lda + o;
+    if ((st = sgemm(c, false, true, r, kSolveBlock, kSolveBlock, 1.f, A21, lda, stride, Linv + o * ldi + o, ldi,
+                    stride_inv, 0.f, A21, lda, stride, batch)) != RF_OK)
+      return st;
+    if ((st = sgemm(c, false, true, r, r, kSolveBlock, -1.f, A21, lda, stride, A21, lda, stride, 1.f,
+                    A21 + kSolveBlock, lda, stride, batch)) != RF_OK)
+      return st;
+  }
+  const long long stride_tmp = static_cast<long long>(kSolveBlock) * n;
+  for (int i = 1; i < nb; ++i) {
+    const long long oi = static_cast<long long>(i) * kSolveBlock;
+    if ((st = sgemm(c, false, false, kSolveBlock, static_cast<int>(oi), static_cast<int>(oi), 1.f, A + oi * lda, lda,
+                    stride, Linv, ldi, stride_inv, 0.f, tmp, n, stride_tmp, batch)) != RF_OK)
+      return st;
+    if ((st = sgemm(c, false, false, kSolveBlock, static_cast<int>(oi), kSolveBlock, -1.f, Linv + oi * ldi + oi, ldi,
+                    stride_inv, tmp, n, stride_tmp, 0.f, Linv + oi * ldi, ldi, stride_inv, batch)) != RF_OK)
+      return st;
+  }
+  return RF_OK;
+}
+
 }  // namespace rf
 
 using namespace rf;
@@ -706,8 +768,7 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
     return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", lay.bytes, workspace_bytes);
   int sms = 0;
   if ((s = current_device(&sms)) != RF_OK) return s;
-  if ((s = set_smem_attr(reinterpret_cast<const void*>(&k_chol_base), kBlkSmem, &g_chol_attr)) != RF_OK) return s;
-  if ((s = set_smem_attr(reinterpret_cast<const void*>(&k_trinv_base), 2 * kBlkSmem, &g_trinv_attr)) != RF_OK) return s;
+  if ((s = solve_kernel_attrs()) != RF_OK) return s;
 
   const int di = static_cast<int>(desc->d_in), dout = static_cast<int>(desc->d_out), P = static_cast<int>(desc->n_maps);
   SolveCtx c{static_cast<cudaStream_t>(stream), sms, lay.tmp, lay.tmp2, dev_status};

@@ -337,3 +337,59 @@ extern "C" rf_status rf_rope_rows(const rf_bf16* in, rf_bf16* out, int64_t n_row
                                      pos_offset, nullptr, nullptr, theta, inverse ? -1.0f : 1.0f);
   return cuda_check(cudaGetLastError(), "k_rope_rows launch");
 }
+
+namespace rf {
+
+// out[t][j] = in[t][j] for t < n_rows, j < width (width % 8 == 0), 16 bytes per step.
+__global__ void __launch_bounds__(256) k_copy_rows(const __nv_bfloat16* __restrict__ in, __nv_bfloat16* __restrict__ out,
+                                                   long long n_rows, long long ld_in, long long ld_out, int width) {
+  const int per_row = width / 8;
+  const long long total = n_rows * per_row;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long t = i / per_row;
+    const int c = static_cast<int>(i - t * per_row) * 8;
+    *reinterpret_cast<uint4*>(out + t * ld_out + c) = __ldg(reinterpret_cast<const uint4*>(in + t * ld_in + c));
+  }
+}
+
+}  // namespace rf
+
+extern "C" rf_status rf_concat_layers(const rf_bf16* src, int64_t n_layers, int64_t layer_stride, int64_t n_rows,
+                                      int64_t ld_src, int64_t n_heads, int64_t head_dim, double theta,
+                                      int64_t pos_offset, rf_bf16* out, int64_t ld_out, rf_stream_t stream) {
+  clear_error();
+  if (n_layers < 0 || n_rows < 0 || n_heads <= 0 || head_dim <= 0 || !(theta >= 0.0))
+    return fail(RF_ERR_INVALID_ARG, "need n_layers, n_rows >= 0, n_heads, head_dim > 0, theta >= 0");
+  if (theta > 0.0 && head_dim != 64 && head_dim != 128)
+    return fail(RF_ERR_SHAPE, "head_dim must be 64 or 128 when keys are un-roped");
+  const int64_t W = n_heads * head_dim;
+  if (W % 8 != 0) return fail(RF_ERR_SHAPE, "n_heads * head_dim must be a multiple of 8");
+  if (ld_src < W || ld_src % 8 != 0 || ld_out < n_layers * W || ld_out % 8 != 0 || layer_stride % 8 != 0 ||
+      (n_layers > 1 && layer_stride < ld_src * n_rows))
+    return fail(RF_ERR_ALIGN, "need ld_src >= W, ld_out >= n_layers*W, layer_stride >= ld_src*n_rows, "
+                              "all multiples of 8");
+  if (n_layers == 0 || n_rows == 0) return RF_OK;
+  if (!src || !out) return fail(RF_ERR_INVALID_ARG, "src and out must be non-NULL");
+  if (!aligned16(src) || !aligned16(out)) return fail(RF_ERR_ALIGN, "src and out must be 16-byte aligned");
+  int sms = 0;
+  rf_status st = current_device(&sms);
+  if (st != RF_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __nv_bfloat16* in = reinterpret_cast<const __nv_bfloat16*>(src);
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+  ProfScope prof(s, RF_STAGE_UNROPE);
+  for (int64_t l = 0; l < n_layers; ++l) {
+    const long long total = theta > 0.0 ? n_rows * n_heads * (head_dim / 16) : n_rows * (W / 8);
+    const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 16LL * sms));
+    if (theta > 0.0) {
+      k_rope_rows<<<blocks, 256, 0, s>>>(in + l * layer_stride, o + l * W, n_rows, ld_src, ld_out,
+                                         static_cast<int>(n_heads), static_cast<int>(head_dim), n_rows, pos_offset,
+                                         nullptr, nullptr, theta, -1.0f);
+    } else {
+      k_copy_rows<<<blocks, 256, 0, s>>>(in + l * layer_stride, o + l * W, n_rows, ld_src, ld_out,
+                                         static_cast<int>(W));
+    }
+  }
+  return cuda_check(cudaGetLastError(), "rf_concat_layers launches");
+}

@@ -48,6 +48,8 @@ def test_status_strings_and_version():
     for s in ("compact", "map_gemm", "kv_gemm", "calib_gemm", "xmodel_gemm"):
         assert s in [rf.rf_stage_name(i) for i in range(1, 13)]
     assert rf.rf_stage_name(12) == "value_rescale"
+    assert [rf.rf_stage_name(i) for i in (18, 19, 20, 21)] == ["select_gemm", "select_factor", "select_score",
+                                                               "select_split"]
 
 
 def _fill_desc(**kw):
@@ -157,3 +159,51 @@ def test_static_fill_scratch_constant_matches_header():
     txt = open(os.path.join(ROOT, "include", "rf.h")).read()
     assert "RF_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)" in txt
     assert rf.RF_STATIC_SCRATCH_BYTES == 64 * 1024 * 1024
+
+
+def _select_desc(**kw):
+    d = dict(L_src=6, F=256, n_targets=4, d_out=256, head_dim=128, k=3, n_kinds=2, group=0)
+    d.update(kw)
+    return rf.rf_select_desc(**d)
+
+
+def test_select_workspace_size_follows_the_layout():
+    base = rf.rf_select_workspace_bytes(_select_desc())
+    assert base > 0
+    # per-pass buffers scale with the targets per pass; the per-kind Gram does not
+    one = rf.rf_select_workspace_bytes(_select_desc(group=1))
+    two = rf.rf_select_workspace_bytes(_select_desc(group=2))
+    assert 0 < one < two < base
+    assert rf.rf_select_workspace_bytes(_select_desc(group=4)) == base
+    for bad in (dict(F=100), dict(d_out=300), dict(k=7), dict(n_kinds=3), dict(head_dim=96),
+                dict(L_src=300), dict(k=0)):
+        assert rf.rf_select_workspace_bytes(_select_desc(**bad)) == 0, bad
+
+
+def test_select_and_concat_validate_on_the_host():
+    st = rf.calib_stats_struct(256, 256, 256, 256, 256, 256)
+    no_syy = rf.calib_stats_struct(256, 256, 256, 256, 256)
+    d = _select_desc(n_kinds=1)
+    wsb = rf.rf_select_workspace_bytes(d)
+    cases = [
+        (dict(desc=_select_desc(F=100), stats=[st]), rf.RF_ERR_SHAPE),
+        (dict(desc=_select_desc(k=9), stats=[st]), rf.RF_ERR_INVALID_ARG),
+        (dict(desc=d, stats=[no_syy]), rf.RF_ERR_INVALID_ARG),
+        (dict(desc=d, stats=[st], alpha_mode=5), rf.RF_ERR_INVALID_ARG),
+        (dict(desc=d, stats=[st], lam=-1.0), rf.RF_ERR_INVALID_ARG),
+        (dict(desc=d, stats=[st], workspace_bytes=wsb - 1), rf.RF_ERR_WORKSPACE),
+    ]
+    for kw, want in cases:
+        args = dict(lam=0.01, alpha_mode=rf.RF_ALPHA_TRACE, workspace_bytes=wsb)
+        args.update(kw)
+        with pytest.raises(rf.RFError) as ei:
+            rf.rf_select_sources(args["desc"], args["stats"], args["lam"], args["alpha_mode"], 256, None, None, 256,
+                                 args["workspace_bytes"], stream=0)
+        assert ei.value.status == want, kw
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_concat_layers(256, 3, 1024 * 10, 10, 1024, 8, 128, 1e6, 0, 256, 2048, stream=0)
+    assert ei.value.status == rf.RF_ERR_ALIGN
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_concat_layers(256, 3, 768 * 10, 10, 768, 8, 96, 1e6, 0, 256, 3 * 768, stream=0)
+    assert ei.value.status == rf.RF_ERR_SHAPE
+    rf.rf_concat_layers(256, 3, 768 * 10, 0, 768, 8, 96, 0.0, 0, 256, 3 * 768, stream=0)   # no rows: nothing to do

@@ -1,0 +1,259 @@
+"""GPU parity of the cross-layer source selection (rf_select_sources), the layer
+concatenation that builds its features (rf_concat_layers) and the calibration's
+per-column sums of squares, against the fp64 oracle.
+
+Cross-model KV cache transfer digest, "소스 층은 몇 개가 필요한가" (greedy forward
+selection by head-mean R²) and "층 교차 소스 선택" (k source layers per target
+layer, chosen by the un-roped keys' and the values' head-mean R², all heads
+sharing them).
+
+Comparison. The selection is an argmax over floating-point scores, taken in fp64
+on the oracle and from fp32 factorisations on the GPU, so near-ties may resolve
+differently. The oracle therefore replays the GPU's own path: every score the
+GPU reports must equal the oracle's score of the same layer set within TOL_R2
+(NaN exactly where a layer was already chosen), each GPU choice must be within
+TOL_R2 of the oracle's best score at that step, and where the oracle's own
+greedy path has a margin above 2·TOL_R2 at every step the two paths must be
+identical.
+
+TOL_R2 = 2e-4 (absolute, on scores in [0, 1]). The GPU's Schur blocks carry fp32
+rounding of the Gram (relative 6e-8) amplified by the condition of the ridge
+system Gc_SS + αI. Measured on these inputs the largest score error is about
+1e-5; the bound leaves a 20x margin.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import ridge_map_kv_gb300 as rf
+import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL_R2 = 2e-4
+KERNELS = pytest.mark.parametrize("flags", [rf.RF_FLAG_SINGLE_CTA, rf.RF_FLAG_CTA_PAIR], ids=["single-cta", "cta-pair"])
+
+
+# --------------------------------------------------------------------------- #
+# helpers
+# --------------------------------------------------------------------------- #
+def _zero_stats(D, Ft, T):
+    return {"G": torch.zeros((D, D), dtype=torch.float64, device=DEV),
+            "C": torch.zeros((T, D, Ft), dtype=torch.float64, device=DEV),
+            "sx": torch.zeros(D, dtype=torch.float64, device=DEV),
+            "sy": torch.zeros((T, Ft), dtype=torch.float64, device=DEV),
+            "syy": torch.zeros((T, Ft), dtype=torch.float64, device=DEV),
+            "n": torch.zeros(1, dtype=torch.int64, device=DEV)}
+
+
+def _struct(st):
+    return rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"], st["syy"])
+
+
+def _rows_and_stats(cfg, kinds, n_rows, chunk_rows=2048):
+    """GPU sums from rf_calib_accumulate and oracle sums from the same bf16 rows."""
+    gpu, ora = [], []
+    for kind in kinds:
+        ld = synth.selection_loadings(cfg, kind, DEV)
+        st = _zero_stats(cfg.D, cfg.F, cfg.L_tgt)
+        cd = rf.rf_calib_desc(d_in=cfg.D, d_out=cfg.F, n_maps=cfg.L_tgt)
+        o = None
+        for ch in range(n_rows // chunk_rows):
+            r = synth.selection_rows(cfg, kind, chunk_rows, ch, DEV, ld)
+            rf.rf_calib_accumulate(cd, r["X"], cfg.D, r["Y"], cfg.F, chunk_rows * cfg.F, chunk_rows, _struct(st))
+            oc = O.calib_stats(O.bf16_bits_to_f64(synth.bits(r["X"])), O.bf16_bits_to_f64(synth.bits(r["Y"])))
+            o = oc if o is None else O.add_stats(o, oc)
+        torch.cuda.synchronize()
+        gpu.append(st)
+        ora.append(o)
+    return gpu, ora
+
+
+def _select(cfg, stats, k, lam, mode, group=0, flags=0, head_dim=None):
+    nk = len(stats)
+    d = rf.rf_select_desc(L_src=cfg.L_src, F=cfg.F, n_targets=cfg.L_tgt, d_out=cfg.F,
+                          head_dim=head_dim or cfg.hd, k=k, n_kinds=nk, group=group, flags=flags)
+    wsb = rf.rf_select_workspace_bytes(d)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    sel = torch.full((cfg.L_tgt, k), -1, dtype=torch.int32, device=DEV)
+    r2 = torch.empty((nk, cfg.L_tgt, k, cfg.L_src), dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rf.rf_select_sources(d, [_struct(s) for s in stats], lam, mode, sel, r2, status, ws, wsb)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return sel.cpu().numpy(), r2.cpu().numpy().astype(np.float64)
+
+
+def _check_against_oracle(cfg, ostats, sel, r2, k, lam, mode, head_dim=None):
+    hd = head_dim or cfg.hd
+    L = cfg.L_src
+    # valid choices
+    for t in range(cfg.L_tgt):
+        assert len(set(sel[t].tolist())) == k and sel[t].min() >= 0 and sel[t].max() < L
+    _, replay = O.select_sources(ostats, L, cfg.F, hd, k, lam, mode, path=sel)
+    np.testing.assert_array_equal(np.isnan(r2), np.isnan(replay))
+    err = np.nanmax(np.abs(r2 - replay))
+    assert err <= TOL_R2, f"largest score error {err:.3g}"
+    joint = replay.mean(axis=0)                       # [T, k, L]
+    for t in range(cfg.L_tgt):
+        for j in range(k):
+            assert joint[t, j, sel[t, j]] >= np.nanmax(joint[t, j]) - TOL_R2
+    # where the oracle's own path is decided by margins above 2·TOL, the paths agree
+    osel, otab = O.select_sources(ostats, L, cfg.F, hd, k, lam, mode)
+    oj = otab.mean(axis=0)
+    for t in range(cfg.L_tgt):
+        for j in range(k):
+            row = np.sort(oj[t, j][~np.isnan(oj[t, j])])[::-1]
+            if row.size > 1 and row[0] - row[1] <= 2 * TOL_R2:
+                break
+            assert sel[t, j] == osel[t, j], (t, j)
+    return err
+
+
+# --------------------------------------------------------------------------- #
+# rf_concat_layers and Σy²
+# --------------------------------------------------------------------------- #
+def test_concat_layers_unropes_keys_and_copies_values():
+    L, N, H, hd, theta, off = 3, 300, 2, 128, 1.0e6, 7
+    W = H * hd
+    src = synth._randn((L, N, W + 16), 91, DEV)       # row pitch with padding
+    out = torch.full((N, L * W + 8), float("nan"), dtype=torch.bfloat16, device=DEV)
+    rf.rf_concat_layers(src, L, N * (W + 16), N, W + 16, H, hd, theta, off, out, L * W + 8)
+    vals = torch.empty((N, L * W), dtype=torch.bfloat16, device=DEV)
+    rf.rf_concat_layers(src, L, N * (W + 16), N, W + 16, H, hd, 0.0, 0, vals, L * W)
+    torch.cuda.synchronize()
+    s = O.bf16_bits_to_f64(synth.bits(src[:, :, :W])).reshape(L, N, H, hd)
+    ref = O.xmodel_features(s, list(range(L)), np.arange(N) + off, theta)
+    got = O.bf16_bits_to_f64(synth.bits(out[:, :L * W]))
+    rel = np.abs(got - ref).max() / np.abs(ref).max()
+    assert rel < 8e-3                                  # bf16 output rounding
+    assert torch.isnan(out[:, L * W:].float()).all()   # padding untouched
+    for l in range(L):
+        assert torch.equal(vals[:, l * W:(l + 1) * W].view(torch.int16), src[l, :, :W].view(torch.int16))
+
+
+def test_calibration_sums_of_squares_match_the_oracle():
+    cfg = synth.SELECT_SMALL
+    gpu, ora = _rows_and_stats(cfg, [1], 4096)
+    g, o = gpu[0], ora[0]
+    np.testing.assert_allclose(g["syy"].cpu().numpy(), o["syy"], rtol=1e-6)
+    np.testing.assert_allclose(g["sy"].cpu().numpy(), o["sy"], rtol=1e-6, atol=1e-6 * np.abs(o["sy"]).max())
+    # without syy the accumulation leaves it alone and still works
+    st = _zero_stats(cfg.D, cfg.F, cfg.L_tgt)
+    cd = rf.rf_calib_desc(d_in=cfg.D, d_out=cfg.F, n_maps=cfg.L_tgt)
+    r = synth.selection_rows(cfg, 1, 512, 0, DEV)
+    rf.rf_calib_accumulate(cd, r["X"], cfg.D, r["Y"], cfg.F, 512 * cfg.F, 512,
+                           rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"]))
+    torch.cuda.synchronize()
+    assert int(st["n"].item()) == 512 and float(st["syy"].abs().max()) == 0.0
+
+
+# --------------------------------------------------------------------------- #
+# rf_select_sources
+# --------------------------------------------------------------------------- #
+@pytest.fixture(scope="module")
+def small_stats():
+    return _rows_and_stats(synth.SELECT_SMALL, [0, 1], synth.SELECT_SMALL.n)
+
+
+@KERNELS
+def test_select_keys_and_values_jointly_matches_oracle(small_stats, flags):
+    cfg = synth.SELECT_SMALL
+    gpu, ora = small_stats
+    sel, r2 = _select(cfg, gpu, cfg.k, cfg.lam, rf.RF_ALPHA_TRACE, flags=flags)
+    _check_against_oracle(cfg, ora, sel, r2, cfg.k, cfg.lam, "trace")
+
+
+def test_select_least_squares_one_kind_in_passes_of_one_target(small_stats):
+    # lambda = 0 (the single-layer survey's least squares), values alone, one target per pass
+    cfg = synth.SELECT_SMALL
+    gpu, ora = small_stats
+    sel, r2 = _select(cfg, [gpu[1]], cfg.k, 0.0, rf.RF_ALPHA_ABSOLUTE, group=1)
+    _check_against_oracle(cfg, [ora[1]], sel, r2, cfg.k, 0.0, "absolute")
+
+
+def test_select_every_layer_and_single_layer_table(small_stats):
+    # k = L_src orders all layers; step 0 is the single-layer R² table; one-column heads
+    cfg = synth.SELECT_SMALL
+    gpu, ora = small_stats
+    sel, r2 = _select(cfg, [gpu[0]], cfg.L_src, 0.05, rf.RF_ALPHA_ABSOLUTE, group=3, head_dim=64)
+    _check_against_oracle(cfg, [ora[0]], sel, r2, cfg.L_src, 0.05, "absolute", head_dim=64)
+    for t in range(cfg.L_tgt):
+        assert sorted(sel[t].tolist()) == list(range(cfg.L_src))
+        single = O.selection_scores([ora[0]], [0], cfg.F, 64, 0.05, "absolute")   # layer 0 alone
+        assert abs(r2[0, t, 0, 0] - single[0, t]) <= TOL_R2
+    # scores never fall along the path
+    best = np.array([[r2[0, t, j, sel[t, j]] for j in range(cfg.L_src)] for t in range(cfg.L_tgt)])
+    assert np.all(np.diff(best, axis=1) >= -TOL_R2)
+
+
+def test_select_handles_a_target_without_variance():
+    # a constant target has TSS = 0 in every head: its scores are 0 and the choice is layer 0 first
+    cfg = synth.SELECT_SMALL
+    ld = synth.selection_loadings(cfg, 0, DEV)
+    r = synth.selection_rows(cfg, 0, 2048, 0, DEV, ld)
+    Y = r["Y"].clone()
+    Y[2] = 0.75
+    st = _zero_stats(cfg.D, cfg.F, cfg.L_tgt)
+    cd = rf.rf_calib_desc(d_in=cfg.D, d_out=cfg.F, n_maps=cfg.L_tgt)
+    rf.rf_calib_accumulate(cd, r["X"], cfg.D, Y, cfg.F, 2048 * cfg.F, 2048, _struct(st))
+    torch.cuda.synchronize()
+    o = O.calib_stats(O.bf16_bits_to_f64(synth.bits(r["X"])), O.bf16_bits_to_f64(synth.bits(Y)))
+    sel, r2 = _select(cfg, [st], 2, cfg.lam, rf.RF_ALPHA_TRACE)
+    assert np.all(r2[0, 2][~np.isnan(r2[0, 2])] == 0.0) and list(sel[2]) == [0, 1]
+    _check_against_oracle(cfg, [o], sel, r2, 2, cfg.lam, "trace")
+
+
+# --------------------------------------------------------------------------- #
+# Full size: 40 -> 64 layers, 8 x 128 heads, k = 8, the model's population sums
+# --------------------------------------------------------------------------- #
+def _sub_stats(st, t, layers, F):
+    """The sums restricted to the features of `layers` and to target t (host fp64)."""
+    idx = torch.cat([torch.arange(s * F, (s + 1) * F, device=DEV) for s in layers])
+    return {"G": st["G"][idx][:, idx].cpu().numpy(), "C": st["C"][t][idx].cpu().numpy()[None],
+            "sx": st["sx"][idx].cpu().numpy(), "sy": st["sy"][t].cpu().numpy()[None],
+            "syy": st["syy"][t].cpu().numpy()[None], "n": int(st["n"].item())}
+
+
+def _trace_alpha(st, lam, D):
+    # alpha = lambda tr(Gc)/D over all source features, Gc = G - n mu mu^T (its diagonal only)
+    n = float(st["n"].item())
+    diag = st["G"].diagonal().cpu().numpy()
+    mu = st["sx"].cpu().numpy() / n
+    return lam * float((diag - n * mu * mu).sum()) / D
+
+
+@pytest.mark.slow
+def test_select_full_size_sampled():
+    cfg = synth.SELECT_XMODEL
+    stats = [synth.selection_population_stats(cfg, kind, DEV) for kind in (0, 1)]
+    torch.cuda.synchronize()
+    sel, r2 = _select(cfg, stats, cfg.k, cfg.lam, rf.RF_ALPHA_TRACE, group=8)
+    for t in range(cfg.L_tgt):
+        assert len(set(sel[t].tolist())) == cfg.k and 0 <= sel[t].min() and sel[t].max() < cfg.L_src
+        best = [r2[:, t, j, sel[t, j]].mean() for j in range(cfg.k)]
+        assert np.all(np.diff(best) >= -TOL_R2)
+        assert np.all((r2[:, t][~np.isnan(r2[:, t])] >= -TOL_R2) & (r2[:, t][~np.isnan(r2[:, t])] <= 1 + TOL_R2))
+    alphas = [_trace_alpha(s, cfg.lam, cfg.D) for s in stats]
+
+    def oracle_score(t, layers):
+        return np.mean([O.selection_scores([_sub_stats(stats[kd], t, layers, cfg.F)], list(range(len(layers))),
+                                           cfg.F, cfg.hd, alphas[kd], "absolute")[0, 0] for kd in (0, 1)])
+
+    # the single-layer table of three targets, every candidate
+    for t in (0, 31, 63):
+        for s in range(cfg.L_src):
+            assert abs(r2[:, t, 0, s].mean() - oracle_score(t, [s])) <= TOL_R2, (t, s)
+    # later steps of two targets along the GPU's path: the choice and the runner-up
+    for t in (0, 63):
+        for j in (1, 2, cfg.k - 1):
+            chosen = sel[t, :j].tolist()
+            joint = r2[:, t, j].mean(axis=0)
+            order = [s for s in np.argsort(-np.nan_to_num(joint, nan=-np.inf)) if s not in chosen]
+            a, b = oracle_score(t, chosen + [order[0]]), oracle_score(t, chosen + [order[1]])
+            assert order[0] == sel[t, j]
+            assert abs(joint[order[0]] - a) <= TOL_R2 and abs(joint[order[1]] - b) <= TOL_R2
+            assert a >= b - TOL_R2
