@@ -19,6 +19,7 @@ sample of the same workload, and prints the same metric.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -48,6 +49,12 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the calibration, solve and cross-model rows")
+    ap.add_argument("--selection-only", action="store_true",
+                    help="time only the source-selection row (all-source calibration + greedy selection)")
+    ap.add_argument("--select-targets", type=int, default=0,
+                    help="target layers for --selection-only (0 = the workload's 64; fewer for a short capture)")
+    ap.add_argument("--select-sources", type=int, default=0,
+                    help="source layers for --selection-only (0 = the workload's 40; fewer for a small capture)")
     ap.add_argument("--gemm", choices=["default", "single", "pair"], default="default",
                     help="tensor-core GEMM kernel: one CTA per 128x256 tile, or a CTA pair per 256x256 tile")
     ap.add_argument("--workload", choices=sorted(workloads()), default=WORKLOAD,
@@ -266,6 +273,17 @@ def gemm_flags(name):
 # --------------------------------------------------------------------------- #
 # Our arm
 # --------------------------------------------------------------------------- #
+def run_selection_only(args):
+    import json
+
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = measured_peaks()
+    row = run_selection(dev, peaks["bf16_tflops"], gemm_flags(args.gemm), args.select_targets, args.select_sources)
+    print(json.dumps({"selection": row}))
+
+
 def run_ours(args):
     import torch
 
@@ -712,7 +730,98 @@ def run_extras(dev, peak_tflops, flags=0):
         "fill_ms": ms_fill, "fill_tflops": f_flops / (ms_fill / 1e3) / 1e12,
         "fill_frac_of_bf16_peak": f_flops / (ms_fill / 1e3) / 1e12 / peak_tflops,
         "fill_row_layers_per_s": n_fill * c.P / (ms_fill / 1e3), "fill_stages_ms": st_fill}
+    del inp, kc, vc, ws, Wkv, vs, x_exact
+    torch.cuda.empty_cache()
+
+    out["next4a_source_selection_xmodel"] = run_selection(dev, peak_tflops, flags)
     return out
+
+
+def run_selection(dev, peak_tflops, flags=0, n_targets=0, n_sources=0):
+    """Greedy source-layer selection for the 40 -> 64 layer pair (8 x 128 heads,
+    k = 8, keys and values scored jointly): the calibration sums over all 40
+    source layers (40,960 features) from 131,072 rows, then rf_select_sources.
+    Rows are generated in chunks outside the timed calls."""
+    import torch
+
+    import ridge_map_kv_gb300 as rf
+    import synth
+    stream = torch.cuda.current_stream(dev)
+    cfg = synth.SELECT_XMODEL
+    if n_sources > 0:
+        cfg = dataclasses.replace(cfg, L_src=max(cfg.k, n_sources))
+    T = cfg.L_tgt if n_targets <= 0 else min(n_targets, cfg.L_tgt)
+    D, F, chunk = cfg.D, cfg.F, 16384
+    cd = rf.rf_calib_desc(d_in=D, d_out=F, n_maps=T, flags=flags)
+    stats, calib_ms = [], []
+    for kind in (0, 1):
+        ld = synth.selection_loadings(cfg, kind, dev)
+        st = {"G": torch.zeros((D, D), dtype=torch.float64, device=dev),
+              "C": torch.zeros((T, D, F), dtype=torch.float64, device=dev),
+              "sx": torch.zeros(D, dtype=torch.float64, device=dev),
+              "sy": torch.zeros((T, F), dtype=torch.float64, device=dev),
+              "syy": torch.zeros((T, F), dtype=torch.float64, device=dev),
+              "n": torch.zeros(1, dtype=torch.int64, device=dev)}
+        cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"], st["syy"])
+        total = 0.0
+        for ch in range(cfg.n // chunk):
+            r = synth.selection_rows(cfg, kind, chunk, ch, dev, ld)
+            Y = r["Y"][:T].contiguous()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            rf.rf_calib_accumulate(cd, r["X"], D, Y, F, chunk * F, chunk, cs)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            total += e0.elapsed_time(e1)
+            del r, Y
+        stats.append((st, cs))
+        calib_ms.append(total)
+        del ld
+    torch.cuda.empty_cache()
+    d = rf.rf_select_desc(L_src=cfg.L_src, F=F, n_targets=T, d_out=F, head_dim=cfg.hd, k=cfg.k, n_kinds=2,
+                          group=min(8, T), flags=flags)
+    wsb = rf.rf_select_workspace_bytes(d)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    sel = torch.empty((T, cfg.k), dtype=torch.int32, device=dev)
+    r2 = torch.empty((2, T, cfg.k, cfg.L_src), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ms, stages = _timed(lambda: rf.rf_select_sources(d, [cs for _, cs in stats], cfg.lam, rf.RF_ALPHA_TRACE, sel, r2,
+                                                     status, ws, wsb), 1, stream)
+    assert int(status.item()) == 0
+    # fp32-accurate products (each is six bf16 plane products on the tensor cores):
+    # per pass of Q problems and step j (m = jF features chosen), the scores of all
+    # L_src candidates (2 D F Ft), and for j < k-1 the new factor column
+    # (2 D F m + 2 D F²), the Schur-block and cross-term updates (2 D F² + 2 Ft F D)
+    # and z_b (2 Ft F²).
+    n_prob = 2 * T
+    prod = 0.0
+    for j in range(cfg.k):
+        m = j * F
+        prod += 2.0 * D * F * F
+        if j < cfg.k - 1:
+            prod += 2.0 * D * F * m + 2.0 * D * F * F + 2.0 * D * F * F + 2.0 * F * F * D + 2.0 * F * F * F
+    prod *= n_prob
+    gm = stages.get("select_gemm", ms)
+    # fp32 SIMT factorisation of every candidate's F x F Schur block at every step
+    # (Cholesky F³/3 and triangular inverse F³/3, algorithmic)
+    fact = n_prob * cfg.L_src * cfg.k * (2.0 * F ** 3 / 3.0)
+    sustained = measured_peaks().get("bf16_tflops_sustained") or peak_tflops   # seconds-long timed region
+    fm = stages.get("select_factor", ms)
+    cflops = 1.0 * cfg.n * D * (D + 1) + 2.0 * cfg.n * D * F * T
+    return {
+        "workload": f"{cfg.name}: source selection for {T} target layers, keys and values jointly, "
+                    f"calibration sums over all {cfg.L_src} source layers ({D} features) from {cfg.n} rows",
+        "calibration_ms_per_kind": calib_ms,
+        "calibration_tflops": cflops / (sum(calib_ms) / 2 / 1e3) / 1e12,
+        "select_ms": ms, "select_stages_ms": stages,
+        "select_products_fp32_tflops": prod / (gm / 1e3) / 1e12,
+        "select_products_bf16_plane_tflops": 6.0 * prod / (gm / 1e3) / 1e12,
+        "select_products_frac_of_sustained_bf16_peak": 6.0 * prod / (gm / 1e3) / 1e12 / sustained,
+        "select_factor_fp32_tflops": fact / (fm / 1e3) / 1e12,
+        "select_workspace_bytes": wsb,
+        "first_target_layers": sel[0].tolist(),
+        "pages_context": "47-87 min to fit one pair's mapper on 8 H100s (XᵀX dominant; whole fit, context only)"}
 
 
 # --------------------------------------------------------------------------- #
@@ -753,6 +862,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.selection_only:
+        run_selection_only(args)
     else:
         run_ours(args)
 

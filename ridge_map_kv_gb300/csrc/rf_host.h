@@ -73,10 +73,10 @@ rf_status centre_system(const double* G, const double* sx, const double* sy, con
                         double lambda, int alpha_mode, double* mu_x, double* mu_y, double* n_out, double* alpha,
                         double* alpha_out, double* H64, float* H32, int sms, cudaStream_t s);
 
-// For b < batch (solve.cu): the SPD n x n matrix A + b*stride (ld lda, n % 128 == 0)
-// is overwritten by its lower Cholesky factor L_b (blocks above the diagonal keep
-// stale values), and Linv + b*n*ldi receives L_b^-1 (lower, zero above). fp32.
-// tmp holds batch * 128 * n floats. A non-positive pivot records RF_ERR_NOT_SPD.
+// For b < batch (solve.cu): Linv + b*n*ldi receives L_b^-1 (lower, zero above) of
+// the SPD n x n matrix A + b*stride = L_b L_bᵀ (ld lda, n % 128 == 0), in fp32. A is
+// used as scratch (its contents are lost). tmp holds batch * n * n / 4 floats.
+// A non-positive pivot records RF_ERR_NOT_SPD.
 rf_status chol_inv_batched(float* A, long long lda, long long stride, float* Linv, long long ldi, int n, int batch,
                            float* tmp, int32_t* dev_status, int sms, cudaStream_t s);
 

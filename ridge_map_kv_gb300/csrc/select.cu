@@ -19,7 +19,8 @@
 // (w the new block). Per pass over a group of target layers, for every kind and
 // target ("problem" q) at once, a step runs:
 //   k_sel_mask_identity      Σ of already-chosen layers := I (never scored)
-//   chol_inv_batched         L_s^-1 for every (q, s), factoring a copy of Σ (fp32 SIMT)
+//   chol_inv_batched         L_s^-1 for every (q, s), from a copy of Σ (fp32 SIMT,
+//                            recursive halving, 128-wide leaves in shared memory)
 //   SelGemm (sum of squares) z_sᵀ = R_sᵀ L_s^-ᵀ, only colsum(z_s²) is kept
 //   k_sel_score              scores, the joint argmax, the tables, e += gain
 //   SelGemm                  z_bᵀ;  H[:, b] − W W_bᵀ;  × L_b^-ᵀ;  Σ_s −= w wᵀ;
@@ -372,10 +373,10 @@ struct SelLayout {
   double* alpha;    // [n_kinds]
   __nv_bfloat16* Wp;  // [3][Qmax * D][m_max]
   float* Sig;       // [Qmax * Ls][F][F]  Schur blocks, kept across steps
-  float* Lf;        // [Qmax * Ls][F][F]  their Cholesky factors (factored in place from a copy)
+  float* Lf;        // [Qmax * Ls][F][F]  a copy of Σ that the factorisation consumes
   float* Linv;      // [Qmax * Ls][F][F]
   __nv_bfloat16* Lp;  // [3][Qmax * Ls * F][F]
-  float* ctmp;      // [Qmax * Ls][128][F]
+  float* ctmp;      // [Qmax * Ls][F * F / 4]
   float* RT;        // [Qmax][Ft][D]
   __nv_bfloat16* RTp;  // [3][Qmax * Ft][D]
   float* part;      // [Qmax * Ls][Ft][2 F / 256]
@@ -410,7 +411,7 @@ static SelLayout sel_layout(const rf_select_desc* d, void* ws) {
   l.Lf = c.take<float>(Q * Ls * F * F);
   l.Linv = c.take<float>(Q * Ls * F * F);
   l.Lp = c.take<__nv_bfloat16>(3 * Q * Ls * F * F);
-  l.ctmp = c.take<float>(Q * Ls * 128 * F);
+  l.ctmp = c.take<float>(Q * Ls * F * F / 4);
   l.RT = c.take<float>(Q * Ft * D);
   l.RTp = c.take<__nv_bfloat16>(3 * Q * Ft * D);
   l.part = c.take<float>(Q * Ls * Ft * 2 * (F / kBN));

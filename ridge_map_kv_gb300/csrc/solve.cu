@@ -37,15 +37,31 @@ constexpr int kSolveBlock = 128;  // diagonal block size of the recursive factor
 // 256 threads, 8 x 8 outputs per thread, double-buffered shared tiles.
 // Requires M % 128 == 0, N % 128 == 0, K % 8 == 0, 16-byte aligned rows.
 // op(A)[m][k] = TA ? A[k*lda + m] : A[m*lda + k]; op(B)[k][n] = TB ? B[n*ldb + k] : B[k*ldb + n].
+// `tri` bits skip work that is known to be zero or unused:
+//   kSgemmLowerOut  only the output tiles on or below the diagonal (bn <= bm);
+//   kSgemmKFromN    op(B) is zero for k < n: an output column tile at bn sums k >= bn;
+//   kSgemmKToN      op(B) is zero for k > n: it sums k < bn + 128;
+//   kSgemmKToM      op(A) is zero for k > m: an output row tile at bm sums k < bm + 128.
 // --------------------------------------------------------------------------
+constexpr int kSgemmLowerOut = 1;
+constexpr int kSgemmKFromN = 2;
+constexpr int kSgemmKToN = 4;
+constexpr int kSgemmKToM = 8;
+
 template <bool TA, bool TB>
 __global__ void __launch_bounds__(256) k_sgemm(int M, int N, int K, float alpha, const float* __restrict__ A,
                                                long long lda, long long sA, const float* __restrict__ B, long long ldb,
-                                               long long sB, float beta, float* C, long long ldc, long long sC) {
+                                               long long sB, float beta, float* C, long long ldc, long long sC,
+                                               int tri) {
   __shared__ __align__(16) float As[2][8][128];
   __shared__ __align__(16) float Bs[2][8][128];
   const int tid = threadIdx.x;
   const int bm = blockIdx.y * 128, bn = blockIdx.x * 128;
+  if ((tri & kSgemmLowerOut) && bn > bm) return;
+  const int kbeg = (tri & kSgemmKFromN) ? bn : 0;
+  int kend = K;
+  if (tri & kSgemmKToN) kend = min(kend, bn + 128);
+  if (tri & kSgemmKToM) kend = min(kend, bm + 128);
   A += blockIdx.z * sA;
   B += blockIdx.z * sB;
   C += blockIdx.z * sC;
@@ -89,14 +105,14 @@ __global__ void __launch_bounds__(256) k_sgemm(int M, int N, int K, float alpha,
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
   float4 ra, rb;
-  load_a(0, ra);
-  load_b(0, rb);
+  load_a(kbeg, ra);
+  load_b(kbeg, rb);
   store_a(0, ra);
   store_b(0, rb);
   __syncthreads();
   int buf = 0;
-  for (int k0 = 0; k0 < K; k0 += 8) {
-    const bool more = k0 + 8 < K;
+  for (int k0 = kbeg; k0 < kend; k0 += 8) {
+    const bool more = k0 + 8 < kend;
     if (more) {
       load_a(k0 + 8, ra);
       load_b(k0 + 8, rb);
@@ -185,6 +201,66 @@ __global__ void __launch_bounds__(256) k_chol_base(float* A, int n, long long ld
     for (int k = threadIdx.x; k < n; k += blockDim.x) A[i * lda + k] = k <= i ? S[i * kBlkLd + k] : 0.f;
 }
 
+// W = L^-1 for the n x n SPD block A = L Lᵀ (n <= 128), one CTA per matrix b
+// (A + b*sA, W + b*sW). The factor is computed in shared memory as in
+// k_chol_base, then inverted in place row by row: with rows k < i already holding
+// W, row i becomes W[i][j] = (δ_ij − Σ_{j<=k<i} L[i][k] W[k][j]) / L[i][i] (thread j,
+// four partial sums), written once every thread has read row i. A is only read;
+// W's upper triangle is zero. A non-positive pivot records RF_ERR_NOT_SPD.
+__global__ void __launch_bounds__(256) k_chol_inv_leaf(const float* __restrict__ A, int n, long long lda, long long sA,
+                                                       float* __restrict__ W, long long ldw, long long sW,
+                                                       int32_t* dev_status) {
+  extern __shared__ float S[];
+  A += blockIdx.x * sA;
+  W += blockIdx.x * sW;
+  for (int i = threadIdx.y; i < n; i += blockDim.y)
+    for (int k = threadIdx.x; k < n; k += blockDim.x) S[i * kBlkLd + k] = A[i * lda + k];
+  const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+  const int nthr = blockDim.x * blockDim.y;
+  __syncthreads();
+  for (int j = 0; j < n; ++j) {
+    if (tid == 0) {
+      float d = S[j * kBlkLd + j];
+      if (!(d > 0.f)) {
+        record_status(dev_status, RF_ERR_NOT_SPD);
+        d = 1.f;
+      }
+      S[j * kBlkLd + j] = sqrtf(d);
+    }
+    __syncthreads();
+    const float inv = 1.f / S[j * kBlkLd + j];
+    for (int i = j + 1 + tid; i < n; i += nthr) S[i * kBlkLd + j] *= inv;
+    __syncthreads();
+    for (int i = j + 1 + (tid >> 1); i < n; i += nthr >> 1) {
+      const float lij = S[i * kBlkLd + j];
+      for (int k = j + 1 + (tid & 1); k <= i; k += 2) S[i * kBlkLd + k] -= lij * S[k * kBlkLd + j];
+    }
+    __syncthreads();
+  }
+  for (int i = 0; i < n; ++i) {
+    const float dinv = 1.f / S[i * kBlkLd + i];
+    float v = 0.f;
+    const int j = tid;
+    if (j <= i) {
+      float s0 = (i == j) ? 1.f : 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      int k = j;
+      for (; k + 3 < i; k += 4) {
+        s0 = fmaf(-S[i * kBlkLd + k], S[k * kBlkLd + j], s0);
+        s1 = fmaf(-S[i * kBlkLd + k + 1], S[(k + 1) * kBlkLd + j], s1);
+        s2 = fmaf(-S[i * kBlkLd + k + 2], S[(k + 2) * kBlkLd + j], s2);
+        s3 = fmaf(-S[i * kBlkLd + k + 3], S[(k + 3) * kBlkLd + j], s3);
+      }
+      for (; k < i; ++k) s0 = fmaf(-S[i * kBlkLd + k], S[k * kBlkLd + j], s0);
+      v = ((s0 + s1) + (s2 + s3)) * dinv;
+    }
+    __syncthreads();
+    if (j <= i) S[i * kBlkLd + j] = v;
+    __syncthreads();
+  }
+  for (int i = threadIdx.y; i < n; i += blockDim.y)
+    for (int k = threadIdx.x; k < n; k += blockDim.x) W[i * ldw + k] = k <= i ? S[i * kBlkLd + k] : 0.f;
+}
+
 // Diagonal blocks of one triangular inverse, inverted by one launch (one CTA each).
 constexpr int kMaxLeaves = 256;
 struct LeafBlocks {
@@ -268,14 +344,24 @@ __global__ void __launch_bounds__(1024) k_trace_alpha(const double* G, const dou
 }
 
 // H = (G + Gᵀ)/2 − n μ_x μ_xᵀ + αI, stored in fp32 and (when H64 is set) fp64.
-__global__ void k_build_h(const double* G, const double* mu_x, const double* n, const double* alpha, int d_in,
-                          double* H64, float* H32) {
-  const long long total = static_cast<long long>(d_in) * d_in;
-  for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
-       e += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int i = static_cast<int>(e / d_in), j = static_cast<int>(e % d_in);
-    double h = 0.5 * (G[e] + G[static_cast<long long>(j) * d_in + i]) - (*n) * mu_x[i] * mu_x[j];
-    if (i == j) h += *alpha;
+// Block (bx, by) writes rows by*32.., columns bx*32.. and reads Gᵀ's matching tile
+// through shared memory, so both reads are row-contiguous. 32 x 8 threads.
+__global__ void __launch_bounds__(256) k_build_h(const double* __restrict__ G, const double* __restrict__ mu_x,
+                                                 const double* __restrict__ n, const double* __restrict__ alpha,
+                                                 int d_in, double* __restrict__ H64, float* __restrict__ H32) {
+  __shared__ double t[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int j = threadIdx.y; j < 32; j += 8)
+    t[j][threadIdx.x] = G[static_cast<size_t>(c0 + j) * d_in + r0 + threadIdx.x];  // G[c0 + j][r0 + x]
+  __syncthreads();
+  const double nn = *n, a = *alpha;
+  const int c = c0 + threadIdx.x;
+  const double mc = mu_x[c];
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int r = r0 + j;
+    const size_t e = static_cast<size_t>(r) * d_in + c;
+    double h = 0.5 * (G[e] + t[threadIdx.x][j]) - nn * mu_x[r] * mc;
+    if (r == c) h += a;
     if (H64 != nullptr) H64[e] = h;
     H32[e] = static_cast<float>(h);
   }
@@ -376,12 +462,16 @@ struct SolveCtx {
 
 static rf_status sgemm(SolveCtx& c, bool ta, bool tb, int M, int N, int K, float alpha, const float* A, long long lda,
                        long long sA, const float* B, long long ldb, long long sB, float beta, float* C, long long ldc,
-                       long long sC, int batch) {
+                       long long sC, int batch, int tri = 0) {
   dim3 grid(N / 128, M / 128, batch);
-  if (!ta && !tb) k_sgemm<false, false><<<grid, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC);
-  else if (ta && !tb) k_sgemm<true, false><<<grid, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC);
-  else if (!ta && tb) k_sgemm<false, true><<<grid, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC);
-  else k_sgemm<true, true><<<grid, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC);
+  if (!ta && !tb)
+    k_sgemm<false, false><<<grid, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC, tri);
+  else if (ta && !tb)
+    k_sgemm<true, false><<<grid, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC, tri);
+  else if (!ta && tb)
+    k_sgemm<false, true><<<grid, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC, tri);
+  else
+    k_sgemm<true, true><<<grid, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC, tri);
   return cuda_check(cudaGetLastError(), "k_sgemm launch");
 }
 
@@ -686,57 +776,58 @@ rf_status centre_system(const double* G, const double* sx, const double* sy, con
   const int eb = 8 * sms;
   k_means<<<eb, 256, 0, s>>>(sx, sy, n, d_in, n_y, mu_x, mu_y, n_out);
   k_trace_alpha<<<1, 1024, 0, s>>>(G, mu_x, n_out, d_in, lambda, alpha_mode, alpha, alpha_out);
-  k_build_h<<<eb, 256, 0, s>>>(G, mu_x, n_out, alpha, d_in, H64, H32);
+  k_build_h<<<dim3(d_in / 32, d_in / 32), dim3(32, 8), 0, s>>>(G, mu_x, n_out, alpha, d_in, H64, H32);
   return cuda_check(cudaGetLastError(), "centring launches");
 }
 
-// Right-looking blocked factorisation over the batch, one 128-wide column block
-// at a time: the diagonal block (one CTA per matrix), its inverse (the diagonal
-// block of L^-1), the panel below it times that inverse's transpose, then the
-// trailing update. The panel product runs in place: with a single 128-wide
-// output column tile, each CTA reads and then writes only its own 128 rows.
-// L^-1's off-diagonal row blocks follow bottom-up from
-//   (L^-1)[i][0:i] = −(L^-1)[i][i] · (L[i][0:i] · (L^-1)[0:i][0:i]).
+static uint64_t g_leaf_attr = 0;
+
+// Batched recursive factorisation: W = L^-1 of every n x n SPD matrix (n % 128 == 0),
+// splitting n = n1 + n2 at a multiple of 128 near n/2:
+//   W11 = L11^-1                      (recursion on A11)
+//   L21 = A21 W11ᵀ                     -> tmp            (W11ᵀ is upper triangular)
+//   A22 −= L21 L21ᵀ                    (tiles on and below the diagonal)
+//   T = L21 W11                        -> A21's storage  (W11 lower triangular)
+//   W22 = L22^-1                       (recursion on A22; it reuses tmp)
+//   W21 = −W22 T                       (W22 lower triangular)
+// with the 128 x 128 leaves factored and inverted in shared memory by one CTA each.
+// Every product is an fp32 SIMT GEMM over the whole batch (k_sgemm, blockIdx.z).
+static rf_status chol_inv_rec(SolveCtx& c, float* A, long long lda, long long sA, float* W, long long ldw,
+                              long long sW, int n, int batch, float* tmp, long long stmp) {
+  rf_status st;
+  if (n <= kSolveBlock) {
+    k_chol_inv_leaf<<<batch, dim3(32, 8), kBlkSmem, c.s>>>(A, n, lda, sA, W, ldw, sW, c.dev_status);
+    return cuda_check(cudaGetLastError(), "k_chol_inv_leaf launch");
+  }
+  const int n1 = split_point(n), n2 = n - n1;
+  float* A21 = A + static_cast<long long>(n1) * lda;
+  float* A22 = A21 + n1;
+  float* W21 = W + static_cast<long long>(n1) * ldw;
+  float* W22 = W21 + n1;
+  if ((st = chol_inv_rec(c, A, lda, sA, W, ldw, sW, n1, batch, tmp, stmp)) != RF_OK) return st;
+  if ((st = sgemm(c, false, true, n2, n1, n1, 1.f, A21, lda, sA, W, ldw, sW, 0.f, tmp, n1, stmp, batch,
+                  kSgemmKToN)) != RF_OK)
+    return st;
+  if ((st = sgemm(c, false, true, n2, n2, n1, -1.f, tmp, n1, stmp, tmp, n1, stmp, 1.f, A22, lda, sA, batch,
+                  kSgemmLowerOut)) != RF_OK)
+    return st;
+  if ((st = sgemm(c, false, false, n2, n1, n1, 1.f, tmp, n1, stmp, W, ldw, sW, 0.f, A21, lda, sA, batch,
+                  kSgemmKFromN)) != RF_OK)
+    return st;
+  if ((st = chol_inv_rec(c, A22, lda, sA, W22, ldw, sW, n2, batch, tmp, stmp)) != RF_OK) return st;
+  return sgemm(c, false, false, n2, n1, n2, -1.f, W22, ldw, sW, A21, lda, sA, 0.f, W21, ldw, sW, batch, kSgemmKToM);
+}
+
 rf_status chol_inv_batched(float* A, long long lda, long long stride, float* Linv, long long ldi, int n, int batch,
                            float* tmp, int32_t* dev_status, int sms, cudaStream_t s) {
-  rf_status st = solve_kernel_attrs();
+  rf_status st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf), kBlkSmem, &g_leaf_attr);
   if (st != RF_OK) return st;
   const long long stride_inv = static_cast<long long>(n) * ldi;
   SolveCtx c{s, sms, nullptr, nullptr, dev_status};
   if ((st = cuda_check(cudaMemsetAsync(Linv, 0, sizeof(float) * stride_inv * batch, s), "zero L^-1")) != RF_OK)
     return st;
-  LeafBlocks one;
-  one.off[0] = 0;
-  one.size[0] = kSolveBlock;
-  const int nb = n / kSolveBlock;
-  for (int kb = 0; kb < nb; ++kb) {
-    const long long o = static_cast<long long>(kb) * kSolveBlock;
-    const int r = n - static_cast<int>(o) - kSolveBlock;
-    float* Akk = A + o * lda + o;
-    k_chol_base<<<batch, dim3(32, 8), kBlkSmem, s>>>(Akk, kSolveBlock, lda, stride, dev_status);
-    k_trinv_base<<<dim3(1, batch), kSolveBlock, 2 * kBlkSmem, s>>>(Akk, lda, stride, Linv + o * ldi + o, ldi,
-                                                                   stride_inv, one);
-    if ((st = cuda_check(cudaGetLastError(), "batched diagonal block launches")) != RF_OK) return st;
-    if (r == 0) break;
-    float* A21 = A + (o + kSolveBlock) * lda + o;
-    if ((st = sgemm(c, false, true, r, kSolveBlock, kSolveBlock, 1.f, A21, lda, stride, Linv + o * ldi + o, ldi,
-                    stride_inv, 0.f, A21, lda, stride, batch)) != RF_OK)
-      return st;
-    if ((st = sgemm(c, false, true, r, r, kSolveBlock, -1.f, A21, lda, stride, A21, lda, stride, 1.f,
-                    A21 + kSolveBlock, lda, stride, batch)) != RF_OK)
-      return st;
-  }
-  const long long stride_tmp = static_cast<long long>(kSolveBlock) * n;
-  for (int i = 1; i < nb; ++i) {
-    const long long oi = static_cast<long long>(i) * kSolveBlock;
-    if ((st = sgemm(c, false, false, kSolveBlock, static_cast<int>(oi), static_cast<int>(oi), 1.f, A + oi * lda, lda,
-                    stride, Linv, ldi, stride_inv, 0.f, tmp, n, stride_tmp, batch)) != RF_OK)
-      return st;
-    if ((st = sgemm(c, false, false, kSolveBlock, static_cast<int>(oi), kSolveBlock, -1.f, Linv + oi * ldi + oi, ldi,
-                    stride_inv, tmp, n, stride_tmp, 0.f, Linv + oi * ldi, ldi, stride_inv, batch)) != RF_OK)
-      return st;
-  }
-  return RF_OK;
+  const long long stmp = static_cast<long long>(n) * n / 4;
+  return chol_inv_rec(c, A, lda, stride, Linv, ldi, stride_inv, n, batch, tmp, stmp);
 }
 
 }  // namespace rf
@@ -777,7 +868,7 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
     ProfScope pf(c.s, RF_STAGE_SOLVE);
     k_means<<<eb, 256, 0, c.s>>>(st->sx, st->sy, st->n, di, static_cast<long long>(P) * dout, lay.mu_x, lay.mu_y, lay.n);
     k_trace_alpha<<<1, 1024, 0, c.s>>>(st->G, lay.mu_x, lay.n, di, lambda, alpha_mode, lay.alpha, alpha_out);
-    k_build_h<<<eb, 256, 0, c.s>>>(st->G, lay.mu_x, lay.n, lay.alpha, di, lay.H64, lay.L);
+    k_build_h<<<dim3(di / 32, di / 32), dim3(32, 8), 0, c.s>>>(st->G, lay.mu_x, lay.n, lay.alpha, di, lay.H64, lay.L);
     const long long ctotal = static_cast<long long>(P) * di * dout;
     k_centre_c<<<eb, 256, 0, c.s>>>(st->C, lay.mu_x, lay.mu_y, lay.n, di, dout, ctotal, lay.work);
     if ((s = cuda_check(cudaGetLastError(), "solve set-up launches")) != RF_OK) return s;

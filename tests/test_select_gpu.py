@@ -247,13 +247,14 @@ def test_select_full_size_sampled():
     for t in (0, 31, 63):
         for s in range(cfg.L_src):
             assert abs(r2[:, t, 0, s].mean() - oracle_score(t, [s])) <= TOL_R2, (t, s)
-    # later steps of two targets along the GPU's path: the choice and the runner-up
+    # later steps of two targets along the GPU's path: the choice and the best other
+    # candidate by the GPU's table (late steps of this model are near-ties, where the
+    # fp32 table may order candidates differently from the fp64 argmax)
     for t in (0, 63):
         for j in (1, 2, cfg.k - 1):
             chosen = sel[t, :j].tolist()
             joint = r2[:, t, j].mean(axis=0)
-            order = [s for s in np.argsort(-np.nan_to_num(joint, nan=-np.inf)) if s not in chosen]
-            a, b = oracle_score(t, chosen + [order[0]]), oracle_score(t, chosen + [order[1]])
-            assert order[0] == sel[t, j]
-            assert abs(joint[order[0]] - a) <= TOL_R2 and abs(joint[order[1]] - b) <= TOL_R2
+            other = max((s for s in range(cfg.L_src) if s not in chosen and s != sel[t, j]), key=lambda s: joint[s])
+            a, b = oracle_score(t, chosen + [int(sel[t, j])]), oracle_score(t, chosen + [other])
+            assert abs(joint[sel[t, j]] - a) <= TOL_R2 and abs(joint[other] - b) <= TOL_R2
             assert a >= b - TOL_R2
