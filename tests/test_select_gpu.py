@@ -16,10 +16,11 @@ TOL_R2 of the oracle's best score at that step, and where the oracle's own
 greedy path has a margin above 2·TOL_R2 at every step the two paths must be
 identical.
 
-TOL_R2 = 2e-4 (absolute, on scores in [0, 1]). The GPU's Schur blocks carry fp32
-rounding of the Gram (relative 6e-8) amplified by the condition of the ridge
-system Gc_SS + αI. Measured on these inputs the largest score error is about
-1e-5; the bound leaves a 20x margin.
+TOL_R2 = 2e-5 (absolute, on scores in [0, 1]). The GPU's Schur blocks carry the
+fp32 rounding of the Gram (relative 6e-8) amplified by the condition of the ridge
+systems Gc_SS + αI. Measured on GB300, the largest score error is 4.7e-7 on the
+small case and 2.0e-6 on 72 sampled scores of the full 40 -> 64-layer case; the
+bound leaves a 10x margin over the latter.
 """
 import math
 
@@ -33,7 +34,7 @@ import synth
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-TOL_R2 = 2e-4
+TOL_R2 = 2e-5
 KERNELS = pytest.mark.parametrize("flags", [rf.RF_FLAG_SINGLE_CTA, rf.RF_FLAG_CTA_PAIR], ids=["single-cta", "cta-pair"])
 
 
