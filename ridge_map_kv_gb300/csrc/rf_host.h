@@ -80,6 +80,12 @@ rf_status centre_system(const double* G, const double* sx, const double* sy, con
 rf_status chol_inv_batched(float* A, long long lda, long long stride, float* Linv, long long ldi, int n, int batch,
                            float* tmp, int32_t* dev_status, int sms, cudaStream_t s);
 
+// The same for n x n sub-blocks (solve.cu): matrix b's block at A + b*sA (ld lda) and
+// its inverse at W + b*sW (ld ldw); W's blocks above the diagonal must already be
+// zero. tmp holds batch * stmp floats, stmp >= n * n / 4.
+rf_status chol_inv_block(float* A, long long lda, long long sA, float* W, long long ldw, long long sW, int n, int batch,
+                         float* tmp, long long stmp, int32_t* dev_status, int sms, cudaStream_t s);
+
 // Brackets one kernel launch with profiling events when rf_profile_start is active.
 struct ProfScope {
   cudaStream_t stream;

@@ -19,8 +19,10 @@
 // (w the new block). Per pass over a group of target layers, for every kind and
 // target ("problem" q) at once, a step runs:
 //   k_sel_mask_identity      Σ of already-chosen layers := I (never scored)
-//   chol_inv_batched         L_s^-1 for every (q, s), from a copy of Σ (fp32 SIMT,
-//                            recursive halving, 128-wide leaves in shared memory)
+//   sel_factor               L_s^-1 for every (q, s), from a copy of Σ: recursive
+//                            halving, the products of widths >= 512 on the tensor
+//                            cores, narrower ones fp32 SIMT, 128-wide leaves in
+//                            shared memory
 //   SelGemm (sum of squares) z_sᵀ = R_sᵀ L_s^-ᵀ, only colsum(z_s²) is kept
 //   k_sel_score              scores, the joint argmax, the tables, e += gain
 //   SelGemm                  z_bᵀ;  H[:, b] − W W_bᵀ;  × L_b^-ᵀ;  Σ_s −= w wᵀ;
@@ -200,6 +202,59 @@ __global__ void __launch_bounds__(256) k_split_rows(const float* __restrict__ sr
   }
 }
 
+// fp32 blocks -> three bf16 planes, one block per matrix b of a batch: the rows x cols
+// block at src + b*s_src (ld ld_src) becomes rows b*rows_out .. of the planes (ld
+// ld_dst), transposed when `tr` (rows_out = cols). Grid (cols/32, rows/32, batch),
+// 32 x 8 threads; the transposed copy goes through a shared tile.
+__global__ void __launch_bounds__(256) k_split_blocks(const float* __restrict__ src, long long ld_src, long long s_src,
+                                                      int rows, int cols, __nv_bfloat16* __restrict__ dst,
+                                                      long long ld_dst, long long plane_stride, int tr) {
+  __shared__ float t[32][33];
+  const int b = blockIdx.z;
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const float* s = src + b * s_src;
+  for (int j = threadIdx.y; j < 32; j += 8) t[j][threadIdx.x] = s[static_cast<long long>(r0 + j) * ld_src + c0 + threadIdx.x];
+  __syncthreads();
+  const long long rows_out = tr ? cols : rows;
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    // untransposed: out[r0 + j][c0 + x] = t[j][x];  transposed: out[c0 + j][r0 + x] = t[x][j]
+    const float v = tr ? t[threadIdx.x][j] : t[j][threadIdx.x];
+    const long long orow = b * rows_out + (tr ? c0 + j : r0 + j);
+    const long long ocol = tr ? r0 + threadIdx.x : c0 + threadIdx.x;
+    __nv_bfloat16 h, m, l;
+    split3(v, h, m, l);
+    __nv_bfloat16* d = dst + orow * ld_dst + ocol;
+    d[0] = h;
+    d[plane_stride] = m;
+    d[2 * plane_stride] = l;
+  }
+}
+
+// The untransposed case, 4 elements per thread-step (cols % 4 == 0).
+__global__ void __launch_bounds__(256) k_split_blocks_rows(const float* __restrict__ src, long long ld_src,
+                                                           long long s_src, int rows, int cols,
+                                                           __nv_bfloat16* __restrict__ dst, long long plane_stride,
+                                                           int batch) {
+  const int per = cols / 4;
+  const long long total = static_cast<long long>(batch) * rows * per;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long br = i / per;  // b * rows + r
+    const int c = static_cast<int>(i - br * per) * 4;
+    const long long b = br / rows, r = br - b * rows;
+    const float4 v = __ldg(reinterpret_cast<const float4*>(src + b * s_src + r * ld_src + c));
+    __nv_bfloat16 h[4], m[4], l[4];
+    split3(v.x, h[0], m[0], l[0]);
+    split3(v.y, h[1], m[1], l[1]);
+    split3(v.z, h[2], m[2], l[2]);
+    split3(v.w, h[3], m[3], l[3]);
+    __nv_bfloat16* d = dst + br * cols + c;
+    *reinterpret_cast<uint2*>(d) = *reinterpret_cast<const uint2*>(h);
+    *reinterpret_cast<uint2*>(d + plane_stride) = *reinterpret_cast<const uint2*>(m);
+    *reinterpret_cast<uint2*>(d + 2 * plane_stride) = *reinterpret_cast<const uint2*>(l);
+  }
+}
+
 // Per-kind inputs of one call.
 struct SelKinds {
   const double* C[kSelMaxKinds];    // [n_targets][D][Ft] raw cross sums
@@ -260,15 +315,19 @@ __global__ void __launch_bounds__(256) k_sel_init_tss(const __grid_constant__ Se
   }
 }
 
-// Σ[q][s] := I for every layer s already chosen for problem q's target.
+// Σ[q][s] := I for every layer s already chosen for problem q's target. Grid
+// (Ls, Q, 16): CTA z writes rows z*F/16 .. of the block, 4 floats per store.
 __global__ void __launch_bounds__(256) k_sel_mask_identity(const uint8_t* __restrict__ mask, int G, int Ls, int F,
                                                            float* __restrict__ Sig) {
   const int q = blockIdx.y, s = blockIdx.x;
   if (!mask[(q % G) * Ls + s]) return;
+  const int rows = F / 16, r0 = blockIdx.z * rows, per = F / 4;
   float* S = Sig + (static_cast<long long>(q) * Ls + s) * F * F;
-  for (long long e = threadIdx.x; e < static_cast<long long>(F) * F; e += blockDim.x) {
-    const long long r = e / F;
-    S[e] = (e - r * F == r) ? 1.f : 0.f;
+  for (int e = threadIdx.x; e < rows * per; e += blockDim.x) {
+    const int r = r0 + e / per, c = (e % per) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r >= c && r < c + 4) (&v.x)[r - c] = 1.f;
+    *reinterpret_cast<float4*>(S + static_cast<long long>(r) * F + c) = v;
   }
 }
 
@@ -377,6 +436,8 @@ struct SelLayout {
   float* Linv;      // [Qmax * Ls][F][F]
   __nv_bfloat16* Lp;  // [3][Qmax * Ls * F][F]
   float* ctmp;      // [Qmax * Ls][F * F / 4]
+  __nv_bfloat16* fpa;  // [3][Qmax * Ls * F / 2][F / 2]  planes of the factorisation's products
+  __nv_bfloat16* fpb;  // [3][Qmax * Ls * F / 2][F / 2]
   float* RT;        // [Qmax][Ft][D]
   __nv_bfloat16* RTp;  // [3][Qmax * Ft][D]
   float* part;      // [Qmax * Ls][Ft][2 F / 256]
@@ -412,6 +473,9 @@ static SelLayout sel_layout(const rf_select_desc* d, void* ws) {
   l.Linv = c.take<float>(Q * Ls * F * F);
   l.Lp = c.take<__nv_bfloat16>(3 * Q * Ls * F * F);
   l.ctmp = c.take<float>(Q * Ls * F * F / 4);
+  const long long fp = F % 512 == 0 ? 3 * Q * Ls * F * F / 4 : 1;
+  l.fpa = c.take<__nv_bfloat16>(fp);
+  l.fpb = c.take<__nv_bfloat16>(fp);
   l.RT = c.take<float>(Q * Ft * D);
   l.RTp = c.take<__nv_bfloat16>(3 * Q * Ft * D);
   l.part = c.take<float>(Q * Ls * Ft * 2 * (F / kBN));
@@ -476,6 +540,7 @@ struct SelGemm {
   long long c_kind = 0, c_b = 0, c_q = 0, c_s = 0, ldc = 0;
   int q_per_kind = 1;
   float* part = nullptr;
+  int stage = RF_STAGE_SELECT_GEMM;  // profiler stage of the launch
 };
 
 template <bool kPair>
@@ -514,7 +579,7 @@ static rf_status run_sel_gemm(SelCtx& c, const SelGemm& g) {
   pr.part = g.part;
   pr.dev_status = c.dev_status;
   pr.timeout_ns = wait_timeout_ns();
-  ProfScope prof(c.s, RF_STAGE_SELECT_GEMM);
+  ProfScope prof(c.s, g.stage);
   return launch_gemm(pr, static_cast<int64_t>(g.Q) * g.nS * pr.m_tiles * pr.n_tiles, c.sms, c.s,
                      "selection GEMM launch");
 }
@@ -534,6 +599,91 @@ static SelOperand op(long long q_rows, long long s_rows, long long b_rows, long 
   o.s_k = s_k;
   o.b_k = b_k;
   return o;
+}
+
+static rf_status split_blocks(SelCtx& c, const float* src, long long ld_src, long long s_src, int rows, int cols,
+                              int batch, __nv_bfloat16* dst, bool tr) {
+  const long long rows_out = tr ? cols : rows;
+  const long long ld_dst = tr ? rows : cols;
+  ProfScope prof(c.s, RF_STAGE_SELECT_FACTOR);
+  if (tr) {
+    k_split_blocks<<<dim3(cols / 32, rows / 32, batch), dim3(32, 8), 0, c.s>>>(src, ld_src, s_src, rows, cols, dst,
+                                                                               ld_dst, rows_out * batch * ld_dst, 1);
+  } else {
+    const long long total = static_cast<long long>(batch) * rows * (cols / 4);
+    const unsigned blocks = static_cast<unsigned>(std::min<long long>((total + 255) / 256, 8LL * c.sms));
+    k_split_blocks_rows<<<blocks, 256, 0, c.s>>>(src, ld_src, s_src, rows, cols, dst, rows_out * batch * ld_dst, batch);
+  }
+  return cuda_check(cudaGetLastError(), "block split launch");
+}
+
+// W = L^-1 for a batch of n x n SPD blocks (matrix b at A + b*sA, W + b*sW; A is
+// consumed), W zero above the diagonal on entry. Widths that are multiples of 512
+// split in halves with the four products on the tensor cores (fp32-accurate split
+// bf16): with W11 = L11^-1 from the first half,
+//   L21 = A21 W11ᵀ,  A22 −= L21 L21ᵀ,  Tᵀ = W11ᵀ L21ᵀ (into A21's storage),
+//   then W22 = L22^-1 from the second half and W21 = −W22 T.
+// Other widths run the fp32 SIMT recursion (chol_inv_block).
+static rf_status sel_factor(SelCtx& c, SelLayout& lay, float* A, long long lda, long long sA, float* W, long long ldw,
+                            long long sW, int n, int batch, long long stmp) {
+  rf_status st;
+  if (n % 512 != 0) {
+    ProfScope prof(c.s, RF_STAGE_SELECT_FACTOR);
+    return chol_inv_block(A, lda, sA, W, ldw, sW, n, batch, lay.ctmp, stmp, c.dev_status, c.sms, c.s);
+  }
+  const int h = n / 2;
+  float* A21 = A + static_cast<long long>(h) * lda;
+  float* A22 = A21 + h;
+  float* W21 = W + static_cast<long long>(h) * ldw;
+  float* W22 = W21 + h;
+  float* L21 = lay.ctmp;  // [batch][h][h]
+  const long long hh = static_cast<long long>(h) * h;
+  const long long rows = static_cast<long long>(batch) * h;  // rows of a plane set
+  if ((st = sel_factor(c, lay, A, lda, sA, W, ldw, sW, h, batch, stmp)) != RF_OK) return st;
+  // L21 = A21 W11ᵀ
+  if ((st = split_blocks(c, A21, lda, sA, h, h, batch, lay.fpa, false)) != RF_OK) return st;
+  if ((st = split_blocks(c, W, ldw, sW, h, h, batch, lay.fpb, false)) != RF_OK) return st;
+  {
+    SelGemm g{};
+    g.pa = lay.fpa, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
+    g.pb = lay.fpb, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
+    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = RF_STAGE_SELECT_FACTOR;
+    g.out = L21, g.o_s = hh, g.ldo = h;
+    if ((st = sel_gemm(c, g)) != RF_OK) return st;
+  }
+  // A22 −= L21 L21ᵀ
+  if ((st = split_blocks(c, L21, h, hh, h, h, batch, lay.fpa, false)) != RF_OK) return st;
+  {
+    SelGemm g{};
+    g.pa = lay.fpa, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
+    g.pb = lay.fpa, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
+    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = RF_STAGE_SELECT_FACTOR;
+    g.alpha = -1.f, g.beta = 1.f;
+    g.out = A22, g.o_s = sA, g.ldo = lda;
+    g.csrc = A22, g.c_s = sA, g.ldc = lda;
+    if ((st = sel_gemm(c, g)) != RF_OK) return st;
+  }
+  // Tᵀ = W11ᵀ L21ᵀ, kept in A21's storage
+  if ((st = split_blocks(c, W, ldw, sW, h, h, batch, lay.fpb, true)) != RF_OK) return st;
+  {
+    SelGemm g{};
+    g.pa = lay.fpb, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
+    g.pb = lay.fpa, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
+    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = RF_STAGE_SELECT_FACTOR;
+    g.out = A21, g.o_s = sA, g.ldo = lda;
+    if ((st = sel_gemm(c, g)) != RF_OK) return st;
+  }
+  if ((st = sel_factor(c, lay, A22, lda, sA, W22, ldw, sW, h, batch, stmp)) != RF_OK) return st;
+  // W21 = −W22 T
+  if ((st = split_blocks(c, W22, ldw, sW, h, h, batch, lay.fpa, false)) != RF_OK) return st;
+  if ((st = split_blocks(c, A21, lda, sA, h, h, batch, lay.fpb, false)) != RF_OK) return st;
+  SelGemm g{};
+  g.pa = lay.fpa, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
+  g.pb = lay.fpb, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
+  g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = RF_STAGE_SELECT_FACTOR;
+  g.alpha = -1.f;
+  g.out = W21, g.o_s = sW, g.ldo = ldw;
+  return sel_gemm(c, g);
 }
 
 }  // namespace rf
@@ -614,15 +764,17 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
       const long long m = static_cast<long long>(j) * F;
       {
         ProfScope pf(c.s, RF_STAGE_SELECT_FACTOR);
-        if (j > 0) k_sel_mask_identity<<<dim3(Ls, Q), 256, 0, c.s>>>(lay.mask, G, Ls, F, lay.Sig);
+        if (j > 0) k_sel_mask_identity<<<dim3(Ls, Q, 16), 256, 0, c.s>>>(lay.mask, G, Ls, F, lay.Sig);
         if ((st = cuda_check(cudaMemcpyAsync(lay.Lf, lay.Sig, sizeof(float) * Q * Ls * F * F,
                                              cudaMemcpyDeviceToDevice, c.s),
                              "Schur block copy")) != RF_OK)
           return st;
-        if ((st = chol_inv_batched(lay.Lf, F, static_cast<long long>(F) * F, lay.Linv, F, F, Q * Ls, lay.ctmp,
-                                   dev_status, sms, c.s)) != RF_OK)
+        if ((st = cuda_check(cudaMemsetAsync(lay.Linv, 0, sizeof(float) * Q * Ls * F * F, c.s), "zero L^-1")) != RF_OK)
           return st;
       }
+      if ((st = sel_factor(c, lay, lay.Lf, F, static_cast<long long>(F) * F, lay.Linv, F, static_cast<long long>(F) * F,
+                           F, Q * Ls, static_cast<long long>(F) * F / 4)) != RF_OK)
+        return st;
       if ((st = split_rows(c, lay.Linv, F, lay.Lp, F, 0, lrows * F, lrows, F)) != RF_OK) return st;
       if ((st = split_rows(c, lay.RT, D, lay.RTp, D, 0, rtrows * D, rtrows, static_cast<int>(D))) != RF_OK) return st;
       // colsum(z_s²) for every (q, s): z_sᵀ = R_sᵀ L_s^-ᵀ

@@ -201,64 +201,130 @@ __global__ void __launch_bounds__(256) k_chol_base(float* A, int n, long long ld
     for (int k = threadIdx.x; k < n; k += blockDim.x) A[i * lda + k] = k <= i ? S[i * kBlkLd + k] : 0.f;
 }
 
-// W = L^-1 for the n x n SPD block A = L Lᵀ (n <= 128), one CTA per matrix b
-// (A + b*sA, W + b*sW). The factor is computed in shared memory as in
-// k_chol_base, then inverted in place row by row: with rows k < i already holding
-// W, row i becomes W[i][j] = (δ_ij − Σ_{j<=k<i} L[i][k] W[k][j]) / L[i][i] (thread j,
-// four partial sums), written once every thread has read row i. A is only read;
-// W's upper triangle is zero. A non-positive pivot records RF_ERR_NOT_SPD.
-__global__ void __launch_bounds__(256) k_chol_inv_leaf(const float* __restrict__ A, int n, long long lda, long long sA,
+// W = L^-1 for the 128 x 128 SPD block A = L Lᵀ, one CTA (8 warps) per matrix b
+// (A + b*sA, W + b*sW), in shared memory and blocked by 8 so that a column or row
+// block costs a few barriers instead of one per column:
+//   factor, per 8-column block k0:  warp 0 factors the 8 x 8 diagonal block
+//     (lanes own rows, warp-synchronous); one thread per row below solves its 8
+//     panel entries against it; the warps apply the rank-8 update to the trailing
+//     lower triangle (warp w takes rows w, w+8, ..., lanes the columns);
+//   invert, per 8-row block i0 (rows above already hold W):
+//     T = L[i0 block][0:i0] W[0:i0][0:i0]  (all threads), and meanwhile warp 0
+//     inverts the diagonal block (lane c forms column c by forward substitution);
+//     then W[i0 block][0:i0] = −W_ii T and W_ii replaces L_ii.
+// A is only read; W's upper triangle is zero. A non-positive pivot records
+// RF_ERR_NOT_SPD and continues with 1.
+constexpr int kLeafN = 128;
+constexpr int kLeafB = 8;
+constexpr size_t kLeafSmem = kBlkSmem + sizeof(float) * (kLeafB * kLeafN + kLeafB * kLeafB);
+
+__global__ void __launch_bounds__(256) k_chol_inv_leaf(const float* __restrict__ A, long long lda, long long sA,
                                                        float* __restrict__ W, long long ldw, long long sW,
                                                        int32_t* dev_status) {
   extern __shared__ float S[];
+  float* Tb = S + kLeafN * kBlkLd;  // [8][128]
+  float* Wd = Tb + kLeafB * kLeafN;  // [8][8]
+  constexpr int n = kLeafN;
   A += blockIdx.x * sA;
   W += blockIdx.x * sW;
-  for (int i = threadIdx.y; i < n; i += blockDim.y)
-    for (int k = threadIdx.x; k < n; k += blockDim.x) S[i * kBlkLd + k] = A[i * lda + k];
-  const int tid = threadIdx.y * blockDim.x + threadIdx.x;
-  const int nthr = blockDim.x * blockDim.y;
+  const int lane = threadIdx.x, warp = threadIdx.y, tid = warp * 32 + lane;
+  for (int i = warp; i < n; i += 8)
+    for (int k = lane; k < n; k += 32) S[i * kBlkLd + k] = A[i * lda + k];
   __syncthreads();
-  for (int j = 0; j < n; ++j) {
-    if (tid == 0) {
-      float d = S[j * kBlkLd + j];
-      if (!(d > 0.f)) {
-        record_status(dev_status, RF_ERR_NOT_SPD);
-        d = 1.f;
+  // ---- factor
+  for (int k0 = 0; k0 < n; k0 += kLeafB) {
+    if (warp == 0) {
+      for (int j = 0; j < kLeafB; ++j) {
+        float d = S[(k0 + j) * kBlkLd + k0 + j];
+        if (!(d > 0.f)) {
+          if (lane == 0) record_status(dev_status, RF_ERR_NOT_SPD);
+          d = 1.f;
+        }
+        d = sqrtf(d);
+        __syncwarp();
+        if (lane == j) S[(k0 + j) * kBlkLd + k0 + j] = d;
+        if (lane > j && lane < kLeafB) S[(k0 + lane) * kBlkLd + k0 + j] /= d;
+        __syncwarp();
+        if (lane > j && lane < kLeafB) {
+          const float lrj = S[(k0 + lane) * kBlkLd + k0 + j];
+          for (int c = j + 1; c <= lane; ++c) S[(k0 + lane) * kBlkLd + k0 + c] -= lrj * S[(k0 + c) * kBlkLd + k0 + j];
+        }
+        __syncwarp();
       }
-      S[j * kBlkLd + j] = sqrtf(d);
     }
     __syncthreads();
-    const float inv = 1.f / S[j * kBlkLd + j];
-    for (int i = j + 1 + tid; i < n; i += nthr) S[i * kBlkLd + j] *= inv;
+    // panel: row r solves x L_ddᵀ = S[r][k0..k0+7]
+    for (int r = k0 + kLeafB + tid; r < n; r += 256) {
+      float x[kLeafB];
+#pragma unroll
+      for (int j = 0; j < kLeafB; ++j) {
+        float v = S[r * kBlkLd + k0 + j];
+#pragma unroll
+        for (int c = 0; c < j; ++c) v = fmaf(-x[c], S[(k0 + j) * kBlkLd + k0 + c], v);
+        x[j] = v / S[(k0 + j) * kBlkLd + k0 + j];
+      }
+#pragma unroll
+      for (int j = 0; j < kLeafB; ++j) S[r * kBlkLd + k0 + j] = x[j];
+    }
     __syncthreads();
-    for (int i = j + 1 + (tid >> 1); i < n; i += nthr >> 1) {
-      const float lij = S[i * kBlkLd + j];
-      for (int k = j + 1 + (tid & 1); k <= i; k += 2) S[i * kBlkLd + k] -= lij * S[k * kBlkLd + j];
+    // trailing lower triangle, rank 8
+    for (int r = k0 + kLeafB + warp; r < n; r += 8) {
+      float a[kLeafB];
+#pragma unroll
+      for (int j = 0; j < kLeafB; ++j) a[j] = S[r * kBlkLd + k0 + j];
+      for (int c = k0 + kLeafB + lane; c <= r; c += 32) {
+        float v = S[r * kBlkLd + c];
+#pragma unroll
+        for (int j = 0; j < kLeafB; ++j) v = fmaf(-a[j], S[c * kBlkLd + k0 + j], v);
+        S[r * kBlkLd + c] = v;
+      }
     }
     __syncthreads();
   }
-  for (int i = 0; i < n; ++i) {
-    const float dinv = 1.f / S[i * kBlkLd + i];
-    float v = 0.f;
-    const int j = tid;
-    if (j <= i) {
-      float s0 = (i == j) ? 1.f : 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-      int k = j;
-      for (; k + 3 < i; k += 4) {
-        s0 = fmaf(-S[i * kBlkLd + k], S[k * kBlkLd + j], s0);
-        s1 = fmaf(-S[i * kBlkLd + k + 1], S[(k + 1) * kBlkLd + j], s1);
-        s2 = fmaf(-S[i * kBlkLd + k + 2], S[(k + 2) * kBlkLd + j], s2);
-        s3 = fmaf(-S[i * kBlkLd + k + 3], S[(k + 3) * kBlkLd + j], s3);
+  // ---- invert in place
+  for (int i0 = 0; i0 < n; i0 += kLeafB) {
+    for (int e = tid; e < kLeafB * i0; e += 256) {
+      const int r = e & (kLeafB - 1), c = e >> 3;
+      float s0 = 0.f, s1 = 0.f;
+      int k = c;
+      for (; k + 1 < i0; k += 2) {
+        s0 = fmaf(S[(i0 + r) * kBlkLd + k], S[k * kBlkLd + c], s0);
+        s1 = fmaf(S[(i0 + r) * kBlkLd + k + 1], S[(k + 1) * kBlkLd + c], s1);
       }
-      for (; k < i; ++k) s0 = fmaf(-S[i * kBlkLd + k], S[k * kBlkLd + j], s0);
-      v = ((s0 + s1) + (s2 + s3)) * dinv;
+      if (k < i0) s0 = fmaf(S[(i0 + r) * kBlkLd + k], S[k * kBlkLd + c], s0);
+      Tb[r * kLeafN + c] = s0 + s1;
+    }
+    if (warp == 0 && lane < kLeafB) {
+      const int c = lane;
+      float col[kLeafB];
+#pragma unroll
+      for (int r = 0; r < kLeafB; ++r) {
+        float v = (r == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int k = 0; k < r; ++k)
+          if (k >= c) v = fmaf(-S[(i0 + r) * kBlkLd + i0 + k], col[k], v);
+        col[r] = r >= c ? v / S[(i0 + r) * kBlkLd + i0 + r] : 0.f;
+      }
+#pragma unroll
+      for (int r = 0; r < kLeafB; ++r) Wd[r * kLeafB + c] = col[r];
     }
     __syncthreads();
-    if (j <= i) S[i * kBlkLd + j] = v;
+    for (int e = tid; e < kLeafB * i0; e += 256) {
+      const int r = e & (kLeafB - 1), c = e >> 3;
+      float v = 0.f;
+#pragma unroll
+      for (int j = 0; j < kLeafB; ++j)
+        if (j <= r) v = fmaf(Wd[r * kLeafB + j], Tb[j * kLeafN + c], v);
+      S[(i0 + r) * kBlkLd + c] = -v;
+    }
+    if (tid < kLeafB * kLeafB) {
+      const int r = tid >> 3, c = tid & (kLeafB - 1);
+      S[(i0 + r) * kBlkLd + i0 + c] = Wd[r * kLeafB + c];
+    }
     __syncthreads();
   }
-  for (int i = threadIdx.y; i < n; i += blockDim.y)
-    for (int k = threadIdx.x; k < n; k += blockDim.x) W[i * ldw + k] = k <= i ? S[i * kBlkLd + k] : 0.f;
+  for (int i = warp; i < n; i += 8)
+    for (int k = lane; k < n; k += 32) W[i * ldw + k] = k <= i ? S[i * kBlkLd + k] : 0.f;
 }
 
 // Diagonal blocks of one triangular inverse, inverted by one launch (one CTA each).
@@ -795,8 +861,8 @@ static uint64_t g_leaf_attr = 0;
 static rf_status chol_inv_rec(SolveCtx& c, float* A, long long lda, long long sA, float* W, long long ldw,
                               long long sW, int n, int batch, float* tmp, long long stmp) {
   rf_status st;
-  if (n <= kSolveBlock) {
-    k_chol_inv_leaf<<<batch, dim3(32, 8), kBlkSmem, c.s>>>(A, n, lda, sA, W, ldw, sW, c.dev_status);
+  if (n == kLeafN) {
+    k_chol_inv_leaf<<<batch, dim3(32, 8), kLeafSmem, c.s>>>(A, lda, sA, W, ldw, sW, c.dev_status);
     return cuda_check(cudaGetLastError(), "k_chol_inv_leaf launch");
   }
   const int n1 = split_point(n), n2 = n - n1;
@@ -818,9 +884,17 @@ static rf_status chol_inv_rec(SolveCtx& c, float* A, long long lda, long long sA
   return sgemm(c, false, false, n2, n1, n2, -1.f, W22, ldw, sW, A21, lda, sA, 0.f, W21, ldw, sW, batch, kSgemmKToM);
 }
 
+rf_status chol_inv_block(float* A, long long lda, long long sA, float* W, long long ldw, long long sW, int n, int batch,
+                         float* tmp, long long stmp, int32_t* dev_status, int sms, cudaStream_t s) {
+  rf_status st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf), kLeafSmem, &g_leaf_attr);
+  if (st != RF_OK) return st;
+  SolveCtx c{s, sms, nullptr, nullptr, dev_status};
+  return chol_inv_rec(c, A, lda, sA, W, ldw, sW, n, batch, tmp, stmp);
+}
+
 rf_status chol_inv_batched(float* A, long long lda, long long stride, float* Linv, long long ldi, int n, int batch,
                            float* tmp, int32_t* dev_status, int sms, cudaStream_t s) {
-  rf_status st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf), kBlkSmem, &g_leaf_attr);
+  rf_status st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf), kLeafSmem, &g_leaf_attr);
   if (st != RF_OK) return st;
   const long long stride_inv = static_cast<long long>(n) * ldi;
   SolveCtx c{s, sms, nullptr, nullptr, dev_status};

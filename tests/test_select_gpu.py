@@ -191,6 +191,17 @@ def test_select_every_layer_and_single_layer_table(small_stats):
     assert np.all(np.diff(best, axis=1) >= -TOL_R2)
 
 
+@KERNELS
+def test_select_wide_layers_factor_on_tensor_cores_matches_oracle(flags):
+    # F = 512 features per layer (4 x 128 heads): the Schur blocks' factorisation
+    # takes its top level on the tensor cores (widths that are multiples of 512)
+    cfg = synth.SelectConfig("selection 4->3 layers 4x128 k3", 8, L_src=4, L_tgt=3, k=3, H=4, hd=128, n=4096, R=40,
+                             lam=0.01)
+    gpu, ora = _rows_and_stats(cfg, [0, 1], cfg.n)
+    sel, r2 = _select(cfg, gpu, cfg.k, cfg.lam, rf.RF_ALPHA_TRACE, flags=flags)
+    _check_against_oracle(cfg, ora, sel, r2, cfg.k, cfg.lam, "trace")
+
+
 def test_select_handles_a_target_without_variance():
     # a constant target has TSS = 0 in every head: its scores are 0 and the choice is layer 0 first
     cfg = synth.SELECT_SMALL
