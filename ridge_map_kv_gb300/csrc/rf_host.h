@@ -73,18 +73,22 @@ rf_status centre_system(const double* G, const double* sx, const double* sy, con
                         double lambda, int alpha_mode, double* mu_x, double* mu_y, double* n_out, double* alpha,
                         double* alpha_out, double* H64, float* H32, int sms, cudaStream_t s);
 
-// For b < batch (solve.cu): Linv + b*n*ldi receives L_b^-1 (lower, zero above) of
-// the SPD n x n matrix A + b*stride = L_b L_bᵀ (ld lda, n % 128 == 0), in fp32. A is
-// used as scratch (its contents are lost). tmp holds batch * n * n / 4 floats.
+// For b < batch (solve.cu): W + b*sW (ld ldw) receives L_b^-1 of the SPD n x n block
+// A + b*sA = L_b L_bᵀ (ld lda, n % 128 == 0), in fp32 SIMT (recursive halving,
+// 128-wide leaves in shared memory). A is used as scratch; W's blocks above the
+// diagonal must already be zero. tmp holds batch * stmp floats, stmp >= n * n / 4.
 // A non-positive pivot records RF_ERR_NOT_SPD.
-rf_status chol_inv_batched(float* A, long long lda, long long stride, float* Linv, long long ldi, int n, int batch,
-                           float* tmp, int32_t* dev_status, int sms, cudaStream_t s);
-
-// The same for n x n sub-blocks (solve.cu): matrix b's block at A + b*sA (ld lda) and
-// its inverse at W + b*sW (ld ldw); W's blocks above the diagonal must already be
-// zero. tmp holds batch * stmp floats, stmp >= n * n / 4.
 rf_status chol_inv_block(float* A, long long lda, long long sA, float* W, long long ldw, long long sW, int n, int batch,
                          float* tmp, long long stmp, int32_t* dev_status, int sms, cudaStream_t s);
+
+// One SPD n x n matrix H (select.cu; n % 128 == 0; H is consumed): Linv = L^-1 of
+// H = L Lᵀ and, when Hinv is set, Hinv = H^-1 = Linvᵀ Linv, exactly symmetric. The
+// products of widths that are multiples of 512 and Linvᵀ Linv run as fp32-accurate
+// split-bf16 tensor-core GEMMs (CTA pairs when `pair`), the rest as fp32 SIMT.
+// ctmp holds n*n/4 floats, planes 3*n*n bf16. A non-positive pivot records
+// RF_ERR_NOT_SPD.
+rf_status spd_inverse(float* H, int n, float* Linv, float* Hinv, float* ctmp, __nv_bfloat16* planes, bool pair,
+                      int32_t* dev_status, int sms, cudaStream_t s);
 
 // Brackets one kernel launch with profiling events when rf_profile_start is active.
 struct ProfScope {

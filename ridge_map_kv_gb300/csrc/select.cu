@@ -511,6 +511,7 @@ struct SelCtx {
   int sms;
   int32_t* dev_status;
   bool pair;
+  int factor_stage = RF_STAGE_SELECT_FACTOR;  // profiler stage of the factorisation's launches
 };
 
 static rf_status split_rows(SelCtx& c, const float* src, long long ld_src, __nv_bfloat16* dst, long long ld_dst,
@@ -601,11 +602,19 @@ static SelOperand op(long long q_rows, long long s_rows, long long b_rows, long 
   return o;
 }
 
+// Scratch of the factorisation: ctmp [batch][n/2][n/2] fp32, fpa and fpb
+// [3][batch * n/2][n/2] bf16 each (only for widths that are multiples of 512).
+struct FactorScratch {
+  float* ctmp;
+  __nv_bfloat16* fpa;
+  __nv_bfloat16* fpb;
+};
+
 static rf_status split_blocks(SelCtx& c, const float* src, long long ld_src, long long s_src, int rows, int cols,
                               int batch, __nv_bfloat16* dst, bool tr) {
   const long long rows_out = tr ? cols : rows;
   const long long ld_dst = tr ? rows : cols;
-  ProfScope prof(c.s, RF_STAGE_SELECT_FACTOR);
+  ProfScope prof(c.s, c.factor_stage);
   if (tr) {
     k_split_blocks<<<dim3(cols / 32, rows / 32, batch), dim3(32, 8), 0, c.s>>>(src, ld_src, s_src, rows, cols, dst,
                                                                                ld_dst, rows_out * batch * ld_dst, 1);
@@ -624,11 +633,11 @@ static rf_status split_blocks(SelCtx& c, const float* src, long long ld_src, lon
 //   L21 = A21 W11ᵀ,  A22 −= L21 L21ᵀ,  Tᵀ = W11ᵀ L21ᵀ (into A21's storage),
 //   then W22 = L22^-1 from the second half and W21 = −W22 T.
 // Other widths run the fp32 SIMT recursion (chol_inv_block).
-static rf_status sel_factor(SelCtx& c, SelLayout& lay, float* A, long long lda, long long sA, float* W, long long ldw,
-                            long long sW, int n, int batch, long long stmp) {
+static rf_status sel_factor(SelCtx& c, const FactorScratch& lay, float* A, long long lda, long long sA, float* W,
+                            long long ldw, long long sW, int n, int batch, long long stmp) {
   rf_status st;
   if (n % 512 != 0) {
-    ProfScope prof(c.s, RF_STAGE_SELECT_FACTOR);
+    ProfScope prof(c.s, c.factor_stage);
     return chol_inv_block(A, lda, sA, W, ldw, sW, n, batch, lay.ctmp, stmp, c.dev_status, c.sms, c.s);
   }
   const int h = n / 2;
@@ -647,7 +656,7 @@ static rf_status sel_factor(SelCtx& c, SelLayout& lay, float* A, long long lda, 
     SelGemm g{};
     g.pa = lay.fpa, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
     g.pb = lay.fpb, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
-    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = RF_STAGE_SELECT_FACTOR;
+    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = c.factor_stage;
     g.out = L21, g.o_s = hh, g.ldo = h;
     if ((st = sel_gemm(c, g)) != RF_OK) return st;
   }
@@ -657,7 +666,7 @@ static rf_status sel_factor(SelCtx& c, SelLayout& lay, float* A, long long lda, 
     SelGemm g{};
     g.pa = lay.fpa, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
     g.pb = lay.fpa, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
-    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = RF_STAGE_SELECT_FACTOR;
+    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = c.factor_stage;
     g.alpha = -1.f, g.beta = 1.f;
     g.out = A22, g.o_s = sA, g.ldo = lda;
     g.csrc = A22, g.c_s = sA, g.ldc = lda;
@@ -669,7 +678,7 @@ static rf_status sel_factor(SelCtx& c, SelLayout& lay, float* A, long long lda, 
     SelGemm g{};
     g.pa = lay.fpb, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
     g.pb = lay.fpa, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
-    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = RF_STAGE_SELECT_FACTOR;
+    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = c.factor_stage;
     g.out = A21, g.o_s = sA, g.ldo = lda;
     if ((st = sel_gemm(c, g)) != RF_OK) return st;
   }
@@ -680,10 +689,46 @@ static rf_status sel_factor(SelCtx& c, SelLayout& lay, float* A, long long lda, 
   SelGemm g{};
   g.pa = lay.fpa, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
   g.pb = lay.fpb, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
-  g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = RF_STAGE_SELECT_FACTOR;
+  g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = c.factor_stage;
   g.alpha = -1.f;
   g.out = W21, g.o_s = sW, g.ldo = ldw;
   return sel_gemm(c, g);
+}
+
+// H = L Lᵀ (n x n SPD, n % 128 == 0, consumed): Linv = L^-1 and, when Hinv is set,
+// Hinv = Linvᵀ Linv = H^-1 as one split tensor-core product of Linvᵀ with itself,
+// its upper triangle then mirrored so that Hinv is exactly symmetric.
+__global__ void __launch_bounds__(256) k_mirror_upper_f32(float* __restrict__ M, int n) {
+  const int bx = blockIdx.x, by = blockIdx.y;  // block (bx, by) writes rows by*32.., columns bx*32..
+  if (bx > by) return;
+  __shared__ float t[32][33];
+  for (int j = threadIdx.y; j < 32; j += 8) t[j][threadIdx.x] = M[static_cast<size_t>(bx * 32 + j) * n + by * 32 + threadIdx.x];
+  __syncthreads();
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int i = by * 32 + j, c = bx * 32 + threadIdx.x;
+    if (i > c) M[static_cast<size_t>(i) * n + c] = t[threadIdx.x][j];
+  }
+}
+
+rf_status spd_inverse(float* H, int n, float* Linv, float* Hinv, float* ctmp, __nv_bfloat16* planes, bool pair,
+                      int32_t* dev_status, int sms, cudaStream_t s) {
+  SelCtx c{s, sms, dev_status, pair, RF_STAGE_SOLVE};
+  rf_status st;
+  if ((st = cuda_check(cudaMemsetAsync(Linv, 0, sizeof(float) * n * n, s), "zero L^-1")) != RF_OK) return st;
+  const long long q = 3LL * n * n / 4;  // one plane set of the factorisation's products
+  if ((st = sel_factor(c, FactorScratch{ctmp, planes, planes + q}, H, n, 0, Linv, n, 0, n, 1,
+                       static_cast<long long>(n) * n / 4)) != RF_OK)
+    return st;
+  if (Hinv == nullptr) return RF_OK;
+  if ((st = split_blocks(c, Linv, n, 0, n, n, 1, planes, true)) != RF_OK) return st;
+  SelGemm g{};
+  g.pa = planes, g.a_rows = n, g.a_kext = n, g.a = op(0, 0, 0, 0, 0, 0);
+  g.pb = planes, g.b_rows = n, g.b_kext = n, g.b = op(0, 0, 0, 0, 0, 0);
+  g.M = n, g.N = n, g.K = n, g.stage = RF_STAGE_SOLVE;
+  g.out = Hinv, g.ldo = n;
+  if ((st = sel_gemm(c, g)) != RF_OK) return st;
+  k_mirror_upper_f32<<<dim3(n / 32, n / 32), dim3(32, 8), 0, s>>>(Hinv, n);
+  return cuda_check(cudaGetLastError(), "k_mirror_upper_f32 launch");
 }
 
 }  // namespace rf
@@ -772,8 +817,9 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
         if ((st = cuda_check(cudaMemsetAsync(lay.Linv, 0, sizeof(float) * Q * Ls * F * F, c.s), "zero L^-1")) != RF_OK)
           return st;
       }
-      if ((st = sel_factor(c, lay, lay.Lf, F, static_cast<long long>(F) * F, lay.Linv, F, static_cast<long long>(F) * F,
-                           F, Q * Ls, static_cast<long long>(F) * F / 4)) != RF_OK)
+      if ((st = sel_factor(c, FactorScratch{lay.ctmp, lay.fpa, lay.fpb}, lay.Lf, F, static_cast<long long>(F) * F,
+                           lay.Linv, F, static_cast<long long>(F) * F, F, Q * Ls, static_cast<long long>(F) * F / 4)) !=
+          RF_OK)
         return st;
       if ((st = split_rows(c, lay.Linv, F, lay.Lp, F, 0, lrows * F, lrows, F)) != RF_OK) return st;
       if ((st = split_rows(c, lay.RT, D, lay.RTp, D, 0, rtrows * D, rtrows, static_cast<int>(D))) != RF_OK) return st;

@@ -7,11 +7,12 @@
 // From the one-pass sums (G, C, sx, sy, n) in fp64:
 //   k_means, k_trace_alpha  μ_x = sx/n, μ_p = sy_p/n, tr(Gc), α
 //   k_build_h               H = Gc + αI with Gc = G − n μ_x μ_xᵀ (fp64 and fp32 copies)
-//   chol_lower (recursive)  H = L Lᵀ in fp32: a one-CTA kernel factors 128 x 128
-//                           diagonal blocks; panels and trailing updates are fp32
-//                           GEMMs (k_sgemm) with the inverse of the diagonal block
-//   trinv_lower (recursive) L^-1 from one-CTA diagonal inverses and fp32 GEMMs
-//   k_sgemm                 H^-1 = L^-ᵀ L^-1 (fp32 SIMT)
+//   spd_inverse (select.cu) H = L Lᵀ, L^-1 by recursive halving (products of widths
+//                           that are multiples of 512 on the tensor cores, the
+//                           narrower ones fp32 SIMT k_sgemm, 128-wide leaves
+//                           factored and inverted in shared memory by
+//                           k_chol_inv_leaf), then H^-1 = L^-ᵀ L^-1 on the tensor
+//                           cores, its upper triangle mirrored
 //   split3 + tc_gemm<Split3Prob>  A_p = Cc_pᵀ H^-1 for every map on the tensor
 //                           cores: each fp32 operand is the sum of three bf16
 //                           planes (hi + mid + lo, exact to fp32 rounding), and
@@ -19,8 +20,9 @@
 //                           (hi·hi, mid·hi, hi·mid, lo·hi, mid·mid, hi·lo) are
 //                           summed over 1024-wide K chunks in TMEM, then in fp32
 //                           registers across chunks and terms
-//   refinement (optional)   R_p = Cc_pᵀ − A_p H with fp64 products (k_resid64),
-//                           A_p += R_p H^-1 (the same split tensor-core product)
+//   refinement (optional)   R_p = Cc_pᵀ − A_p H, fp64-accurate on the tensor cores
+//                           (OzakiProb: integer digit planes, exact chunk sums,
+//                           fp64 epilogue), A_p += R_p H^-1 (the split product)
 //   k_bias                  b_p = μ_p − A_p μ_x (fp64 accumulation)
 #include <algorithm>
 
@@ -163,44 +165,6 @@ __global__ void __launch_bounds__(256) k_sgemm(int M, int N, int K, float alpha,
 constexpr int kBlkLd = kSolveBlock + 1;
 constexpr size_t kBlkSmem = sizeof(float) * kSolveBlock * kBlkLd;
 
-// In-place lower Cholesky of the n x n block at A (n <= 128); zeroes the upper
-// triangle. A non-positive pivot records RF_ERR_NOT_SPD and continues with 1.
-// Column by column: the pivot, the column scale, then the trailing update with
-// two threads per row (no index divisions; the 129-float row pitch keeps both
-// the row and the column accesses free of bank conflicts). CTA b works on the
-// block at A + b * stride.
-__global__ void __launch_bounds__(256) k_chol_base(float* A, int n, long long lda, long long stride,
-                                                   int32_t* dev_status) {
-  extern __shared__ float S[];
-  A += blockIdx.x * stride;
-  for (int i = threadIdx.y; i < n; i += blockDim.y)
-    for (int k = threadIdx.x; k < n; k += blockDim.x) S[i * kBlkLd + k] = A[i * lda + k];
-  const int tid = threadIdx.y * blockDim.x + threadIdx.x;
-  const int nthr = blockDim.x * blockDim.y;
-  __syncthreads();
-  for (int j = 0; j < n; ++j) {
-    if (tid == 0) {
-      float d = S[j * kBlkLd + j];
-      if (!(d > 0.f)) {
-        record_status(dev_status, RF_ERR_NOT_SPD);
-        d = 1.f;
-      }
-      S[j * kBlkLd + j] = sqrtf(d);
-    }
-    __syncthreads();
-    const float inv = 1.f / S[j * kBlkLd + j];
-    for (int i = j + 1 + tid; i < n; i += nthr) S[i * kBlkLd + j] *= inv;
-    __syncthreads();
-    for (int i = j + 1 + (tid >> 1); i < n; i += nthr >> 1) {
-      const float lij = S[i * kBlkLd + j];
-      for (int k = j + 1 + (tid & 1); k <= i; k += 2) S[i * kBlkLd + k] -= lij * S[k * kBlkLd + j];
-    }
-    __syncthreads();
-  }
-  for (int i = threadIdx.y; i < n; i += blockDim.y)
-    for (int k = threadIdx.x; k < n; k += blockDim.x) A[i * lda + k] = k <= i ? S[i * kBlkLd + k] : 0.f;
-}
-
 // W = L^-1 for the 128 x 128 SPD block A = L Lᵀ, one CTA (8 warps) per matrix b
 // (A + b*sA, W + b*sW), in shared memory and blocked by 8 so that a column or row
 // block costs a few barriers instead of one per column:
@@ -327,53 +291,6 @@ __global__ void __launch_bounds__(256) k_chol_inv_leaf(const float* __restrict__
     for (int k = lane; k < n; k += 32) W[i * ldw + k] = k <= i ? S[i * kBlkLd + k] : 0.f;
 }
 
-// Diagonal blocks of one triangular inverse, inverted by one launch (one CTA each).
-constexpr int kMaxLeaves = 256;
-struct LeafBlocks {
-  int off[kMaxLeaves];
-  int size[kMaxLeaves];
-};
-
-// W = L^-1 for lower n x n diagonal blocks L (n <= 128), row by row in shared
-// memory: W[i][j] = (δ_ij − Σ_{j<=k<i} L[i][k] W[k][j]) / L[i][i], thread j
-// computing column j of row i once rows < i are done (four partial sums keep the
-// dependent chain short); the upper triangle of W is zero. CTA b inverts the
-// block at (off[b], off[b]) of size size[b], in matrix blockIdx.y (L0 + y * sL,
-// W0 + y * sW).
-__global__ void __launch_bounds__(128) k_trinv_base(const float* L0, long long ldl, long long sL, float* W0,
-                                                    long long ldw, long long sW, const __grid_constant__ LeafBlocks lb) {
-  const int off = lb.off[blockIdx.x], n = lb.size[blockIdx.x];
-  const float* L = L0 + blockIdx.y * sL + static_cast<long long>(off) * ldl + off;
-  float* W = W0 + blockIdx.y * sW + static_cast<long long>(off) * ldw + off;
-  extern __shared__ float S[];
-  float* Wi = S + kSolveBlock * kBlkLd;
-  for (int i = 0; i < n; ++i)
-    for (int k = threadIdx.x; k < n; k += blockDim.x) S[i * kBlkLd + k] = L[i * ldl + k];
-  __syncthreads();
-  const int j = threadIdx.x;
-  for (int i = 0; i < n; ++i) {
-    if (j < n) {
-      float s = 0.f;
-      if (j <= i) {
-        float s0 = (i == j) ? 1.f : 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-        int k = j;
-        for (; k + 3 < i; k += 4) {
-          s0 = fmaf(-S[i * kBlkLd + k], Wi[k * kBlkLd + j], s0);
-          s1 = fmaf(-S[i * kBlkLd + k + 1], Wi[(k + 1) * kBlkLd + j], s1);
-          s2 = fmaf(-S[i * kBlkLd + k + 2], Wi[(k + 2) * kBlkLd + j], s2);
-          s3 = fmaf(-S[i * kBlkLd + k + 3], Wi[(k + 3) * kBlkLd + j], s3);
-        }
-        for (; k < i; ++k) s0 = fmaf(-S[i * kBlkLd + k], Wi[k * kBlkLd + j], s0);
-        s = ((s0 + s1) + (s2 + s3)) / S[i * kBlkLd + i];
-      }
-      Wi[i * kBlkLd + j] = s;
-    }
-    __syncthreads();
-  }
-  for (int i = 0; i < n; ++i)
-    for (int k = threadIdx.x; k < n; k += blockDim.x) W[i * ldw + k] = Wi[i * kBlkLd + k];
-}
-
 // --------------------------------------------------------------------------
 // Statistics -> centred system (fp64)
 // --------------------------------------------------------------------------
@@ -446,56 +363,6 @@ __global__ void k_centre_c(const double* C, const double* mu_x, const double* mu
   }
 }
 
-// R_p[o][i] = (C_p[i][o] − n μ_x[i] μ_p[o]) − Σ_j A_p[o][j] H[j][i], fp64 products and
-// sums, stored as fp32. 64 x 64 tiles, 256 threads, 4 x 4 outputs per thread.
-__global__ void __launch_bounds__(256) k_resid64(int d_out, int d_in, const float* __restrict__ A,
-                                                 const double* __restrict__ H, const double* __restrict__ C,
-                                                 const double* __restrict__ mu_x, const double* __restrict__ mu_y,
-                                                 const double* __restrict__ n, float* __restrict__ R) {
-  __shared__ double As[16][65];
-  __shared__ double Hs[16][64];
-  const int p = blockIdx.z;
-  const int o0 = blockIdx.y * 64, i0 = blockIdx.x * 64;
-  const float* Ap = A + static_cast<long long>(p) * d_out * d_in;
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  double acc[4][4] = {};
-  for (int k0 = 0; k0 < d_in; k0 += 16) {
-    for (int e = tid; e < 16 * 64; e += 256) {
-      const int r = e >> 4, c = e & 15;  // A tile: rows o0+r, cols k0+c
-      As[c][r] = static_cast<double>(Ap[static_cast<long long>(o0 + r) * d_in + k0 + c]);
-      const int kr = e >> 6, ic = e & 63;  // H tile: rows k0+kr, cols i0+ic
-      Hs[kr][ic] = H[static_cast<long long>(k0 + kr) * d_in + i0 + ic];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      double a[4], h[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        a[q] = As[kk][ty * 4 + q];
-        h[q] = Hs[kk][tx * 4 + q];
-      }
-#pragma unroll
-      for (int x = 0; x < 4; ++x)
-#pragma unroll
-        for (int y = 0; y < 4; ++y) acc[x][y] = fma(a[x], h[y], acc[x][y]);
-    }
-    __syncthreads();
-  }
-  const double nn = *n;
-#pragma unroll
-  for (int x = 0; x < 4; ++x) {
-    const int o = o0 + ty * 4 + x;
-#pragma unroll
-    for (int y = 0; y < 4; ++y) {
-      const int i = i0 + tx * 4 + y;
-      const double cc = C[(static_cast<long long>(p) * d_in + i) * d_out + o] -
-                        nn * mu_x[i] * mu_y[static_cast<long long>(p) * d_out + o];
-      R[(static_cast<long long>(p) * d_out + o) * d_in + i] = static_cast<float>(cc - acc[x][y]);
-    }
-  }
-}
-
 // b_p[o] = μ_p[o] − Σ_i A_p[o][i] μ_x[i] (fp64), one warp per output; also the
 // optional bf16 copy of A.
 __global__ void k_bias(const float* A, const double* mu_x, const double* mu_y, long long rows, int d_in, float* b) {
@@ -521,8 +388,6 @@ __global__ void k_to_bf16(const float* A, long long total, __nv_bfloat16* out) {
 struct SolveCtx {
   cudaStream_t s;
   int sms;
-  float* tmp;    // d_in^2 scratch for panels
-  float* tmp2;   // d_in^2 scratch inside the triangular inverse
   int32_t* dev_status;
 };
 
@@ -711,74 +576,165 @@ static rf_status split_gemm(SolveCtx& c, const float* a, bool a_tr, const float*
   return launch_gemm(pr, static_cast<int64_t>(P) * pr.m_tiles * pr.n_tiles, c.sms, c.s, "split GEMM launch");
 }
 
+// --------------------------------------------------------------------------
+// fp64-accurate residual on the tensor cores (Ozaki-scheme splitting: Ozaki,
+// Ogita, Oishi and Rump, "Error-free transformations of matrix multiplication by
+// using fast routines of matrix multiplication", 2012), for the refinement
+//   R_p = Cc_pᵀ − A_p H.
+// Each row of A_p (fp32) and each row of H (fp64; H is symmetric, so its rows are
+// its columns) is scaled by a power of two σ ≥ its largest magnitude and cut into
+// kOzDigits integer digits of 6 bits: x/σ = Σ_s d_s 2^(−6s), |d_1| <= 64, |d_s| <= 32
+// after, every digit exact in bf16. A digit product summed over a K chunk of 2048
+// is an integer below 2^23, exact in the fp32 accumulator; the epilogue adds the
+// chunks and the digit pairs of one weight m = s + t as exact int32 sums J_m, then
+// R −= σ_o τ_i 2^(−6m) J_m in fp64. Pairs with s + t <= kOzDigits + 1 are kept:
+// 42-bit operands, a residual accurate to about 2^-41 of Σ|A||H| in the worst case.
+// --------------------------------------------------------------------------
+constexpr int kOzDigits = 7;
+constexpr int kOzChunk = 2048;
+constexpr int kOzPairs = kOzDigits * (kOzDigits + 1) / 2;
+
+// Digits of each row of an fp32 or fp64 matrix [rows][cols]: planes [kOzDigits][rows][cols]
+// bf16 and the row scale σ (a power of two, 0 for a zero row). One warp per row.
+template <class T>
+__global__ void __launch_bounds__(256) k_oz_digits(const T* __restrict__ X, int rows, int cols,
+                                                   __nv_bfloat16* __restrict__ planes, double* __restrict__ scale) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= rows) return;
+  const T* x = X + static_cast<size_t>(warp) * cols;
+  double mx = 0.0;
+  for (int k = lane; k < cols; k += 32) mx = fmax(mx, fabs(static_cast<double>(x[k])));
+  for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  int e = 0;
+  if (mx > 0.0) frexp(mx, &e);  // mx = f 2^e, f in [0.5, 1): σ = 2^e >= mx
+  if (lane == 0) scale[warp] = mx > 0.0 ? ldexp(1.0, e) : 0.0;
+  const size_t plane = static_cast<size_t>(rows) * cols;
+  for (int k = lane; k < cols; k += 32) {
+    double v = mx > 0.0 ? ldexp(static_cast<double>(x[k]), -e) : 0.0;  // exact, |v| <= 1
+#pragma unroll
+    for (int d = 0; d < kOzDigits; ++d) {
+      const double t = v * 64.0;
+      const double r = rint(t);
+      v = t - r;  // exact
+      planes[d * plane + static_cast<size_t>(warp) * cols + k] = __float2bfloat16_rn(static_cast<float>(r));
+    }
+  }
+}
+
+// R64[o][i] = C_p[i][o] − n μ_x[i] μ_p[o] (fp64), through 32 x 32 shared tiles.
+// Grid (d_out/32, d_in/32), 32 x 8 threads.
+__global__ void __launch_bounds__(256) k_oz_init(const double* __restrict__ C, const double* __restrict__ mu_x,
+                                                 const double* __restrict__ mu_y, const double* __restrict__ n,
+                                                 int d_in, int d_out, double* __restrict__ R64) {
+  __shared__ double t[32][33];
+  const int o0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
+  const double nn = *n;
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int i = i0 + j, o = o0 + threadIdx.x;
+    t[j][threadIdx.x] = C[static_cast<size_t>(i) * d_out + o] - nn * mu_x[i] * mu_y[o];
+  }
+  __syncthreads();
+  for (int j = threadIdx.y; j < 32; j += 8) R64[static_cast<size_t>(o0 + j) * d_in + i0 + threadIdx.x] = t[threadIdx.x][j];
+}
+
+// Digit pair number pi (0 <= pi < kOzPairs) in weight order: m = s + t = 2, 3, ...,
+// and within a weight s = 1 .. m−1.
+__device__ __forceinline__ void oz_pair(int pi, int& m, int& s) {
+  m = 2;
+  int base = 0;
+  while (pi >= base + (m - 1)) {
+    base += m - 1;
+    ++m;
+  }
+  s = pi - base + 1;
+}
+
+template <bool kPair_>
+struct OzakiProb {
+  CUtensorMap tmA;  // digits of A_p rows: [kOzDigits * d_out][d_in]
+  CUtensorMap tmB;  // digits of H rows:   [kOzDigits * d_in][d_in]
+  const double* sA;  // [d_out] row scales of A_p
+  const double* sH;  // [d_in]  row scales of H
+  double* R64;       // [d_out][d_in] fp64 residual, initialised to Cc_pᵀ
+  float* R32;        // [d_out][d_in] fp32 result
+  int d_out, d_in, m_tiles, n_tiles, n_chunks;
+  int32_t* dev_status;
+  uint64_t timeout_ns;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kPair = kPair_;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kCols = kBN / 2;
+  struct EpiState {
+    int32_t rs[kCols];
+  };
+  using Cfg = GemmCfg<kPair_>;
+
+  __device__ void prefetch() const {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  __device__ int num_units() const { return m_tiles * n_tiles; }
+  __device__ int num_subtiles(int) const { return kOzPairs * n_chunks; }
+  __device__ int num_kb(int, int sb) const {
+    const int c = sb % n_chunks;
+    return (min(kOzChunk, d_in - c * kOzChunk) + kBK - 1) / kBK;
+  }
+  struct Coords {
+    int a_row, b_row, k0;
+  };
+  __device__ Coords coords(int u, int sb, uint32_t rank) const {
+    const int nt = u % n_tiles, mt = u / n_tiles;
+    const int pi = sb / n_chunks, c = sb - pi * n_chunks;
+    int m, s;
+    oz_pair(pi, m, s);
+    const int t = m - s;
+    return {(s - 1) * d_out + mt * Cfg::kUnitM + static_cast<int>(rank) * kBM,
+            (t - 1) * d_in + nt * kBN + static_cast<int>(rank) * Cfg::kBRows, c * kOzChunk};
+  }
+  __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    load_operand<kBM, false, kPair>(sa, &tmA, bar, c.k0 + kb * kBK, c.a_row);
+    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, c.k0 + kb * kBK, c.b_row);
+  }
+  __device__ void epilogue(EpiState& es, int, int sb, int, uint32_t tacc, int, int, uint32_t) const {
+    const int pi = sb / n_chunks, c = sb - pi * n_chunks;
+    int m, s;
+    oz_pair(pi, m, s);
+    const bool first = c == 0 && s == 1;  // first sub-tile of weight m
+#pragma unroll
+    for (int ch = 0; ch < kCols / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(tacc + ch * 32, v);
+      tmem_wait_ld32(v);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int32_t x = __float2int_rn(u2f(v[q]));  // an exact integer
+        es.rs[ch * 32 + q] = first ? x : es.rs[ch * 32 + q] + x;
+      }
+    }
+  }
+  __device__ void epilogue_after(EpiState& es, int u, int sb, int nsub, int row, int col0, uint32_t rank) const {
+    const int pi = sb / n_chunks, c = sb - pi * n_chunks;
+    int m, s;
+    oz_pair(pi, m, s);
+    if (c != n_chunks - 1 || s != m - 1) return;  // weight m not complete yet
+    const int nt = u % n_tiles, mt = u / n_tiles;
+    const size_t o = static_cast<size_t>(mt) * Cfg::kUnitM + rank * kBM + row;
+    const size_t i0 = static_cast<size_t>(nt) * kBN + col0;
+    const double so = ldexp(sA[o], -6 * m);
+    double* r = R64 + o * d_in + i0;
+    if (sb == nsub - 1) {
+      float* w = R32 + o * d_in + i0;
+#pragma unroll
+      for (int q = 0; q < kCols; ++q) w[q] = static_cast<float>(r[q] - so * sH[i0 + q] * static_cast<double>(es.rs[q]));
+    } else {
+#pragma unroll
+      for (int q = 0; q < kCols; ++q) r[q] -= so * sH[i0 + q] * static_cast<double>(es.rs[q]);
+    }
+  }
+};
+
 static int split_point(int n) { return std::max(kSolveBlock, (n / 2) / kSolveBlock * kSolveBlock); }
-
-// W (n x n, ld ldw) = L^-1 for the lower-triangular L (n x n, ld ldl); n % 128 == 0.
-static void trinv_leaves(int off, int n, LeafBlocks& lb, int& count) {
-  if (n <= kSolveBlock) {
-    lb.off[count] = off;
-    lb.size[count] = n;
-    ++count;
-    return;
-  }
-  const int n1 = split_point(n);
-  trinv_leaves(off, n1, lb, count);
-  trinv_leaves(off + n1, n - n1, lb, count);
-}
-
-// Combines the inverted diagonal blocks bottom-up: W21 = −W22 (L21 W11).
-static rf_status trinv_combine(SolveCtx& c, const float* L, int n, long long ldl, float* W, long long ldw) {
-  if (n <= kSolveBlock) return RF_OK;
-  const int n1 = split_point(n), n2 = n - n1;
-  rf_status st;
-  if ((st = trinv_combine(c, L, n1, ldl, W, ldw)) != RF_OK) return st;
-  if ((st = trinv_combine(c, L + n1 * ldl + n1, n2, ldl, W + n1 * ldw + n1, ldw)) != RF_OK) return st;
-  // T = L21 W11 ;  W21 = −W22 T ;  W12 = 0
-  if ((st = sgemm(c, false, false, n2, n1, n1, 1.f, L + n1 * ldl, ldl, 0, W, ldw, 0, 0.f, c.tmp2, n1, 0, 1)) != RF_OK)
-    return st;
-  if ((st = sgemm(c, false, false, n2, n1, n2, -1.f, W + n1 * ldw + n1, ldw, 0, c.tmp2, n1, 0, 0.f, W + n1 * ldw, ldw,
-                  0, 1)) != RF_OK)
-    return st;
-  return cuda_check(cudaMemset2DAsync(W + n1, ldw * sizeof(float), 0, n2 * sizeof(float), n1, c.s), "zero W12");
-}
-
-// W = L^-1 for the lower n x n L: every diagonal block of the split tree in one
-// launch, then the products that join them.
-static rf_status trinv_lower(SolveCtx& c, const float* L, int n, long long ldl, float* W, long long ldw) {
-  LeafBlocks lb;
-  int count = 0;
-  trinv_leaves(0, n, lb, count);
-  k_trinv_base<<<count, kSolveBlock, 2 * kBlkSmem, c.s>>>(L, ldl, 0, W, ldw, 0, lb);
-  rf_status st = cuda_check(cudaGetLastError(), "k_trinv_base launch");
-  if (st != RF_OK) return st;
-  return trinv_combine(c, L, n, ldl, W, ldw);
-}
-
-// In-place lower Cholesky of the n x n matrix A (ld lda); n % 128 == 0.
-static rf_status chol_lower(SolveCtx& c, float* A, int n, long long lda, float* winv) {
-  if (n <= kSolveBlock) {
-    k_chol_base<<<1, dim3(32, 8), kBlkSmem, c.s>>>(A, n, lda, 0, c.dev_status);
-    return cuda_check(cudaGetLastError(), "k_chol_base launch");
-  }
-  const int n1 = split_point(n), n2 = n - n1;
-  rf_status st;
-  if ((st = chol_lower(c, A, n1, lda, winv)) != RF_OK) return st;
-  // W11 = L11^-1 ;  L21 = A21 W11ᵀ ;  A22 −= L21 L21ᵀ
-  if ((st = trinv_lower(c, A, n1, lda, winv, n1)) != RF_OK) return st;
-  if ((st = sgemm(c, false, true, n2, n1, n1, 1.f, A + n1 * lda, lda, 0, winv, n1, 0, 0.f, c.tmp, n1, 0, 1)) != RF_OK)
-    return st;
-  if ((st = cuda_check(cudaMemcpy2DAsync(A + n1 * lda, lda * sizeof(float), c.tmp, n1 * sizeof(float),
-                                         n1 * sizeof(float), n2, cudaMemcpyDeviceToDevice, c.s),
-                       "copy L21")) != RF_OK)
-    return st;
-  if ((st = sgemm(c, false, true, n2, n2, n1, -1.f, A + n1 * lda, lda, 0, A + n1 * lda, lda, 0, 1.f,
-                  A + n1 * lda + n1, lda, 0, 1)) != RF_OK)
-    return st;
-  // zero the upper block so that later full-block products see a triangular L
-  if ((st = cuda_check(cudaMemset2DAsync(A + n1, lda * sizeof(float), 0, n2 * sizeof(float), n1, c.s), "zero U12")) != RF_OK)
-    return st;
-  return chol_lower(c, A + n1 * lda + n1, n2, lda, winv);
-}
 
 struct SolveLayout {
   double* mu_x;
@@ -789,11 +745,15 @@ struct SolveLayout {
   float* L;
   float* Linv;
   float* Hinv;
-  float* tmp;
-  float* tmp2;
+  float* tmp;   // [d_in/2][d_in/2] scratch of the factorisation
   float* work;  // Cc (first solve) then R (refinement), [P][d_in][d_out] floats
   __nv_bfloat16* planes_a;  // [3][P][d_out][d_in] bf16 split of Cc_pᵀ or R_p
   __nv_bfloat16* planes_b;  // [3][d_in][d_in] bf16 split of H^-1
+  __nv_bfloat16* ozH;       // [kOzDigits][d_in][d_in] digits of H's rows (refinement)
+  double* sH;               // [d_in] their scales
+  __nv_bfloat16* ozA;       // [kOzDigits][d_out][d_in] digits of one map's rows
+  double* sA;               // [d_out]
+  double* R64;              // [d_out][d_in] one map's fp64 residual
   size_t bytes;
 };
 
@@ -809,13 +769,56 @@ static SolveLayout solve_layout(const rf_calib_desc* d, void* ws) {
   l.L = c.take<float>(di * di);
   l.Linv = c.take<float>(di * di);
   l.Hinv = c.take<float>(di * di);
-  l.tmp = c.take<float>(di * di);
-  l.tmp2 = c.take<float>(di * di);
+  l.tmp = c.take<float>(di * di / 4);
   l.work = c.take<float>(std::max<int64_t>(P * di * dout, 1));
   l.planes_a = c.take<__nv_bfloat16>(3 * std::max<int64_t>(P * di * dout, 1));
   l.planes_b = c.take<__nv_bfloat16>(3 * di * di);
+  l.ozH = c.take<__nv_bfloat16>(kOzDigits * di * di);
+  l.sH = c.take<double>(di);
+  l.ozA = c.take<__nv_bfloat16>(kOzDigits * dout * di);
+  l.sA = c.take<double>(dout);
+  l.R64 = c.take<double>(dout * di);
   l.bytes = c.bytes();
   return l;
+}
+
+// R_p = Cc_pᵀ − A_p H for every map, fp64-accurate (OzakiProb), into R32 [P][d_out][d_in].
+template <bool kPair>
+static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* C, const float* A, int P, int di,
+                             int dout, float* R32) {
+  using Cfg = GemmCfg<kPair>;
+  rf_status st;
+  const unsigned hb = static_cast<unsigned>((static_cast<long long>(di) * 32 + 255) / 256);
+  const unsigned ab = static_cast<unsigned>((static_cast<long long>(dout) * 32 + 255) / 256);
+  k_oz_digits<double><<<hb, 256, 0, c.s>>>(lay.H64, di, di, lay.ozH, lay.sH);
+  OzakiProb<kPair> pr;
+  if ((st = make_tmap_bf16_2d(&pr.tmA, lay.ozA, di, static_cast<uint64_t>(kOzDigits) * dout, di, kBK, kBM)) != RF_OK)
+    return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmB, lay.ozH, di, static_cast<uint64_t>(kOzDigits) * di, di, kBK, Cfg::kBRows)) !=
+      RF_OK)
+    return st;
+  pr.sA = lay.sA;
+  pr.sH = lay.sH;
+  pr.R64 = lay.R64;
+  pr.d_out = dout;
+  pr.d_in = di;
+  pr.m_tiles = dout / Cfg::kUnitM;
+  pr.n_tiles = di / kBN;
+  pr.n_chunks = (di + kOzChunk - 1) / kOzChunk;
+  pr.dev_status = c.dev_status;
+  pr.timeout_ns = wait_timeout_ns();
+  for (int p = 0; p < P; ++p) {
+    const size_t off = static_cast<size_t>(p) * dout * di;
+    k_oz_digits<float><<<ab, 256, 0, c.s>>>(A + off, dout, di, lay.ozA, lay.sA);
+    k_oz_init<<<dim3(dout / 32, di / 32), dim3(32, 8), 0, c.s>>>(C + off, lay.mu_x, lay.mu_y + static_cast<size_t>(p) * dout,
+                                                                 lay.n, di, dout, lay.R64);
+    if ((st = cuda_check(cudaGetLastError(), "residual set-up launches")) != RF_OK) return st;
+    pr.R32 = R32 + off;
+    if ((st = launch_gemm(pr, static_cast<int64_t>(pr.m_tiles) * pr.n_tiles, c.sms, c.s, "residual GEMM launch")) !=
+        RF_OK)
+      return st;
+  }
+  return RF_OK;
 }
 
 static rf_status check_solve_desc(const rf_calib_desc* d) {
@@ -824,16 +827,8 @@ static rf_status check_solve_desc(const rf_calib_desc* d) {
   if (d->d_in % 256 != 0 || d->d_out % 256 != 0)
     return fail(RF_ERR_SHAPE, "d_in and d_out must be multiples of 256");
   if (d->d_in > 32768 || d->n_maps > 65535) return fail(RF_ERR_SHAPE, "d_in must be <= 32768, n_maps <= 65535");
-  // (d_in <= 32768 keeps the triangular inverse's leaf blocks within kMaxLeaves.)
+  // (d_in <= 32768 keeps the d_in x d_in work arrays of the workspace within 32 GB.)
   return RF_OK;
-}
-
-static uint64_t g_chol_attr = 0, g_trinv_attr = 0;
-
-static rf_status solve_kernel_attrs() {
-  rf_status s = set_smem_attr(reinterpret_cast<const void*>(&k_chol_base), kBlkSmem, &g_chol_attr);
-  if (s != RF_OK) return s;
-  return set_smem_attr(reinterpret_cast<const void*>(&k_trinv_base), 2 * kBlkSmem, &g_trinv_attr);
 }
 
 rf_status centre_system(const double* G, const double* sx, const double* sy, const int64_t* n, int d_in, long long n_y,
@@ -888,20 +883,8 @@ rf_status chol_inv_block(float* A, long long lda, long long sA, float* W, long l
                          float* tmp, long long stmp, int32_t* dev_status, int sms, cudaStream_t s) {
   rf_status st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf), kLeafSmem, &g_leaf_attr);
   if (st != RF_OK) return st;
-  SolveCtx c{s, sms, nullptr, nullptr, dev_status};
+  SolveCtx c{s, sms, dev_status};
   return chol_inv_rec(c, A, lda, sA, W, ldw, sW, n, batch, tmp, stmp);
-}
-
-rf_status chol_inv_batched(float* A, long long lda, long long stride, float* Linv, long long ldi, int n, int batch,
-                           float* tmp, int32_t* dev_status, int sms, cudaStream_t s) {
-  rf_status st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf), kLeafSmem, &g_leaf_attr);
-  if (st != RF_OK) return st;
-  const long long stride_inv = static_cast<long long>(n) * ldi;
-  SolveCtx c{s, sms, nullptr, nullptr, dev_status};
-  if ((st = cuda_check(cudaMemsetAsync(Linv, 0, sizeof(float) * stride_inv * batch, s), "zero L^-1")) != RF_OK)
-    return st;
-  const long long stmp = static_cast<long long>(n) * n / 4;
-  return chol_inv_rec(c, A, lda, stride, Linv, ldi, stride_inv, n, batch, tmp, stmp);
 }
 
 }  // namespace rf
@@ -933,10 +916,9 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
     return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", lay.bytes, workspace_bytes);
   int sms = 0;
   if ((s = current_device(&sms)) != RF_OK) return s;
-  if ((s = solve_kernel_attrs()) != RF_OK) return s;
 
   const int di = static_cast<int>(desc->d_in), dout = static_cast<int>(desc->d_out), P = static_cast<int>(desc->n_maps);
-  SolveCtx c{static_cast<cudaStream_t>(stream), sms, lay.tmp, lay.tmp2, dev_status};
+  SolveCtx c{static_cast<cudaStream_t>(stream), sms, dev_status};
   const int eb = 8 * sms;
   {
     ProfScope pf(c.s, RF_STAGE_SOLVE);
@@ -946,15 +928,13 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
     const long long ctotal = static_cast<long long>(P) * di * dout;
     k_centre_c<<<eb, 256, 0, c.s>>>(st->C, lay.mu_x, lay.mu_y, lay.n, di, dout, ctotal, lay.work);
     if ((s = cuda_check(cudaGetLastError(), "solve set-up launches")) != RF_OK) return s;
-
-    // H = L Lᵀ ; L^-1 ; H^-1 = L^-ᵀ L^-1
-    if ((s = chol_lower(c, lay.L, di, di, lay.Linv)) != RF_OK) return s;
-    if ((s = trinv_lower(c, lay.L, di, di, lay.Linv, di)) != RF_OK) return s;
-    if ((s = sgemm(c, true, false, di, di, di, 1.f, lay.Linv, di, 0, lay.Linv, di, 0, 0.f, lay.Hinv, di, 0, 1)) != RF_OK)
-      return s;
   }
-  // A_p = Cc_pᵀ H^-1  (Cc_p stored [d_in][d_out]); H^-1 is symmetric bit for bit
-  // (both triangles come from the same products in the same order).
+  // H = L Lᵀ ; L^-1 ; H^-1 = L^-ᵀ L^-1  (planes_b is free until the product below)
+  if ((s = spd_inverse(lay.L, di, lay.Linv, lay.Hinv, lay.tmp, lay.planes_b, use_pair(desc->flags, true), dev_status,
+                       sms, c.s)) != RF_OK)
+    return s;
+  // A_p = Cc_pᵀ H^-1  (Cc_p stored [d_in][d_out]); H^-1 is exactly symmetric (its
+  // lower triangle mirrors the upper), so its rows serve as the B operand.
   {
     ProfScope pp(c.s, RF_STAGE_SOLVE_PRODUCT);
     if ((s = split_gemm(c, lay.work, true, lay.Hinv, P, dout, di, di, 1.f, 0.f, A, lay.planes_a, lay.planes_b)) !=
@@ -963,9 +943,9 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
   }
   for (int it = 0; it < refine_iters; ++it) {
     ProfScope pr(c.s, RF_STAGE_SOLVE_REFINE);
-    dim3 g(di / 64, dout / 64, P);
-    k_resid64<<<g, 256, 0, c.s>>>(dout, di, A, lay.H64, st->C, lay.mu_x, lay.mu_y, lay.n, lay.work);
-    if ((s = cuda_check(cudaGetLastError(), "k_resid64 launch")) != RF_OK) return s;
+    s = use_pair(desc->flags, true) ? oz_residual<true>(c, lay, st->C, A, P, di, dout, lay.work)
+                                    : oz_residual<false>(c, lay, st->C, A, P, di, dout, lay.work);
+    if (s != RF_OK) return s;
     if ((s = split_gemm(c, lay.work, false, lay.Hinv, P, dout, di, di, 1.f, 1.f, A, lay.planes_a, lay.planes_b)) !=
         RF_OK)
       return s;

@@ -177,6 +177,29 @@ def test_gpu_calibration_then_solve_recovers_planted_maps():
         assert _rel(A[p], At[p]) <= 0.05
 
 
+def test_solve_refinement_restores_accuracy_when_ill_conditioned():
+    """κ(Gc) ≈ 1e4: the fp32 factorisation alone loses about κ·2^-24; one sweep with the
+    fp64-accurate residual (tensor-core digit products, exact integer chunk sums)
+    brings A back to fp32 accuracy. A residual accurate only to fp32 would not."""
+    d, P, n = 512, 2, 4096
+    rng = np.random.default_rng(21)
+    Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    X = (rng.standard_normal((n, d)) * np.geomspace(1.0, 1e-2, d)) @ Q.T
+    At = rng.standard_normal((P, d, d)) / math.sqrt(d)
+    Y = np.einsum("pij,nj->pni", At, X) + 0.01 * rng.standard_normal((P, n, d))
+    Xb = torch.as_tensor(X, dtype=torch.float32).to(torch.bfloat16)
+    Yb = torch.as_tensor(Y, dtype=torch.float32).to(torch.bfloat16)
+    ref = O.calib_stats(_f64(Xb), _f64(Yb))
+    lam = 1e-9
+    Ar, _, _ = O.ridge_solve(ref, lam)
+    A0, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=0)
+    A1, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=1)
+    e0 = max(_rel(A0[p], Ar[p]) for p in range(P))
+    e1 = max(_rel(A1[p], Ar[p]) for p in range(P))
+    assert e0 > 1e-5, e0              # the case is hard enough to need refinement
+    assert e1 <= 1e-5 and e1 < e0 / 20, (e0, e1)
+
+
 @pytest.mark.slow
 def test_solve_full_width_sampled_rows():
     d, P, n = 4096, 2, 8192
