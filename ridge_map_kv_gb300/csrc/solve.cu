@@ -592,12 +592,14 @@ static rf_status split_gemm(SolveCtx& c, const float* a, bool a_tr, const float*
 // --------------------------------------------------------------------------
 constexpr int kOzDigits = 7;
 constexpr int kOzChunk = 2048;
+constexpr int kOzMaps = 4;  // maps per residual launch (keeps the last wave of units small)
 constexpr int kOzPairs = kOzDigits * (kOzDigits + 1) / 2;
 
-// Digits of each row of an fp32 or fp64 matrix [rows][cols]: planes [kOzDigits][rows][cols]
-// bf16 and the row scale σ (a power of two, 0 for a zero row). One warp per row.
+// Digits of each row of an fp32 or fp64 matrix [rows][cols]: digit d of row r at
+// planes[(d * plane_rows + r) * cols ...] in bf16 (plane_rows >= rows), and the row
+// scale σ (a power of two, 0 for a zero row). One warp per row.
 template <class T>
-__global__ void __launch_bounds__(256) k_oz_digits(const T* __restrict__ X, int rows, int cols,
+__global__ void __launch_bounds__(256) k_oz_digits(const T* __restrict__ X, int rows, int plane_rows, int cols,
                                                    __nv_bfloat16* __restrict__ planes, double* __restrict__ scale) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= rows) return;
@@ -608,7 +610,7 @@ __global__ void __launch_bounds__(256) k_oz_digits(const T* __restrict__ X, int 
   int e = 0;
   if (mx > 0.0) frexp(mx, &e);  // mx = f 2^e, f in [0.5, 1): σ = 2^e >= mx
   if (lane == 0) scale[warp] = mx > 0.0 ? ldexp(1.0, e) : 0.0;
-  const size_t plane = static_cast<size_t>(rows) * cols;
+  const size_t plane = static_cast<size_t>(plane_rows) * cols;
   for (int k = lane; k < cols; k += 32) {
     double v = mx > 0.0 ? ldexp(static_cast<double>(x[k]), -e) : 0.0;  // exact, |v| <= 1
 #pragma unroll
@@ -651,13 +653,13 @@ __device__ __forceinline__ void oz_pair(int pi, int& m, int& s) {
 
 template <bool kPair_>
 struct OzakiProb {
-  CUtensorMap tmA;  // digits of A_p rows: [kOzDigits * d_out][d_in]
-  CUtensorMap tmB;  // digits of H rows:   [kOzDigits * d_in][d_in]
-  const double* sA;  // [d_out] row scales of A_p
+  CUtensorMap tmA;  // digits of the maps' rows: [kOzDigits * maps * d_out][d_in]
+  CUtensorMap tmB;  // digits of H rows:        [kOzDigits * d_in][d_in]
+  const double* sA;  // [maps][d_out] row scales
   const double* sH;  // [d_in]  row scales of H
-  double* R64;       // [d_out][d_in] fp64 residual, initialised to Cc_pᵀ
-  float* R32;        // [d_out][d_in] fp32 result
-  int d_out, d_in, m_tiles, n_tiles, n_chunks;
+  double* R64;       // [maps][d_out][d_in] fp64 residuals, initialised to Cc_pᵀ
+  float* R32;        // [maps][d_out][d_in] fp32 results
+  int maps, plane_maps, d_out, d_in, m_tiles, n_tiles, n_chunks;  // maps in this launch; maps per digit plane
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = false;
@@ -674,8 +676,14 @@ struct OzakiProb {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  __device__ int num_units() const { return m_tiles * n_tiles; }
+  __device__ int num_units() const { return maps * m_tiles * n_tiles; }
   __device__ int num_subtiles(int) const { return kOzPairs * n_chunks; }
+  __device__ void decode(int u, int& p, int& mt, int& nt) const {
+    nt = u % n_tiles;
+    u /= n_tiles;
+    mt = u % m_tiles;
+    p = u / m_tiles;
+  }
   __device__ int num_kb(int, int sb) const {
     const int c = sb % n_chunks;
     return (min(kOzChunk, d_in - c * kOzChunk) + kBK - 1) / kBK;
@@ -684,12 +692,13 @@ struct OzakiProb {
     int a_row, b_row, k0;
   };
   __device__ Coords coords(int u, int sb, uint32_t rank) const {
-    const int nt = u % n_tiles, mt = u / n_tiles;
+    int p, mt, nt;
+    decode(u, p, mt, nt);
     const int pi = sb / n_chunks, c = sb - pi * n_chunks;
     int m, s;
     oz_pair(pi, m, s);
     const int t = m - s;
-    return {(s - 1) * d_out + mt * Cfg::kUnitM + static_cast<int>(rank) * kBM,
+    return {((s - 1) * plane_maps + p) * d_out + mt * Cfg::kUnitM + static_cast<int>(rank) * kBM,
             (t - 1) * d_in + nt * kBN + static_cast<int>(rank) * Cfg::kBRows, c * kOzChunk};
   }
   __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
@@ -718,8 +727,9 @@ struct OzakiProb {
     int m, s;
     oz_pair(pi, m, s);
     if (c != n_chunks - 1 || s != m - 1) return;  // weight m not complete yet
-    const int nt = u % n_tiles, mt = u / n_tiles;
-    const size_t o = static_cast<size_t>(mt) * Cfg::kUnitM + rank * kBM + row;
+    int p, mt, nt;
+    decode(u, p, mt, nt);
+    const size_t o = static_cast<size_t>(p) * d_out + static_cast<size_t>(mt) * Cfg::kUnitM + rank * kBM + row;
     const size_t i0 = static_cast<size_t>(nt) * kBN + col0;
     const double so = ldexp(sA[o], -6 * m);
     double* r = R64 + o * d_in + i0;
@@ -751,9 +761,9 @@ struct SolveLayout {
   __nv_bfloat16* planes_b;  // [3][d_in][d_in] bf16 split of H^-1
   __nv_bfloat16* ozH;       // [kOzDigits][d_in][d_in] digits of H's rows (refinement)
   double* sH;               // [d_in] their scales
-  __nv_bfloat16* ozA;       // [kOzDigits][d_out][d_in] digits of one map's rows
-  double* sA;               // [d_out]
-  double* R64;              // [d_out][d_in] one map's fp64 residual
+  __nv_bfloat16* ozA;       // [kOzDigits][kOzMaps * d_out][d_in] digits of a group of maps' rows
+  double* sA;               // [kOzMaps * d_out]
+  double* R64;              // [kOzMaps][d_out][d_in] their fp64 residuals
   size_t bytes;
 };
 
@@ -775,9 +785,10 @@ static SolveLayout solve_layout(const rf_calib_desc* d, void* ws) {
   l.planes_b = c.take<__nv_bfloat16>(3 * di * di);
   l.ozH = c.take<__nv_bfloat16>(kOzDigits * di * di);
   l.sH = c.take<double>(di);
-  l.ozA = c.take<__nv_bfloat16>(kOzDigits * dout * di);
-  l.sA = c.take<double>(dout);
-  l.R64 = c.take<double>(dout * di);
+  const int64_t om = std::min<int64_t>(P, kOzMaps);
+  l.ozA = c.take<__nv_bfloat16>(kOzDigits * om * dout * di);
+  l.sA = c.take<double>(om * dout);
+  l.R64 = c.take<double>(om * dout * di);
   l.bytes = c.bytes();
   return l;
 }
@@ -789,10 +800,11 @@ static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* 
   using Cfg = GemmCfg<kPair>;
   rf_status st;
   const unsigned hb = static_cast<unsigned>((static_cast<long long>(di) * 32 + 255) / 256);
-  const unsigned ab = static_cast<unsigned>((static_cast<long long>(dout) * 32 + 255) / 256);
-  k_oz_digits<double><<<hb, 256, 0, c.s>>>(lay.H64, di, di, lay.ozH, lay.sH);
+  k_oz_digits<double><<<hb, 256, 0, c.s>>>(lay.H64, di, di, di, lay.ozH, lay.sH);
   OzakiProb<kPair> pr;
-  if ((st = make_tmap_bf16_2d(&pr.tmA, lay.ozA, di, static_cast<uint64_t>(kOzDigits) * dout, di, kBK, kBM)) != RF_OK)
+  const int om = std::min(P, kOzMaps);
+  if ((st = make_tmap_bf16_2d(&pr.tmA, lay.ozA, di, static_cast<uint64_t>(kOzDigits) * om * dout, di, kBK, kBM)) !=
+      RF_OK)
     return st;
   if ((st = make_tmap_bf16_2d(&pr.tmB, lay.ozH, di, static_cast<uint64_t>(kOzDigits) * di, di, kBK, Cfg::kBRows)) !=
       RF_OK)
@@ -807,14 +819,22 @@ static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* 
   pr.n_chunks = (di + kOzChunk - 1) / kOzChunk;
   pr.dev_status = c.dev_status;
   pr.timeout_ns = wait_timeout_ns();
-  for (int p = 0; p < P; ++p) {
-    const size_t off = static_cast<size_t>(p) * dout * di;
-    k_oz_digits<float><<<ab, 256, 0, c.s>>>(A + off, dout, di, lay.ozA, lay.sA);
-    k_oz_init<<<dim3(dout / 32, di / 32), dim3(32, 8), 0, c.s>>>(C + off, lay.mu_x, lay.mu_y + static_cast<size_t>(p) * dout,
-                                                                 lay.n, di, dout, lay.R64);
+  for (int p0 = 0; p0 < P; p0 += om) {
+    const int g = std::min(om, P - p0);
+    const size_t off = static_cast<size_t>(p0) * dout * di;
+    // digits of the group's rows: the planes hold `om` maps per digit; a short last
+    // group leaves the rest unused (its units are not launched)
+    const unsigned gb = static_cast<unsigned>((static_cast<long long>(g) * dout * 32 + 255) / 256);
+    k_oz_digits<float><<<gb, 256, 0, c.s>>>(A + off, g * dout, om * dout, di, lay.ozA, lay.sA);
+    for (int j = 0; j < g; ++j)
+      k_oz_init<<<dim3(dout / 32, di / 32), dim3(32, 8), 0, c.s>>>(
+          C + off + static_cast<size_t>(j) * di * dout, lay.mu_x, lay.mu_y + static_cast<size_t>(p0 + j) * dout, lay.n,
+          di, dout, lay.R64 + static_cast<size_t>(j) * dout * di);
     if ((st = cuda_check(cudaGetLastError(), "residual set-up launches")) != RF_OK) return st;
+    pr.maps = g;
+    pr.plane_maps = om;
     pr.R32 = R32 + off;
-    if ((st = launch_gemm(pr, static_cast<int64_t>(pr.m_tiles) * pr.n_tiles, c.sms, c.s, "residual GEMM launch")) !=
+    if ((st = launch_gemm(pr, static_cast<int64_t>(g) * pr.m_tiles * pr.n_tiles, c.sms, c.s, "residual GEMM launch")) !=
         RF_OK)
       return st;
   }
