@@ -39,6 +39,7 @@ struct GramProb {
   double* C;        // [P][d_in][d_out]
   int d_in, d_out, P, n_rows, n_chunks;
   int g_mt, g_nt, c_nt, g_units;
+  int c_group;  // M-tiles per group of the XᵀY units (their X rows stay in L2 together)
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = true;
@@ -78,13 +79,21 @@ struct GramProb {
       nt = c;
       mt = u - rr * c * (c + 1) / 2;
     } else {
+      // XᵀY units in groups of c_group M-tiles: a group's X rows serve every map
+      // and N-tile (map, then N-tile, then the group's M-tiles fastest) before the
+      // next group starts, so they stay in L2 while the Y strips stream past.
       is_g = false;
       u -= g_units;
-      const int per = g_mt * c_nt;
-      p = u / per;
-      const int r = u - p * per;
-      nt = r / g_mt;
-      mt = r - nt * g_mt;
+      const int full = c_group * c_nt * P;  // units of a whole group
+      const int gi = u / full;
+      const int m0 = gi * c_group;
+      const int gs = min(c_group, g_mt - m0);  // this group's M-tiles
+      const int r0 = u - gi * full;
+      const int per = gs * c_nt;
+      p = r0 / per;
+      const int r = r0 - p * per;
+      nt = r / gs;
+      mt = m0 + (r - nt * gs);
     }
   }
   struct Coords {
@@ -166,13 +175,14 @@ __global__ void __launch_bounds__(256) k_mirror_lower(double* __restrict__ G, in
 
 // Column sums of `n_maps` row-major bf16 matrices [n_rows][ld] (map p at
 // base + p*map_stride): out[p][c] += Σ_t M_p[t][c], and out_sq[p][c] += Σ_t M_p[t][c]²
-// when out_sq is set. One thread per column, 512 rows per block; fp32 over 64 rows
-// (a bf16 square is exact in fp32), then fp64, then one fp64 atomic per block.
+// when out_sq is set. Each thread takes 8 adjacent columns (one 16-byte load per
+// row) over 512 rows of a block; fp32 over 64 rows (a bf16 square is exact in
+// fp32), then fp64, then one fp64 atomic per column and block. n_cols % 8 == 0.
 __global__ void __launch_bounds__(256) k_colsum(const __nv_bfloat16* __restrict__ M, long long ld, long long map_stride,
                                                 int n_rows, int n_cols, double* __restrict__ out,
                                                 double* __restrict__ out_sq, int64_t* __restrict__ n_counter,
                                                 long long add_n) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
   const int r0 = blockIdx.y * 512;
   const int p = blockIdx.z;
   if (n_counter != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
@@ -180,20 +190,36 @@ __global__ void __launch_bounds__(256) k_colsum(const __nv_bfloat16* __restrict_
   if (c >= n_cols) return;
   const __nv_bfloat16* col = M + static_cast<long long>(p) * map_stride + c;
   const int r1 = min(r0 + 512, n_rows);
-  double acc = 0.0, acc_sq = 0.0;
+  double acc[8] = {}, acc_sq[8] = {};
   for (int r = r0; r < r1; r += 64) {
-    float s = 0.f, q = 0.f;
+    float s[8] = {}, q[8] = {};
     const int re = min(r + 64, r1);
     for (int t = r; t < re; ++t) {
-      const float v = __bfloat162float(col[static_cast<long long>(t) * ld]);
-      s += v;
-      q = fmaf(v, v, q);
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(col + static_cast<long long>(t) * ld));
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(h[j]);
+        s[2 * j] += f.x;
+        s[2 * j + 1] += f.y;
+        q[2 * j] = fmaf(f.x, f.x, q[2 * j]);
+        q[2 * j + 1] = fmaf(f.y, f.y, q[2 * j + 1]);
+      }
     }
-    acc += static_cast<double>(s);
-    acc_sq += static_cast<double>(q);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      acc[j] += static_cast<double>(s[j]);
+      acc_sq[j] += static_cast<double>(q[j]);
+    }
   }
-  atomicAdd(out + static_cast<size_t>(p) * n_cols + c, acc);
-  if (out_sq != nullptr) atomicAdd(out_sq + static_cast<size_t>(p) * n_cols + c, acc_sq);
+  double* o = out + static_cast<size_t>(p) * n_cols + c;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) atomicAdd(o + j, acc[j]);
+  if (out_sq != nullptr) {
+    double* oq = out_sq + static_cast<size_t>(p) * n_cols + c;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) atomicAdd(oq + j, acc_sq[j]);
+  }
 }
 
 template <bool kPair>
@@ -223,6 +249,9 @@ rf_status calib_gemm(const rf_calib_desc* desc, const rf_bf16* X, int64_t ld_x, 
   pr.g_nt = static_cast<int>(d_in / kBN);
   pr.c_nt = static_cast<int>(P > 0 ? d_out / kBN : 0);
   pr.g_units = (kBN / Cfg::kUnitM) * pr.g_nt * (pr.g_nt + 1) / 2;  // upper-triangle tiles
+  // about 48 MB of X rows per group (a third of L2)
+  const int64_t panel = static_cast<int64_t>(Cfg::kUnitM) * n_rows * 2;
+  pr.c_group = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(pr.g_mt, (int64_t(48) << 20) / std::max<int64_t>(panel, 1))));
   pr.dev_status = dev_status;
   pr.timeout_ns = wait_timeout_ns();
   ProfScope prof(cs, RF_STAGE_CALIB_GEMM);
@@ -279,11 +308,11 @@ extern "C" rf_status rf_calib_accumulate(const rf_calib_desc* desc, const rf_bf1
 
   {
     ProfScope prof(cs, RF_STAGE_COLSUM);
-    dim3 gx(static_cast<unsigned>((d_in + 255) / 256), static_cast<unsigned>((n_rows + 511) / 512), 1);
+    dim3 gx(static_cast<unsigned>((d_in + 2047) / 2048), static_cast<unsigned>((n_rows + 511) / 512), 1);
     k_colsum<<<gx, 256, 0, cs>>>(reinterpret_cast<const __nv_bfloat16*>(X), ld_x, 0, static_cast<int>(n_rows),
                                  static_cast<int>(d_in), st->sx, nullptr, st->n, n_rows);
     if (P > 0) {
-      dim3 gy(static_cast<unsigned>((d_out + 255) / 256), static_cast<unsigned>((n_rows + 511) / 512),
+      dim3 gy(static_cast<unsigned>((d_out + 2047) / 2048), static_cast<unsigned>((n_rows + 511) / 512),
               static_cast<unsigned>(P));
       k_colsum<<<gy, 256, 0, cs>>>(reinterpret_cast<const __nv_bfloat16*>(Y), ld_y, y_map_stride,
                                    static_cast<int>(n_rows), static_cast<int>(d_out), st->sy, st->syy, nullptr, 0);

@@ -129,12 +129,14 @@ struct XMProb {
     nt = r - mt * 2 * n_half;
   }
   // K-blocks run in order 0, 1, ...; the feature column c walks through one
-  // source layer's KV columns, then the next source layer (row base a_src).
+  // source layer's KV columns, then the next source layer (row base a_src). The
+  // next layer's index is read from the table one whole layer (KV/64 K-blocks)
+  // before it is needed, so the load is never waited on in the copy loop.
   struct Coords {
     const CUtensorMap* ta;
     const CUtensorMap* tb;
     const int32_t* srcs;  // this target layer's k source layers
-    int a_row, b_row, a_src, c, j;
+    int a_row, b_row, a_src, next_src, c, j;
   };
   __device__ Coords coords(int u, int, uint32_t rank) const {
     int l, mt, nt;
@@ -149,12 +151,15 @@ struct XMProb {
     c.j = 0;
     c.c = 0;
     c.a_src = __ldg(c.srcs) * N;
+    c.next_src = k > 1 ? __ldg(c.srcs + 1) : 0;
     return c;
   }
   __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
     if (c.c == KV) {
       c.c = 0;
-      c.a_src = __ldg(c.srcs + ++c.j) * N;
+      ++c.j;
+      c.a_src = c.next_src * N;
+      c.next_src = c.j + 1 < k ? __ldg(c.srcs + c.j + 1) : 0;
     }
     tma2<kPair>(sa, c.ta, bar, c.c, c.a_src + c.a_row);
     tma2<kPair>(sb, c.tb, bar, kb * kBK, c.b_row);
