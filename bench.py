@@ -49,6 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the calibration, solve and cross-model rows")
+    ap.add_argument("--extra", choices=EXTRA_ROWS, default=None,
+                    help="time one row of the extras alone and print it (for short captures)")
     ap.add_argument("--selection-only", action="store_true",
                     help="time only the source-selection row (all-source calibration + greedy selection)")
     ap.add_argument("--select-targets", type=int, default=0,
@@ -273,6 +275,16 @@ def gemm_flags(name):
 # --------------------------------------------------------------------------- #
 # Our arm
 # --------------------------------------------------------------------------- #
+def run_extra_only(args):
+    import json
+
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = measured_peaks()
+    print(json.dumps(run_extras(dev, peaks["bf16_tflops"], gemm_flags(args.gemm), only=args.extra)))
+
+
 def run_selection_only(args):
     import json
 
@@ -509,9 +521,16 @@ def _zero_stats(d_in, d_out, P, dev):
             "n": torch.zeros(1, dtype=torch.int64, device=dev)}
 
 
-def run_extras(dev, peak_tflops, flags=0):
-    """Calibration (27B shape), ridge solve (8B shape, 20 maps) and the cross-model
-    mapper (40 -> 64 layers, N = 32768), each timed with CUDA events."""
+EXTRA_ROWS = ("a5_calibration", "a5_calibration_xmodel", "a6_solve", "a7_xmodel", "next3_map_storage_8b",
+              "next2_key_norm_qwen3", "next4_nonsquare_flash_next", "next1_value_rescale_27b",
+              "next4a_source_selection_xmodel")
+
+
+def run_extras(dev, peak_tflops, flags=0, only=None):
+    """The other rows of the path, each timed with CUDA events at its workload's
+    size: calibration (27B shape, and the cross-model Gram), the ridge solve (8B
+    shape, 20 maps), the cross-model mapper (40 -> 64 layers, N = 32768), the NEXT
+    rows and the source selection. `only` names one row (EXTRA_ROWS) to run alone."""
     import torch
 
     import ridge_map_kv_gb300 as rf
@@ -519,221 +538,231 @@ def run_extras(dev, peak_tflops, flags=0):
     stream = torch.cuda.current_stream(dev)
     out = {}
 
-    # a5: calibration statistics, 27B-shaped: XᵀX and XᵀY_l for 48 maps over 16,384 rows
-    c = synth.DENSE27B
-    d, P, n = c.d, c.P, c.calib_n
-    cal = synth.calib_inputs(d, d, P, n, index=c.index, device=dev)
-    st = _zero_stats(d, d, P, dev)
-    cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
-    cd = rf.rf_calib_desc(d_in=d, d_out=d, n_maps=P, flags=flags)
-    ms, stages = _timed(lambda: rf.rf_calib_accumulate(cd, cal["X"], d, cal["Y"], d, n * d, n, cs), 3, stream)
-    # algorithmic flops: XᵀX is symmetric, so its upper triangle (with the diagonal), plus every XᵀY_l
-    flops = 1.0 * n * d * (d + 1) + 2.0 * n * d * d * P
-    gm = stages.get("calib_gemm", ms)
-    out["a5_calibration"] = {
-        "workload": f"27b-shaped XᵀX + XᵀY, d={d}, {P} maps, {n} rows per call",
-        "ms_per_call": ms, "tflops": flops / (ms / 1e3) / 1e12, "gemm_ms": gm,
-        "gemm_frac_of_bf16_peak": flops / (gm / 1e3) / 1e12 / peak_tflops, "stages_ms": stages}
-    del cal, st, cs
-    torch.cuda.empty_cache()
+    if only in (None, "a5_calibration"):
+        # a5: calibration statistics, 27B-shaped: XᵀX and XᵀY_l for 48 maps over 16,384 rows
+        c = synth.DENSE27B
+        d, P, n = c.d, c.P, c.calib_n
+        cal = synth.calib_inputs(d, d, P, n, index=c.index, device=dev)
+        st = _zero_stats(d, d, P, dev)
+        cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
+        cd = rf.rf_calib_desc(d_in=d, d_out=d, n_maps=P, flags=flags)
+        ms, stages = _timed(lambda: rf.rf_calib_accumulate(cd, cal["X"], d, cal["Y"], d, n * d, n, cs), 3, stream)
+        # algorithmic flops: XᵀX is symmetric, so its upper triangle (with the diagonal), plus every XᵀY_l
+        flops = 1.0 * n * d * (d + 1) + 2.0 * n * d * d * P
+        gm = stages.get("calib_gemm", ms)
+        out["a5_calibration"] = {
+            "workload": f"27b-shaped XᵀX + XᵀY, d={d}, {P} maps, {n} rows per call",
+            "ms_per_call": ms, "tflops": flops / (ms / 1e3) / 1e12, "gemm_ms": gm,
+            "gemm_frac_of_bf16_peak": flops / (gm / 1e3) / 1e12 / peak_tflops, "stages_ms": stages}
+        del cal, st, cs
+        torch.cuda.empty_cache()
 
-    # a5, cross-model: the 8192-feature Gram over 131,072 rows and XᵀY for one target layer (1024 columns)
-    x = synth.XMODEL
-    d_in, d_out, n = x.d_in, x.KV, x.calib_n
-    cal = synth.calib_inputs(d_in, d_out, 1, n, index=x.index, device=dev)
-    st = _zero_stats(d_in, d_out, 1, dev)
-    cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
-    cd = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=1, flags=flags)
-    ms, stages = _timed(lambda: rf.rf_calib_accumulate(cd, cal["X"], d_in, cal["Y"], d_out, n * d_out, n, cs), 3,
-                        stream)
-    flops = 1.0 * n * d_in * (d_in + 1) + 2.0 * n * d_in * d_out
-    gm = stages.get("calib_gemm", ms)
-    out["a5_calibration_xmodel"] = {
-        "workload": f"cross-model calibration: XᵀX over d_in={d_in} features and XᵀY for {d_out} target columns, "
-                    f"{n} rows per call",
-        "ms_per_call": ms, "tflops": flops / (ms / 1e3) / 1e12, "gemm_ms": gm,
-        "gemm_frac_of_bf16_peak": flops / (gm / 1e3) / 1e12 / peak_tflops, "stages_ms": stages}
-    del cal, st, cs
-    torch.cuda.empty_cache()
+    if only in (None, "a5_calibration_xmodel"):
+        # a5, cross-model: the 8192-feature Gram over 131,072 rows and XᵀY for one target layer (1024 columns)
+        x = synth.XMODEL
+        d_in, d_out, n = x.d_in, x.KV, x.calib_n
+        cal = synth.calib_inputs(d_in, d_out, 1, n, index=x.index, device=dev)
+        st = _zero_stats(d_in, d_out, 1, dev)
+        cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
+        cd = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=1, flags=flags)
+        ms, stages = _timed(lambda: rf.rf_calib_accumulate(cd, cal["X"], d_in, cal["Y"], d_out, n * d_out, n, cs), 3,
+                            stream)
+        flops = 1.0 * n * d_in * (d_in + 1) + 2.0 * n * d_in * d_out
+        gm = stages.get("calib_gemm", ms)
+        out["a5_calibration_xmodel"] = {
+            "workload": f"cross-model calibration: XᵀX over d_in={d_in} features and XᵀY for {d_out} target columns, "
+                        f"{n} rows per call",
+            "ms_per_call": ms, "tflops": flops / (ms / 1e3) / 1e12, "gemm_ms": gm,
+            "gemm_frac_of_bf16_peak": flops / (gm / 1e3) / 1e12 / peak_tflops, "stages_ms": stages}
+        del cal, st, cs
+        torch.cuda.empty_cache()
 
-    # a6: ridge solve, 8B-shaped (d = 4096, 20 maps) from 8192 calibration rows
-    c = synth.LLAMA8B
-    d, P, n = c.d, c.P, c.calib_n
-    cal = synth.calib_inputs(d, d, P, n, index=c.index, device=dev)
-    st = _zero_stats(d, d, P, dev)
-    cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
-    cd = rf.rf_calib_desc(d_in=d, d_out=d, n_maps=P, flags=flags)
-    rf.rf_calib_accumulate(cd, cal["X"], d, cal["Y"], d, n * d, n, cs)
-    del cal
-    A = torch.empty((P, d, d), dtype=torch.float32, device=dev)
-    b = torch.empty((P, d), dtype=torch.float32, device=dev)
-    Ab = torch.empty((P, d, d), dtype=torch.bfloat16, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    wsb = rf.rf_solve_workspace_bytes(cd)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    sol = {}
-    for refine in (0, 1):
-        ms, stages = _timed(lambda: rf.rf_solve(cd, cs, c.lam, rf.RF_ALPHA_TRACE, refine, A, b, Ab, None, status,
-                                               ws, wsb), 1, stream)
-        sol[f"refine_{refine}_ms"] = ms
-    assert int(status.item()) == 0
-    out["a6_solve"] = {"workload": f"8b-shaped ridge solve, d={d}, {P} maps, lambda={c.lam}", **sol}
-    del st, cs, A, b, Ab, ws
-    torch.cuda.empty_cache()
-
-    # a7: cross-model mapper, 40 -> 64 layers, k = 8, 8 x 128 heads, N = 32768
-    x = synth.XMODEL
-    inp = synth.xmodel_inputs(x, device=dev)
-    xd = rf.rf_xmodel_desc(L_src=x.L_src, L_tgt=x.L_tgt, k=x.k, n_kv_heads=x.H, head_dim=x.hd, N=x.N,
-                           theta_src=x.theta_src, theta_tgt=x.theta_tgt, pos_offset=0, flags=flags)
-    kt = torch.empty((x.L_tgt, x.N, x.KV), dtype=torch.bfloat16, device=dev)
-    vt = torch.empty_like(kt)
-    wsb = rf.rf_xmodel_workspace_bytes(xd)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    ms, stages = _timed(lambda: rf.rf_xmodel_map(xd, inp["src"], inp["k_src"], inp["v_src"], inp["Wk"], inp["bk"],
-                                                 inp["Wv"], inp["bv"], kt, vt, None, ws, wsb), 3, stream)
-    flops = 2.0 * x.N * x.d_in * 2 * x.KV * x.L_tgt
-    gm = stages.get("xmodel_gemm", ms)
-    out["a7_xmodel"] = {"workload": x.name, "ms_per_call": ms, "tflops": flops / (ms / 1e3) / 1e12,
-                        "gemm_ms": gm, "gemm_frac_of_bf16_peak": flops / (gm / 1e3) / 1e12 / peak_tflops,
-                        "stages_ms": stages,
-                        "pages_context": "277.6 ms for a 40->64 layer pair at 32K on unstated hardware (context only)"}
-    del inp, kt, vt, ws
-    torch.cuda.empty_cache()
-
-    # Map storage at the bench workload (8B shape): the resident fill against the
-    # layer-by-layer fill with maps on the device or the host, bf16 or int8
-    c = synth.LLAMA8B
-    inp = synth.fill_inputs(c, device=dev)
-    fd = rf.rf_fill_desc(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
-                         rms_eps=c.rms_eps, pos_offset=0, flags=flags)
-    Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
-    rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
-    del inp["Wk"], inp["Wv"]
-    q = torch.empty((c.P, c.d, c.d), dtype=torch.int8, device=dev)
-    qs = torch.empty((c.P, c.d), dtype=torch.float32, device=dev)
-    rf.rf_quantize_maps_int8(fd, inp["A"], q, qs)
-    A_host = inp["A"].cpu().pin_memory()
-    q_host = q.cpu().pin_memory()
-    kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
-    vc = torch.zeros_like(kc)
-    nf = torch.zeros(1, dtype=torch.int32, device=dev)
-    row = {"workload": workload_label(c), "map_bytes_bf16": c.P * c.d * c.d * 2, "map_bytes_int8": c.P * c.d * c.d}
-    wsb = rf.rf_fill_workspace_bytes(fd)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    row["resident_ms"], _ = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], Wkv, kc,
-                                                         vc, c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
-    row["resident_workspace_bytes"] = wsb
-    del ws
-    variants = {"layered_device_bf16": rf.map_source(rf.RF_MAPS_BF16, inp["A"]),
-                "layered_host_bf16": rf.map_source(rf.RF_MAPS_BF16, A_host, on_host=True),
-                "layered_device_int8": rf.map_source(rf.RF_MAPS_INT8, q, row_scale=qs),
-                "layered_host_int8": rf.map_source(rf.RF_MAPS_INT8, q_host, on_host=True, row_scale=qs)}
-    for key, ms_ in variants.items():
-        wsb = rf.rf_fill_layered_workspace_bytes(fd, ms_)
+    if only in (None, "a6_solve"):
+        # a6: ridge solve, 8B-shaped (d = 4096, 20 maps) from 8192 calibration rows
+        c = synth.LLAMA8B
+        d, P, n = c.d, c.P, c.calib_n
+        cal = synth.calib_inputs(d, d, P, n, index=c.index, device=dev)
+        st = _zero_stats(d, d, P, dev)
+        cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
+        cd = rf.rf_calib_desc(d_in=d, d_out=d, n_maps=P, flags=flags)
+        rf.rf_calib_accumulate(cd, cal["X"], d, cal["Y"], d, n * d, n, cs)
+        del cal
+        A = torch.empty((P, d, d), dtype=torch.float32, device=dev)
+        b = torch.empty((P, d), dtype=torch.float32, device=dev)
+        Ab = torch.empty((P, d, d), dtype=torch.bfloat16, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        wsb = rf.rf_solve_workspace_bytes(cd)
         ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-        row[f"{key}_ms"], st = _timed(lambda: rf.rf_fill_kv_layered(fd, inp["x_S"], c.d, inp["mask"], ms_, inp["b"],
-                                                                    Wkv, kc, vc, c.N * c.KV, c.KV, nf, None, ws,
-                                                                    wsb), 3, stream)
-        row[f"{key}_workspace_bytes"] = wsb
-        if "int8_expand" in st:
-            row[f"{key}_expand_ms"] = st["int8_expand"]
-        del ws
-    out["next3_map_storage_8b"] = row
-    del inp, kc, vc, Wkv, q, qs, A_host, q_host
-    torch.cuda.empty_cache()
+        sol = {}
+        for refine in (0, 1):
+            ms, stages = _timed(lambda: rf.rf_solve(cd, cs, c.lam, rf.RF_ALPHA_TRACE, refine, A, b, Ab, None, status,
+                                                   ws, wsb), 1, stream)
+            sol[f"refine_{refine}_ms"] = ms
+        assert int(status.item()) == 0
+        out["a6_solve"] = {"workload": f"8b-shaped ridge solve, d={d}, {P} maps, lambda={c.lam}", **sol}
+        del st, cs, A, b, Ab, ws
+        torch.cuda.empty_cache()
 
-    # Key normalisation: the Qwen3-8B-shaped fill without and with per-head K norm
-    c = synth.QWEN3_8B
-    inp = synth.fill_inputs(c, device=dev)
-    kg = synth.key_norm_gain(c, device=dev)
-    fd = rf.rf_fill_desc(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
-                         rms_eps=c.rms_eps, pos_offset=0, flags=flags)
-    Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
-    rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
-    del inp["Wk"], inp["Wv"]
-    kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
-    vc = torch.zeros_like(kc)
-    wsb = rf.rf_fill_workspace_bytes(fd)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    nf = torch.zeros(1, dtype=torch.int32, device=dev)
-    row = {"workload": f"qwen3-8b-shaped fill (d={c.d}, {c.P} upper layers, N={c.N}, T={c.T}, no exact rows)"}
-    for key, gain_ptr in (("plain", None), ("key_norm", kg.data_ptr())):
-        fd.k_norm_gain = gain_ptr
-        ms, st = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
+    if only in (None, "a7_xmodel"):
+        # a7: cross-model mapper, 40 -> 64 layers, k = 8, 8 x 128 heads, N = 32768
+        x = synth.XMODEL
+        inp = synth.xmodel_inputs(x, device=dev)
+        xd = rf.rf_xmodel_desc(L_src=x.L_src, L_tgt=x.L_tgt, k=x.k, n_kv_heads=x.H, head_dim=x.hd, N=x.N,
+                               theta_src=x.theta_src, theta_tgt=x.theta_tgt, pos_offset=0, flags=flags)
+        kt = torch.empty((x.L_tgt, x.N, x.KV), dtype=torch.bfloat16, device=dev)
+        vt = torch.empty_like(kt)
+        wsb = rf.rf_xmodel_workspace_bytes(xd)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        ms, stages = _timed(lambda: rf.rf_xmodel_map(xd, inp["src"], inp["k_src"], inp["v_src"], inp["Wk"], inp["bk"],
+                                                     inp["Wv"], inp["bv"], kt, vt, None, ws, wsb), 3, stream)
+        flops = 2.0 * x.N * x.d_in * 2 * x.KV * x.L_tgt
+        gm = stages.get("xmodel_gemm", ms)
+        out["a7_xmodel"] = {"workload": x.name, "ms_per_call": ms, "tflops": flops / (ms / 1e3) / 1e12,
+                            "gemm_ms": gm, "gemm_frac_of_bf16_peak": flops / (gm / 1e3) / 1e12 / peak_tflops,
+                            "stages_ms": stages,
+                            "pages_context": "277.6 ms for a 40->64 layer pair at 32K on unstated hardware (context only)"}
+        del inp, kt, vt, ws
+        torch.cuda.empty_cache()
+
+    if only in (None, "next3_map_storage_8b"):
+        # Map storage at the bench workload (8B shape): the resident fill against the
+        # layer-by-layer fill with maps on the device or the host, bf16 or int8
+        c = synth.LLAMA8B
+        inp = synth.fill_inputs(c, device=dev)
+        fd = rf.rf_fill_desc(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
+                             rms_eps=c.rms_eps, pos_offset=0, flags=flags)
+        Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
+        rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
+        del inp["Wk"], inp["Wv"]
+        q = torch.empty((c.P, c.d, c.d), dtype=torch.int8, device=dev)
+        qs = torch.empty((c.P, c.d), dtype=torch.float32, device=dev)
+        rf.rf_quantize_maps_int8(fd, inp["A"], q, qs)
+        A_host = inp["A"].cpu().pin_memory()
+        q_host = q.cpu().pin_memory()
+        kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
+        vc = torch.zeros_like(kc)
+        nf = torch.zeros(1, dtype=torch.int32, device=dev)
+        row = {"workload": workload_label(c), "map_bytes_bf16": c.P * c.d * c.d * 2, "map_bytes_int8": c.P * c.d * c.d}
+        wsb = rf.rf_fill_workspace_bytes(fd)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        row["resident_ms"], _ = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], Wkv, kc,
+                                                             vc, c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
+        row["resident_workspace_bytes"] = wsb
+        del ws
+        variants = {"layered_device_bf16": rf.map_source(rf.RF_MAPS_BF16, inp["A"]),
+                    "layered_host_bf16": rf.map_source(rf.RF_MAPS_BF16, A_host, on_host=True),
+                    "layered_device_int8": rf.map_source(rf.RF_MAPS_INT8, q, row_scale=qs),
+                    "layered_host_int8": rf.map_source(rf.RF_MAPS_INT8, q_host, on_host=True, row_scale=qs)}
+        for key, ms_ in variants.items():
+            wsb = rf.rf_fill_layered_workspace_bytes(fd, ms_)
+            ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+            row[f"{key}_ms"], st = _timed(lambda: rf.rf_fill_kv_layered(fd, inp["x_S"], c.d, inp["mask"], ms_, inp["b"],
+                                                                        Wkv, kc, vc, c.N * c.KV, c.KV, nf, None, ws,
+                                                                        wsb), 3, stream)
+            row[f"{key}_workspace_bytes"] = wsb
+            if "int8_expand" in st:
+                row[f"{key}_expand_ms"] = st["int8_expand"]
+            del ws
+        out["next3_map_storage_8b"] = row
+        del inp, kc, vc, Wkv, q, qs, A_host, q_host
+        torch.cuda.empty_cache()
+
+    if only in (None, "next2_key_norm_qwen3"):
+        # Key normalisation: the Qwen3-8B-shaped fill without and with per-head K norm
+        c = synth.QWEN3_8B
+        inp = synth.fill_inputs(c, device=dev)
+        kg = synth.key_norm_gain(c, device=dev)
+        fd = rf.rf_fill_desc(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
+                             rms_eps=c.rms_eps, pos_offset=0, flags=flags)
+        Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
+        rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
+        del inp["Wk"], inp["Wv"]
+        kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
+        vc = torch.zeros_like(kc)
+        wsb = rf.rf_fill_workspace_bytes(fd)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        nf = torch.zeros(1, dtype=torch.int32, device=dev)
+        row = {"workload": f"qwen3-8b-shaped fill (d={c.d}, {c.P} upper layers, N={c.N}, T={c.T}, no exact rows)"}
+        for key, gain_ptr in (("plain", None), ("key_norm", kg.data_ptr())):
+            fd.k_norm_gain = gain_ptr
+            ms, st = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
+                                                  c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
+            n_fill = int(nf.item())
+            f_flops = 2.0 * n_fill * c.P * (c.d * c.d + c.d * 2 * c.KV)
+            row[f"{key}_ms"] = ms
+            row[f"{key}_tflops"] = f_flops / (ms / 1e3) / 1e12
+            row[f"{key}_kv_gemm_ms"] = st.get("kv_gemm")
+        out["next2_key_norm_qwen3"] = row
+        del inp, kc, vc, ws, Wkv
+        torch.cuda.empty_cache()
+
+    if only in (None, "next4_nonsquare_flash_next"):
+        # Non-square maps: the Flash-Next-shaped fill (10,240 -> 2,560, 24 upper layers)
+        c = synth.FLASH_NEXT
+        inp = synth.fill_inputs(c, device=dev)
+        fd = rf.rf_fill_desc(d=c.d, d_in=c.d_in, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd,
+                             rope_theta=c.rope_theta, rms_eps=c.rms_eps, pos_offset=0, flags=flags)
+        Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
+        rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
+        kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
+        vc = torch.zeros_like(kc)
+        wsb = rf.rf_fill_workspace_bytes(fd)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        nf = torch.zeros(1, dtype=torch.int32, device=dev)
+        ms, st = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d_in, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
                                               c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
         n_fill = int(nf.item())
+        f_flops = 2.0 * n_fill * c.P * (c.d * c.d_in + c.d * 2 * c.KV)
+        mg = st.get("map_gemm")
+        out["next4_nonsquare_flash_next"] = {
+            "workload": c.name + f", n_fill={n_fill}", "fill_ms": ms, "fill_tflops": f_flops / (ms / 1e3) / 1e12,
+            "fill_frac_of_bf16_peak": f_flops / (ms / 1e3) / 1e12 / peak_tflops,
+            "map_gemm_ms": mg, "map_gemm_tflops": 2.0 * n_fill * c.P * c.d * c.d_in / (mg / 1e3) / 1e12 if mg else None,
+            "fill_row_layers_per_s": n_fill * c.P / (ms / 1e3), "stages_ms": st}
+        del inp, kc, vc, ws, Wkv
+        torch.cuda.empty_cache()
+
+    if only in (None, "next1_value_rescale_27b"):
+        # Value rescale (the 27B deployment, c = 512), then the 27B fill with the scale
+        c = synth.DENSE27B
+        n_tail = 512
+        inp = synth.fill_inputs(c, device=dev)
+        x_exact = synth.rescale_inputs(c, inp["x_S"], n_tail, device=dev)
+        fd = rf.rf_fill_desc(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
+                             rms_eps=c.rms_eps, pos_offset=0, flags=flags)
+        Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
+        rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
+        del inp["Wk"], inp["Wv"]
+        vs = torch.empty((c.P, c.H), dtype=torch.float32, device=dev)
+        wsb = rf.rf_value_scale_workspace_bytes(fd, n_tail)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        ms_scale, st_scale = _timed(lambda: rf.rf_value_scale(fd, n_tail, inp["x_S"], c.d, x_exact, c.d, inp["A"], inp["b"],
+                                                              Wkv, vs, None, ws, wsb), 3, stream)
+        del ws
+        fd.v_scale = vs.data_ptr()
+        kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
+        vc = torch.zeros_like(kc)
+        wsb = rf.rf_fill_workspace_bytes(fd)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        nf = torch.zeros(1, dtype=torch.int32, device=dev)
+        ms_fill, st_fill = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
+                                                        c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
+        n_fill = int(nf.item())
         f_flops = 2.0 * n_fill * c.P * (c.d * c.d + c.d * 2 * c.KV)
-        row[f"{key}_ms"] = ms
-        row[f"{key}_tflops"] = f_flops / (ms / 1e3) / 1e12
-        row[f"{key}_kv_gemm_ms"] = st.get("kv_gemm")
-    out["next2_key_norm_qwen3"] = row
-    del inp, kc, vc, ws, Wkv
-    torch.cuda.empty_cache()
+        s_flops = 2.0 * n_tail * c.P * (c.d * c.d + 2 * c.d * c.KV)
+        out["next1_value_rescale_27b"] = {
+            "workload": f"27b-shaped deployment: value rescale over c={n_tail} tail rows, then the fill with the scale "
+                        f"(d={c.d}, {c.P} upper layers, n_fill={n_fill})",
+            "rescale_ms": ms_scale, "rescale_tflops": s_flops / (ms_scale / 1e3) / 1e12, "rescale_stages_ms": st_scale,
+            "fill_ms": ms_fill, "fill_tflops": f_flops / (ms_fill / 1e3) / 1e12,
+            "fill_frac_of_bf16_peak": f_flops / (ms_fill / 1e3) / 1e12 / peak_tflops,
+            "fill_row_layers_per_s": n_fill * c.P / (ms_fill / 1e3), "fill_stages_ms": st_fill}
+        del inp, kc, vc, ws, Wkv, vs, x_exact
+        torch.cuda.empty_cache()
 
-    # Non-square maps: the Flash-Next-shaped fill (10,240 -> 2,560, 24 upper layers)
-    c = synth.FLASH_NEXT
-    inp = synth.fill_inputs(c, device=dev)
-    fd = rf.rf_fill_desc(d=c.d, d_in=c.d_in, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd,
-                         rope_theta=c.rope_theta, rms_eps=c.rms_eps, pos_offset=0, flags=flags)
-    Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
-    rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
-    kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
-    vc = torch.zeros_like(kc)
-    wsb = rf.rf_fill_workspace_bytes(fd)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    nf = torch.zeros(1, dtype=torch.int32, device=dev)
-    ms, st = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d_in, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
-                                          c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
-    n_fill = int(nf.item())
-    f_flops = 2.0 * n_fill * c.P * (c.d * c.d_in + c.d * 2 * c.KV)
-    mg = st.get("map_gemm")
-    out["next4_nonsquare_flash_next"] = {
-        "workload": c.name + f", n_fill={n_fill}", "fill_ms": ms, "fill_tflops": f_flops / (ms / 1e3) / 1e12,
-        "fill_frac_of_bf16_peak": f_flops / (ms / 1e3) / 1e12 / peak_tflops,
-        "map_gemm_ms": mg, "map_gemm_tflops": 2.0 * n_fill * c.P * c.d * c.d_in / (mg / 1e3) / 1e12 if mg else None,
-        "fill_row_layers_per_s": n_fill * c.P / (ms / 1e3), "stages_ms": st}
-    del inp, kc, vc, ws, Wkv
-    torch.cuda.empty_cache()
+    if only in (None, "next4a_source_selection_xmodel"):
+        out["next4a_source_selection_xmodel"] = run_selection(dev, peak_tflops, flags)
 
-    # Value rescale (the 27B deployment, c = 512), then the 27B fill with the scale
-    c = synth.DENSE27B
-    n_tail = 512
-    inp = synth.fill_inputs(c, device=dev)
-    x_exact = synth.rescale_inputs(c, inp["x_S"], n_tail, device=dev)
-    fd = rf.rf_fill_desc(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
-                         rms_eps=c.rms_eps, pos_offset=0, flags=flags)
-    Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
-    rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
-    del inp["Wk"], inp["Wv"]
-    vs = torch.empty((c.P, c.H), dtype=torch.float32, device=dev)
-    wsb = rf.rf_value_scale_workspace_bytes(fd, n_tail)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    ms_scale, st_scale = _timed(lambda: rf.rf_value_scale(fd, n_tail, inp["x_S"], c.d, x_exact, c.d, inp["A"], inp["b"],
-                                                          Wkv, vs, None, ws, wsb), 3, stream)
-    del ws
-    fd.v_scale = vs.data_ptr()
-    kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
-    vc = torch.zeros_like(kc)
-    wsb = rf.rf_fill_workspace_bytes(fd)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    nf = torch.zeros(1, dtype=torch.int32, device=dev)
-    ms_fill, st_fill = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
-                                                    c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
-    n_fill = int(nf.item())
-    f_flops = 2.0 * n_fill * c.P * (c.d * c.d + c.d * 2 * c.KV)
-    s_flops = 2.0 * n_tail * c.P * (c.d * c.d + 2 * c.d * c.KV)
-    out["next1_value_rescale_27b"] = {
-        "workload": f"27b-shaped deployment: value rescale over c={n_tail} tail rows, then the fill with the scale "
-                    f"(d={c.d}, {c.P} upper layers, n_fill={n_fill})",
-        "rescale_ms": ms_scale, "rescale_tflops": s_flops / (ms_scale / 1e3) / 1e12, "rescale_stages_ms": st_scale,
-        "fill_ms": ms_fill, "fill_tflops": f_flops / (ms_fill / 1e3) / 1e12,
-        "fill_frac_of_bf16_peak": f_flops / (ms_fill / 1e3) / 1e12 / peak_tflops,
-        "fill_row_layers_per_s": n_fill * c.P / (ms_fill / 1e3), "fill_stages_ms": st_fill}
-    del inp, kc, vc, ws, Wkv, vs, x_exact
-    torch.cuda.empty_cache()
-
-    out["next4a_source_selection_xmodel"] = run_selection(dev, peak_tflops, flags)
     return out
 
 
@@ -864,6 +893,8 @@ def main(argv=None):
         run_reference(args)
     elif args.selection_only:
         run_selection_only(args)
+    elif args.extra:
+        run_extra_only(args)
     else:
         run_ours(args)
 

@@ -40,6 +40,7 @@ struct GramProb {
   int d_in, d_out, P, n_rows, n_chunks;
   int g_mt, g_nt, c_nt, g_units;
   int c_group;  // M-tiles per group of the XᵀY units (their X rows stay in L2 together)
+  int red_flush;  // add into G and C with fp64 reductions (no read) instead of read-modify-write
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = true;
@@ -147,6 +148,11 @@ struct GramProb {
     const size_t i = static_cast<size_t>(mt) * Cfg::kUnitM + rank * kBM + row;
     double* o = (is_g ? G + i * d_in : C + (static_cast<size_t>(p) * d_in + i) * d_out) + static_cast<size_t>(nt) * kBN +
                 col0;
+    if (red_flush) {
+#pragma unroll
+      for (int q = 0; q < kCols; ++q) atomicAdd(o + q, static_cast<double>(es.rs[q]));
+      return;
+    }
     double2* o2 = reinterpret_cast<double2*>(o);
 #pragma unroll
     for (int q = 0; q < kCols / 2; ++q) {
@@ -222,6 +228,15 @@ __global__ void __launch_bounds__(256) k_colsum(const __nv_bfloat16* __restrict_
   }
 }
 
+// Rows per GEMM launch. Every unit of a launch streams all of its rows, and over
+// long launches the pairs drift apart, so that rows they share leave L2 between
+// readers (the 8,192-feature Gram over 131,072 rows read 58 GB from DRAM for
+// 2.4 GB of operands). Launching slab by slab restarts every pair on the same
+// rows. The launches run in stream order and a tile is flushed once per launch,
+// so the fp64 totals are written by one unit at a time; calls of several slabs
+// flush with fp64 reductions, which spare the epilogue the read of the totals.
+constexpr int64_t kCalibSlabRows = 16 * kCalibChunk;
+
 template <bool kPair>
 rf_status calib_gemm(const rf_calib_desc* desc, const rf_bf16* X, int64_t ld_x, const rf_bf16* Y, int64_t ld_y,
                      int64_t y_map_stride, int64_t n_rows, const rf_calib_stats* st, int32_t* dev_status, int sms,
@@ -229,33 +244,41 @@ rf_status calib_gemm(const rf_calib_desc* desc, const rf_bf16* X, int64_t ld_x, 
   using Cfg = GemmCfg<kPair>;
   const int64_t d_in = desc->d_in, d_out = desc->d_out, P = desc->n_maps;
   rf_status s;
-  GramProb<kPair> pr;
-  if ((s = make_tmap_bf16_2d(&pr.tmX, X, d_in, n_rows, ld_x, 64, kBK)) != RF_OK) return s;
-  if (P > 0) {
-    if ((s = make_tmap_bf16_3d(&pr.tmY, Y, d_out, n_rows, P, ld_y, P > 1 ? y_map_stride : ld_y * n_rows, 64, kBK)) !=
-        RF_OK)
-      return s;
-  } else {
-    pr.tmY = pr.tmX;
-  }
-  pr.G = st->G;
-  pr.C = st->C;
-  pr.d_in = static_cast<int>(d_in);
-  pr.d_out = static_cast<int>(P > 0 ? d_out : 0);
-  pr.P = static_cast<int>(P);
-  pr.n_rows = static_cast<int>(n_rows);
-  pr.n_chunks = static_cast<int>((n_rows + kCalibChunk - 1) / kCalibChunk);
-  pr.g_mt = static_cast<int>(d_in / Cfg::kUnitM);
-  pr.g_nt = static_cast<int>(d_in / kBN);
-  pr.c_nt = static_cast<int>(P > 0 ? d_out / kBN : 0);
-  pr.g_units = (kBN / Cfg::kUnitM) * pr.g_nt * (pr.g_nt + 1) / 2;  // upper-triangle tiles
-  // about 48 MB of X rows per group (a third of L2)
-  const int64_t panel = static_cast<int64_t>(Cfg::kUnitM) * n_rows * 2;
-  pr.c_group = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(pr.g_mt, (int64_t(48) << 20) / std::max<int64_t>(panel, 1))));
-  pr.dev_status = dev_status;
-  pr.timeout_ns = wait_timeout_ns();
   ProfScope prof(cs, RF_STAGE_CALIB_GEMM);
-  if ((s = launch_gemm(pr, pr.g_units + P * pr.g_mt * pr.c_nt, sms, cs, "calibration GEMM launch")) != RF_OK) return s;
+  for (int64_t r0 = 0; r0 < n_rows; r0 += kCalibSlabRows) {
+    const int64_t rows = std::min(kCalibSlabRows, n_rows - r0);
+    GramProb<kPair> pr;
+    const __nv_bfloat16* Xs = reinterpret_cast<const __nv_bfloat16*>(X) + r0 * ld_x;
+    if ((s = make_tmap_bf16_2d(&pr.tmX, Xs, d_in, rows, ld_x, 64, kBK)) != RF_OK) return s;
+    if (P > 0) {
+      const __nv_bfloat16* Ys = reinterpret_cast<const __nv_bfloat16*>(Y) + r0 * ld_y;
+      if ((s = make_tmap_bf16_3d(&pr.tmY, Ys, d_out, rows, P, ld_y, P > 1 ? y_map_stride : ld_y * rows, 64, kBK)) !=
+          RF_OK)
+        return s;
+    } else {
+      pr.tmY = pr.tmX;
+    }
+    pr.G = st->G;
+    pr.C = st->C;
+    pr.d_in = static_cast<int>(d_in);
+    pr.d_out = static_cast<int>(P > 0 ? d_out : 0);
+    pr.P = static_cast<int>(P);
+    pr.n_rows = static_cast<int>(rows);
+    pr.n_chunks = static_cast<int>((rows + kCalibChunk - 1) / kCalibChunk);
+    pr.g_mt = static_cast<int>(d_in / Cfg::kUnitM);
+    pr.g_nt = static_cast<int>(d_in / kBN);
+    pr.c_nt = static_cast<int>(P > 0 ? d_out / kBN : 0);
+    pr.g_units = (kBN / Cfg::kUnitM) * pr.g_nt * (pr.g_nt + 1) / 2;  // upper-triangle tiles
+    // about 48 MB of X rows per group (a third of L2)
+    const int64_t panel = static_cast<int64_t>(Cfg::kUnitM) * rows * 2;
+    pr.c_group = static_cast<int>(
+        std::max<int64_t>(1, std::min<int64_t>(pr.g_mt, (int64_t(48) << 20) / std::max<int64_t>(panel, 1))));
+    pr.red_flush = n_rows > kCalibSlabRows ? 1 : 0;
+    pr.dev_status = dev_status;
+    pr.timeout_ns = wait_timeout_ns();
+    if ((s = launch_gemm(pr, pr.g_units + P * pr.g_mt * pr.c_nt, sms, cs, "calibration GEMM launch")) != RF_OK)
+      return s;
+  }
   // The GEMM accumulates G's tiles on and above the diagonal; the lower triangle
   // becomes their mirror (the accumulated upper triangle is the whole sum).
   k_mirror_lower<<<dim3(static_cast<unsigned>(d_in / 32), static_cast<unsigned>(d_in / 32)), dim3(32, 8), 0, cs>>>(
