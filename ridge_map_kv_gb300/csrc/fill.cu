@@ -498,27 +498,33 @@ extern "C" rf_status rf_fill_kv_layered(const rf_fill_desc* desc, const rf_bf16*
   int sms = 0;
   if ((st = current_device(&sms)) != RF_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  bool work = false;
-  if ((st = fill_prologue(desc, x_S, ld_x, exact_mask, n_fill_out, lay, sms, s, &work)) != RF_OK || !work) return st;
-
-  const bool pair = use_pair(desc->flags, true);
-  const bool staged = maps_staged(maps);
-  const int64_t M_pad = round_up(n_prefix, kFillRowAlign);
-  const size_t map_elems = static_cast<size_t>(d) * static_cast<size_t>(d_in);
-  const size_t elem = int8 ? 1 : 2;
-  const int64_t H = desc->n_kv_heads;
+  const bool staged = maps_staged(maps) && n_prefix > 0 && P > 0;
   cudaStream_t cs = nullptr;
   EventSet ev;
   cudaEvent_t* ready = ev.e + 1;
   cudaEvent_t* freed = ev.e + 3;
   if (staged) {
+    // The ring lives in the caller's workspace: earlier work on `s` may still use
+    // it. The event is taken before this call's prologue (which does not touch
+    // the ring), so the first copy overlaps the compaction and the gather.
     if ((st = copy_stream(&cs)) != RF_OK || (st = ev.create()) != RF_OK) return st;
-    // The ring lives in the caller's workspace: earlier work on `s` may still use it.
     if ((st = cuda_check(cudaEventRecord(ev.e[0], s), "cudaEventRecord")) != RF_OK) return st;
     if ((st = cuda_check(cudaStreamWaitEvent(cs, ev.e[0], 0), "cudaStreamWaitEvent")) != RF_OK) return st;
   }
-  for (int64_t c0 = 0, step = 0; c0 < P; c0 += kLayerChunk, ++step) {
-    const int64_t g = std::min<int64_t>(kLayerChunk, P - c0);  // layers S+c0 .. S+c0+g-1
+  bool work = false;
+  if ((st = fill_prologue(desc, x_S, ld_x, exact_mask, n_fill_out, lay, sms, s, &work)) != RF_OK || !work) return st;
+
+  const bool pair = use_pair(desc->flags, true);
+  const int64_t M_pad = round_up(n_prefix, kFillRowAlign);
+  const size_t map_elems = static_cast<size_t>(d) * static_cast<size_t>(d_in);
+  const size_t elem = int8 ? 1 : 2;
+  const int64_t H = desc->n_kv_heads;
+  // Staged maps start with chunks of 1 and 2 layers, then kLayerChunk: only the
+  // first chunk's copy waits in front of the first GEMM, and every later copy
+  // fits under the GEMMs of the chunk before it.
+  int64_t g = 0;
+  for (int64_t c0 = 0, step = 0; c0 < P; c0 += g, ++step) {
+    g = std::min<int64_t>(staged && step < 2 ? int64_t(1) << step : kLayerChunk, P - c0);  // layers S+c0 .. +g-1
     const int r = static_cast<int>(step & 1);
     const size_t n = static_cast<size_t>(g) * map_elems;
     const char* src = static_cast<const char*>(maps->A) + static_cast<size_t>(c0) * map_elems * elem;
