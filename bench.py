@@ -598,7 +598,19 @@ def run_extras(dev, peak_tflops, flags=0, only=None):
             ms, stages = _timed(lambda: rf.rf_solve(cd, cs, c.lam, rf.RF_ALPHA_TRACE, refine, A, b, Ab, None, status,
                                                    ws, wsb), 1, stream)
             sol[f"refine_{refine}_ms"] = ms
+            sol[f"refine_{refine}_stages_ms"] = stages
         assert int(status.item()) == 0
+        # A_p = Cc_pᵀ H^-1: 2 P d³ fp32-accurate flops, as six bf16 plane products each
+        prod = 2.0 * P * d ** 3
+        pm = sol["refine_0_stages_ms"].get("solve_product")
+        if pm:
+            sol["product_bf16_plane_tflops"] = 6.0 * prod / (pm / 1e3) / 1e12
+            sol["product_frac_of_bf16_peak"] = sol["product_bf16_plane_tflops"] / peak_tflops
+        # one refinement sweep: the residual A_p H as 28 digit-pair products (7 digits a side,
+        # weights s + t <= 8) plus the correction R_p H^-1 (six plane products)
+        rm = sol["refine_1_stages_ms"].get("solve_refine")
+        if rm:
+            sol["refine_bf16_tflops"] = (28.0 + 6.0) * prod / (rm / 1e3) / 1e12
         out["a6_solve"] = {"workload": f"8b-shaped ridge solve, d={d}, {P} maps, lambda={c.lam}", **sol}
         del st, cs, A, b, Ab, ws
         torch.cuda.empty_cache()
