@@ -606,11 +606,11 @@ def run_extras(dev, peak_tflops, flags=0, only=None):
         if pm:
             sol["product_bf16_plane_tflops"] = 6.0 * prod / (pm / 1e3) / 1e12
             sol["product_frac_of_bf16_peak"] = sol["product_bf16_plane_tflops"] / peak_tflops
-        # one refinement sweep: the residual A_p H as 28 digit-pair products (7 digits a side,
-        # weights s + t <= 8) plus the correction R_p H^-1 (six plane products)
+        # one refinement sweep: the residual A_p H as 21 digit-pair products (6 digits a side,
+        # weights s + t <= 7) plus the correction R_p H^-1 (six plane products)
         rm = sol["refine_1_stages_ms"].get("solve_refine")
         if rm:
-            sol["refine_bf16_tflops"] = (28.0 + 6.0) * prod / (rm / 1e3) / 1e12
+            sol["refine_bf16_tflops"] = (21.0 + 6.0) * prod / (rm / 1e3) / 1e12
         out["a6_solve"] = {"workload": f"8b-shaped ridge solve, d={d}, {P} maps, lambda={c.lam}", **sol}
         del st, cs, A, b, Ab, ws
         torch.cuda.empty_cache()

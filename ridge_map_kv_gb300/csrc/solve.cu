@@ -25,6 +25,7 @@
 //                           fp64 epilogue), A_p += R_p H^-1 (the split product)
 //   k_bias                  b_p = μ_p − A_p μ_x (fp64 accumulation)
 #include <algorithm>
+#include <cstring>
 
 #include "rf_host.h"
 #include "rf_device.cuh"
@@ -582,40 +583,42 @@ static rf_status split_gemm(SolveCtx& c, const float* a, bool a_tr, const float*
 // using fast routines of matrix multiplication", 2012), for the refinement
 //   R_p = Cc_pᵀ − A_p H.
 // Each row of A_p (fp32) and each row of H (fp64; H is symmetric, so its rows are
-// its columns) is scaled by a power of two σ ≥ its largest magnitude and cut into
-// kOzDigits integer digits of 6 bits: x/σ = Σ_s d_s 2^(−6s), |d_1| <= 64, |d_s| <= 32
-// after, every digit exact in bf16. A digit product summed over a K chunk of 2048
-// is an integer below 2^23, exact in the fp32 accumulator; the epilogue adds the
-// chunks and the digit pairs of one weight m = s + t as exact int32 sums J_m, then
-// R −= σ_o τ_i 2^(−6m) J_m in fp64. Pairs with s + t <= kOzDigits + 1 are kept:
-// 42-bit operands, a residual accurate to about 2^-41 of Σ|A||H| in the worst case.
+// its columns) is scaled by a power of two σ ≥ 2 × its largest magnitude and cut
+// into kOzDigits integer digits of 7 bits: x/σ = Σ_s d_s 2^(−7s), |d_s| <= 64, every
+// digit exact in bf16. A digit product summed over a K chunk of 2048 is an integer
+// of magnitude at most 2^23, exact in the fp32 accumulator; the epilogue adds the
+// chunks and the digit pairs of one weight m = s + t as exact int32 sums J_m and
+// stores them (one launch per weight). A last pass forms T = Σ_m J_m 2^(7(7−m))
+// exactly in int64 and R = Cc − σ_o τ_i 2^(−49) T in fp64. Pairs with
+// s + t <= kOzDigits + 1 are kept: 41-bit operands, a residual accurate to about
+// 2^-40 of Σ|A||H| in the worst case.
 // --------------------------------------------------------------------------
-constexpr int kOzDigits = 7;
+constexpr int kOzDigits = 6;
+constexpr int kOzBits = 7;
 constexpr int kOzChunk = 2048;
 constexpr int kOzMaps = 4;  // maps per residual launch (keeps the last wave of units small)
-constexpr int kOzPairs = kOzDigits * (kOzDigits + 1) / 2;
 
-// Digits of each row of an fp32 or fp64 matrix [rows][cols]: digit d of row r at
+// Digits of each row of an fp64 matrix [rows][cols]: digit d of row r at
 // planes[(d * plane_rows + r) * cols ...] in bf16 (plane_rows >= rows), and the row
 // scale σ (a power of two, 0 for a zero row). One warp per row.
-template <class T>
-__global__ void __launch_bounds__(256) k_oz_digits(const T* __restrict__ X, int rows, int plane_rows, int cols,
-                                                   __nv_bfloat16* __restrict__ planes, double* __restrict__ scale) {
+__global__ void __launch_bounds__(256) k_oz_digits_f64(const double* __restrict__ X, int rows, int plane_rows, int cols,
+                                                       __nv_bfloat16* __restrict__ planes, double* __restrict__ scale) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= rows) return;
-  const T* x = X + static_cast<size_t>(warp) * cols;
+  const double* x = X + static_cast<size_t>(warp) * cols;
   double mx = 0.0;
-  for (int k = lane; k < cols; k += 32) mx = fmax(mx, fabs(static_cast<double>(x[k])));
+  for (int k = lane; k < cols; k += 32) mx = fmax(mx, fabs(x[k]));
   for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   int e = 0;
-  if (mx > 0.0) frexp(mx, &e);  // mx = f 2^e, f in [0.5, 1): σ = 2^e >= mx
+  if (mx > 0.0) frexp(mx, &e);  // mx = f 2^e, f in [0.5, 1): σ = 2^(e+1) >= 2 mx
+  ++e;
   if (lane == 0) scale[warp] = mx > 0.0 ? ldexp(1.0, e) : 0.0;
   const size_t plane = static_cast<size_t>(plane_rows) * cols;
   for (int k = lane; k < cols; k += 32) {
-    double v = mx > 0.0 ? ldexp(static_cast<double>(x[k]), -e) : 0.0;  // exact, |v| <= 1
+    double v = mx > 0.0 ? ldexp(x[k], -e) : 0.0;  // exact, |v| <= 1/2
 #pragma unroll
     for (int d = 0; d < kOzDigits; ++d) {
-      const double t = v * 64.0;
+      const double t = v * static_cast<double>(1 << kOzBits);  // |t| <= 64, |t − rint(t)| <= 1/2
       const double r = rint(t);
       v = t - r;  // exact
       planes[d * plane + static_cast<size_t>(warp) * cols + k] = __float2bfloat16_rn(static_cast<float>(r));
@@ -623,43 +626,107 @@ __global__ void __launch_bounds__(256) k_oz_digits(const T* __restrict__ X, int 
   }
 }
 
-// R64[o][i] = C_p[i][o] − n μ_x[i] μ_p[o] (fp64), through 32 x 32 shared tiles.
-// Grid (d_out/32, d_in/32), 32 x 8 threads.
-__global__ void __launch_bounds__(256) k_oz_init(const double* __restrict__ C, const double* __restrict__ mu_x,
-                                                 const double* __restrict__ mu_y, const double* __restrict__ n,
-                                                 int d_in, int d_out, double* __restrict__ R64) {
-  __shared__ double t[32][33];
-  const int o0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
-  const double nn = *n;
-  for (int j = threadIdx.y; j < 32; j += 8) {
-    const int i = i0 + j, o = o0 + threadIdx.x;
-    t[j][threadIdx.x] = C[static_cast<size_t>(i) * d_out + o] - nn * mu_x[i] * mu_y[o];
+// The same digits of an fp32 matrix, from fp32 arithmetic: for |v| <= 1/2, v·2^7,
+// its nearest integer and their difference are all exact in fp32, so the digits are
+// those of the fp64 procedure without using the (slow) fp64 units. Four columns a
+// lane; cols % 128 == 0 and X 16-byte aligned.
+__global__ void __launch_bounds__(256) k_oz_digits_f32(const float* __restrict__ X, int rows, int plane_rows, int cols,
+                                                       __nv_bfloat16* __restrict__ planes, double* __restrict__ scale) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= rows) return;
+  const float4* x = reinterpret_cast<const float4*>(X + static_cast<size_t>(warp) * cols);
+  const int c4 = cols / 4;
+  float mx = 0.0f;
+  for (int k = lane; k < c4; k += 32) {
+    const float4 a = x[k];
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
   }
-  __syncthreads();
-  for (int j = threadIdx.y; j < 32; j += 8) R64[static_cast<size_t>(o0 + j) * d_in + i0 + threadIdx.x] = t[threadIdx.x][j];
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  int e = 0;
+  if (mx > 0.0f) frexpf(mx, &e);  // σ = 2^(e+1) >= 2 mx
+  ++e;
+  if (lane == 0) scale[warp] = mx > 0.0f ? ldexp(1.0, e) : 0.0;
+  const size_t plane = static_cast<size_t>(plane_rows) * cols;
+  for (int k = lane; k < c4; k += 32) {
+    const float4 a = x[k];
+    float v[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = mx > 0.0f ? ldexpf(v[j], -e) : 0.0f;  // |v| <= 1/2
+#pragma unroll
+    for (int d = 0; d < kOzDigits; ++d) {
+      __nv_bfloat16 r[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float t = v[j] * static_cast<float>(1 << kOzBits);
+        const float q = rintf(t);
+        v[j] = t - q;
+        r[j] = __float2bfloat16_rn(q);
+      }
+      uint2 w;
+      memcpy(&w, r, sizeof(w));
+      *reinterpret_cast<uint2*>(planes + d * plane + static_cast<size_t>(warp) * cols + 4 * k) = w;
+    }
+  }
 }
 
-// Digit pair number pi (0 <= pi < kOzPairs) in weight order: m = s + t = 2, 3, ...,
-// and within a weight s = 1 .. m−1.
-__device__ __forceinline__ void oz_pair(int pi, int& m, int& s) {
-  m = 2;
-  int base = 0;
-  while (pi >= base + (m - 1)) {
-    base += m - 1;
-    ++m;
+// Exponent e of a power of two 2^e held as a normal double.
+__device__ __forceinline__ int pow2_exponent(double x) {
+  return static_cast<int>((static_cast<unsigned long long>(__double_as_longlong(x)) >> 52) & 0x7ff) - 1023;
+}
+
+// 2^e as a double, for -1022 <= e <= 1023.
+__device__ __forceinline__ double pow2_double(int e) {
+  return __longlong_as_double(static_cast<long long>(static_cast<uint64_t>(e + 1023) << 52));
+}
+
+// v · 2^e: an exponent shift (integer operations: GB300's fp64 rate is low) for normal
+// v and result, else two products that round only if they must (|e| <= 2044).
+__device__ __forceinline__ double scale_pow2(double v, int e) {
+  const long long b = __double_as_longlong(v);
+  const int E = static_cast<int>((b >> 52) & 0x7ff);
+  if (E > 0 && E < 2047 && E + e > 0 && E + e < 2047) return __longlong_as_double(b + (static_cast<long long>(e) << 52));
+  return v * pow2_double(e / 2) * pow2_double(e - e / 2);
+}
+
+// R_p[o][i] = C_p[i][o] − n μ_x[i] μ_p[o] − σ_o τ_i 2^(−49) T[o][i] for the maps of a
+// group, with T = Σ_m J_m 2^(7(7−m)) built exactly in int64 from the weights' sums
+// (|J_m| <= (m−1) 2^12 d_in, so |T| < 2^47.1 d_in <= 2^62.1 for d_in <= 32768) and
+// rounded once to fp64. Through 32 x 32 shared tiles (C is [i][o], R [o][i]).
+// Grid (d_out/32, d_in/32, maps), 32 x 8 threads.
+__global__ void __launch_bounds__(256) k_oz_combine(const double* __restrict__ C, const double* __restrict__ mu_x,
+                                                    const double* __restrict__ mu_y, const double* __restrict__ n,
+                                                    const double* __restrict__ sA, const double* __restrict__ sH,
+                                                    const int32_t* __restrict__ J, size_t plane, int d_in, int d_out,
+                                                    float* __restrict__ R32) {
+  __shared__ double t[32][33];
+  const int o0 = blockIdx.x * 32, i0 = blockIdx.y * 32, p = blockIdx.z;
+  const double nn = *n;
+  const double* Cp = C + static_cast<size_t>(p) * d_in * d_out;
+  const double* my = mu_y + static_cast<size_t>(p) * d_out;
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int i = i0 + r, o = o0 + threadIdx.x;
+    t[r][threadIdx.x] = Cp[static_cast<size_t>(i) * d_out + o] - nn * mu_x[i] * my[o];
   }
-  s = pi - base + 1;
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int o = o0 + r, i = i0 + threadIdx.x;
+    const size_t e = (static_cast<size_t>(p) * d_out + o) * d_in + i;
+    long long T = 0;
+#pragma unroll
+    for (int w = 0; w < kOzDigits; ++w) T = T * (1 << kOzBits) + J[w * plane + e];  // weights m = 2, 3, ...
+    const int k = pow2_exponent(sA[static_cast<size_t>(p) * d_out + o]) + pow2_exponent(sH[i]) -
+                  kOzBits * (kOzDigits + 1);
+    R32[e] = static_cast<float>(t[threadIdx.x][r] - scale_pow2(static_cast<double>(T), k));
+  }
 }
 
 template <bool kPair_>
 struct OzakiProb {
   CUtensorMap tmA;  // digits of the maps' rows: [kOzDigits * maps * d_out][d_in]
   CUtensorMap tmB;  // digits of H rows:        [kOzDigits * d_in][d_in]
-  const double* sA;  // [maps][d_out] row scales
-  const double* sH;  // [d_in]  row scales of H
-  double* R64;       // [maps][d_out][d_in] fp64 residuals, initialised to Cc_pᵀ
-  float* R32;        // [maps][d_out][d_in] fp32 results
+  int32_t* J;        // [maps][d_out][d_in] this weight's exact sums J_m
   int maps, plane_maps, d_out, d_in, m_tiles, n_tiles, n_chunks;  // maps in this launch; maps per digit plane
+  int m;  // the digit weight s + t of this launch (pairs s = 1 .. m−1)
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = false;
@@ -677,7 +744,7 @@ struct OzakiProb {
     tma_prefetch_desc(&tmB);
   }
   __device__ int num_units() const { return maps * m_tiles * n_tiles; }
-  __device__ int num_subtiles(int) const { return kOzPairs * n_chunks; }
+  __device__ int num_subtiles(int) const { return (m - 1) * n_chunks; }
   __device__ void decode(int u, int& p, int& mt, int& nt) const {
     nt = u % n_tiles;
     u /= n_tiles;
@@ -694,9 +761,7 @@ struct OzakiProb {
   __device__ Coords coords(int u, int sb, uint32_t rank) const {
     int p, mt, nt;
     decode(u, p, mt, nt);
-    const int pi = sb / n_chunks, c = sb - pi * n_chunks;
-    int m, s;
-    oz_pair(pi, m, s);
+    const int s = sb / n_chunks + 1, c = sb % n_chunks;
     const int t = m - s;
     return {((s - 1) * plane_maps + p) * d_out + mt * Cfg::kUnitM + static_cast<int>(rank) * kBM,
             (t - 1) * d_in + nt * kBN + static_cast<int>(rank) * Cfg::kBRows, c * kOzChunk};
@@ -706,10 +771,7 @@ struct OzakiProb {
     load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, c.k0 + kb * kBK, c.b_row);
   }
   __device__ void epilogue(EpiState& es, int, int sb, int, uint32_t tacc, int, int, uint32_t) const {
-    const int pi = sb / n_chunks, c = sb - pi * n_chunks;
-    int m, s;
-    oz_pair(pi, m, s);
-    const bool first = c == 0 && s == 1;  // first sub-tile of weight m
+    const bool first = sb == 0;
 #pragma unroll
     for (int ch = 0; ch < kCols / 32; ++ch) {
       uint32_t v[32];
@@ -723,24 +785,14 @@ struct OzakiProb {
     }
   }
   __device__ void epilogue_after(EpiState& es, int u, int sb, int nsub, int row, int col0, uint32_t rank) const {
-    const int pi = sb / n_chunks, c = sb - pi * n_chunks;
-    int m, s;
-    oz_pair(pi, m, s);
-    if (c != n_chunks - 1 || s != m - 1) return;  // weight m not complete yet
+    if (sb != nsub - 1) return;  // weight m not complete yet
     int p, mt, nt;
     decode(u, p, mt, nt);
     const size_t o = static_cast<size_t>(p) * d_out + static_cast<size_t>(mt) * Cfg::kUnitM + rank * kBM + row;
-    const size_t i0 = static_cast<size_t>(nt) * kBN + col0;
-    const double so = ldexp(sA[o], -6 * m);
-    double* r = R64 + o * d_in + i0;
-    if (sb == nsub - 1) {
-      float* w = R32 + o * d_in + i0;
+    int4* dst = reinterpret_cast<int4*>(J + o * d_in + static_cast<size_t>(nt) * kBN + col0);
 #pragma unroll
-      for (int q = 0; q < kCols; ++q) w[q] = static_cast<float>(r[q] - so * sH[i0 + q] * static_cast<double>(es.rs[q]));
-    } else {
-#pragma unroll
-      for (int q = 0; q < kCols; ++q) r[q] -= so * sH[i0 + q] * static_cast<double>(es.rs[q]);
-    }
+    for (int q = 0; q < kCols / 4; ++q)
+      dst[q] = make_int4(es.rs[4 * q], es.rs[4 * q + 1], es.rs[4 * q + 2], es.rs[4 * q + 3]);
   }
 };
 
@@ -763,7 +815,7 @@ struct SolveLayout {
   double* sH;               // [d_in] their scales
   __nv_bfloat16* ozA;       // [kOzDigits][kOzMaps * d_out][d_in] digits of a group of maps' rows
   double* sA;               // [kOzMaps * d_out]
-  double* R64;              // [kOzMaps][d_out][d_in] their fp64 residuals
+  int32_t* J;               // [kOzDigits][kOzMaps][d_out][d_in] their sums J_m, one plane per weight
   size_t bytes;
 };
 
@@ -788,7 +840,7 @@ static SolveLayout solve_layout(const rf_calib_desc* d, void* ws) {
   const int64_t om = std::min<int64_t>(P, kOzMaps);
   l.ozA = c.take<__nv_bfloat16>(kOzDigits * om * dout * di);
   l.sA = c.take<double>(om * dout);
-  l.R64 = c.take<double>(om * dout * di);
+  l.J = c.take<int32_t>(kOzDigits * om * dout * di);
   l.bytes = c.bytes();
   return l;
 }
@@ -800,7 +852,7 @@ static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* 
   using Cfg = GemmCfg<kPair>;
   rf_status st;
   const unsigned hb = static_cast<unsigned>((static_cast<long long>(di) * 32 + 255) / 256);
-  k_oz_digits<double><<<hb, 256, 0, c.s>>>(lay.H64, di, di, di, lay.ozH, lay.sH);
+  k_oz_digits_f64<<<hb, 256, 0, c.s>>>(lay.H64, di, di, di, lay.ozH, lay.sH);
   OzakiProb<kPair> pr;
   const int om = std::min(P, kOzMaps);
   if ((st = make_tmap_bf16_2d(&pr.tmA, lay.ozA, di, static_cast<uint64_t>(kOzDigits) * om * dout, di, kBK, kBM)) !=
@@ -809,9 +861,6 @@ static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* 
   if ((st = make_tmap_bf16_2d(&pr.tmB, lay.ozH, di, static_cast<uint64_t>(kOzDigits) * di, di, kBK, Cfg::kBRows)) !=
       RF_OK)
     return st;
-  pr.sA = lay.sA;
-  pr.sH = lay.sH;
-  pr.R64 = lay.R64;
   pr.d_out = dout;
   pr.d_in = di;
   pr.m_tiles = dout / Cfg::kUnitM;
@@ -825,18 +874,24 @@ static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* 
     // digits of the group's rows: the planes hold `om` maps per digit; a short last
     // group leaves the rest unused (its units are not launched)
     const unsigned gb = static_cast<unsigned>((static_cast<long long>(g) * dout * 32 + 255) / 256);
-    k_oz_digits<float><<<gb, 256, 0, c.s>>>(A + off, g * dout, om * dout, di, lay.ozA, lay.sA);
-    for (int j = 0; j < g; ++j)
-      k_oz_init<<<dim3(dout / 32, di / 32), dim3(32, 8), 0, c.s>>>(
-          C + off + static_cast<size_t>(j) * di * dout, lay.mu_x, lay.mu_y + static_cast<size_t>(p0 + j) * dout, lay.n,
-          di, dout, lay.R64 + static_cast<size_t>(j) * dout * di);
-    if ((st = cuda_check(cudaGetLastError(), "residual set-up launches")) != RF_OK) return st;
+    k_oz_digits_f32<<<gb, 256, 0, c.s>>>(A + off, g * dout, om * dout, di, lay.ozA, lay.sA);
+    if ((st = cuda_check(cudaGetLastError(), "residual digit launch")) != RF_OK) return st;
     pr.maps = g;
     pr.plane_maps = om;
-    pr.R32 = R32 + off;
-    if ((st = launch_gemm(pr, static_cast<int64_t>(g) * pr.m_tiles * pr.n_tiles, c.sms, c.s, "residual GEMM launch")) !=
-        RF_OK)
-      return st;
+    // One launch per digit weight m, each storing its own plane of sums, so that the
+    // epilogues only write (fire and forget) and never wait on a read.
+    const size_t plane = static_cast<size_t>(om) * dout * di;
+    for (int m = 2; m <= kOzDigits + 1; ++m) {
+      pr.m = m;
+      pr.J = lay.J + (m - 2) * plane;
+      if ((st = launch_gemm(pr, static_cast<int64_t>(g) * pr.m_tiles * pr.n_tiles, c.sms, c.s,
+                            "residual GEMM launch")) != RF_OK)
+        return st;
+    }
+    k_oz_combine<<<dim3(dout / 32, di / 32, g), dim3(32, 8), 0, c.s>>>(
+        C + off, lay.mu_x, lay.mu_y + static_cast<size_t>(p0) * dout, lay.n, lay.sA, lay.sH, lay.J, plane, di, dout,
+        R32 + off);
+    if ((st = cuda_check(cudaGetLastError(), "residual combine launch")) != RF_OK) return st;
   }
   return RF_OK;
 }
