@@ -200,6 +200,30 @@ def test_solve_refinement_restores_accuracy_when_ill_conditioned():
     assert e1 <= 1e-5 and e1 < e0 / 20, (e0, e1)
 
 
+def test_solve_repeated_refinement_converges_when_badly_conditioned():
+    """κ(Gc) ≈ 1e5: the fp32 solve alone is off by about κ·2^-24 and each sweep shrinks
+    the error by about that factor again, down to the residual's own accuracy. Reaching
+    1e-5 needs the residual good to about 1e-5/κ ≈ 2^-33 of its terms; an fp32-accurate
+    residual would stall near the unrefined error."""
+    d, P, n = 512, 2, 8192
+    rng = np.random.default_rng(22)
+    Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    X = (rng.standard_normal((n, d)) * np.geomspace(1.0, 10 ** -2.5, d)) @ Q.T
+    At = rng.standard_normal((P, d, d)) / math.sqrt(d)
+    Y = np.einsum("pij,nj->pni", At, X) + 0.01 * rng.standard_normal((P, n, d))
+    Xb = torch.as_tensor(X, dtype=torch.float32).to(torch.bfloat16)
+    Yb = torch.as_tensor(Y, dtype=torch.float32).to(torch.bfloat16)
+    ref = O.calib_stats(_f64(Xb), _f64(Yb))
+    lam = 1e-9
+    Ar, _, _ = O.ridge_solve(ref, lam)
+    errs = {}
+    for refine in (0, 4):
+        A, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=refine)
+        errs[refine] = max(_rel(A[p], Ar[p]) for p in range(P))
+    assert errs[0] > 1e-4, errs   # hard enough that fp32 alone is far off
+    assert errs[4] <= 1e-5 and errs[4] < errs[0] / 100, errs
+
+
 @pytest.mark.slow
 def test_solve_full_width_sampled_rows():
     d, P, n = 4096, 2, 8192
