@@ -11,7 +11,8 @@
 //                      is summed in fp32 in TMEM, so the tensor cores never sum
 //                      more than kCalibChunk rows. Eight epilogue warps add the
 //                      chunk blocks into fp32 running sums in registers and flush
-//                      them into the fp64 totals every 16 chunks.
+//                      them into the fp64 totals every 16 chunks, with fp64
+//                      reductions over whole row segments.
 //   k_colsum           Σx, Σy_p, optionally Σy_p² (fp32 over 64 rows, fp64 across)
 //                      and n += rows.
 #include <algorithm>
@@ -40,7 +41,6 @@ struct GramProb {
   int d_in, d_out, P, n_rows, n_chunks;
   int g_mt, g_nt, c_nt, g_units;
   int c_group;  // M-tiles per group of the XᵀY units (their X rows stay in L2 together)
-  int red_flush;  // add into G and C with fp64 reductions (no read) instead of read-modify-write
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = true;
@@ -139,27 +139,35 @@ struct GramProb {
     }
   }
   // The flush runs after the accumulator is handed back, overlapping the MMAs of
-  // the next chunk.
+  // the next chunks. Each warp turns its 32 rows x 16 columns around through shared
+  // memory, so that its fp64 reductions cover whole 128-byte row segments, and
+  // nothing is read back: a read-modify-write of the totals, one thread per row,
+  // waited on its loads for longer than the next unit's MMAs (measured: the 27B-
+  // shaped Gram GEMM took 29.8 ms that way, 25.3 ms this way). (Static shared
+  // memory, on top of the GEMM stages.)
   __device__ void epilogue_after(EpiState& es, int u, int sb, int nsub, int row, int col0, uint32_t rank) const {
     if ((sb % kFlushChunks) != kFlushChunks - 1 && sb != nsub - 1) return;
+    __shared__ float turn[kEpiWarps][32][17];
     bool is_g;
     int p, mt, nt;
     decode(u, is_g, p, mt, nt);
-    const size_t i = static_cast<size_t>(mt) * Cfg::kUnitM + rank * kBM + row;
+    const int lane = row & 31, w = (row >> 5) + 4 * (col0 / kCols);
+    const size_t i = static_cast<size_t>(mt) * Cfg::kUnitM + rank * kBM + (row - lane);  // the warp's first row
+    const size_t ld = is_g ? d_in : d_out;
     double* o = (is_g ? G + i * d_in : C + (static_cast<size_t>(p) * d_in + i) * d_out) + static_cast<size_t>(nt) * kBN +
                 col0;
-    if (red_flush) {
+    const int half = lane >> 4, col = lane & 15;
+    o += half * ld + col;  // lanes 0-15 take the even rows, 16-31 the odd ones
+    const float* t = &turn[w][half][col];
 #pragma unroll
-      for (int q = 0; q < kCols; ++q) atomicAdd(o + q, static_cast<double>(es.rs[q]));
-      return;
-    }
-    double2* o2 = reinterpret_cast<double2*>(o);
+    for (int c = 0; c < kCols; c += 16) {
 #pragma unroll
-    for (int q = 0; q < kCols / 2; ++q) {
-      double2 a = o2[q];
-      a.x += static_cast<double>(es.rs[2 * q]);
-      a.y += static_cast<double>(es.rs[2 * q + 1]);
-      o2[q] = a;
+      for (int j = 0; j < 16; ++j) turn[w][lane][j] = es.rs[c + j];
+      __syncwarp();
+      double* q = o + c;
+#pragma unroll 4
+      for (int k = 0; k < 16; ++k, q += 2 * ld) atomicAdd(q, static_cast<double>(t[k * 2 * 17]));
+      __syncwarp();
     }
   }
 };
@@ -233,8 +241,7 @@ __global__ void __launch_bounds__(256) k_colsum(const __nv_bfloat16* __restrict_
 // readers (the 8,192-feature Gram over 131,072 rows read 58 GB from DRAM for
 // 2.4 GB of operands). Launching slab by slab restarts every pair on the same
 // rows. The launches run in stream order and a tile is flushed once per launch,
-// so the fp64 totals are written by one unit at a time; calls of several slabs
-// flush with fp64 reductions, which spare the epilogue the read of the totals.
+// so every fp64 total receives its additions in a fixed order.
 constexpr int64_t kCalibSlabRows = 16 * kCalibChunk;
 
 template <bool kPair>
@@ -273,7 +280,6 @@ rf_status calib_gemm(const rf_calib_desc* desc, const rf_bf16* X, int64_t ld_x, 
     const int64_t panel = static_cast<int64_t>(Cfg::kUnitM) * rows * 2;
     pr.c_group = static_cast<int>(
         std::max<int64_t>(1, std::min<int64_t>(pr.g_mt, (int64_t(48) << 20) / std::max<int64_t>(panel, 1))));
-    pr.red_flush = n_rows > kCalibSlabRows ? 1 : 0;
     pr.dev_status = dev_status;
     pr.timeout_ns = wait_timeout_ns();
     if ((s = launch_gemm(pr, pr.g_units + P * pr.g_mt * pr.c_nt, sms, cs, "calibration GEMM launch")) != RF_OK)
