@@ -23,7 +23,7 @@
 //   refinement (optional)   R_p = Cc_pᵀ − A_p H, fp64-accurate on the tensor cores
 //                           (OzakiProb: integer digit planes, exact chunk sums,
 //                           fp64 epilogue), A_p += R_p H^-1 (the split product)
-//   k_bias                  b_p = μ_p − A_p μ_x (fp64 accumulation)
+//   k_bias                  b_p = μ_p − A_p μ_x (compensated fp32 pairs, fp64 across lanes)
 #include <algorithm>
 #include <cstring>
 
@@ -351,36 +351,65 @@ __global__ void __launch_bounds__(256) k_build_h(const double* __restrict__ G, c
   }
 }
 
-// Cc32[p][i][o] = C[p][i][o] − n μ_x[i] μ_p[o]
-__global__ void k_centre_c(const double* C, const double* mu_x, const double* mu_y, const double* n, int d_in,
-                           int d_out, long long total, float* Cc) {
-  for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
-       e += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long per = static_cast<long long>(d_in) * d_out;
-    const int p = static_cast<int>(e / per);
-    const long long r = e - p * per;
-    const int i = static_cast<int>(r / d_out), o = static_cast<int>(r % d_out);
-    Cc[e] = static_cast<float>(C[e] - (*n) * mu_x[i] * mu_y[static_cast<long long>(p) * d_out + o]);
-  }
+// Cc32[p][i][o] = C[p][i][o] − n μ_x[i] μ_p[o], one (p, i) row per block x: one
+// fp64 fma per element (GB300's fp64 rate is low, so no per-element index division).
+__global__ void __launch_bounds__(256) k_centre_c(const double* __restrict__ C, const double* __restrict__ mu_x,
+                                                  const double* __restrict__ mu_y, const double* __restrict__ n,
+                                                  int d_in, int d_out, float* __restrict__ Cc) {
+  const long long row = blockIdx.x;  // p * d_in + i
+  const int p = static_cast<int>(row / d_in), i = static_cast<int>(row - static_cast<long long>(p) * d_in);
+  const double a = -(*n) * mu_x[i];
+  const double* c = C + row * d_out;
+  const double* my = mu_y + static_cast<long long>(p) * d_out;
+  float* out = Cc + row * d_out;
+  for (int o = threadIdx.x; o < d_out; o += blockDim.x) out[o] = static_cast<float>(fma(a, my[o], c[o]));
 }
 
-// b_p[o] = μ_p[o] − Σ_i A_p[o][i] μ_x[i] (fp64), one warp per output; also the
-// optional bf16 copy of A.
-__global__ void k_bias(const float* A, const double* mu_x, const double* mu_y, long long rows, int d_in, float* b) {
+// μ_x as an unevaluated pair of floats, hi + lo (|lo| <= 2^-24 |hi|), for k_bias.
+__global__ void k_split_mu(const double* __restrict__ mu_x, int d_in, float2* __restrict__ mu2) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= d_in) return;
+  const float hi = static_cast<float>(mu_x[i]);
+  mu2[i] = make_float2(hi, static_cast<float>(mu_x[i] - static_cast<double>(hi)));
+}
+
+// b_p[o] = μ_p[o] − Σ_i A_p[o][i] μ_x[i], one warp per output. Each lane sums in
+// fp32 pairs (hi, lo) with error-free products (fma) and sums (Knuth's two-sum),
+// about 2^-44 of Σ|A||μ|; the lanes combine in fp64.
+__global__ void k_bias(const float* __restrict__ A, const float2* __restrict__ mu2, const double* __restrict__ mu_y,
+                       long long rows, int d_in, float* __restrict__ b) {
   const long long w = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= rows) return;
   const float* a = A + w * d_in;
-  double s = 0.0;
-  for (int i = lane; i < d_in; i += 32) s += static_cast<double>(a[i]) * mu_x[i];
+  float hi = 0.f, lo = 0.f;
+  for (int i = lane; i < d_in; i += 32) {
+    const float x = a[i];
+    const float2 m = mu2[i];
+    // (the _rn intrinsics keep the compiler from fusing these into fma's)
+    const float p = __fmul_rn(x, m.x);
+    const float pe = fmaf(x, m.x, -p) + x * m.y;  // the product's error and the low part
+    const float t = __fadd_rn(hi, p);
+    const float bb = __fsub_rn(t, hi);
+    lo += __fadd_rn(__fsub_rn(hi, __fsub_rn(t, bb)), __fsub_rn(p, bb)) + pe;  // two-sum error of hi + p
+    hi = t;
+  }
+  double s = static_cast<double>(hi) + static_cast<double>(lo);
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   if (lane == 0) b[w] = static_cast<float>(mu_y[w] - s);
 }
 
-__global__ void k_to_bf16(const float* A, long long total, __nv_bfloat16* out) {
-  for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
-       e += static_cast<long long>(gridDim.x) * blockDim.x)
-    out[e] = __float2bfloat16_rn(A[e]);
+// bf16 copy of A, four elements a thread (total % 4 == 0, 16-byte aligned).
+__global__ void k_to_bf16(const float* __restrict__ A, long long total, __nv_bfloat16* __restrict__ out) {
+  for (long long e = 4 * (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x); e < total;
+       e += 4 * static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 v = *reinterpret_cast<const float4*>(A + e);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 w;
+    memcpy(&w.x, &lo, 4);
+    memcpy(&w.y, &hi, 4);
+    *reinterpret_cast<uint2*>(out + e) = w;
+  }
 }
 
 // --------------------------------------------------------------------------
@@ -801,6 +830,7 @@ static int split_point(int n) { return std::max(kSolveBlock, (n / 2) / kSolveBlo
 struct SolveLayout {
   double* mu_x;
   double* mu_y;
+  float2* mu2;  // μ_x as float pairs (the bias)
   double* alpha;
   double* n;
   double* H64;
@@ -824,6 +854,7 @@ static SolveLayout solve_layout(const rf_calib_desc* d, void* ws) {
   Carve c(ws);
   SolveLayout l;
   l.mu_x = c.take<double>(di);
+  l.mu2 = c.take<float2>(di);
   l.mu_y = c.take<double>(std::max<int64_t>(P * dout, 1));
   l.alpha = c.take<double>(1);
   l.n = c.take<double>(1);
@@ -1000,8 +1031,8 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
     k_means<<<eb, 256, 0, c.s>>>(st->sx, st->sy, st->n, di, static_cast<long long>(P) * dout, lay.mu_x, lay.mu_y, lay.n);
     k_trace_alpha<<<1, 1024, 0, c.s>>>(st->G, lay.mu_x, lay.n, di, lambda, alpha_mode, lay.alpha, alpha_out);
     k_build_h<<<dim3(di / 32, di / 32), dim3(32, 8), 0, c.s>>>(st->G, lay.mu_x, lay.n, lay.alpha, di, lay.H64, lay.L);
-    const long long ctotal = static_cast<long long>(P) * di * dout;
-    k_centre_c<<<eb, 256, 0, c.s>>>(st->C, lay.mu_x, lay.mu_y, lay.n, di, dout, ctotal, lay.work);
+    k_centre_c<<<static_cast<unsigned>(static_cast<long long>(P) * di), 256, 0, c.s>>>(st->C, lay.mu_x, lay.mu_y, lay.n,
+                                                                                     di, dout, lay.work);
     if ((s = cuda_check(cudaGetLastError(), "solve set-up launches")) != RF_OK) return s;
   }
   // H = L Lᵀ ; L^-1 ; H^-1 = L^-ᵀ L^-1  (planes_b is free until the product below)
@@ -1026,7 +1057,8 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
       return s;
   }
   const long long rows = static_cast<long long>(P) * dout;
-  k_bias<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, c.s>>>(A, lay.mu_x, lay.mu_y, rows, di, b);
+  k_split_mu<<<(di + 255) / 256, 256, 0, c.s>>>(lay.mu_x, di, lay.mu2);
+  k_bias<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, c.s>>>(A, lay.mu2, lay.mu_y, rows, di, b);
   if (A_bf16) k_to_bf16<<<eb, 256, 0, c.s>>>(A, rows * di, reinterpret_cast<__nv_bfloat16*>(A_bf16));
   return cuda_check(cudaGetLastError(), "solve tail launches");
 }
