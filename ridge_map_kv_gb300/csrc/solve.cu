@@ -169,9 +169,10 @@ constexpr size_t kBlkSmem = sizeof(float) * kSolveBlock * kBlkLd;
 // W = L^-1 for the 128 x 128 SPD block A = L Lᵀ, one CTA (8 warps) per matrix b
 // (A + b*sA, W + b*sW), in shared memory and blocked by 8 so that a column or row
 // block costs a few barriers instead of one per column:
-//   factor, per 8-column block k0:  warp 0 factors the 8 x 8 diagonal block
-//     (lanes own rows, warp-synchronous); one thread per row below solves its 8
-//     panel entries against it; the warps apply the rank-8 update to the trailing
+//   factor, per 8-column block k0:  warp 0 factors the 8 x 8 diagonal block in
+//     registers (lanes own rows, columns exchanged by shuffles) and keeps the
+//     pivots' reciprocals; one thread per row below solves its 8 panel entries
+//     against it (multiplying by those reciprocals); the warps apply the rank-8 update to the trailing
 //     lower triangle (warp w takes rows w, w+8, ..., lanes the columns);
 //   invert, per 8-row block i0 (rows above already hold W):
 //     T = L[i0 block][0:i0] W[0:i0][0:i0]  (all threads), and meanwhile warp 0
@@ -181,59 +182,77 @@ constexpr size_t kBlkSmem = sizeof(float) * kSolveBlock * kBlkLd;
 // RF_ERR_NOT_SPD and continues with 1.
 constexpr int kLeafN = 128;
 constexpr int kLeafB = 8;
-constexpr size_t kLeafSmem = kBlkSmem + sizeof(float) * (kLeafB * kLeafN + kLeafB * kLeafB);
+constexpr size_t kLeafSmem = kBlkSmem + sizeof(float) * (kLeafB * kLeafN + kLeafB * kLeafB + kLeafN);
 
-__global__ void __launch_bounds__(256) k_chol_inv_leaf(const float* __restrict__ A, long long lda, long long sA,
-                                                       float* __restrict__ W, long long ldw, long long sW,
-                                                       int32_t* dev_status) {
+template <int kWarps>
+__global__ void __launch_bounds__(32 * kWarps) k_chol_inv_leaf(const float* __restrict__ A, long long lda, long long sA,
+                                                               float* __restrict__ W, long long ldw, long long sW,
+                                                               int32_t* dev_status) {
+  constexpr int kThreads = 32 * kWarps;
   extern __shared__ float S[];
   float* Tb = S + kLeafN * kBlkLd;  // [8][128]
   float* Wd = Tb + kLeafB * kLeafN;  // [8][8]
+  float* Dinv = Wd + kLeafB * kLeafB;  // [128] 1 / L_jj
   constexpr int n = kLeafN;
   A += blockIdx.x * sA;
   W += blockIdx.x * sW;
   const int lane = threadIdx.x, warp = threadIdx.y, tid = warp * 32 + lane;
-  for (int i = warp; i < n; i += 8)
+  for (int i = warp; i < n; i += kWarps)
     for (int k = lane; k < n; k += 32) S[i * kBlkLd + k] = A[i * lda + k];
   __syncthreads();
   // ---- factor
   for (int k0 = 0; k0 < n; k0 += kLeafB) {
     if (warp == 0) {
+      // lane r < 8 holds row k0 + r of the block (lanes 8.. repeat lane 0 and store nothing)
+      const int rr = lane < kLeafB ? lane : 0;
+      float a[kLeafB];
+#pragma unroll
+      for (int c = 0; c < kLeafB; ++c) a[c] = S[(k0 + rr) * kBlkLd + k0 + c];
+      float my_inv = 1.f;
+#pragma unroll
       for (int j = 0; j < kLeafB; ++j) {
-        float d = S[(k0 + j) * kBlkLd + k0 + j];
+        float d = __shfl_sync(0xffffffffu, a[j], j);
         if (!(d > 0.f)) {
           if (lane == 0) record_status(dev_status, RF_ERR_NOT_SPD);
           d = 1.f;
         }
-        d = sqrtf(d);
-        __syncwarp();
-        if (lane == j) S[(k0 + j) * kBlkLd + k0 + j] = d;
-        if (lane > j && lane < kLeafB) S[(k0 + lane) * kBlkLd + k0 + j] /= d;
-        __syncwarp();
-        if (lane > j && lane < kLeafB) {
-          const float lrj = S[(k0 + lane) * kBlkLd + k0 + j];
-          for (int c = j + 1; c <= lane; ++c) S[(k0 + lane) * kBlkLd + k0 + c] -= lrj * S[(k0 + c) * kBlkLd + k0 + j];
+        const float sd = sqrtf(d), inv = __frcp_rn(sd);
+        if (rr == j) {
+          a[j] = sd;
+          my_inv = inv;
+        } else if (rr > j) {
+          a[j] *= inv;
         }
-        __syncwarp();
+#pragma unroll
+        for (int c = j + 1; c < kLeafB; ++c) {
+          const float lcj = __shfl_sync(0xffffffffu, a[j], c);
+          if (rr >= c) a[c] = fmaf(-a[j], lcj, a[c]);
+        }
+      }
+      if (lane < kLeafB) {
+#pragma unroll
+        for (int c = 0; c < kLeafB; ++c)
+          if (c <= lane) S[(k0 + lane) * kBlkLd + k0 + c] = a[c];
+        Dinv[k0 + lane] = my_inv;
       }
     }
     __syncthreads();
     // panel: row r solves x L_ddᵀ = S[r][k0..k0+7]
-    for (int r = k0 + kLeafB + tid; r < n; r += 256) {
+    for (int r = k0 + kLeafB + tid; r < n; r += kThreads) {
       float x[kLeafB];
 #pragma unroll
       for (int j = 0; j < kLeafB; ++j) {
         float v = S[r * kBlkLd + k0 + j];
 #pragma unroll
         for (int c = 0; c < j; ++c) v = fmaf(-x[c], S[(k0 + j) * kBlkLd + k0 + c], v);
-        x[j] = v / S[(k0 + j) * kBlkLd + k0 + j];
+        x[j] = v * Dinv[k0 + j];
       }
 #pragma unroll
       for (int j = 0; j < kLeafB; ++j) S[r * kBlkLd + k0 + j] = x[j];
     }
     __syncthreads();
     // trailing lower triangle, rank 8
-    for (int r = k0 + kLeafB + warp; r < n; r += 8) {
+    for (int r = k0 + kLeafB + warp; r < n; r += kWarps) {
       float a[kLeafB];
 #pragma unroll
       for (int j = 0; j < kLeafB; ++j) a[j] = S[r * kBlkLd + k0 + j];
@@ -248,7 +267,7 @@ __global__ void __launch_bounds__(256) k_chol_inv_leaf(const float* __restrict__
   }
   // ---- invert in place
   for (int i0 = 0; i0 < n; i0 += kLeafB) {
-    for (int e = tid; e < kLeafB * i0; e += 256) {
+    for (int e = tid; e < kLeafB * i0; e += kThreads) {
       const int r = e & (kLeafB - 1), c = e >> 3;
       float s0 = 0.f, s1 = 0.f;
       int k = c;
@@ -268,13 +287,13 @@ __global__ void __launch_bounds__(256) k_chol_inv_leaf(const float* __restrict__
 #pragma unroll
         for (int k = 0; k < r; ++k)
           if (k >= c) v = fmaf(-S[(i0 + r) * kBlkLd + i0 + k], col[k], v);
-        col[r] = r >= c ? v / S[(i0 + r) * kBlkLd + i0 + r] : 0.f;
+        col[r] = r >= c ? v * Dinv[i0 + r] : 0.f;
       }
 #pragma unroll
       for (int r = 0; r < kLeafB; ++r) Wd[r * kLeafB + c] = col[r];
     }
     __syncthreads();
-    for (int e = tid; e < kLeafB * i0; e += 256) {
+    for (int e = tid; e < kLeafB * i0; e += kThreads) {
       const int r = e & (kLeafB - 1), c = e >> 3;
       float v = 0.f;
 #pragma unroll
@@ -288,7 +307,7 @@ __global__ void __launch_bounds__(256) k_chol_inv_leaf(const float* __restrict__
     }
     __syncthreads();
   }
-  for (int i = warp; i < n; i += 8)
+  for (int i = warp; i < n; i += kWarps)
     for (int k = lane; k < n; k += 32) W[i * ldw + k] = k <= i ? S[i * kBlkLd + k] : 0.f;
 }
 
@@ -947,7 +966,7 @@ rf_status centre_system(const double* G, const double* sx, const double* sy, con
   return cuda_check(cudaGetLastError(), "centring launches");
 }
 
-static uint64_t g_leaf_attr = 0;
+static uint64_t g_leaf_attr = 0, g_leaf16_attr = 0;
 
 // Batched recursive factorisation: W = L^-1 of every n x n SPD matrix (n % 128 == 0),
 // splitting n = n1 + n2 at a multiple of 128 near n/2:
@@ -963,7 +982,12 @@ static rf_status chol_inv_rec(SolveCtx& c, float* A, long long lda, long long sA
                               long long sW, int n, int batch, float* tmp, long long stmp) {
   rf_status st;
   if (n == kLeafN) {
-    k_chol_inv_leaf<<<batch, dim3(32, 8), kLeafSmem, c.s>>>(A, lda, sA, W, ldw, sW, c.dev_status);
+    // A few leaves (the solve's single matrix) are a latency chain: 16 warps share
+    // each step's work. Many (the selection's batches) keep 8, for occupancy.
+    if (batch < c.sms)
+      k_chol_inv_leaf<16><<<batch, dim3(32, 16), kLeafSmem, c.s>>>(A, lda, sA, W, ldw, sW, c.dev_status);
+    else
+      k_chol_inv_leaf<8><<<batch, dim3(32, 8), kLeafSmem, c.s>>>(A, lda, sA, W, ldw, sW, c.dev_status);
     return cuda_check(cudaGetLastError(), "k_chol_inv_leaf launch");
   }
   const int n1 = split_point(n), n2 = n - n1;
@@ -987,8 +1011,10 @@ static rf_status chol_inv_rec(SolveCtx& c, float* A, long long lda, long long sA
 
 rf_status chol_inv_block(float* A, long long lda, long long sA, float* W, long long ldw, long long sW, int n, int batch,
                          float* tmp, long long stmp, int32_t* dev_status, int sms, cudaStream_t s) {
-  rf_status st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf), kLeafSmem, &g_leaf_attr);
+  rf_status st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf<8>), kLeafSmem, &g_leaf_attr);
   if (st != RF_OK) return st;
+  if ((st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf<16>), kLeafSmem, &g_leaf16_attr)) != RF_OK)
+    return st;
   SolveCtx c{s, sms, dev_status};
   return chol_inv_rec(c, A, lda, sA, W, ldw, sW, n, batch, tmp, stmp);
 }
