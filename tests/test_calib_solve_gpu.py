@@ -65,8 +65,9 @@ def _check_stats(st, ref, Yref_sq=None, rows=None, cols_x=None, cols_y=None):
         assert np.all(np.abs(C - ref["C"]) <= tolC), np.max(np.abs(C - ref["C"]) / tolC)
 
 
-@pytest.mark.parametrize("shape", [(256, 256, 4, 2048, [1000]), (512, 768, 3, 3000, []), (256, 512, 1, 100, [40])],
-                         ids=["toy two batches", "3 chunks ragged", "tiny ragged batches"])
+@pytest.mark.parametrize("shape", [(256, 256, 4, 2048, [1000]), (512, 768, 3, 3000, []), (256, 512, 1, 100, [40]),
+                                   (256, 512, 2, 40000, [])],
+                         ids=["toy two batches", "3 chunks ragged", "tiny ragged batches", "three slabs, ragged last"])
 @pytest.mark.parametrize("flags", [rf.RF_FLAG_SINGLE_CTA, rf.RF_FLAG_CTA_PAIR], ids=["single-cta", "cta-pair"])
 def test_calib_sums_match_oracle(shape, flags):
     d_in, d_out, P, n, splits = shape
