@@ -20,10 +20,14 @@
 //                           (hi·hi, mid·hi, hi·mid, lo·hi, mid·mid, hi·lo) are
 //                           summed over 1024-wide K chunks in TMEM, then in fp32
 //                           registers across chunks and terms
+//   k_centre_c              Cc_p = C_p − n μ_x μ_pᵀ (fp32, the product's operand)
 //   refinement (optional)   R_p = Cc_pᵀ − A_p H, fp64-accurate on the tensor cores
-//                           (OzakiProb: integer digit planes, exact chunk sums,
-//                           fp64 epilogue), A_p += R_p H^-1 (the split product)
-//   k_bias                  b_p = μ_p − A_p μ_x (compensated fp32 pairs, fp64 across lanes)
+//                           (k_oz_digits_*: integer digit planes; OzakiProb: exact
+//                           int32 sums per digit weight; k_oz_combine: their exact
+//                           int64 combination, one fp64 rounding), then
+//                           A_p += R_p H^-1 (the split product)
+//   k_bias                  b_p = μ_p − A_p μ_x (compensated fp32 pairs, fp64 across
+//                           lanes); k_to_bf16 the optional bf16 copy of A
 #include <algorithm>
 #include <cstring>
 
