@@ -51,6 +51,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-extras", action="store_true", help="skip timing the calibration, solve and cross-model rows")
     ap.add_argument("--extra", choices=EXTRA_ROWS, default=None,
                     help="time one row of the extras alone and print it (for short captures)")
+    ap.add_argument("--capture-size", action="store_true",
+                    help="with --extra: run a5_calibration with 4 maps and a7_xmodel with 12 -> 4 layers "
+                         "(same per-unit work, a few GB on the device, for a full ncu capture)")
     ap.add_argument("--selection-only", action="store_true",
                     help="time only the source-selection row (all-source calibration + greedy selection)")
     ap.add_argument("--select-targets", type=int, default=0,
@@ -282,7 +285,8 @@ def run_extra_only(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     peaks = measured_peaks()
-    print(json.dumps(run_extras(dev, peaks["bf16_tflops"], gemm_flags(args.gemm), only=args.extra)))
+    print(json.dumps(run_extras(dev, peaks["bf16_tflops"], gemm_flags(args.gemm), only=args.extra,
+                                capture=args.capture_size)))
 
 
 def run_selection_only(args):
@@ -526,11 +530,13 @@ EXTRA_ROWS = ("a5_calibration", "a5_calibration_xmodel", "a6_solve", "a7_xmodel"
               "next4a_source_selection_xmodel")
 
 
-def run_extras(dev, peak_tflops, flags=0, only=None):
+def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
     """The other rows of the path, each timed with CUDA events at its workload's
     size: calibration (27B shape, and the cross-model Gram), the ridge solve (8B
     shape, 20 maps), the cross-model mapper (40 -> 64 layers, N = 32768), the NEXT
-    rows and the source selection. `only` names one row (EXTRA_ROWS) to run alone."""
+    rows and the source selection. `only` names one row (EXTRA_ROWS) to run alone.
+    `capture` shrinks the 27B calibration to 4 maps and the mapper to 12 -> 4
+    layers: the same units at a size a full ncu capture can save and restore."""
     import torch
 
     import ridge_map_kv_gb300 as rf
@@ -541,7 +547,7 @@ def run_extras(dev, peak_tflops, flags=0, only=None):
     if only in (None, "a5_calibration"):
         # a5: calibration statistics, 27B-shaped: XᵀX and XᵀY_l for 48 maps over 16,384 rows
         c = synth.DENSE27B
-        d, P, n = c.d, c.P, c.calib_n
+        d, P, n = c.d, (4 if capture else c.P), c.calib_n
         cal = synth.calib_inputs(d, d, P, n, index=c.index, device=dev)
         st = _zero_stats(d, d, P, dev)
         cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
@@ -618,6 +624,8 @@ def run_extras(dev, peak_tflops, flags=0, only=None):
     if only in (None, "a7_xmodel"):
         # a7: cross-model mapper, 40 -> 64 layers, k = 8, 8 x 128 heads, N = 32768
         x = synth.XMODEL
+        if capture:
+            x = dataclasses.replace(x, name="xmodel 12->4 layers 8x128 k8 N32768 (capture size)", L_src=12, L_tgt=4)
         inp = synth.xmodel_inputs(x, device=dev)
         xd = rf.rf_xmodel_desc(L_src=x.L_src, L_tgt=x.L_tgt, k=x.k, n_kv_heads=x.H, head_dim=x.hd, N=x.N,
                                theta_src=x.theta_src, theta_tgt=x.theta_tgt, pos_offset=0, flags=flags)
