@@ -20,7 +20,8 @@
 //                           (hi·hi, mid·hi, hi·mid, lo·hi, mid·mid, hi·lo) are
 //                           summed over 1024-wide K chunks in TMEM, then in fp32
 //                           registers across chunks and terms
-//   k_centre_c              Cc_p = C_p − n μ_x μ_pᵀ (fp32, the product's operand)
+//   k_centre_split_t        Cc_p = C_p − n μ_x μ_pᵀ, written transposed as the product's
+//                           three bf16 planes
 //   refinement (optional)   R_p = Cc_pᵀ − A_p H, fp64-accurate on the tensor cores
 //                           (k_oz_digits_*: integer digit planes; OzakiProb: exact
 //                           int32 sums per digit weight; k_oz_combine: their exact
@@ -374,18 +375,33 @@ __global__ void __launch_bounds__(256) k_build_h(const double* __restrict__ G, c
   }
 }
 
-// Cc32[p][i][o] = C[p][i][o] − n μ_x[i] μ_p[o], one (p, i) row per block x: one
-// fp64 fma per element (GB300's fp64 rate is low, so no per-element index division).
-__global__ void __launch_bounds__(256) k_centre_c(const double* __restrict__ C, const double* __restrict__ mu_x,
-                                                  const double* __restrict__ mu_y, const double* __restrict__ n,
-                                                  int d_in, int d_out, float* __restrict__ Cc) {
-  const long long row = blockIdx.x;  // p * d_in + i
-  const int p = static_cast<int>(row / d_in), i = static_cast<int>(row - static_cast<long long>(p) * d_in);
-  const double a = -(*n) * mu_x[i];
-  const double* c = C + row * d_out;
-  const double* my = mu_y + static_cast<long long>(p) * d_out;
-  float* out = Cc + row * d_out;
-  for (int o = threadIdx.x; o < d_out; o += blockDim.x) out[o] = static_cast<float>(fma(a, my[o], c[o]));
+// Cc_p = C_p − n μ_x μ_pᵀ, transposed and split into the product's A operand:
+// planes [3][P][d_out][d_in] (K-major), straight from the fp64 sums through a
+// 32 x 32 tile. One fp64 fma per element (GB300's fp64 rate is low): the row
+// factors −n μ_x[i] are formed once per tile. Grid (d_in/32, d_out/32, P), 32 x 8.
+__global__ void __launch_bounds__(256) k_centre_split_t(const double* __restrict__ C, const double* __restrict__ mu_x,
+                                                        const double* __restrict__ mu_y, const double* __restrict__ n,
+                                                        int d_in, int d_out, __nv_bfloat16* __restrict__ planes,
+                                                        size_t plane) {
+  __shared__ float t[32][33];
+  __shared__ double a[32];
+  const int p = blockIdx.z, i0 = blockIdx.x * 32, o0 = blockIdx.y * 32;
+  if (threadIdx.y == 0) a[threadIdx.x] = -(*n) * mu_x[i0 + threadIdx.x];
+  __syncthreads();
+  const double* Cp = C + static_cast<size_t>(p) * d_in * d_out;
+  const double my = mu_y[static_cast<size_t>(p) * d_out + o0 + threadIdx.x];
+  for (int j = threadIdx.y; j < 32; j += 8)  // t[j][x] = Cc[i0 + j][o0 + x]
+    t[j][threadIdx.x] = static_cast<float>(fma(a[j], my, Cp[static_cast<size_t>(i0 + j) * d_out + o0 + threadIdx.x]));
+  __syncthreads();
+  __nv_bfloat16* out = planes + static_cast<size_t>(p) * d_out * d_in;
+  for (int j = threadIdx.y; j < 32; j += 8) {  // element (o0 + j, i0 + x) = t[x][j]
+    __nv_bfloat16 h, m, l;
+    split3(t[threadIdx.x][j], h, m, l);
+    const size_t o = static_cast<size_t>(o0 + j) * d_in + i0 + threadIdx.x;
+    out[o] = h;
+    out[plane + o] = m;
+    out[2 * plane + o] = l;
+  }
 }
 
 // μ_x as an unevaluated pair of floats, hi + lo (|lo| <= 2^-24 |hi|), for k_bias.
@@ -478,27 +494,6 @@ __global__ void __launch_bounds__(256) k_split3(const float* __restrict__ src, _
     *reinterpret_cast<uint2*>(planes + 4 * i) = *reinterpret_cast<const uint2*>(h);
     *reinterpret_cast<uint2*>(planes + plane + 4 * i) = *reinterpret_cast<const uint2*>(m);
     *reinterpret_cast<uint2*>(planes + 2 * plane + 4 * i) = *reinterpret_cast<const uint2*>(l);
-  }
-}
-
-// Transposed copy through a 32 x 32 shared tile: out rows r < R, columns c < Cn
-// of matrix p read src[p][c][r]. Grid (Cn/32, R/32, P), 32 x 8 threads.
-__global__ void __launch_bounds__(256) k_split3_t(const float* __restrict__ src, __nv_bfloat16* __restrict__ planes,
-                                                  int R, int Cn, size_t plane) {
-  __shared__ float t[32][33];
-  const int p = blockIdx.z;
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  const float* s = src + static_cast<size_t>(p) * R * Cn;
-  for (int j = threadIdx.y; j < 32; j += 8) t[j][threadIdx.x] = s[static_cast<size_t>(c0 + j) * R + r0 + threadIdx.x];
-  __syncthreads();
-  __nv_bfloat16* out = planes + static_cast<size_t>(p) * R * Cn;
-  for (int j = threadIdx.y; j < 32; j += 8) {
-    __nv_bfloat16 h, m, l;
-    split3(t[threadIdx.x][j], h, m, l);
-    const size_t o = static_cast<size_t>(r0 + j) * Cn + c0 + threadIdx.x;
-    out[o] = h;
-    out[plane + o] = m;
-    out[2 * plane + o] = l;
   }
 }
 
@@ -599,16 +594,13 @@ struct Split3Prob {
 // out_p = alpha A_p B + beta out_p with A_p [M][K] read from `a` ([P][M][K], or
 // its transpose [P][K][M] when a_tr) and B [K][N] symmetric (its rows serve as
 // Bᵀ), through the split planes in `planes_a` (3·P·M·K) and `planes_b` (3·N·K).
-static rf_status split_gemm(SolveCtx& c, const float* a, bool a_tr, const float* Bsym, int P, int M, int N, int K,
-                            float alpha, float beta, float* out, __nv_bfloat16* planes_a, __nv_bfloat16* planes_b) {
+// A_p is fp32 [P][M][K], split here, or null when planes_a already hold its planes.
+static rf_status split_gemm(SolveCtx& c, const float* a, const float* Bsym, int P, int M, int N, int K, float alpha,
+                            float beta, float* out, __nv_bfloat16* planes_a, __nv_bfloat16* planes_b) {
   rf_status st;
   const size_t pa = static_cast<size_t>(P) * M * K, pb = static_cast<size_t>(N) * K;
   const unsigned eb = static_cast<unsigned>(8 * c.sms);
-  if (a_tr) {
-    k_split3_t<<<dim3(K / 32, M / 32, P), dim3(32, 8), 0, c.s>>>(a, planes_a, M, K, pa);
-  } else {
-    k_split3<<<eb, 256, 0, c.s>>>(a, planes_a, pa / 4, pa);
-  }
+  if (a != nullptr) k_split3<<<eb, 256, 0, c.s>>>(a, planes_a, pa / 4, pa);
   k_split3<<<eb, 256, 0, c.s>>>(Bsym, planes_b, pb / 4, pb);
   if ((st = cuda_check(cudaGetLastError(), "split launches")) != RF_OK) return st;
   Split3Prob<true> pr;
@@ -861,7 +853,7 @@ struct SolveLayout {
   float* Linv;
   float* Hinv;
   float* tmp;   // [d_in/2][d_in/2] scratch of the factorisation
-  float* work;  // Cc (first solve) then R (refinement), [P][d_in][d_out] floats
+  float* work;  // R (refinement), [P][d_out][d_in] floats
   __nv_bfloat16* planes_a;  // [3][P][d_out][d_in] bf16 split of Cc_pᵀ or R_p
   __nv_bfloat16* planes_b;  // [3][d_in][d_in] bf16 split of H^-1
   __nv_bfloat16* ozH;       // [kOzDigits][d_in][d_in] digits of H's rows (refinement)
@@ -1061,19 +1053,19 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
     k_means<<<eb, 256, 0, c.s>>>(st->sx, st->sy, st->n, di, static_cast<long long>(P) * dout, lay.mu_x, lay.mu_y, lay.n);
     k_trace_alpha<<<1, 1024, 0, c.s>>>(st->G, lay.mu_x, lay.n, di, lambda, alpha_mode, lay.alpha, alpha_out);
     k_build_h<<<dim3(di / 32, di / 32), dim3(32, 8), 0, c.s>>>(st->G, lay.mu_x, lay.n, lay.alpha, di, lay.H64, lay.L);
-    k_centre_c<<<static_cast<unsigned>(static_cast<long long>(P) * di), 256, 0, c.s>>>(st->C, lay.mu_x, lay.mu_y, lay.n,
-                                                                                     di, dout, lay.work);
+    k_centre_split_t<<<dim3(di / 32, dout / 32, P), dim3(32, 8), 0, c.s>>>(
+        st->C, lay.mu_x, lay.mu_y, lay.n, di, dout, lay.planes_a, static_cast<size_t>(P) * dout * di);
     if ((s = cuda_check(cudaGetLastError(), "solve set-up launches")) != RF_OK) return s;
   }
   // H = L Lᵀ ; L^-1 ; H^-1 = L^-ᵀ L^-1  (planes_b is free until the product below)
   if ((s = spd_inverse(lay.L, di, lay.Linv, lay.Hinv, lay.tmp, lay.planes_b, use_pair(desc->flags, true), dev_status,
                        sms, c.s)) != RF_OK)
     return s;
-  // A_p = Cc_pᵀ H^-1  (Cc_p stored [d_in][d_out]); H^-1 is exactly symmetric (its
-  // lower triangle mirrors the upper), so its rows serve as the B operand.
+  // A_p = Cc_pᵀ H^-1 (Cc_pᵀ's planes written by k_centre_split_t); H^-1 is exactly
+  // symmetric (its lower triangle mirrors the upper), so its rows serve as the B operand.
   {
     ProfScope pp(c.s, RF_STAGE_SOLVE_PRODUCT);
-    if ((s = split_gemm(c, lay.work, true, lay.Hinv, P, dout, di, di, 1.f, 0.f, A, lay.planes_a, lay.planes_b)) !=
+    if ((s = split_gemm(c, nullptr, lay.Hinv, P, dout, di, di, 1.f, 0.f, A, lay.planes_a, lay.planes_b)) !=
         RF_OK)
       return s;
   }
@@ -1082,7 +1074,7 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
     s = use_pair(desc->flags, true) ? oz_residual<true>(c, lay, st->C, A, P, di, dout, lay.work)
                                     : oz_residual<false>(c, lay, st->C, A, P, di, dout, lay.work);
     if (s != RF_OK) return s;
-    if ((s = split_gemm(c, lay.work, false, lay.Hinv, P, dout, di, di, 1.f, 1.f, A, lay.planes_a, lay.planes_b)) !=
+    if ((s = split_gemm(c, lay.work, lay.Hinv, P, dout, di, di, 1.f, 1.f, A, lay.planes_a, lay.planes_b)) !=
         RF_OK)
       return s;
   }
