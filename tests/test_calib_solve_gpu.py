@@ -109,9 +109,56 @@ def test_calib_full_width_sampled(d_in, d_out, P, n, flags):
     _check_stats(st, ref, (Ys ** 2).sum(axis=1) if P else None, cols_x=cx, cols_y=cy)
 
 
+def test_calib_zero_rows_leaves_the_sums_unchanged():
+    """n_rows = 0 is a valid call that adds nothing: every sum stays bit for bit."""
+    cal = synth.calib_inputs(256, 256, 2, 512, index=93)
+    X, Y = cal["X"].to(DEV), cal["Y"].to(DEV)
+    st = _zeros_stats(256, 256, 2)
+    _accumulate(X, Y, st, [])
+    before = {k: v.clone() for k, v in st.items()}
+    desc = rf.rf_calib_desc(d_in=256, d_out=256, n_maps=2)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rf.rf_calib_accumulate(desc, X, 256, Y, 256, 512 * 256, 0, _struct(st), status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for k in st:
+        assert torch.equal(st[k], before[k]), k
+
+
 # --------------------------------------------------------------------------- #
 # Solve
 # --------------------------------------------------------------------------- #
+def test_solve_reports_a_non_positive_pivot():
+    """Sums whose centred Gram has a negative eigenvalue (no rows give that, but a
+    caller can pass any sums) make the fp32 Cholesky meet a pivot <= 0: the call
+    returns RF_OK, RF_ERR_NOT_SPD lands in the status word, and the context
+    stays usable (a well-posed solve follows in the same process)."""
+    d, P = 256, 1
+    G = np.eye(d)
+    G[100, 100] = -1.0
+    rng = np.random.default_rng(4)
+    st = {"G": torch.as_tensor(G, device=DEV), "C": torch.as_tensor(rng.standard_normal((P, d, d)), device=DEV),
+          "sx": torch.zeros(d, dtype=torch.float64, device=DEV),
+          "sy": torch.zeros((P, d), dtype=torch.float64, device=DEV),
+          "n": torch.tensor([10], dtype=torch.int64, device=DEV)}
+    desc = rf.rf_calib_desc(d_in=d, d_out=d, n_maps=P)
+    A = torch.empty((P, d, d), dtype=torch.float32, device=DEV)
+    b = torch.empty((P, d), dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    wsb = rf.rf_solve_workspace_bytes(desc)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    rf.rf_solve(desc, _struct(st), 0.0, rf.RF_ALPHA_TRACE, 0, A, b, None, None, status, ws, wsb)
+    torch.cuda.synchronize()
+    assert int(status.item()) == rf.RF_ERR_NOT_SPD
+    # the same process solves a well-posed system afterwards
+    cal = synth.calib_inputs(256, 256, 2, 2048, index=0)
+    ref = O.calib_stats(_f64(cal["X"]), _f64(cal["Y"]))
+    A2, _, _, _ = _solve(_upload_stats(ref), 256, 256, 2, 0.03)
+    Ar, _, _ = O.ridge_solve(ref, 0.03)
+    assert max(_rel(A2[p], Ar[p]) for p in range(2)) <= 1e-5
+
+
+
 def _upload_stats(ref):
     P = ref["C"].shape[0]
     return {"G": torch.as_tensor(ref["G"], device=DEV), "C": torch.as_tensor(ref["C"], device=DEV),
