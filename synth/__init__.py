@@ -164,7 +164,7 @@ _TENSOR_IDS = {name: i for i, name in enumerate(
     ["x_S", "mask", "A", "b", "gain", "Wk", "Wv", "calib_X", "calib_Atrue", "calib_btrue",
      "calib_noise", "k_src", "v_src", "xWk", "xWv", "xbk", "xbv", "cache", "extra",
      "rescale_scale", "rescale_noise", "key_norm_gain", "sel_P", "sel_M", "sel_mu", "sel_latent",
-     "sel_noise"])}
+     "sel_noise", "fit_perm", "fit_Mk", "fit_Mv", "fit_noise"])}
 
 
 def sub_seed(index: int, tensor: str, salt: int = 0) -> int:
@@ -315,6 +315,40 @@ def xmodel_inputs(cfg: XModelConfig, device="cpu", L_tgt: Optional[int] = None,
         "bv": _randn((L_t, KV), sub_seed(ix, "xbv"), device, std=0.1, dtype=torch.float32),
         "src": source_table(cfg.L_src, cfg.L_tgt, cfg.k)[:L_t].copy(),
     }
+
+
+# A model pair for an end-to-end mapper fit: 6 source and 3 target layers of 2 x 128
+# heads, k = 2, 4,096 rows, different RoPE bases on the two sides.
+MAPPER_FIT = XModelConfig("mapper fit 6->3 layers 2x128 k2 N4096", 8, L_src=6, L_tgt=3, k=2, H=2, hd=128, N=4096,
+                          theta_src=1.0e6, theta_tgt=5.0e5, calib_n=4096, lam=0.01)
+
+
+def mapper_fit_caches(cfg: XModelConfig, device="cpu") -> dict:
+    """Source and target caches [L, N, H, hd] bf16 for a mapper fit with planted
+    sources: source K, V ~ N(0, 1); target layer t's K (V) is the sum over its
+    planted source layers j = 0..k-1 of the source cache rows times w_j M_{t,j},
+    M ~ N(0, 1/KV) and w_j falling from 1 to 0.6 (so every greedy step has a clear
+    best layer), plus 0.1 N(0, 1). The planted sets (disjoint, k layers each, in
+    order of weight, from a seeded permutation of the source layers; needs
+    L_tgt k <= L_src) are returned too."""
+    L, T, k, KV, ix = cfg.L_src, cfg.L_tgt, cfg.k, cfg.KV, cfg.index
+    assert T * k <= L
+    g = _gen("cpu", sub_seed(ix, "fit_perm"))
+    perm = torch.randperm(L, generator=g).numpy()
+    plant = perm[:T * k].reshape(T, k).astype(np.int32)
+    ks = _randn((L, cfg.N, cfg.H, cfg.hd), sub_seed(ix, "k_src"), device)
+    vs = _randn((L, cfg.N, cfg.H, cfg.hd), sub_seed(ix, "v_src"), device)
+    out = {"k_src": ks, "v_src": vs, "plant": plant}
+    for name, src, mix in (("k_tgt", ks, "fit_Mk"), ("v_tgt", vs, "fit_Mv")):
+        M = _randn((T, k, KV, KV), sub_seed(ix, mix), device, std=1.0 / math.sqrt(KV), dtype=torch.float32)
+        tgt = _randn((T, cfg.N, KV), sub_seed(ix, "fit_noise", 0 if name == "k_tgt" else 1), device, std=0.1,
+                     dtype=torch.float32)
+        for t in range(T):
+            for j in range(k):
+                w = 1.0 - 0.4 * j / max(k - 1, 1)
+                tgt[t] += src[int(plant[t, j])].reshape(cfg.N, KV).float() @ (w * M[t, j])
+        out[name] = tgt.to(torch.bfloat16).reshape(T, cfg.N, cfg.H, cfg.hd)
+    return out
 
 
 def canary_cache(L: int, N_cap: int, H: int, hd: int, kind: int, device="cpu") -> torch.Tensor:

@@ -1,0 +1,152 @@
+"""End-to-end fit of the cross-model mapper on the GPU against the same pipeline
+in the fp64 oracle ([XM] "층 교차 소스 선택", "헤드별 리지 회귀", and the
+content-space mapping equation):
+
+  1. the un-roped source keys and the values of every source layer side by side
+     (rf_concat_layers), and the un-roped target keys (rf_rope_rows);
+  2. the calibration sums over all source layers (rf_calib_accumulate, with Σy²);
+  3. greedy source selection by head-mean R² of keys and values (rf_select_sources);
+  4. for every target layer, the ridge fit of its keys and its values on the
+     chosen layers' features (rf_calib_accumulate + rf_solve, weights in bf16);
+  5. the mapping itself (rf_xmodel_map).
+
+The oracle runs the same five steps in fp64 from the same caches. Planted sources
+(synth.mapper_fit_caches) give every greedy step a clear winner, so both sides must
+choose the planted layers in order of weight.
+
+Tolerance on the mapped heads: the GPU chain rounds to bf16 four times (the
+un-roped source features, the un-roped targets, the fitted weights, the output),
+each adding about 2^-9/sqrt(3) = 1.1e-3 RMS relative error, so about 2.3e-3 per
+head together. The fit's Gram (independent N(0, 1) features) is well conditioned,
+so its response to the rounding of its inputs is of the same order: mean <= 5e-3.
+A head's error is an RMS over its 128 values, so it stays within a small factor of
+the mean: max <= 1e-2. (Measured on a GB300: mean 2.3e-3 for values, 3.2e-3 for
+keys, whose fit explains less; max 4.3e-3.)
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import ridge_map_kv_gb300 as rf
+import synth
+from fillcheck import head_errors
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+CFG = synth.MAPPER_FIT
+TOL_MEAN, TOL_MAX = 5e-3, 1e-2
+
+
+def _stats(D, F, T):
+    return {"G": torch.zeros((D, D), dtype=torch.float64, device=DEV),
+            "C": torch.zeros((T, D, F), dtype=torch.float64, device=DEV),
+            "sx": torch.zeros(D, dtype=torch.float64, device=DEV),
+            "sy": torch.zeros((T, F), dtype=torch.float64, device=DEV),
+            "syy": torch.zeros((T, F), dtype=torch.float64, device=DEV),
+            "n": torch.zeros(1, dtype=torch.int64, device=DEV)}
+
+
+def _struct(st):
+    return rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"], st["syy"])
+
+
+def _gpu_fit(caches):
+    c = CFG
+    N, L, T, k, H, hd, KV = c.N, c.L_src, c.L_tgt, c.k, c.H, c.hd, c.KV
+    D = L * KV
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ks, vs = caches["k_src"].to(DEV), caches["v_src"].to(DEV)
+    kt, vt = caches["k_tgt"].to(DEV), caches["v_tgt"].to(DEV)
+    # 1. features and targets
+    Xk = torch.empty((N, D), dtype=torch.bfloat16, device=DEV)
+    Xv = torch.empty_like(Xk)
+    rf.rf_concat_layers(ks, L, N * KV, N, KV, H, hd, c.theta_src, 0, Xk, D)
+    rf.rf_concat_layers(vs, L, N * KV, N, KV, H, hd, 0.0, 0, Xv, D)
+    Yk = torch.empty((T, N, KV), dtype=torch.bfloat16, device=DEV)
+    for t in range(T):
+        rf.rf_rope_rows(kt[t], Yk[t], N, KV, H, hd, c.theta_tgt, 0, inverse=True)
+    Yv = vt.reshape(T, N, KV)
+    # 2. sums over all source layers
+    cd = rf.rf_calib_desc(d_in=D, d_out=KV, n_maps=T)
+    stk, stv = _stats(D, KV, T), _stats(D, KV, T)
+    rf.rf_calib_accumulate(cd, Xk, D, Yk, KV, N * KV, N, _struct(stk), status)
+    rf.rf_calib_accumulate(cd, Xv, D, Yv, KV, N * KV, N, _struct(stv), status)
+    # 3. selection
+    sd = rf.rf_select_desc(L_src=L, F=KV, n_targets=T, d_out=KV, head_dim=hd, k=k, n_kinds=2, group=0, flags=0)
+    swb = rf.rf_select_workspace_bytes(sd)
+    sws = torch.empty(swb, dtype=torch.uint8, device=DEV)
+    sel = torch.full((T, k), -1, dtype=torch.int32, device=DEV)
+    rf.rf_select_sources(sd, [_struct(stk), _struct(stv)], c.lam, rf.RF_ALPHA_TRACE, sel, None, status, sws, swb)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sel_h = sel.cpu().numpy()
+    # 4. one ridge fit per target layer and kind, on the chosen layers' features
+    Wk = torch.empty((T, KV, k * KV), dtype=torch.bfloat16, device=DEV)
+    Wv = torch.empty_like(Wk)
+    bk = torch.empty((T, KV), dtype=torch.float32, device=DEV)
+    bv = torch.empty_like(bk)
+    fd = rf.rf_calib_desc(d_in=k * KV, d_out=KV, n_maps=1)
+    fwb = rf.rf_solve_workspace_bytes(fd)
+    fws = torch.empty(fwb, dtype=torch.uint8, device=DEV)
+    A = torch.empty((1, KV, k * KV), dtype=torch.float32, device=DEV)
+    b = torch.empty((1, KV), dtype=torch.float32, device=DEV)
+    for t in range(T):
+        for X_all, Y, W, bias in ((Xk, Yk, Wk, bk), (Xv, Yv, Wv, bv)):
+            Xt = torch.cat([X_all[:, j * KV:(j + 1) * KV] for j in sel_h[t]], dim=1).contiguous()
+            st = _stats(k * KV, KV, 1)
+            rf.rf_calib_accumulate(fd, Xt, k * KV, Y[t:t + 1], KV, N * KV, N, _struct(st), status)
+            rf.rf_solve(fd, _struct(st), c.lam, rf.RF_ALPHA_TRACE, 1, A, b, W[t:t + 1], None, status, fws, fwb)
+            bias[t] = b[0]
+            torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    # 5. the mapping
+    xd = rf.rf_xmodel_desc(L_src=L, L_tgt=T, k=k, n_kv_heads=H, head_dim=hd, N=N, theta_src=c.theta_src,
+                           theta_tgt=c.theta_tgt, pos_offset=0, flags=0)
+    xwb = rf.rf_xmodel_workspace_bytes(xd)
+    xws = torch.empty(xwb, dtype=torch.uint8, device=DEV)
+    out_k = torch.empty((T, N, H, hd), dtype=torch.bfloat16, device=DEV)
+    out_v = torch.empty_like(out_k)
+    rf.rf_xmodel_map(xd, sel_h, ks, vs, Wk, bk, Wv, bv, out_k, out_v, status, xws, xwb)  # host table
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return sel_h, out_k, out_v
+
+
+def _oracle_fit(caches, rows):
+    c = CFG
+    N, L, T, k, KV = c.N, c.L_src, c.L_tgt, c.k, c.KV
+    f64 = lambda t: O.bf16_bits_to_f64(synth.bits(t))  # noqa: E731
+    ks, vs, kt, vt = f64(caches["k_src"]), f64(caches["v_src"]), f64(caches["k_tgt"]), f64(caches["v_tgt"])
+    pos = np.arange(N)
+    Xk = O.xmodel_features(ks, range(L), pos, c.theta_src)
+    Xv = O.xmodel_features(vs, range(L), pos, None)
+    Yk = np.stack([O.rope(kt[t], pos[:, None], c.theta_tgt, inverse=True).reshape(N, KV) for t in range(T)])
+    Yv = vt.reshape(T, N, KV)
+    sel, _ = O.select_sources([O.calib_stats(Xk, Yk), O.calib_stats(Xv, Yv)], L, KV, c.hd, k, c.lam, "trace")
+    outs = []
+    for t in range(T):
+        fits = []
+        for src, Y, theta in ((ks, Yk, c.theta_src), (vs, Yv, None)):
+            A, b, _ = O.ridge_solve(O.calib_stats(O.xmodel_features(src, sel[t], pos, theta), Y[t][None]), c.lam)
+            fits += [A[0], b[0]]
+        outs.append(O.xmodel_map_layer(ks[:, rows], vs[:, rows], list(sel[t]), fits[0], fits[1], fits[2], fits[3],
+                                       rows, c.theta_src, c.theta_tgt, c.H, c.hd))
+    return sel, outs
+
+
+def test_mapper_fit_end_to_end_matches_oracle():
+    caches = synth.mapper_fit_caches(CFG)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, CFG.N - 1],
+                                     np.random.default_rng(8).choice(CFG.N, 123, replace=False)]))
+    sel, out_k, out_v = _gpu_fit(caches)
+    osel, outs = _oracle_fit(caches, rows)
+    np.testing.assert_array_equal(osel, caches["plant"])    # the planted layers, in order of weight
+    np.testing.assert_array_equal(sel, osel)
+    rt = torch.as_tensor(rows, device=DEV)
+    errs = []
+    for t, (K, V) in enumerate(outs):
+        errs.append(head_errors(synth.bits(out_k[t].index_select(0, rt)), K).ravel())
+        errs.append(head_errors(synth.bits(out_v[t].index_select(0, rt)), V).ravel())
+    e = np.concatenate(errs)
+    assert np.all(np.isfinite(e)) and e.max() <= TOL_MAX and e.mean() <= TOL_MEAN, (e.max(), e.mean())
