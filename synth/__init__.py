@@ -24,6 +24,10 @@ Recipe (one per workload):
     so nearby layers carry most of a target and far ones a little; keys and values
     share the walk and draw their own loadings. Raw rows are drawn from this
     model; the full-size case uses its exact population sums instead.
+  * mapper fit (6 -> 3 layers): source K, V ~ N(0, 1); each target layer's K (V)
+    is a sum over k planted source layers (disjoint sets from a seeded
+    permutation) of the source cache rows times w_j M, M ~ N(0, 1/KV), w_j from 1
+    to 0.6, plus 0.1 N(0, 1).
 Seeds: base = 20261202 + workload index; one sub-seed per named tensor.
 """
 from __future__ import annotations
