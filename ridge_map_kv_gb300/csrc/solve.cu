@@ -171,14 +171,16 @@ __global__ void __launch_bounds__(256) k_sgemm(int M, int N, int K, float alpha,
 constexpr int kBlkLd = kSolveBlock + 1;
 constexpr size_t kBlkSmem = sizeof(float) * kSolveBlock * kBlkLd;
 
-// W = L^-1 for the 128 x 128 SPD block A = L Lᵀ, one CTA (8 warps) per matrix b
+// W = L^-1 for the 128 x 128 SPD block A = L Lᵀ, one CTA (8 or 16 warps) per matrix b
 // (A + b*sA, W + b*sW), in shared memory and blocked by 8 so that a column or row
 // block costs a few barriers instead of one per column:
-//   factor, per 8-column block k0:  warp 0 factors the 8 x 8 diagonal block in
-//     registers (lanes own rows, columns exchanged by shuffles) and keeps the
-//     pivots' reciprocals; one thread per row below solves its 8 panel entries
-//     against it (multiplying by those reciprocals); the warps apply the rank-8 update to the trailing
-//     lower triangle (warp w takes rows w, w+8, ..., lanes the columns);
+//   factor, per 8-column block k0: one thread per row below the diagonal block
+//     solves its 8 panel entries against it (multiplying by the pivots'
+//     reciprocals); then warp 0 applies that panel's rank-8 update to the next
+//     diagonal block and factors it in registers (lanes own rows, columns
+//     exchanged by shuffles), while the other warps update the rows below it
+//     (warp w takes rows w−1, w−1 + (warps − 1), ..., lanes the columns): two
+//     barriers a block, and the serial factorisation off the critical path;
 //   invert, per 8-row block i0 (rows above already hold W):
 //     T = L[i0 block][0:i0] W[0:i0][0:i0]  (all threads), and meanwhile warp 0
 //     inverts the diagonal block (lane c forms column c by forward substitution);
@@ -206,42 +208,58 @@ __global__ void __launch_bounds__(32 * kWarps) k_chol_inv_leaf(const float* __re
     for (int k = lane; k < n; k += 32) S[i * kBlkLd + k] = A[i * lda + k];
   __syncthreads();
   // ---- factor
-  for (int k0 = 0; k0 < n; k0 += kLeafB) {
-    if (warp == 0) {
-      // lane r < 8 holds row k0 + r of the block (lanes 8.. repeat lane 0 and store nothing)
-      const int rr = lane < kLeafB ? lane : 0;
-      float a[kLeafB];
+  // Warp 0 factors the diagonal block at kd in registers (lane r < 8 holds row kd + r;
+  // lanes 8.. repeat lane 0 and store nothing). With `update` it first applies the
+  // previous panel's rank-8 update to the block, which the other warps skip.
+  auto factor_diag = [&](int kd, bool update) {
+    const int rr = lane < kLeafB ? lane : 0;
+    float a[kLeafB];
 #pragma unroll
-      for (int c = 0; c < kLeafB; ++c) a[c] = S[(k0 + rr) * kBlkLd + k0 + c];
-      float my_inv = 1.f;
+    for (int c = 0; c < kLeafB; ++c) a[c] = S[(kd + rr) * kBlkLd + kd + c];
+    if (update) {
+      const int kp = kd - kLeafB;
+      float pr[kLeafB];
 #pragma unroll
-      for (int j = 0; j < kLeafB; ++j) {
-        float d = __shfl_sync(0xffffffffu, a[j], j);
-        if (!(d > 0.f)) {
-          if (lane == 0) record_status(dev_status, RF_ERR_NOT_SPD);
-          d = 1.f;
-        }
-        const float sd = sqrtf(d), inv = __frcp_rn(sd);
-        if (rr == j) {
-          a[j] = sd;
-          my_inv = inv;
-        } else if (rr > j) {
-          a[j] *= inv;
-        }
+      for (int j = 0; j < kLeafB; ++j) pr[j] = S[(kd + rr) * kBlkLd + kp + j];
 #pragma unroll
-        for (int c = j + 1; c < kLeafB; ++c) {
-          const float lcj = __shfl_sync(0xffffffffu, a[j], c);
-          if (rr >= c) a[c] = fmaf(-a[j], lcj, a[c]);
-        }
-      }
-      if (lane < kLeafB) {
+      for (int c = 0; c < kLeafB; ++c) {
+        float v = a[c];
 #pragma unroll
-        for (int c = 0; c < kLeafB; ++c)
-          if (c <= lane) S[(k0 + lane) * kBlkLd + k0 + c] = a[c];
-        Dinv[k0 + lane] = my_inv;
+        for (int j = 0; j < kLeafB; ++j) v = fmaf(-pr[j], S[(kd + c) * kBlkLd + kp + j], v);
+        a[c] = v;
       }
     }
-    __syncthreads();
+    float my_inv = 1.f;
+#pragma unroll
+    for (int j = 0; j < kLeafB; ++j) {
+      float d = __shfl_sync(0xffffffffu, a[j], j);
+      if (!(d > 0.f)) {
+        if (lane == 0) record_status(dev_status, RF_ERR_NOT_SPD);
+        d = 1.f;
+      }
+      const float sd = sqrtf(d), inv = __frcp_rn(sd);
+      if (rr == j) {
+        a[j] = sd;
+        my_inv = inv;
+      } else if (rr > j) {
+        a[j] *= inv;
+      }
+#pragma unroll
+      for (int c = j + 1; c < kLeafB; ++c) {
+        const float lcj = __shfl_sync(0xffffffffu, a[j], c);
+        if (rr >= c) a[c] = fmaf(-a[j], lcj, a[c]);
+      }
+    }
+    if (lane < kLeafB) {
+#pragma unroll
+      for (int c = 0; c < kLeafB; ++c)
+        if (c <= lane) S[(kd + lane) * kBlkLd + kd + c] = a[c];
+      Dinv[kd + lane] = my_inv;
+    }
+  };
+  if (warp == 0) factor_diag(0, false);
+  __syncthreads();
+  for (int k0 = 0; k0 < n; k0 += kLeafB) {
     // panel: row r solves x L_ddᵀ = S[r][k0..k0+7]
     for (int r = k0 + kLeafB + tid; r < n; r += kThreads) {
       float x[kLeafB];
@@ -256,16 +274,22 @@ __global__ void __launch_bounds__(32 * kWarps) k_chol_inv_leaf(const float* __re
       for (int j = 0; j < kLeafB; ++j) S[r * kBlkLd + k0 + j] = x[j];
     }
     __syncthreads();
-    // trailing lower triangle, rank 8
-    for (int r = k0 + kLeafB + warp; r < n; r += kWarps) {
-      float a[kLeafB];
+    if (warp == 0) {
+      // look-ahead: the next diagonal block, updated and factored while the other
+      // warps update the rows below it
+      if (k0 + kLeafB < n) factor_diag(k0 + kLeafB, true);
+    } else {
+      // trailing lower triangle below the next diagonal block, rank 8
+      for (int r = k0 + 2 * kLeafB + warp - 1; r < n; r += kWarps - 1) {
+        float a[kLeafB];
 #pragma unroll
-      for (int j = 0; j < kLeafB; ++j) a[j] = S[r * kBlkLd + k0 + j];
-      for (int c = k0 + kLeafB + lane; c <= r; c += 32) {
-        float v = S[r * kBlkLd + c];
+        for (int j = 0; j < kLeafB; ++j) a[j] = S[r * kBlkLd + k0 + j];
+        for (int c = k0 + kLeafB + lane; c <= r; c += 32) {
+          float v = S[r * kBlkLd + c];
 #pragma unroll
-        for (int j = 0; j < kLeafB; ++j) v = fmaf(-a[j], S[c * kBlkLd + k0 + j], v);
-        S[r * kBlkLd + c] = v;
+          for (int j = 0; j < kLeafB; ++j) v = fmaf(-a[j], S[c * kBlkLd + k0 + j], v);
+          S[r * kBlkLd + c] = v;
+        }
       }
     }
     __syncthreads();
