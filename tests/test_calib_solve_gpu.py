@@ -250,9 +250,10 @@ def test_solve_refinement_restores_accuracy_when_ill_conditioned():
 
 def test_solve_repeated_refinement_converges_when_badly_conditioned():
     """κ(Gc) ≈ 1e5: the fp32 solve alone is off by about κ·2^-24 and each sweep shrinks
-    the error by about that factor again, down to the residual's own accuracy. Reaching
-    1e-5 needs the residual good to about 1e-5/κ ≈ 2^-33 of its terms; an fp32-accurate
-    residual would stall near the unrefined error."""
+    the error by about that factor again, down to the residual's own accuracy or the
+    fp32 rounding of A (about 6e-8). Reaching 1e-6 needs the residual good to about
+    1e-6/κ ≈ 2^-36 of its terms; an fp32-accurate residual would stall near the
+    unrefined error. (Measured on a GB300: 1.7e-3 unrefined, 5.4e-8 after four sweeps.)"""
     d, P, n = 512, 2, 8192
     rng = np.random.default_rng(22)
     Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
@@ -269,7 +270,7 @@ def test_solve_repeated_refinement_converges_when_badly_conditioned():
         A, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=refine)
         errs[refine] = max(_rel(A[p], Ar[p]) for p in range(P))
     assert errs[0] > 1e-4, errs   # hard enough that fp32 alone is far off
-    assert errs[4] <= 1e-5 and errs[4] < errs[0] / 100, errs
+    assert errs[4] <= 1e-6 and errs[4] < errs[0] / 1000, errs
 
 
 @pytest.mark.slow
