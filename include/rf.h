@@ -204,9 +204,10 @@ rf_status rf_fill_kv(const rf_fill_desc* desc,
  * process exits. It makes no allocating call.
  *   - Fills whose rf_fill_workspace_bytes(desc) exceeds RF_STATIC_SCRATCH_BYTES
  *     are rejected with RF_ERR_WORKSPACE before anything runs.
- *   - The first call on each device looks up the array's device address (and may
- *     load the library's device code there); make that first call before any
- *     stream capture.
+ *   - Every call looks up the array's device address in the current context (a
+ *     host call; the first one in a context may load the library's device code
+ *     there), so a cudaDeviceReset or another context never sees a stale address.
+ *     Make the first call in each context before any stream capture.
  *   - All calls on a device share the array, which keeps the previous call's
  *     contents; nothing in it needs clearing between calls. Calls that overlap
  *     on the GPU race on it: order them on one stream. */

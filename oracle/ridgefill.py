@@ -24,7 +24,7 @@ Sources (cited by page and section):
        selection), "RoPE를 제거한 내용 공간 매핑" (content-space mapping, equation
        for K̂_t).
 
-Readings where the pages leave a step open (each is listed in the design doc):
+Readings where the pages leave a step open:
   * x_S is the residual stream entering layer S; one map per layer l in [S, L).
   * RMSNorm is y = g * x / sqrt(mean(x^2) + eps); K/V projections have no bias.
   * RoPE is the rotate-half form: pair (i, i + hd/2), inv_freq_i = theta^(-2i/hd),

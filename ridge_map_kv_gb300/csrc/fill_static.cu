@@ -12,9 +12,12 @@
 //
 // Every GPU that loads the library holds this array (64 MiB) until the process
 // exits. Host code cannot use the array's name as a device address (on the host
-// it is only a stand-in symbol), so the address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, and handed to the kernels as
-// their workspace.
+// it is only a stand-in symbol), so every call looks the address up with
+// cudaGetSymbolAddress in the caller's current context and hands it to the kernels
+// as their workspace. Nothing is cached: after a cudaDeviceReset, or in another
+// context of the same device, the array can sit at another address, and a cached
+// one would send the fill's writes to memory it does not own. The lookup is a host
+// call (the first one in a context loads the library's device code there).
 //
 // No allocation: the call makes no cudaMalloc, cudaFree or any other allocating
 // call; it only launches kernels on the caller's stream.
@@ -24,32 +27,19 @@
 // the same call, so nothing has to be cleared between calls. Two calls whose work
 // overlaps on the GPU (for example on two streams without ordering) race on the
 // array and corrupt each other's results; order such calls on one stream.
-#include <mutex>
-
 #include "rf_host.h"
 
 namespace rf {
 
 static __device__ __align__(256) unsigned char g_fill_scratch[RF_STATIC_SCRATCH_BYTES];
 
-static std::mutex g_scratch_mu;
-static void* g_scratch_ptr[64] = {nullptr};
-
-// Device address of g_fill_scratch on the current device; set up on first use
-// per device (this may load the library's device code on that device).
+// Device address of g_fill_scratch in the current context, looked up on every call.
 static rf_status static_scratch(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_check(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return fail(RF_ERR_UNSUPPORTED, "device index %d out of range", dev);
-  std::lock_guard<std::mutex> g(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_fill_scratch);
-    if (e != cudaSuccess) return cuda_check(e, "cudaGetSymbolAddress(static fill scratch)");
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_fill_scratch);
+  if (e != cudaSuccess) return cuda_check(e, "cudaGetSymbolAddress(static fill scratch)");
+  if (reinterpret_cast<uintptr_t>(p) & 255u) return fail(RF_ERR_CUDA, "static fill scratch is not 256-byte aligned");
+  *out = p;
   return RF_OK;
 }
 

@@ -5,8 +5,10 @@ sampled entries at full width (27B-shaped d=5120, and the cross-model Gram 8192^
 over 131,072 rows). Tolerance: |ΔG_ij| <= 1e-5 sqrt(G_ii G_jj), the same scale for C
 with the y column's sum of squares.
 Solve: on the toy, the fp32 solve (with fp64 refinement) equals the oracle's A
-and b within 1e-5 relative (Frobenius per map); at full width d=4096, sampled
-rows of A match and satisfy the normal equations.
+and b within 1e-5 relative (Frobenius per map); widths that split unevenly in
+the recursive factorisation (768, 1280, 2560) match every entry; at the configs'
+own sizes (d=4096 sampled rows; d=5120 for the 27B shape and 8192 -> 1024 for
+the cross-model mapper, every entry) A matches and satisfies the normal equations.
 """
 import math
 
@@ -289,3 +291,75 @@ def test_solve_full_width_sampled_rows():
         ne = _rel(A[p][rows] @ H, Cc[p][:, rows].T)      # normal equations
         assert ne <= 1e-5, ne
         assert _rel(b[p][rows], my[p][rows] - Ar @ mx) <= 1e-5
+
+
+# --------------------------------------------------------------------------- #
+# Widths that are not powers of two, and the configs' own solve sizes
+# --------------------------------------------------------------------------- #
+def _solve_vs_oracle(d_in, d_out, P, n, lam, index, refines, device="cpu"):
+    """Oracle sums of seeded planted rows -> GPU solve at each refinement count.
+    Returns the oracle's (A, b, alpha, H, Cc) and the GPU results by refinement."""
+    cal = synth.calib_inputs(d_in, d_out, P, n, index=index, device=device)
+    ref = O.calib_stats(_f64(cal["X"]), _f64(cal["Y"]))
+    del cal
+    Ar, br, alr = O.ridge_solve(ref, lam)
+    Gc, Cc, _, _ = O.centre_stats(ref)
+    H = Gc + alr * np.eye(d_in)
+    st = _upload_stats(ref)
+    got = {r: _solve(st, d_in, d_out, P, lam, refine=r) for r in refines}
+    return (Ar, br, alr, H, Cc), got
+
+
+@pytest.mark.parametrize("d_in,d_out,P,n", [(1280, 768, 2, 4096), (768, 512, 3, 3072), (2560, 512, 2, 8192)],
+                         ids=["1280: 640+640, then 256+384", "768: 384+384, then 128+256",
+                              "2560: tensor-core halves of 1280"])
+def test_solve_widths_that_split_unevenly_match_oracle(d_in, d_out, P, n):
+    """The factorisation halves its width at multiples of 128 near the middle, so
+    widths that are not powers of two split unevenly (640 -> 256 + 384, 384 -> 128 +
+    256), and 2560 takes one tensor-core level before the SIMT recursion at 1280:
+    the branches the 27B-shaped solve (d = 5120) takes. Every entry of A and b is
+    checked against the oracle, unrefined and after one refinement sweep."""
+    (Ar, br, alr, H, Cc), got = _solve_vs_oracle(d_in, d_out, P, n, 0.03, index=95, refines=(0, 1))
+    for refine, (A, b, Ab, alpha) in got.items():
+        assert abs(alpha - alr) <= 1e-12 * alr
+        for p in range(P):
+            assert _rel(A[p], Ar[p]) <= 1e-5, (refine, p, _rel(A[p], Ar[p]))
+            assert _rel(b[p], br[p]) <= 1e-5, (refine, p, _rel(b[p], br[p]))
+            assert _rel(A[p] @ H, Cc[p].T) <= 1e-5          # the normal equations
+
+
+def _full_width_solve(d_in, d_out, P, n, lam, index):
+    (Ar, br, alr, H, Cc), got = _solve_vs_oracle(d_in, d_out, P, n, lam, index, refines=(0, 1), device=DEV)
+    errs = {}
+    for refine, (A, b, _, alpha) in got.items():
+        assert abs(alpha - alr) <= 1e-12 * alr
+        errs[refine] = max(_rel(A[p], Ar[p]) for p in range(P))
+        for p in range(P):
+            assert _rel(b[p], br[p]) <= (1e-5 if refine else 1e-4)
+            rows = np.sort(np.random.default_rng(3 + p).choice(d_out, 64, replace=False))
+            assert _rel(A[p][rows] @ H, Cc[p][:, rows].T) <= (1e-5 if refine else 1e-4)   # normal equations
+    # fp32 factorisation and products alone: about κ·sqrt(d)·2^-24 (κ ≈ 13-30 here);
+    # one sweep with the fp64-accurate residual brings A to fp32 accuracy
+    assert errs[0] <= 1e-4, errs
+    assert errs[1] <= 1e-5 and errs[1] <= errs[0], errs
+    return errs
+
+
+@pytest.mark.slow
+def test_solve_27b_shape_matches_oracle():
+    """The 27B-shaped solve, d = 5120 (5120 -> 2560 -> 1280 on the tensor cores,
+    then 640 -> 256 + 384 in fp32 SIMT), from 16,384 planted calibration rows,
+    λ = 0.03: every entry of two maps against the oracle, and the normal equations
+    on sampled rows."""
+    c = synth.DENSE27B
+    _full_width_solve(c.d, c.d, 2, c.calib_n, c.lam, index=c.index)
+
+
+@pytest.mark.slow
+def test_solve_cross_model_gram_shape_matches_oracle():
+    """The cross-model mapper's solve: d_in = 8192 concatenated features (k = 8 source
+    layers x 8 heads x 128) onto d_out = 1024 target columns, λ = 0.01 with α
+    trace-scaled. The fp64 sums come from 16,384 rows (fewer than the 131,072 of the
+    calibration, to keep the oracle's Gram quick; the solve's sizes are the same)."""
+    x = synth.XMODEL
+    _full_width_solve(x.d_in, x.KV, 2, 16384, x.lam, index=x.index)

@@ -109,7 +109,7 @@ def _sample_rows(idx: np.ndarray, mask_np, n_prefix: int, n_random=192, seed=1):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["llama8b", "dense27b"])
+@pytest.mark.parametrize("name", ["llama8b", "qwen3_8b", "dense27b"])
 @KERNELS
 def test_fill_full_size_sampled(name, flags):
     cfg = synth.FILL_CONFIGS[name]

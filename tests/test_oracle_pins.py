@@ -852,3 +852,33 @@ def test_calibration_sum_of_squares_gives_total_variance():
     st = O.add_stats(O.calib_stats(X[:60], Y[:, :60]), O.calib_stats(X[60:], Y[:, 60:]))
     tss = st["syy"] - st["n"] * (st["sy"] / st["n"]) ** 2
     np.testing.assert_allclose(tss, Y.var(axis=1) * 100, rtol=1e-12)
+
+
+def test_replayed_path_reproduces_the_greedy_run_and_scores_its_prefixes():
+    # Replaying the oracle's own greedy choices must give back its selection and its
+    # whole score table exactly. Replaying a hand-chosen path (not the greedy one)
+    # must record, at each step, every remaining layer's score as the head-mean R²
+    # of a least-squares fit (lstsq with an intercept column, from the raw rows) on
+    # the path's prefix plus that layer, NaN for the prefix's own layers, and must
+    # return the path itself as the selection.
+    n, L, F, P, Ft, hd, k = 400, 5, 2, 2, 4, 2, 4
+    X, Ys = _layered_rows(n, L, F, P, Ft, seed=16)
+    st = O.calib_stats(X, Ys)
+    sel, table = O.select_sources([st], L, F, hd, k, 0.0, "absolute")
+    sel2, table2 = O.select_sources([st], L, F, hd, k, 0.0, "absolute", path=sel)
+    np.testing.assert_array_equal(sel2, sel)
+    np.testing.assert_array_equal(table2, table)          # NaNs in the same places
+    path = np.array([[4, 0, 2, 1], [1, 3, 0, 4]])
+    assert not np.array_equal(path, sel)
+    selp, tablep = O.select_sources([st], L, F, hd, k, 0.0, "absolute", path=path)
+    np.testing.assert_array_equal(selp, path)
+    for p in range(P):
+        for j in range(k):
+            prefix = [int(c) for c in path[p, :j]]
+            for s in range(L):
+                if s in prefix:
+                    assert np.isnan(tablep[0, p, j, s])
+                    continue
+                Z = np.concatenate([X[:, _cols(prefix + [s], F)], np.ones((n, 1))], axis=1)
+                w, *_ = np.linalg.lstsq(Z, Ys[p], rcond=None)
+                assert abs(tablep[0, p, j, s] - _head_r2_from_fit(Ys[p], Z @ w, hd)) < 1e-10
