@@ -1,18 +1,23 @@
 #!/usr/bin/env python3
 """Benchmark of the RidgeFill upper-layer KV fill on GB300 (librf.so, C ABI).
 
-One step = one rf_fill_kv call over the Llama-3.1-8B-shaped workload
-(d=4096, L=32, S=12, N=16384, T=4096, 8 KV heads x 128, 10% of prefix rows exact):
-row compaction, gather, RoPE table, the map GEMM for all 20 upper layers and the
-K/V GEMM with norm scale, RoPE and cache scatter. Inputs are seeded synthetic
-tensors resident in HBM. They are larger than L2 (1.1 GB of maps, weights and x_S
+One step = one rf_fill_kv call over the 27B-shaped workload (d=5120, L=64, S=16,
+N=32768, T=4096, 8 KV heads x 128, 5% of prefix rows exact in blocks of 16, all
+layers full attention): row compaction, gather, RoPE table, the map GEMM for all 48
+upper layers and the K/V GEMM with norm scale, RoPE and cache scatter. The RMSNorm
+gains are folded into the projections once, before the timed region
+(RF_WEIGHTS_PREFOLDED), and that fold is reported on its own. Inputs are seeded
+synthetic tensors resident in HBM, larger than L2 (3.9 GB of maps, weights and x_S
 are read per step), so no L2 flush is needed. Timing uses CUDA events on the
 launching stream, bracketed by a barrier and a device synchronize.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-N > 1 (under torchrun): every rank runs an independent fill on its own GPU (weak
-scaling; no data-path collective). value = all ranks' row-layers / max rank time.
+N > 1 (under torchrun): the fill is sharded by upper layer: rank r fills its own
+contiguous block of the upper layers (their maps, projections and cache slice),
+with no data-path collective, so together the ranks fill the whole workload once
+per step. value = all ranks' row-layers / max rank time (the only collective
+reduces the timing numbers).
 --impl reference times the fp64 CPU oracle on the host cores over a bounded row
 sample of the same workload, and prints the same metric.
 """
@@ -35,8 +40,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "filled rows×layers/s and fill TFLOP/s vs GB300 bf16 dense peak (1 GPU)"
 UNIT = "row-layers/s"
-WORKLOAD = "llama8b"
-KERNELS_PER_FILL = 5
+WORKLOAD = "dense27b"
+KERNELS_PER_FILL = 6   # compaction, gather, RoPE table, map GEMM, row RMS, K/V GEMM
 
 
 def parse_args(argv=None):
@@ -45,7 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=1024, help="oracle row sample for the CPU baseline")
+    ap.add_argument("--cpu-rows", type=int, default=512, help="oracle row sample for the CPU baseline (all cores)")
+    ap.add_argument("--cpu-rows-1core", type=int, default=16, help="oracle row sample for the single-core rate")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the calibration, solve and cross-model rows")
@@ -63,7 +69,7 @@ def parse_args(argv=None):
     ap.add_argument("--gemm", choices=["default", "single", "pair"], default="default",
                     help="tensor-core GEMM kernel: one CTA per 128x256 tile, or a CTA pair per 256x256 tile")
     ap.add_argument("--workload", choices=sorted(workloads()), default=WORKLOAD,
-                    help="llama8b (default, the metric's workload); others for profiling and parity runs")
+                    help="dense27b (default: the largest single-GPU workload); others for profiling runs")
     return ap.parse_args(argv)
 
 
@@ -199,15 +205,17 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-# The sources the map GEMM is compiled from (its kernel is instantiated in fill.cu
-# only); a committed DRAM-traffic figure is valid while these hash the same.
-MAP_GEMM_SOURCES = ("api.cu", "epilogue.cuh", "fill.cu", "fill_gemm.cuh", "rf_device.cuh", "rf_host.h", "tc_gemm.cuh")
+# The sources the fill GEMMs are compiled from (their kernels are instantiated in
+# fill.cu only); a committed DRAM-traffic figure is valid while these hash the same.
+FILL_GEMM_SOURCES = ("api.cu", "epilogue.cuh", "fill.cu", "fill_gemm.cuh", "rf_device.cuh", "rf_host.h",
+                     "tc_gemm.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ridge_map_kv_gb300", "csrc")
-    for f in MAP_GEMM_SOURCES:
+    for f in FILL_GEMM_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     h.update(b"rf.h\0" + open(os.path.join(ROOT, "include", "rf.h"), "rb").read())
@@ -215,17 +223,16 @@ def kernel_source_sha() -> str:
 
 
 def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel sources (else None)."""
-    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
-    if not os.path.exists(p):
+    """DRAM bytes per launch of ``kernel`` on ``workload`` from the machine-readable
+    record written with the ncu capture (profiles/dram_traffic.json), if it was taken
+    on the current kernel sources; else None."""
+    if not os.path.exists(TRAFFIC_FILE):
         return None
-    txt = open(p).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    s = re.search(r"source_sha:\s*([0-9a-f]+)", txt)
-    if not m or not s or s.group(1) != kernel_source_sha():
+    with open(TRAFFIC_FILE) as f:
+        rec = json.load(f).get(f"{kernel}/{workload}")
+    if not rec or rec.get("source_sha") != kernel_source_sha():
         return None
-    return float(m.group(1))
+    return float(rec["bytes_per_launch"])
 
 
 def fill_units(cfg, mask):
@@ -266,8 +273,86 @@ def cpu_oracle_rate(oi: "OracleInputs", n_rows: int, seed: int = 7):
         O.fill_rows(x, rows + cfg.pos_offset, oi.A[p], oi.b[p], oi.g[p], oi.Wk[p], oi.Wv[p],
                     cfg.H, cfg.hd, cfg.rope_theta, cfg.rms_eps)
     dt = time.perf_counter() - t0
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return len(rows) * cfg.P / dt, dt, len(rows), cores
+    return len(rows) * cfg.P / dt, dt, len(rows), host_cores()
+
+
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+class BlasThreads:
+    """Thread count of the BLAS library numpy loaded (OpenBLAS builds export a
+    set/get pair), so the oracle can be timed on one core. ``available`` is False
+    when no such library is found; nothing is changed then."""
+    PAIRS = (("scipy_openblas_get_num_threads64_", "scipy_openblas_set_num_threads64_"),
+             ("openblas_get_num_threads64_", "openblas_set_num_threads64_"),
+             ("openblas_get_num_threads", "openblas_set_num_threads"))
+
+    def __init__(self):
+        import ctypes
+
+        import numpy as np
+        np.ones((2, 2)) @ np.ones((2, 2))          # make sure the BLAS library is loaded
+        self.get = self.set = None
+        paths = []
+        with open("/proc/self/maps") as f:
+            for line in f:
+                if "blas" in line.lower() and line.split()[-1] not in paths:
+                    paths.append(line.split()[-1])
+        for path in paths:
+            try:
+                lib = ctypes.CDLL(path)
+            except OSError:
+                continue
+            for g, s_ in self.PAIRS:
+                if hasattr(lib, g) and hasattr(lib, s_):
+                    self.get, self.set = getattr(lib, g), getattr(lib, s_)
+                    self.get.restype = ctypes.c_int
+                    self.set.argtypes = [ctypes.c_int]
+                    return
+
+    @property
+    def available(self) -> bool:
+        return self.set is not None
+
+
+def cpu_baseline(cfg, inp, n_rows: int, n_rows_1core: int) -> dict:
+    """The fp64 oracle as it stands, on this host: all cores on ``n_rows`` sampled
+    filled rows x every upper layer, one core on ``n_rows_1core`` rows, and the
+    whole toy workload (every filled row and layer of the 8-layer toy) once."""
+    import numpy as np
+
+    import oracle as O
+    import synth
+    oi = OracleInputs(cfg, inp)
+    rate, dt, nrows, cores = cpu_oracle_rate(oi, n_rows)
+    out = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"{nrows} filled rows x {cfg.P} upper layers of the same workload, fp64 numpy, {dt:.1f} s"}
+    bt = BlasThreads()
+    if bt.available:
+        before = bt.get()
+        bt.set(1)
+        try:
+            r1, dt1, n1, _ = cpu_oracle_rate(oi, n_rows_1core, seed=8)
+        finally:
+            bt.set(before)
+        out["single_core"] = {"value": r1, "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} filled rows x {cfg.P} upper layers, BLAS on one thread, {dt1:.1f} s"}
+    else:
+        out["single_core"] = {"value": None, "why": "no OpenBLAS thread control found in this numpy"}
+    toy = synth.TOY
+    ti = synth.fill_inputs(toy)
+    f64 = O.bf16_bits_to_f64
+    zeros = np.zeros((toy.L, toy.N, toy.H, toy.hd))
+    t0 = time.perf_counter()
+    O.fill_kv(zeros, zeros, f64(synth.bits(ti["x_S"])), synth.f32(ti["mask"]), f64(synth.bits(ti["A"])),
+              synth.f32(ti["b"]).astype(np.float64), f64(synth.bits(ti["gain"])), f64(synth.bits(ti["Wk"])),
+              f64(synth.bits(ti["Wv"])), L=toy.L, S=toy.S, N=toy.N, T=toy.T, n_kv_heads=toy.H, head_dim=toy.hd,
+              rope_theta=toy.rope_theta, rms_eps=toy.rms_eps)
+    out["toy_full_s"] = time.perf_counter() - t0
+    out["toy_workload"] = f"{toy.name}: the whole fill (every filled row and upper layer, bookkeeping included)"
+    del oi
+    return out
 
 
 def gemm_flags(name):
@@ -300,25 +385,36 @@ def run_selection_only(args):
     print(json.dumps({"selection": row}))
 
 
+def fill_plan(cfg, world: int, rank: int, flags: int):
+    """The rank's share of the fill: its layer block and the rf_fill_desc fields of
+    that block (see ridge_map_kv_gb300.shard). One rank covers the whole fill."""
+    from ridge_map_kv_gb300 import shard as sh
+    block = sh.layer_shard(cfg.P, cfg.S, world, rank)
+    fields = dict(d=cfg.d, d_in=cfg.d_in, L=cfg.L, S=cfg.S, N=cfg.N, T=cfg.T, n_kv_heads=cfg.H, head_dim=cfg.hd,
+                  rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, pos_offset=cfg.pos_offset, flags=flags)
+    return block, sh.shard_desc_fields(fields, block)
+
+
 def run_ours(args):
     import torch
 
     import ridge_map_kv_gb300 as rf
     import synth
+    from ridge_map_kv_gb300 import shard as sh
 
     ws_n, rank, local = dist_env()
     torch.cuda.set_device(local)
     dist_init("nccl")
     dev = torch.device("cuda", local)
     cfg = workloads()[args.workload]
-    inp = synth.fill_inputs(cfg, device=dev)
-    n_fill, units = fill_units(cfg, inp["mask"])
-    P, d, KV, di = cfg.P, cfg.d, cfg.KV, cfg.D_in
-    desc = rf.rf_fill_desc(d=d, d_in=cfg.d_in, L=cfg.L, S=cfg.S, N=cfg.N, T=cfg.T, n_kv_heads=cfg.H, head_dim=cfg.hd,
-                           rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, pos_offset=0,
-                           flags=gemm_flags(args.gemm))
-    Wkv = torch.empty((P, 2 * KV, d), dtype=torch.bfloat16, device=dev)
-    kc = torch.zeros((cfg.L, cfg.N, cfg.H, cfg.hd), dtype=torch.bfloat16, device=dev)
+    full = synth.fill_inputs(cfg, device=dev)
+    n_fill, _ = fill_units(cfg, full["mask"])
+    block, fields = fill_plan(cfg, ws_n, rank, gemm_flags(args.gemm) | rf.RF_WEIGHTS_PREFOLDED)
+    inp = sh.shard_weights(full, block)
+    P, d, KV, di = block.layers, cfg.d, cfg.KV, cfg.D_in
+    units = n_fill * P
+    desc = rf.rf_fill_desc(**fields)
+    kc = torch.zeros((max(P, 1), cfg.N, cfg.H, cfg.hd), dtype=torch.bfloat16, device=dev)   # this rank's layers
     vc = torch.zeros_like(kc)
     ws_bytes = rf.rf_fill_workspace_bytes(desc)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -326,13 +422,15 @@ def run_ours(args):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    # one-time weight preparation (reported separately)
-    rf.rf_profile_start(4)
-    rf.rf_fold_kv_weights(desc, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
+    # one-time weight preparation (reported separately, outside the step)
+    Wk = torch.empty_like(inp["Wk"])
+    Wv = torch.empty_like(inp["Wv"])
+    rf.rf_profile_start(8)
+    rf.rf_fold_kv_weights(desc, inp["gain"], inp["Wk"], inp["Wv"], Wk, Wv)
     fold_ms = sum(ms for _, ms in rf.rf_profile_stop())
 
     def step():
-        rf.rf_fill_kv(desc, inp["x_S"], di, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc, cfg.N * KV, KV,
+        rf.rf_fill_kv(desc, inp["x_S"], di, inp["mask"], inp["A"], inp["b"], None, Wk, Wv, kc, vc, cfg.N * KV, KV,
                       nfill, status, ws, ws_bytes)
 
     for _ in range(max(args.warmup, 3)):
@@ -344,7 +442,8 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.4)                      # let the sampler start before the timed region
-    rf.rf_profile_start(args.steps * KERNELS_PER_FILL + 8)
+    cap = args.steps * KERNELS_PER_FILL + 64
+    rf.rf_profile_start(cap)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier()
@@ -356,9 +455,10 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    prof = rf.rf_profile_stop()
+    prof = rf.rf_profile_stop(cap)
     elapsed_ms = e0.elapsed_time(e1)
     assert int(status.item()) == 0
+    assert len(prof) < cap, "profiler capacity reached: launch count would be cut short"
     value, ms_per_step, t_max = aggregate_timing(units, args.steps, elapsed_ms, dev)
 
     stage_ms = {}
@@ -369,24 +469,34 @@ def run_ours(args):
 
     map_flops = 2.0 * n_fill * P * d * di
     kv_flops = 2.0 * n_fill * P * d * 2 * KV
-    fill_flops = map_flops + kv_flops
+    fill_flops_rank = map_flops + kv_flops
+    fill_flops_all = reduce_sum(fill_flops_rank, dev)
     peaks = measured_peaks()
-    map_ms = stage_avg.get("map_gemm")
-    achieved = map_flops / (map_ms / 1e3) / 1e12 if map_ms else None
-    # The map GEMM is timed inside the whole run of K steps: a run of 0.2 s or
-    # more is a sustained load (the 1.4 kW power cap engages within it), so its
-    # denominator is the sustained bf16 figure; a shorter run takes the burst one.
+    # The GEMMs are timed inside the whole run of K steps: a run of 0.2 s or more is
+    # a sustained load (the 1.4 kW power cap engages within it), so the denominator
+    # is the sustained bf16 figure; a shorter run takes the burst one. Both fractions
+    # are in the line.
     sustained = t_max >= 200.0 and peaks.get("bf16_tflops_sustained")
     peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
-    roofline = {"kernel": "map_gemm (tc_gemm<MapProb>)", "bound": "tensor", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": (achieved / peak) if achieved else None,
-                "traffic": profiled_traffic("map_gemm", args.workload),
+    m_pad = -(-n_fill // 256) * 256
+
+    def roofline_of(stage, kernel, flops, nbytes, traffic_key):
+        ms_k = stage_avg.get(stage)
+        achieved = flops / (ms_k / 1e3) / 1e12 if ms_k else None
+        return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": (achieved / peak) if achieved else None,
+                "frac_of_burst": (achieved / peaks["bf16_tflops"]) if achieved else None,
+                "traffic": profiled_traffic(traffic_key, args.workload) if ws_n == 1 else None,
                 "peak_source": f"{peaks['source']} {'sustained' if sustained else 'burst'} bf16 (MEASURED_PEAKS.json)"
                                f"; timed region {t_max:.0f} ms",
                 "peak_burst": peaks["bf16_tflops"], "peak_sustained": peaks.get("bf16_tflops_sustained"),
-                "algorithmic_flops_per_launch": map_flops,
-                "algorithmic_bytes_per_launch": n_fill * di * 2 + P * d * di * 2 + n_fill * P * d * 2
-                + n_fill * P * (d // 256) * 4 + P * d * 4}
+                "ms_per_launch": ms_k, "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes}
+
+    # algorithmic bytes: map GEMM = Xf + maps + x̂ + Σx̂² partials + b; K/V GEMM = x̂ + Wk/Wv + the cache rows
+    map_bytes = n_fill * di * 2 + P * d * di * 2 + n_fill * P * d * 2 + n_fill * P * (d // 256) * 4 + P * d * 4
+    kv_bytes = n_fill * P * d * 2 + P * 2 * KV * d * 2 + n_fill * P * 2 * KV * 2
+    roofline = roofline_of("map_gemm", "map_gemm (tc_gemm_pair_kernel<MapProb>)", map_flops, map_bytes, "map_gemm")
+    roofline_kv = roofline_of("kv_gemm", "kv_gemm (tc_gemm_pair_kernel<KVProb>)", kv_flops, kv_bytes, "kv_gemm")
 
     # HBM-bound kernels of the step against the measured copy bandwidth:
     # gather = read n_fill rows of x_S + write Xf (n_fill rows, zero pad to the
@@ -394,7 +504,6 @@ def run_ours(args):
     # read the mask + write fill_idx; row_rms = read the map GEMM's d/256 partial
     # sums per row and layer + write the row scale.
     n_prefix = cfg.N - cfg.T
-    m_pad = -(-n_fill // 256) * 256
     hbm_bytes = {"gather": n_fill * di * 2 + m_pad * di * 2,
                  "rope_table": 2 * n_prefix * (cfg.hd // 2) * 4,
                  "compact": n_prefix + n_fill * 4,
@@ -439,8 +548,8 @@ def run_ours(args):
                         md[r].copy_(mh, non_blocking=True)
                     ready[r].record(copy_stream)
                 stream.wait_event(ready[r])
-                rf.rf_fill_kv(desc, xd[r], di, md[r], inp["A"], inp["b"], Wkv, kc, vc, cfg.N * KV, KV, outd[0:1],
-                              outd[1:2], ws, ws_bytes, stream=stream.cuda_stream)
+                rf.rf_fill_kv(desc, xd[r], di, md[r], inp["A"], inp["b"], None, Wk, Wv, kc, vc, cfg.N * KV, KV,
+                              outd[0:1], outd[1:2], ws, ws_bytes, stream=stream.cuda_stream)
                 freed[r].record(stream)
                 outh.copy_(outd, non_blocking=True)
         run_e2e(3)
@@ -459,13 +568,11 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        rate, dt, nrows, cores = cpu_oracle_rate(OracleInputs(cfg, inp), args.cpu_rows)
-        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{nrows} filled rows x {P} upper layers of the same workload, fp64 numpy, {dt:.1f} s"}
+        cpu = cpu_baseline(cfg, full, args.cpu_rows, args.cpu_rows_1core)
 
     extras = None
     if rank == 0 and ws_n == 1 and not args.no_extras:
-        del ws, kc, vc, inp, Wkv
+        del ws, kc, vc, inp, full, Wk, Wv
         torch.cuda.empty_cache()
         extras = run_extras(dev, peaks["bf16_tflops"], gemm_flags(args.gemm))
 
@@ -473,16 +580,19 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "strong" if ws_n > 1 else "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
             "config": {"workload": workload_label(cfg), "n_fill": n_fill,
-                       "upper_layers": P, "row_layers_per_step": units, "parallelism": f"independent fills x{ws_n}",
-                       "gemm": args.gemm,
-                       "l2": "no flush: inputs larger than L2 (1.1 GB of maps, weights and x_S read per step)"},
-            "tflops": fill_flops * args.steps * ws_n / (t_max / 1e3) / 1e12,
-            "frac_of_bf16_peak": fill_flops * args.steps * ws_n / (t_max / 1e3) / 1e12 / peak,
-            "roofline": roofline, "hbm_kernels": hbm_kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches,
-            "clocks": clk,
+                       "upper_layers": cfg.P, "row_layers_per_step": n_fill * cfg.P,
+                       "parallelism": f"upper layers sharded over {ws_n} GPU(s), {block.layers} layers on rank 0"
+                                      if ws_n > 1 else "1 GPU, whole fill",
+                       "gemm": args.gemm, "weights": "RMSNorm gain folded into W_k/W_v once, before the timed "
+                                                     "region (RF_WEIGHTS_PREFOLDED); fold_once_ms",
+                       "l2": "no flush: inputs larger than L2 (maps, projections and x_S read per step)"},
+            "tflops": fill_flops_all * args.steps / (t_max / 1e3) / 1e12,
+            "frac_of_bf16_peak": fill_flops_all * args.steps / (t_max / 1e3) / 1e12 / peak,
+            "roofline": roofline, "roofline_kv_gemm": roofline_kv, "hbm_kernels": hbm_kernels,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
             "stages_ms": stage_avg, "fold_once_ms": fold_ms, "extras": extras,
         }
         print(json.dumps(line))
@@ -516,6 +626,20 @@ def _timed(fn, reps, stream):
     return e0.elapsed_time(e1) / reps, stages
 
 
+def _prefolded(c, inp, flags):
+    """rf_fill_desc of workload ``c`` with RF_WEIGHTS_PREFOLDED, and its folded K/V
+    projections (the unfolded ones are dropped from ``inp``)."""
+    import torch
+
+    import ridge_map_kv_gb300 as rf
+    fd = rf.rf_fill_desc(d=c.d, d_in=c.d_in, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd,
+                         rope_theta=c.rope_theta, rms_eps=c.rms_eps, pos_offset=0, flags=flags | rf.RF_WEIGHTS_PREFOLDED)
+    Wk, Wv = torch.empty_like(inp["Wk"]), torch.empty_like(inp["Wv"])
+    rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wk, Wv)
+    del inp["Wk"], inp["Wv"]
+    return fd, Wk, Wv
+
+
 def _zero_stats(d_in, d_out, P, dev):
     import torch
     return {"G": torch.zeros((d_in, d_in), dtype=torch.float64, device=dev),
@@ -525,7 +649,8 @@ def _zero_stats(d_in, d_out, P, dev):
             "n": torch.zeros(1, dtype=torch.int64, device=dev)}
 
 
-EXTRA_ROWS = ("a5_calibration", "a5_calibration_xmodel", "a6_solve", "a7_xmodel", "next3_map_storage_8b",
+EXTRA_ROWS = ("fill_llama8b", "a5_calibration", "a5_calibration_xmodel", "a6_solve", "a6_solve_27b",
+              "a6_solve_xmodel", "a7_xmodel", "next3_map_storage_8b",
               "next2_key_norm_qwen3", "next4_nonsquare_flash_next", "next1_value_rescale_27b",
               "next4a_source_selection_xmodel")
 
@@ -543,6 +668,31 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
     import synth
     stream = torch.cuda.current_stream(dev)
     out = {}
+
+    if only in (None, "fill_llama8b"):
+        # the Llama-3.1-8B-shaped fill (20 upper layers, n_fill = 11,059), weights prefolded
+        c = synth.LLAMA8B
+        inp = synth.fill_inputs(c, device=dev)
+        fd, Wk, Wv = _prefolded(c, inp, flags)
+        kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
+        vc = torch.zeros_like(kc)
+        wsb = rf.rf_fill_workspace_bytes(fd)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        nf = torch.zeros(1, dtype=torch.int32, device=dev)
+        ms, st = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], None, Wk, Wv, kc,
+                                              vc, c.N * c.KV, c.KV, nf, None, ws, wsb), 20, stream)
+        n_fill = int(nf.item())
+        f_flops = 2.0 * n_fill * c.P * (c.d * c.d + c.d * 2 * c.KV)
+        mg, kg = st.get("map_gemm"), st.get("kv_gemm")
+        out["fill_llama8b"] = {
+            "workload": workload_label(c) + f", n_fill={n_fill}", "fill_ms": ms,
+            "fill_row_layers_per_s": n_fill * c.P / (ms / 1e3), "fill_tflops": f_flops / (ms / 1e3) / 1e12,
+            "fill_frac_of_bf16_peak": f_flops / (ms / 1e3) / 1e12 / peak_tflops,
+            "map_gemm_frac_of_bf16_peak": 2.0 * n_fill * c.P * c.d * c.d / (mg / 1e3) / 1e12 / peak_tflops if mg else None,
+            "kv_gemm_frac_of_bf16_peak": 2.0 * n_fill * c.P * c.d * 2 * c.KV / (kg / 1e3) / 1e12 / peak_tflops
+            if kg else None, "stages_ms": st}
+        del inp, kc, vc, ws, Wk, Wv
+        torch.cuda.empty_cache()
 
     if only in (None, "a5_calibration"):
         # a5: calibration statistics, 27B-shaped: XᵀX and XᵀY_l for 48 maps over 16,384 rows
@@ -621,6 +771,21 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
         del st, cs, A, b, Ab, ws
         torch.cuda.empty_cache()
 
+    if only in (None, "a6_solve_27b"):
+        # a6 at the 27B shape: d = 5120, 48 maps, sums over 16,384 rows accumulated on the device
+        c = synth.DENSE27B
+        out["a6_solve_27b"] = _solve_row(dev, c.d, c.d, c.P, c.calib_n, c.lam, c.index, flags, peak_tflops,
+                                         f"27b-shaped ridge solve, d={c.d}, {c.P} maps, lambda={c.lam}, "
+                                         f"sums from {c.calib_n} calibration rows")
+
+    if only in (None, "a6_solve_xmodel"):
+        # a6 for the cross-model mapper: 8192 concatenated features -> 1024 target columns, one map
+        # (one kind of one target layer), sums over 131,072 rows
+        x = synth.XMODEL
+        out["a6_solve_xmodel"] = _solve_row(dev, x.d_in, x.KV, 1, x.calib_n, x.lam, x.index, flags, peak_tflops,
+                                            f"cross-model ridge solve, d_in={x.d_in} -> d_out={x.KV}, one map, "
+                                            f"lambda={x.lam}, sums from {x.calib_n} rows")
+
     if only in (None, "a7_xmodel"):
         # a7: cross-model mapper, 40 -> 64 layers, k = 8, 8 x 128 heads, N = 32768
         x = synth.XMODEL
@@ -633,7 +798,8 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
         vt = torch.empty_like(kt)
         wsb = rf.rf_xmodel_workspace_bytes(xd)
         ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-        ms, stages = _timed(lambda: rf.rf_xmodel_map(xd, inp["src"], inp["k_src"], inp["v_src"], inp["Wk"], inp["bk"],
+        src = torch.as_tensor(inp["src"], dtype=torch.int32, device=dev)
+        ms, stages = _timed(lambda: rf.rf_xmodel_map(xd, src, inp["k_src"], inp["v_src"], inp["Wk"], inp["bk"],
                                                      inp["Wv"], inp["bv"], kt, vt, None, ws, wsb), 3, stream)
         flops = 2.0 * x.N * x.d_in * 2 * x.KV * x.L_tgt
         gm = stages.get("xmodel_gemm", ms)
@@ -649,11 +815,7 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
         # layer-by-layer fill with maps on the device or the host, bf16 or int8
         c = synth.LLAMA8B
         inp = synth.fill_inputs(c, device=dev)
-        fd = rf.rf_fill_desc(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
-                             rms_eps=c.rms_eps, pos_offset=0, flags=flags)
-        Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
-        rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
-        del inp["Wk"], inp["Wv"]
+        fd, Wk, Wv = _prefolded(c, inp, flags)
         q = torch.empty((c.P, c.d, c.d), dtype=torch.int8, device=dev)
         qs = torch.empty((c.P, c.d), dtype=torch.float32, device=dev)
         rf.rf_quantize_maps_int8(fd, inp["A"], q, qs)
@@ -665,8 +827,9 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
         row = {"workload": workload_label(c), "map_bytes_bf16": c.P * c.d * c.d * 2, "map_bytes_int8": c.P * c.d * c.d}
         wsb = rf.rf_fill_workspace_bytes(fd)
         ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-        row["resident_ms"], _ = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], Wkv, kc,
-                                                             vc, c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
+        row["resident_ms"], _ = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], None,
+                                                             Wk, Wv, kc, vc, c.N * c.KV, c.KV, nf, None, ws, wsb), 3,
+                                       stream)
         row["resident_workspace_bytes"] = wsb
         del ws
         variants = {"layered_device_bf16": rf.map_source(rf.RF_MAPS_BF16, inp["A"]),
@@ -677,14 +840,14 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
             wsb = rf.rf_fill_layered_workspace_bytes(fd, ms_)
             ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
             row[f"{key}_ms"], st = _timed(lambda: rf.rf_fill_kv_layered(fd, inp["x_S"], c.d, inp["mask"], ms_, inp["b"],
-                                                                        Wkv, kc, vc, c.N * c.KV, c.KV, nf, None, ws,
-                                                                        wsb), 3, stream)
+                                                                        None, Wk, Wv, kc, vc, c.N * c.KV, c.KV, nf,
+                                                                        None, ws, wsb), 3, stream)
             row[f"{key}_workspace_bytes"] = wsb
             if "int8_expand" in st:
                 row[f"{key}_expand_ms"] = st["int8_expand"]
             del ws
         out["next3_map_storage_8b"] = row
-        del inp, kc, vc, Wkv, q, qs, A_host, q_host
+        del inp, kc, vc, Wk, Wv, q, qs, A_host, q_host
         torch.cuda.empty_cache()
 
     if only in (None, "next2_key_norm_qwen3"):
@@ -692,11 +855,7 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
         c = synth.QWEN3_8B
         inp = synth.fill_inputs(c, device=dev)
         kg = synth.key_norm_gain(c, device=dev)
-        fd = rf.rf_fill_desc(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
-                             rms_eps=c.rms_eps, pos_offset=0, flags=flags)
-        Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
-        rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
-        del inp["Wk"], inp["Wv"]
+        fd, Wk, Wv = _prefolded(c, inp, flags)
         kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
         vc = torch.zeros_like(kc)
         wsb = rf.rf_fill_workspace_bytes(fd)
@@ -705,32 +864,30 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
         row = {"workload": f"qwen3-8b-shaped fill (d={c.d}, {c.P} upper layers, N={c.N}, T={c.T}, no exact rows)"}
         for key, gain_ptr in (("plain", None), ("key_norm", kg.data_ptr())):
             fd.k_norm_gain = gain_ptr
-            ms, st = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
-                                                  c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
+            ms, st = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], None, Wk, Wv, kc,
+                                                  vc, c.N * c.KV, c.KV, nf, None, ws, wsb), 5, stream)
             n_fill = int(nf.item())
             f_flops = 2.0 * n_fill * c.P * (c.d * c.d + c.d * 2 * c.KV)
             row[f"{key}_ms"] = ms
             row[f"{key}_tflops"] = f_flops / (ms / 1e3) / 1e12
             row[f"{key}_kv_gemm_ms"] = st.get("kv_gemm")
+            row[f"{key}_map_gemm_ms"] = st.get("map_gemm")
         out["next2_key_norm_qwen3"] = row
-        del inp, kc, vc, ws, Wkv
+        del inp, kc, vc, ws, Wk, Wv
         torch.cuda.empty_cache()
 
     if only in (None, "next4_nonsquare_flash_next"):
         # Non-square maps: the Flash-Next-shaped fill (10,240 -> 2,560, 24 upper layers)
         c = synth.FLASH_NEXT
         inp = synth.fill_inputs(c, device=dev)
-        fd = rf.rf_fill_desc(d=c.d, d_in=c.d_in, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd,
-                             rope_theta=c.rope_theta, rms_eps=c.rms_eps, pos_offset=0, flags=flags)
-        Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
-        rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
+        fd, Wk, Wv = _prefolded(c, inp, flags)
         kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
         vc = torch.zeros_like(kc)
         wsb = rf.rf_fill_workspace_bytes(fd)
         ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
         nf = torch.zeros(1, dtype=torch.int32, device=dev)
-        ms, st = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d_in, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
-                                              c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
+        ms, st = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d_in, inp["mask"], inp["A"], inp["b"], None, Wk, Wv, kc,
+                                              vc, c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
         n_fill = int(nf.item())
         f_flops = 2.0 * n_fill * c.P * (c.d * c.d_in + c.d * 2 * c.KV)
         mg = st.get("map_gemm")
@@ -739,7 +896,7 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
             "fill_frac_of_bf16_peak": f_flops / (ms / 1e3) / 1e12 / peak_tflops,
             "map_gemm_ms": mg, "map_gemm_tflops": 2.0 * n_fill * c.P * c.d * c.d_in / (mg / 1e3) / 1e12 if mg else None,
             "fill_row_layers_per_s": n_fill * c.P / (ms / 1e3), "stages_ms": st}
-        del inp, kc, vc, ws, Wkv
+        del inp, kc, vc, ws, Wk, Wv
         torch.cuda.empty_cache()
 
     if only in (None, "next1_value_rescale_27b"):
@@ -748,16 +905,12 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
         n_tail = 512
         inp = synth.fill_inputs(c, device=dev)
         x_exact = synth.rescale_inputs(c, inp["x_S"], n_tail, device=dev)
-        fd = rf.rf_fill_desc(d=c.d, L=c.L, S=c.S, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd, rope_theta=c.rope_theta,
-                             rms_eps=c.rms_eps, pos_offset=0, flags=flags)
-        Wkv = torch.empty((c.P, 2 * c.KV, c.d), dtype=torch.bfloat16, device=dev)
-        rf.rf_fold_kv_weights(fd, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
-        del inp["Wk"], inp["Wv"]
+        fd, Wk, Wv = _prefolded(c, inp, flags)
         vs = torch.empty((c.P, c.H), dtype=torch.float32, device=dev)
         wsb = rf.rf_value_scale_workspace_bytes(fd, n_tail)
         ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
         ms_scale, st_scale = _timed(lambda: rf.rf_value_scale(fd, n_tail, inp["x_S"], c.d, x_exact, c.d, inp["A"], inp["b"],
-                                                              Wkv, vs, None, ws, wsb), 3, stream)
+                                                              None, Wv, vs, None, ws, wsb), 3, stream)
         del ws
         fd.v_scale = vs.data_ptr()
         kc = torch.zeros((c.L, c.N, c.KV), dtype=torch.bfloat16, device=dev)
@@ -765,8 +918,8 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
         wsb = rf.rf_fill_workspace_bytes(fd)
         ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
         nf = torch.zeros(1, dtype=torch.int32, device=dev)
-        ms_fill, st_fill = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
-                                                        c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
+        ms_fill, st_fill = _timed(lambda: rf.rf_fill_kv(fd, inp["x_S"], c.d, inp["mask"], inp["A"], inp["b"], None, Wk, Wv,
+                                                        kc, vc, c.N * c.KV, c.KV, nf, None, ws, wsb), 3, stream)
         n_fill = int(nf.item())
         f_flops = 2.0 * n_fill * c.P * (c.d * c.d + c.d * 2 * c.KV)
         s_flops = 2.0 * n_tail * c.P * (c.d * c.d + 2 * c.d * c.KV)
@@ -777,13 +930,65 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
             "fill_ms": ms_fill, "fill_tflops": f_flops / (ms_fill / 1e3) / 1e12,
             "fill_frac_of_bf16_peak": f_flops / (ms_fill / 1e3) / 1e12 / peak_tflops,
             "fill_row_layers_per_s": n_fill * c.P / (ms_fill / 1e3), "fill_stages_ms": st_fill}
-        del inp, kc, vc, ws, Wkv, vs, x_exact
+        del inp, kc, vc, ws, Wk, Wv, vs, x_exact
         torch.cuda.empty_cache()
 
     if only in (None, "next4a_source_selection_xmodel"):
         out["next4a_source_selection_xmodel"] = run_selection(dev, peak_tflops, flags)
 
     return out
+
+
+def _solve_row(dev, d_in, d_out, P, n, lam, index, flags, peak_tflops, label):
+    """One rf_solve row: planted calibration rows accumulated on the device, then the
+    solve timed unrefined and with one refinement sweep."""
+    import torch
+
+    import ridge_map_kv_gb300 as rf
+    import synth
+    stream = torch.cuda.current_stream(dev)
+    st = _zero_stats(d_in, d_out, P, dev)
+    cs = rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
+    cd = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P, flags=flags)
+    chunk = min(n, 16384)
+    for r0 in range(0, n, chunk):      # rows generated in chunks outside the timed calls
+        cal = synth.calib_inputs(d_in, d_out, P, chunk, index=index, device=dev, salt=r0 // chunk)
+        rf.rf_calib_accumulate(cd, cal["X"], d_in, cal["Y"], d_out, chunk * d_out, chunk, cs)
+        del cal
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    A = torch.empty((P, d_out, d_in), dtype=torch.float32, device=dev)
+    b = torch.empty((P, d_out), dtype=torch.float32, device=dev)
+    Ab = torch.empty((P, d_out, d_in), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    wsb = rf.rf_solve_workspace_bytes(cd)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    row = {"workload": label, "workspace_bytes": wsb}
+    for refine in (0, 1):
+        ms, stages = _timed(lambda: rf.rf_solve(cd, cs, lam, rf.RF_ALPHA_TRACE, refine, A, b, Ab, None, status, ws,
+                                                wsb), 1, stream)
+        row[f"refine_{refine}_ms"] = ms
+        row[f"refine_{refine}_stages_ms"] = stages
+    assert int(status.item()) == 0
+    # A_p = Cc_pᵀ H^-1: 2 P d_out d_in² fp32-accurate flops, as six bf16 plane products
+    prod = 2.0 * P * d_out * d_in ** 2
+    pm = row["refine_0_stages_ms"].get("solve_product")
+    if pm:
+        row["product_fp32_tflops"] = prod / (pm / 1e3) / 1e12
+        row["product_bf16_plane_tflops"] = 6.0 * prod / (pm / 1e3) / 1e12
+        row["product_frac_of_bf16_peak"] = row["product_bf16_plane_tflops"] / peak_tflops
+    # factorisation and inverse: Cholesky d³/3, L^-1 d³/3, H^-1 = L^-ᵀL^-1 d³ (fp32-equivalent)
+    fm = row["refine_0_stages_ms"].get("solve")
+    if fm:
+        row["factor_inverse_fp32_tflops"] = (5.0 / 3.0) * d_in ** 3 / (fm / 1e3) / 1e12
+    rm = row["refine_1_stages_ms"].get("solve_refine")
+    if rm:
+        # the residual A_p H as 21 digit-pair products plus the correction R_p H^-1 (six plane products)
+        row["refine_bf16_tflops"] = (21.0 + 6.0) * prod / (rm / 1e3) / 1e12
+    row["solve_fp32_equiv_tflops_unrefined"] = (prod + (5.0 / 3.0) * d_in ** 3) / (row["refine_0_ms"] / 1e3) / 1e12
+    del st, cs, A, b, Ab, ws
+    torch.cuda.empty_cache()
+    return row
 
 
 def run_selection(dev, peak_tflops, flags=0, n_targets=0, n_sources=0):
@@ -877,6 +1082,10 @@ def run_selection(dev, peak_tflops, flags=0, n_targets=0, n_sources=0):
 # Reference arm: the fp64 oracle on the host cores
 # --------------------------------------------------------------------------- #
 def run_reference(args):
+    """The reference arm: the fp64 oracle as it stands, on the host cores, over the
+    same workload, metric and unit as our arm. Each step is a bounded sample of the
+    workload (REF_ROWS_PER_STEP filled rows x every upper layer), so that K steps end
+    within a few minutes."""
     import synth
     ws_n, rank, _ = dist_env()
     if rank != 0:
@@ -884,12 +1093,14 @@ def run_reference(args):
     cfg = workloads()[args.workload]
     inp = synth.fill_inputs(cfg, device="cpu")
     n_fill, units = fill_units(cfg, inp["mask"])
-    rows_per_step = 64
+    rows_per_step = REF_ROWS_PER_STEP
     oi = OracleInputs(cfg, inp)
+    del inp
     for _ in range(max(args.warmup, 3)):
-        cpu_oracle_rate(oi, 8, seed=0)
+        cpu_oracle_rate(oi, 2, seed=0)
     t = 0.0
     done = 0
+    cores = host_cores()
     for k in range(args.steps):
         _, dt, n, cores = cpu_oracle_rate(oi, rows_per_step, seed=100 + k)
         t += dt
@@ -905,6 +1116,9 @@ def run_reference(args):
                              "sample": f"{rows_per_step} filled rows x {cfg.P} upper layers per step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
+
+
+REF_ROWS_PER_STEP = 16
 
 
 def main(argv=None):

@@ -149,25 +149,36 @@ typedef struct rf_fill_desc {
  * additions. */
 #define RF_FLAG_SINGLE_CTA 1u
 #define RF_FLAG_CTA_PAIR 2u
+/* Flag of rf_fill_desc: the K and V projections passed to the fill already hold
+ * the RMSNorm gain, Wk[p][j][i] = W_k,p[j][i] g_p[i] (likewise Wv), for example
+ * from rf_fold_kv_weights; `gain` is then ignored and may be NULL. Without it the
+ * fill folds the gain into its workspace on every call. */
+#define RF_WEIGHTS_PREFOLDED 4u
 
 /* Supported fill shapes: d % 256 == 0, head_dim in {64, 128}, KV % 128 == 0,
- * 1 <= N - T <= 2^30 when anything is filled. */
+ * N - T <= 2^24. */
 
-/* Workspace bytes rf_fill_kv needs for `desc` (0 on invalid desc). */
+/* Workspace bytes rf_fill_kv needs for `desc` (0 on invalid desc). Without
+ * RF_WEIGHTS_PREFOLDED in desc->flags this includes 2*P*KV*d bf16 for the folded
+ * projections. */
 size_t rf_fill_workspace_bytes(const rf_fill_desc* desc);
 
-/* One-time weight preparation for rf_fill_kv: folds each layer's RMSNorm gain into
- * its K and V projections and stacks them,
- *   Wkv[p][j][i]      = bf16(Wk[p][j][i] * gain[p][i])   j <  KV
- *   Wkv[p][KV + j][i] = bf16(Wv[p][j][i] * gain[p][i])   j <  KV
- * gain [P][d], Wk and Wv [P][KV][d] (row = output channel), Wkv [P][2*KV][d]. */
+/* Weight preparation for the fill (run once per weight set, then pass the results
+ * with RF_WEIGHTS_PREFOLDED): folds each layer's RMSNorm gain into its K and V
+ * projections,
+ *   Wk_folded[p][j][i] = bf16(Wk[p][j][i] * gain[p][i]),
+ *   Wv_folded[p][j][i] = bf16(Wv[p][j][i] * gain[p][i]),
+ * gain [P][d], Wk, Wv, Wk_folded, Wv_folded [P][KV][d] (row = output channel),
+ * all device. The bf16 x bf16 product is exact in fp32, so the only rounding is
+ * the last one. In place (Wk_folded == Wk, Wv_folded == Wv) is allowed. */
 rf_status rf_fold_kv_weights(const rf_fill_desc* desc, const rf_bf16* gain,
-                             const rf_bf16* Wk, const rf_bf16* Wv, rf_bf16* Wkv,
-                             rf_stream_t stream);
+                             const rf_bf16* Wk, const rf_bf16* Wv,
+                             rf_bf16* Wk_folded, rf_bf16* Wv_folded, rf_stream_t stream);
 
 /* The fill. For every filled row t (t < N-T, exact_mask[t] == 0, ascending) and
  * every layer l = S + p:
- *   x̂ = A_p x_S[t] + b_p;  r = (mean(x̂²) + ε)^-1/2;  [k | v] = r · Wkv_p x̂;
+ *   x̂ = A_p x_S[t] + b_p;  r = (mean(x̂²) + ε)^-1/2;
+ *   k = r · (Wk_p ⊙ g_p) x̂,  v = r · (Wv_p ⊙ g_p) x̂   (g_p scales the input channels);
  *   k_h <- g_k,p ⊙ k_h / sqrt(mean(k_h²) + ε)   when desc->k_norm_gain is set;
  *   v_h <- v_scale[p][h] · v_h                  when desc->v_scale is set;
  *   k_h <- RoPE(k_h, t + pos_offset) per head;
@@ -178,16 +189,21 @@ rf_status rf_fold_kv_weights(const rf_fill_desc* desc, const rf_bf16* gain,
  *   exact_mask [N-T] uint8, nonzero = exact row (never filled); NULL = none
  *   A          [P][d][d_in] bf16, A_p[o][i] (row = output)
  *   b          [P][d] fp32
- *   Wkv        [P][2*KV][d] bf16 from rf_fold_kv_weights
+ *   gain       [P][d] bf16, the layers' RMSNorm gains (ignored with RF_WEIGHTS_PREFOLDED)
+ *   Wk, Wv     [P][KV][d] bf16, the layers' K and V projections (row = output
+ *              channel); with RF_WEIGHTS_PREFOLDED they already include the gain
+ *              (rf_fold_kv_weights), else the call folds it into its workspace
  *   k_cache, v_cache: element (l, t, h, c) at l*layer_stride + t*row_stride + h*hd + c
  *   n_fill_out device int32 (may be NULL): number of filled rows
- * Kernels: row compaction + gather, one tcgen05 GEMM for all maps (bias, bf16 x̂
- * and per-row sum-of-squares in its epilogue), one tcgen05 GEMM for all K/V
- * projections (RMS scale, RoPE and cache scatter in its epilogue). */
+ * Kernels: the gain fold (unless prefolded), row compaction + gather, one tcgen05
+ * GEMM for all maps (bias, bf16 x̂ and per-row sum-of-squares in its epilogue), one
+ * tcgen05 GEMM for all K/V projections (RMS scale, RoPE and cache scatter in its
+ * epilogue). */
 rf_status rf_fill_kv(const rf_fill_desc* desc,
                      const rf_bf16* x_S, int64_t ld_x,
                      const uint8_t* exact_mask,
-                     const rf_bf16* A, const float* b, const rf_bf16* Wkv,
+                     const rf_bf16* A, const float* b,
+                     const rf_bf16* gain, const rf_bf16* Wk, const rf_bf16* Wv,
                      rf_bf16* k_cache, rf_bf16* v_cache,
                      int64_t layer_stride, int64_t row_stride,
                      int32_t* n_fill_out, int32_t* dev_status,
@@ -199,7 +215,8 @@ rf_status rf_fill_kv(const rf_fill_desc* desc,
  * all belongs to the engine's own pool, or a latency-critical path where a
  * cudaMalloc would synchronise the device. This call computes exactly what
  * rf_fill_kv computes, with the same arguments minus the workspace: its scratch
- * is a fixed 256-byte aligned array of RF_STATIC_SCRATCH_BYTES inside the
+ * (including the gain fold, unless the weights are prefolded) is a fixed 256-byte
+ * aligned array of RF_STATIC_SCRATCH_BYTES inside the
  * library's device code, which every GPU that loads the library keeps until the
  * process exits. It makes no allocating call.
  *   - Fills whose rf_fill_workspace_bytes(desc) exceeds RF_STATIC_SCRATCH_BYTES
@@ -215,7 +232,8 @@ rf_status rf_fill_kv(const rf_fill_desc* desc,
 rf_status rf_fill_kv_static(const rf_fill_desc* desc,
                             const rf_bf16* x_S, int64_t ld_x,
                             const uint8_t* exact_mask,
-                            const rf_bf16* A, const float* b, const rf_bf16* Wkv,
+                            const rf_bf16* A, const float* b,
+                            const rf_bf16* gain, const rf_bf16* Wk, const rf_bf16* Wv,
                             rf_bf16* k_cache, rf_bf16* v_cache,
                             int64_t layer_stride, int64_t row_stride,
                             int32_t* n_fill_out, int32_t* dev_status, rf_stream_t stream);
@@ -226,7 +244,9 @@ rf_status rf_fill_kv_static(const rf_fill_desc* desc,
  *   v_scale[p*H + h] = mean over t in [0, c) of ||v_exact_h(t)|| / ||v_pred_h(t)||
  *   v_pred(t)  = r(x̂) · Wv'_p x̂,  x̂ = bf16(A_p x_S[N-T+t] + b_p)   (as in the fill)
  *   v_exact(t) = r(x)  · Wv'_p x,  x  = x_exact[p][t]
- * where Wv'_p is the V half of Wkv (gain folded), r(x) = (mean(x²) + ε)^-1/2 and
+ * where Wv'_p = bf16(Wv_p ⊙ g_p) is the gain-folded V projection (Wv as given with
+ * RF_WEIGHTS_PREFOLDED in desc->flags, else folded into the workspace from `gain`
+ * and `Wv`, both [P][KV][d] / [P][d] bf16), r(x) = (mean(x²) + ε)^-1/2 and
  * ||.|| is the L2 norm of the head's hd values. Rows whose predicted norm is 0 are
  * left out of a head's mean (scale 1 if none is left). The result is meant for
  * rf_fill_desc.v_scale.
@@ -234,7 +254,7 @@ rf_status rf_fill_kv_static(const rf_fill_desc* desc,
  *   x_S, ld_x as for rf_fill_kv (only rows N-T .. N-T+c-1 are read)
  *   x_exact   [P][c][ld_e] bf16 (device): the exact inputs of layers S .. L-1
  *             at those rows (the tail runs every layer exactly)
- *   A, b, Wkv as for rf_fill_kv;  v_scale  [P][H] fp32 (device), written
+ *   A, b, gain, Wv as for rf_fill_kv;  v_scale  [P][H] fp32 (device), written
  * Requires d % 256 == 0, head_dim 64 or 128, KV % 128 == 0, S < L. Kernels: the
  * fill's map GEMM on the c tail rows, one tcgen05 GEMM for the V projections of
  * the predicted and the exact rows with per-head norms in its epilogue, and a
@@ -243,7 +263,8 @@ size_t rf_value_scale_workspace_bytes(const rf_fill_desc* desc, int64_t c);
 rf_status rf_value_scale(const rf_fill_desc* desc, int64_t c,
                          const rf_bf16* x_S, int64_t ld_x,
                          const rf_bf16* x_exact, int64_t ld_e,
-                         const rf_bf16* A, const float* b, const rf_bf16* Wkv,
+                         const rf_bf16* A, const float* b,
+                         const rf_bf16* gain, const rf_bf16* Wv,
                          float* v_scale, int32_t* dev_status,
                          void* workspace, size_t workspace_bytes, rf_stream_t stream);
 
@@ -279,14 +300,16 @@ typedef struct rf_map_source {
  * scales are applied to the map GEMM's output
  * columns with the bias. Device bf16 maps are read in place. The results equal
  * rf_fill_kv's bit for bit when the maps are the same bf16 values (same kernels,
- * same summation order). Arguments as for rf_fill_kv, with `maps` replacing A;
- * the workspace is rf_fill_layered_workspace_bytes(desc, maps). Everything is
- * asynchronous on `stream`. */
+ * same summation order). Arguments as for rf_fill_kv, with `maps` replacing A
+ * (gain, Wk, Wv and RF_WEIGHTS_PREFOLDED as there); the workspace is
+ * rf_fill_layered_workspace_bytes(desc, maps). Everything is asynchronous on
+ * `stream`. */
 size_t rf_fill_layered_workspace_bytes(const rf_fill_desc* desc, const rf_map_source* maps);
 rf_status rf_fill_kv_layered(const rf_fill_desc* desc,
                              const rf_bf16* x_S, int64_t ld_x,
                              const uint8_t* exact_mask,
-                             const rf_map_source* maps, const float* b, const rf_bf16* Wkv,
+                             const rf_map_source* maps, const float* b,
+                             const rf_bf16* gain, const rf_bf16* Wk, const rf_bf16* Wv,
                              rf_bf16* k_cache, rf_bf16* v_cache,
                              int64_t layer_stride, int64_t row_stride,
                              int32_t* n_fill_out, int32_t* dev_status,
@@ -386,7 +409,10 @@ size_t rf_xmodel_workspace_bytes(const rf_xmodel_desc* desc);
  *   F_K = [RoPE_src^-1(k_src[s_j][t]) for j < k] (feature order: j, head, dim),
  *   F_V = [v_src[s_j][t] for j < k],  s_j = src_layers[l*k + j],
  *   k_tgt[l][t] = bf16(RoPE_tgt(F_K Wk_lᵀ + bk_l)),  v_tgt[l][t] = bf16(F_V Wv_lᵀ + bv_l).
- *   src_layers  HOST int32 [L_tgt][k], each in [0, L_src) (copied before return)
+ *   src_layers  device int32 [L_tgt][k], each in [0, L_src) (e.g. rf_select_sources'
+ *               output, used with no host round trip). The table is checked on the
+ *               device: an entry outside [0, L_src) writes RF_ERR_INVALID_ARG to
+ *               *dev_status and the call then writes no target entry.
  *   k_src, v_src [L_src][N][KV] bf16;  k_tgt, v_tgt [L_tgt][N][KV] bf16
  *   Wk, Wv [L_tgt][KV][k*KV] bf16 (row = output);  bk, bv [L_tgt][KV] fp32 */
 rf_status rf_xmodel_map(const rf_xmodel_desc* desc, const int32_t* src_layers,

@@ -35,6 +35,7 @@ class RFError(RuntimeError):
 
 RF_FLAG_SINGLE_CTA = 1
 RF_FLAG_CTA_PAIR = 2
+RF_WEIGHTS_PREFOLDED = 4
 
 
 RF_MAPS_BF16 = 0
@@ -83,21 +84,23 @@ _SIGS = {
     "rf_profile_stop": (c_int, [POINTER(c_int32), POINTER(ctypes.c_float), c_int]),
     "rf_stage_name": (c_char_p, [c_int]),
     "rf_fill_workspace_bytes": (c_size_t, [POINTER(rf_fill_desc)]),
-    "rf_fold_kv_weights": (c_int, [POINTER(rf_fill_desc), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "rf_fold_kv_weights": (c_int, [POINTER(rf_fill_desc), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                   c_void_p]),
     "rf_fill_kv": (c_int, [POINTER(rf_fill_desc), c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p,
-                           c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p, c_size_t,
-                           c_void_p]),
+                           c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
+                           c_size_t, c_void_p]),
     "rf_fill_kv_static": (c_int, [POINTER(rf_fill_desc), c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
-                                  c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p]),
+                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p,
+                                  c_void_p, c_void_p]),
     "rf_selftest_wait_timeout": (c_int, [c_int, c_void_p, c_void_p]),
     "rf_quantize_maps_int8": (c_int, [POINTER(rf_fill_desc), c_void_p, c_void_p, c_void_p, c_void_p]),
     "rf_fill_layered_workspace_bytes": (c_size_t, [POINTER(rf_fill_desc), POINTER(rf_map_source)]),
     "rf_fill_kv_layered": (c_int, [POINTER(rf_fill_desc), c_void_p, c_int64, c_void_p, POINTER(rf_map_source),
-                                   c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p,
-                                   c_void_p, c_size_t, c_void_p]),
+                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64,
+                                   c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "rf_value_scale_workspace_bytes": (c_size_t, [POINTER(rf_fill_desc), c_int64]),
     "rf_value_scale": (c_int, [POINTER(rf_fill_desc), c_int64, c_void_p, c_int64, c_void_p, c_int64, c_void_p,
-                               c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+                               c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "rf_calib_workspace_bytes": (c_size_t, [POINTER(rf_calib_desc), c_int64]),
     "rf_calib_accumulate": (c_int, [POINTER(rf_calib_desc), c_void_p, c_int64, c_void_p, c_int64, c_int64,
                                     c_int64, POINTER(rf_calib_stats), c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -105,7 +108,7 @@ _SIGS = {
     "rf_solve": (c_int, [POINTER(rf_calib_desc), POINTER(rf_calib_stats), c_double, c_int, c_int, c_void_p,
                          c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "rf_xmodel_workspace_bytes": (c_size_t, [POINTER(rf_xmodel_desc)]),
-    "rf_xmodel_map": (c_int, [POINTER(rf_xmodel_desc), POINTER(c_int32), c_void_p, c_void_p, c_void_p, c_void_p,
+    "rf_xmodel_map": (c_int, [POINTER(rf_xmodel_desc), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                               c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "rf_rope_rows": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_double, c_int64, c_int,
                              c_void_p]),
@@ -204,28 +207,29 @@ def rf_fill_workspace_bytes(desc: rf_fill_desc) -> int:
     return int(lib().rf_fill_workspace_bytes(ctypes.byref(desc)))
 
 
-def rf_fold_kv_weights(desc, gain, Wk, Wv, Wkv, stream=None):
-    _check(lib().rf_fold_kv_weights(ctypes.byref(desc), _p(gain), _p(Wk), _p(Wv), _p(Wkv), _s(stream)),
-           "rf_fold_kv_weights")
+def rf_fold_kv_weights(desc, gain, Wk, Wv, Wk_folded, Wv_folded, stream=None):
+    _check(lib().rf_fold_kv_weights(ctypes.byref(desc), _p(gain), _p(Wk), _p(Wv), _p(Wk_folded), _p(Wv_folded),
+                                    _s(stream)), "rf_fold_kv_weights")
 
 
-def rf_fill_kv(desc, x_S, ld_x, exact_mask, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride,
+def rf_fill_kv(desc, x_S, ld_x, exact_mask, A, b, gain, Wk, Wv, k_cache, v_cache, layer_stride, row_stride,
                n_fill_out=None, dev_status=None, workspace=None, workspace_bytes=0, stream=None):
-    _check(lib().rf_fill_kv(ctypes.byref(desc), _p(x_S), int(ld_x), _p(exact_mask), _p(A), _p(b), _p(Wkv),
-                            _p(k_cache), _p(v_cache), int(layer_stride), int(row_stride), _p(n_fill_out),
+    """The fill; with RF_WEIGHTS_PREFOLDED in desc.flags, Wk and Wv hold the gain and ``gain`` may be None."""
+    _check(lib().rf_fill_kv(ctypes.byref(desc), _p(x_S), int(ld_x), _p(exact_mask), _p(A), _p(b), _p(gain), _p(Wk),
+                            _p(Wv), _p(k_cache), _p(v_cache), int(layer_stride), int(row_stride), _p(n_fill_out),
                             _p(dev_status), _p(workspace), int(workspace_bytes), _s(stream)), "rf_fill_kv")
 
 
 RF_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
-def rf_fill_kv_static(desc, x_S, ld_x, exact_mask, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride,
+def rf_fill_kv_static(desc, x_S, ld_x, exact_mask, A, b, gain, Wk, Wv, k_cache, v_cache, layer_stride, row_stride,
                       n_fill_out=None, dev_status=None, stream=None):
     """rf_fill_kv for callers that cannot allocate device memory: the library's own
     fixed 64 MiB device array serves as scratch (see include/rf.h)."""
-    _check(lib().rf_fill_kv_static(ctypes.byref(desc), _p(x_S), int(ld_x), _p(exact_mask), _p(A), _p(b), _p(Wkv),
-                                   _p(k_cache), _p(v_cache), int(layer_stride), int(row_stride), _p(n_fill_out),
-                                   _p(dev_status), _s(stream)), "rf_fill_kv_static")
+    _check(lib().rf_fill_kv_static(ctypes.byref(desc), _p(x_S), int(ld_x), _p(exact_mask), _p(A), _p(b), _p(gain),
+                                   _p(Wk), _p(Wv), _p(k_cache), _p(v_cache), int(layer_stride), int(row_stride),
+                                   _p(n_fill_out), _p(dev_status), _s(stream)), "rf_fill_kv_static")
 
 
 def rf_selftest_wait_timeout(cta_pair, dev_status, stream=None):
@@ -248,11 +252,12 @@ def rf_fill_layered_workspace_bytes(desc, maps) -> int:
     return int(lib().rf_fill_layered_workspace_bytes(ctypes.byref(desc), ctypes.byref(maps)))
 
 
-def rf_fill_kv_layered(desc, x_S, ld_x, exact_mask, maps, b, Wkv, k_cache, v_cache, layer_stride, row_stride,
-                       n_fill_out=None, dev_status=None, workspace=None, workspace_bytes=0, stream=None):
+def rf_fill_kv_layered(desc, x_S, ld_x, exact_mask, maps, b, gain, Wk, Wv, k_cache, v_cache, layer_stride,
+                       row_stride, n_fill_out=None, dev_status=None, workspace=None, workspace_bytes=0, stream=None):
     """rf_fill_kv one layer at a time, maps from the device or the host, bf16 or int8 (see include/rf.h)."""
     _check(lib().rf_fill_kv_layered(ctypes.byref(desc), _p(x_S), int(ld_x), _p(exact_mask), ctypes.byref(maps),
-                                    _p(b), _p(Wkv), _p(k_cache), _p(v_cache), int(layer_stride), int(row_stride),
+                                    _p(b), _p(gain), _p(Wk), _p(Wv), _p(k_cache), _p(v_cache), int(layer_stride),
+                                    int(row_stride),
                                     _p(n_fill_out), _p(dev_status), _p(workspace), int(workspace_bytes),
                                     _s(stream)), "rf_fill_kv_layered")
 
@@ -261,11 +266,11 @@ def rf_value_scale_workspace_bytes(desc: rf_fill_desc, c: int) -> int:
     return int(lib().rf_value_scale_workspace_bytes(ctypes.byref(desc), int(c)))
 
 
-def rf_value_scale(desc, c, x_S, ld_x, x_exact, ld_e, A, b, Wkv, v_scale, dev_status=None, workspace=None,
+def rf_value_scale(desc, c, x_S, ld_x, x_exact, ld_e, A, b, gain, Wv, v_scale, dev_status=None, workspace=None,
                    workspace_bytes=0, stream=None):
     """Per-(layer, KV head) value-rescale factors into v_scale [P][H] fp32 (see include/rf.h)."""
     _check(lib().rf_value_scale(ctypes.byref(desc), int(c), _p(x_S), int(ld_x), _p(x_exact), int(ld_e), _p(A), _p(b),
-                                _p(Wkv), _p(v_scale), _p(dev_status), _p(workspace), int(workspace_bytes),
+                                _p(gain), _p(Wv), _p(v_scale), _p(dev_status), _p(workspace), int(workspace_bytes),
                                 _s(stream)), "rf_value_scale")
 
 
@@ -304,10 +309,8 @@ def rf_xmodel_workspace_bytes(desc: rf_xmodel_desc) -> int:
 
 def rf_xmodel_map(desc, src_layers, k_src, v_src, Wk, bk, Wv, bv, k_tgt, v_tgt, dev_status=None,
                   workspace=None, workspace_bytes=0, stream=None):
-    """``src_layers``: host int32 array-like [L_tgt][k]."""
-    import numpy as np
-    tab = np.ascontiguousarray(np.asarray(src_layers, dtype=np.int32).reshape(-1))
-    _check(lib().rf_xmodel_map(ctypes.byref(desc), tab.ctypes.data_as(POINTER(c_int32)), _p(k_src), _p(v_src),
+    """``src_layers``: device int32 tensor [L_tgt][k] (e.g. rf_select_sources' output)."""
+    _check(lib().rf_xmodel_map(ctypes.byref(desc), _p(src_layers), _p(k_src), _p(v_src),
                                _p(Wk), _p(bk), _p(Wv), _p(bv), _p(k_tgt), _p(v_tgt), _p(dev_status),
                                _p(workspace), int(workspace_bytes), _s(stream)), "rf_xmodel_map")
 

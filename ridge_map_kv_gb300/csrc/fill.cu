@@ -6,12 +6,14 @@
 // (x̂_l = A_l x_S + b_l, then the layer's own norm, K/V projections and RoPE).
 //
 // Launch sequence on the caller's stream (no host synchronisation):
+//   0. k_fold_gain     (unless RF_WEIGHTS_PREFOLDED) W_k·diag(g), W_v·diag(g)
+//                      into the workspace
 //   1. k_compact       exact-row mask -> ascending fill_idx, n_fill        (1 CTA)
 //   2. k_gather_rows   Xf[m] = x_S[fill_idx[m]], zero pad to the M tile     (HBM)
 //   3. k_rope_table    cos/sin of (t + pos_offset) * θ^(-2i/hd), fp64 angle (tiny)
 //   4. tc_gemm<MapProb> x̂ = Xf · [A_S; …; A_{L-1}]ᵀ + b, all maps in one GEMM;
 //                       epilogue: bf16 x̂ and fp32 Σx̂² per (row, layer, N-tile)
-//   5. tc_gemm<KVProb>  [k|v] = r · x̂_l · Wkv_lᵀ for every layer in one GEMM;
+//   5. tc_gemm<KVProb>  [k|v] = r · x̂_l · [Wk'_l; Wv'_l]ᵀ for every layer in one GEMM;
 //                       epilogue: r = rsqrt(Σx̂²/d + ε), RoPE on k, scatter
 //                       into cache[l][fill_idx[m]] with 16-byte stores.
 #include <algorithm>
@@ -112,20 +114,17 @@ __global__ void __launch_bounds__(256) k_rope_table(float* __restrict__ cos_t, f
 }
 
 // --------------------------------------------------------------------------
-// Gain fold: Wkv[p][j][i] = bf16(W[p][j][i] * g[p][i]); the bf16 x bf16 product
-// is exact in fp32, so the only rounding is the final one.
+// Gain fold: out[p][j][i] = bf16(W[p][j][i] * g[p][i]) for one projection
+// [P][rows][d]; the bf16 x bf16 product is exact in fp32, so the only rounding is
+// the final one. 16 bytes per step; in place is allowed.
 // --------------------------------------------------------------------------
-__global__ void k_fold_gain(const uint4* __restrict__ gain, const uint4* __restrict__ Wk,
-                            const uint4* __restrict__ Wv, uint4* __restrict__ Wkv, int P, int KV, int d_vec) {
-  const long long total = static_cast<long long>(P) * 2 * KV * d_vec;
+__global__ void k_fold_gain(const uint4* __restrict__ gain, const uint4* W, uint4* out, int P, int rows, int d_vec) {
+  const long long total = static_cast<long long>(P) * rows * d_vec;
   for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int c = static_cast<int>(idx % d_vec);
-    const long long r = idx / d_vec;
-    const int j = static_cast<int>(r % (2 * KV));
-    const int p = static_cast<int>(r / (2 * KV));
-    const uint4 w = j < KV ? __ldg(Wk + (static_cast<long long>(p) * KV + j) * d_vec + c)
-                           : __ldg(Wv + (static_cast<long long>(p) * KV + (j - KV)) * d_vec + c);
+    const int p = static_cast<int>(idx / (static_cast<long long>(rows) * d_vec));
+    const uint4 w = W[idx];
     const uint4 g = __ldg(gain + static_cast<long long>(p) * d_vec + c);
     const __nv_bfloat162* wh = reinterpret_cast<const __nv_bfloat162*>(&w);
     const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&g);
@@ -137,8 +136,19 @@ __global__ void k_fold_gain(const uint4* __restrict__ gain, const uint4* __restr
       const float2 b = __bfloat1622float2(gh[q]);
       ou[q] = pack_bf16x2(a.x * b.x, a.y * b.y);
     }
-    Wkv[idx] = o;
+    out[idx] = o;
   }
+}
+
+rf_status fold_gain(const void* gain, const void* W, void* out, int64_t P, int64_t rows, int64_t d, int sms,
+                    cudaStream_t s) {
+  const long long total = P * rows * (d / 8);
+  const int blocks = static_cast<int>(std::max<long long>(1, std::min<long long>((total + 255) / 256, 8LL * sms)));
+  ProfScope prof(s, RF_STAGE_FOLD);
+  k_fold_gain<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(gain), static_cast<const uint4*>(W),
+                                     static_cast<uint4*>(out), static_cast<int>(P), static_cast<int>(rows),
+                                     static_cast<int>(d / 8));
+  return cuda_check(cudaGetLastError(), "k_fold_gain launch");
 }
 
 // --------------------------------------------------------------------------
@@ -154,6 +164,8 @@ struct FillLayout {
   float* rope_sin;
   __nv_bfloat16* slot[2];   // layered fill: bf16 map ring (when maps are copied or expanded)
   int8_t* stage[2];         // layered fill: int8 landing slots for host int8 maps
+  __nv_bfloat16* wk;        // gain-folded projections [P][KV][d] (without RF_WEIGHTS_PREFOLDED)
+  __nv_bfloat16* wv;
   size_t bytes;
 };
 
@@ -168,6 +180,8 @@ static bool maps_staged(const rf_map_source* m) { return !(m->kind == RF_MAPS_BF
 
 // Width of x_S rows and of the maps' input (d_in = 0 means square maps).
 static int64_t fill_din(const rf_fill_desc* d) { return d->d_in > 0 ? d->d_in : d->d; }
+
+static bool prefolded(const rf_fill_desc* d) { return (d->flags & RF_WEIGHTS_PREFOLDED) != 0; }
 
 static rf_status check_fill_desc(const rf_fill_desc* d) {
   if (d == nullptr) return fail(RF_ERR_INVALID_ARG, "desc is NULL");
@@ -204,6 +218,11 @@ static FillLayout fill_layout(const rf_fill_desc* d, void* ws, const rf_map_sour
   l.ssp = c.take<float>(xhat_layers * (d->d / kBN) * M_pad);
   l.rope_cos = c.take<float>(std::max<int64_t>(n_prefix, 1) * (d->head_dim / 2));
   l.rope_sin = c.take<float>(std::max<int64_t>(n_prefix, 1) * (d->head_dim / 2));
+  if (!prefolded(d) && P > 0 && n_prefix > 0) {
+    const int64_t w = P * d->n_kv_heads * d->head_dim * d->d;
+    l.wk = c.take<__nv_bfloat16>(w);
+    l.wv = c.take<__nv_bfloat16>(w);
+  }
   if (maps != nullptr && maps_staged(maps)) {
     const int64_t n = xhat_layers * d->d * fill_din(d);
     for (int i = 0; i < 2; ++i) l.slot[i] = c.take<__nv_bfloat16>(n);
@@ -216,7 +235,7 @@ static FillLayout fill_layout(const rf_fill_desc* d, void* ws, const rf_map_sour
 
 // The two fill GEMMs, on CTA pairs or single CTAs.
 static rf_status fill_gemms(bool pair, const rf_fill_desc* desc, const FillLayout& lay, const rf_bf16* A,
-                            const float* b, const rf_bf16* Wkv, rf_bf16* k_cache, rf_bf16* v_cache,
+                            const float* b, const void* Wk, const void* Wv, rf_bf16* k_cache, rf_bf16* v_cache,
                             int64_t layer_stride, int64_t row_stride, int32_t* dev_status, int sms, cudaStream_t s) {
   rf_status st;
   const int64_t d = desc->d, P = desc->L - desc->S, KV = desc->n_kv_heads * desc->head_dim;
@@ -224,7 +243,7 @@ static rf_status fill_gemms(bool pair, const rf_fill_desc* desc, const FillLayou
   const int64_t d_in = fill_din(desc);
   MapGemmArgs ma{lay.xf, d_in, M_pad, lay.n_fill, A, b, nullptr, lay.xhat, lay.ssp, d, d_in, P, M_pad, dev_status};
   if ((st = map_gemm(pair, ma, sms, s)) != RF_OK) return st;
-  KvGemmArgs ka{lay.xhat, lay.ssp, lay.n_fill, lay.fill_idx, lay.rope_cos, lay.rope_sin, Wkv, k_cache, v_cache,
+  KvGemmArgs ka{lay.xhat, lay.ssp, lay.n_fill, lay.fill_idx, lay.rope_cos, lay.rope_sin, Wk, Wv, k_cache, v_cache,
                 desc->v_scale, desc->k_norm_gain, layer_stride, row_stride, d, P, desc->S, M_pad, KV,
                 desc->head_dim, desc->rms_eps, dev_status};
   return kv_gemm(pair, ka, sms, s);
@@ -280,7 +299,8 @@ static rf_status kv_gemm_t(const KvGemmArgs& a, int sms, cudaStream_t s) {
   rf_status st;
   KVProb<kPair> pr;
   if ((st = make_tmap_bf16_2d(&pr.tmA, a.xhat, a.d, a.P * a.M_pad, a.d, kBK, kBM)) != RF_OK) return st;
-  if ((st = make_tmap_bf16_2d(&pr.tmB, a.Wkv, a.d, a.P * 2 * a.KV, a.d, kBK, Cfg::kBRows)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmBk, a.Wk, a.d, a.P * a.KV, a.d, kBK, kKvBoxRows)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmBv, a.Wv, a.d, a.P * a.KV, a.d, kBK, kKvBoxRows)) != RF_OK) return st;
   pr.n_fill = a.n_fill;
   pr.fill_idx = a.fill_idx;
   pr.ssp = a.ssp;
@@ -329,46 +349,63 @@ extern "C" size_t rf_fill_workspace_bytes(const rf_fill_desc* desc) {
 }
 
 extern "C" rf_status rf_fold_kv_weights(const rf_fill_desc* desc, const rf_bf16* gain, const rf_bf16* Wk,
-                                        const rf_bf16* Wv, rf_bf16* Wkv, rf_stream_t stream) {
+                                        const rf_bf16* Wv, rf_bf16* Wk_folded, rf_bf16* Wv_folded,
+                                        rf_stream_t stream) {
   clear_error();
   rf_status st = check_fill_desc(desc);
   if (st != RF_OK) return st;
   const int64_t P = desc->L - desc->S;
   if (P == 0) return RF_OK;
-  if (!gain || !Wk || !Wv || !Wkv) return fail(RF_ERR_INVALID_ARG, "gain, Wk, Wv and Wkv must be non-NULL");
-  if (!aligned16(gain) || !aligned16(Wk) || !aligned16(Wv) || !aligned16(Wkv))
-    return fail(RF_ERR_ALIGN, "gain, Wk, Wv, Wkv must be 16-byte aligned");
+  if (!gain || !Wk || !Wv || !Wk_folded || !Wv_folded)
+    return fail(RF_ERR_INVALID_ARG, "gain, Wk, Wv, Wk_folded and Wv_folded must be non-NULL");
+  if (!aligned16(gain) || !aligned16(Wk) || !aligned16(Wv) || !aligned16(Wk_folded) || !aligned16(Wv_folded))
+    return fail(RF_ERR_ALIGN, "gain, Wk, Wv, Wk_folded and Wv_folded must be 16-byte aligned");
   int sms = 0;
   if ((st = current_device(&sms)) != RF_OK) return st;
-  const int KV = static_cast<int>(desc->n_kv_heads * desc->head_dim);
-  const int d_vec = static_cast<int>(desc->d / 8);
-  const long long total = P * 2LL * KV * d_vec;
-  const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 8LL * sms));
-  ProfScope prof(static_cast<cudaStream_t>(stream), RF_STAGE_FOLD);
-  k_fold_gain<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const uint4*>(gain), reinterpret_cast<const uint4*>(Wk), reinterpret_cast<const uint4*>(Wv),
-      reinterpret_cast<uint4*>(Wkv), static_cast<int>(P), KV, d_vec);
-  return cuda_check(cudaGetLastError(), "k_fold_gain launch");
+  const int64_t KV = desc->n_kv_heads * desc->head_dim;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = fold_gain(gain, Wk, Wk_folded, P, KV, desc->d, sms, s)) != RF_OK) return st;
+  return fold_gain(gain, Wv, Wv_folded, P, KV, desc->d, sms, s);
 }
 
 // Argument checks shared by rf_fill_kv and rf_fill_kv_layered (the maps are
 // checked by the caller).
 static rf_status check_fill_args(const rf_fill_desc* desc, const rf_bf16* x_S, int64_t ld_x, const float* b,
-                                 const rf_bf16* Wkv, const rf_bf16* k_cache, const rf_bf16* v_cache,
-                                 int64_t layer_stride, int64_t row_stride) {
+                                 const rf_bf16* gain, const rf_bf16* Wk, const rf_bf16* Wv, const rf_bf16* k_cache,
+                                 const rf_bf16* v_cache, int64_t layer_stride, int64_t row_stride) {
   const int64_t n_prefix = desc->N - desc->T;
   const int64_t P = desc->L - desc->S;
   const int64_t KV = desc->n_kv_heads * desc->head_dim;
   if (n_prefix > 0 && P > 0) {
     if (!x_S) return fail(RF_ERR_INVALID_ARG, "x_S is NULL");
-    if (!b || !Wkv || !k_cache || !v_cache) return fail(RF_ERR_INVALID_ARG, "A, b, Wkv, k_cache, v_cache must be non-NULL");
-    if (!aligned16(x_S) || !aligned16(b) || !aligned16(Wkv) || !aligned16(k_cache) || !aligned16(v_cache))
-      return fail(RF_ERR_ALIGN, "x_S, A, b, Wkv and the caches must be 16-byte aligned");
+    if (!b || !Wk || !Wv || !k_cache || !v_cache)
+      return fail(RF_ERR_INVALID_ARG, "A, b, Wk, Wv, k_cache, v_cache must be non-NULL");
+    if (!prefolded(desc) && !gain)
+      return fail(RF_ERR_INVALID_ARG, "gain is NULL (set RF_WEIGHTS_PREFOLDED when Wk and Wv hold the gain)");
+    if (!aligned16(x_S) || !aligned16(b) || !aligned16(Wk) || !aligned16(Wv) || !aligned16(k_cache) ||
+        !aligned16(v_cache) || (!prefolded(desc) && !aligned16(gain)))
+      return fail(RF_ERR_ALIGN, "x_S, A, b, gain, Wk, Wv and the caches must be 16-byte aligned");
     if (ld_x < fill_din(desc) || ld_x % 8 != 0)
       return fail(RF_ERR_ALIGN, "ld_x must be >= d_in (d for square maps) and a multiple of 8");
     if (row_stride < KV || row_stride % 8 != 0 || layer_stride < 0 || layer_stride % 8 != 0)
       return fail(RF_ERR_ALIGN, "row_stride must be >= H*hd and a multiple of 8; layer_stride a multiple of 8");
   }
+  return RF_OK;
+}
+
+// The projections the K/V GEMM reads: the caller's when prefolded, else the gain
+// folded into the workspace now (on stream s, ahead of the GEMMs).
+static rf_status kv_weights(const rf_fill_desc* desc, const FillLayout& lay, const rf_bf16* gain, const rf_bf16* Wk,
+                            const rf_bf16* Wv, int sms, cudaStream_t s, const void** wk, const void** wv) {
+  *wk = Wk;
+  *wv = Wv;
+  if (prefolded(desc)) return RF_OK;
+  const int64_t P = desc->L - desc->S, KV = desc->n_kv_heads * desc->head_dim;
+  rf_status st;
+  if ((st = fold_gain(gain, Wk, lay.wk, P, KV, desc->d, sms, s)) != RF_OK) return st;
+  if ((st = fold_gain(gain, Wv, lay.wv, P, KV, desc->d, sms, s)) != RF_OK) return st;
+  *wk = lay.wk;
+  *wv = lay.wv;
   return RF_OK;
 }
 
@@ -411,17 +448,19 @@ static rf_status fill_prologue(const rf_fill_desc* desc, const rf_bf16* x_S, int
 }
 
 extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, int64_t ld_x, const uint8_t* exact_mask,
-                                const rf_bf16* A, const float* b, const rf_bf16* Wkv, rf_bf16* k_cache,
-                                rf_bf16* v_cache, int64_t layer_stride, int64_t row_stride, int32_t* n_fill_out,
-                                int32_t* dev_status, void* workspace, size_t workspace_bytes, rf_stream_t stream) {
+                                const rf_bf16* A, const float* b, const rf_bf16* gain, const rf_bf16* Wk,
+                                const rf_bf16* Wv, rf_bf16* k_cache, rf_bf16* v_cache, int64_t layer_stride,
+                                int64_t row_stride, int32_t* n_fill_out, int32_t* dev_status, void* workspace,
+                                size_t workspace_bytes, rf_stream_t stream) {
   clear_error();
   rf_status st = check_fill_desc(desc);
   if (st != RF_OK) return st;
-  if ((st = check_fill_args(desc, x_S, ld_x, b, Wkv, k_cache, v_cache, layer_stride, row_stride)) != RF_OK) return st;
+  if ((st = check_fill_args(desc, x_S, ld_x, b, gain, Wk, Wv, k_cache, v_cache, layer_stride, row_stride)) != RF_OK)
+    return st;
   const int64_t n_prefix = desc->N - desc->T;
   if (n_prefix > 0 && desc->L > desc->S) {
-    if (!A) return fail(RF_ERR_INVALID_ARG, "A, b, Wkv, k_cache, v_cache must be non-NULL");
-    if (!aligned16(A)) return fail(RF_ERR_ALIGN, "x_S, A, b, Wkv and the caches must be 16-byte aligned");
+    if (!A) return fail(RF_ERR_INVALID_ARG, "A, b, Wk, Wv, k_cache, v_cache must be non-NULL");
+    if (!aligned16(A)) return fail(RF_ERR_ALIGN, "x_S, A, b, gain, Wk, Wv and the caches must be 16-byte aligned");
   }
   FillLayout lay = fill_layout(desc, workspace);
   if (n_prefix > 0) {
@@ -433,7 +472,9 @@ extern "C" rf_status rf_fill_kv(const rf_fill_desc* desc, const rf_bf16* x_S, in
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   bool work = false;
   if ((st = fill_prologue(desc, x_S, ld_x, exact_mask, n_fill_out, lay, sms, s, &work)) != RF_OK || !work) return st;
-  return fill_gemms(use_pair(desc->flags, true), desc, lay, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride,
+  const void *wk = nullptr, *wv = nullptr;
+  if ((st = kv_weights(desc, lay, gain, Wk, Wv, sms, s, &wk, &wv)) != RF_OK) return st;
+  return fill_gemms(use_pair(desc->flags, true), desc, lay, A, b, wk, wv, k_cache, v_cache, layer_stride, row_stride,
                     dev_status, sms, s);
 }
 
@@ -473,14 +514,16 @@ extern "C" size_t rf_fill_layered_workspace_bytes(const rf_fill_desc* desc, cons
 
 extern "C" rf_status rf_fill_kv_layered(const rf_fill_desc* desc, const rf_bf16* x_S, int64_t ld_x,
                                         const uint8_t* exact_mask, const rf_map_source* maps, const float* b,
-                                        const rf_bf16* Wkv, rf_bf16* k_cache, rf_bf16* v_cache, int64_t layer_stride,
+                                        const rf_bf16* gain, const rf_bf16* Wk, const rf_bf16* Wv, rf_bf16* k_cache,
+                                        rf_bf16* v_cache, int64_t layer_stride,
                                         int64_t row_stride, int32_t* n_fill_out, int32_t* dev_status, void* workspace,
                                         size_t workspace_bytes, rf_stream_t stream) {
   clear_error();
   rf_status st = check_fill_desc(desc);
   if (st != RF_OK) return st;
   if ((st = check_maps(maps)) != RF_OK) return st;
-  if ((st = check_fill_args(desc, x_S, ld_x, b, Wkv, k_cache, v_cache, layer_stride, row_stride)) != RF_OK) return st;
+  if ((st = check_fill_args(desc, x_S, ld_x, b, gain, Wk, Wv, k_cache, v_cache, layer_stride, row_stride)) != RF_OK)
+    return st;
   const int64_t n_prefix = desc->N - desc->T;
   const int64_t P = desc->L - desc->S, d = desc->d, d_in = fill_din(desc), KV = desc->n_kv_heads * desc->head_dim;
   const bool int8 = maps->kind == RF_MAPS_INT8;
@@ -513,6 +556,8 @@ extern "C" rf_status rf_fill_kv_layered(const rf_fill_desc* desc, const rf_bf16*
   }
   bool work = false;
   if ((st = fill_prologue(desc, x_S, ld_x, exact_mask, n_fill_out, lay, sms, s, &work)) != RF_OK || !work) return st;
+  const void *wk = nullptr, *wv = nullptr;
+  if ((st = kv_weights(desc, lay, gain, Wk, Wv, sms, s, &wk, &wv)) != RF_OK) return st;
 
   const bool pair = use_pair(desc->flags, true);
   const int64_t M_pad = round_up(n_prefix, kFillRowAlign);
@@ -550,7 +595,8 @@ extern "C" rf_status rf_fill_kv_layered(const rf_fill_desc* desc, const rf_bf16*
     if ((st = map_gemm(pair, ma, sms, s)) != RF_OK) return st;
     if (staged && (st = cuda_check(cudaEventRecord(freed[r], s), "cudaEventRecord")) != RF_OK) return st;
     KvGemmArgs ka{lay.xhat, lay.ssp, lay.n_fill, lay.fill_idx, lay.rope_cos, lay.rope_sin,
-                  reinterpret_cast<const __nv_bfloat16*>(Wkv) + static_cast<size_t>(c0) * 2 * KV * d, k_cache, v_cache,
+                  static_cast<const __nv_bfloat16*>(wk) + static_cast<size_t>(c0) * KV * d,
+                  static_cast<const __nv_bfloat16*>(wv) + static_cast<size_t>(c0) * KV * d, k_cache, v_cache,
                   desc->v_scale ? desc->v_scale + c0 * H : nullptr,
                   desc->k_norm_gain ? reinterpret_cast<const __nv_bfloat16*>(desc->k_norm_gain) + c0 * desc->head_dim
                                     : nullptr,

@@ -121,14 +121,19 @@ struct MapProb {
 };
 
 // --------------------------------------------------------------------------
-// 5. K/V GEMM: A operand x̂ [P*M_pad][d], B operand Wkv [P*2KV][d] (K-major).
-//    Unit u: layer p, M-tile mt, N-tile nt (N fastest: the A tile is reused by
-//    the CTAs in flight, and a layer's 2KV x d weights stay in L2).
+// 5. K/V GEMM: A operand x̂ [P*M_pad][d]; B operand the folded projections,
+//    Wk [P*KV][d] for output columns [0, KV) and Wv [P*KV][d] for [KV, 2KV) of a
+//    layer (both K-major, read in boxes of 128 rows; KV % 128 == 0, so a box lies
+//    in one of them). Unit u: layer p, M-tile mt, N-tile nt (N fastest: the A
+//    tile is reused by the CTAs in flight, and a layer's 2KV x d weights stay in L2).
 // --------------------------------------------------------------------------
+constexpr int kKvBoxRows = 128;
+
 template <bool kPair_>
 struct KVProb {
   CUtensorMap tmA;
-  CUtensorMap tmB;
+  CUtensorMap tmBk;
+  CUtensorMap tmBv;
   const int32_t* n_fill;
   const int32_t* fill_idx;
   const float* ssp;        // [P][d/256][M_pad]; slot 0 holds the row scale r after k_row_rms
@@ -153,7 +158,8 @@ struct KVProb {
 
   __device__ void prefetch() const {
     tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmBk);
+    tma_prefetch_desc(&tmBv);
   }
   __device__ int m_tiles() const { return (*n_fill + Cfg::kUnitM - 1) / Cfg::kUnitM; }
   __device__ int num_units() const { return P * m_tiles() * n_ntiles; }
@@ -166,18 +172,30 @@ struct KVProb {
     mt = r / n_ntiles;
     nt = r - mt * n_ntiles;
   }
+  static constexpr int kBoxes = Cfg::kBRows / kKvBoxRows;  // B boxes per K-block (1 pair, 2 single)
   struct Coords {
-    int a_row, b_row;
+    const CUtensorMap* tb[kBoxes];
+    int a_row, b_row[kBoxes];
   };
   __device__ Coords coords(int u, int, uint32_t rank) const {
     int p, mt, nt;
     decode(u, m_tiles(), p, mt, nt);
-    return {p * M_pad + mt * Cfg::kUnitM + static_cast<int>(rank) * kBM,
-            p * 2 * KV + nt * kBN + static_cast<int>(rank) * Cfg::kBRows};
+    Coords c;
+    c.a_row = p * M_pad + mt * Cfg::kUnitM + static_cast<int>(rank) * kBM;
+#pragma unroll
+    for (int j = 0; j < kBoxes; ++j) {
+      const int col = nt * kBN + static_cast<int>(rank) * Cfg::kBRows + j * kKvBoxRows;  // output column
+      const bool v = col >= KV;
+      c.tb[j] = v ? &tmBv : &tmBk;
+      c.b_row[j] = p * KV + (v ? col - KV : col);
+    }
+    return c;
   }
   __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
     load_operand<kBM, false, kPair>(sa, &tmA, bar, kb * kBK, c.a_row);
-    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, kb * kBK, c.b_row);
+#pragma unroll
+    for (int j = 0; j < kBoxes; ++j)
+      load_operand<kKvBoxRows, false, kPair>(sb + j * (kKvBoxRows * kBK * 2), c.tb[j], bar, kb * kBK, c.b_row[j]);
   }
   __device__ void epilogue(EpiState&, int u, int, int, uint32_t tacc, int row, int, uint32_t rank) const {
     const int nf = *n_fill;
@@ -256,7 +274,8 @@ struct KvGemmArgs {
   const int32_t* fill_idx;
   const float* rope_cos;
   const float* rope_sin;
-  const void* Wkv;            // [P][2KV][d]
+  const void* Wk;             // [P][KV][d], gain folded
+  const void* Wv;             // [P][KV][d], gain folded
   void* k_cache;
   void* v_cache;
   const float* v_scale;       // [P][H] or nullptr
@@ -266,5 +285,11 @@ struct KvGemmArgs {
   int32_t* dev_status;
 };
 rf_status kv_gemm(bool pair, const KvGemmArgs& a, int sms, cudaStream_t s);
+
+// Gain fold of one projection, out[p][j][i] = bf16(W[p][j][i] * gain[p][i]) for
+// W [P][rows][d] bf16 and gain [P][d] bf16 (in place allowed; d % 8 == 0), on
+// stream s. Defined in fill.cu.
+rf_status fold_gain(const void* gain, const void* W, void* out, int64_t P, int64_t rows, int64_t d, int sms,
+                    cudaStream_t s);
 
 }  // namespace rf

@@ -47,13 +47,14 @@ static rf_status static_scratch(void** out) {
 
 extern "C" rf_status rf_fill_kv_static(const rf_fill_desc* desc, const rf_bf16* x_S, int64_t ld_x,
                                        const uint8_t* exact_mask, const rf_bf16* A, const float* b,
-                                       const rf_bf16* Wkv, rf_bf16* k_cache, rf_bf16* v_cache,
-                                       int64_t layer_stride, int64_t row_stride, int32_t* n_fill_out,
-                                       int32_t* dev_status, rf_stream_t stream) {
+                                       const rf_bf16* gain, const rf_bf16* Wk, const rf_bf16* Wv, rf_bf16* k_cache,
+                                       rf_bf16* v_cache, int64_t layer_stride, int64_t row_stride,
+                                       int32_t* n_fill_out, int32_t* dev_status, rf_stream_t stream) {
   rf::clear_error();
   const size_t need = rf_fill_workspace_bytes(desc);
-  if (need == 0) return rf_fill_kv(desc, x_S, ld_x, exact_mask, A, b, Wkv, k_cache, v_cache, layer_stride,
-                                   row_stride, n_fill_out, dev_status, nullptr, 0, stream);
+  if (need == 0)
+    return rf_fill_kv(desc, x_S, ld_x, exact_mask, A, b, gain, Wk, Wv, k_cache, v_cache, layer_stride, row_stride,
+                      n_fill_out, dev_status, nullptr, 0, stream);
   if (need > RF_STATIC_SCRATCH_BYTES)
     return rf::fail(RF_ERR_WORKSPACE,
                     "rf_fill_kv_static: this fill needs %zu bytes of scratch; the static scratch holds %zu bytes "
@@ -62,6 +63,6 @@ extern "C" rf_status rf_fill_kv_static(const rf_fill_desc* desc, const rf_bf16* 
   void* scratch = nullptr;
   rf_status st = rf::static_scratch(&scratch);
   if (st != RF_OK) return st;
-  return rf_fill_kv(desc, x_S, ld_x, exact_mask, A, b, Wkv, k_cache, v_cache, layer_stride, row_stride, n_fill_out,
-                    dev_status, scratch, RF_STATIC_SCRATCH_BYTES, stream);
+  return rf_fill_kv(desc, x_S, ld_x, exact_mask, A, b, gain, Wk, Wv, k_cache, v_cache, layer_stride, row_stride,
+                    n_fill_out, dev_status, scratch, RF_STATIC_SCRATCH_BYTES, stream);
 }

@@ -52,10 +52,11 @@ __global__ void __launch_bounds__(256) k_row_sumsq(const __nv_bfloat16* __restri
 
 // --------------------------------------------------------------------------
 // V-norm GEMM: A operand = the predicted rows x̂ [P][Mc][d] (source 0) or the
-// exact rows [P][c][ld_e] (source 1), B operand = the V rows of Wkv. Unit u:
-// layer p, source, M-tile, N-tile (N fastest, so a row strip is reused at once).
-// When KV % 256 == 128 the last N-tile reaches past the layer's V rows; its
-// heads h >= H are not written.
+// exact rows [P][c][ld_e] (source 1), B operand = the gain-folded V projection
+// Wv' [P][KV][d]. Unit u: layer p, source, M-tile, N-tile (N fastest, so a row
+// strip is reused at once). When KV % 256 == 128 the last N-tile reaches past the
+// layer's V rows (into the next layer's, or past the end, where TMA reads zeros);
+// its heads h >= H are not written.
 // The epilogue writes, for every valid row and each head of the N-tile,
 // norms[p][src][t][h] = r · ‖acc_h‖ with r the row's RMS scale.
 // --------------------------------------------------------------------------
@@ -104,7 +105,7 @@ struct VNormProb {
     decode(u, p, src, mt, nt);
     const int m0 = mt * Cfg::kUnitM + static_cast<int>(rank) * kBM;
     return {src == 0 ? &tmP : &tmX, src == 0 ? p * Mc + m0 : p * c + m0,
-            p * 2 * KV + KV + nt * kBN + static_cast<int>(rank) * Cfg::kBRows};
+            p * KV + nt * kBN + static_cast<int>(rank) * Cfg::kBRows};
   }
   __device__ void issue_loads(Coords& co, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
     load_operand<kBM, false, kPair>(sa, co.ta, bar, kb * kBK, co.a_row);
@@ -170,6 +171,7 @@ struct RescaleLayout {
   float* ssp;
   float* ssx;
   float* norms;
+  __nv_bfloat16* wv;  // gain-folded V projection [P][KV][d] (without RF_WEIGHTS_PREFOLDED)
   size_t bytes;
 };
 
@@ -182,6 +184,7 @@ static RescaleLayout rescale_layout(const rf_fill_desc* d, int64_t c, void* ws) 
   l.ssp = cv.take<float>(P * (d->d / kBN) * Mc);
   l.ssx = cv.take<float>(P * c);
   l.norms = cv.take<float>(P * 2 * c * H);
+  l.wv = (d->flags & RF_WEIGHTS_PREFOLDED) ? nullptr : cv.take<__nv_bfloat16>(P * H * d->head_dim * d->d);
   l.bytes = cv.bytes();
   return l;
 }
@@ -208,7 +211,7 @@ static rf_status check_rescale(const rf_fill_desc* d, int64_t c) {
 template <bool kPair>
 static rf_status rescale_gemms(const rf_fill_desc* desc, int64_t c, const RescaleLayout& lay, const rf_bf16* x_tail,
                                int64_t ld_x, const rf_bf16* x_exact, int64_t ld_e, const rf_bf16* A, const float* b,
-                               const rf_bf16* Wkv, int32_t* dev_status, int sms, cudaStream_t s) {
+                               const void* Wv, int32_t* dev_status, int sms, cudaStream_t s) {
   using Cfg = GemmCfg<kPair>;
   rf_status st;
   const int64_t d = desc->d, P = desc->L - desc->S, KV = desc->n_kv_heads * desc->head_dim;
@@ -229,7 +232,7 @@ static rf_status rescale_gemms(const rf_fill_desc* desc, int64_t c, const Rescal
     VNormProb<kPair> pr;
     if ((st = make_tmap_bf16_2d(&pr.tmP, lay.xhat, d, P * Mc, d, kBK, kBM)) != RF_OK) return st;
     if ((st = make_tmap_bf16_2d(&pr.tmX, x_exact, d, P * c, ld_e, kBK, kBM)) != RF_OK) return st;
-    if ((st = make_tmap_bf16_2d(&pr.tmB, Wkv, d, P * 2 * KV, d, kBK, Cfg::kBRows)) != RF_OK) return st;
+    if ((st = make_tmap_bf16_2d(&pr.tmB, Wv, d, P * KV, d, kBK, Cfg::kBRows)) != RF_OK) return st;
     pr.ssp = lay.ssp;
     pr.ssx = lay.ssx;
     pr.norms = lay.norms;
@@ -264,21 +267,24 @@ extern "C" size_t rf_value_scale_workspace_bytes(const rf_fill_desc* desc, int64
 
 extern "C" rf_status rf_value_scale(const rf_fill_desc* desc, int64_t c, const rf_bf16* x_S, int64_t ld_x,
                                     const rf_bf16* x_exact, int64_t ld_e, const rf_bf16* A, const float* b,
-                                    const rf_bf16* Wkv, float* v_scale, int32_t* dev_status, void* workspace,
-                                    size_t workspace_bytes, rf_stream_t stream) {
+                                    const rf_bf16* gain, const rf_bf16* Wv, float* v_scale, int32_t* dev_status,
+                                    void* workspace, size_t workspace_bytes, rf_stream_t stream) {
   clear_error();
   rf_status st = check_rescale(desc, c);
   if (st != RF_OK) return st;
-  if (!x_S || !x_exact || !A || !b || !Wkv || !v_scale)
-    return fail(RF_ERR_INVALID_ARG, "x_S, x_exact, A, b, Wkv and v_scale must be non-NULL");
+  const bool prefolded = (desc->flags & RF_WEIGHTS_PREFOLDED) != 0;
+  if (!x_S || !x_exact || !A || !b || !Wv || !v_scale || (!prefolded && !gain))
+    return fail(RF_ERR_INVALID_ARG, "x_S, x_exact, A, b, Wv, v_scale (and gain unless RF_WEIGHTS_PREFOLDED) "
+                                    "must be non-NULL");
   const int64_t d = desc->d;
   const int64_t d_in = desc->d_in > 0 ? desc->d_in : d;
   if (ld_x < d_in || ld_x % 8 != 0 || ld_e < d || ld_e % 8 != 0)
     return fail(RF_ERR_ALIGN, "ld_x must be >= d_in, ld_e >= d, both multiples of 8");
   const rf_bf16* x_tail = reinterpret_cast<const rf_bf16*>(reinterpret_cast<const __nv_bfloat16*>(x_S) +
                                                            (desc->N - desc->T) * ld_x);
-  if (!aligned16(x_tail) || !aligned16(x_exact) || !aligned16(A) || !aligned16(b) || !aligned16(Wkv))
-    return fail(RF_ERR_ALIGN, "x_S, x_exact, A, b and Wkv must be 16-byte aligned");
+  if (!aligned16(x_tail) || !aligned16(x_exact) || !aligned16(A) || !aligned16(b) || !aligned16(Wv) ||
+      (!prefolded && !aligned16(gain)))
+    return fail(RF_ERR_ALIGN, "x_S, x_exact, A, b, gain and Wv must be 16-byte aligned");
   RescaleLayout lay = rescale_layout(desc, c, workspace);
   if (workspace == nullptr || workspace_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", lay.bytes, workspace_bytes);
@@ -287,9 +293,15 @@ extern "C" rf_status rf_value_scale(const rf_fill_desc* desc, int64_t c, const r
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   k_set_count<<<1, 1, 0, s>>>(lay.n_c, static_cast<int>(c));
   if ((st = cuda_check(cudaGetLastError(), "k_set_count launch")) != RF_OK) return st;
+  const void* wv = Wv;
+  if (!prefolded) {
+    if ((st = fold_gain(gain, Wv, lay.wv, desc->L - desc->S, desc->n_kv_heads * desc->head_dim, d, sms, s)) != RF_OK)
+      return st;
+    wv = lay.wv;
+  }
   st = use_pair(desc->flags, true)
-           ? rescale_gemms<true>(desc, c, lay, x_tail, ld_x, x_exact, ld_e, A, b, Wkv, dev_status, sms, s)
-           : rescale_gemms<false>(desc, c, lay, x_tail, ld_x, x_exact, ld_e, A, b, Wkv, dev_status, sms, s);
+           ? rescale_gemms<true>(desc, c, lay, x_tail, ld_x, x_exact, ld_e, A, b, wv, dev_status, sms, s)
+           : rescale_gemms<false>(desc, c, lay, x_tail, ld_x, x_exact, ld_e, A, b, wv, dev_status, sms, s);
   if (st != RF_OK) return st;
   const int64_t PH = (desc->L - desc->S) * desc->n_kv_heads;
   {

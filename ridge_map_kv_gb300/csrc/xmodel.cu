@@ -7,6 +7,9 @@
 // inference is one batched matmul per target layer.
 //
 // Launch sequence on the caller's stream:
+//   0. k_check_layers    the caller's device table of source layers: range check
+//                        (an entry outside [0, L_src) sets RF_ERR_INVALID_ARG and
+//                        turns the GEMM into a no-op) and a copy into the workspace
 //   1. k_rope_table x2   cos/sin tables for θ_src and θ_tgt (fp64 angles)
 //   2. k_rope_rows       un-rope every source layer's keys once into the workspace
 //   3. tc_gemm<XMProb>   for every target layer l, M-tile of rows and N-tile of
@@ -86,6 +89,27 @@ __global__ void __launch_bounds__(256) k_rope_rows(const __nv_bfloat16* __restri
   }
 }
 
+// Checks the source-layer table on the device and copies it to the workspace:
+// *ok = 1 if every entry lies in [0, L_src), else 0 with RF_ERR_INVALID_ARG in
+// *dev_status (out-of-range entries are copied as 0, so nothing downstream ever
+// indexes with them). One CTA.
+__global__ void __launch_bounds__(256) k_check_layers(const int32_t* __restrict__ in, int n, int L_src,
+                                                      int32_t* __restrict__ out, int32_t* __restrict__ ok,
+                                                      int32_t* dev_status) {
+  int bad = 0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int v = in[i];
+    const bool good = v >= 0 && v < L_src;
+    out[i] = good ? v : 0;
+    bad |= good ? 0 : 1;
+  }
+  bad = __syncthreads_or(bad);
+  if (threadIdx.x == 0) {
+    *ok = bad ? 0 : 1;
+    if (bad) record_status(dev_status, RF_ERR_INVALID_ARG);
+  }
+}
+
 template <bool kPair_>
 struct XMProb {
   CUtensorMap tmKu;  // un-roped source keys   {KV, L_src*N}, box {64, 128}
@@ -93,6 +117,7 @@ struct XMProb {
   CUtensorMap tmWk;  // W_K                    {k*KV, L_tgt*KV}, box {64, 256}
   CUtensorMap tmWv;  // W_V
   const int32_t* src;  // [L_tgt][k]
+  const int32_t* ok;   // 1 if the table passed k_check_layers; else the GEMM does nothing
   const float* bk;     // [L_tgt][KV]
   const float* bv;
   const float* cos_t;  // target table [N][hd/2]
@@ -116,7 +141,7 @@ struct XMProb {
     tma_prefetch_desc(&tmWk);
     tma_prefetch_desc(&tmWv);
   }
-  __device__ int num_units() const { return L_tgt * m_tiles * 2 * n_half; }
+  __device__ int num_units() const { return *ok ? L_tgt * m_tiles * 2 * n_half : 0; }
   __device__ int num_subtiles(int) const { return 1; }
   __device__ int num_kb(int, int) const { return k * KV / kBK; }
   // Unit order: target layer, M-tile, then the 2*n_half N-tiles (K then V), so
@@ -188,6 +213,7 @@ struct XMProb {
 struct XLayout {
   __nv_bfloat16* ku;
   int32_t* src;
+  int32_t* ok;
   float* cos_s;
   float* sin_s;
   float* cos_t;
@@ -201,6 +227,7 @@ static XLayout xmodel_layout(const rf_xmodel_desc* d, void* ws) {
   XLayout l;
   l.ku = c.take<__nv_bfloat16>(d->L_src * d->N * KV);
   l.src = c.take<int32_t>(d->L_tgt * d->k);
+  l.ok = c.take<int32_t>(1);
   l.cos_s = c.take<float>(d->N * (d->head_dim / 2));
   l.sin_s = c.take<float>(d->N * (d->head_dim / 2));
   l.cos_t = c.take<float>(d->N * (d->head_dim / 2));
@@ -239,6 +266,7 @@ rf_status xmodel_gemm(const rf_xmodel_desc* desc, const XLayout& lay, const rf_b
   if ((st = make_tmap_bf16_2d(&pr.tmWv, Wv, desc->k * KV, desc->L_tgt * KV, desc->k * KV, kBK, Cfg::kBRows)) != RF_OK)
     return st;
   pr.src = lay.src;
+  pr.ok = lay.ok;
   pr.bk = bk;
   pr.bv = bv;
   pr.cos_t = lay.cos_t;
@@ -275,9 +303,7 @@ extern "C" rf_status rf_xmodel_map(const rf_xmodel_desc* desc, const int32_t* sr
   rf_status st = check_xmodel_desc(desc);
   if (st != RF_OK) return st;
   if (src_layers == nullptr) return fail(RF_ERR_INVALID_ARG, "src_layers is NULL");
-  for (int64_t i = 0; i < desc->L_tgt * desc->k; ++i)
-    if (src_layers[i] < 0 || src_layers[i] >= desc->L_src)
-      return fail(RF_ERR_INVALID_ARG, "src_layers[%lld] = %d is outside [0, L_src)", (long long)i, src_layers[i]);
+  if (desc->L_tgt * desc->k > (int64_t(1) << 24)) return fail(RF_ERR_SHAPE, "L_tgt * k must be <= 2^24");
   if (!k_src || !v_src || !Wk || !bk || !Wv || !bv || !k_tgt || !v_tgt)
     return fail(RF_ERR_INVALID_ARG, "tensor pointers must be non-NULL");
   if (!aligned16(k_src) || !aligned16(v_src) || !aligned16(Wk) || !aligned16(bk) || !aligned16(Wv) || !aligned16(bv) ||
@@ -292,10 +318,10 @@ extern "C" rf_status rf_xmodel_map(const rf_xmodel_desc* desc, const int32_t* sr
   const int64_t KV = desc->n_kv_heads * desc->head_dim, N = desc->N;
   const int half = static_cast<int>(desc->head_dim / 2);
 
-  // the layer table is copied from host memory before this call returns
-  if ((st = cuda_check(cudaMemcpyAsync(lay.src, src_layers, sizeof(int32_t) * desc->L_tgt * desc->k,
-                                       cudaMemcpyHostToDevice, s), "copy src_layers")) != RF_OK)
-    return st;
+  // the caller's device table, checked and copied on the device (no host round trip)
+  k_check_layers<<<1, 256, 0, s>>>(src_layers, static_cast<int>(desc->L_tgt * desc->k), static_cast<int>(desc->L_src),
+                                   lay.src, lay.ok, dev_status);
+  if ((st = cuda_check(cudaGetLastError(), "k_check_layers launch")) != RF_OK) return st;
   {
     ProfScope prof(s, RF_STAGE_ROPE_TABLE);
     const int blocks = static_cast<int>(std::min<int64_t>((N * half + 255) / 256, 4LL * sms));

@@ -21,20 +21,30 @@ def desc_of(cfg, flags: int = 0, v_scale=None, k_norm_gain=None) -> rf.rf_fill_d
                            k_norm_gain=None if k_norm_gain is None else k_norm_gain.data_ptr())
 
 
+def fold(desc, g):
+    """Gain-folded K and V projections of the device inputs ``g`` (rf_fold_kv_weights)."""
+    Wkf, Wvf = torch.empty_like(g["Wk"]), torch.empty_like(g["Wv"])
+    rf.rf_fold_kv_weights(desc, g["gain"], g["Wk"], g["Wv"], Wkf, Wvf)
+    return Wkf, Wvf
+
+
 def run_fill(cfg, inp: dict, dev="cuda", mask="inp", canary=True, flags: int = 0, v_scale=None,
-             k_norm_gain=None):
-    """Runs fold + fill on device copies of ``inp``. Returns a dict with the
-    caches before/after, n_fill and the device status. ``flags`` selects the GEMM
-    kernels (rf.RF_FLAG_SINGLE_CTA or rf.RF_FLAG_CTA_PAIR; 0 = library default)."""
+             k_norm_gain=None, prefolded=False):
+    """Runs the fill on device copies of ``inp``. Returns a dict with the caches
+    before/after, n_fill and the device status. ``flags`` selects the GEMM kernels
+    (rf.RF_FLAG_SINGLE_CTA or rf.RF_FLAG_CTA_PAIR; 0 = library default). The fill
+    folds the RMSNorm gain into its workspace, or with ``prefolded`` it gets
+    projections folded beforehand by rf_fold_kv_weights (RF_WEIGHTS_PREFOLDED)."""
     dev = torch.device(dev)
     kng = None if k_norm_gain is None else k_norm_gain.to(dev)   # alive until the fill is done
-    desc = desc_of(cfg, flags, v_scale, kng)
+    desc = desc_of(cfg, flags | (rf.RF_WEIGHTS_PREFOLDED if prefolded else 0), v_scale, kng)
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     m = g["mask"] if mask == "inp" else (mask.to(dev) if mask is not None else None)
-    P, KV, d = cfg.P, cfg.KV, cfg.d
-    Wkv = torch.empty((max(P, 1), 2 * KV, d), dtype=torch.bfloat16, device=dev)
-    if P > 0:
-        rf.rf_fold_kv_weights(desc, g["gain"], g["Wk"], g["Wv"], Wkv)
+    P, KV = cfg.P, cfg.KV
+    gain, Wk, Wv = (g["gain"], g["Wk"], g["Wv"]) if P > 0 else (None, None, None)
+    if prefolded and P > 0:
+        Wk, Wv = fold(desc, g)
+        gain = None
     if canary:
         kc = synth.canary_cache(cfg.L, cfg.N, cfg.H, cfg.hd, 0, dev)
         vc = synth.canary_cache(cfg.L, cfg.N, cfg.H, cfg.hd, 1, dev)
@@ -47,10 +57,10 @@ def run_fill(cfg, inp: dict, dev="cuda", mask="inp", canary=True, flags: int = 0
     nfill = torch.full((1,), -1, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     rf.rf_fill_kv(desc, g["x_S"], cfg.D_in, m, g["A"] if P > 0 else None, g["b"] if P > 0 else None,
-                  Wkv if P > 0 else None, kc, vc, cfg.N * KV, KV, nfill, status, ws, ws_bytes)
+                  gain, Wk, Wv, kc, vc, cfg.N * KV, KV, nfill, status, ws, ws_bytes)
     torch.cuda.synchronize()
     return {"kc": kc, "vc": vc, "kc0": kc0, "vc0": vc0, "n_fill": int(nfill.item()),
-            "status": int(status.item()), "ws": ws, "Wkv": Wkv}
+            "status": int(status.item()), "ws": ws}
 
 
 def _f64_of(t) -> np.ndarray:

@@ -61,14 +61,16 @@ def _fill_desc(**kw):
 
 
 def test_fill_workspace_size_follows_the_layout():
-    desc = _fill_desc()
+    desc = _fill_desc(flags=rf.RF_WEIGHTS_PREFOLDED)
     # fill_idx, n_fill, Xf [M x d], x̂ [P x M x d], ss partials [P x d/256 x M], cos/sin [n_prefix x hd/2],
     # with M = the prefix rows padded to a whole 256-row unit
     r = lambda x: (x + 255) // 256 * 256
-    n_prefix, M, P, d, half = 9, 256, 4, 256, 32
+    n_prefix, M, P, d, half, KV = 9, 256, 4, 256, 32, 128
     want = r(n_prefix * 4) + r(4) + r(M * d * 2) + r(P * M * d * 2) + r(P * (d // 256) * M * 4) \
         + r(n_prefix * half * 4) + r(n_prefix * half * 4)
     assert rf.rf_fill_workspace_bytes(desc) == want
+    # without RF_WEIGHTS_PREFOLDED the call folds the gain into two [P][KV][d] bf16 arrays of its own
+    assert rf.rf_fill_workspace_bytes(_fill_desc()) == want + 2 * r(P * KV * d * 2)
 
 
 @pytest.mark.parametrize("bad", [dict(d=100), dict(head_dim=96), dict(S=9), dict(T=13), dict(n_kv_heads=1),
@@ -77,25 +79,62 @@ def test_fill_rejects_bad_descriptors_on_the_host(bad):
     desc = _fill_desc(**bad)
     assert rf.rf_fill_workspace_bytes(desc) == 0
     with pytest.raises(rf.RFError) as ei:
-        rf.rf_fill_kv(desc, 16, 256, None, 16, 16, 16, 16, 16, 0, 128, None, None, 256, 1 << 30, stream=0)
+        rf.rf_fill_kv(desc, 16, 256, None, 16, 16, 16, 16, 16, 16, 16, 0, 128, None, None, 256, 1 << 30, stream=0)
     assert ei.value.status in (rf.RF_ERR_INVALID_ARG, rf.RF_ERR_SHAPE)
 
 
-def test_fill_rejects_null_and_misaligned_pointers_and_small_workspace():
-    desc = _fill_desc()
+def _fill_call(desc, **kw):
+    """rf_fill_kv with valid-looking (aligned, non-NULL, never dereferenced) arguments,
+    some replaced by ``kw``; the host checks reject before any launch."""
+    a = dict(x_S=256, ld_x=256, mask=None, A=256, b=256, gain=256, Wk=256, Wv=256, kc=256, vc=256, ls=0, rs=128,
+             ws=256, wsb=1 << 30)
+    a.update(kw)
+    rf.rf_fill_kv(desc, a["x_S"], a["ld_x"], a["mask"], a["A"], a["b"], a["gain"], a["Wk"], a["Wv"], a["kc"],
+                  a["vc"], a["ls"], a["rs"], None, None, a["ws"], a["wsb"], stream=0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(A=None), rf.RF_ERR_INVALID_ARG),
+    (dict(Wk=None), rf.RF_ERR_INVALID_ARG),
+    (dict(Wv=None), rf.RF_ERR_INVALID_ARG),
+    (dict(gain=None), rf.RF_ERR_INVALID_ARG),           # the call must fold, so it needs the gain
+    (dict(x_S=258), rf.RF_ERR_ALIGN),
+    (dict(gain=264), rf.RF_ERR_ALIGN),
+    (dict(Wv=264), rf.RF_ERR_ALIGN),
+    (dict(rs=100), rf.RF_ERR_ALIGN),
+    (dict(wsb=1024), rf.RF_ERR_WORKSPACE),
+], ids=["A NULL", "Wk NULL", "Wv NULL", "gain NULL", "x_S misaligned", "gain misaligned", "Wv misaligned",
+        "row stride", "small workspace"])
+def test_fill_rejects_null_and_misaligned_pointers_and_small_workspace(kw, status):
     with pytest.raises(rf.RFError) as ei:
-        rf.rf_fill_kv(desc, 256, 256, None, None, 256, 256, 256, 256, 0, 128, None, None, 256, 1 << 30, stream=0)
-    assert ei.value.status == rf.RF_ERR_INVALID_ARG
+        _fill_call(_fill_desc(), **kw)
+    assert ei.value.status == status
+    if status == rf.RF_ERR_WORKSPACE:
+        assert "workspace" in rf.rf_last_error()
+
+
+def test_prefolded_fill_needs_no_gain_and_a_smaller_workspace():
+    pre = _fill_desc(flags=rf.RF_WEIGHTS_PREFOLDED)
+    need = rf.rf_fill_workspace_bytes(pre)
+    assert need < rf.rf_fill_workspace_bytes(_fill_desc())
+    # gain NULL is accepted with the flag: the first complaint is about the workspace
     with pytest.raises(rf.RFError) as ei:
-        rf.rf_fill_kv(desc, 258, 256, None, 256, 256, 256, 256, 256, 0, 128, None, None, 256, 1 << 30, stream=0)
-    assert ei.value.status == rf.RF_ERR_ALIGN
-    with pytest.raises(rf.RFError) as ei:
-        rf.rf_fill_kv(desc, 256, 256, None, 256, 256, 256, 256, 256, 0, 100, None, None, 256, 1 << 30, stream=0)
-    assert ei.value.status == rf.RF_ERR_ALIGN
-    with pytest.raises(rf.RFError) as ei:
-        rf.rf_fill_kv(desc, 256, 256, None, 256, 256, 256, 256, 256, 0, 128, None, None, 256, 1024, stream=0)
+        _fill_call(pre, gain=None, wsb=need - 1)
     assert ei.value.status == rf.RF_ERR_WORKSPACE
-    assert "workspace" in rf.rf_last_error()
+    with pytest.raises(rf.RFError) as ei:
+        _fill_call(pre, gain=None, Wk=None)
+    assert ei.value.status == rf.RF_ERR_INVALID_ARG
+
+
+def test_fold_validates_on_the_host():
+    desc = _fill_desc()
+    for args, status in (((None, 256, 256, 256, 256), rf.RF_ERR_INVALID_ARG),
+                         ((256, 256, 256, None, 256), rf.RF_ERR_INVALID_ARG),
+                         ((256, 256, 256, 256, 264), rf.RF_ERR_ALIGN)):
+        with pytest.raises(rf.RFError) as ei:
+            rf.rf_fold_kv_weights(desc, *args, stream=0)
+        assert ei.value.status == status
+    rf.rf_fold_kv_weights(_fill_desc(S=8), None, None, None, None, None, stream=0)   # no upper layer: nothing to do
 
 
 def test_calib_and_xmodel_and_solve_validate_on_the_host():
@@ -109,11 +148,22 @@ def test_calib_and_xmodel_and_solve_validate_on_the_host():
     assert ei.value.status == rf.RF_ERR_INVALID_ARG
     xd = rf.rf_xmodel_desc(L_src=4, L_tgt=2, k=2, n_kv_heads=2, head_dim=128, N=64, theta_src=1e6, theta_tgt=1e6,
                            pos_offset=0)
+    # the source-layer table is a device pointer (its range is checked on the device)
     with pytest.raises(rf.RFError) as ei:
-        rf.rf_xmodel_map(xd, [[0, 1], [2, 9]], 256, 256, 256, 256, 256, 256, 256, 256, workspace=256,
+        rf.rf_xmodel_map(xd, None, 256, 256, 256, 256, 256, 256, 256, 256, workspace=256,
                          workspace_bytes=1 << 34, stream=0)
     assert ei.value.status == rf.RF_ERR_INVALID_ARG
     assert "src_layers" in rf.rf_last_error()
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_xmodel_map(xd, 256, 256, 256, 256, 256, 256, 256, 264, 256, workspace=256,
+                         workspace_bytes=1 << 34, stream=0)
+    assert ei.value.status == rf.RF_ERR_ALIGN
+    big = rf.rf_xmodel_desc(L_src=4, L_tgt=1 << 13, k=1 << 12, n_kv_heads=2, head_dim=128, N=64, theta_src=1e6,
+                            theta_tgt=1e6, pos_offset=0)
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_xmodel_map(big, 256, 256, 256, 256, 256, 256, 256, 256, 256, workspace=256, workspace_bytes=1 << 40,
+                         stream=0)
+    assert ei.value.status == rf.RF_ERR_SHAPE
 
 
 def test_value_scale_validates_on_the_host():
@@ -123,15 +173,25 @@ def test_value_scale_validates_on_the_host():
     assert rf.rf_value_scale_workspace_bytes(desc, 3) > 0
     for c in (0, 4):
         with pytest.raises(rf.RFError) as ei:
-            rf.rf_value_scale(desc, c, 256, 256, 256, 256, 256, 256, 256, 256, workspace=256,
+            rf.rf_value_scale(desc, c, 256, 256, 256, 256, 256, 256, 256, 256, 256, workspace=256,
                               workspace_bytes=1 << 30, stream=0)
         assert ei.value.status == rf.RF_ERR_INVALID_ARG
     with pytest.raises(rf.RFError) as ei:
-        rf.rf_value_scale(desc, 2, 256, 256, None, 256, 256, 256, 256, 256, workspace=256,
+        rf.rf_value_scale(desc, 2, 256, 256, None, 256, 256, 256, 256, 256, 256, workspace=256,
+                          workspace_bytes=1 << 30, stream=0)
+    assert ei.value.status == rf.RF_ERR_INVALID_ARG
+    with pytest.raises(rf.RFError) as ei:              # the call folds the gain, so it needs it
+        rf.rf_value_scale(desc, 2, 256, 256, 256, 256, 256, 256, None, 256, 256, workspace=256,
                           workspace_bytes=1 << 30, stream=0)
     assert ei.value.status == rf.RF_ERR_INVALID_ARG
     with pytest.raises(rf.RFError) as ei:
-        rf.rf_value_scale(desc, 2, 256, 256, 256, 256, 256, 256, 256, 256, workspace=256, workspace_bytes=64,
+        rf.rf_value_scale(desc, 2, 256, 256, 256, 256, 256, 256, 256, 256, 256, workspace=256, workspace_bytes=64,
+                          stream=0)
+    assert ei.value.status == rf.RF_ERR_WORKSPACE
+    pre = _fill_desc(flags=rf.RF_WEIGHTS_PREFOLDED)
+    assert rf.rf_value_scale_workspace_bytes(pre, 3) < rf.rf_value_scale_workspace_bytes(desc, 3)
+    with pytest.raises(rf.RFError) as ei:              # prefolded: no gain needed, the workspace is checked next
+        rf.rf_value_scale(pre, 2, 256, 256, 256, 256, 256, 256, None, 256, 256, workspace=256, workspace_bytes=64,
                           stream=0)
     assert ei.value.status == rf.RF_ERR_WORKSPACE
 
@@ -150,8 +210,8 @@ def test_layered_fill_workspace_and_host_checks():
     assert int8_host == staged + 2 * r(4 * 256 * 256)    # plus two int8 landing slots
     assert rf.rf_fill_layered_workspace_bytes(desc, rf.map_source(7, 256)) == 0
     with pytest.raises(rf.RFError) as ei:
-        rf.rf_fill_kv_layered(desc, 256, 256, None, rf.map_source(rf.RF_MAPS_INT8, 256), 256, 256, 256, 256, 0,
-                              128, workspace=256, workspace_bytes=1 << 30, stream=0)
+        rf.rf_fill_kv_layered(desc, 256, 256, None, rf.map_source(rf.RF_MAPS_INT8, 256), 256, 256, 256, 256, 256,
+                              256, 0, 128, workspace=256, workspace_bytes=1 << 30, stream=0)
     assert ei.value.status == rf.RF_ERR_INVALID_ARG and "row_scale" in rf.rf_last_error()
 
 

@@ -64,6 +64,19 @@ def test_fill_small_shapes_match_oracle(cfg, flags):
     assert_values(cfg, inp, res, idx)
 
 
+@KERNELS
+def test_prefolded_weights_give_the_same_caches_bit_for_bit(flags):
+    """Projections folded once by rf_fold_kv_weights (RF_WEIGHTS_PREFOLDED) and the
+    gain folded inside the call give the same caches, bit for bit."""
+    cfg = _small("prefolded vs folded in the call")
+    inp = synth.fill_inputs(cfg)
+    a = run_fill(cfg, inp, flags=flags)
+    b = run_fill(cfg, inp, flags=flags, prefolded=True)
+    assert a["status"] == 0 and b["status"] == 0
+    assert torch.equal(a["kc"].view(torch.int16), b["kc"].view(torch.int16))
+    assert torch.equal(a["vc"].view(torch.int16), b["vc"].view(torch.int16))
+
+
 @pytest.mark.parametrize("case", ["all_exact", "tail_is_everything", "no_upper_layers", "one_row", "two_tiles_plus_one"])
 def test_fill_degenerate_arms(case):
     cfg = _small(case, d=256, L=4, S=2, N=140, T=10, H=2, hd=64, exact=None)
@@ -192,3 +205,26 @@ def test_fill_flash_next_shaped_maps_sampled():
     assert res["n_fill"] == len(idx)
     assert_bookkeeping(cfg, res, mnp)
     assert_values(cfg, inp, res, _sample_rows(idx, mnp, cfg.N - cfg.T))
+
+
+# --------------------------------------------------------------------------- #
+# Layer shards: the blocks of a multi-GPU fill, run one after another here
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("world", [2, 3])
+def test_layer_blocks_filled_separately_equal_the_whole_fill(world):
+    """Each rank of a sharded fill calls rf_fill_kv on its block of upper layers as a
+    fill of its own (L = its layer count, S = 0, a cache of just those layers, its
+    slices of the maps and projections). Run block by block on one GPU, the blocks'
+    caches put together equal the whole fill's upper layers bit for bit."""
+    from ridge_map_kv_gb300 import shard as sh
+    cfg = _small("sharded by layer", L=7, S=2)
+    inp = synth.fill_inputs(cfg)
+    whole = run_fill(cfg, inp, canary=False)       # zero caches: entries never written stay 0 in both
+    assert whole["status"] == 0
+    for r in range(world):
+        b = sh.layer_shard(cfg.P, cfg.S, world, r)
+        part = dataclasses.replace(cfg, L=b.layers, S=0)
+        res = run_fill(part, sh.shard_weights(inp, b), canary=False)
+        assert res["status"] == 0 and res["n_fill"] == whole["n_fill"]
+        for key in ("kc", "vc"):
+            assert torch.equal(res[key].view(torch.int16), whole[key][cfg.S + b.p0:cfg.S + b.p1].view(torch.int16))

@@ -107,7 +107,7 @@ def _gpu_fit(caches):
     xws = torch.empty(xwb, dtype=torch.uint8, device=DEV)
     out_k = torch.empty((T, N, H, hd), dtype=torch.bfloat16, device=DEV)
     out_v = torch.empty_like(out_k)
-    rf.rf_xmodel_map(xd, sel_h, ks, vs, Wk, bk, Wv, bv, out_k, out_v, status, xws, xwb)  # host table
+    rf.rf_xmodel_map(xd, sel, ks, vs, Wk, bk, Wv, bv, out_k, out_v, status, xws, xwb)  # the selection's device table
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return sel_h, out_k, out_v

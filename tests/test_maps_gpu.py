@@ -18,7 +18,7 @@ import torch
 import oracle as O
 import ridge_map_kv_gb300 as rf
 import synth
-from fillcheck import assert_bookkeeping, assert_values, desc_of, run_fill
+from fillcheck import assert_bookkeeping, assert_values, desc_of, fold, run_fill
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -41,12 +41,11 @@ def _quantize(cfg, A):
     return q, s
 
 
-def _run_layered(cfg, inp, maps, flags=0, v_scale=None, k_norm_gain=None):
-    desc = desc_of(cfg, flags, v_scale, k_norm_gain)
+def _run_layered(cfg, inp, maps, flags=0, v_scale=None, k_norm_gain=None, prefolded=False):
+    desc = desc_of(cfg, flags | (rf.RF_WEIGHTS_PREFOLDED if prefolded else 0), v_scale, k_norm_gain)
     g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     P, KV = cfg.P, cfg.KV
-    Wkv = torch.empty((P, 2 * KV, cfg.d), dtype=torch.bfloat16, device=DEV)
-    rf.rf_fold_kv_weights(desc, g["gain"], g["Wk"], g["Wv"], Wkv)
+    W = (None, *fold(desc, g)) if prefolded else (g["gain"], g["Wk"], g["Wv"])
     kc = synth.canary_cache(cfg.L, cfg.N, cfg.H, cfg.hd, 0, DEV)
     vc = synth.canary_cache(cfg.L, cfg.N, cfg.H, cfg.hd, 1, DEV)
     kc0, vc0 = kc.clone(), vc.clone()
@@ -54,7 +53,7 @@ def _run_layered(cfg, inp, maps, flags=0, v_scale=None, k_norm_gain=None):
     ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=DEV)
     nf = torch.full((1,), -1, dtype=torch.int32, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    rf.rf_fill_kv_layered(desc, g["x_S"], cfg.D_in, g["mask"], maps, g["b"], Wkv, kc, vc, cfg.N * KV, KV, nf, status,
+    rf.rf_fill_kv_layered(desc, g["x_S"], cfg.D_in, g["mask"], maps, g["b"], *W, kc, vc, cfg.N * KV, KV, nf, status,
                           ws, wsb)
     torch.cuda.synchronize()
     return {"kc": kc, "vc": vc, "kc0": kc0, "vc0": vc0, "n_fill": int(nf.item()), "status": int(status.item()),
@@ -87,9 +86,10 @@ def test_layered_bf16_fill_equals_the_resident_fill(cfg, flags):
     ref = run_fill(cfg, inp, flags=flags)
     assert ref["status"] == 0
     A_host = inp["A"].pin_memory()
-    for maps in (rf.map_source(rf.RF_MAPS_BF16, inp["A"].to(DEV)),
-                 rf.map_source(rf.RF_MAPS_BF16, A_host, on_host=True)):
-        res = _run_layered(cfg, inp, maps, flags)
+    # device maps with the gain folded in the call; host maps with prefolded projections
+    for maps, pre in ((rf.map_source(rf.RF_MAPS_BF16, inp["A"].to(DEV)), False),
+                      (rf.map_source(rf.RF_MAPS_BF16, A_host, on_host=True), True)):
+        res = _run_layered(cfg, inp, maps, flags, prefolded=pre)
         assert res["status"] == 0 and res["n_fill"] == ref["n_fill"]
         assert _same_bits(res["kc"], ref["kc"]) and _same_bits(res["vc"], ref["vc"])
 

@@ -15,7 +15,7 @@ import torch
 import oracle as O
 import ridge_map_kv_gb300 as rf
 import synth
-from fillcheck import assert_bookkeeping, assert_values, desc_of, run_fill
+from fillcheck import assert_bookkeeping, assert_values, desc_of, fold, run_fill
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -33,16 +33,18 @@ def _f64(t):
     return O.bf16_bits_to_f64(synth.bits(t))
 
 
-def _gpu_scale(cfg, inp, x_exact, c, flags=0):
-    desc = desc_of(cfg, flags)
+def _gpu_scale(cfg, inp, x_exact, c, flags=0, prefolded=False):
+    """rf_value_scale with the gain folded in the call, or (``prefolded``) with the V
+    projection folded beforehand by rf_fold_kv_weights."""
+    desc = desc_of(cfg, flags | (rf.RF_WEIGHTS_PREFOLDED if prefolded else 0))
     g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    Wkv = torch.empty((cfg.P, 2 * cfg.KV, cfg.d), dtype=torch.bfloat16, device=DEV)
-    rf.rf_fold_kv_weights(desc, g["gain"], g["Wk"], g["Wv"], Wkv)
+    gain, Wv = (None, fold(desc, g)[1]) if prefolded else (g["gain"], g["Wv"])
     vs = torch.full((cfg.P, cfg.H), float("nan"), dtype=torch.float32, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     wsb = rf.rf_value_scale_workspace_bytes(desc, c)
     ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
-    rf.rf_value_scale(desc, c, g["x_S"], cfg.D_in, x_exact.to(DEV), cfg.d, g["A"], g["b"], Wkv, vs, status, ws, wsb)
+    rf.rf_value_scale(desc, c, g["x_S"], cfg.D_in, x_exact.to(DEV), cfg.d, g["A"], g["b"], gain, Wv, vs, status, ws,
+                      wsb)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return vs
@@ -85,6 +87,9 @@ def test_value_scale_matches_oracle(cfg, c, flags):
     ref = _oracle_scale(cfg, inp, x_exact, c, range(cfg.P))
     assert np.abs(ref - 1.0).max() > 0.05          # the inputs move the scale away from 1
     _assert_scales(vs, ref)
+    # the V projection folded beforehand gives the same scales, bit for bit
+    pre = _gpu_scale(cfg, inp, x_exact, c, flags, prefolded=True).cpu().numpy().astype(np.float64)
+    np.testing.assert_array_equal(pre, vs)
 
 
 def test_value_scale_is_near_one_when_the_exact_rows_are_the_predictions():

@@ -29,7 +29,8 @@ def _run(cfg, inp, L_tgt, N, flags=0):
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     wsb = rf.rf_xmodel_workspace_bytes(desc)
     ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
-    rf.rf_xmodel_map(desc, g["src"], g["k_src"], g["v_src"], g["Wk"], g["bk"], g["Wv"], g["bv"], kt, vt, status,
+    src = torch.as_tensor(np.asarray(g["src"], np.int32), device=DEV)     # the device table the call takes
+    rf.rf_xmodel_map(desc, src, g["k_src"], g["v_src"], g["Wk"], g["bk"], g["Wv"], g["bv"], kt, vt, status,
                      ws, wsb)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
@@ -101,9 +102,38 @@ def test_xmodel_full_size_sampled(flags):
     cfg = synth.XMODEL
     inp = synth.xmodel_inputs(cfg, device=DEV)
     kt, vt = _run(cfg, inp, cfg.L_tgt, cfg.N, flags)
+    # every target entry was written: no NaN canary is left anywhere (checked on the device)
+    assert not bool(torch.isnan(kt).any()) and not bool(torch.isnan(vt).any())
     rows = np.unique(np.concatenate([[0, 1, 127, 128, cfg.N - 1],
                                      np.random.default_rng(3).choice(cfg.N, 59, replace=False)]))
     _check(cfg, inp, kt, vt, [0, 21, 40, 63], rows)
+
+
+@pytest.mark.parametrize("bad", [-1, 5, 1 << 30], ids=["negative", "L_src", "huge"])
+def test_xmodel_table_out_of_range_is_reported_on_the_device_and_writes_nothing(bad):
+    """The source-layer table lives on the device, so its range is checked there: an
+    entry outside [0, L_src) sets RF_ERR_INVALID_ARG in the status word and the call
+    writes no target entry (the NaN canaries stay); the context stays usable and a
+    valid table afterwards maps as usual."""
+    cfg = SMALL
+    inp = synth.xmodel_inputs(cfg)
+    desc = rf.rf_xmodel_desc(L_src=cfg.L_src, L_tgt=cfg.L_tgt, k=cfg.k, n_kv_heads=cfg.H, head_dim=cfg.hd, N=cfg.N,
+                             theta_src=cfg.theta_src, theta_tgt=cfg.theta_tgt, pos_offset=0)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    tab = np.asarray(inp["src"], np.int32).copy()
+    tab[1, 0] = bad
+    kt = torch.full((cfg.L_tgt, cfg.N, cfg.H, cfg.hd), float("nan"), dtype=torch.bfloat16, device=DEV)
+    vt = torch.full_like(kt, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    wsb = rf.rf_xmodel_workspace_bytes(desc)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    rf.rf_xmodel_map(desc, torch.as_tensor(tab, device=DEV), g["k_src"], g["v_src"], g["Wk"], g["bk"], g["Wv"],
+                     g["bv"], kt, vt, status, ws, wsb)
+    torch.cuda.synchronize()
+    assert int(status.item()) == rf.RF_ERR_INVALID_ARG
+    assert bool(torch.isnan(kt).all()) and bool(torch.isnan(vt).all())
+    kt2, vt2 = _run(cfg, inp, cfg.L_tgt, cfg.N)
+    _check(cfg, inp, kt2, vt2, range(cfg.L_tgt), np.arange(cfg.N))
 
 
 @pytest.mark.parametrize("hd,theta,off", [(128, 1.0e6, 0), (64, 5.0e5, 12345)])

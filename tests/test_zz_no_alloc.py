@@ -22,7 +22,7 @@ import torch
 import oracle as O
 import ridge_map_kv_gb300 as rf
 import synth
-from fillcheck import desc_of
+from fillcheck import desc_of, fold
 
 pytestmark = pytest.mark.gpu
 
@@ -34,13 +34,14 @@ def _cfg(name, **kw):
     return synth.FillConfig(**base)
 
 
-def _prepare(cfg):
+def _prepare(cfg, prefolded):
+    """Device inputs and the weights the fill takes: projections folded beforehand
+    (RF_WEIGHTS_PREFOLDED), or gain and projections for the call to fold in its scratch."""
     dev = torch.device("cuda")
     inp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in synth.fill_inputs(cfg).items()}
-    desc = desc_of(cfg)
-    Wkv = torch.empty((cfg.P, 2 * cfg.KV, cfg.d), dtype=torch.bfloat16, device=dev)
-    rf.rf_fold_kv_weights(desc, inp["gain"], inp["Wk"], inp["Wv"], Wkv)
-    return desc, inp, Wkv
+    desc = desc_of(cfg, rf.RF_WEIGHTS_PREFOLDED if prefolded else 0)
+    W = (None, *fold(desc, inp)) if prefolded else (inp["gain"], inp["Wk"], inp["Wv"])
+    return desc, inp, W
 
 
 def _caches(cfg):
@@ -65,10 +66,10 @@ def _compare(cfg, inp, got_k, got_v, ref_k, ref_v):
 
 
 def _static_fill(cfg, prepared):
-    desc, inp, Wkv = prepared
+    desc, inp, W = prepared
     kc, vc = _caches(cfg)
     nf, st = _out()
-    rf.rf_fill_kv_static(desc, inp["x_S"], cfg.d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc,
+    rf.rf_fill_kv_static(desc, inp["x_S"], cfg.d, inp["mask"], inp["A"], inp["b"], *W, kc, vc,
                          cfg.N * cfg.KV, cfg.KV, nf, st)
     return kc, vc, nf, st
 
@@ -76,17 +77,17 @@ def _static_fill(cfg, prepared):
 def test_static_fill_matches_workspace_fill_on_two_calls_in_a_row():
     cfgs = [_cfg("static fill A"),
             _cfg("static fill B", index=92, d=768, L=4, S=2, N=300, T=20, H=4, hd=64, exact="blocks16_5")]
-    prepared = [_prepare(c) for c in cfgs]
+    prepared = [_prepare(cfgs[0], True), _prepare(cfgs[1], False)]
 
     # references through rf_fill_kv with a caller workspace
     refs = []
-    for cfg, (desc, inp, Wkv) in zip(cfgs, prepared):
+    for cfg, (desc, inp, W) in zip(cfgs, prepared):
         kc, vc = _caches(cfg)
         nf, st = _out()
         ws_bytes = rf.rf_fill_workspace_bytes(desc)
         assert ws_bytes <= rf.RF_STATIC_SCRATCH_BYTES
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-        rf.rf_fill_kv(desc, inp["x_S"], cfg.d, inp["mask"], inp["A"], inp["b"], Wkv, kc, vc, cfg.N * cfg.KV, cfg.KV,
+        rf.rf_fill_kv(desc, inp["x_S"], cfg.d, inp["mask"], inp["A"], inp["b"], *W, kc, vc, cfg.N * cfg.KV, cfg.KV,
                       nf, st, ws, ws_bytes)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
@@ -97,7 +98,7 @@ def test_static_fill_matches_workspace_fill_on_two_calls_in_a_row():
     again = _static_fill(cfgs[0], prepared[0])
     torch.cuda.synchronize()
 
-    for cfg, (desc, inp, Wkv), (rk, rv, rn), (kc, vc, nf, st) in zip(cfgs, prepared, refs, outs):
+    for cfg, (desc, inp, W), (rk, rv, rn), (kc, vc, nf, st) in zip(cfgs, prepared, refs, outs):
         assert int(st.item()) == 0
         assert int(nf.item()) == rn
         _compare(cfg, inp, kc, vc, rk, rv)
@@ -110,6 +111,6 @@ def test_static_fill_refuses_fills_larger_than_its_scratch():
     desc = desc_of(synth.LLAMA8B)
     assert rf.rf_fill_workspace_bytes(desc) > rf.RF_STATIC_SCRATCH_BYTES
     with pytest.raises(rf.RFError) as ei:
-        rf.rf_fill_kv_static(desc, None, synth.LLAMA8B.d, None, None, None, None, None, None, 0, 0)
+        rf.rf_fill_kv_static(desc, None, synth.LLAMA8B.d, None, None, None, None, None, None, None, None, 0, 0)
     assert ei.value.status == rf.RF_ERR_WORKSPACE
     assert "static scratch" in str(ei.value)
