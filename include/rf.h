@@ -80,7 +80,7 @@ void rf_set_wait_timeout_ms(int64_t ms);
 enum rf_stage {
   RF_STAGE_COMPACT = 1,      /* exact-row mask -> fill_idx                    */
   RF_STAGE_GATHER = 2,       /* x_S rows -> dense operand                      */
-  RF_STAGE_ROPE_TABLE = 3,   /* cos/sin table                                  */
+  RF_STAGE_ROPE_TABLE = 3,   /* (unused: RoPE angles are computed in the kernels) */
   RF_STAGE_MAP_GEMM = 4,     /* x̂ = x_S A_lᵀ + b_l, all upper layers           */
   RF_STAGE_KV_GEMM = 5,      /* K/V projection + norm scale + RoPE + scatter   */
   RF_STAGE_FOLD = 6,         /* gain fold into W_k / W_v                       */
@@ -423,7 +423,10 @@ rf_status rf_xmodel_map(const rf_xmodel_desc* desc, const int32_t* src_layers,
                         void* workspace, size_t workspace_bytes, rf_stream_t stream);
 
 /* RoPE (inverse = 0) or its inverse (inverse = 1) on rows of heads, out of place
- * or in place: out[t][h][:] = R^{±1}(t + pos_offset) in[t][h][:].
+ * or in place: out[t][h][:] = R^{±1}(t + pos_offset) in[t][h][:]. The angle
+ * (t + pos_offset)·θ^(-2i/hd) is reduced mod 2π exactly in 64-bit fixed point,
+ * then its sine and cosine are taken in fp32 (absolute error about 2^-21); the
+ * fill and the mapper rotate the same way.
  * in, out [n_rows][ld] bf16 with H*hd <= ld. Used to build cross-model
  * calibration features (un-roped keys). [XM] content-space mapping. */
 rf_status rf_rope_rows(const rf_bf16* in, rf_bf16* out, int64_t n_rows, int64_t ld,

@@ -10,12 +10,14 @@
 //                      into the workspace
 //   1. k_compact       exact-row mask -> ascending fill_idx, n_fill        (1 CTA)
 //   2. k_gather_rows   Xf[m] = x_S[fill_idx[m]], zero pad to the M tile     (HBM)
-//   3. k_rope_table    cos/sin of (t + pos_offset) * θ^(-2i/hd), fp64 angle (tiny)
-//   4. tc_gemm<MapProb> x̂ = Xf · [A_S; …; A_{L-1}]ᵀ + b, all maps in one GEMM;
+//   3. tc_gemm<MapProb> x̂ = Xf · [A_S; …; A_{L-1}]ᵀ + b, all maps in one GEMM;
 //                       epilogue: bf16 x̂ and fp32 Σx̂² per (row, layer, N-tile)
+//   4. k_row_rms       r = rsqrt(Σx̂²/d + ε) per (row, layer) from the partials
 //   5. tc_gemm<KVProb>  [k|v] = r · x̂_l · [Wk'_l; Wv'_l]ᵀ for every layer in one GEMM;
-//                       epilogue: r = rsqrt(Σx̂²/d + ε), RoPE on k, scatter
-//                       into cache[l][fill_idx[m]] with 16-byte stores.
+//                       epilogue: the row scale r, RoPE on k at position
+//                       t + pos_offset (angle reduced in 64-bit fixed point), and
+//                       the scatter into cache[l][fill_idx[m]], whole head rows per
+//                       warp store through shared-memory staging.
 #include <algorithm>
 
 #include "rf_host.h"
@@ -24,44 +26,60 @@
 namespace rf {
 
 // --------------------------------------------------------------------------
-// 1. Row compaction: one CTA, each thread scans a contiguous chunk of the mask.
+// 1. Row compaction: one CTA walks the mask in tiles of 4 bytes per thread (one
+//    coalesced 32-bit load per thread where the mask is 4-byte aligned), scans the
+//    per-thread counts across the block and writes the filled rows' indices in
+//    ascending order, carrying the running count from tile to tile.
 // --------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) k_compact(const uint8_t* __restrict__ mask, int n_prefix,
                                                   int32_t* __restrict__ fill_idx, int32_t* __restrict__ n_fill,
                                                   int32_t* __restrict__ n_fill_out) {
   __shared__ int warp_sums[32];
   const int tid = threadIdx.x;
-  const int nthr = blockDim.x;
-  const int per = (n_prefix + nthr - 1) / nthr;
-  const int lo = min(tid * per, n_prefix);
-  const int hi = min(lo + per, n_prefix);
-  int cnt = 0;
-  for (int i = lo; i < hi; ++i) cnt += (mask == nullptr || mask[i] == 0) ? 1 : 0;
   const int lane = tid & 31, w = tid >> 5;
-  int x = cnt;
+  const bool vec = mask != nullptr && (reinterpret_cast<uintptr_t>(mask) & 3u) == 0;
+  int carry = 0;
+  for (int base = 0; base < n_prefix; base += 4 * 1024) {
+    const int i0 = base + 4 * tid;
+    unsigned keep = 0;  // bit j: row i0 + j is filled
+    if (vec && i0 + 3 < n_prefix) {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(mask + i0);
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_sums[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    int s = (lane < nthr / 32) ? warp_sums[lane] : 0;
+      for (int j = 0; j < 4; ++j) keep |= (((v >> (8 * j)) & 0xffu) == 0u ? 1u : 0u) << j;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (i0 + j < n_prefix && (mask == nullptr || mask[i0 + j] == 0)) keep |= 1u << j;
+    }
+    const int cnt = __popc(keep);
+    int x = cnt;  // inclusive scan over the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
     }
-    warp_sums[lane] = s;
+    if (lane == 31) warp_sums[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      int s = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += y;
+      }
+      warp_sums[lane] = s;
+    }
+    __syncthreads();
+    int pos = carry + x - cnt + (w > 0 ? warp_sums[w - 1] : 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if ((keep >> j) & 1u) fill_idx[pos++] = i0 + j;
+    carry += warp_sums[31];
+    __syncthreads();  // warp_sums is rewritten by the next tile
   }
-  __syncthreads();
-  int pos = x - cnt + (w > 0 ? warp_sums[w - 1] : 0);
-  for (int i = lo; i < hi; ++i)
-    if (mask == nullptr || mask[i] == 0) fill_idx[pos++] = i;
-  if (tid == nthr - 1) {
-    *n_fill = pos;
-    if (n_fill_out != nullptr) *n_fill_out = pos;
+  if (tid == 0) {
+    *n_fill = carry;
+    if (n_fill_out != nullptr) *n_fill_out = carry;
   }
 }
 
@@ -82,34 +100,6 @@ __global__ void __launch_bounds__(128) k_gather_rows(const uint4* __restrict__ x
     for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) dst[c] = __ldg(src + c);
   } else {
     for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) dst[c] = make_uint4(0, 0, 0, 0);
-  }
-}
-
-// --------------------------------------------------------------------------
-// 3. RoPE table: angle (t + pos_offset) θ^(-2i/hd) in fp64, reduced mod 2π in
-//    fp64 (two-constant Cody–Waite), then sincosf on the reduced angle.
-// --------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_rope_table(float* __restrict__ cos_t, float* __restrict__ sin_t, int n_rows,
-                                                    int half, double theta, long long pos_offset) {
-  __shared__ double inv_freq[128];
-  for (int i = threadIdx.x; i < half; i += blockDim.x) inv_freq[i] = pow(theta, -2.0 * i / (2.0 * half));
-  __syncthreads();
-  const double kInv2Pi = 0.15915494309189535;
-  const double k2PiHi = 6.283185307179586;
-  const double k2PiLo = 2.4492935982947064e-16;
-  const long long total = static_cast<long long>(n_rows) * half;
-  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long t = idx / half;
-    const int i = static_cast<int>(idx - t * half);
-    const double ang = static_cast<double>(t + pos_offset) * inv_freq[i];
-    const double k = rint(ang * kInv2Pi);
-    double r = fma(-k, k2PiHi, ang);
-    r = fma(-k, k2PiLo, r);
-    float s, c;
-    sincosf(static_cast<float>(r), &s, &c);
-    cos_t[idx] = c;
-    sin_t[idx] = s;
   }
 }
 
@@ -160,8 +150,6 @@ struct FillLayout {
   __nv_bfloat16* xf;
   __nv_bfloat16* xhat;      // [P][M_pad][d], or one layer in the layered fill
   float* ssp;
-  float* rope_cos;
-  float* rope_sin;
   __nv_bfloat16* slot[2];   // layered fill: bf16 map ring (when maps are copied or expanded)
   int8_t* stage[2];         // layered fill: int8 landing slots for host int8 maps
   __nv_bfloat16* wk;        // gain-folded projections [P][KV][d] (without RF_WEIGHTS_PREFOLDED)
@@ -216,8 +204,6 @@ static FillLayout fill_layout(const rf_fill_desc* d, void* ws, const rf_map_sour
   l.xf = c.take<__nv_bfloat16>(M_pad * fill_din(d));
   l.xhat = c.take<__nv_bfloat16>(xhat_layers * M_pad * d->d);
   l.ssp = c.take<float>(xhat_layers * (d->d / kBN) * M_pad);
-  l.rope_cos = c.take<float>(std::max<int64_t>(n_prefix, 1) * (d->head_dim / 2));
-  l.rope_sin = c.take<float>(std::max<int64_t>(n_prefix, 1) * (d->head_dim / 2));
   if (!prefolded(d) && P > 0 && n_prefix > 0) {
     const int64_t w = P * d->n_kv_heads * d->head_dim * d->d;
     l.wk = c.take<__nv_bfloat16>(w);
@@ -243,9 +229,9 @@ static rf_status fill_gemms(bool pair, const rf_fill_desc* desc, const FillLayou
   const int64_t d_in = fill_din(desc);
   MapGemmArgs ma{lay.xf, d_in, M_pad, lay.n_fill, A, b, nullptr, lay.xhat, lay.ssp, d, d_in, P, M_pad, dev_status};
   if ((st = map_gemm(pair, ma, sms, s)) != RF_OK) return st;
-  KvGemmArgs ka{lay.xhat, lay.ssp, lay.n_fill, lay.fill_idx, lay.rope_cos, lay.rope_sin, Wk, Wv, k_cache, v_cache,
+  KvGemmArgs ka{lay.xhat, lay.ssp, lay.n_fill, lay.fill_idx, Wk, Wv, k_cache, v_cache,
                 desc->v_scale, desc->k_norm_gain, layer_stride, row_stride, d, P, desc->S, M_pad, KV,
-                desc->head_dim, desc->rms_eps, dev_status};
+                desc->head_dim, desc->rms_eps, desc->rope_theta, desc->pos_offset, dev_status};
   return kv_gemm(pair, ka, sms, s);
 }
 
@@ -304,8 +290,8 @@ static rf_status kv_gemm_t(const KvGemmArgs& a, int sms, cudaStream_t s) {
   pr.n_fill = a.n_fill;
   pr.fill_idx = a.fill_idx;
   pr.ssp = a.ssp;
-  pr.rope_cos = a.rope_cos;
-  pr.rope_sin = a.rope_sin;
+  pr.pos_offset = a.pos_offset;
+  pr.rope = rope_freqs(a.rope_theta, static_cast<int>(a.hd));
   pr.kc = static_cast<__nv_bfloat16*>(a.k_cache);
   pr.vc = static_cast<__nv_bfloat16*>(a.v_cache);
   pr.v_scale = a.v_scale;
@@ -409,8 +395,8 @@ static rf_status kv_weights(const rf_fill_desc* desc, const FillLayout& lay, con
   return RF_OK;
 }
 
-// Row compaction, and when anything is filled the gather and the RoPE table, on
-// stream s. *work is false when there is nothing left to fill.
+// Row compaction, and when anything is filled the gather, on stream s. *work is
+// false when there is nothing left to fill.
 static rf_status fill_prologue(const rf_fill_desc* desc, const rf_bf16* x_S, int64_t ld_x, const uint8_t* exact_mask,
                                int32_t* n_fill_out, const FillLayout& lay, int sms, cudaStream_t s, bool* work) {
   *work = false;
@@ -435,14 +421,7 @@ static rf_status fill_prologue(const rf_fill_desc* desc, const rf_bf16* x_S, int
                                                               static_cast<int>(fill_din(desc) / 8),
                                                               static_cast<int>(M_pad));
   }
-  const int half = static_cast<int>(desc->head_dim / 2);
-  const int rope_blocks = static_cast<int>(std::min<int64_t>((n_prefix * half + 255) / 256, 4LL * sms));
-  {
-    ProfScope prof(s, RF_STAGE_ROPE_TABLE);
-    k_rope_table<<<rope_blocks, 256, 0, s>>>(lay.rope_cos, lay.rope_sin, static_cast<int>(n_prefix), half,
-                                             desc->rope_theta, static_cast<long long>(desc->pos_offset));
-  }
-  if ((st = cuda_check(cudaGetLastError(), "gather / rope launch")) != RF_OK) return st;
+  if ((st = cuda_check(cudaGetLastError(), "gather launch")) != RF_OK) return st;
   *work = true;
   return RF_OK;
 }
@@ -594,13 +573,14 @@ extern "C" rf_status rf_fill_kv_layered(const rf_fill_desc* desc, const rf_bf16*
                    lay.xhat, lay.ssp, d, d_in, g, M_pad, dev_status};
     if ((st = map_gemm(pair, ma, sms, s)) != RF_OK) return st;
     if (staged && (st = cuda_check(cudaEventRecord(freed[r], s), "cudaEventRecord")) != RF_OK) return st;
-    KvGemmArgs ka{lay.xhat, lay.ssp, lay.n_fill, lay.fill_idx, lay.rope_cos, lay.rope_sin,
+    KvGemmArgs ka{lay.xhat, lay.ssp, lay.n_fill, lay.fill_idx,
                   static_cast<const __nv_bfloat16*>(wk) + static_cast<size_t>(c0) * KV * d,
                   static_cast<const __nv_bfloat16*>(wv) + static_cast<size_t>(c0) * KV * d, k_cache, v_cache,
                   desc->v_scale ? desc->v_scale + c0 * H : nullptr,
                   desc->k_norm_gain ? reinterpret_cast<const __nv_bfloat16*>(desc->k_norm_gain) + c0 * desc->head_dim
                                     : nullptr,
-                  layer_stride, row_stride, d, g, desc->S + c0, M_pad, KV, desc->head_dim, desc->rms_eps, dev_status};
+                  layer_stride, row_stride, d, g, desc->S + c0, M_pad, KV, desc->head_dim, desc->rms_eps,
+                  desc->rope_theta, desc->pos_offset, dev_status};
     if ((st = kv_gemm(pair, ka, sms, s)) != RF_OK) return st;
   }
   return RF_OK;

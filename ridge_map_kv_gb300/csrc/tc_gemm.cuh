@@ -44,6 +44,7 @@
 // outstanding copies and MMAs are drained, and TMEM is freed.
 #pragma once
 #include <algorithm>
+#include <type_traits>
 
 #include "rf_device.cuh"
 #include "rf_host.h"
@@ -86,9 +87,26 @@ struct GemmShared {
   int abort;
 };
 
+// Shared memory of a CTA: the stage ring, the barriers, then (from a 128-byte
+// boundary) `Prob::kEpiSmemBytes` of epilogue scratch when the problem declares it,
+// e.g. the staging rows of the cache-writing epilogues.
+template <class P, class = void>
+struct EpiSmemBytes {
+  static constexpr size_t value = 0;
+};
+template <class P>
+struct EpiSmemBytes<P, std::void_t<decltype(P::kEpiSmemBytes)>> {
+  static constexpr size_t value = P::kEpiSmemBytes;
+};
+
 template <bool kPair>
+constexpr size_t gemm_epi_offset() {
+  return (static_cast<size_t>(GemmCfg<kPair>::kStages) * GemmCfg<kPair>::kStageBytes + sizeof(GemmShared) + 127) &
+         ~size_t(127);
+}
+template <class Prob>
 constexpr size_t gemm_smem_bytes() {
-  return 1024 + static_cast<size_t>(GemmCfg<kPair>::kStages) * GemmCfg<kPair>::kStageBytes + sizeof(GemmShared);
+  return 1024 + gemm_epi_offset<Prob::kPair>() + EpiSmemBytes<Prob>::value;
 }
 
 template <bool kPair>
@@ -127,6 +145,14 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int k) {
 
 __device__ __forceinline__ uint8_t* gemm_smem_base(uint8_t* raw) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+}
+
+// The epilogue scratch of the running GEMM kernel (see gemm_smem_bytes), for the
+// problem's epilogue to call.
+template <bool kPair>
+__device__ __forceinline__ uint8_t* gemm_epi_smem() {
+  extern __shared__ uint8_t smem_raw[];
+  return gemm_smem_base(smem_raw) + gemm_epi_offset<kPair>();
 }
 
 // --------------------------------------------------------------------------
@@ -464,16 +490,18 @@ rf_status launch_gemm(const Prob& pr, int64_t max_units, int sms, cudaStream_t s
   const void* fn;
   if constexpr (kPair) fn = reinterpret_cast<const void*>(&tc_gemm_pair_kernel<Prob>);
   else fn = reinterpret_cast<const void*>(&tc_gemm_kernel<Prob>);
-  rf_status st = set_smem_attr(fn, gemm_smem_bytes<kPair>(), &attr_mask);
+  constexpr size_t smem = gemm_smem_bytes<Prob>();
+  static_assert(smem <= 227 * 1024, "shared memory beyond the 227 KB a CTA may hold");
+  rf_status st = set_smem_attr(fn, smem, &attr_mask);
   if (st != RF_OK) return st;
   if (max_units <= 0) max_units = 1;
   if constexpr (kPair) {
-    const int cap = max_active_pairs(fn, gemm_smem_bytes<true>(), gemm_threads<Prob>(), sms, pair_cap);
+    const int cap = max_active_pairs(fn, smem, gemm_threads<Prob>(), sms, pair_cap);
     const int pairs = static_cast<int>(std::min<int64_t>(max_units, cap));
-    tc_gemm_pair_kernel<Prob><<<2 * pairs, gemm_threads<Prob>(), gemm_smem_bytes<true>(), s>>>(pr);
+    tc_gemm_pair_kernel<Prob><<<2 * pairs, gemm_threads<Prob>(), smem, s>>>(pr);
   } else {
     const int grid = static_cast<int>(std::min<int64_t>(max_units, sms));
-    tc_gemm_kernel<Prob><<<grid, gemm_threads<Prob>(), gemm_smem_bytes<false>(), s>>>(pr);
+    tc_gemm_kernel<Prob><<<grid, gemm_threads<Prob>(), smem, s>>>(pr);
   }
   return cuda_check(cudaGetLastError(), what);
 }

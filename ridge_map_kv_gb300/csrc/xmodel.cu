@@ -10,14 +10,16 @@
 //   0. k_check_layers    the caller's device table of source layers: range check
 //                        (an entry outside [0, L_src) sets RF_ERR_INVALID_ARG and
 //                        turns the GEMM into a no-op) and a copy into the workspace
-//   1. k_rope_table x2   cos/sin tables for θ_src and θ_tgt (fp64 angles)
-//   2. k_rope_rows       un-rope every source layer's keys once into the workspace
-//   3. tc_gemm<XMProb>   for every target layer l, M-tile of rows and N-tile of
+//   1. k_rope_rows       un-rope every source layer's keys once into the workspace
+//   2. tc_gemm<XMProb>   for every target layer l, M-tile of rows and N-tile of
 //                        [K | V] columns: A = the selected source features (the
 //                        K-loop walks the k source layers, 64 features per step,
 //                        reading the table src[l][j]), B = W_K or W_V of layer l;
 //                        epilogue: + b, target RoPE on K, store into the target
-//                        caches (16-byte stores).
+//                        caches, whole head rows per warp store through
+//                        shared-memory staging.
+// RoPE angles are reduced in 64-bit fixed point (RopeFreqs, epilogue.cuh) and
+// their sine and cosine taken on the SFU, in both kernels: no tables.
 #include <algorithm>
 #include <vector>
 
@@ -27,17 +29,13 @@
 
 namespace rf {
 
-__global__ void k_rope_table(float* cos_t, float* sin_t, int n_rows, int half, double theta, long long pos_offset);
-
-// out[row][h][:] = R^{sign}(pos) in[row][h][:], pos = row % rows_per_position + pos_offset.
-// With a table (cos_t, sin_t: [rows_per_position][hd/2]) the angle comes from it;
-// without, the angle is computed here (fp64 angle, fp64 reduction mod 2π, sincosf).
-// Each thread handles 8 rotation pairs of one head of one row.
+// out[row][h][:] = R^{sign}(pos) in[row][h][:], pos = row % rows_per_position + pos_offset,
+// with the frequencies `rf` of (θ, hd). Each thread handles 8 rotation pairs of one
+// head of one row.
 __global__ void __launch_bounds__(256) k_rope_rows(const __nv_bfloat16* __restrict__ in, __nv_bfloat16* out,
                                                    long long n_rows, long long ld_in, long long ld_out, int n_heads,
                                                    int hd, long long rows_per_position, long long pos_offset,
-                                                   const float* __restrict__ cos_t, const float* __restrict__ sin_t,
-                                                   double theta, float sign) {
+                                                   const __grid_constant__ RopeFreqs rf, float sign) {
   const int half = hd >> 1;
   const int chunks = half / 8;
   const long long total = n_rows * n_heads * chunks;
@@ -53,23 +51,9 @@ __global__ void __launch_bounds__(256) k_rope_rows(const __nv_bfloat16* __restri
     const uint4 a = *reinterpret_cast<const uint4*>(src + i0);
     const uint4 b = *reinterpret_cast<const uint4*>(src + half + i0);
     float c[8], s[8];
-    if (cos_t != nullptr) {
-      const float4* cp = reinterpret_cast<const float4*>(cos_t + t * half + i0);
-      const float4* sp = reinterpret_cast<const float4*>(sin_t + t * half + i0);
-      const float4 c0 = cp[0], c1 = cp[1], s0 = sp[0], s1 = sp[1];
-      c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w; c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
-      s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w; s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
-    } else {
-      const double kInv2Pi = 0.15915494309189535, k2PiHi = 6.283185307179586, k2PiLo = 2.4492935982947064e-16;
+    const unsigned long long pos = static_cast<unsigned long long>(t + pos_offset);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const double ang = static_cast<double>(t + pos_offset) * pow(theta, -2.0 * (i0 + q) / hd);
-        const double k = rint(ang * kInv2Pi);
-        double r = fma(-k, k2PiHi, ang);
-        r = fma(-k, k2PiLo, r);
-        sincosf(static_cast<float>(r), &s[q], &c[q]);
-      }
-    }
+    for (int q = 0; q < 8; ++q) rope_cs(pos, rf.g[i0 + q], c[q], s[q]);
     const __nv_bfloat162* ah = reinterpret_cast<const __nv_bfloat162*>(&a);
     const __nv_bfloat162* bh = reinterpret_cast<const __nv_bfloat162*>(&b);
     uint4 o1, o2;
@@ -120,8 +104,8 @@ struct XMProb {
   const int32_t* ok;   // 1 if the table passed k_check_layers; else the GEMM does nothing
   const float* bk;     // [L_tgt][KV]
   const float* bv;
-  const float* cos_t;  // target table [N][hd/2]
-  const float* sin_t;
+  RopeFreqs rope_t;      // target RoPE frequencies (θ_tgt, hd)
+  long long pos_offset;  // position of row 0
   __nv_bfloat16* k_tgt;  // [L_tgt][N][KV]
   __nv_bfloat16* v_tgt;
   int N, KV, hd, k, L_tgt, m_tiles, n_half;
@@ -131,6 +115,7 @@ struct XMProb {
   static constexpr bool kBMN = false;
   static constexpr bool kPair = kPair_;
   static constexpr int kEpiWarps = 4;
+  static constexpr size_t kEpiSmemBytes = kEpiWarps * kStageBytesPerWarp;  // staging rows of the target stores
   struct EpiState {};
   __device__ void epilogue_after(EpiState&, int, int, int, int, int, uint32_t) const {}
   using Cfg = GemmCfg<kPair_>;
@@ -198,14 +183,15 @@ struct XMProb {
     const int t = mt * Cfg::kUnitM + static_cast<int>(rank) * kBM + row;
     const bool valid = t < N;
     const int tt = valid ? t : 0;
-    const int half = hd >> 1;
-    const float* cs = cos_t + static_cast<size_t>(tt) * half;
-    const float* sn = sin_t + static_cast<size_t>(tt) * half;
+    const unsigned long long pos = static_cast<unsigned long long>(static_cast<long long>(tt) + pos_offset);
     const float* bias = (is_k ? bk : bv) + static_cast<size_t>(l) * KV + col0;
     __nv_bfloat16* dst = (is_k ? k_tgt : v_tgt) + (static_cast<size_t>(l) * N + tt) * KV + col0;
+    const uint32_t stage =
+        smem_u32(gemm_epi_smem<kPair_>()) + static_cast<uint32_t>(((threadIdx.x >> 5) - 2) * kStageBytesPerWarp);
 #pragma unroll 1
     for (int hh = 0; hh < kBN / hd; ++hh)
-      emit_head(tacc + hh * hd, hd, 1.0f, bias + hh * hd, nullptr, is_k, cs, sn, dst + hh * hd, valid);
+      emit_head(tacc + hh * hd, hd, 1.0f, bias + hh * hd, nullptr, is_k ? rope_t.g : nullptr, pos,
+                valid ? dst + hh * hd : nullptr, stage);
   }
 };
 
@@ -214,10 +200,6 @@ struct XLayout {
   __nv_bfloat16* ku;
   int32_t* src;
   int32_t* ok;
-  float* cos_s;
-  float* sin_s;
-  float* cos_t;
-  float* sin_t;
   size_t bytes;
 };
 
@@ -228,10 +210,6 @@ static XLayout xmodel_layout(const rf_xmodel_desc* d, void* ws) {
   l.ku = c.take<__nv_bfloat16>(d->L_src * d->N * KV);
   l.src = c.take<int32_t>(d->L_tgt * d->k);
   l.ok = c.take<int32_t>(1);
-  l.cos_s = c.take<float>(d->N * (d->head_dim / 2));
-  l.sin_s = c.take<float>(d->N * (d->head_dim / 2));
-  l.cos_t = c.take<float>(d->N * (d->head_dim / 2));
-  l.sin_t = c.take<float>(d->N * (d->head_dim / 2));
   l.bytes = c.bytes();
   return l;
 }
@@ -269,8 +247,8 @@ rf_status xmodel_gemm(const rf_xmodel_desc* desc, const XLayout& lay, const rf_b
   pr.ok = lay.ok;
   pr.bk = bk;
   pr.bv = bv;
-  pr.cos_t = lay.cos_t;
-  pr.sin_t = lay.sin_t;
+  pr.rope_t = rope_freqs(desc->theta_tgt, static_cast<int>(desc->head_dim));
+  pr.pos_offset = static_cast<long long>(desc->pos_offset);
   pr.k_tgt = reinterpret_cast<__nv_bfloat16*>(k_tgt);
   pr.v_tgt = reinterpret_cast<__nv_bfloat16*>(v_tgt);
   pr.N = static_cast<int>(N);
@@ -317,27 +295,19 @@ extern "C" rf_status rf_xmodel_map(const rf_xmodel_desc* desc, const int32_t* sr
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t KV = desc->n_kv_heads * desc->head_dim, N = desc->N;
   const int half = static_cast<int>(desc->head_dim / 2);
-
   // the caller's device table, checked and copied on the device (no host round trip)
   k_check_layers<<<1, 256, 0, s>>>(src_layers, static_cast<int>(desc->L_tgt * desc->k), static_cast<int>(desc->L_src),
                                    lay.src, lay.ok, dev_status);
   if ((st = cuda_check(cudaGetLastError(), "k_check_layers launch")) != RF_OK) return st;
-  {
-    ProfScope prof(s, RF_STAGE_ROPE_TABLE);
-    const int blocks = static_cast<int>(std::min<int64_t>((N * half + 255) / 256, 4LL * sms));
-    k_rope_table<<<blocks, 256, 0, s>>>(lay.cos_s, lay.sin_s, static_cast<int>(N), half, desc->theta_src,
-                                        static_cast<long long>(desc->pos_offset));
-    k_rope_table<<<blocks, 256, 0, s>>>(lay.cos_t, lay.sin_t, static_cast<int>(N), half, desc->theta_tgt,
-                                        static_cast<long long>(desc->pos_offset));
-  }
   {
     ProfScope prof(s, RF_STAGE_UNROPE);
     const long long n_rows = desc->L_src * N;
     const long long total = n_rows * desc->n_kv_heads * (half / 8);
     const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 16LL * sms));
     k_rope_rows<<<blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(k_src), lay.ku, n_rows, KV, KV,
-                                       static_cast<int>(desc->n_kv_heads), static_cast<int>(desc->head_dim), N, 0,
-                                       lay.cos_s, lay.sin_s, 0.0, -1.0f);
+                                       static_cast<int>(desc->n_kv_heads), static_cast<int>(desc->head_dim), N,
+                                       static_cast<long long>(desc->pos_offset),
+                                       rope_freqs(desc->theta_src, static_cast<int>(desc->head_dim)), -1.0f);
   }
   if ((st = cuda_check(cudaGetLastError(), "rope launches")) != RF_OK) return st;
 
@@ -365,7 +335,7 @@ extern "C" rf_status rf_rope_rows(const rf_bf16* in, rf_bf16* out, int64_t n_row
   ProfScope prof(s, RF_STAGE_UNROPE);
   k_rope_rows<<<blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(in), reinterpret_cast<__nv_bfloat16*>(out),
                                      n_rows, ld, ld, static_cast<int>(n_heads), static_cast<int>(head_dim), n_rows,
-                                     pos_offset, nullptr, nullptr, theta, inverse ? -1.0f : 1.0f);
+                                     pos_offset, rope_freqs(theta, static_cast<int>(head_dim)), inverse ? -1.0f : 1.0f);
   return cuda_check(cudaGetLastError(), "k_rope_rows launch");
 }
 
@@ -410,13 +380,14 @@ extern "C" rf_status rf_concat_layers(const rf_bf16* src, int64_t n_layers, int6
   const __nv_bfloat16* in = reinterpret_cast<const __nv_bfloat16*>(src);
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
   ProfScope prof(s, RF_STAGE_UNROPE);
+  const RopeFreqs rf = theta > 0.0 ? rope_freqs(theta, static_cast<int>(head_dim)) : RopeFreqs{};
   for (int64_t l = 0; l < n_layers; ++l) {
     const long long total = theta > 0.0 ? n_rows * n_heads * (head_dim / 16) : n_rows * (W / 8);
     const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 16LL * sms));
     if (theta > 0.0) {
       k_rope_rows<<<blocks, 256, 0, s>>>(in + l * layer_stride, o + l * W, n_rows, ld_src, ld_out,
                                          static_cast<int>(n_heads), static_cast<int>(head_dim), n_rows, pos_offset,
-                                         nullptr, nullptr, theta, -1.0f);
+                                         rf, -1.0f);
     } else {
       k_copy_rows<<<blocks, 256, 0, s>>>(in + l * layer_stride, o + l * W, n_rows, ld_src, ld_out,
                                          static_cast<int>(W));

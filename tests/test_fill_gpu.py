@@ -104,6 +104,31 @@ def test_fill_degenerate_arms(case):
         assert_values(cfg, inp, res, idx)
 
 
+@pytest.mark.parametrize("offset", [0, 1, 3, 4])
+def test_compaction_over_several_mask_tiles_at_any_mask_alignment(offset):
+    """The compaction reads the mask 4 bytes per thread in tiles of 4096 rows, with
+    32-bit loads where the mask is 4-byte aligned and byte loads elsewhere. A prefix
+    of 3 tiles less one row, its mask at byte offsets 0..4 into a buffer: fill_idx
+    (the workspace's first region) must equal the oracle's partition exactly, and the
+    cache bookkeeping must hold bit for bit."""
+    cfg = _small("compaction tiles", d=256, L=2, S=1, N=12300, T=13, H=2, hd=64, exact=None)
+    n_prefix = cfg.N - cfg.T                                    # 12,287 = 3 * 4096 - 1
+    rng = np.random.default_rng(17)
+    mnp = (rng.random(n_prefix) < 0.3).astype(np.uint8)
+    mnp[4090:4110] = 1                                          # an exact run across a tile edge
+    mnp[-5:] = 0
+    buf = torch.zeros(n_prefix + 8, dtype=torch.uint8, device="cuda")
+    buf[offset:offset + n_prefix] = torch.as_tensor(mnp, device="cuda")
+    inp = synth.fill_inputs(cfg)
+    res = run_fill(cfg, inp, mask=buf[offset:offset + n_prefix])
+    assert res["status"] == 0
+    idx = O.prefix_partition(cfg.N, cfg.T, mnp)
+    assert res["n_fill"] == len(idx)
+    got = res["ws"][: n_prefix * 4].view(torch.int32)[: len(idx)].cpu().numpy()
+    assert np.array_equal(got, idx)
+    assert_bookkeeping(cfg, res, mnp)
+
+
 def _sample_rows(idx: np.ndarray, mask_np, n_prefix: int, n_random=192, seed=1):
     rng = np.random.default_rng(seed)
     pick = {int(idx[0]), int(idx[-1])}
