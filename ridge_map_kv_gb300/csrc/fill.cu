@@ -147,6 +147,7 @@ rf_status fold_gain(const void* gain, const void* W, void* out, int64_t P, int64
 struct FillLayout {
   int32_t* fill_idx;
   int32_t* n_fill;
+  int* sched;               // unit counter of the GEMM launches (each clears it first)
   __nv_bfloat16* xf;
   __nv_bfloat16* xhat;      // [P][M_pad][d], or one layer in the layered fill
   float* ssp;
@@ -201,6 +202,7 @@ static FillLayout fill_layout(const rf_fill_desc* d, void* ws, const rf_map_sour
   FillLayout l{};
   l.fill_idx = c.take<int32_t>(std::max<int64_t>(n_prefix, 1));
   l.n_fill = c.take<int32_t>(1);
+  l.sched = c.take<int>(1);
   l.xf = c.take<__nv_bfloat16>(M_pad * fill_din(d));
   l.xhat = c.take<__nv_bfloat16>(xhat_layers * M_pad * d->d);
   l.ssp = c.take<float>(xhat_layers * (d->d / kBN) * M_pad);
@@ -227,11 +229,12 @@ static rf_status fill_gemms(bool pair, const rf_fill_desc* desc, const FillLayou
   const int64_t d = desc->d, P = desc->L - desc->S, KV = desc->n_kv_heads * desc->head_dim;
   const int64_t M_pad = round_up(desc->N - desc->T, kFillRowAlign);
   const int64_t d_in = fill_din(desc);
-  MapGemmArgs ma{lay.xf, d_in, M_pad, lay.n_fill, A, b, nullptr, lay.xhat, lay.ssp, d, d_in, P, M_pad, dev_status};
+  MapGemmArgs ma{lay.xf, d_in, M_pad, lay.n_fill, A, b, nullptr, lay.xhat, lay.ssp, d, d_in, P, M_pad, dev_status,
+                 lay.sched};
   if ((st = map_gemm(pair, ma, sms, s)) != RF_OK) return st;
   KvGemmArgs ka{lay.xhat, lay.ssp, lay.n_fill, lay.fill_idx, Wk, Wv, k_cache, v_cache,
                 desc->v_scale, desc->k_norm_gain, layer_stride, row_stride, d, P, desc->S, M_pad, KV,
-                desc->head_dim, desc->rms_eps, desc->rope_theta, desc->pos_offset, dev_status};
+                desc->head_dim, desc->rms_eps, desc->rope_theta, desc->pos_offset, dev_status, lay.sched};
   return kv_gemm(pair, ka, sms, s);
 }
 
@@ -255,6 +258,7 @@ static rf_status map_gemm_t(const MapGemmArgs& a, int sms, cudaStream_t s) {
   pr.n_ntiles = static_cast<int>(a.P * a.d / kBN);
   pr.m_band = static_cast<int>(
       std::max<long long>(1, std::min<long long>(m_tiles_max, kMapBandBytes / (Cfg::kUnitM * a.d_in * 2))));
+  pr.sched = a.sched;
   pr.dev_status = a.dev_status;
   pr.timeout_ns = wait_timeout_ns();
   ProfScope prof(s, RF_STAGE_MAP_GEMM);
@@ -308,6 +312,7 @@ static rf_status kv_gemm_t(const KvGemmArgs& a, int sms, cudaStream_t s) {
   pr.n_ss = static_cast<int>(a.d / kBN);
   pr.inv_d = 1.0f / static_cast<float>(a.d);
   pr.eps = static_cast<float>(a.eps);
+  pr.sched = a.sched;
   pr.dev_status = a.dev_status;
   pr.timeout_ns = wait_timeout_ns();
   const int64_t m_tiles_max = a.M_pad / Cfg::kUnitM;
@@ -570,7 +575,7 @@ extern "C" rf_status rf_fill_kv_layered(const rf_fill_desc* desc, const rf_bf16*
       Ap = lay.slot[r];
     }
     MapGemmArgs ma{lay.xf, d_in, M_pad, lay.n_fill, Ap, b + c0 * d, int8 ? maps->row_scale + c0 * d : nullptr,
-                   lay.xhat, lay.ssp, d, d_in, g, M_pad, dev_status};
+                   lay.xhat, lay.ssp, d, d_in, g, M_pad, dev_status, lay.sched};
     if ((st = map_gemm(pair, ma, sms, s)) != RF_OK) return st;
     if (staged && (st = cuda_check(cudaEventRecord(freed[r], s), "cudaEventRecord")) != RF_OK) return st;
     KvGemmArgs ka{lay.xhat, lay.ssp, lay.n_fill, lay.fill_idx,
@@ -580,7 +585,7 @@ extern "C" rf_status rf_fill_kv_layered(const rf_fill_desc* desc, const rf_bf16*
                   desc->k_norm_gain ? reinterpret_cast<const __nv_bfloat16*>(desc->k_norm_gain) + c0 * desc->head_dim
                                     : nullptr,
                   layer_stride, row_stride, d, g, desc->S + c0, M_pad, KV, desc->head_dim, desc->rms_eps,
-                  desc->rope_theta, desc->pos_offset, dev_status};
+                  desc->rope_theta, desc->pos_offset, dev_status, lay.sched};
     if ((st = kv_gemm(pair, ka, sms, s)) != RF_OK) return st;
   }
   return RF_OK;

@@ -38,6 +38,7 @@ struct MapProb {
   __nv_bfloat16* xhat;     // [P][M_pad][d]
   float* ssp;              // [P][d/256][M_pad]
   int d, k_in, P, M_pad, n_ntiles, m_band;  // d: map output width; k_in: map input width
+  int* sched;              // unit counter (dynamic unit order), or nullptr
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = false;
@@ -150,6 +151,7 @@ struct KVProb {
   RopeFreqs rope;          // the layers' RoPE frequencies (θ, hd)
   int d, P, S, M_pad, KV, hd, n_ntiles, n_ss;
   float inv_d, eps;
+  int* sched;              // unit counter (dynamic unit order), or nullptr
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = false;
@@ -267,6 +269,7 @@ struct MapGemmArgs {
   float* ssp;
   int64_t d, d_in, P, M_pad;
   int32_t* dev_status;
+  int* sched = nullptr;       // a device int the launch may use for its dynamic unit order
 };
 rf_status map_gemm(bool pair, const MapGemmArgs& a, int sms, cudaStream_t s);
 
@@ -288,6 +291,7 @@ struct KvGemmArgs {
   double rope_theta;
   int64_t pos_offset;
   int32_t* dev_status;
+  int* sched = nullptr;       // a device int the launch may use for its dynamic unit order
 };
 rf_status kv_gemm(bool pair, const KvGemmArgs& a, int sms, cudaStream_t s);
 

@@ -144,6 +144,11 @@ __device__ __forceinline__ void cluster_sync_all() {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Store of a 32-bit value to shared memory given by its shared::cluster address
+// (this CTA or a peer).
+__device__ __forceinline__ void st_shared_cluster_s32(uint32_t cluster_addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
 // TMA load into this CTA's shared memory whose completion is signalled on an
 // mbarrier that may live in the peer CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tmap, uint32_t bar_cluster, int32_t x,

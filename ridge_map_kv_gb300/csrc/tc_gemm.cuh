@@ -36,9 +36,19 @@
 // per (unit, sub-tile) for its `Coords` (`coords(u, sb)`), and per K-block only
 // issues the loads from them (`issue_loads(c, kb, ...)`): one thread issues every
 // copy of the CTA, so any per-K-block arithmetic or memory read there would
-// throttle the whole pipeline. Units are dealt round-robin over
-// CTAs (pairs). Operands may be K-major (box {64, rows}) or MN-major (boxes
-// {64, 64} per 64 rows of M or N).
+// throttle the whole pipeline. Operands may be K-major (box {64, rows}) or
+// MN-major (boxes {64, 64} per 64 rows of M or N).
+//
+// Unit order. By default units are dealt round-robin over CTAs (pairs). A problem
+// that holds a non-null `int* sched` (a zeroed device int, one per launch; the
+// launcher clears it) is scheduled dynamically instead: the leading CTA's producer
+// takes each next unit from that counter with an atomic add, one unit ahead, and
+// posts it to every role of both CTAs through a ring of kUnitRing slots in shared
+// memory (unit_full / unit_empty mbarriers; -1 ends the sequence). Units then run
+// in the order they are asked for, so a CTA pair that runs faster takes more
+// units rather than drifting away from the pairs that read the same operand tiles
+// through L2 (with round-robin dealing, pairs that ran a few units apart over a
+// long launch re-read shared tiles from DRAM).
 //
 // All waits are bounded (rf_device.cuh); on a timeout every role stops,
 // outstanding copies and MMAs are drained, and TMEM is freed.
@@ -77,15 +87,131 @@ struct GemmCfg {
   static constexpr int kStageBytes = kTileABytes + kTileBBytes;
 };
 
+constexpr int kUnitRing = 4;  // posted units in flight (dynamic order)
+
 struct GemmShared {
   uint64_t full[8];
   uint64_t empty[8];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t mma_done;
+  uint64_t unit_full[kUnitRing];   // in each CTA: the leader's producer posted the slot
+  uint64_t unit_empty[kUnitRing];  // the leader's only: every consumer of both CTAs took it
+  int unit_ring[kUnitRing];
   uint32_t tmem_base;
   int abort;
 };
+
+// Dynamic unit order (see above): the problem's `sched` counter, or nullptr.
+template <class P, class = void>
+struct HasSched : std::false_type {};
+template <class P>
+struct HasSched<P, std::void_t<decltype(std::declval<const P&>().sched)>> : std::true_type {};
+template <class Prob>
+__host__ __device__ __forceinline__ int* sched_of(const Prob& p) {
+  if constexpr (HasSched<Prob>::value) return p.sched;
+  else return nullptr;
+}
+
+// The leader's producer: posts unit u (or -1) to slot `slot` of the ring of this
+// CTA and, for a pair, of the peer, once every consumer took the slot's previous
+// unit. False after an abort. The leader's own CTA is reached with CTA-scope
+// operations (its MMA thread, on the critical path, then waits at CTA scope); only
+// the peer's copy goes through cluster-scope release.
+template <bool kPair>
+__device__ __forceinline__ bool post_unit(GemmShared* sh, int u, int& slot, uint32_t& phase, volatile int* abort_flag,
+                                          uint64_t timeout) {
+  if (!mbar_wait<kPair>(&sh->unit_empty[slot], phase ^ 1u, abort_flag, timeout)) return false;
+  *reinterpret_cast<volatile int*>(&sh->unit_ring[slot]) = u;
+  mbar_arrive(&sh->unit_full[slot]);  // release at CTA scope
+  if constexpr (kPair) {
+    st_shared_cluster_s32(mapa_shared(smem_u32(&sh->unit_ring[slot]), 1), u);
+    mbar_arrive_cluster(mapa_shared(smem_u32(&sh->unit_full[slot]), 1));  // release at cluster scope
+  }
+  if (++slot == kUnitRing) {
+    slot = 0;
+    phase ^= 1u;
+  }
+  return true;
+}
+// A consumer thread: the next posted unit (-1 at the end), or -2 after an abort.
+// `remote` is true in the peer CTA of a pair (its ring is written by the leader
+// from the other CTA). The caller then hands the slot back with give_back_unit
+// (once per consumer: one thread, or lane 0 of a warp after __syncwarp) and
+// advances with next_unit_slot.
+__device__ __forceinline__ int take_unit(GemmShared* sh, int slot, uint32_t phase, bool remote,
+                                         volatile int* abort_flag, uint64_t timeout) {
+  const bool ok = remote ? mbar_wait<true>(&sh->unit_full[slot], phase, abort_flag, timeout)
+                         : mbar_wait<false>(&sh->unit_full[slot], phase, abort_flag, timeout);
+  if (!ok) return -2;
+  return *reinterpret_cast<volatile int*>(&sh->unit_ring[slot]);
+}
+__device__ __forceinline__ void give_back_unit(GemmShared* sh, int slot, bool remote) {
+  if (remote) mbar_arrive_cluster(mapa_shared(smem_u32(&sh->unit_empty[slot]), 0));
+  else mbar_arrive(&sh->unit_empty[slot]);
+}
+__device__ __forceinline__ void next_unit_slot(int& slot, uint32_t& phase) {
+  if (++slot == kUnitRing) {
+    slot = 0;
+    phase ^= 1u;
+  }
+}
+// The leader's producer: the next unit from the counter, or -1 once all are taken.
+__device__ __forceinline__ int fetch_unit(int* sched, int n_units) {
+  const int u = atomicAdd(sched, 1);
+  return u < n_units ? u : -1;
+}
+
+// The leader's producer, dynamic order: fetches and posts the first unit before
+// its loop, so that every consumer learns each unit one unit ahead. Returns the
+// posted unit (-1 when there is none), or -2 after an abort.
+template <bool kPair>
+__device__ __forceinline__ int leader_start(GemmShared* sh, int* sched, int n_units, int& slot, uint32_t& phase,
+                                            volatile int* abort_flag, uint64_t timeout) {
+  if (sched == nullptr) return -1;
+  const int u = fetch_unit(sched, n_units);
+  return post_unit<kPair>(sh, u, slot, phase, abort_flag, timeout) ? u : -2;
+}
+// The unit after `cur` for the leader's producer, -1 at the end, -2 after an abort.
+// Dynamic order: `next` is the unit posted ahead; it is returned, and the one after
+// it is fetched and posted now. Static order: cur + stride. Start with
+// cur = first − stride.
+template <bool kPair>
+__device__ __forceinline__ int leader_next(GemmShared* sh, int* sched, int cur, int stride, int n_units, int& next,
+                                           int& slot, uint32_t& phase, volatile int* abort_flag, uint64_t timeout) {
+  if (sched == nullptr) {
+    const int n = cur + stride;
+    return n < n_units ? n : -1;
+  }
+  const int u = next;
+  if (u >= 0) {
+    next = fetch_unit(sched, n_units);
+    if (!post_unit<kPair>(sh, next, slot, phase, abort_flag, timeout)) return -2;
+  }
+  return u;
+}
+// The same for a consumer role: one thread, or a whole warp (`warp_role`: every
+// lane takes the unit, lane 0 hands the slot back once for the warp). `remote`:
+// the consumer is in the peer CTA of a pair.
+__device__ __forceinline__ int consumer_next(GemmShared* sh, int* sched, int cur, int stride, int n_units, int& slot,
+                                             uint32_t& phase, bool warp_role, bool remote, volatile int* abort_flag,
+                                             uint64_t timeout) {
+  if (sched == nullptr) {
+    const int n = cur + stride;
+    return n < n_units ? n : -1;
+  }
+  const int u = take_unit(sh, slot, phase, remote, abort_flag, timeout);
+  if (warp_role) {
+    if (!__all_sync(0xffffffffu, u != -2)) return -2;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) give_back_unit(sh, slot, remote);
+  } else {
+    if (u == -2) return -2;
+    give_back_unit(sh, slot, remote);
+  }
+  next_unit_slot(slot, phase);
+  return u;
+}
 
 // Shared memory of a CTA: the stage ring, the barriers, then (from a 128-byte
 // boundary) `Prob::kEpiSmemBytes` of epilogue scratch when the problem declares it,
@@ -179,6 +305,10 @@ __global__ void __launch_bounds__(gemm_threads<Prob>(), 1) tc_gemm_kernel(const 
       mbar_init(&sh->tmem_full[a], 1);
       mbar_init(&sh->tmem_empty[a], 32 * Prob::kEpiWarps);
     }
+    for (int i = 0; i < kUnitRing; ++i) {
+      mbar_init(&sh->unit_full[i], 1);
+      mbar_init(&sh->unit_empty[i], 1 + Prob::kEpiWarps);  // the MMA thread and each epilogue warp
+    }
     mbar_init(&sh->mma_done, 1);
     sh->abort = 0;
     fence_mbar_init();
@@ -193,13 +323,19 @@ __global__ void __launch_bounds__(gemm_threads<Prob>(), 1) tc_gemm_kernel(const 
   tc_fence_after();
   const uint32_t tmem_base = sh->tmem_base;
   const int n_units = prob.num_units();
+  int* const sched = sched_of(prob);
+  const int first = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), stride = static_cast<int>(gridDim.x);
+  int uslot = 0;
+  uint32_t uphase = 0;
 
   if (warp == 0) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
-      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      int next = leader_start<false>(sh, sched, n_units, uslot, uphase, abort_flag, timeout);
+      for (int u = leader_next<false>(sh, sched, first, stride, n_units, next, uslot, uphase, abort_flag, timeout);
+           u >= 0; u = leader_next<false>(sh, sched, u, stride, n_units, next, uslot, uphase, abort_flag, timeout)) {
         const int nsub = prob.num_subtiles(u);
         for (int sb = 0; sb < nsub; ++sb) {
           const int nkb = prob.num_kb(u, sb);
@@ -238,7 +374,9 @@ __global__ void __launch_bounds__(gemm_threads<Prob>(), 1) tc_gemm_kernel(const 
       int stage = 0;
       uint32_t phase = 0;
       uint32_t it = 0;
-      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      for (int u = consumer_next(sh, sched, first, stride, n_units, uslot, uphase, false, false, abort_flag, timeout);
+           u >= 0;
+           u = consumer_next(sh, sched, u, stride, n_units, uslot, uphase, false, false, abort_flag, timeout)) {
         const int nsub = prob.num_subtiles(u);
         for (int sb = 0; sb < nsub; ++sb, ++it) {
           const uint32_t acc = it & 1u;
@@ -275,7 +413,8 @@ __global__ void __launch_bounds__(gemm_threads<Prob>(), 1) tc_gemm_kernel(const 
     const int col0 = ((warp - 2) >> 2) * (kBN * 4 / Prob::kEpiWarps);
     typename Prob::EpiState es{};
     uint32_t it = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    for (int u = consumer_next(sh, sched, first, stride, n_units, uslot, uphase, true, false, abort_flag, timeout);
+         u >= 0; u = consumer_next(sh, sched, u, stride, n_units, uslot, uphase, true, false, abort_flag, timeout)) {
       const int nsub = prob.num_subtiles(u);
       for (int sb = 0; sb < nsub; ++sb, ++it) {
         const uint32_t acc = it & 1u;
@@ -342,6 +481,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>()
       mbar_init(&sh->tmem_full[a], 1);
       mbar_init(&sh->tmem_empty[a], 2 * Prob::kEpiWarps);
     }
+    for (int i = 0; i < kUnitRing; ++i) {
+      mbar_init(&sh->unit_full[i], 1);
+      // rank 0's: its MMA thread, the odd CTA's producer and every epilogue warp of both
+      mbar_init(&sh->unit_empty[i], 2 + 2 * Prob::kEpiWarps);
+    }
     mbar_init(&sh->mma_done, 1);
     sh->abort = 0;
     fence_mbar_init();
@@ -358,6 +502,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>()
   tc_fence_after();
   const uint32_t tmem_base = sh->tmem_base;
   const int n_units = prob.num_units();
+  int* const sched = sched_of(prob);
+  const int first = pair - n_pairs;
+  int uslot = 0;
+  uint32_t uphase = 0;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -366,7 +514,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>()
       long long issued = 0;
       // rank 0's full barriers, as shared::cluster addresses (8 bytes apart)
       const uint32_t full_leader = mapa_shared(smem_u32(&sh->full[0]), 0);
-      for (int u = pair; u < n_units; u += n_pairs) {
+      // rank 0's producer leads the unit order; rank 1's follows its posts
+      int next = rank == 0 ? leader_start<true>(sh, sched, n_units, uslot, uphase, abort_flag, timeout) : -1;
+      auto advance = [&](int cur) {
+        return rank == 0
+                   ? leader_next<true>(sh, sched, cur, n_pairs, n_units, next, uslot, uphase, abort_flag, timeout)
+                   : consumer_next(sh, sched, cur, n_pairs, n_units, uslot, uphase, false, true, abort_flag, timeout);
+      };
+      for (int u = advance(first); u >= 0; u = advance(u)) {
         const int nsub = prob.num_subtiles(u);
         for (int sb = 0; sb < nsub; ++sb) {
           // K-blocks rounded up to whole stages: a missing last atom is read past
@@ -414,7 +569,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>()
       int stage = 0;
       uint32_t phase = 0;
       uint32_t it = 0;
-      for (int u = pair; u < n_units; u += n_pairs) {
+      for (int u = consumer_next(sh, sched, first, n_pairs, n_units, uslot, uphase, false, false, abort_flag, timeout);
+           u >= 0;
+           u = consumer_next(sh, sched, u, n_pairs, n_units, uslot, uphase, false, false, abort_flag, timeout)) {
         const int nsub = prob.num_subtiles(u);
         for (int sb = 0; sb < nsub; ++sb, ++it) {
           const uint32_t acc = it & 1u;
@@ -450,7 +607,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>()
     const int col0 = ((warp - 2) >> 2) * (kBN * 4 / Prob::kEpiWarps);
     typename Prob::EpiState es{};
     uint32_t it = 0;
-    for (int u = pair; u < n_units; u += n_pairs) {
+    for (int u = consumer_next(sh, sched, first, n_pairs, n_units, uslot, uphase, true, rank != 0, abort_flag, timeout);
+         u >= 0; u = consumer_next(sh, sched, u, n_pairs, n_units, uslot, uphase, true, rank != 0, abort_flag, timeout)) {
       const int nsub = prob.num_subtiles(u);
       for (int sb = 0; sb < nsub; ++sb, ++it) {
         const uint32_t acc = it & 1u;
@@ -495,6 +653,9 @@ rf_status launch_gemm(const Prob& pr, int64_t max_units, int sms, cudaStream_t s
   rf_status st = set_smem_attr(fn, smem, &attr_mask);
   if (st != RF_OK) return st;
   if (max_units <= 0) max_units = 1;
+  if (int* sc = sched_of(pr); sc != nullptr) {
+    if ((st = cuda_check(cudaMemsetAsync(sc, 0, sizeof(int), s), "unit counter clear")) != RF_OK) return st;
+  }
   if constexpr (kPair) {
     const int cap = max_active_pairs(fn, smem, gemm_threads<Prob>(), sms, pair_cap);
     const int pairs = static_cast<int>(std::min<int64_t>(max_units, cap));

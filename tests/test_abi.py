@@ -62,11 +62,11 @@ def _fill_desc(**kw):
 
 def test_fill_workspace_size_follows_the_layout():
     desc = _fill_desc(flags=rf.RF_WEIGHTS_PREFOLDED)
-    # fill_idx, n_fill, Xf [M x d], x̂ [P x M x d], ss partials [P x d/256 x M], with M = the prefix
-    # rows padded to a whole 256-row unit (RoPE angles are computed in the kernel: no table)
+    # fill_idx, n_fill, the GEMMs' unit counter, Xf [M x d], x̂ [P x M x d], ss partials [P x d/256 x M],
+    # with M = the prefix rows padded to a whole 256-row unit (RoPE angles are computed in the kernel: no table)
     r = lambda x: (x + 255) // 256 * 256
     n_prefix, M, P, d, KV = 9, 256, 4, 256, 128
-    want = r(n_prefix * 4) + r(4) + r(M * d * 2) + r(P * M * d * 2) + r(P * (d // 256) * M * 4)
+    want = r(n_prefix * 4) + r(4) + r(4) + r(M * d * 2) + r(P * M * d * 2) + r(P * (d // 256) * M * 4)
     assert rf.rf_fill_workspace_bytes(desc) == want
     # without RF_WEIGHTS_PREFOLDED the call folds the gain into two [P][KV][d] bf16 arrays of its own
     assert rf.rf_fill_workspace_bytes(_fill_desc()) == want + 2 * r(P * KV * d * 2)
