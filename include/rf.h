@@ -344,14 +344,21 @@ typedef struct rf_calib_stats {
   double* syy;
 } rf_calib_stats;
 
-/* Supported: d_in % 128 == 0, d_out % 256 == 0 (or n_maps == 0), n_rows % 8 == 0. */
+/* Supported: d_in % 128 == 0, d_out % 256 == 0 (or n_maps == 0), n_rows % 8 == 0.
+ * The workspace is optional (see rf_calib_accumulate); this is its size (256). */
 size_t rf_calib_workspace_bytes(const rf_calib_desc* desc, int64_t n_rows);
 
 /* Adds one batch of rows: G += XᵀX, C_p += XᵀY_p, sx += Σx, sy_p += Σy_p, n += n_rows
  * (and syy_p += Σy_p² when stats->syy is set).
  *   X [n_rows][ld_x] bf16; Y_p at Y + p*y_map_stride, [n_rows][ld_y] bf16.
  * Products are exact in fp32, summed in fp32 over chunks of rows on the tensor
- * cores and added to the fp64 totals. */
+ * cores and added to the fp64 totals.
+ *   workspace  NULL, or rf_calib_workspace_bytes(...) bytes, 256-byte aligned: with
+ *              it the GEMM takes its output tiles in dynamic order (a device
+ *              counter), which keeps the CTAs that share operand rows together in
+ *              L2; without it, in a fixed round-robin order. The sums are the same
+ *              bit for bit either way (each tile is added to the totals once per
+ *              16 chunks of rows, in stream order). */
 rf_status rf_calib_accumulate(const rf_calib_desc* desc,
                               const rf_bf16* X, int64_t ld_x,
                               const rf_bf16* Y, int64_t ld_y, int64_t y_map_stride,

@@ -41,6 +41,7 @@ struct GramProb {
   int d_in, d_out, P, n_rows, n_chunks;
   int g_mt, g_nt, c_nt, g_units;
   int c_group;  // M-tiles per group of the XᵀY units (their X rows stay in L2 together)
+  int* sched;   // unit counter (dynamic unit order) when the caller gave a workspace, else nullptr
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = true;
@@ -246,8 +247,8 @@ constexpr int64_t kCalibSlabRows = 16 * kCalibChunk;
 
 template <bool kPair>
 rf_status calib_gemm(const rf_calib_desc* desc, const rf_bf16* X, int64_t ld_x, const rf_bf16* Y, int64_t ld_y,
-                     int64_t y_map_stride, int64_t n_rows, const rf_calib_stats* st, int32_t* dev_status, int sms,
-                     cudaStream_t cs) {
+                     int64_t y_map_stride, int64_t n_rows, const rf_calib_stats* st, int32_t* dev_status, int* sched,
+                     int sms, cudaStream_t cs) {
   using Cfg = GemmCfg<kPair>;
   const int64_t d_in = desc->d_in, d_out = desc->d_out, P = desc->n_maps;
   rf_status s;
@@ -280,6 +281,7 @@ rf_status calib_gemm(const rf_calib_desc* desc, const rf_bf16* X, int64_t ld_x, 
     const int64_t panel = static_cast<int64_t>(Cfg::kUnitM) * rows * 2;
     pr.c_group = static_cast<int>(
         std::max<int64_t>(1, std::min<int64_t>(pr.g_mt, (int64_t(48) << 20) / std::max<int64_t>(panel, 1))));
+    pr.sched = sched;
     pr.dev_status = dev_status;
     pr.timeout_ns = wait_timeout_ns();
     if ((s = launch_gemm(pr, pr.g_units + P * pr.g_mt * pr.c_nt, sms, cs, "calibration GEMM launch")) != RF_OK)
@@ -307,15 +309,18 @@ static rf_status check_calib_desc(const rf_calib_desc* d) {
   return RF_OK;
 }
 
+// The optional workspace holds the GEMM's unit counter (dynamic unit order).
+constexpr size_t kCalibWorkspace = 256;
+
 extern "C" size_t rf_calib_workspace_bytes(const rf_calib_desc* desc, int64_t) {
   if (check_calib_desc(desc) != RF_OK) return 0;
-  return 0;  // the accumulation needs no scratch memory
+  return kCalibWorkspace;
 }
 
 extern "C" rf_status rf_calib_accumulate(const rf_calib_desc* desc, const rf_bf16* X, int64_t ld_x, const rf_bf16* Y,
                                          int64_t ld_y, int64_t y_map_stride, int64_t n_rows,
-                                         const rf_calib_stats* st, int32_t* dev_status, void*, size_t,
-                                         rf_stream_t stream) {
+                                         const rf_calib_stats* st, int32_t* dev_status, void* workspace,
+                                         size_t workspace_bytes, rf_stream_t stream) {
   clear_error();
   rf_status s = check_calib_desc(desc);
   if (s != RF_OK) return s;
@@ -331,6 +336,11 @@ extern "C" rf_status rf_calib_accumulate(const rf_calib_desc* desc, const rf_bf1
   if (P > 0 && (ld_y < d_out || ld_y % 8 != 0 || y_map_stride % 8 != 0 || (P > 1 && y_map_stride < ld_y * n_rows)))
     return fail(RF_ERR_ALIGN, "ld_y must be >= d_out and a multiple of 8; y_map_stride a multiple of 8 "
                               "covering n_rows rows");
+  if (workspace != nullptr &&
+      (workspace_bytes < kCalibWorkspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return fail(RF_ERR_WORKSPACE, "workspace, when given, needs %zu bytes, 256-byte aligned (got %zu)",
+                kCalibWorkspace, workspace_bytes);
+  int* const sched = static_cast<int*>(workspace);
   int sms = 0;
   if ((s = current_device(&sms)) != RF_OK) return s;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -350,6 +360,6 @@ extern "C" rf_status rf_calib_accumulate(const rf_calib_desc* desc, const rf_bf1
   if ((s = cuda_check(cudaGetLastError(), "k_colsum launch")) != RF_OK) return s;
 
   if (use_pair(desc->flags, true))
-    return calib_gemm<true>(desc, X, ld_x, Y, ld_y, y_map_stride, n_rows, st, dev_status, sms, cs);
-  return calib_gemm<false>(desc, X, ld_x, Y, ld_y, y_map_stride, n_rows, st, dev_status, sms, cs);
+    return calib_gemm<true>(desc, X, ld_x, Y, ld_y, y_map_stride, n_rows, st, dev_status, sched, sms, cs);
+  return calib_gemm<false>(desc, X, ld_x, Y, ld_y, y_map_stride, n_rows, st, dev_status, sched, sms, cs);
 }

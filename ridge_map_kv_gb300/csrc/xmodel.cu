@@ -106,6 +106,7 @@ struct XMProb {
   const float* bv;
   RopeFreqs rope_t;      // target RoPE frequencies (θ_tgt, hd)
   long long pos_offset;  // position of row 0
+  int* sched;            // unit counter (dynamic unit order)
   __nv_bfloat16* k_tgt;  // [L_tgt][N][KV]
   __nv_bfloat16* v_tgt;
   int N, KV, hd, k, L_tgt, m_tiles, n_half;
@@ -200,6 +201,7 @@ struct XLayout {
   __nv_bfloat16* ku;
   int32_t* src;
   int32_t* ok;
+  int* sched;  // the mapping GEMM's unit counter
   size_t bytes;
 };
 
@@ -210,6 +212,7 @@ static XLayout xmodel_layout(const rf_xmodel_desc* d, void* ws) {
   l.ku = c.take<__nv_bfloat16>(d->L_src * d->N * KV);
   l.src = c.take<int32_t>(d->L_tgt * d->k);
   l.ok = c.take<int32_t>(1);
+  l.sched = c.take<int>(1);
   l.bytes = c.bytes();
   return l;
 }
@@ -248,6 +251,7 @@ rf_status xmodel_gemm(const rf_xmodel_desc* desc, const XLayout& lay, const rf_b
   pr.bk = bk;
   pr.bv = bv;
   pr.rope_t = rope_freqs(desc->theta_tgt, static_cast<int>(desc->head_dim));
+  pr.sched = lay.sched;
   pr.pos_offset = static_cast<long long>(desc->pos_offset);
   pr.k_tgt = reinterpret_cast<__nv_bfloat16*>(k_tgt);
   pr.v_tgt = reinterpret_cast<__nv_bfloat16*>(v_tgt);

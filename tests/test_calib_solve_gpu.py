@@ -36,14 +36,18 @@ def _struct(st):
     return rf.calib_stats_struct(st["G"], st["C"], st["sx"], st["sy"], st["n"])
 
 
-def _accumulate(X, Y, st, row_splits, flags=0):
+def _accumulate(X, Y, st, row_splits, flags=0, workspace=True):
+    """Adds the rows of X, Y to ``st`` in the batches ``row_splits`` cuts; with
+    ``workspace`` the GEMM takes its tiles in dynamic order (a device counter)."""
     n, d_in = X.shape
     P, _, d_out = Y.shape
     desc = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P, flags=flags)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(rf.rf_calib_workspace_bytes(desc, n), dtype=torch.uint8, device=DEV) if workspace else None
     bounds = [0] + list(row_splits) + [n]
     for a, b in zip(bounds[:-1], bounds[1:]):
-        rf.rf_calib_accumulate(desc, X[a:], d_in, Y[:, a:], d_out, n * d_out, b - a, _struct(st), status)
+        rf.rf_calib_accumulate(desc, X[a:], d_in, Y[:, a:], d_out, n * d_out, b - a, _struct(st), status,
+                               ws, 0 if ws is None else ws.numel())
     torch.cuda.synchronize()
     assert int(status.item()) == 0
 
@@ -95,7 +99,8 @@ def test_calib_full_width_sampled(d_in, d_out, P, n, flags):
     st = _zeros_stats(d_in, d_out, P)
     desc = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P, flags=flags)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    rf.rf_calib_accumulate(desc, X, d_in, Y if P else None, d_out, n * d_out, n, _struct(st), status)
+    ws = torch.empty(rf.rf_calib_workspace_bytes(desc, n), dtype=torch.uint8, device=DEV)
+    rf.rf_calib_accumulate(desc, X, d_in, Y if P else None, d_out, n * d_out, n, _struct(st), status, ws, ws.numel())
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     rng = np.random.default_rng(5)
@@ -109,6 +114,21 @@ def test_calib_full_width_sampled(d_in, d_out, P, n, flags):
         ref = O.calib_stats(Xs, np.zeros((1, n, 1)))
         ref["C"] = np.zeros((0, len(cx), len(cy)))
     _check_stats(st, ref, (Ys ** 2).sum(axis=1) if P else None, cols_x=cx, cols_y=cy)
+
+
+@pytest.mark.parametrize("flags", [rf.RF_FLAG_SINGLE_CTA, rf.RF_FLAG_CTA_PAIR], ids=["single-cta", "cta-pair"])
+def test_calib_dynamic_and_round_robin_tile_orders_give_the_same_sums(flags):
+    """With a workspace the calibration GEMM takes its tiles from a device counter,
+    without one in a fixed round-robin order. Each tile is added to the fp64 totals
+    once per 16 chunks of rows, in stream order, so the two orders give the same sums
+    bit for bit: here over three row slabs with a ragged last one, in two batches."""
+    cal = synth.calib_inputs(512, 256, 3, 16384 * 2 + 1288, index=96)
+    X, Y = cal["X"].to(DEV), cal["Y"].to(DEV)
+    a, b = _zeros_stats(512, 256, 3), _zeros_stats(512, 256, 3)
+    _accumulate(X, Y, a, [20000], flags, workspace=True)
+    _accumulate(X, Y, b, [20000], flags, workspace=False)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
 
 
 def test_calib_zero_rows_leaves_the_sums_unchanged():
