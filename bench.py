@@ -772,7 +772,11 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
         # weights s + t <= 7) plus the correction R_p H^-1 (six plane products)
         rm = sol["refine_1_stages_ms"].get("solve_refine")
         if rm:
-            sol["refine_bf16_tflops"] = (21.0 + 6.0) * prod / (rm / 1e3) / 1e12
+            # one sweep = the residual A_p H plus the correction R_p H^-1: 2 products of the
+            # solve's size, fp64-accurate and fp32-accurate (how many bf16 digit and plane
+            # products that takes depends on the conditioning the library estimates)
+            sol["refine_sweep_ms"] = rm
+            sol["refine_product_equiv_tflops"] = 2.0 * prod / (rm / 1e3) / 1e12
         out["a6_solve"] = {"workload": f"8b-shaped ridge solve, d={d}, {P} maps, lambda={c.lam}", **sol}
         del st, cs, A, b, Ab, ws
         torch.cuda.empty_cache()
@@ -989,8 +993,9 @@ def _solve_row(dev, d_in, d_out, P, n, lam, index, flags, peak_tflops, label):
         row["factor_inverse_fp32_tflops"] = (5.0 / 3.0) * d_in ** 3 / (fm / 1e3) / 1e12
     rm = row["refine_1_stages_ms"].get("solve_refine")
     if rm:
-        # the residual A_p H as 21 digit-pair products plus the correction R_p H^-1 (six plane products)
-        row["refine_bf16_tflops"] = (21.0 + 6.0) * prod / (rm / 1e3) / 1e12
+        # one sweep = the residual A_p H plus the correction R_p H^-1 (see a6_solve)
+        row["refine_sweep_ms"] = rm
+        row["refine_product_equiv_tflops"] = 2.0 * prod / (rm / 1e3) / 1e12
     row["solve_fp32_equiv_tflops_unrefined"] = (prod + (5.0 / 3.0) * d_in ** 3) / (row["refine_0_ms"] / 1e3) / 1e12
     del st, cs, A, b, Ab, ws
     torch.cuda.empty_cache()

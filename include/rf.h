@@ -379,9 +379,13 @@ size_t rf_solve_workspace_bytes(const rf_calib_desc* desc);
  *   Gc = G − n μ_x μ_xᵀ, Cc_p = C_p − n μ_x μ_pᵀ, α = λ tr(Gc)/d_in (TRACE) or λ,
  *   Gc + αI = L Lᵀ (fp32 Cholesky), A_p = Cc_pᵀ (Gc + αI)^-1 (fp32), then
  *   `refine_iters` sweeps of A_p += (Cc_pᵀ − A_p (Gc + αI)) (Gc + αI)^-1 with the
- *   residual fp64-accurate (exact integer digit products on the tensor cores,
- *   within about 2^-40 of Σ|A||Gc + αI|); b_p = μ_p − A_p μ_x (compensated, to
- *   about 2^-44 of Σ|A||μ|, rounded to fp32).
+ *   residual computed beyond fp32 accuracy (exact integer digit products on the
+ *   tensor cores); b_p = μ_p − A_p μ_x (compensated, to about 2^-44 of Σ|A||μ|,
+ *   rounded to fp32). How accurate the residual and the correction are is chosen on
+ *   the device from κ(Gc + αI), estimated once by power iteration: accurate enough
+ *   for a sweep to bring A to fp32 accuracy, the residual to about 2^-(25 + log2 4κ)
+ *   of Σ|A||Gc + αI| (2^-34 for κ below about 2^7, else about 2^-41, its limit), the
+ *   correction to fp32 when 4κ > 2^10, else to about 2^-16 of its terms.
  *   A [n_maps][d_out][d_in] fp32, b [n_maps][d_out] fp32,
  *   A_bf16 (may be NULL) bf16 copy of A for rf_fill_kv, alpha_out (device, may be NULL).
  * A non-positive pivot sets RF_ERR_NOT_SPD in *dev_status. */

@@ -463,6 +463,20 @@ __global__ void k_bias(const float* __restrict__ A, const float2* __restrict__ m
 }
 
 // bf16 copy of A, four elements a thread (total % 4 == 0, 16-byte aligned).
+// a[i] += b[i], 16 bytes per step.
+__global__ void __launch_bounds__(256) k_add_f32(float4* __restrict__ a, const float4* __restrict__ b, long long n4) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float4 x = a[i];
+    const float4 y = b[i];
+    x.x += y.x;
+    x.y += y.y;
+    x.z += y.z;
+    x.w += y.w;
+    a[i] = x;
+  }
+}
+
 __global__ void k_to_bf16(const float* __restrict__ A, long long total, __nv_bfloat16* __restrict__ out) {
   for (long long e = 4 * (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x); e < total;
        e += 4 * static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -538,6 +552,7 @@ struct Split3Prob {
   CUtensorMap tmA;
   CUtensorMap tmB;
   float* out;  // [P][M][N]
+  const int* n_terms;  // device: product terms to sum, the first of the six in order (nullptr: all six)
   float alpha, beta;
   int P, M, N, K, m_tiles, n_tiles, n_chunks;
   int32_t* dev_status;
@@ -557,7 +572,7 @@ struct Split3Prob {
     tma_prefetch_desc(&tmB);
   }
   __device__ int num_units() const { return P * m_tiles * n_tiles; }
-  __device__ int num_subtiles(int) const { return 6 * n_chunks; }
+  __device__ int num_subtiles(int) const { return (n_terms != nullptr ? *n_terms : 6) * n_chunks; }
   __device__ int num_kb(int, int sb) const {
     const int c = sb % n_chunks;
     return (min(kSplitChunk, K - c * kSplitChunk) + kBK - 1) / kBK;
@@ -620,7 +635,8 @@ struct Split3Prob {
 // Bᵀ), through the split planes in `planes_a` (3·P·M·K) and `planes_b` (3·N·K).
 // A_p is fp32 [P][M][K], split here, or null when planes_a already hold its planes.
 static rf_status split_gemm(SolveCtx& c, const float* a, const float* Bsym, int P, int M, int N, int K, float alpha,
-                            float beta, float* out, __nv_bfloat16* planes_a, __nv_bfloat16* planes_b) {
+                            float beta, float* out, __nv_bfloat16* planes_a, __nv_bfloat16* planes_b,
+                            const int* n_terms = nullptr) {
   rf_status st;
   const size_t pa = static_cast<size_t>(P) * M * K, pb = static_cast<size_t>(N) * K;
   const unsigned eb = static_cast<unsigned>(8 * c.sms);
@@ -631,6 +647,7 @@ static rf_status split_gemm(SolveCtx& c, const float* a, const float* Bsym, int 
   if ((st = make_tmap_bf16_2d(&pr.tmA, planes_a, K, 3LL * P * M, K, kBK, kBM)) != RF_OK) return st;
   if ((st = make_tmap_bf16_2d(&pr.tmB, planes_b, K, 3LL * N, K, kBK, GemmCfg<true>::kBRows)) != RF_OK) return st;
   pr.out = out;
+  pr.n_terms = n_terms;
   pr.alpha = alpha;
   pr.beta = beta;
   pr.P = P;
@@ -668,7 +685,12 @@ constexpr int kOzMaps = 4;  // maps per residual launch (keeps the last wave of 
 
 // Digits of each row of an fp64 matrix [rows][cols]: digit d of row r at
 // planes[(d * plane_rows + r) * cols ...] in bf16 (plane_rows >= rows), and the row
-// scale σ (a power of two, 0 for a zero row). One warp per row.
+// scale σ (a power of two, 0 for a zero row). One warp per row. The digits come
+// from integer arithmetic on v = x/σ as a 62-bit fixed-point integer q = v·2^62
+// (exact: |v| <= 1/2, and a double has 53 significant bits): digit s is q's
+// bits from 62 − 7s, rounded half up, and taking it out leaves the remainder
+// within half a unit of that position, so |d_s| <= 64 as in the fp32 split. (In
+// fp64 arithmetic the same split took about 1 ms at d = 4,096: GB300's fp64 rate.)
 __global__ void __launch_bounds__(256) k_oz_digits_f64(const double* __restrict__ X, int rows, int plane_rows, int cols,
                                                        __nv_bfloat16* __restrict__ planes, double* __restrict__ scale) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
@@ -683,12 +705,12 @@ __global__ void __launch_bounds__(256) k_oz_digits_f64(const double* __restrict_
   if (lane == 0) scale[warp] = mx > 0.0 ? ldexp(1.0, e) : 0.0;
   const size_t plane = static_cast<size_t>(plane_rows) * cols;
   for (int k = lane; k < cols; k += 32) {
-    double v = mx > 0.0 ? ldexp(x[k], -e) : 0.0;  // exact, |v| <= 1/2
+    long long q = mx > 0.0 ? __double2ll_rn(ldexp(x[k], 62 - e)) : 0;  // exact, |q| <= 2^61
 #pragma unroll
     for (int d = 0; d < kOzDigits; ++d) {
-      const double t = v * static_cast<double>(1 << kOzBits);  // |t| <= 64, |t − rint(t)| <= 1/2
-      const double r = rint(t);
-      v = t - r;  // exact
+      const int sh = 62 - kOzBits * (d + 1);
+      const long long r = (q + (1ll << (sh - 1))) >> sh;  // |r| <= 64
+      q -= r << sh;                                       // |q| <= 2^(sh-1)
       planes[d * plane + static_cast<size_t>(warp) * cols + k] = __float2bfloat16_rn(static_cast<float>(r));
     }
   }
@@ -756,8 +778,9 @@ __device__ __forceinline__ double scale_pow2(double v, int e) {
   return v * pow2_double(e / 2) * pow2_double(e - e / 2);
 }
 
-// R_p[o][i] = C_p[i][o] − n μ_x[i] μ_p[o] − σ_o τ_i 2^(−49) T[o][i] for the maps of a
-// group, with T = Σ_m J_m 2^(7(7−m)) built exactly in int64 from the weights' sums
+// R_p[o][i] = C_p[i][o] − n μ_x[i] μ_p[o] − σ_o τ_i 2^(−7M) T[o][i] for the maps of a
+// group, with M = *m_max (the largest digit weight computed, 7 at most) and
+// T = Σ_{m <= M} J_m 2^(7(M−m)) built exactly in int64 from the weights' sums
 // (|J_m| <= (m−1) 2^12 d_in, so |T| < 2^47.1 d_in <= 2^62.1 for d_in <= 32768) and
 // rounded once to fp64. Through 32 x 32 shared tiles (C is [i][o], R [o][i]).
 // Grid (d_out/32, d_in/32, maps), 32 x 8 threads.
@@ -765,10 +788,11 @@ __global__ void __launch_bounds__(256) k_oz_combine(const double* __restrict__ C
                                                     const double* __restrict__ mu_y, const double* __restrict__ n,
                                                     const double* __restrict__ sA, const double* __restrict__ sH,
                                                     const int32_t* __restrict__ J, size_t plane, int d_in, int d_out,
-                                                    float* __restrict__ R32) {
+                                                    const int* __restrict__ m_max, float* __restrict__ R32) {
   __shared__ double t[32][33];
   const int o0 = blockIdx.x * 32, i0 = blockIdx.y * 32, p = blockIdx.z;
   const double nn = *n;
+  const int mm = *m_max;
   const double* Cp = C + static_cast<size_t>(p) * d_in * d_out;
   const double* my = mu_y + static_cast<size_t>(p) * d_out;
   for (int r = threadIdx.y; r < 32; r += 8) {
@@ -780,10 +804,8 @@ __global__ void __launch_bounds__(256) k_oz_combine(const double* __restrict__ C
     const int o = o0 + r, i = i0 + threadIdx.x;
     const size_t e = (static_cast<size_t>(p) * d_out + o) * d_in + i;
     long long T = 0;
-#pragma unroll
-    for (int w = 0; w < kOzDigits; ++w) T = T * (1 << kOzBits) + J[w * plane + e];  // weights m = 2, 3, ...
-    const int k = pow2_exponent(sA[static_cast<size_t>(p) * d_out + o]) + pow2_exponent(sH[i]) -
-                  kOzBits * (kOzDigits + 1);
+    for (int w = 0; w + 2 <= mm; ++w) T = T * (1 << kOzBits) + J[w * plane + e];  // weights m = 2, 3, ..., M
+    const int k = pow2_exponent(sA[static_cast<size_t>(p) * d_out + o]) + pow2_exponent(sH[i]) - kOzBits * mm;
     R32[e] = static_cast<float>(t[threadIdx.x][r] - scale_pow2(static_cast<double>(T), k));
   }
 }
@@ -793,6 +815,7 @@ struct OzakiProb {
   CUtensorMap tmA;  // digits of the maps' rows: [kOzDigits * maps * d_out][d_in]
   CUtensorMap tmB;  // digits of H rows:        [kOzDigits * d_in][d_in]
   int32_t* J;        // [maps][d_out][d_in] this weight's exact sums J_m
+  const int* m_max;  // device: the largest weight the refinement needs (weights above it run no unit)
   int maps, plane_maps, d_out, d_in, m_tiles, n_tiles, n_chunks;  // maps in this launch; maps per digit plane
   int m;  // the digit weight s + t of this launch (pairs s = 1 .. m−1)
   int32_t* dev_status;
@@ -811,7 +834,7 @@ struct OzakiProb {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  __device__ int num_units() const { return maps * m_tiles * n_tiles; }
+  __device__ int num_units() const { return m <= *m_max ? maps * m_tiles * n_tiles : 0; }
   __device__ int num_subtiles(int) const { return (m - 1) * n_chunks; }
   __device__ void decode(int u, int& p, int& mt, int& nt) const {
     nt = u % n_tiles;
@@ -864,6 +887,101 @@ struct OzakiProb {
   }
 };
 
+// --------------------------------------------------------------------------
+// How much refinement arithmetic the conditioning calls for. κ(H) is estimated as
+// λmax(H)·λmax(H^-1), each by power iteration (H read as fp32 from its fp64 copy,
+// H^-1 in fp32); the Rayleigh quotients approach from below, so the estimate is
+// taken 4 times over. A sweep's correction R H^-1 moves A by |R||H^-1|, so to
+// bring A to fp32 accuracy (2^-24) the residual must be good to about
+// 2^-(25 + log2 κ) of Σ|A||H|, and the correction product's own relative error
+// times κ must stay well below 1. With 7-bit digits and the pairs s + t <= n + 1
+// kept, n digits give about (n+1)·2^(-7n-2): 2^-27.7 at n = 4, 2^-34.4 at n = 5,
+// 2^-41.2 at n = 6 (all six, the most there are); the first three split terms of
+// the correction give about 2^-16, all six about 2^-24.
+// --------------------------------------------------------------------------
+constexpr int kPowerSteps = 12;
+
+// x_m = a fixed ±1/sqrt(d) vector (signs from a multiplicative hash) for m = 0, 1.
+__global__ void k_pow_init(float* __restrict__ x, int d) {
+  const float v = rsqrtf(static_cast<float>(d));
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 2 * d; i += gridDim.x * blockDim.x)
+    x[i] = ((static_cast<unsigned>(i % d) * 2654435761u) >> 31) ? -v : v;
+}
+
+// y_0 = H x_0 (H fp64, summed in fp32), y_1 = H^-1 x_1: one warp per row, grid
+// (ceil(d/8), 2) of 256 threads.
+__global__ void __launch_bounds__(256) k_pow_matvec(const double* __restrict__ H, const float* __restrict__ Hinv, int d,
+                                                    const float* __restrict__ x, float* __restrict__ y) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31, m = blockIdx.y;
+  if (r >= d) return;
+  const float* xv = x + static_cast<size_t>(m) * d;
+  float acc = 0.f;
+  if (m == 0) {
+    const double* row = H + static_cast<size_t>(r) * d;
+    for (int c = lane; c < d; c += 32) acc = fmaf(static_cast<float>(row[c]), xv[c], acc);
+  } else {
+    const float* row = Hinv + static_cast<size_t>(r) * d;
+    for (int c = lane; c < d; c += 32) acc = fmaf(row[c], xv[c], acc);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) y[static_cast<size_t>(m) * d + r] = acc;
+}
+
+// est[m] = x_mᵀ y_m (x_m has unit norm: the Rayleigh quotient), then x_m = y_m / ‖y_m‖.
+// One CTA of 1024 threads per matrix.
+__global__ void __launch_bounds__(1024) k_pow_norm(float* __restrict__ x, const float* __restrict__ y, int d,
+                                                   float* __restrict__ est) {
+  __shared__ double part[2][32];
+  const int m = blockIdx.x, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  float* xv = x + static_cast<size_t>(m) * d;
+  const float* yv = y + static_cast<size_t>(m) * d;
+  double xy = 0.0, yy = 0.0;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    xy += static_cast<double>(xv[i]) * yv[i];
+    yy += static_cast<double>(yv[i]) * yv[i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    xy += __shfl_xor_sync(0xffffffffu, xy, o);
+    yy += __shfl_xor_sync(0xffffffffu, yy, o);
+  }
+  if (lane == 0) {
+    part[0][w] = xy;
+    part[1][w] = yy;
+  }
+  __syncthreads();
+  if (w == 0) {
+    xy = part[0][lane];
+    yy = part[1][lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      xy += __shfl_xor_sync(0xffffffffu, xy, o);
+      yy += __shfl_xor_sync(0xffffffffu, yy, o);
+    }
+    if (lane == 0) {
+      part[0][0] = xy;
+      part[1][0] = yy;
+    }
+  }
+  __syncthreads();
+  const double inv = part[1][0] > 0.0 ? rsqrt(part[1][0]) : 0.0;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) xv[i] = static_cast<float>(yv[i] * inv);
+  if (threadIdx.x == 0) est[m] = static_cast<float>(part[0][0]);
+}
+
+// plan[0] = the largest digit weight the residual keeps (n + 1), plan[1] = the
+// correction's split terms (see above). A non-finite estimate keeps everything.
+__global__ void k_refine_plan(const float* __restrict__ est, int* __restrict__ plan) {
+  const double kappa = 4.0 * static_cast<double>(est[0]) * static_cast<double>(est[1]);
+  const double bits = 25.0 + log2(fmax(kappa, 1.0));
+  int n = kOzDigits;
+  if (bits <= 27.5) n = 4;
+  else if (bits <= 34.0) n = 5;
+  plan[0] = n + 1;
+  plan[1] = kappa <= 1024.0 ? 3 : 6;
+}
+
 static int split_point(int n) { return std::max(kSolveBlock, (n / 2) / kSolveBlock * kSolveBlock); }
 
 struct SolveLayout {
@@ -885,6 +1003,9 @@ struct SolveLayout {
   __nv_bfloat16* ozA;       // [kOzDigits][kOzMaps * d_out][d_in] digits of a group of maps' rows
   double* sA;               // [kOzMaps * d_out]
   int32_t* J;               // [kOzDigits][kOzMaps][d_out][d_in] their sums J_m, one plane per weight
+  float* pvec;              // [2][2][d_in] power-iteration vectors (x, y; H and H^-1)
+  float* est;               // [2] their Rayleigh quotients
+  int* plan;                // [2] refinement plan (largest digit weight, correction terms)
   size_t bytes;
 };
 
@@ -911,6 +1032,9 @@ static SolveLayout solve_layout(const rf_calib_desc* d, void* ws) {
   l.ozA = c.take<__nv_bfloat16>(kOzDigits * om * dout * di);
   l.sA = c.take<double>(om * dout);
   l.J = c.take<int32_t>(kOzDigits * om * dout * di);
+  l.pvec = c.take<float>(4 * di);
+  l.est = c.take<float>(2);
+  l.plan = c.take<int>(2);
   l.bytes = c.bytes();
   return l;
 }
@@ -919,6 +1043,7 @@ static SolveLayout solve_layout(const rf_calib_desc* d, void* ws) {
 template <bool kPair>
 static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* C, const float* A, int P, int di,
                              int dout, float* R32) {
+  // the weights above lay.plan[0] run no unit and the combine leaves them out
   using Cfg = GemmCfg<kPair>;
   rf_status st;
   const unsigned hb = static_cast<unsigned>((static_cast<long long>(di) * 32 + 255) / 256);
@@ -936,6 +1061,7 @@ static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* 
   pr.m_tiles = dout / Cfg::kUnitM;
   pr.n_tiles = di / kBN;
   pr.n_chunks = (di + kOzChunk - 1) / kOzChunk;
+  pr.m_max = lay.plan;
   pr.dev_status = c.dev_status;
   pr.timeout_ns = wait_timeout_ns();
   for (int p0 = 0; p0 < P; p0 += om) {
@@ -960,7 +1086,7 @@ static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* 
     }
     k_oz_combine<<<dim3(dout / 32, di / 32, g), dim3(32, 8), 0, c.s>>>(
         C + off, lay.mu_x, lay.mu_y + static_cast<size_t>(p0) * dout, lay.n, lay.sA, lay.sH, lay.J, plane, di, dout,
-        R32 + off);
+        lay.plan, R32 + off);
     if ((st = cuda_check(cudaGetLastError(), "residual combine launch")) != RF_OK) return st;
   }
   return RF_OK;
@@ -1093,14 +1219,31 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
         RF_OK)
       return s;
   }
+  if (refine_iters > 0) {
+    // the refinement's precision from the conditioning (see k_refine_plan), once
+    ProfScope pr(c.s, RF_STAGE_SOLVE_REFINE);
+    k_pow_init<<<(2 * di + 255) / 256, 256, 0, c.s>>>(lay.pvec, di);
+    for (int k = 0; k < kPowerSteps; ++k) {
+      k_pow_matvec<<<dim3((di + 7) / 8, 2), 256, 0, c.s>>>(lay.H64, lay.Hinv, di, lay.pvec, lay.pvec + 2 * di);
+      k_pow_norm<<<2, 1024, 0, c.s>>>(lay.pvec, lay.pvec + 2 * di, di, lay.est);
+    }
+    k_refine_plan<<<1, 1, 0, c.s>>>(lay.est, lay.plan);
+    if ((s = cuda_check(cudaGetLastError(), "refinement plan launches")) != RF_OK) return s;
+  }
   for (int it = 0; it < refine_iters; ++it) {
     ProfScope pr(c.s, RF_STAGE_SOLVE_REFINE);
     s = use_pair(desc->flags, true) ? oz_residual<true>(c, lay, st->C, A, P, di, dout, lay.work)
                                     : oz_residual<false>(c, lay, st->C, A, P, di, dout, lay.work);
     if (s != RF_OK) return s;
-    if ((s = split_gemm(c, lay.work, lay.Hinv, P, dout, di, di, 1.f, 1.f, A, lay.planes_a, lay.planes_b)) !=
-        RF_OK)
+    // ΔA = R H^-1 into the residual's own buffer (split into planes_a first, so free),
+    // then A += ΔA in one coalesced pass: an in-epilogue read-modify-write of A (one
+    // thread per row) held the accumulators long enough to stall the MMAs.
+    if ((s = split_gemm(c, lay.work, lay.Hinv, P, dout, di, di, 1.f, 0.f, lay.work, lay.planes_a, lay.planes_b,
+                        lay.plan + 1)) != RF_OK)
       return s;
+    const long long n4 = static_cast<long long>(P) * dout * di / 4;
+    k_add_f32<<<eb, 256, 0, c.s>>>(reinterpret_cast<float4*>(A), reinterpret_cast<const float4*>(lay.work), n4);
+    if ((s = cuda_check(cudaGetLastError(), "correction add launch")) != RF_OK) return s;
   }
   const long long rows = static_cast<long long>(P) * dout;
   k_split_mu<<<(di + 255) / 256, 256, 0, c.s>>>(lay.mu_x, di, lay.mu2);

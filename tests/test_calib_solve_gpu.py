@@ -270,6 +270,29 @@ def test_solve_refinement_restores_accuracy_when_ill_conditioned():
     assert e1 <= 1e-5 and e1 < e0 / 20, (e0, e1)
 
 
+def test_solve_refinement_at_moderate_conditioning():
+    """κ(Gc) ≈ 90: the band where the library's plan keeps five residual digits and
+    three correction terms (its κ estimate, 4x over, stays under 2^9). One sweep must
+    still reach fp32-level accuracy (the residual's truncation, about κ·2^-34, and the
+    correction's, about κ²·2^-40, are both near 1e-8 or below here)."""
+    d, P, n = 512, 2, 4096
+    rng = np.random.default_rng(23)
+    Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    X = (rng.standard_normal((n, d)) * np.geomspace(1.0, 10 ** -0.9, d)) @ Q.T
+    At = rng.standard_normal((P, d, d)) / math.sqrt(d)
+    Y = np.einsum("pij,nj->pni", At, X) + 0.01 * rng.standard_normal((P, n, d))
+    Xb = torch.as_tensor(X, dtype=torch.float32).to(torch.bfloat16)
+    Yb = torch.as_tensor(Y, dtype=torch.float32).to(torch.bfloat16)
+    ref = O.calib_stats(_f64(Xb), _f64(Yb))
+    lam = 1e-9
+    Ar, _, _ = O.ridge_solve(ref, lam)
+    A0, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=0)
+    A1, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=1)
+    e0 = max(_rel(A0[p], Ar[p]) for p in range(P))
+    e1 = max(_rel(A1[p], Ar[p]) for p in range(P))
+    assert e1 <= 1e-6 and e1 <= e0, (e0, e1)
+
+
 def test_solve_repeated_refinement_converges_when_badly_conditioned():
     """κ(Gc) ≈ 1e5: the fp32 solve alone is off by about κ·2^-24 and each sweep shrinks
     the error by about that factor again, down to the residual's own accuracy or the
