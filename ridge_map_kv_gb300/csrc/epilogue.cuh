@@ -9,9 +9,10 @@
 //
 // Why the turn: a lane owns one row, so storing straight from registers puts 32
 // rows into every warp store, 16 bytes each: 32 sectors per request, each half
-// written. From the staging rows the warp stores 512 contiguous-per-row bytes per
-// instruction (two 256-byte head rows at hd = 128, four 128-byte rows at hd = 64):
-// 16 sectors per request, every one written whole.
+// written. Each step of 16 rotation pairs (or 32 columns without rotation) instead
+// goes to the warp's staging rows, 64 bytes a row, and the warp then stores 8 rows
+// per instruction, two whole 32-byte sectors in each: 16 sectors per request, every
+// one written whole.
 //
 // Why the rotation is computed, not looked up: a cos/sin table row per lane puts
 // 32 rows into every table load as well, and on the K/V GEMM those loads kept the
@@ -26,34 +27,33 @@
 namespace rf {
 
 constexpr int kHeadDimMax = 128;
-// Staging rows of one epilogue warp: 32 rows of up to kHeadDimMax bf16.
-constexpr int kStageBytesPerWarp = 32 * kHeadDimMax * 2;
+// Staging rows of one epilogue warp: 32 rows of 64 bytes (one step of a head).
+constexpr int kStageBytesPerWarp = 32 * 64;
 
-// Byte offset of 16-byte chunk `ch` of staged row `r` (rows of hd bf16). The
-// chunk index is XOR-swizzled by the row's low three bits, so that the eight
-// lanes of a shared-memory phase hit distinct banks both when they write one
-// chunk of eight rows and when they read eight chunks of one row.
-__device__ __forceinline__ uint32_t stage_off(int r, int ch, int hd) {
-  return static_cast<uint32_t>(r * hd * 2 + ((ch ^ (r & 7)) << 4));
+// Byte offset of 16-byte piece `pc` (0..3) of staged row `r`. The piece index is
+// XOR-swizzled by bits 1-2 of the row, so that the eight lanes of a shared-memory
+// phase hit distinct banks both when they write one piece of eight rows and when
+// they read the four pieces of two rows.
+__device__ __forceinline__ uint32_t stage_off(int r, int pc) {
+  return static_cast<uint32_t>(r * 64 + ((pc ^ ((r >> 1) & 3)) << 4));
 }
 
-// Writes the warp's 32 staged rows of hd bf16 (hd = 64 or 128): row r, staged by
-// lane r, goes to lane r's `dst`, or nowhere when that is nullptr. Ends with the
-// warp converged, so the staging rows may be reused at once.
-__device__ __forceinline__ void store_staged_rows(uint32_t stage, int hd, __nv_bfloat16* dst) {
+// Writes the warp's 32 staged rows: piece pc of row r (staged by lane r) goes to
+// lane r's `dst` + c_lo + 8 pc for pc < 2 and + c_hi + 8 (pc − 2) for pc >= 2, or
+// nowhere when lane r's `dst` is nullptr. Starts and ends with the warp converged,
+// so the staging rows may be rewritten at once.
+__device__ __forceinline__ void store_staged_rows(uint32_t stage, int c_lo, int c_hi, __nv_bfloat16* dst) {
   const int lane = threadIdx.x & 31;
-  const int cpr_log = hd == 128 ? 4 : 3;  // 16-byte chunks per row: 16 or 8
-  const int ch = lane & ((1 << cpr_log) - 1);
-  const int lr = lane >> cpr_log;
-  const int rpi = 32 >> cpr_log;          // rows per warp store: 2 or 4
+  const int pc = lane & 3;
+  const int col = pc < 2 ? c_lo + 8 * pc : c_hi + 8 * (pc - 2);
   const unsigned long long mine = reinterpret_cast<unsigned long long>(dst);
   __syncwarp();
-#pragma unroll 4
-  for (int r0 = 0; r0 < 32; r0 += rpi) {
-    const int r = r0 + lr;
+#pragma unroll
+  for (int r0 = 0; r0 < 32; r0 += 8) {
+    const int r = r0 + (lane >> 2);
     const unsigned long long p = __shfl_sync(0xffffffffu, mine, r);
-    const uint4 v = ld_shared_v4(stage + stage_off(r, ch, hd));
-    if (p != 0ull) st_global_v4(reinterpret_cast<__nv_bfloat16*>(p) + ch * 8, v.x, v.y, v.z, v.w);
+    const uint4 v = ld_shared_v4(stage + stage_off(r, pc));
+    if (p != 0ull) st_global_v4(reinterpret_cast<__nv_bfloat16*>(p) + col, v.x, v.y, v.z, v.w);
   }
   __syncwarp();
 }
@@ -133,11 +133,11 @@ __device__ __forceinline__ void emit_head(uint32_t tcol, int hd, float scale, co
         o2[i / 2] = pack_bf16x2(r2[0], r2[1]);
         o2[i / 2 + 1] = pack_bf16x2(r2[2], r2[3]);
       }
-      const int c1 = i0 >> 3, c2 = (half + i0) >> 3;  // 16-byte chunks of the row
-      st_shared_v4(stage + stage_off(lane, c1, hd), o1[0], o1[1], o1[2], o1[3]);
-      st_shared_v4(stage + stage_off(lane, c1 + 1, hd), o1[4], o1[5], o1[6], o1[7]);
-      st_shared_v4(stage + stage_off(lane, c2, hd), o2[0], o2[1], o2[2], o2[3]);
-      st_shared_v4(stage + stage_off(lane, c2 + 1, hd), o2[4], o2[5], o2[6], o2[7]);
+      st_shared_v4(stage + stage_off(lane, 0), o1[0], o1[1], o1[2], o1[3]);
+      st_shared_v4(stage + stage_off(lane, 1), o1[4], o1[5], o1[6], o1[7]);
+      st_shared_v4(stage + stage_off(lane, 2), o2[0], o2[1], o2[2], o2[3]);
+      st_shared_v4(stage + stage_off(lane, 3), o2[4], o2[5], o2[6], o2[7]);
+      store_staged_rows(stage, i0, half + i0, dst);  // columns i0.., half + i0..
     }
   } else {
 #pragma unroll 1
@@ -157,12 +157,10 @@ __device__ __forceinline__ void emit_head(uint32_t tcol, int hd, float scale, co
                                     fmaf(u2f(v[i + 3]), scale, bb.w) * gain_at(gain, c + 3));
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        st_shared_v4(stage + stage_off(lane, (i0 >> 3) + q, hd), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                     pk[4 * q + 3]);
+      for (int q = 0; q < 4; ++q) st_shared_v4(stage + stage_off(lane, q), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      store_staged_rows(stage, i0, i0 + 16, dst);  // columns i0 .. i0 + 31
     }
   }
-  store_staged_rows(stage, hd, dst);
 }
 
 }  // namespace rf

@@ -157,7 +157,10 @@ struct KVProb {
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
   static constexpr bool kPair = kPair_;
-  static constexpr int kEpiWarps = 4;
+  // Eight epilogue warps, each on 128 columns of a tile (one head at hd = 128):
+  // with four, each on 256 columns, the epilogue held the accumulators long enough
+  // to show in the GEMM's time.
+  static constexpr int kEpiWarps = 8;
   static constexpr size_t kEpiSmemBytes = kEpiWarps * kStageBytesPerWarp;  // staging rows of the cache stores
   struct EpiState {};
   __device__ void epilogue_after(EpiState&, int, int, int, int, int, uint32_t) const {}
@@ -204,7 +207,7 @@ struct KVProb {
     for (int j = 0; j < kBoxes; ++j)
       load_operand<kKvBoxRows, false, kPair>(sb + j * (kKvBoxRows * kBK * 2), c.tb[j], bar, kb * kBK, c.b_row[j]);
   }
-  __device__ void epilogue(EpiState&, int u, int, int, uint32_t tacc, int row, int, uint32_t rank) const {
+  __device__ void epilogue(EpiState&, int u, int, int, uint32_t tacc, int row, int wcol0, uint32_t rank) const {
     const int nf = *n_fill;
     int p, mt, nt;
     decode(u, (nf + Cfg::kUnitM - 1) / Cfg::kUnitM, p, mt, nt);
@@ -220,9 +223,10 @@ struct KVProb {
     const unsigned long long pos = static_cast<unsigned long long>(static_cast<long long>(t) + pos_offset);
     const uint32_t stage =
         smem_u32(gemm_epi_smem<kPair_>()) + static_cast<uint32_t>(((threadIdx.x >> 5) - 2) * kStageBytesPerWarp);
+    // this warp's columns of the tile: wcol0 .. wcol0 + kBN * 4 / kEpiWarps (tacc points at wcol0)
 #pragma unroll 1
-    for (int hh = 0; hh < kBN / hd; ++hh) {
-      const int col0 = nt * kBN + hh * hd;
+    for (int hh = 0; hh < kBN * 4 / kEpiWarps / hd; ++hh) {
+      const int col0 = nt * kBN + wcol0 + hh * hd;
       const bool is_k = col0 < KV;
       const int h = (is_k ? col0 : col0 - KV) / hd;
       __nv_bfloat16* dst = (is_k ? kc : vc) + row_off + static_cast<size_t>(h) * hd;

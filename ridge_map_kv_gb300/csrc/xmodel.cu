@@ -115,7 +115,7 @@ struct XMProb {
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
   static constexpr bool kPair = kPair_;
-  static constexpr int kEpiWarps = 4;
+  static constexpr int kEpiWarps = 8;  // 128 columns of a tile each (one head at hd = 128)
   static constexpr size_t kEpiSmemBytes = kEpiWarps * kStageBytesPerWarp;  // staging rows of the target stores
   struct EpiState {};
   __device__ void epilogue_after(EpiState&, int, int, int, int, int, uint32_t) const {}
@@ -176,11 +176,11 @@ struct XMProb {
     tma2<kPair>(sb, c.tb, bar, kb * kBK, c.b_row);
     c.c += kBK;
   }
-  __device__ void epilogue(EpiState&, int u, int, int, uint32_t tacc, int row, int, uint32_t rank) const {
+  __device__ void epilogue(EpiState&, int u, int, int, uint32_t tacc, int row, int wcol0, uint32_t rank) const {
     int l, mt, nt;
     decode(u, l, mt, nt);
     const bool is_k = nt < n_half;
-    const int col0 = (is_k ? nt : nt - n_half) * kBN;
+    const int col0 = (is_k ? nt : nt - n_half) * kBN + wcol0;  // this warp's first column (tacc points at it)
     const int t = mt * Cfg::kUnitM + static_cast<int>(rank) * kBM + row;
     const bool valid = t < N;
     const int tt = valid ? t : 0;
@@ -190,7 +190,7 @@ struct XMProb {
     const uint32_t stage =
         smem_u32(gemm_epi_smem<kPair_>()) + static_cast<uint32_t>(((threadIdx.x >> 5) - 2) * kStageBytesPerWarp);
 #pragma unroll 1
-    for (int hh = 0; hh < kBN / hd; ++hh)
+    for (int hh = 0; hh < kBN * 4 / kEpiWarps / hd; ++hh)
       emit_head(tacc + hh * hd, hd, 1.0f, bias + hh * hd, nullptr, is_k ? rope_t.g : nullptr, pos,
                 valid ? dst + hh * hd : nullptr, stage);
   }
