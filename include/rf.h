@@ -101,14 +101,16 @@ enum rf_stage {
   RF_STAGE_SELECT_SPLIT = 21   /* source selection: fp32 -> three bf16 planes      */
 };
 rf_status rf_profile_start(int max_records);
-/* Diagnostic: runs the tensor-core GEMM kernel (cta_pair != 0: the CTA-pair
- * kernel, else the single-CTA one) on a problem whose operand copies are never
- * issued, so its MMA thread's bounded wait runs out after the wait limit
+/* Diagnostic: runs the tensor-core GEMM kernel on a problem whose operand copies
+ * are never issued, so its MMA thread's bounded wait runs out after the wait limit
  * (rf_set_wait_timeout_ms). The kernel then drains, frees its TMEM and writes
  * RF_ERR_TIMEOUT to *dev_status (device int32, must be 0 before the call). It
  * tests the library's failure path without faulting the GPU: nothing is ever in
- * flight, and the context stays usable. */
-rf_status rf_selftest_wait_timeout(int cta_pair, int32_t* dev_status, rf_stream_t stream);
+ * flight, and the context stays usable.
+ *   mode  bit 0: the CTA-pair kernel (else the single-CTA one); bit 1: the dynamic
+ *         unit order (units posted through the shared-memory ring, from a counter
+ *         inside the library's device code), else round-robin. */
+rf_status rf_selftest_wait_timeout(int mode, int32_t* dev_status, rf_stream_t stream);
 int rf_profile_stop(int32_t* stage_ids, float* ms, int capacity);
 const char* rf_stage_name(int stage_id);
 

@@ -232,10 +232,10 @@ def rf_fill_kv_static(desc, x_S, ld_x, exact_mask, A, b, gain, Wk, Wv, k_cache, 
                                    _p(n_fill_out), _p(dev_status), _s(stream)), "rf_fill_kv_static")
 
 
-def rf_selftest_wait_timeout(cta_pair, dev_status, stream=None):
+def rf_selftest_wait_timeout(mode, dev_status, stream=None):
     """Runs the GEMM core on a problem whose copies never arrive: *dev_status becomes
-    RF_ERR_TIMEOUT after the wait limit (see include/rf.h)."""
-    _check(lib().rf_selftest_wait_timeout(int(bool(cta_pair)), _p(dev_status), _s(stream)), "rf_selftest_wait_timeout")
+    RF_ERR_TIMEOUT after the wait limit. mode bit 0: CTA pair; bit 1: dynamic unit order."""
+    _check(lib().rf_selftest_wait_timeout(int(mode), _p(dev_status), _s(stream)), "rf_selftest_wait_timeout")
 
 
 def rf_quantize_maps_int8(desc, A, q, s, stream=None):

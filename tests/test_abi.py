@@ -165,6 +165,25 @@ def test_calib_and_xmodel_and_solve_validate_on_the_host():
     assert ei.value.status == rf.RF_ERR_SHAPE
 
 
+def test_calib_workspace_is_optional_but_checked_when_given():
+    desc = rf.rf_calib_desc(d_in=256, d_out=256, n_maps=1)
+    assert rf.rf_calib_workspace_bytes(desc, 1024) == 256
+    stats = rf.calib_stats_struct(256, 256, 256, 256, 256)
+    with pytest.raises(rf.RFError) as ei:     # too small
+        rf.rf_calib_accumulate(desc, 256, 256, 256, 256, 1024 * 256, 1024, stats, None, 256, 128, stream=0)
+    assert ei.value.status == rf.RF_ERR_WORKSPACE
+    with pytest.raises(rf.RFError) as ei:     # not 256-byte aligned
+        rf.rf_calib_accumulate(desc, 256, 256, 256, 256, 1024 * 256, 1024, stats, None, 272, 256, stream=0)
+    assert ei.value.status == rf.RF_ERR_WORKSPACE
+
+
+def test_selftest_mode_is_checked_on_the_host():
+    for mode in (-1, 4):
+        with pytest.raises(rf.RFError) as ei:
+            rf.rf_selftest_wait_timeout(mode, 256, stream=0)
+        assert ei.value.status == rf.RF_ERR_INVALID_ARG
+
+
 def test_value_scale_validates_on_the_host():
     desc = _fill_desc()                       # toy: T = 3
     assert rf.rf_value_scale_workspace_bytes(desc, 0) == 0

@@ -1,8 +1,8 @@
 """Failure path on the GPU without a fault: the GEMM core's bounded waits.
 
-rf_selftest_wait_timeout runs the real single-CTA and CTA-pair GEMM kernels on a
-problem whose operand copies are never issued, so the MMA thread waits for data
-that nothing sends. With a 200 ms wait limit each role must give up, drain, free
+rf_selftest_wait_timeout runs the real single-CTA and CTA-pair GEMM kernels, in
+round-robin and in dynamic unit order, on a problem whose operand copies are never
+issued, so the MMA thread waits for data that nothing sends. With a 200 ms wait limit each role must give up, drain, free
 TMEM, report RF_ERR_TIMEOUT in the status word and exit; afterwards the context
 must still run a fill correctly.
 """
@@ -19,13 +19,15 @@ from fillcheck import assert_bookkeeping, assert_values, run_fill
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("pair", [0, 1], ids=["single-cta", "cta-pair"])
-def test_gemm_wait_runs_out_reports_timeout_and_context_survives(pair):
+@pytest.mark.parametrize("mode", [0, 1, 2, 3],
+                         ids=["single-cta", "cta-pair", "single-cta-dynamic-order", "cta-pair-dynamic-order"])
+def test_gemm_wait_runs_out_reports_timeout_and_context_survives(mode):
+    pair = mode & 1
     rf.rf_set_wait_timeout_ms(200)
     try:
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         t0 = time.monotonic()
-        rf.rf_selftest_wait_timeout(pair, status)
+        rf.rf_selftest_wait_timeout(mode, status)
         torch.cuda.synchronize()
         elapsed = time.monotonic() - t0
     finally:
