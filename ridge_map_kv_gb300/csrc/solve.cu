@@ -683,11 +683,30 @@ constexpr int kOzBits = 7;
 constexpr int kOzChunk = 2048;
 constexpr int kOzMaps = 4;  // maps per residual launch (keeps the last wave of units small)
 
+// round(x · 2^(62 − e)) for |x| < 2^(e−1), from the bits of x with integer
+// operations only: x = ±m·2^(E−1075) with m its 53-bit significand (E its biased
+// exponent; a subnormal has no hidden bit and the exponent of E = 1), so the
+// result is m shifted by E − 1013 − e, rounded half away from zero when the
+// shift drops bits. Exact when no bit is dropped: always, unless x is below
+// 2^(e−63), which lies below the digits kept anyway.
+__device__ __forceinline__ long long fixed62(double x, int e) {
+  const long long b = __double_as_longlong(x);
+  const int E = static_cast<int>((b >> 52) & 0x7ff);
+  long long m = b & ((1ll << 52) - 1);
+  if (E != 0) m |= 1ll << 52;
+  const int sh = (E != 0 ? E : 1) - 1013 - e;  // q = m · 2^sh; sh <= 8 since |q| < 2^61
+  long long q;
+  if (sh >= 0) q = m << sh;
+  else if (sh > -63) q = (m + (1ll << (-sh - 1))) >> (-sh);
+  else q = 0;
+  return b < 0 ? -q : q;
+}
+
 // Digits of each row of an fp64 matrix [rows][cols]: digit d of row r at
 // planes[(d * plane_rows + r) * cols ...] in bf16 (plane_rows >= rows), and the row
 // scale σ (a power of two, 0 for a zero row). One warp per row. The digits come
 // from integer arithmetic on v = x/σ as a 62-bit fixed-point integer q = v·2^62
-// (exact: |v| <= 1/2, and a double has 53 significant bits): digit s is q's
+// (fixed62; |v| < 1/2, and a double has 53 significant bits): digit s is q's
 // bits from 62 − 7s, rounded half up, and taking it out leaves the remainder
 // within half a unit of that position, so |d_s| <= 64 as in the fp32 split. (In
 // fp64 arithmetic the same split took about 1 ms at d = 4,096: GB300's fp64 rate.)
@@ -705,7 +724,7 @@ __global__ void __launch_bounds__(256) k_oz_digits_f64(const double* __restrict_
   if (lane == 0) scale[warp] = mx > 0.0 ? ldexp(1.0, e) : 0.0;
   const size_t plane = static_cast<size_t>(plane_rows) * cols;
   for (int k = lane; k < cols; k += 32) {
-    long long q = mx > 0.0 ? __double2ll_rn(ldexp(x[k], 62 - e)) : 0;  // exact, |q| <= 2^61
+    long long q = mx > 0.0 ? fixed62(x[k], e) : 0;  // |q| < 2^61
 #pragma unroll
     for (int d = 0; d < kOzDigits; ++d) {
       const int sh = 62 - kOzBits * (d + 1);
