@@ -406,3 +406,29 @@ def test_solve_cross_model_gram_shape_matches_oracle():
     calibration, to keep the oracle's Gram quick; the solve's sizes are the same)."""
     x = synth.XMODEL
     _full_width_solve(x.d_in, x.KV, 2, 16384, x.lam, index=x.index)
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_calibration_and_solve_by_layer_block_equal_the_whole(world):
+    """Calibration and solve shard by upper layer like the fill, with no collective:
+    rank r accumulates C and sy for its block of maps from the same X (its G and sx
+    are those of every rank) and solves just those maps. Run block by block on one
+    GPU, the blocks' sums and maps (with a refinement sweep) equal the whole call's
+    bit for bit: every map's sums, factorisation, products and residual are computed
+    from its own columns and the shared G alone."""
+    from ridge_map_kv_gb300 import shard as sh
+    d, P, n = 512, 7, 4096
+    cal = synth.calib_inputs(d, d, P, n, index=97)
+    X, Y = cal["X"].to(DEV), cal["Y"].to(DEV)
+    whole = _zeros_stats(d, d, P)
+    _accumulate(X, Y, whole, [2048])
+    Aw, bw, _, _ = _solve(whole, d, d, P, 0.03, refine=1)
+    for r in range(world):
+        blk = sh.layer_shard(P, 0, world, r)
+        part = _zeros_stats(d, d, blk.layers)
+        _accumulate(X, Y[blk.p0:blk.p1].contiguous(), part, [2048])
+        for k in ("G", "sx", "n"):
+            assert torch.equal(part[k], whole[k]), k
+        assert torch.equal(part["C"], whole["C"][blk.p0:blk.p1]) and torch.equal(part["sy"], whole["sy"][blk.p0:blk.p1])
+        A, b, _, _ = _solve(part, d, d, blk.layers, 0.03, refine=1)
+        assert np.array_equal(A, Aw[blk.p0:blk.p1]) and np.array_equal(b, bw[blk.p0:blk.p1])

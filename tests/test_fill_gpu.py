@@ -52,6 +52,8 @@ def test_toy_fill_matches_oracle_everywhere(flags):
     _small("hd64, 4 heads, 2 layers", d=768, L=4, S=2, N=300, T=20, H=4, hd=64, exact="blocks16_5"),
     _small("one layer, no exact rows", d=256, L=3, S=2, N=129, T=0, H=1, hd=128, exact=None),
     _small("position offset", d=256, L=4, S=1, N=200, T=8, H=2, hd=64, exact="uniform10", pos_offset=1000),
+    _small("positions near 2^26", d=256, L=3, S=1, N=300, T=8, H=2, hd=128, exact="uniform10",
+           pos_offset=(1 << 26) + 777),
 ], ids=lambda c: c.name)
 @KERNELS
 def test_fill_small_shapes_match_oracle(cfg, flags):

@@ -65,7 +65,8 @@ SMALL = synth.XModelConfig("xmodel small", 94, L_src=5, L_tgt=3, k=2, H=2, hd=12
 
 @pytest.mark.parametrize("cfg", [SMALL,
                                  dataclasses.replace(SMALL, name="hd64 4 heads offset", H=4, hd=64, k=3, N=131,
-                                                     pos_offset=700, theta_tgt=1.0e6)],
+                                                     pos_offset=700, theta_tgt=1.0e6),
+                                 dataclasses.replace(SMALL, name="positions near 2^25", pos_offset=(1 << 25) + 321)],
                          ids=lambda c: c.name)
 @pytest.mark.parametrize("flags", [rf.RF_FLAG_SINGLE_CTA, rf.RF_FLAG_CTA_PAIR], ids=["single-cta", "cta-pair"])
 def test_xmodel_small_matches_oracle(cfg, flags):
@@ -136,8 +137,12 @@ def test_xmodel_table_out_of_range_is_reported_on_the_device_and_writes_nothing(
     _check(cfg, inp, kt2, vt2, range(cfg.L_tgt), np.arange(cfg.N))
 
 
-@pytest.mark.parametrize("hd,theta,off", [(128, 1.0e6, 0), (64, 5.0e5, 12345)])
+@pytest.mark.parametrize("hd,theta,off", [(128, 1.0e6, 0), (64, 5.0e5, 12345), (128, 1.0e6, (1 << 27) + 12345),
+                                          (64, 1.0e4, -4096)])
 def test_rope_rows_matches_oracle_and_inverts(hd, theta, off):
+    """RoPE at positions off .. off + 512 against the fp64 oracle, and its inverse: the
+    angle is reduced mod 2π in 64-bit fixed point, so positions near 2^27 and negative
+    ones are as accurate as small ones."""
     n, H = 513, 3
     ld = H * hd + 8
     x = synth._randn((n, ld), 77, DEV)
