@@ -648,7 +648,7 @@ def _zero_stats(d_in, d_out, P, dev):
 
 
 EXTRA_ROWS = ("fill_llama8b", "a5_calibration", "a5_calibration_xmodel", "a6_solve", "a6_solve_27b",
-              "a6_solve_xmodel", "a7_xmodel", "next3_map_storage_8b",
+              "a6_solve_xmodel", "a7_xmodel", "next3_map_storage_8b", "next3_map_storage_27b",
               "next2_key_norm_qwen3", "next4_nonsquare_flash_next", "next1_value_rescale_27b",
               "next4a_source_selection_xmodel")
 
@@ -858,6 +858,54 @@ def run_extras(dev, peak_tflops, flags=0, only=None, capture=False):
             del ws
         out["next3_map_storage_8b"] = row
         del inp, kc, vc, Wk, Wv, q, qs, A_host, q_host
+        torch.cuda.empty_cache()
+
+    if only in (None, "next3_map_storage_27b"):
+        # The 27B deployment's map storage: the 48 maps in int8 (1.26 GB, the pages'
+        # "1.2 GiB") streamed layer by layer from pinned host memory, against the same
+        # int8 maps on the device, the layered fill from the bf16 maps on the device,
+        # and the resident bf16 fill. The synthetic maps are I + N(0, 0.02²/d): their
+        # per-row int8 codes are 0 off the diagonal for almost every entry, so the int8
+        # arms multiply mostly zeros, draw less power and run at higher power-capped
+        # clocks; compare the int8 arms with each other (the cost of streaming) and the
+        # bf16 arms with each other (the cost of going layer by layer).
+        c = synth.DENSE27B
+        inp = synth.fill_inputs(c, device=dev)
+        fd, Wk, Wv = _prefolded(c, inp, flags)
+        q = torch.empty((c.P, c.d, c.d), dtype=torch.int8, device=dev)
+        qs = torch.empty((c.P, c.d), dtype=torch.float32, device=dev)
+        rf.rf_quantize_maps_int8(fd, inp["A"], q, qs)
+        q_host = q.cpu().pin_memory()
+        kc = torch.zeros((c.P, c.N, c.KV), dtype=torch.bfloat16, device=dev)
+        vc = torch.zeros_like(kc)
+        nf = torch.zeros(1, dtype=torch.int32, device=dev)
+        fd0 = rf.rf_fill_desc(d=c.d, d_in=c.d_in, L=c.P, S=0, N=c.N, T=c.T, n_kv_heads=c.H, head_dim=c.hd,
+                              rope_theta=c.rope_theta, rms_eps=c.rms_eps, pos_offset=c.pos_offset, flags=fd.flags)
+        row = {"workload": workload_label(c), "map_bytes_bf16": c.P * c.d * c.d * 2, "map_bytes_int8": c.P * c.d * c.d}
+        wsb = rf.rf_fill_workspace_bytes(fd0)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        row["resident_bf16_ms"], _ = _timed(lambda: rf.rf_fill_kv(fd0, inp["x_S"], c.d, inp["mask"], inp["A"],
+                                                                  inp["b"], None, Wk, Wv, kc, vc, c.N * c.KV, c.KV, nf,
+                                                                  None, ws, wsb), 3, stream)
+        row["resident_workspace_bytes"] = wsb
+        del ws
+        torch.cuda.empty_cache()
+        for key, ms_ in (("layered_device_bf16", rf.map_source(rf.RF_MAPS_BF16, inp["A"])),
+                         ("layered_device_int8", rf.map_source(rf.RF_MAPS_INT8, q, row_scale=qs)),
+                         ("layered_host_int8", rf.map_source(rf.RF_MAPS_INT8, q_host, on_host=True, row_scale=qs))):
+            wsb = rf.rf_fill_layered_workspace_bytes(fd0, ms_)
+            ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+            row[f"{key}_ms"], st = _timed(lambda: rf.rf_fill_kv_layered(fd0, inp["x_S"], c.d, inp["mask"], ms_,
+                                                                        inp["b"], None, Wk, Wv, kc, vc, c.N * c.KV,
+                                                                        c.KV, nf, None, ws, wsb), 3, stream)
+            row[f"{key}_workspace_bytes"] = wsb
+            if "int8_expand" in st:
+                row[f"{key}_expand_ms"] = st["int8_expand"]
+            del ws
+        row["note"] = ("int8 codes of the synthetic maps are mostly 0 off the diagonal: the int8 arms draw less "
+                       "power and clock higher; compare int8 with int8 and bf16 with bf16")
+        out["next3_map_storage_27b"] = row
+        del inp, kc, vc, Wk, Wv, q, qs, q_host
         torch.cuda.empty_cache()
 
     if only in (None, "next2_key_norm_qwen3"):
