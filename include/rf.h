@@ -156,6 +156,12 @@ typedef struct rf_fill_desc {
  * from rf_fold_kv_weights; `gain` is then ignored and may be NULL. Without it the
  * fill folds the gain into its workspace on every call. */
 #define RF_WEIGHTS_PREFOLDED 4u
+/* Flag of rf_calib_desc for rf_solve: the refinement's residual cuts its operands
+ * into 7-bit digits at every width. By default it takes 8-bit digits up to
+ * d_in = 21845 and 7-bit ones above, where the int32 sums of 8-bit digit products
+ * could overflow; the flag runs the wider widths' arithmetic at any size (the
+ * result meets the same accuracy, with more digit products). */
+#define RF_SOLVE_DIGITS7 8u
 
 /* Supported fill shapes: d % 256 == 0, head_dim in {64, 128}, KV % 128 == 0,
  * N - T <= 2^24. */
@@ -384,10 +390,13 @@ size_t rf_solve_workspace_bytes(const rf_calib_desc* desc);
  *   residual computed beyond fp32 accuracy (exact integer digit products on the
  *   tensor cores); b_p = μ_p − A_p μ_x (compensated, to about 2^-44 of Σ|A||μ|,
  *   rounded to fp32). How accurate the residual and the correction are is chosen on
- *   the device from κ(Gc + αI), estimated once by power iteration: accurate enough
- *   for a sweep to bring A to fp32 accuracy, the residual to about 2^-(25 + log2 4κ)
- *   of Σ|A||Gc + αI| (2^-34 for κ below about 2^7, else about 2^-41, its limit), the
- *   correction to fp32 when 4κ > 2^10, else to about 2^-16 of its terms.
+ *   the device from κ(Gc + αI), estimated once by power iteration (24 steps, whose
+ *   estimate is taken twice over): accurate enough for a sweep to bring A to fp32
+ *   accuracy, the residual to at least 2^-(25 + log2 2κ) of Σ|A||Gc + αI| (with
+ *   8-bit digits 2^-31.7 for κ up to about 51, 2^-39.4 up to about 10,800, else
+ *   2^-47.2, its limit; with 7-bit digits, above d_in = 21845 or under
+ *   RF_SOLVE_DIGITS7, 2^-27.7 up to about 3, 2^-34.4 up to about 330, else 2^-41.2),
+ *   the correction to fp32 when 4κ > 2^10, else to about 2^-16 of its terms.
  *   A [n_maps][d_out][d_in] fp32, b [n_maps][d_out] fp32,
  *   A_bf16 (may be NULL) bf16 copy of A for rf_fill_kv, alpha_out (device, may be NULL).
  * A non-positive pivot sets RF_ERR_NOT_SPD in *dev_status. */

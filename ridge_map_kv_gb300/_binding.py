@@ -36,6 +36,7 @@ class RFError(RuntimeError):
 RF_FLAG_SINGLE_CTA = 1
 RF_FLAG_CTA_PAIR = 2
 RF_WEIGHTS_PREFOLDED = 4
+RF_SOLVE_DIGITS7 = 8
 
 
 RF_MAPS_BF16 = 0

@@ -23,9 +23,10 @@
 //   k_centre_split_t        Cc_p = C_p − n μ_x μ_pᵀ, written transposed as the product's
 //                           three bf16 planes
 //   refinement (optional)   R_p = Cc_pᵀ − A_p H, fp64-accurate on the tensor cores
-//                           (k_oz_digits_*: integer digit planes; OzakiProb: exact
-//                           int32 sums per digit weight; k_oz_combine: their exact
-//                           int64 combination, one fp64 rounding), then
+//                           (k_oz_digits_*: integer digit planes of 8 bits, or 7
+//                           above d_in = 21845; OzakiProb: exact int32 sums per
+//                           digit weight; k_oz_combine: two exact int64 halves, one
+//                           fp64 rounding), then
 //                           A_p += R_p H^-1 (the split product)
 //   k_bias                  b_p = μ_p − A_p μ_x (compensated fp32 pairs, fp64 across
 //                           lanes); k_to_bf16 the optional bf16 copy of A
@@ -669,19 +670,28 @@ static rf_status split_gemm(SolveCtx& c, const float* a, const float* Bsym, int 
 //   R_p = Cc_pᵀ − A_p H.
 // Each row of A_p (fp32) and each row of H (fp64; H is symmetric, so its rows are
 // its columns) is scaled by a power of two σ ≥ 2 × its largest magnitude and cut
-// into kOzDigits integer digits of 7 bits: x/σ = Σ_s d_s 2^(−7s), |d_s| <= 64, every
-// digit exact in bf16. A digit product summed over a K chunk of 2048 is an integer
-// of magnitude at most 2^23, exact in the fp32 accumulator; the epilogue adds the
-// chunks and the digit pairs of one weight m = s + t as exact int32 sums J_m and
-// stores them (one launch per weight). A last pass forms T = Σ_m J_m 2^(7(7−m))
-// exactly in int64 and R = Cc − σ_o τ_i 2^(−49) T in fp64. Pairs with
-// s + t <= kOzDigits + 1 are kept: 41-bit operands, a residual accurate to about
-// 2^-40 of Σ|A||H| in the worst case.
+// into integer digits of b bits: x/σ = Σ_s d_s 2^(−bs), |d_s| <= 2^(b−1), every digit
+// exact in bf16 (b <= 8). A digit product summed over a K chunk of 2^(26−2b) is an
+// integer of magnitude at most 2^24, exact in the fp32 accumulator; the epilogue adds
+// the chunks and the digit pairs of one weight m = s + t as exact int32 sums J_m
+// (|J_m| <= (m−1) 2^(2b−2) d_in) and stores them (one launch per weight). A last pass
+// forms T = Σ_m J_m 2^(b(M−m)) from two exact int64 halves joined in fp64 (one
+// rounding, 2^-53 of |T|) and R = Cc − σ_o τ_i 2^(−bM) T. b = 8 wherever the int32
+// sums cannot overflow (d_in <= 21845), else 7. Of n digits, the pairs with
+// s + t <= n + 1 are kept: a residual within about (n+1)/4 · 2^(−bn) of Σ|A||H| in
+// the worst case (the dropped pairs of weight n + 2 and both truncations).
 // --------------------------------------------------------------------------
-constexpr int kOzDigits = 6;
-constexpr int kOzBits = 7;
-constexpr int kOzChunk = 2048;
-constexpr int kOzMaps = 4;  // maps per residual launch (keeps the last wave of units small)
+constexpr int kOzDigits = 6;  // digits per operand at most (21 pairs, weights 2 .. 7)
+constexpr int kOzMaps = 4;    // maps per residual launch (keeps the last wave of units small)
+
+// Digit width for a contraction of length d_in: 8 bits while the largest weight's
+// sum, 6 pairs of 2^14 products over d_in, stays below 2^31; else 7.
+static int oz_bits(int d_in) {
+  return static_cast<long long>(kOzDigits) * (1ll << 14) * d_in < (1ll << 31) ? 8 : 7;
+}
+
+// K chunk over which a digit product's sum stays within 2^24: 2^(26 − 2b).
+static int oz_chunk(int bits) { return 1 << (26 - 2 * bits); }
 
 // round(x · 2^(62 − e)) for |x| < 2^(e−1), from the bits of x with integer
 // operations only: x = ±m·2^(E−1075) with m its 53-bit significand (E its biased
@@ -702,47 +712,80 @@ __device__ __forceinline__ long long fixed62(double x, int e) {
   return b < 0 ? -q : q;
 }
 
-// Digits of each row of an fp64 matrix [rows][cols]: digit d of row r at
-// planes[(d * plane_rows + r) * cols ...] in bf16 (plane_rows >= rows), and the row
-// scale σ (a power of two, 0 for a zero row). One warp per row. The digits come
-// from integer arithmetic on v = x/σ as a 62-bit fixed-point integer q = v·2^62
-// (fixed62; |v| < 1/2, and a double has 53 significant bits): digit s is q's
-// bits from 62 − 7s, rounded half up, and taking it out leaves the remainder
-// within half a unit of that position, so |d_s| <= 64 as in the fp32 split. (In
+// Digits kept this sweep: plan[0] is the largest digit weight n + 1 (k_refine_plan).
+__device__ __forceinline__ int oz_planned_digits(const int* plan) { return max(1, min(kOzDigits, *plan - 1)); }
+
+// The first n digits (n from the plan) of each row of an fp64 matrix [rows][cols]:
+// digit d of row r at planes[(d * plane_rows + r) * cols ...] in bf16 (plane_rows >=
+// rows), and the row scale σ (a power of two, 0 for a zero row). One warp per row.
+// The digits come from integer arithmetic on v = x/σ as a 62-bit fixed-point integer
+// q = v·2^62 (fixed62; |v| < 1/2, and a double has 53 significant bits): digit s is
+// q's bits from 62 − b·s, rounded half up, and taking it out leaves the remainder
+// within half a unit of that position, so |d_s| <= 2^(b−1) as in the fp32 split. (In
 // fp64 arithmetic the same split took about 1 ms at d = 4,096: GB300's fp64 rate.)
 __global__ void __launch_bounds__(256) k_oz_digits_f64(const double* __restrict__ X, int rows, int plane_rows, int cols,
+                                                       int bits, const int* __restrict__ plan,
                                                        __nv_bfloat16* __restrict__ planes, double* __restrict__ scale) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= rows) return;
-  const double* x = X + static_cast<size_t>(warp) * cols;
-  double mx = 0.0;
-  for (int k = lane; k < cols; k += 32) mx = fmax(mx, fabs(x[k]));
-  for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const int nd = oz_planned_digits(plan);
+  const double2* x = reinterpret_cast<const double2*>(X + static_cast<size_t>(warp) * cols);
+  // the largest magnitude from the bit patterns (for non-negative doubles the integer
+  // order is the numeric one), four columns a lane (cols % 128 == 0)
+  long long mb = 0;
+  for (int k = lane; k < cols / 4; k += 32) {
+    const double2 a = x[2 * k], b = x[2 * k + 1];
+    const long long m0 = max(__double_as_longlong(a.x) & 0x7fffffffffffffffll,
+                             __double_as_longlong(a.y) & 0x7fffffffffffffffll);
+    const long long m1 = max(__double_as_longlong(b.x) & 0x7fffffffffffffffll,
+                             __double_as_longlong(b.y) & 0x7fffffffffffffffll);
+    mb = max(mb, max(m0, m1));
+  }
+  for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+  const double mx = __longlong_as_double(mb);
   int e = 0;
   if (mx > 0.0) frexp(mx, &e);  // mx = f 2^e, f in [0.5, 1): σ = 2^(e+1) >= 2 mx
   ++e;
   if (lane == 0) scale[warp] = mx > 0.0 ? ldexp(1.0, e) : 0.0;
   const size_t plane = static_cast<size_t>(plane_rows) * cols;
-  for (int k = lane; k < cols; k += 32) {
-    long long q = mx > 0.0 ? fixed62(x[k], e) : 0;  // |q| < 2^61
+  for (int k = lane; k < cols / 4; k += 32) {
+    const double2 a = x[2 * k], b = x[2 * k + 1];
+    long long q[4] = {0, 0, 0, 0};
+    if (mb > 0) {
+      q[0] = fixed62(a.x, e);
+      q[1] = fixed62(a.y, e);
+      q[2] = fixed62(b.x, e);
+      q[3] = fixed62(b.y, e);
+    }
 #pragma unroll
     for (int d = 0; d < kOzDigits; ++d) {
-      const int sh = 62 - kOzBits * (d + 1);
-      const long long r = (q + (1ll << (sh - 1))) >> sh;  // |r| <= 64
-      q -= r << sh;                                       // |q| <= 2^(sh-1)
-      planes[d * plane + static_cast<size_t>(warp) * cols + k] = __float2bfloat16_rn(static_cast<float>(r));
+      if (d >= nd) break;
+      const int sh = 62 - bits * (d + 1);
+      __nv_bfloat16 r[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const long long v = (q[j] + (1ll << (sh - 1))) >> sh;  // |v| <= 2^(bits-1)
+        q[j] -= v * (1ll << sh);                                // |q| <= 2^(sh-1)
+        r[j] = __float2bfloat16_rn(static_cast<float>(static_cast<int>(v)));
+      }
+      uint2 w;
+      memcpy(&w, r, sizeof(w));
+      *reinterpret_cast<uint2*>(planes + d * plane + static_cast<size_t>(warp) * cols + 4 * k) = w;
     }
   }
 }
 
-// The same digits of an fp32 matrix, from fp32 arithmetic: for |v| <= 1/2, v·2^7,
+// The same digits of an fp32 matrix, from fp32 arithmetic: for |v| <= 1/2, v·2^b,
 // its nearest integer and their difference are all exact in fp32, so the digits are
 // those of the fp64 procedure without using the (slow) fp64 units. Four columns a
 // lane; cols % 128 == 0 and X 16-byte aligned.
 __global__ void __launch_bounds__(256) k_oz_digits_f32(const float* __restrict__ X, int rows, int plane_rows, int cols,
+                                                       int bits, const int* __restrict__ plan,
                                                        __nv_bfloat16* __restrict__ planes, double* __restrict__ scale) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= rows) return;
+  const int nd = oz_planned_digits(plan);
+  const float radix = static_cast<float>(1 << bits);
   const float4* x = reinterpret_cast<const float4*>(X + static_cast<size_t>(warp) * cols);
   const int c4 = cols / 4;
   float mx = 0.0f;
@@ -763,10 +806,11 @@ __global__ void __launch_bounds__(256) k_oz_digits_f32(const float* __restrict__
     for (int j = 0; j < 4; ++j) v[j] = mx > 0.0f ? ldexpf(v[j], -e) : 0.0f;  // |v| <= 1/2
 #pragma unroll
     for (int d = 0; d < kOzDigits; ++d) {
+      if (d >= nd) break;
       __nv_bfloat16 r[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float t = v[j] * static_cast<float>(1 << kOzBits);
+        const float t = v[j] * radix;
         const float q = rintf(t);
         v[j] = t - q;
         r[j] = __float2bfloat16_rn(q);
@@ -797,35 +841,101 @@ __device__ __forceinline__ double scale_pow2(double v, int e) {
   return v * pow2_double(e / 2) * pow2_double(e - e / 2);
 }
 
-// R_p[o][i] = C_p[i][o] − n μ_x[i] μ_p[o] − σ_o τ_i 2^(−7M) T[o][i] for the maps of a
-// group, with M = *m_max (the largest digit weight computed, 7 at most) and
-// T = Σ_{m <= M} J_m 2^(7(M−m)) built exactly in int64 from the weights' sums
-// (|J_m| <= (m−1) 2^12 d_in, so |T| < 2^47.1 d_in <= 2^62.1 for d_in <= 32768) and
-// rounded once to fp64. Through 32 x 32 shared tiles (C is [i][o], R [o][i]).
-// Grid (d_out/32, d_in/32, maps), 32 x 8 threads.
+// round(x / 2^k), ties away from zero, from the bits of the double with integer
+// operations only (GB300's fp64 rate is low); saturates at ±2^62.
+__device__ __forceinline__ long long to_grid(double x, int k) {
+  const long long b = __double_as_longlong(x);
+  const int E = static_cast<int>((b >> 52) & 0x7ff);
+  long long m = b & ((1ll << 52) - 1);
+  if (E != 0) m |= 1ll << 52;
+  const int sh = (E != 0 ? E : 1) - 1075 - k;  // |x| / 2^k = m · 2^sh, m < 2^53
+  long long q;
+  if (E == 0x7ff || sh > 9) q = 1ll << 62;
+  else if (sh >= 0) q = m << sh;
+  else if (sh > -63) q = (m + (1ll << (-sh - 1))) >> (-sh);
+  else q = 0;
+  return b < 0 ? -q : q;
+}
+
+// v as fp32 (within about 2 ulp) from two 32-bit conversions of |v|.
+__device__ __forceinline__ float ll_to_float(long long v) {
+  const unsigned long long a = v < 0 ? 0ull - static_cast<unsigned long long>(v) : static_cast<unsigned long long>(v);
+  const float f = fmaf(static_cast<float>(static_cast<unsigned>(a >> 32)), 4294967296.0f,
+                       static_cast<float>(static_cast<unsigned>(a & 0xffffffffull)));
+  return v < 0 ? -f : f;
+}
+
+// R_p[o][i] = Cc_p[i][o] − σ_o τ_i 2^(−bM) T[o][i] for the maps of a group, with
+// Cc_p = C_p − n μ_x μ_pᵀ, M = *m_max (the largest digit weight computed, 7 at most)
+// and T = Σ_{m <= M} J_m 2^(b(M−m)). The difference is taken exactly in integers on
+// T's grid 2^k, k = log2(σ_o τ_i) − bM: Cc rounded to the grid (half a unit of
+// 2^(−bM) σ_o τ_i, below the residual's own accuracy) minus T as an int64, then
+// rounded to fp32. For an accurate A, |Cc| and |T| stay within d_in 2^(bM−2) units of
+// the grid; where that passes 2^61 (8-bit digits at M = 7) the grid is 2^8 coarser
+// and T's lowest weights are rounded to it. Only the centring (one fma per element)
+// uses the fp64 units. C is [i][o] and R [o][i]: a CTA turns a tile of 32 o × 128 i
+// through shared memory, each thread then writing 4 consecutive i of 4 rows o (int4
+// sums in, float4 out). Grid (d_out/32, d_in/128, maps), 32 x 8 threads; d_in % 128 == 0.
+constexpr int kCombI = 128;
 __global__ void __launch_bounds__(256) k_oz_combine(const double* __restrict__ C, const double* __restrict__ mu_x,
                                                     const double* __restrict__ mu_y, const double* __restrict__ n,
                                                     const double* __restrict__ sA, const double* __restrict__ sH,
                                                     const int32_t* __restrict__ J, size_t plane, int d_in, int d_out,
-                                                    const int* __restrict__ m_max, float* __restrict__ R32) {
-  __shared__ double t[32][33];
-  const int o0 = blockIdx.x * 32, i0 = blockIdx.y * 32, p = blockIdx.z;
-  const double nn = *n;
-  const int mm = *m_max;
-  const double* Cp = C + static_cast<size_t>(p) * d_in * d_out;
-  const double* my = mu_y + static_cast<size_t>(p) * d_out;
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int i = i0 + r, o = o0 + threadIdx.x;
-    t[r][threadIdx.x] = Cp[static_cast<size_t>(i) * d_out + o] - nn * mu_x[i] * my[o];
-  }
+                                                    int bits, const int* __restrict__ m_max, float* __restrict__ R32) {
+  __shared__ __align__(16) double t[32][kCombI + 2];  // [o][i], rows 16-byte aligned
+  __shared__ double u[kCombI];                         // n μ_x over the tile's i
+  const int o0 = blockIdx.x * 32, i0 = blockIdx.y * kCombI, p = blockIdx.z;
+  const int tx = threadIdx.x, ty = threadIdx.y, tid = ty * 32 + tx;
+  const int mm = *m_max, mid = min(mm, 4);
+  const int g = (bits == 8 && mm == 7) ? 8 : 0;  // grid coarsening (see above)
+  if (tid < kCombI) u[tid] = *n * mu_x[i0 + tid];
   __syncthreads();
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int o = o0 + r, i = i0 + threadIdx.x;
-    const size_t e = (static_cast<size_t>(p) * d_out + o) * d_in + i;
-    long long T = 0;
-    for (int w = 0; w + 2 <= mm; ++w) T = T * (1 << kOzBits) + J[w * plane + e];  // weights m = 2, 3, ..., M
-    const int k = pow2_exponent(sA[static_cast<size_t>(p) * d_out + o]) + pow2_exponent(sH[i]) - kOzBits * mm;
-    R32[e] = static_cast<float>(t[threadIdx.x][r] - scale_pow2(static_cast<double>(T), k));
+  const double* Cp = C + static_cast<size_t>(p) * d_in * d_out;
+  const double my = mu_y[static_cast<size_t>(p) * d_out + o0 + tx];
+#pragma unroll 4
+  for (int r = ty; r < kCombI; r += 8)
+    t[tx][r] = fma(-u[r], my, __ldcs(Cp + static_cast<size_t>(i0 + r) * d_out + o0 + tx));
+  __syncthreads();
+  int eh[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) eh[q] = pow2_exponent(sH[i0 + 4 * tx + q]);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int oo = ty + 8 * j, o = o0 + oo;
+    const size_t e = (static_cast<size_t>(p) * d_out + o) * d_in + i0 + 4 * tx;
+    // every planned weight's sums loaded before any is used (the weights above the
+    // plan read as 0 and are skipped below)
+    int4 v[kOzDigits];
+#pragma unroll
+    for (int w = 0; w < kOzDigits; ++w)
+      v[w] = w + 2 <= mm ? __ldcs(reinterpret_cast<const int4*>(J + w * plane + e)) : make_int4(0, 0, 0, 0);
+    long long T1[4] = {0, 0, 0, 0}, T2[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int w = 0; w < kOzDigits; ++w) {
+      const int m = w + 2;
+      if (m > mm) break;
+      const int x[4] = {v[w].x, v[w].y, v[w].z, v[w].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (m <= mid) T1[q] = T1[q] * (1ll << bits) + x[q];
+        else T2[q] = T2[q] * (1ll << bits) + x[q];
+      }
+    }
+    const int ea = pow2_exponent(sA[static_cast<size_t>(p) * d_out + o]) - bits * mm + g;
+    const double2 c01 = *reinterpret_cast<const double2*>(&t[oo][4 * tx]);
+    const double2 c23 = *reinterpret_cast<const double2*>(&t[oo][4 * tx + 2]);
+    const double cc[4] = {c01.x, c01.y, c23.x, c23.y};
+    float r[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int k = ea + eh[q];  // the grid 2^k
+      // T on the grid: T1 2^(b(M−mid) − g) + round(T2 / 2^g)
+      const long long tg = T1[q] * (1ll << (bits * (mm - mid) - g)) + (g ? (T2[q] + (1ll << (g - 1))) >> g : T2[q]);
+      const long long d = static_cast<long long>(static_cast<unsigned long long>(to_grid(cc[q], k)) -
+                                                 static_cast<unsigned long long>(tg));
+      r[q] = ldexpf(ll_to_float(d), k);
+    }
+    __stcs(reinterpret_cast<float4*>(R32 + e), make_float4(r[0], r[1], r[2], r[3]));
   }
 }
 
@@ -836,7 +946,8 @@ struct OzakiProb {
   int32_t* J;        // [maps][d_out][d_in] this weight's exact sums J_m
   const int* m_max;  // device: the largest weight the refinement needs (weights above it run no unit)
   int maps, plane_maps, d_out, d_in, m_tiles, n_tiles, n_chunks;  // maps in this launch; maps per digit plane
-  int m;  // the digit weight s + t of this launch (pairs s = 1 .. m−1)
+  int chunk;  // K chunk (oz_chunk): each chunk's sum is exact in the fp32 accumulator
+  int m;      // the digit weight s + t of this launch (pairs s = 1 .. m−1)
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = false;
@@ -863,7 +974,7 @@ struct OzakiProb {
   }
   __device__ int num_kb(int, int sb) const {
     const int c = sb % n_chunks;
-    return (min(kOzChunk, d_in - c * kOzChunk) + kBK - 1) / kBK;
+    return (min(chunk, d_in - c * chunk) + kBK - 1) / kBK;
   }
   struct Coords {
     int a_row, b_row, k0;
@@ -874,7 +985,7 @@ struct OzakiProb {
     const int s = sb / n_chunks + 1, c = sb % n_chunks;
     const int t = m - s;
     return {((s - 1) * plane_maps + p) * d_out + mt * Cfg::kUnitM + static_cast<int>(rank) * kBM,
-            (t - 1) * d_in + nt * kBN + static_cast<int>(rank) * Cfg::kBRows, c * kOzChunk};
+            (t - 1) * d_in + nt * kBN + static_cast<int>(rank) * Cfg::kBRows, c * chunk};
   }
   __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
     load_operand<kBM, false, kPair>(sa, &tmA, bar, c.k0 + kb * kBK, c.a_row);
@@ -909,16 +1020,26 @@ struct OzakiProb {
 // --------------------------------------------------------------------------
 // How much refinement arithmetic the conditioning calls for. κ(H) is estimated as
 // λmax(H)·λmax(H^-1), each by power iteration (H read as fp32 from its fp64 copy,
-// H^-1 in fp32); the Rayleigh quotients approach from below, so the estimate is
-// taken 4 times over. A sweep's correction R H^-1 moves A by |R||H^-1|, so to
-// bring A to fp32 accuracy (2^-24) the residual must be good to about
-// 2^-(25 + log2 κ) of Σ|A||H|, and the correction product's own relative error
-// times κ must stay well below 1. With 7-bit digits and the pairs s + t <= n + 1
-// kept, n digits give about (n+1)·2^(-7n-2): 2^-27.7 at n = 4, 2^-34.4 at n = 5,
-// 2^-41.2 at n = 6 (all six, the most there are); the first three split terms of
-// the correction give about 2^-16, all six about 2^-24.
+// H^-1 in fp32). The Rayleigh quotients approach from below: after k steps from a
+// start vector holding a share w of the top eigenvector, the worst spectrum (the
+// rest at the ratio ρ where ρ^(2k) (1−w)/w is a few) leaves a quotient of at least
+// 0.79 of its eigenvalue for k = 24, d <= 32768 and w 100 times below a random
+// vector's 1/d, so twice the product of the two is above κ. A sweep's correction
+// R H^-1 moves A by |R||H^-1|, so to bring A to fp32 accuracy (2^-24) the residual
+// must be good to about 2^-(25 + log2 κ) of Σ|A||H|, and the correction product's
+// own relative error times κ must stay well below 1. With b-bit digits and the pairs
+// s + t <= n + 1 kept, n digits give (n+1)/4 · 2^(−bn): for b = 8, 2^-31.7 at n = 4,
+// 2^-39.4 at n = 5, 2^-47.2 at n = 6 (all six, the most there are); for b = 7,
+// 2^-27.7, 2^-34.4 and 2^-41.2. The first three split terms of the correction give
+// about 2^-16, all six about 2^-24.
 // --------------------------------------------------------------------------
-constexpr int kPowerSteps = 12;
+constexpr int kPowerSteps = 24;
+constexpr double kKappaMargin = 2.0;
+
+// log2 of the inverse worst-case residual error with n digits of b bits.
+__device__ __forceinline__ double oz_precision_bits(int n, int bits) {
+  return static_cast<double>(bits) * n + 2.0 - log2(static_cast<double>(n + 1));
+}
 
 // x_m = a fixed ±1/sqrt(d) vector (signs from a multiplicative hash) for m = 0, 1.
 __global__ void k_pow_init(float* __restrict__ x, int d) {
@@ -927,78 +1048,94 @@ __global__ void k_pow_init(float* __restrict__ x, int d) {
     x[i] = ((static_cast<unsigned>(i % d) * 2654435761u) >> 31) ? -v : v;
 }
 
-// y_0 = H x_0 (H fp64, summed in fp32), y_1 = H^-1 x_1: one warp per row, grid
-// (ceil(d/8), 2) of 256 threads.
-__global__ void __launch_bounds__(256) k_pow_matvec(const double* __restrict__ H, const float* __restrict__ Hinv, int d,
-                                                    const float* __restrict__ x, float* __restrict__ y) {
-  const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31, m = blockIdx.y;
-  if (r >= d) return;
+// Hf = H as fp32 (the power iteration's copy; 8 bytes a step read instead of 12).
+// n % 2 == 0, both 16-byte aligned.
+__global__ void __launch_bounds__(256) k_to_f32(const double2* __restrict__ H, long long n2, float2* __restrict__ Hf) {
+  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n2; i += static_cast<long long>(gridDim.x) * 256) {
+    const double2 v = H[i];
+    Hf[i] = make_float2(static_cast<float>(v.x), static_cast<float>(v.y));
+  }
+}
+
+// Sum of squares of x[0 .. d) over the CTA (d % 4 == 0, x 16-byte aligned),
+// returned to every thread.
+__device__ __forceinline__ double block_sumsq(const float* __restrict__ x, int d, double* red) {
+  double s = 0.0;
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
+    const float4 v = x4[i];
+    s += static_cast<double>(v.x) * v.x + static_cast<double>(v.y) * v.y + static_cast<double>(v.z) * v.z +
+         static_cast<double>(v.w) * v.w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[w] = s;
+  __syncthreads();
+  double t = 0.0;
+  for (int k = 0; k < nw; ++k) t += red[k];
+  return t;
+}
+
+// One power step on both matrices: y_m = M_m x_m / ‖x_m‖ (M_0 = H in fp32, M_1 = H^-1),
+// so the next step's input needs no separate normalisation. One warp per row, grid
+// (d/8, 2) of 256 threads; every CTA takes ‖x_m‖ over the whole vector itself.
+__global__ void __launch_bounds__(256) k_pow_step(const float* __restrict__ Hf, const float* __restrict__ Hinv, int d,
+                                                  const float* __restrict__ x, float* __restrict__ y) {
+  __shared__ double red[8];
+  const int m = blockIdx.y, r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const float* xv = x + static_cast<size_t>(m) * d;
+  const double ss = block_sumsq(xv, d, red);
+  if (r >= d) return;
+  const float4* row = reinterpret_cast<const float4*>((m == 0 ? Hf : Hinv) + static_cast<size_t>(r) * d);
+  const float4* x4 = reinterpret_cast<const float4*>(xv);
   float acc = 0.f;
-  if (m == 0) {
-    const double* row = H + static_cast<size_t>(r) * d;
-    for (int c = lane; c < d; c += 32) acc = fmaf(static_cast<float>(row[c]), xv[c], acc);
-  } else {
-    const float* row = Hinv + static_cast<size_t>(r) * d;
-    for (int c = lane; c < d; c += 32) acc = fmaf(row[c], xv[c], acc);
+  for (int c = lane; c < d / 4; c += 32) {
+    const float4 a = row[c], b = x4[c];
+    acc = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) y[static_cast<size_t>(m) * d + r] = acc;
+  if (lane == 0) y[static_cast<size_t>(m) * d + r] = static_cast<float>(acc * (ss > 0.0 ? rsqrt(ss) : 0.0));
 }
 
-// est[m] = x_mᵀ y_m (x_m has unit norm: the Rayleigh quotient), then x_m = y_m / ‖y_m‖.
-// One CTA of 1024 threads per matrix.
-__global__ void __launch_bounds__(1024) k_pow_norm(float* __restrict__ x, const float* __restrict__ y, int d,
-                                                   float* __restrict__ est) {
-  __shared__ double part[2][32];
-  const int m = blockIdx.x, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  float* xv = x + static_cast<size_t>(m) * d;
+// est[m] = the Rayleigh quotient of x_m / ‖x_m‖ with y_m = M_m x_m / ‖x_m‖ (the last
+// step's input and output): x_mᵀ y_m / ‖x_m‖. One CTA of 256 threads per matrix.
+__global__ void __launch_bounds__(256) k_pow_est(const float* __restrict__ x, const float* __restrict__ y, int d,
+                                                 float* __restrict__ est) {
+  __shared__ double red[8];
+  const int m = blockIdx.x;
+  const float* xv = x + static_cast<size_t>(m) * d;
   const float* yv = y + static_cast<size_t>(m) * d;
-  double xy = 0.0, yy = 0.0;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    xy += static_cast<double>(xv[i]) * yv[i];
-    yy += static_cast<double>(yv[i]) * yv[i];
-  }
+  const double ss = block_sumsq(xv, d, red);
+  __syncthreads();  // red is reused below
+  double xy = 0.0;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) xy += static_cast<double>(xv[i]) * yv[i];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    xy += __shfl_xor_sync(0xffffffffu, xy, o);
-    yy += __shfl_xor_sync(0xffffffffu, yy, o);
-  }
-  if (lane == 0) {
-    part[0][w] = xy;
-    part[1][w] = yy;
-  }
+  for (int o = 16; o > 0; o >>= 1) xy += __shfl_xor_sync(0xffffffffu, xy, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = xy;
   __syncthreads();
-  if (w == 0) {
-    xy = part[0][lane];
-    yy = part[1][lane];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      xy += __shfl_xor_sync(0xffffffffu, xy, o);
-      yy += __shfl_xor_sync(0xffffffffu, yy, o);
-    }
-    if (lane == 0) {
-      part[0][0] = xy;
-      part[1][0] = yy;
-    }
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int k = 0; k < 8; ++k) t += red[k];
+    est[m] = static_cast<float>(ss > 0.0 ? t * rsqrt(ss) : 0.0);
   }
-  __syncthreads();
-  const double inv = part[1][0] > 0.0 ? rsqrt(part[1][0]) : 0.0;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) xv[i] = static_cast<float>(yv[i] * inv);
-  if (threadIdx.x == 0) est[m] = static_cast<float>(part[0][0]);
 }
 
 // plan[0] = the largest digit weight the residual keeps (n + 1), plan[1] = the
 // correction's split terms (see above). A non-finite estimate keeps everything.
-__global__ void k_refine_plan(const float* __restrict__ est, int* __restrict__ plan) {
-  const double kappa = 4.0 * static_cast<double>(est[0]) * static_cast<double>(est[1]);
-  const double bits = 25.0 + log2(fmax(kappa, 1.0));
+__global__ void k_refine_plan(const float* __restrict__ est, int bits, int* __restrict__ plan) {
+  const double prod = static_cast<double>(est[0]) * static_cast<double>(est[1]);
+  const double need = 25.0 + log2(fmax(kKappaMargin * prod, 1.0));
   int n = kOzDigits;
-  if (bits <= 27.5) n = 4;
-  else if (bits <= 34.0) n = 5;
+  for (int k = 4; k < kOzDigits; ++k)
+    if (oz_precision_bits(k, bits) >= need) {
+      n = k;
+      break;
+    }
   plan[0] = n + 1;
-  plan[1] = kappa <= 1024.0 ? 3 : 6;
+  // the correction's band is kept where twelve steps and a margin of 4 put it
+  plan[1] = 4.0 * prod <= 1024.0 ? 3 : 6;
 }
 
 static int split_point(int n) { return std::max(kSolveBlock, (n / 2) / kSolveBlock * kSolveBlock); }
@@ -1061,12 +1198,13 @@ static SolveLayout solve_layout(const rf_calib_desc* d, void* ws) {
 // R_p = Cc_pᵀ − A_p H for every map, fp64-accurate (OzakiProb), into R32 [P][d_out][d_in].
 template <bool kPair>
 static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* C, const float* A, int P, int di,
-                             int dout, float* R32) {
+                             int dout, int bits, float* R32) {
   // the weights above lay.plan[0] run no unit and the combine leaves them out
   using Cfg = GemmCfg<kPair>;
   rf_status st;
   const unsigned hb = static_cast<unsigned>((static_cast<long long>(di) * 32 + 255) / 256);
-  k_oz_digits_f64<<<hb, 256, 0, c.s>>>(lay.H64, di, di, di, lay.ozH, lay.sH);
+  const int chunk = oz_chunk(bits);
+  k_oz_digits_f64<<<hb, 256, 0, c.s>>>(lay.H64, di, di, di, bits, lay.plan, lay.ozH, lay.sH);
   OzakiProb<kPair> pr;
   const int om = std::min(P, kOzMaps);
   if ((st = make_tmap_bf16_2d(&pr.tmA, lay.ozA, di, static_cast<uint64_t>(kOzDigits) * om * dout, di, kBK, kBM)) !=
@@ -1079,7 +1217,8 @@ static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* 
   pr.d_in = di;
   pr.m_tiles = dout / Cfg::kUnitM;
   pr.n_tiles = di / kBN;
-  pr.n_chunks = (di + kOzChunk - 1) / kOzChunk;
+  pr.chunk = chunk;
+  pr.n_chunks = (di + chunk - 1) / chunk;
   pr.m_max = lay.plan;
   pr.dev_status = c.dev_status;
   pr.timeout_ns = wait_timeout_ns();
@@ -1089,7 +1228,7 @@ static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* 
     // digits of the group's rows: the planes hold `om` maps per digit; a short last
     // group leaves the rest unused (its units are not launched)
     const unsigned gb = static_cast<unsigned>((static_cast<long long>(g) * dout * 32 + 255) / 256);
-    k_oz_digits_f32<<<gb, 256, 0, c.s>>>(A + off, g * dout, om * dout, di, lay.ozA, lay.sA);
+    k_oz_digits_f32<<<gb, 256, 0, c.s>>>(A + off, g * dout, om * dout, di, bits, lay.plan, lay.ozA, lay.sA);
     if ((st = cuda_check(cudaGetLastError(), "residual digit launch")) != RF_OK) return st;
     pr.maps = g;
     pr.plane_maps = om;
@@ -1103,9 +1242,9 @@ static rf_status oz_residual(SolveCtx& c, const SolveLayout& lay, const double* 
                             "residual GEMM launch")) != RF_OK)
         return st;
     }
-    k_oz_combine<<<dim3(dout / 32, di / 32, g), dim3(32, 8), 0, c.s>>>(
+    k_oz_combine<<<dim3(dout / 32, di / kCombI, g), dim3(32, 8), 0, c.s>>>(
         C + off, lay.mu_x, lay.mu_y + static_cast<size_t>(p0) * dout, lay.n, lay.sA, lay.sH, lay.J, plane, di, dout,
-        lay.plan, R32 + off);
+        bits, lay.plan, R32 + off);
     if ((st = cuda_check(cudaGetLastError(), "residual combine launch")) != RF_OK) return st;
   }
   return RF_OK;
@@ -1238,21 +1377,29 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
         RF_OK)
       return s;
   }
+  const int oz_bits = (desc->flags & RF_SOLVE_DIGITS7) ? 7 : rf::oz_bits(di);
   if (refine_iters > 0) {
     // the refinement's precision from the conditioning (see k_refine_plan), once
     ProfScope pr(c.s, RF_STAGE_SOLVE_REFINE);
+    // H in fp32 into L's storage (free once H^-1 exists), then the steps, ping-ponging
+    // between the two halves of pvec
+    const long long n2 = static_cast<long long>(di) * di / 2;
+    k_to_f32<<<eb, 256, 0, c.s>>>(reinterpret_cast<const double2*>(lay.H64), n2, reinterpret_cast<float2*>(lay.L));
     k_pow_init<<<(2 * di + 255) / 256, 256, 0, c.s>>>(lay.pvec, di);
+    float* xs = lay.pvec;
+    float* ys = lay.pvec + 2 * di;
     for (int k = 0; k < kPowerSteps; ++k) {
-      k_pow_matvec<<<dim3((di + 7) / 8, 2), 256, 0, c.s>>>(lay.H64, lay.Hinv, di, lay.pvec, lay.pvec + 2 * di);
-      k_pow_norm<<<2, 1024, 0, c.s>>>(lay.pvec, lay.pvec + 2 * di, di, lay.est);
+      k_pow_step<<<dim3((di + 7) / 8, 2), 256, 0, c.s>>>(lay.L, lay.Hinv, di, xs, ys);
+      if (k + 1 < kPowerSteps) std::swap(xs, ys);
     }
-    k_refine_plan<<<1, 1, 0, c.s>>>(lay.est, lay.plan);
+    k_pow_est<<<2, 256, 0, c.s>>>(xs, ys, di, lay.est);
+    k_refine_plan<<<1, 1, 0, c.s>>>(lay.est, oz_bits, lay.plan);
     if ((s = cuda_check(cudaGetLastError(), "refinement plan launches")) != RF_OK) return s;
   }
   for (int it = 0; it < refine_iters; ++it) {
     ProfScope pr(c.s, RF_STAGE_SOLVE_REFINE);
-    s = use_pair(desc->flags, true) ? oz_residual<true>(c, lay, st->C, A, P, di, dout, lay.work)
-                                    : oz_residual<false>(c, lay, st->C, A, P, di, dout, lay.work);
+    s = use_pair(desc->flags, true) ? oz_residual<true>(c, lay, st->C, A, P, di, dout, oz_bits, lay.work)
+                                    : oz_residual<false>(c, lay, st->C, A, P, di, dout, oz_bits, lay.work);
     if (s != RF_OK) return s;
     // ΔA = R H^-1 into the residual's own buffer (split into planes_a first, so free),
     // then A += ΔA in one coalesced pass: an in-epilogue read-modify-write of A (one

@@ -233,6 +233,17 @@ def test_layered_fill_workspace_and_host_checks():
     assert ei.value.status == rf.RF_ERR_INVALID_ARG and "row_scale" in rf.rf_last_error()
 
 
+def test_flag_and_mode_constants_match_header():
+    txt = open(os.path.join(ROOT, "include", "rf.h")).read()
+    defs = dict(re.findall(r"#define (RF_(?:FLAG|WEIGHTS|SOLVE|MAPS)_\w+) (\d+)u?\b", txt))
+    assert {"RF_FLAG_SINGLE_CTA", "RF_FLAG_CTA_PAIR", "RF_WEIGHTS_PREFOLDED", "RF_SOLVE_DIGITS7",
+            "RF_MAPS_BF16", "RF_MAPS_INT8"} <= set(defs)
+    for name, val in defs.items():
+        assert getattr(rf, name) == int(val), name
+    flags = [int(defs[n]) for n in defs if not n.startswith("RF_MAPS_")]
+    assert all(f & (f - 1) == 0 for f in flags) and len(set(flags)) == len(flags)   # distinct single bits
+
+
 def test_static_fill_scratch_constant_matches_header():
     txt = open(os.path.join(ROOT, "include", "rf.h")).read()
     assert "RF_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)" in txt

@@ -188,8 +188,8 @@ def _upload_stats(ref):
             "n": torch.tensor([ref["n"]], dtype=torch.int64, device=DEV)}
 
 
-def _solve(st, d_in, d_out, P, lam, mode=rf.RF_ALPHA_TRACE, refine=1):
-    desc = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P)
+def _solve(st, d_in, d_out, P, lam, mode=rf.RF_ALPHA_TRACE, refine=1, flags=0):
+    desc = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P, flags=flags)
     A = torch.empty((P, d_out, d_in), dtype=torch.float32, device=DEV)
     b = torch.empty((P, d_out), dtype=torch.float32, device=DEV)
     Ab = torch.empty((P, d_out, d_in), dtype=torch.bfloat16, device=DEV)
@@ -247,45 +247,50 @@ def test_gpu_calibration_then_solve_recovers_planted_maps():
         assert _rel(A[p], At[p]) <= 0.05
 
 
-def test_solve_refinement_restores_accuracy_when_ill_conditioned():
-    """κ(Gc) ≈ 1e4: the fp32 factorisation alone loses about κ·2^-24; one sweep with the
-    fp64-accurate residual (tensor-core digit products, exact integer chunk sums)
-    brings A back to fp32 accuracy. A residual accurate only to fp32 would not."""
-    d, P, n = 512, 2, 4096
-    rng = np.random.default_rng(21)
+def _conditioned_case(seed, n, decades):
+    """Planted maps on rows whose spectrum falls geometrically over ``decades``
+    (κ(Gc) about 10^(2·decades), times the sampling spread), λ = 1e-9: the oracle's
+    A and the sums, with κ(H) from the oracle's H."""
+    d, P = 512, 2
+    rng = np.random.default_rng(seed)
     Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
-    X = (rng.standard_normal((n, d)) * np.geomspace(1.0, 1e-2, d)) @ Q.T
+    X = (rng.standard_normal((n, d)) * np.geomspace(1.0, 10 ** -decades, d)) @ Q.T
     At = rng.standard_normal((P, d, d)) / math.sqrt(d)
     Y = np.einsum("pij,nj->pni", At, X) + 0.01 * rng.standard_normal((P, n, d))
     Xb = torch.as_tensor(X, dtype=torch.float32).to(torch.bfloat16)
     Yb = torch.as_tensor(Y, dtype=torch.float32).to(torch.bfloat16)
     ref = O.calib_stats(_f64(Xb), _f64(Yb))
     lam = 1e-9
-    Ar, _, _ = O.ridge_solve(ref, lam)
-    A0, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=0)
-    A1, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=1)
+    Ar, _, alpha = O.ridge_solve(ref, lam)
+    Gc, _, _, _ = O.centre_stats(ref)
+    ev = np.linalg.eigvalsh(Gc + alpha * np.eye(d))
+    return ref, Ar, lam, ev[-1] / ev[0], d, P
+
+
+DIGITS = pytest.mark.parametrize("flags", [0, rf.RF_SOLVE_DIGITS7], ids=["8-bit digits", "7-bit digits"])
+
+
+@DIGITS
+def test_solve_refinement_restores_accuracy_when_ill_conditioned(flags):
+    """κ(Gc) ≈ 1e4: the fp32 factorisation alone loses about κ·2^-24; one sweep with the
+    fp64-accurate residual (tensor-core digit products, exact integer chunk sums)
+    brings A back to fp32 accuracy. A residual accurate only to fp32 would not."""
+    ref, Ar, lam, kappa, d, P = _conditioned_case(21, 4096, 2.0)
+    A0, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=0, flags=flags)
+    A1, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=1, flags=flags)
     e0 = max(_rel(A0[p], Ar[p]) for p in range(P))
     e1 = max(_rel(A1[p], Ar[p]) for p in range(P))
     assert e0 > 1e-5, e0              # the case is hard enough to need refinement
     assert e1 <= 1e-5 and e1 < e0 / 20, (e0, e1)
 
 
-def test_solve_refinement_at_moderate_conditioning():
-    """κ(Gc) ≈ 90: the band where the library's plan keeps five residual digits and
-    three correction terms (its κ estimate, 4x over, stays under 2^9). One sweep must
-    still reach fp32-level accuracy (the residual's truncation, about κ·2^-34, and the
-    correction's, about κ²·2^-40, are both near 1e-8 or below here)."""
-    d, P, n = 512, 2, 4096
-    rng = np.random.default_rng(23)
-    Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
-    X = (rng.standard_normal((n, d)) * np.geomspace(1.0, 10 ** -0.9, d)) @ Q.T
-    At = rng.standard_normal((P, d, d)) / math.sqrt(d)
-    Y = np.einsum("pij,nj->pni", At, X) + 0.01 * rng.standard_normal((P, n, d))
-    Xb = torch.as_tensor(X, dtype=torch.float32).to(torch.bfloat16)
-    Yb = torch.as_tensor(Y, dtype=torch.float32).to(torch.bfloat16)
-    ref = O.calib_stats(_f64(Xb), _f64(Yb))
-    lam = 1e-9
-    Ar, _, _ = O.ridge_solve(ref, lam)
+def test_solve_refinement_in_the_four_digit_band():
+    """κ(H) below 51: every estimate of it is too (the Rayleigh quotients approach from
+    below), so the plan certainly keeps four 8-bit digits (10 digit pairs, a residual
+    within 2^-31.7 of Σ|A||H|) and three correction terms. One sweep must still reach
+    fp32-level accuracy (the residual's truncation times κ is about 1.4e-8 here)."""
+    ref, Ar, lam, kappa, d, P = _conditioned_case(24, 4096, 0.7)
+    assert 20 < kappa < 51, kappa
     A0, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=0)
     A1, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=1)
     e0 = max(_rel(A0[p], Ar[p]) for p in range(P))
@@ -293,26 +298,33 @@ def test_solve_refinement_at_moderate_conditioning():
     assert e1 <= 1e-6 and e1 <= e0, (e0, e1)
 
 
-def test_solve_repeated_refinement_converges_when_badly_conditioned():
+@DIGITS
+def test_solve_refinement_at_moderate_conditioning(flags):
+    """κ(Gc) ≈ 90: with 8-bit digits the band where the plan keeps five digits (15
+    pairs, 2^-39.4) and three correction terms; with 7-bit digits it keeps five as
+    well (2^-34.4). One sweep must still reach fp32-level accuracy (the residual's
+    truncation times κ, and the correction's error, about κ²·2^-40, are near 1e-8
+    or below here)."""
+    ref, Ar, lam, kappa, d, P = _conditioned_case(23, 4096, 0.9)
+    A0, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=0, flags=flags)
+    A1, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=1, flags=flags)
+    e0 = max(_rel(A0[p], Ar[p]) for p in range(P))
+    e1 = max(_rel(A1[p], Ar[p]) for p in range(P))
+    assert e1 <= 1e-6 and e1 <= e0, (e0, e1)
+
+
+@DIGITS
+def test_solve_repeated_refinement_converges_when_badly_conditioned(flags):
     """κ(Gc) ≈ 1e5: the fp32 solve alone is off by about κ·2^-24 and each sweep shrinks
     the error by about that factor again, down to the residual's own accuracy or the
     fp32 rounding of A (about 6e-8). Reaching 1e-6 needs the residual good to about
     1e-6/κ ≈ 2^-36 of its terms; an fp32-accurate residual would stall near the
-    unrefined error. (Measured on a GB300: 1.7e-3 unrefined, 5.4e-8 after four sweeps.)"""
-    d, P, n = 512, 2, 8192
-    rng = np.random.default_rng(22)
-    Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
-    X = (rng.standard_normal((n, d)) * np.geomspace(1.0, 10 ** -2.5, d)) @ Q.T
-    At = rng.standard_normal((P, d, d)) / math.sqrt(d)
-    Y = np.einsum("pij,nj->pni", At, X) + 0.01 * rng.standard_normal((P, n, d))
-    Xb = torch.as_tensor(X, dtype=torch.float32).to(torch.bfloat16)
-    Yb = torch.as_tensor(Y, dtype=torch.float32).to(torch.bfloat16)
-    ref = O.calib_stats(_f64(Xb), _f64(Yb))
-    lam = 1e-9
-    Ar, _, _ = O.ridge_solve(ref, lam)
+    unrefined error. (Measured on a GB300 with 7-bit digits: 1.7e-3 unrefined, 5.4e-8
+    after four sweeps.)"""
+    ref, Ar, lam, kappa, d, P = _conditioned_case(22, 8192, 2.5)
     errs = {}
     for refine in (0, 4):
-        A, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=refine)
+        A, _, _, _ = _solve(_upload_stats(ref), d, d, P, lam, refine=refine, flags=flags)
         errs[refine] = max(_rel(A[p], Ar[p]) for p in range(P))
     assert errs[0] > 1e-4, errs   # hard enough that fp32 alone is far off
     assert errs[4] <= 1e-6 and errs[4] < errs[0] / 1000, errs
