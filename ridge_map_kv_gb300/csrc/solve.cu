@@ -1078,25 +1078,62 @@ __device__ __forceinline__ double block_sumsq(const float* __restrict__ x, int d
 }
 
 // One power step on both matrices: y_m = M_m x_m / ‖x_m‖ (M_0 = H in fp32, M_1 = H^-1),
-// so the next step's input needs no separate normalisation. One warp per row, grid
-// (d/8, 2) of 256 threads; every CTA takes ‖x_m‖ over the whole vector itself.
+// so the next step's input needs no separate normalisation. A CTA of 8 warps takes
+// 16 rows of one matrix (two a warp, summed side by side); x passes through shared
+// memory in chunks of 2,048, and ‖x‖ is summed from the chunks on the way. Grid
+// (d/16, 2) of 256 threads; d % 256 == 0.
+constexpr int kPowRows = 16, kPowChunk = 2048;
 __global__ void __launch_bounds__(256) k_pow_step(const float* __restrict__ Hf, const float* __restrict__ Hinv, int d,
                                                   const float* __restrict__ x, float* __restrict__ y) {
+  __shared__ __align__(16) float xs[kPowChunk];
   __shared__ double red[8];
-  const int m = blockIdx.y, r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int m = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = blockIdx.x * kPowRows + 2 * warp;
   const float* xv = x + static_cast<size_t>(m) * d;
-  const double ss = block_sumsq(xv, d, red);
-  if (r >= d) return;
-  const float4* row = reinterpret_cast<const float4*>((m == 0 ? Hf : Hinv) + static_cast<size_t>(r) * d);
-  const float4* x4 = reinterpret_cast<const float4*>(xv);
-  float acc = 0.f;
-  for (int c = lane; c < d / 4; c += 32) {
-    const float4 a = row[c], b = x4[c];
-    acc = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
+  const float* M = (m == 0 ? Hf : Hinv);
+  const float4* row0 = reinterpret_cast<const float4*>(M + static_cast<size_t>(r0) * d);
+  const float4* row1 = reinterpret_cast<const float4*>(M + static_cast<size_t>(r0 + 1) * d);
+  double ss = 0.0;
+  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+  for (int c0 = 0; c0 < d; c0 += kPowChunk) {
+    const int len = min(kPowChunk, d - c0);
+    __syncthreads();  // the previous chunk is consumed
+    for (int i = threadIdx.x; i < len / 4; i += 256) {
+      const float4 v = reinterpret_cast<const float4*>(xv + c0)[i];
+      reinterpret_cast<float4*>(xs)[i] = v;
+      ss += static_cast<double>(v.x) * v.x + static_cast<double>(v.y) * v.y + static_cast<double>(v.z) * v.z +
+            static_cast<double>(v.w) * v.w;
+    }
+    __syncthreads();
+    const float4* x4 = reinterpret_cast<const float4*>(xs);
+    const int base = c0 / 4;
+#pragma unroll 4
+    for (int c = lane; c < len / 4; c += 32) {
+      const float4 p = row0[base + c], q = row1[base + c], v = x4[c];
+      a0 = fmaf(p.x, v.x, fmaf(p.y, v.y, a0));
+      a1 = fmaf(p.z, v.z, fmaf(p.w, v.w, a1));
+      b0 = fmaf(q.x, v.x, fmaf(q.y, v.y, b0));
+      b1 = fmaf(q.z, v.z, fmaf(q.w, v.w, b1));
+    }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) y[static_cast<size_t>(m) * d + r] = static_cast<float>(acc * (ss > 0.0 ? rsqrt(ss) : 0.0));
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) red[warp] = ss;
+  float s0 = a0 + a1, s1 = b0 + b1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+  }
+  __syncthreads();
+  double tot = 0.0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) tot += red[k];
+  const float inv = static_cast<float>(tot > 0.0 ? rsqrt(tot) : 0.0);
+  if (lane == 0) {
+    y[static_cast<size_t>(m) * d + r0] = s0 * inv;
+    y[static_cast<size_t>(m) * d + r0 + 1] = s1 * inv;
+  }
 }
 
 // est[m] = the Rayleigh quotient of x_m / ‖x_m‖ with y_m = M_m x_m / ‖x_m‖ (the last
@@ -1389,7 +1426,7 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
     float* xs = lay.pvec;
     float* ys = lay.pvec + 2 * di;
     for (int k = 0; k < kPowerSteps; ++k) {
-      k_pow_step<<<dim3((di + 7) / 8, 2), 256, 0, c.s>>>(lay.L, lay.Hinv, di, xs, ys);
+      k_pow_step<<<dim3(di / kPowRows, 2), 256, 0, c.s>>>(lay.L, lay.Hinv, di, xs, ys);
       if (k + 1 < kPowerSteps) std::swap(xs, ys);
     }
     k_pow_est<<<2, 256, 0, c.s>>>(xs, ys, di, lay.est);
