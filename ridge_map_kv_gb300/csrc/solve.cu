@@ -174,34 +174,51 @@ constexpr size_t kBlkSmem = sizeof(float) * kSolveBlock * kBlkLd;
 
 // W = L^-1 for the 128 x 128 SPD block A = L Lᵀ, one CTA (8 or 16 warps) per matrix b
 // (A + b*sA, W + b*sW), in shared memory and blocked by 8 so that a column or row
-// block costs a few barriers instead of one per column:
+// block costs two barriers instead of one per column:
 //   factor, per 8-column block k0: one thread per row below the diagonal block
 //     solves its 8 panel entries against it (multiplying by the pivots'
-//     reciprocals); then warp 0 applies that panel's rank-8 update to the next
-//     diagonal block and factors it in registers (lanes own rows, columns
-//     exchanged by shuffles), while the other warps update the rows below it
-//     (warp w takes rows w−1, w−1 + (warps − 1), ..., lanes the columns): two
-//     barriers a block, and the serial factorisation off the critical path;
+//     reciprocals) and also writes them to an aligned copy of the panel; then warp 0
+//     applies that panel's rank-8 update to the next diagonal block (two entries a
+//     lane) and factors it (every lane the whole block in registers: no shuffles on
+//     the chain of pivots), while the other warps update the rows below it, two rows
+//     and two columns a step, each element from two 16-byte loads of the panel copy
+//     (two float4 arrays, read without bank conflicts);
 //   invert, per 8-row block i0 (rows above already hold W):
-//     T = L[i0 block][0:i0] W[0:i0][0:i0]  (all threads), and meanwhile warp 0
-//     inverts the diagonal block (lane c forms column c by forward substitution);
-//     then W[i0 block][0:i0] = −W_ii T and W_ii replaces L_ii.
-// A is only read; W's upper triangle is zero. A non-positive pivot records
-// RF_ERR_NOT_SPD and continues with 1.
+//     T = L[i0 block][0:i0] W[0:i0][0:i0] with those 8 rows of L staged transposed:
+//     a warp takes 32 columns and one of KQ interleaved ranges of k, all its lanes on
+//     the same k, so that the staged rows are read by broadcast; meanwhile the last
+//     warp inverts the diagonal block (lane c forms column c by forward
+//     substitution); then one thread per column adds the KQ partial sums and forms
+//     W[i0 block][c] = −W_ii T[:, c], W_ii replaces L_ii, and the next block's rows of
+//     L are staged.
+// The pivots' reciprocals are rsqrt with one Newton–Raphson step (relative error a
+// few units of the last place). A is only read; W's upper triangle is zero. A
+// non-positive pivot records RF_ERR_NOT_SPD and continues with 1.
 constexpr int kLeafN = 128;
 constexpr int kLeafB = 8;
-constexpr size_t kLeafSmem = kBlkSmem + sizeof(float) * (kLeafB * kLeafN + kLeafB * kLeafB + kLeafN);
+template <int kWarps>
+constexpr size_t leaf_smem() {  // S, the panel copy / T's KQ partials, the staged rows, W_ii, 1/L_jj
+  return kBlkSmem + sizeof(float) * ((kWarps / 4) * kLeafB * kLeafN + kLeafN * kLeafB + kLeafB * kLeafB + kLeafN);
+}
+static_assert(kBlkSmem % 16 == 0, "the panel copy must be 16-byte aligned");
 
 template <int kWarps>
 __global__ void __launch_bounds__(32 * kWarps) k_chol_inv_leaf(const float* __restrict__ A, long long lda, long long sA,
                                                                float* __restrict__ W, long long ldw, long long sW,
                                                                int32_t* dev_status) {
   constexpr int kThreads = 32 * kWarps;
-  extern __shared__ float S[];
-  float* Tb = S + kLeafN * kBlkLd;  // [8][128]
-  float* Wd = Tb + kLeafB * kLeafN;  // [8][8]
-  float* Dinv = Wd + kLeafB * kLeafB;  // [128] 1 / L_jj
-  constexpr int n = kLeafN;
+  constexpr int n = kLeafN, B = kLeafB;
+  constexpr int KQ = kWarps / 4;  // ranges of k in T (4 column blocks of 32)
+  static_assert(kWarps == 8 || kWarps == 16, "8 or 16 warps");
+  extern __shared__ __align__(16) float S[];
+  float* P = S + n * kBlkLd;    // the panel's rows as two [n] float4 arrays, entries 0-3 and 4-7
+                                // (factor); T's partials [KQ][B][n] (inversion)
+  float* Lt = P + KQ * B * n;   // [n][B]: Lt[k][r] = L[i0 + r][k] (inversion)
+  float* Wd = Lt + n * B;       // [B][B]: the diagonal block (factor), W_ii (inversion)
+  float* Dinv = Wd + B * B;     // [n] 1 / L_jj
+  const float4* Plo = reinterpret_cast<const float4*>(P);
+  const float4* Phi = Plo + n;
+  const float4* Lt4 = reinterpret_cast<const float4*>(Lt);
   A += blockIdx.x * sA;
   W += blockIdx.x * sW;
   const int lane = threadIdx.x, warp = threadIdx.y, tid = warp * 32 + lane;
@@ -209,110 +226,148 @@ __global__ void __launch_bounds__(32 * kWarps) k_chol_inv_leaf(const float* __re
     for (int k = lane; k < n; k += 32) S[i * kBlkLd + k] = A[i * lda + k];
   __syncthreads();
   // ---- factor
-  // Warp 0 factors the diagonal block at kd in registers (lane r < 8 holds row kd + r;
-  // lanes 8.. repeat lane 0 and store nothing). With `update` it first applies the
-  // previous panel's rank-8 update to the block, which the other warps skip.
+  // Warp 0 factors the diagonal block at kd. With `update` it first applies the
+  // previous panel's rank-8 update to the block (lane: entries (lane/8, lane%8) and
+  // (lane/8 + 4, lane%8)), which the other warps skip. Every lane then factors the
+  // whole block in registers; lane r < 8 stores row r and 1/L_rr.
   auto factor_diag = [&](int kd, bool update) {
-    const int rr = lane < kLeafB ? lane : 0;
-    float a[kLeafB];
-#pragma unroll
-    for (int c = 0; c < kLeafB; ++c) a[c] = S[(kd + rr) * kBlkLd + kd + c];
-    if (update) {
-      const int kp = kd - kLeafB;
-      float pr[kLeafB];
-#pragma unroll
-      for (int j = 0; j < kLeafB; ++j) pr[j] = S[(kd + rr) * kBlkLd + kp + j];
-#pragma unroll
-      for (int c = 0; c < kLeafB; ++c) {
-        float v = a[c];
-#pragma unroll
-        for (int j = 0; j < kLeafB; ++j) v = fmaf(-pr[j], S[(kd + c) * kBlkLd + kp + j], v);
-        a[c] = v;
+    {
+      const int c = lane & 7, r0 = lane >> 3, r1 = r0 + 4;
+      float v0 = S[(kd + r0) * kBlkLd + kd + c], v1 = S[(kd + r1) * kBlkLd + kd + c];
+      if (update) {
+        const float4 q0 = Plo[kd + c], q1 = Phi[kd + c];
+        const float4 a0 = Plo[kd + r0], a1 = Phi[kd + r0];
+        const float4 b0 = Plo[kd + r1], b1 = Phi[kd + r1];
+        v0 -= (a0.x * q0.x + a0.y * q0.y + a0.z * q0.z + a0.w * q0.w) +
+              (a1.x * q1.x + a1.y * q1.y + a1.z * q1.z + a1.w * q1.w);
+        v1 -= (b0.x * q0.x + b0.y * q0.y + b0.z * q0.z + b0.w * q0.w) +
+              (b1.x * q1.x + b1.y * q1.y + b1.z * q1.z + b1.w * q1.w);
       }
+      Wd[r0 * B + c] = v0;
+      Wd[r1 * B + c] = v1;
     }
-    float my_inv = 1.f;
+    __syncwarp();
+    float a[B][B];
 #pragma unroll
-    for (int j = 0; j < kLeafB; ++j) {
-      float d = __shfl_sync(0xffffffffu, a[j], j);
+    for (int r = 0; r < B; ++r)
+#pragma unroll
+      for (int c = 0; c <= r; ++c) a[r][c] = Wd[r * B + c];
+    __syncwarp();  // Wd is rewritten by the next call only after every lane has read it
+    float dinv[B];
+#pragma unroll
+    for (int j = 0; j < B; ++j) {
+      float d = a[j][j];
       if (!(d > 0.f)) {
         if (lane == 0) record_status(dev_status, RF_ERR_NOT_SPD);
         d = 1.f;
       }
-      const float sd = sqrtf(d), inv = __frcp_rn(sd);
-      if (rr == j) {
-        a[j] = sd;
-        my_inv = inv;
-      } else if (rr > j) {
-        a[j] *= inv;
-      }
+      float inv = rsqrtf(d);
+      inv = inv * fmaf(-0.5f * d * inv, inv, 1.5f);  // one Newton–Raphson step for d^-1/2
+      dinv[j] = inv;
+      a[j][j] = d * inv;
 #pragma unroll
-      for (int c = j + 1; c < kLeafB; ++c) {
-        const float lcj = __shfl_sync(0xffffffffu, a[j], c);
-        if (rr >= c) a[c] = fmaf(-a[j], lcj, a[c]);
-      }
-    }
-    if (lane < kLeafB) {
+      for (int r = j + 1; r < B; ++r) a[r][j] *= inv;
 #pragma unroll
-      for (int c = 0; c < kLeafB; ++c)
-        if (c <= lane) S[(kd + lane) * kBlkLd + kd + c] = a[c];
-      Dinv[kd + lane] = my_inv;
+      for (int c = j + 1; c < B; ++c)
+#pragma unroll
+        for (int r = c; r < B; ++r) a[r][c] = fmaf(-a[r][j], a[c][j], a[r][c]);
     }
+#pragma unroll
+    for (int r = 0; r < B; ++r)
+      if (lane == r) {
+#pragma unroll
+        for (int c = 0; c <= r; ++c) S[(kd + r) * kBlkLd + kd + c] = a[r][c];
+        Dinv[kd + r] = dinv[r];
+      }
   };
   if (warp == 0) factor_diag(0, false);
   __syncthreads();
-  for (int k0 = 0; k0 < n; k0 += kLeafB) {
-    // panel: row r solves x L_ddᵀ = S[r][k0..k0+7]
-    for (int r = k0 + kLeafB + tid; r < n; r += kThreads) {
-      float x[kLeafB];
+  for (int k0 = 0; k0 < n; k0 += B) {
+    // panel: row r solves x L_ddᵀ = S[r][k0..k0+7]; x into S and into the panel copy
+    for (int r = k0 + B + tid; r < n; r += kThreads) {
+      float x[B];
 #pragma unroll
-      for (int j = 0; j < kLeafB; ++j) {
+      for (int j = 0; j < B; ++j) {
         float v = S[r * kBlkLd + k0 + j];
 #pragma unroll
         for (int c = 0; c < j; ++c) v = fmaf(-x[c], S[(k0 + j) * kBlkLd + k0 + c], v);
         x[j] = v * Dinv[k0 + j];
       }
 #pragma unroll
-      for (int j = 0; j < kLeafB; ++j) S[r * kBlkLd + k0 + j] = x[j];
+      for (int j = 0; j < B; ++j) S[r * kBlkLd + k0 + j] = x[j];
+      float4* pl = reinterpret_cast<float4*>(P);
+      pl[r] = make_float4(x[0], x[1], x[2], x[3]);
+      pl[n + r] = make_float4(x[4], x[5], x[6], x[7]);
     }
     __syncthreads();
     if (warp == 0) {
       // look-ahead: the next diagonal block, updated and factored while the other
       // warps update the rows below it
-      if (k0 + kLeafB < n) factor_diag(k0 + kLeafB, true);
+      if (k0 + B < n) factor_diag(k0 + B, true);
     } else {
-      // trailing lower triangle below the next diagonal block, rank 8
-      for (int r = k0 + 2 * kLeafB + warp - 1; r < n; r += kWarps - 1) {
-        float a[kLeafB];
-#pragma unroll
-        for (int j = 0; j < kLeafB; ++j) a[j] = S[r * kBlkLd + k0 + j];
-        for (int c = k0 + kLeafB + lane; c <= r; c += 32) {
-          float v = S[r * kBlkLd + c];
-#pragma unroll
-          for (int j = 0; j < kLeafB; ++j) v = fmaf(-a[j], S[c * kBlkLd + k0 + j], v);
-          S[r * kBlkLd + c] = v;
+      // trailing lower triangle below the next diagonal block, rank 8: rows ra and
+      // rb = ra + (warps − 1) together, columns k0 + 8 .. r, two columns a step
+      constexpr int WU = kWarps - 1;
+      auto upd = [&](float* dst, const float4& a0, const float4& a1, const float4& q0, const float4& q1) {
+        float s0 = a0.x * q0.x, s1 = a0.y * q0.y;
+        s0 = fmaf(a0.z, q0.z, s0);
+        s1 = fmaf(a0.w, q0.w, s1);
+        s0 = fmaf(a1.x, q1.x, s0);
+        s1 = fmaf(a1.y, q1.y, s1);
+        s0 = fmaf(a1.z, q1.z, s0);
+        s1 = fmaf(a1.w, q1.w, s1);
+        *dst -= s0 + s1;
+      };
+      for (int ra = k0 + 2 * B + warp - 1; ra < n; ra += 2 * WU) {
+        const int rb = ra + WU;
+        const bool hb = rb < n;
+        const int rr = hb ? rb : ra;
+        const float4 a0 = Plo[ra], a1 = Phi[ra], b0 = Plo[rr], b1 = Phi[rr];
+        for (int c = k0 + B + lane; c <= rr; c += 64) {
+          const int c2 = c + 32;
+          const bool h2 = c2 <= rr;
+          const float4 q0 = Plo[c], q1 = Phi[c];
+          const float4 u0 = Plo[h2 ? c2 : c], u1 = Phi[h2 ? c2 : c];
+          if (c <= ra) upd(&S[ra * kBlkLd + c], a0, a1, q0, q1);
+          if (hb) upd(&S[rb * kBlkLd + c], b0, b1, q0, q1);
+          if (h2 && c2 <= ra) upd(&S[ra * kBlkLd + c2], a0, a1, u0, u1);
+          if (h2 && hb) upd(&S[rb * kBlkLd + c2], b0, b1, u0, u1);
         }
       }
     }
     __syncthreads();
   }
-  // ---- invert in place
-  for (int i0 = 0; i0 < n; i0 += kLeafB) {
-    for (int e = tid; e < kLeafB * i0; e += kThreads) {
-      const int r = e & (kLeafB - 1), c = e >> 3;
-      float s0 = 0.f, s1 = 0.f;
-      int k = c;
-      for (; k + 1 < i0; k += 2) {
-        s0 = fmaf(S[(i0 + r) * kBlkLd + k], S[k * kBlkLd + c], s0);
-        s1 = fmaf(S[(i0 + r) * kBlkLd + k + 1], S[(k + 1) * kBlkLd + c], s1);
-      }
-      if (k < i0) s0 = fmaf(S[(i0 + r) * kBlkLd + k], S[k * kBlkLd + c], s0);
-      Tb[r * kLeafN + c] = s0 + s1;
-    }
-    if (warp == 0 && lane < kLeafB) {
-      const int c = lane;
-      float col[kLeafB];
+  // ---- invert in place (block 0 stages nothing: T is empty there)
+  for (int i0 = 0; i0 < n; i0 += B) {
+    {
+      // T's partial sums: column c = 32 (warp % 4) + lane, k = kb + q, kb + q + KQ, ...
+      const int cb = warp & 3, q = warp >> 2, c = cb * 32 + lane, kb = cb * 32;
+      if (kb < i0) {
+        float acc[B];
 #pragma unroll
-      for (int r = 0; r < kLeafB; ++r) {
+        for (int r = 0; r < B; ++r) acc[r] = 0.f;
+#pragma unroll 2
+        for (int k = kb + q; k < i0; k += KQ) {
+          const float w = k >= c ? S[k * kBlkLd + c] : 0.f;  // W[k][c], lower triangle
+          const float4 l0 = Lt4[2 * k], l1 = Lt4[2 * k + 1];
+          acc[0] = fmaf(l0.x, w, acc[0]);
+          acc[1] = fmaf(l0.y, w, acc[1]);
+          acc[2] = fmaf(l0.z, w, acc[2]);
+          acc[3] = fmaf(l0.w, w, acc[3]);
+          acc[4] = fmaf(l1.x, w, acc[4]);
+          acc[5] = fmaf(l1.y, w, acc[5]);
+          acc[6] = fmaf(l1.z, w, acc[6]);
+          acc[7] = fmaf(l1.w, w, acc[7]);
+        }
+#pragma unroll
+        for (int r = 0; r < B; ++r) P[(q * B + r) * n + c] = acc[r];
+      }
+    }
+    if (warp == kWarps - 1 && lane < B) {
+      const int c = lane;
+      float col[B];
+#pragma unroll
+      for (int r = 0; r < B; ++r) {
         float v = (r == c) ? 1.f : 0.f;
 #pragma unroll
         for (int k = 0; k < r; ++k)
@@ -320,21 +375,36 @@ __global__ void __launch_bounds__(32 * kWarps) k_chol_inv_leaf(const float* __re
         col[r] = r >= c ? v * Dinv[i0 + r] : 0.f;
       }
 #pragma unroll
-      for (int r = 0; r < kLeafB; ++r) Wd[r * kLeafB + c] = col[r];
+      for (int r = 0; r < B; ++r) Wd[r * B + c] = col[r];
     }
     __syncthreads();
-    for (int e = tid; e < kLeafB * i0; e += kThreads) {
-      const int r = e & (kLeafB - 1), c = e >> 3;
-      float v = 0.f;
+    for (int c = tid; c < i0; c += kThreads) {
+      float t[B];
 #pragma unroll
-      for (int j = 0; j < kLeafB; ++j)
-        if (j <= r) v = fmaf(Wd[r * kLeafB + j], Tb[j * kLeafN + c], v);
-      S[(i0 + r) * kBlkLd + c] = -v;
+      for (int j = 0; j < B; ++j) {
+        float v = P[j * n + c];
+#pragma unroll
+        for (int qq = 1; qq < KQ; ++qq) v += P[(qq * B + j) * n + c];
+        t[j] = v;
+      }
+#pragma unroll
+      for (int r = 0; r < B; ++r) {
+        float v = 0.f;
+#pragma unroll
+        for (int j = 0; j <= r; ++j) v = fmaf(Wd[r * B + j], t[j], v);
+        S[(i0 + r) * kBlkLd + c] = -v;
+      }
     }
-    if (tid < kLeafB * kLeafB) {
-      const int r = tid >> 3, c = tid & (kLeafB - 1);
-      S[(i0 + r) * kBlkLd + i0 + c] = Wd[r * kLeafB + c];
+    if (tid < B * B) {
+      const int r = tid >> 3, c = tid & (B - 1);
+      S[(i0 + r) * kBlkLd + i0 + c] = Wd[r * B + c];
     }
+    // the next block's rows of L, transposed (rows i0 + 8 .. are still L)
+    if (i0 + B < n)
+      for (int e = tid; e < B * (i0 + B); e += kThreads) {
+        const int k = e >> 3, r = e & (B - 1);
+        Lt[k * B + r] = S[(i0 + B + r) * kBlkLd + k];
+      }
     __syncthreads();
   }
   for (int i = warp; i < n; i += kWarps)
@@ -1326,9 +1396,9 @@ static rf_status chol_inv_rec(SolveCtx& c, float* A, long long lda, long long sA
     // A few leaves (the solve's single matrix) are a latency chain: 16 warps share
     // each step's work. Many (the selection's batches) keep 8, for occupancy.
     if (batch < c.sms)
-      k_chol_inv_leaf<16><<<batch, dim3(32, 16), kLeafSmem, c.s>>>(A, lda, sA, W, ldw, sW, c.dev_status);
+      k_chol_inv_leaf<16><<<batch, dim3(32, 16), leaf_smem<16>(), c.s>>>(A, lda, sA, W, ldw, sW, c.dev_status);
     else
-      k_chol_inv_leaf<8><<<batch, dim3(32, 8), kLeafSmem, c.s>>>(A, lda, sA, W, ldw, sW, c.dev_status);
+      k_chol_inv_leaf<8><<<batch, dim3(32, 8), leaf_smem<8>(), c.s>>>(A, lda, sA, W, ldw, sW, c.dev_status);
     return cuda_check(cudaGetLastError(), "k_chol_inv_leaf launch");
   }
   const int n1 = split_point(n), n2 = n - n1;
@@ -1352,9 +1422,9 @@ static rf_status chol_inv_rec(SolveCtx& c, float* A, long long lda, long long sA
 
 rf_status chol_inv_block(float* A, long long lda, long long sA, float* W, long long ldw, long long sW, int n, int batch,
                          float* tmp, long long stmp, int32_t* dev_status, int sms, cudaStream_t s) {
-  rf_status st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf<8>), kLeafSmem, &g_leaf_attr);
+  rf_status st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf<8>), leaf_smem<8>(), &g_leaf_attr);
   if (st != RF_OK) return st;
-  if ((st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf<16>), kLeafSmem, &g_leaf16_attr)) != RF_OK)
+  if ((st = set_smem_attr(reinterpret_cast<const void*>(&k_chol_inv_leaf<16>), leaf_smem<16>(), &g_leaf16_attr)) != RF_OK)
     return st;
   SolveCtx c{s, sms, dev_status};
   return chol_inv_rec(c, A, lda, sA, W, ldw, sW, n, batch, tmp, stmp);
