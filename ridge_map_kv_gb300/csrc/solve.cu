@@ -446,24 +446,36 @@ __global__ void __launch_bounds__(1024) k_trace_alpha(const double* G, const dou
   }
 }
 
+// v / 2 from the double's bits (an exponent decrement, integer operations only) for
+// normal v whose half is normal; otherwise one fp64 multiply.
+__device__ __forceinline__ double half_of(double v) {
+  const long long bits = __double_as_longlong(v);
+  const int E = static_cast<int>((bits >> 52) & 0x7ff);
+  return (E > 1 && E < 2047) ? __longlong_as_double(bits - (1ll << 52)) : 0.5 * v;
+}
+
 // H = (G + Gᵀ)/2 − n μ_x μ_xᵀ + αI, stored in fp32 and (when H64 is set) fp64.
 // Block (bx, by) writes rows by*32.., columns bx*32.. and reads Gᵀ's matching tile
-// through shared memory, so both reads are row-contiguous. 32 x 8 threads.
+// through shared memory, so both reads are row-contiguous. 32 x 8 threads. Per
+// element one fp64 addition and one fma (GB300's fp64 rate is low): the row
+// factors n μ_x[r] are formed once per tile and the halving is an exponent shift.
 __global__ void __launch_bounds__(256) k_build_h(const double* __restrict__ G, const double* __restrict__ mu_x,
                                                  const double* __restrict__ n, const double* __restrict__ alpha,
                                                  int d_in, double* __restrict__ H64, float* __restrict__ H32) {
   __shared__ double t[32][33];
+  __shared__ double u[32];
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
   for (int j = threadIdx.y; j < 32; j += 8)
     t[j][threadIdx.x] = G[static_cast<size_t>(c0 + j) * d_in + r0 + threadIdx.x];  // G[c0 + j][r0 + x]
+  if (threadIdx.y == 0) u[threadIdx.x] = *n * mu_x[r0 + threadIdx.x];
   __syncthreads();
-  const double nn = *n, a = *alpha;
+  const double a = *alpha;
   const int c = c0 + threadIdx.x;
   const double mc = mu_x[c];
   for (int j = threadIdx.y; j < 32; j += 8) {
     const int r = r0 + j;
     const size_t e = static_cast<size_t>(r) * d_in + c;
-    double h = 0.5 * (G[e] + t[threadIdx.x][j]) - nn * mu_x[r] * mc;
+    double h = fma(-u[j], mc, half_of(G[e] + t[threadIdx.x][j]));
     if (r == c) h += a;
     if (H64 != nullptr) H64[e] = h;
     H32[e] = static_cast<float>(h);
