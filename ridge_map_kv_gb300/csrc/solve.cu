@@ -1496,7 +1496,7 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
         RF_OK)
       return s;
   }
-  const int oz_bits = (desc->flags & RF_SOLVE_DIGITS7) ? 7 : rf::oz_bits(di);
+  const int digit_bits = (desc->flags & RF_SOLVE_DIGITS7) ? 7 : oz_bits(di);
   if (refine_iters > 0) {
     // the refinement's precision from the conditioning (see k_refine_plan), once
     ProfScope pr(c.s, RF_STAGE_SOLVE_REFINE);
@@ -1512,13 +1512,13 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
       if (k + 1 < kPowerSteps) std::swap(xs, ys);
     }
     k_pow_est<<<2, 256, 0, c.s>>>(xs, ys, di, lay.est);
-    k_refine_plan<<<1, 1, 0, c.s>>>(lay.est, oz_bits, lay.plan);
+    k_refine_plan<<<1, 1, 0, c.s>>>(lay.est, digit_bits, lay.plan);
     if ((s = cuda_check(cudaGetLastError(), "refinement plan launches")) != RF_OK) return s;
   }
   for (int it = 0; it < refine_iters; ++it) {
     ProfScope pr(c.s, RF_STAGE_SOLVE_REFINE);
-    s = use_pair(desc->flags, true) ? oz_residual<true>(c, lay, st->C, A, P, di, dout, oz_bits, lay.work)
-                                    : oz_residual<false>(c, lay, st->C, A, P, di, dout, oz_bits, lay.work);
+    s = use_pair(desc->flags, true) ? oz_residual<true>(c, lay, st->C, A, P, di, dout, digit_bits, lay.work)
+                                    : oz_residual<false>(c, lay, st->C, A, P, di, dout, digit_bits, lay.work);
     if (s != RF_OK) return s;
     // ΔA = R H^-1 into the residual's own buffer (split into planes_a first, so free),
     // then A += ΔA in one coalesced pass: an in-epilogue read-modify-write of A (one
