@@ -82,6 +82,47 @@ def test_fill_rejects_bad_descriptors_on_the_host(bad):
     assert ei.value.status in (rf.RF_ERR_INVALID_ARG, rf.RF_ERR_SHAPE)
 
 
+def test_fill_row_limit_is_the_documented_one():
+    """rf.h: N − T may be at most 2^24 (row indices, tile and unit counts are 32-bit in
+    the kernels). The limit itself is accepted, one row past it is refused on the host."""
+    at = _fill_desc(N=(1 << 24) + 3, T=3)
+    assert rf.rf_fill_workspace_bytes(at) > 0
+    past = _fill_desc(N=(1 << 24) + 4, T=3)
+    assert rf.rf_fill_workspace_bytes(past) == 0
+    with pytest.raises(rf.RFError) as ei:
+        _fill_call(past)
+    assert ei.value.status == rf.RF_ERR_SHAPE and "2^24" in rf.rf_last_error()
+
+
+@pytest.mark.parametrize("d_in,d_out,P,ok", [(32768, 256, 1, True), (33024, 256, 1, False), (256, 256, 65535, True),
+                                            (256, 256, 65536, False), (384, 256, 1, False), (256, 320, 1, False),
+                                            (256, 256, 0, False)],
+                         ids=["d_in at its limit", "d_in past it", "maps at their limit", "maps past it",
+                              "d_in not a multiple of 256", "d_out not a multiple of 256", "no maps"])
+def test_solve_shape_limits(d_in, d_out, P, ok):
+    """rf.h: d_in and d_out multiples of 256, d_in <= 32768, 1 <= n_maps <= 65535; the
+    workspace query answers 0 outside them and the call refuses with RF_ERR_SHAPE or
+    RF_ERR_INVALID_ARG before any launch."""
+    desc = rf.rf_calib_desc(d_in=d_in, d_out=d_out, n_maps=P)
+    wsb = rf.rf_solve_workspace_bytes(desc)
+    assert (wsb > 0) == ok
+    if not ok:
+        with pytest.raises(rf.RFError) as ei:
+            rf.rf_solve(desc, rf.calib_stats_struct(256, 256, 256, 256, 256), 0.03, rf.RF_ALPHA_TRACE, 0, 256, 256,
+                        workspace=256, workspace_bytes=1 << 40, stream=0)
+        assert ei.value.status in (rf.RF_ERR_SHAPE, rf.RF_ERR_INVALID_ARG)
+
+
+@pytest.mark.parametrize("lam,refine", [(-1.0, 0), (float("nan"), 0), (0.03, -1), (0.03, 9)],
+                         ids=["negative lambda", "NaN lambda", "negative sweeps", "more than 8 sweeps"])
+def test_solve_rejects_bad_lambda_and_sweep_counts(lam, refine):
+    desc = rf.rf_calib_desc(d_in=256, d_out=256, n_maps=1)
+    with pytest.raises(rf.RFError) as ei:
+        rf.rf_solve(desc, rf.calib_stats_struct(256, 256, 256, 256, 256), lam, rf.RF_ALPHA_TRACE, refine, 256, 256,
+                    workspace=256, workspace_bytes=1 << 40, stream=0)
+    assert ei.value.status == rf.RF_ERR_INVALID_ARG
+
+
 def _fill_call(desc, **kw):
     """rf_fill_kv with valid-looking (aligned, non-NULL, never dereferenced) arguments,
     some replaced by ``kw``; the host checks reject before any launch."""
