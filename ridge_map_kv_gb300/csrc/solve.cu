@@ -954,8 +954,8 @@ __device__ __forceinline__ float ll_to_float(long long v) {
 // 2^(−bM) σ_o τ_i, below the residual's own accuracy) minus T as an int64, then
 // rounded to fp32. For an accurate A, |Cc| and |T| stay within d_in 2^(bM−2) units of
 // the grid; where that passes 2^61 (8-bit digits at M = 7) the grid is 2^8 coarser
-// and T's lowest weights are rounded to it. Only the centring (one fma per element)
-// uses the fp64 units. C is [i][o] and R [o][i]: a CTA turns a tile of 32 o × 128 i
+// and T's lowest weights are rounded to it. A zero row of A (σ_o = 0) has T = 0 and
+// takes R = Cc directly. Only the centring (one fma per element) uses the fp64 units. C is [i][o] and R [o][i]: a CTA turns a tile of 32 o × 128 i
 // through shared memory, each thread then writing 4 consecutive i of 4 rows o (int4
 // sums in, float4 out). Grid (d_out/32, d_in/128, maps), 32 x 8 threads; d_in % 128 == 0.
 constexpr int kCombI = 128;
@@ -1003,7 +1003,8 @@ __global__ void __launch_bounds__(256) k_oz_combine(const double* __restrict__ C
         else T2[q] = T2[q] * (1ll << bits) + x[q];
       }
     }
-    const int ea = pow2_exponent(sA[static_cast<size_t>(p) * d_out + o]) - bits * mm + g;
+    const double sa = sA[static_cast<size_t>(p) * d_out + o];  // 0 for a zero row of A: then T = 0 and R = Cc
+    const int ea = pow2_exponent(sa) - bits * mm + g;
     const double2 c01 = *reinterpret_cast<const double2*>(&t[oo][4 * tx]);
     const double2 c23 = *reinterpret_cast<const double2*>(&t[oo][4 * tx + 2]);
     const double cc[4] = {c01.x, c01.y, c23.x, c23.y};
@@ -1015,7 +1016,7 @@ __global__ void __launch_bounds__(256) k_oz_combine(const double* __restrict__ C
       const long long tg = T1[q] * (1ll << (bits * (mm - mid) - g)) + (g ? (T2[q] + (1ll << (g - 1))) >> g : T2[q]);
       const long long d = static_cast<long long>(static_cast<unsigned long long>(to_grid(cc[q], k)) -
                                                  static_cast<unsigned long long>(tg));
-      r[q] = ldexpf(ll_to_float(d), k);
+      r[q] = sa != 0.0 ? ldexpf(ll_to_float(d), k) : static_cast<float>(cc[q]);
     }
     __stcs(reinterpret_cast<float4*>(R32 + e), make_float4(r[0], r[1], r[2], r[3]));
   }

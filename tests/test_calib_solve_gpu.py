@@ -330,6 +330,27 @@ def test_solve_repeated_refinement_converges_when_badly_conditioned(flags):
     assert errs[4] <= 1e-6 and errs[4] < errs[0] / 1000, errs
 
 
+@DIGITS
+def test_solve_degenerate_maps_with_refinement(flags):
+    """Maps that exercise the refinement's corner cases, two sweeps: Y = 0 (Cc = 0, so A
+    and b stay exactly 0: zero digit rows, T = 0), Y = X (the self map, A = Gc(Gc +
+    αI)^-1, [RF] "Ridge map" at l = S), and Y = 1000 X + 7 (the same map scaled by 10^3,
+    digits scaled by their row's power of two, b = μ_y − A μ_x). Each against the oracle."""
+    d, P, n = 512, 3, 4096
+    rng = np.random.default_rng(31)
+    X = rng.standard_normal((n, d)) * np.geomspace(1.0, 0.3, d)
+    Y = np.stack([np.zeros((n, d)), X, 1000.0 * X + 7.0])
+    Xb = torch.as_tensor(X, dtype=torch.float32).to(torch.bfloat16)
+    Yb = torch.as_tensor(Y, dtype=torch.float32).to(torch.bfloat16)
+    ref = O.calib_stats(_f64(Xb), _f64(Yb))
+    Ar, br, _ = O.ridge_solve(ref, 0.03)
+    A, b, _, _ = _solve(_upload_stats(ref), d, d, P, 0.03, refine=2, flags=flags)
+    assert not np.any(A[0]) and not np.any(b[0])
+    for p in (1, 2):
+        assert _rel(A[p], Ar[p]) <= 1e-6, (p, _rel(A[p], Ar[p]))
+        assert _rel(b[p], br[p]) <= 1e-5, (p, _rel(b[p], br[p]))
+
+
 @pytest.mark.slow
 def test_solve_full_width_sampled_rows():
     d, P, n = 4096, 2, 8192
