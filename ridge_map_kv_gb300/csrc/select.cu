@@ -636,7 +636,9 @@ static rf_status split_blocks(SelCtx& c, const float* src, long long ld_src, lon
 static rf_status sel_factor(SelCtx& c, const FactorScratch& lay, float* A, long long lda, long long sA, float* W,
                             long long ldw, long long sW, int n, int batch, long long stmp) {
   rf_status st;
-  if (n % 512 != 0) {
+  // A single matrix's 512-wide nodes (products of 256³, one tile each) run faster as
+  // three SIMT products than as ten launches of plane splits and tensor-core GEMMs.
+  if (n % 512 != 0 || (batch == 1 && n < 1024)) {
     ProfScope prof(c.s, c.factor_stage);
     return chol_inv_block(A, lda, sA, W, ldw, sW, n, batch, lay.ctmp, stmp, c.dev_status, c.sms, c.s);
   }
