@@ -30,46 +30,50 @@
 namespace rf {
 
 // out[row][h][:] = R^{sign}(pos) in[row][h][:], pos = row % rows_per_position + pos_offset,
-// with the frequencies `rf` of (θ, hd). Each thread handles 8 rotation pairs of one
-// head of one row.
+// with the frequencies `rf` of (θ, hd). Each thread takes 8 rotation pairs (one chunk)
+// of one row for every head: the 8 angles are formed once and serve all the row's
+// heads, and a step costs two index divisions (8 lanes cover a head's 128-byte half
+// row, so a warp's loads stay whole-sector).
 __global__ void __launch_bounds__(256) k_rope_rows(const __nv_bfloat16* __restrict__ in, __nv_bfloat16* out,
                                                    long long n_rows, long long ld_in, long long ld_out, int n_heads,
                                                    int hd, long long rows_per_position, long long pos_offset,
                                                    const __grid_constant__ RopeFreqs rf, float sign) {
   const int half = hd >> 1;
   const int chunks = half / 8;
-  const long long total = n_rows * n_heads * chunks;
+  const long long total = n_rows * chunks;
   for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int ch = static_cast<int>(idx % chunks);
-    const long long rh = idx / chunks;
-    const int h = static_cast<int>(rh % n_heads);
-    const long long row = rh / n_heads;
+    const long long row = idx / chunks;
+    const int i0 = static_cast<int>(idx - row * chunks) * 8;
     const long long t = row % rows_per_position;
-    const int i0 = ch * 8;
-    const __nv_bfloat16* src = in + row * ld_in + static_cast<long long>(h) * hd;
-    const uint4 a = *reinterpret_cast<const uint4*>(src + i0);
-    const uint4 b = *reinterpret_cast<const uint4*>(src + half + i0);
     float c[8], s[8];
     const unsigned long long pos = static_cast<unsigned long long>(t + pos_offset);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) rope_cs(pos, rf.g[i0 + q], c[q], s[q]);
-    const __nv_bfloat162* ah = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* bh = reinterpret_cast<const __nv_bfloat162*>(&b);
-    uint4 o1, o2;
-    uint32_t* u1 = reinterpret_cast<uint32_t*>(&o1);
-    uint32_t* u2 = reinterpret_cast<uint32_t*>(&o2);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 x1 = __bfloat1622float2(ah[q]);
-      const float2 x2 = __bfloat1622float2(bh[q]);
-      const float sa = sign * s[2 * q], sb = sign * s[2 * q + 1];
-      u1[q] = pack_bf16x2(x1.x * c[2 * q] - x2.x * sa, x1.y * c[2 * q + 1] - x2.y * sb);
-      u2[q] = pack_bf16x2(x2.x * c[2 * q] + x1.x * sa, x2.y * c[2 * q + 1] + x1.y * sb);
+    for (int q = 0; q < 8; ++q) {
+      rope_cs(pos, rf.g[i0 + q], c[q], s[q]);
+      s[q] *= sign;
     }
-    __nv_bfloat16* dst = out + row * ld_out + static_cast<long long>(h) * hd;
-    *reinterpret_cast<uint4*>(dst + i0) = o1;
-    *reinterpret_cast<uint4*>(dst + half + i0) = o2;
+    const __nv_bfloat16* src = in + row * ld_in + i0;
+    __nv_bfloat16* dst = out + row * ld_out + i0;
+#pragma unroll 4
+    for (int h = 0; h < n_heads; ++h) {
+      const uint4 a = *reinterpret_cast<const uint4*>(src + static_cast<long long>(h) * hd);
+      const uint4 b = *reinterpret_cast<const uint4*>(src + static_cast<long long>(h) * hd + half);
+      const __nv_bfloat162* ah = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* bh = reinterpret_cast<const __nv_bfloat162*>(&b);
+      uint4 o1, o2;
+      uint32_t* u1 = reinterpret_cast<uint32_t*>(&o1);
+      uint32_t* u2 = reinterpret_cast<uint32_t*>(&o2);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 x1 = __bfloat1622float2(ah[q]);
+        const float2 x2 = __bfloat1622float2(bh[q]);
+        u1[q] = pack_bf16x2(x1.x * c[2 * q] - x2.x * s[2 * q], x1.y * c[2 * q + 1] - x2.y * s[2 * q + 1]);
+        u2[q] = pack_bf16x2(x2.x * c[2 * q] + x1.x * s[2 * q], x2.y * c[2 * q + 1] + x1.y * s[2 * q + 1]);
+      }
+      *reinterpret_cast<uint4*>(dst + static_cast<long long>(h) * hd) = o1;
+      *reinterpret_cast<uint4*>(dst + static_cast<long long>(h) * hd + half) = o2;
+    }
   }
 }
 
@@ -306,7 +310,7 @@ extern "C" rf_status rf_xmodel_map(const rf_xmodel_desc* desc, const int32_t* sr
   {
     ProfScope prof(s, RF_STAGE_UNROPE);
     const long long n_rows = desc->L_src * N;
-    const long long total = n_rows * desc->n_kv_heads * (half / 8);
+    const long long total = n_rows * (half / 8);  // one thread a row and chunk of 8 pairs
     const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 16LL * sms));
     k_rope_rows<<<blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(k_src), lay.ku, n_rows, KV, KV,
                                        static_cast<int>(desc->n_kv_heads), static_cast<int>(desc->head_dim), N,
@@ -334,7 +338,7 @@ extern "C" rf_status rf_rope_rows(const rf_bf16* in, rf_bf16* out, int64_t n_row
   rf_status st = current_device(&sms);
   if (st != RF_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const long long total = n_rows * n_heads * (head_dim / 16);
+  const long long total = n_rows * (head_dim / 16);
   const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 16LL * sms));
   ProfScope prof(s, RF_STAGE_UNROPE);
   k_rope_rows<<<blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(in), reinterpret_cast<__nv_bfloat16*>(out),
@@ -386,7 +390,7 @@ extern "C" rf_status rf_concat_layers(const rf_bf16* src, int64_t n_layers, int6
   ProfScope prof(s, RF_STAGE_UNROPE);
   const RopeFreqs rf = theta > 0.0 ? rope_freqs(theta, static_cast<int>(head_dim)) : RopeFreqs{};
   for (int64_t l = 0; l < n_layers; ++l) {
-    const long long total = theta > 0.0 ? n_rows * n_heads * (head_dim / 16) : n_rows * (W / 8);
+    const long long total = theta > 0.0 ? n_rows * (head_dim / 16) : n_rows * (W / 8);
     const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 16LL * sms));
     if (theta > 0.0) {
       k_rope_rows<<<blocks, 256, 0, s>>>(in + l * layer_stride, o + l * W, n_rows, ld_src, ld_out,
