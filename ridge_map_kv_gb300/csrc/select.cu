@@ -178,6 +178,152 @@ struct SelGemmProb {
   }
 };
 
+// One split product of the factorisation on square 256 x 256 tiles, for every matrix s
+// of a batch: out_s = alpha · A_s B_sᵀ + beta · C_s with A_s, B_s the h x h blocks of
+// planes [3][batch * h][h] (K-major, matrix s at rows s*h ..). The factors' triangles
+// are known, so a unit computes only the output tiles that are read later and only
+// the K-range where both operands can be nonzero (whole 256-wide tiles of zeros
+// skipped, so the sums are those of the full product up to the fp32 chunking):
+//   tiles: kTriAll, kTriLower (nt <= mt), kTriUpper (nt >= mt);
+//   K:     kKAll, kKUpToN (k < 256 (nt + 1)), kKUpToM (k < 256 (mt + 1)),
+//          kKFromM (k >= 256 mt), kKFromN (k >= 256 nt).
+enum { kTriAll = 0, kTriLower = 1, kTriUpper = 2 };
+enum { kKAll = 0, kKUpToN = 1, kKUpToM = 2, kKFromM = 3, kKFromN = 4 };
+// K rows summed in TMEM per chunk. Skipping the zero triangles packs every chunk with
+// nonzero terms, and the tensor core's fp32 accumulation truncates with a bias that
+// grows with the chunk (1024-row chunks left the unrefined 2,560-wide solve's normal
+// equations at 1.1e-5 against 8.1e-6 for the full products); 512 keeps it below.
+constexpr int kTriChunk = 512;
+
+// CTA pairs only: their 256 x 256 unit is square (a single CTA's is 128 x 256).
+struct TriGemmProb {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  long long plane_rows;  // batch * h
+  int h, T, tiles, tile_mode, k_mode;  // T = h / 256 tiles a side; tiles per matrix
+  float alpha, beta;
+  float* out;
+  long long o_s, ldo;
+  const float* csrc;
+  long long c_s, ldc;
+  int32_t* dev_status;
+  uint64_t timeout_ns;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kPair = true;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kCols = kBN / 2;
+  struct EpiState {
+    float rs[kCols];
+  };
+  using Cfg = GemmCfg<true>;
+  static_assert(Cfg::kUnitM == kBN, "square tiles");
+
+  __device__ void prefetch() const {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  __device__ int num_units() const { return static_cast<int>(plane_rows / h) * tiles; }
+  // unit -> (matrix s, tile row mt, tile column nt)
+  __device__ void decode(int u, int& s, int& mt, int& nt) const {
+    s = u / tiles;
+    const int r = u - s * tiles;
+    if (tile_mode == kTriAll) {
+      mt = r / T;
+      nt = r - mt * T;
+      return;
+    }
+    // r-th entry of the lower triangle in row order: row i holds i + 1 entries
+    // (T is at most 128, so a walk down the rows is short)
+    int i = 0, j = r;
+    while (j > i) {
+      ++i;
+      j -= i;
+    }
+    mt = tile_mode == kTriLower ? i : j;
+    nt = tile_mode == kTriLower ? j : i;
+  }
+  __device__ void k_range(int mt, int nt, int& lo, int& hi) const {
+    lo = 0;
+    hi = h;
+    switch (k_mode) {
+      case kKUpToN: hi = min(h, kBN * (nt + 1)); break;
+      case kKUpToM: hi = min(h, kBN * (mt + 1)); break;
+      case kKFromM: lo = kBN * mt; break;
+      case kKFromN: lo = kBN * nt; break;
+      default: break;
+    }
+  }
+  __device__ int n_chunks(int u) const {
+    int s, mt, nt, lo, hi;
+    decode(u, s, mt, nt);
+    k_range(mt, nt, lo, hi);
+    return (hi - lo + kTriChunk - 1) / kTriChunk;
+  }
+  __device__ int num_subtiles(int u) const { return 6 * n_chunks(u); }
+  __device__ int num_kb(int u, int sb) const {
+    int s, mt, nt, lo, hi;
+    decode(u, s, mt, nt);
+    k_range(mt, nt, lo, hi);
+    const int nch = (hi - lo + kTriChunk - 1) / kTriChunk;
+    const int c = sb % nch;
+    return (min(kTriChunk, hi - lo - c * kTriChunk) + kBK - 1) / kBK;
+  }
+  struct Coords {
+    int a_row, b_row, k0;
+  };
+  __device__ Coords coords(int u, int sb, uint32_t rank) const {
+    int s, mt, nt, lo, hi;
+    decode(u, s, mt, nt);
+    k_range(mt, nt, lo, hi);
+    const int nch = (hi - lo + kTriChunk - 1) / kTriChunk;
+    const int t = sb / nch, c = sb - t * nch;
+    Coords r;
+    r.a_row = static_cast<int>(sel_term_a(t) * plane_rows + static_cast<long long>(s) * h +
+                               static_cast<long long>(mt) * Cfg::kUnitM + rank * kBM);
+    r.b_row = static_cast<int>(sel_term_b(t) * plane_rows + static_cast<long long>(s) * h +
+                               static_cast<long long>(nt) * kBN + rank * Cfg::kBRows);
+    r.k0 = lo + c * kTriChunk;
+    return r;
+  }
+  __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    load_operand<kBM, false, kPair>(sa, &tmA, bar, c.k0 + kb * kBK, c.a_row);
+    load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, c.k0 + kb * kBK, c.b_row);
+  }
+  __device__ void epilogue(EpiState& es, int, int sb, int, uint32_t tacc, int, int, uint32_t) const {
+#pragma unroll
+    for (int ch = 0; ch < kCols / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(tacc + ch * 32, v);
+      tmem_wait_ld32(v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) es.rs[ch * 32 + i] = sb == 0 ? u2f(v[i]) : es.rs[ch * 32 + i] + u2f(v[i]);
+    }
+  }
+  __device__ void epilogue_after(EpiState& es, int u, int sb, int nsub, int row, int col0, uint32_t rank) const {
+    if (sb != nsub - 1) return;
+    int s, mt, nt;
+    decode(u, s, mt, nt);
+    const long long m = static_cast<long long>(mt) * Cfg::kUnitM + rank * kBM + row;
+    const long long n0 = static_cast<long long>(nt) * kBN + col0;
+    float4* o = reinterpret_cast<float4*>(out + s * o_s + m * ldo + n0);
+    const float4* cp = beta != 0.f ? reinterpret_cast<const float4*>(csrc + s * c_s + m * ldc + n0) : nullptr;
+#pragma unroll
+    for (int i = 0; i < kCols / 4; ++i) {
+      float4 v = make_float4(alpha * es.rs[4 * i], alpha * es.rs[4 * i + 1], alpha * es.rs[4 * i + 2],
+                             alpha * es.rs[4 * i + 3]);
+      if (cp != nullptr) {
+        const float4 c = cp[i];
+        v.x = fmaf(beta, c.x, v.x);
+        v.y = fmaf(beta, c.y, v.y);
+        v.z = fmaf(beta, c.z, v.z);
+        v.w = fmaf(beta, c.w, v.w);
+      }
+      o[i] = v;
+    }
+  }
+};
+
 // fp32 rows -> three bf16 planes: dst[j][r][col_off + c] for r < rows, c < cols
 // (cols % 4 == 0); plane j at dst + j * plane_stride.
 __global__ void __launch_bounds__(256) k_split_rows(const float* __restrict__ src, long long ld_src,
@@ -590,6 +736,51 @@ static rf_status sel_gemm(SelCtx& c, const SelGemm& g) {
 }
 
 static SelOperand op(long long q_rows, long long s_rows, long long b_rows, long long k0, long long s_k,
+                     long long b_k);
+
+// out_s = alpha · A_s B_sᵀ + beta · C_s for the batch's h x h blocks (planes pa, pb:
+// [3][batch * h][h]) with the factors' triangles skipped (TriGemmProb); on single
+// CTAs, or for h not a multiple of 256, the plain split product over every tile and K.
+static rf_status tri_gemm(SelCtx& c, const __nv_bfloat16* pa, const __nv_bfloat16* pb, int batch, int h,
+                          int tile_mode, int k_mode, float alpha, float beta, float* out, long long o_s,
+                          long long ldo, const float* csrc, long long c_s, long long ldc, int stage) {
+  const long long rows = static_cast<long long>(batch) * h;
+  if (!c.pair || h % kBN != 0) {
+    SelGemm g{};
+    g.pa = pa, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
+    g.pb = pb, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
+    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = stage;
+    g.alpha = alpha, g.beta = beta;
+    g.out = out, g.o_s = o_s, g.ldo = ldo;
+    g.csrc = csrc, g.c_s = c_s, g.ldc = ldc;
+    return sel_gemm(c, g);
+  }
+  using Cfg = GemmCfg<true>;
+  TriGemmProb pr;
+  rf_status st;
+  if ((st = make_tmap_bf16_2d(&pr.tmA, pa, h, 3 * rows, h, kBK, kBM)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmB, pb, h, 3 * rows, h, kBK, Cfg::kBRows)) != RF_OK) return st;
+  pr.plane_rows = rows;
+  pr.h = h;
+  pr.T = h / kBN;
+  pr.tiles = tile_mode == kTriAll ? pr.T * pr.T : pr.T * (pr.T + 1) / 2;
+  pr.tile_mode = tile_mode;
+  pr.k_mode = k_mode;
+  pr.alpha = alpha;
+  pr.beta = beta;
+  pr.out = out;
+  pr.o_s = o_s;
+  pr.ldo = ldo;
+  pr.csrc = csrc;
+  pr.c_s = c_s;
+  pr.ldc = ldc;
+  pr.dev_status = c.dev_status;
+  pr.timeout_ns = wait_timeout_ns();
+  ProfScope prof(c.s, stage);
+  return launch_gemm(pr, static_cast<int64_t>(batch) * pr.tiles, c.sms, c.s, "factorisation product launch");
+}
+
+static SelOperand op(long long q_rows, long long s_rows, long long b_rows, long long k0, long long s_k,
                      long long b_k) {
   SelOperand o;
   o.plane_rows = 0;
@@ -649,52 +840,29 @@ static rf_status sel_factor(SelCtx& c, const FactorScratch& lay, float* A, long 
   float* W22 = W21 + h;
   float* L21 = lay.ctmp;  // [batch][h][h]
   const long long hh = static_cast<long long>(h) * h;
-  const long long rows = static_cast<long long>(batch) * h;  // rows of a plane set
   if ((st = sel_factor(c, lay, A, lda, sA, W, ldw, sW, h, batch, stmp)) != RF_OK) return st;
-  // L21 = A21 W11ᵀ
+  const int fs = c.factor_stage;
+  // L21 = A21 W11ᵀ (W11 lower triangular: k <= n)
   if ((st = split_blocks(c, A21, lda, sA, h, h, batch, lay.fpa, false)) != RF_OK) return st;
   if ((st = split_blocks(c, W, ldw, sW, h, h, batch, lay.fpb, false)) != RF_OK) return st;
-  {
-    SelGemm g{};
-    g.pa = lay.fpa, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
-    g.pb = lay.fpb, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
-    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = c.factor_stage;
-    g.out = L21, g.o_s = hh, g.ldo = h;
-    if ((st = sel_gemm(c, g)) != RF_OK) return st;
-  }
-  // A22 −= L21 L21ᵀ
+  if ((st = tri_gemm(c, lay.fpa, lay.fpb, batch, h, kTriAll, kKUpToN, 1.f, 0.f, L21, hh, h, nullptr, 0, 0, fs)) !=
+      RF_OK)
+    return st;
+  // A22 −= L21 L21ᵀ (only the tiles on and below the diagonal are read later)
   if ((st = split_blocks(c, L21, h, hh, h, h, batch, lay.fpa, false)) != RF_OK) return st;
-  {
-    SelGemm g{};
-    g.pa = lay.fpa, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
-    g.pb = lay.fpa, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
-    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = c.factor_stage;
-    g.alpha = -1.f, g.beta = 1.f;
-    g.out = A22, g.o_s = sA, g.ldo = lda;
-    g.csrc = A22, g.c_s = sA, g.ldc = lda;
-    if ((st = sel_gemm(c, g)) != RF_OK) return st;
-  }
-  // Tᵀ = W11ᵀ L21ᵀ, kept in A21's storage
+  if ((st = tri_gemm(c, lay.fpa, lay.fpa, batch, h, kTriLower, kKAll, -1.f, 1.f, A22, sA, lda, A22, sA, lda, fs)) !=
+      RF_OK)
+    return st;
+  // Tᵀ = W11ᵀ L21ᵀ, kept in A21's storage (W11ᵀ's row m is zero below k = m)
   if ((st = split_blocks(c, W, ldw, sW, h, h, batch, lay.fpb, true)) != RF_OK) return st;
-  {
-    SelGemm g{};
-    g.pa = lay.fpb, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
-    g.pb = lay.fpa, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
-    g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = c.factor_stage;
-    g.out = A21, g.o_s = sA, g.ldo = lda;
-    if ((st = sel_gemm(c, g)) != RF_OK) return st;
-  }
+  if ((st = tri_gemm(c, lay.fpb, lay.fpa, batch, h, kTriAll, kKFromM, 1.f, 0.f, A21, sA, lda, nullptr, 0, 0, fs)) !=
+      RF_OK)
+    return st;
   if ((st = sel_factor(c, lay, A22, lda, sA, W22, ldw, sW, h, batch, stmp)) != RF_OK) return st;
-  // W21 = −W22 T
+  // W21 = −W22 T (W22 lower triangular: k <= m)
   if ((st = split_blocks(c, W22, ldw, sW, h, h, batch, lay.fpa, false)) != RF_OK) return st;
   if ((st = split_blocks(c, A21, lda, sA, h, h, batch, lay.fpb, false)) != RF_OK) return st;
-  SelGemm g{};
-  g.pa = lay.fpa, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
-  g.pb = lay.fpb, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
-  g.nS = batch, g.M = h, g.N = h, g.K = h, g.stage = c.factor_stage;
-  g.alpha = -1.f;
-  g.out = W21, g.o_s = sW, g.ldo = ldw;
-  return sel_gemm(c, g);
+  return tri_gemm(c, lay.fpa, lay.fpb, batch, h, kTriAll, kKUpToM, -1.f, 0.f, W21, sW, ldw, nullptr, 0, 0, fs);
 }
 
 // H = L Lᵀ (n x n SPD, n % 128 == 0, consumed): Linv = L^-1 and, when Hinv is set,
@@ -723,12 +891,10 @@ rf_status spd_inverse(float* H, int n, float* Linv, float* Hinv, float* ctmp, __
     return st;
   if (Hinv == nullptr) return RF_OK;
   if ((st = split_blocks(c, Linv, n, 0, n, n, 1, planes, true)) != RF_OK) return st;
-  SelGemm g{};
-  g.pa = planes, g.a_rows = n, g.a_kext = n, g.a = op(0, 0, 0, 0, 0, 0);
-  g.pb = planes, g.b_rows = n, g.b_kext = n, g.b = op(0, 0, 0, 0, 0, 0);
-  g.M = n, g.N = n, g.K = n, g.stage = RF_STAGE_SOLVE;
-  g.out = Hinv, g.ldo = n;
-  if ((st = sel_gemm(c, g)) != RF_OK) return st;
+  // the tiles on and above the diagonal, k >= the column tile (L^-1 is lower triangular)
+  if ((st = tri_gemm(c, planes, planes, 1, n, kTriUpper, kKFromN, 1.f, 0.f, Hinv, 0, n, nullptr, 0, 0,
+                     RF_STAGE_SOLVE)) != RF_OK)
+    return st;
   k_mirror_upper_f32<<<dim3(n / 32, n / 32), dim3(32, 8), 0, s>>>(Hinv, n);
   return cuda_check(cudaGetLastError(), "k_mirror_upper_f32 launch");
 }
