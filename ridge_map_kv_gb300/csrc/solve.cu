@@ -581,9 +581,131 @@ struct SolveCtx {
   int32_t* dev_status;
 };
 
+// The same product on 64 x 64 x 16 tiles (4 x 4 outputs per thread), for products too
+// small to fill the GPU with 128 x 128 tiles (the single matrix's narrow levels):
+// four times the CTAs, a quarter of the serial work in each. Every output sums k in
+// the same ascending order as k_sgemm, so the results are the same bit for bit (the
+// `tri` ranges, now in steps of 64, skip only more zero terms). M % 64 == 0,
+// N % 64 == 0, K % 16 == 0.
+template <bool TA, bool TB>
+__global__ void __launch_bounds__(256) k_sgemm64(int M, int N, int K, float alpha, const float* __restrict__ A,
+                                                 long long lda, long long sA, const float* __restrict__ B,
+                                                 long long ldb, long long sB, float beta, float* C, long long ldc,
+                                                 long long sC, int tri) {
+  __shared__ __align__(16) float As[2][16][64];
+  __shared__ __align__(16) float Bs[2][16][64];
+  const int tid = threadIdx.x;
+  const int bm = blockIdx.y * 64, bn = blockIdx.x * 64;
+  if ((tri & kSgemmLowerOut) && bn > bm) return;
+  const int kbeg = (tri & kSgemmKFromN) ? bn : 0;
+  int kend = K;
+  if (tri & kSgemmKToN) kend = min(kend, bn + 64);
+  if (tri & kSgemmKToM) kend = min(kend, bm + 64);
+  A += blockIdx.z * sA;
+  B += blockIdx.z * sB;
+  C += blockIdx.z * sC;
+  const int ty = tid >> 4, tx = tid & 15;
+
+  auto load_a = [&](int k0, float4& r) {
+    if (TA) r = *reinterpret_cast<const float4*>(A + static_cast<long long>(k0 + (tid >> 4)) * lda + bm + (tid & 15) * 4);
+    else r = *reinterpret_cast<const float4*>(A + static_cast<long long>(bm + (tid >> 2)) * lda + k0 + (tid & 3) * 4);
+  };
+  auto load_b = [&](int k0, float4& r) {
+    if (TB) r = *reinterpret_cast<const float4*>(B + static_cast<long long>(bn + (tid >> 2)) * ldb + k0 + (tid & 3) * 4);
+    else r = *reinterpret_cast<const float4*>(B + static_cast<long long>(k0 + (tid >> 4)) * ldb + bn + (tid & 15) * 4);
+  };
+  auto store_a = [&](int buf, const float4& r) {
+    if (TA) {
+      *reinterpret_cast<float4*>(&As[buf][tid >> 4][(tid & 15) * 4]) = r;
+    } else {
+      const int m = tid >> 2, k = (tid & 3) * 4;
+      As[buf][k][m] = r.x;
+      As[buf][k + 1][m] = r.y;
+      As[buf][k + 2][m] = r.z;
+      As[buf][k + 3][m] = r.w;
+    }
+  };
+  auto store_b = [&](int buf, const float4& r) {
+    if (TB) {
+      const int n = tid >> 2, k = (tid & 3) * 4;
+      Bs[buf][k][n] = r.x;
+      Bs[buf][k + 1][n] = r.y;
+      Bs[buf][k + 2][n] = r.z;
+      Bs[buf][k + 3][n] = r.w;
+    } else {
+      *reinterpret_cast<float4*>(&Bs[buf][tid >> 4][(tid & 15) * 4]) = r;
+    }
+  };
+
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  if (kbeg < kend) {
+    float4 ra, rb;
+    load_a(kbeg, ra);
+    load_b(kbeg, rb);
+    store_a(0, ra);
+    store_b(0, rb);
+    __syncthreads();
+    int buf = 0;
+    for (int k0 = kbeg; k0 < kend; k0 += 16) {
+      const bool more = k0 + 16 < kend;
+      if (more) {
+        load_a(k0 + 16, ra);
+        load_b(k0 + 16, rb);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const float4 a = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+        const float4 b = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+        const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      }
+      if (more) {
+        store_a(buf ^ 1, ra);
+        store_b(buf ^ 1, rb);
+      }
+      __syncthreads();
+      buf ^= 1;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float* cp = C + static_cast<long long>(bm + ty * 4 + i) * ldc + bn + tx * 4;
+    float4 o = make_float4(alpha * acc[i][0], alpha * acc[i][1], alpha * acc[i][2], alpha * acc[i][3]);
+    if (beta != 0.f) {
+      const float4 cv = *reinterpret_cast<const float4*>(cp);
+      o.x = fmaf(beta, cv.x, o.x);
+      o.y = fmaf(beta, cv.y, o.y);
+      o.z = fmaf(beta, cv.z, o.z);
+      o.w = fmaf(beta, cv.w, o.w);
+    }
+    *reinterpret_cast<float4*>(cp) = o;
+  }
+}
+
 static rf_status sgemm(SolveCtx& c, bool ta, bool tb, int M, int N, int K, float alpha, const float* A, long long lda,
                        long long sA, const float* B, long long ldb, long long sB, float beta, float* C, long long ldc,
                        long long sC, int batch, int tri = 0) {
+  if (static_cast<long long>(N / 128) * (M / 128) * batch < c.sms) {
+    // too few 128 x 128 tiles to fill the GPU: 64 x 64 tiles, same sums
+    dim3 g64(N / 64, M / 64, batch);
+    if (!ta && !tb)
+      k_sgemm64<false, false><<<g64, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC, tri);
+    else if (ta && !tb)
+      k_sgemm64<true, false><<<g64, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC, tri);
+    else if (!ta && tb)
+      k_sgemm64<false, true><<<g64, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC, tri);
+    else
+      k_sgemm64<true, true><<<g64, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC, tri);
+    return cuda_check(cudaGetLastError(), "k_sgemm64 launch");
+  }
   dim3 grid(N / 128, M / 128, batch);
   if (!ta && !tb)
     k_sgemm<false, false><<<grid, 256, 0, c.s>>>(M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC, tri);
