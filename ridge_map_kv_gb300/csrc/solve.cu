@@ -222,8 +222,26 @@ __global__ void __launch_bounds__(32 * kWarps) k_chol_inv_leaf(const float* __re
   A += blockIdx.x * sA;
   W += blockIdx.x * sW;
   const int lane = threadIdx.x, warp = threadIdx.y, tid = warp * 32 + lane;
-  for (int i = warp; i < n; i += kWarps)
-    for (int k = lane; k < n; k += 32) S[i * kBlkLd + k] = A[i * lda + k];
+  {
+    // all of a thread's 16-byte loads issued before any is stored (rows of S are 129
+    // floats apart, so the stores are scalar); lda % 4 == 0
+    constexpr int kLoads = n * n / 4 / kThreads;
+    float4 v[kLoads];
+#pragma unroll
+    for (int q = 0; q < kLoads; ++q) {
+      const int e = q * kThreads + tid, i = e / (n / 4), k4 = e % (n / 4);
+      v[q] = *reinterpret_cast<const float4*>(A + i * lda + 4 * k4);
+    }
+#pragma unroll
+    for (int q = 0; q < kLoads; ++q) {
+      const int e = q * kThreads + tid, i = e / (n / 4), k4 = e % (n / 4);
+      float* d = S + i * kBlkLd + 4 * k4;
+      d[0] = v[q].x;
+      d[1] = v[q].y;
+      d[2] = v[q].z;
+      d[3] = v[q].w;
+    }
+  }
   __syncthreads();
   // ---- factor
   // Warp 0 factors the diagonal block at kd. With `update` it first applies the
