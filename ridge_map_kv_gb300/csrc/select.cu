@@ -827,9 +827,12 @@ static rf_status split_blocks(SelCtx& c, const float* src, long long ld_src, lon
 static rf_status sel_factor(SelCtx& c, const FactorScratch& lay, float* A, long long lda, long long sA, float* W,
                             long long ldw, long long sW, int n, int batch, long long stmp) {
   rf_status st;
-  // A single matrix's 512-wide nodes (products of 256³, one tile each) run faster as
-  // three SIMT products than as ten launches of plane splits and tensor-core GEMMs.
-  if (n % 512 != 0 || (batch == 1 && n < 1024)) {
+  // A single matrix's nodes below 2,048 (products of at most 512³, a few tiles each)
+  // run faster as SIMT products (64-tile k_sgemm64) than as ten launches of plane
+  // splits and tensor-core GEMMs: the solve's factorisation stage at d = 4,096 and
+  // 8,192 took 5.7 and 11.2 ms this way, 5.9 and 11.6 ms with SIMT below 1,024 only,
+  // 5.8 and 11.4 ms with SIMT below 4,096.
+  if (n % 512 != 0 || (batch == 1 && n < 2048)) {
     ProfScope prof(c.s, c.factor_stage);
     return chol_inv_block(A, lda, sA, W, ldw, sW, n, batch, lay.ctmp, stmp, c.dev_status, c.sms, c.s);
   }

@@ -8,7 +8,7 @@
 //   k_means, k_trace_alpha  μ_x = sx/n, μ_p = sy_p/n, tr(Gc), α
 //   k_build_h               H = Gc + αI with Gc = G − n μ_x μ_xᵀ (fp64 and fp32 copies)
 //   spd_inverse (select.cu) H = L Lᵀ, L^-1 by recursive halving (products of widths
-//                           that are multiples of 512, from 1,024 up, on the tensor
+//                           that are multiples of 512, from 2,048 up, on the tensor
 //                           cores, the narrower ones fp32 SIMT k_sgemm, 128-wide leaves
 //                           factored and inverted in shared memory by
 //                           k_chol_inv_leaf), then H^-1 = L^-ᵀ L^-1 on the tensor
