@@ -464,6 +464,41 @@ __global__ void __launch_bounds__(1024) k_trace_alpha(const double* G, const dou
   }
 }
 
+// x rounded to the nearest float, ties to even (IEEE 754), from the double's bits
+// with integer operations only (GB300 runs double-to-float conversions on its slow
+// fp64 units; this gives the same bits for every double): the sign, the exponent rebased from 1023 to 127, and
+// the 53-bit significand cut to 24 bits (or to a subnormal's width) with the
+// remainder deciding the rounding; NaN stays NaN, overflow gives infinity.
+__device__ __forceinline__ float f64_to_f32_rn(double x) {
+  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(x));
+  const unsigned sign = static_cast<unsigned>(b >> 32) & 0x80000000u;
+  const int E = static_cast<int>((b >> 52) & 0x7ff);
+  const unsigned long long frac = b & ((1ull << 52) - 1);
+  if (E == 0x7ff) return __uint_as_float(sign | 0x7f800000u | (frac != 0 ? 0x400000u : 0u));
+  const unsigned long long M = E != 0 ? (frac | (1ull << 52)) : frac;  // x = M 2^(max(E,1) − 1075)
+  const int e = (E != 0 ? E : 1) - 1023 + 127;  // the float's biased exponent if normal
+  // bits of M dropped: 29 for a normal float, more below (the subnormal step 2^-149)
+  const int drop = e >= 1 ? 29 : 29 + (1 - e);
+  if (drop > 54) return __uint_as_float(sign);  // below half the smallest subnormal
+  const unsigned long long keep = M >> drop, rem = M & ((1ull << drop) - 1), half = 1ull << (drop - 1);
+  unsigned long long r = keep + ((rem > half || (rem == half && (keep & 1))) ? 1 : 0);
+  // normal: r holds the implicit bit at 2^23 (r may carry to 2^24: the exponent steps
+  // up); subnormal: r < 2^23 (or = 2^23: the smallest normal), exponent field 0
+  unsigned bits;
+  if (e >= 1) {
+    int ee = e;
+    if (r >> 24) {
+      r >>= 1;
+      ++ee;
+    }
+    if (ee >= 255) return __uint_as_float(sign | 0x7f800000u);
+    bits = (static_cast<unsigned>(ee) << 23) | (static_cast<unsigned>(r) & 0x7fffffu);
+  } else {
+    bits = static_cast<unsigned>(r);  // r = 2^23 reads as the smallest normal
+  }
+  return __uint_as_float(sign | bits);
+}
+
 // v / 2 from the double's bits (an exponent decrement, integer operations only) for
 // normal v whose half is normal; otherwise one fp64 multiply.
 __device__ __forceinline__ double half_of(double v) {
@@ -496,36 +531,48 @@ __global__ void __launch_bounds__(256) k_build_h(const double* __restrict__ G, c
     double h = fma(-u[j], mc, half_of(G[e] + t[threadIdx.x][j]));
     if (r == c) h += a;
     if (H64 != nullptr) H64[e] = h;
-    H32[e] = static_cast<float>(h);
+    H32[e] = f64_to_f32_rn(h);
   }
 }
 
 // Cc_p = C_p − n μ_x μ_pᵀ, transposed and split into the product's A operand:
-// planes [3][P][d_out][d_in] (K-major), straight from the fp64 sums through a
-// 32 x 32 tile. One fp64 fma per element (GB300's fp64 rate is low): the row
-// factors −n μ_x[i] are formed once per tile. Grid (d_in/32, d_out/32, P), 32 x 8.
+// planes [3][P][d_out][d_in] (K-major), straight from the fp64 sums. One fp64 fma per
+// element (GB300's fp64 rate is low): the row factors −n μ_x[i] are formed once per
+// tile, and the rounding to fp32 is done in integers (f64_to_f32_rn). A CTA turns a
+// tile of 128 i × 32 o through shared memory ([o][i], rows 16-byte aligned): 16 row
+// reads of 256 bytes a thread, then 4 consecutive i of 4 rows o per thread, 8 bytes
+// a plane per store. Grid (d_in/128, d_out/32, P), 32 x 8 threads; d_in % 128 == 0.
+constexpr int kCentreI = 128;
 __global__ void __launch_bounds__(256) k_centre_split_t(const double* __restrict__ C, const double* __restrict__ mu_x,
                                                         const double* __restrict__ mu_y, const double* __restrict__ n,
                                                         int d_in, int d_out, __nv_bfloat16* __restrict__ planes,
                                                         size_t plane) {
-  __shared__ float t[32][33];
-  __shared__ double a[32];
-  const int p = blockIdx.z, i0 = blockIdx.x * 32, o0 = blockIdx.y * 32;
-  if (threadIdx.y == 0) a[threadIdx.x] = -(*n) * mu_x[i0 + threadIdx.x];
+  __shared__ __align__(16) float t[32][kCentreI + 4];
+  __shared__ double a[kCentreI];
+  const int p = blockIdx.z, i0 = blockIdx.x * kCentreI, o0 = blockIdx.y * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y, tid = ty * 32 + tx;
+  if (tid < kCentreI) a[tid] = -(*n) * mu_x[i0 + tid];
   __syncthreads();
   const double* Cp = C + static_cast<size_t>(p) * d_in * d_out;
-  const double my = mu_y[static_cast<size_t>(p) * d_out + o0 + threadIdx.x];
-  for (int j = threadIdx.y; j < 32; j += 8)  // t[j][x] = Cc[i0 + j][o0 + x]
-    t[j][threadIdx.x] = static_cast<float>(fma(a[j], my, Cp[static_cast<size_t>(i0 + j) * d_out + o0 + threadIdx.x]));
+  const double my = mu_y[static_cast<size_t>(p) * d_out + o0 + tx];
+#pragma unroll 4
+  for (int j = ty; j < kCentreI; j += 8)  // t[x][j] = Cc[i0 + j][o0 + x]
+    t[tx][j] = f64_to_f32_rn(fma(a[j], my, Cp[static_cast<size_t>(i0 + j) * d_out + o0 + tx]));
   __syncthreads();
   __nv_bfloat16* out = planes + static_cast<size_t>(p) * d_out * d_in;
-  for (int j = threadIdx.y; j < 32; j += 8) {  // element (o0 + j, i0 + x) = t[x][j]
-    __nv_bfloat16 h, m, l;
-    split3(t[threadIdx.x][j], h, m, l);
-    const size_t o = static_cast<size_t>(o0 + j) * d_in + i0 + threadIdx.x;
-    out[o] = h;
-    out[plane + o] = m;
-    out[2 * plane + o] = l;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {  // elements (o0 + oo, i0 + 4 tx .. + 3)
+    const int oo = ty + 8 * k;
+    const float4 v = *reinterpret_cast<const float4*>(&t[oo][4 * tx]);
+    __nv_bfloat16 h[4], m[4], l[4];
+    split3(v.x, h[0], m[0], l[0]);
+    split3(v.y, h[1], m[1], l[1]);
+    split3(v.z, h[2], m[2], l[2]);
+    split3(v.w, h[3], m[3], l[3]);
+    const size_t o = static_cast<size_t>(o0 + oo) * d_in + i0 + 4 * tx;
+    *reinterpret_cast<uint2*>(out + o) = *reinterpret_cast<const uint2*>(h);
+    *reinterpret_cast<uint2*>(out + plane + o) = *reinterpret_cast<const uint2*>(m);
+    *reinterpret_cast<uint2*>(out + 2 * plane + o) = *reinterpret_cast<const uint2*>(l);
   }
 }
 
@@ -1621,7 +1668,7 @@ extern "C" rf_status rf_solve(const rf_calib_desc* desc, const rf_calib_stats* s
     k_means<<<eb, 256, 0, c.s>>>(st->sx, st->sy, st->n, di, static_cast<long long>(P) * dout, lay.mu_x, lay.mu_y, lay.n);
     k_trace_alpha<<<1, 1024, 0, c.s>>>(st->G, lay.mu_x, lay.n, di, lambda, alpha_mode, lay.alpha, alpha_out);
     k_build_h<<<dim3(di / 32, di / 32), dim3(32, 8), 0, c.s>>>(st->G, lay.mu_x, lay.n, lay.alpha, di, lay.H64, lay.L);
-    k_centre_split_t<<<dim3(di / 32, dout / 32, P), dim3(32, 8), 0, c.s>>>(
+    k_centre_split_t<<<dim3(di / kCentreI, dout / 32, P), dim3(32, 8), 0, c.s>>>(
         st->C, lay.mu_x, lay.mu_y, lay.n, di, dout, lay.planes_a, static_cast<size_t>(P) * dout * di);
     if ((s = cuda_check(cudaGetLastError(), "solve set-up launches")) != RF_OK) return s;
   }
