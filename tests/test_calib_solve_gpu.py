@@ -404,6 +404,27 @@ def test_solve_widths_that_split_unevenly_match_oracle(d_in, d_out, P, n):
             assert _rel(A[p] @ H, Cc[p].T) <= 1e-5          # the normal equations
 
 
+@pytest.mark.parametrize("flags", [rf.RF_FLAG_SINGLE_CTA, rf.RF_FLAG_CTA_PAIR], ids=["single-cta", "cta-pair"])
+def test_solve_on_either_gemm_kernel_matches_oracle(flags):
+    """d_in = 2560: the factorisation's top node runs its four products on the tensor
+    cores (on CTA pairs skipping the factors' zero triangles and unread tiles, on single
+    CTAs as full split products), and H^-1 = L^-T L^-1 likewise; both kernels' maps,
+    unrefined and after one sweep, against the oracle and the normal equations."""
+    d_in, d_out, P, n = 2560, 256, 2, 8192
+    cal = synth.calib_inputs(d_in, d_out, P, n, index=96)
+    ref = O.calib_stats(_f64(cal["X"]), _f64(cal["Y"]))
+    Ar, br, alr = O.ridge_solve(ref, 0.03)
+    Gc, Cc, _, _ = O.centre_stats(ref)
+    H = Gc + alr * np.eye(d_in)
+    st = _upload_stats(ref)
+    for refine, tol in ((0, 1e-4), (1, 1e-5)):
+        A, b, _, _ = _solve(st, d_in, d_out, P, 0.03, refine=refine, flags=flags)
+        for p in range(P):
+            assert _rel(A[p], Ar[p]) <= tol, (refine, p, _rel(A[p], Ar[p]))
+            assert _rel(b[p], br[p]) <= tol, (refine, p, _rel(b[p], br[p]))
+            assert _rel(A[p] @ H, Cc[p].T) <= tol, (refine, p, _rel(A[p] @ H, Cc[p].T))
+
+
 def _full_width_solve(d_in, d_out, P, n, lam, index):
     (Ar, br, alr, H, Cc), got = _solve_vs_oracle(d_in, d_out, P, n, lam, index, refines=(0, 1), device=DEV)
     errs = {}
