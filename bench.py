@@ -1106,15 +1106,20 @@ def run_selection(dev, peak_tflops, flags=0, n_targets=0, n_sources=0):
     # per pass of Q problems and step j (m = jF features chosen), the scores of all
     # L_src candidates (2 D F Ft), and for j < k-1 the new factor column
     # (2 D F m + 2 D F²), the Schur-block and cross-term updates (2 D F² + 2 Ft F D)
-    # and z_b (2 Ft F²).
+    # and z_b (2 Ft F²). The scores, z_b and the new column's "× L_b^-ᵀ" multiply by
+    # a lower-triangular L^-1: algorithmically (F+1)/2F of a full product, and the
+    # kernel runs the tiles up to each column tile's diagonal, (T+1)/2T with T = F/256.
     n_prob = 2 * T
-    prod = 0.0
+    tri_alg, tri_exec = (F + 1) / (2.0 * F), (F // 256 + 1) / (2.0 * (F // 256))
+    prod, prod_exec = 0.0, 0.0
     for j in range(cfg.k):
         m = j * F
-        prod += 2.0 * D * F * F
-        if j < cfg.k - 1:
-            prod += 2.0 * D * F * m + 2.0 * D * F * F + 2.0 * D * F * F + 2.0 * F * F * D + 2.0 * F * F * F
+        full = 2.0 * D * F * m + 2.0 * D * F * F + 2.0 * F * F * D if j < cfg.k - 1 else 0.0
+        tri = 2.0 * D * F * F + (2.0 * D * F * F + 2.0 * F * F * F if j < cfg.k - 1 else 0.0)
+        prod += full + tri_alg * tri
+        prod_exec += full + tri_exec * tri
     prod *= n_prob
+    prod_exec *= n_prob
     gm = stages.get("select_gemm", ms)
     # fp32 SIMT factorisation of every candidate's F x F Schur block at every step
     # (Cholesky F³/3 and triangular inverse F³/3, algorithmic)
@@ -1129,8 +1134,10 @@ def run_selection(dev, peak_tflops, flags=0, n_targets=0, n_sources=0):
         "calibration_tflops": cflops / (sum(calib_ms) / 2 / 1e3) / 1e12,
         "select_ms": ms, "select_stages_ms": stages,
         "select_products_fp32_tflops": prod / (gm / 1e3) / 1e12,
-        "select_products_bf16_plane_tflops": 6.0 * prod / (gm / 1e3) / 1e12,
-        "select_products_frac_of_sustained_bf16_peak": 6.0 * prod / (gm / 1e3) / 1e12 / sustained,
+        "select_products_algorithmic_fp32_tflop": prod / 1e12,
+        "select_products_executed_fp32_tflop": prod_exec / 1e12,
+        "select_products_bf16_plane_tflops": 6.0 * prod_exec / (gm / 1e3) / 1e12,
+        "select_products_frac_of_sustained_bf16_peak": 6.0 * prod_exec / (gm / 1e3) / 1e12 / sustained,
         "select_factor_fp32_tflops": fact / (fm / 1e3) / 1e12,
         "select_workspace_bytes": wsb,
         "first_target_layers": sel[0].tolist(),

@@ -77,6 +77,10 @@ struct SelGemmProb {
   int q_per_kind;
   // sum of squares: part[(p*M + m)*2*n_tiles + 2*nt + half] = Σ (alpha·acc)² over 128 columns
   float* part;
+  // B lower triangular in (row n, column k), an L^-1: tile column nt reads only
+  // k < 256 (nt + 1), the rest of its K range being exact zeros
+  int b_tri;
+  int* sched;  // unit counter (dynamic unit order), or nullptr for round-robin dealing
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = false;
@@ -94,10 +98,13 @@ struct SelGemmProb {
     tma_prefetch_desc(&tmB);
   }
   __device__ int num_units() const { return Q * nS * m_tiles * n_tiles; }
-  __device__ int num_subtiles(int) const { return 6 * n_chunks; }
-  __device__ int num_kb(int, int sb) const {
-    const int c = sb % n_chunks;
-    return (min(kSelChunk, K - c * kSelChunk) + kBK - 1) / kBK;
+  // K extent of unit u and its number of kSelChunk-wide chunks (nt = u % n_tiles)
+  __device__ int k_ext(int u) const { return b_tri ? min(K, kBN * (u % n_tiles + 1)) : K; }
+  __device__ int chunks(int u) const { return b_tri ? (k_ext(u) + kSelChunk - 1) / kSelChunk : n_chunks; }
+  __device__ int num_subtiles(int u) const { return 6 * chunks(u); }
+  __device__ int num_kb(int u, int sb) const {
+    const int c = sb % chunks(u);
+    return (min(kSelChunk, k_ext(u) - c * kSelChunk) + kBK - 1) / kBK;
   }
   __device__ void decode(int u, int& q, int& s, int& mt, int& nt) const {
     nt = u % n_tiles;
@@ -113,7 +120,8 @@ struct SelGemmProb {
   __device__ Coords coords(int u, int sb, uint32_t rank) const {
     int q, s, mt, nt;
     decode(u, q, s, mt, nt);
-    const int t = sb / n_chunks, c = sb - t * n_chunks;
+    const int nch = chunks(u);
+    const int t = sb / nch, c = sb - t * nch;
     const long long bq = chosen != nullptr ? chosen[q] : 0;
     Coords r;
     r.a_row = static_cast<int>(sel_term_a(t) * a.plane_rows + q * a.q_rows + s * a.s_rows + bq * a.b_rows +
@@ -206,6 +214,7 @@ struct TriGemmProb {
   long long o_s, ldo;
   const float* csrc;
   long long c_s, ldc;
+  int* sched;  // unit counter (dynamic unit order), or nullptr for round-robin dealing
   int32_t* dev_status;
   uint64_t timeout_ns;
   static constexpr bool kAMN = false;
@@ -325,16 +334,20 @@ struct TriGemmProb {
 };
 
 // fp32 rows -> three bf16 planes: dst[j][r][col_off + c] for r < rows, c < cols
-// (cols % 4 == 0); plane j at dst + j * plane_stride.
+// (cols % 4 == 0); plane j at dst + j * plane_stride. With `tri`, the rows are
+// stacked cols x cols lower-triangular matrices and row r stops at the end of its
+// diagonal 256-column tile, c < 256 (⌊(r mod cols)/256⌋ + 1): the columns beyond are
+// zeros that no product reads (SelGemmProb's b_tri).
 __global__ void __launch_bounds__(256) k_split_rows(const float* __restrict__ src, long long ld_src,
                                                     __nv_bfloat16* __restrict__ dst, long long ld_dst, long long col_off,
-                                                    long long plane_stride, long long rows, int cols) {
+                                                    long long plane_stride, long long rows, int cols, int tri) {
   const int per = cols / 4;
   const long long total = rows * per;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long r = i / per;
     const int c = static_cast<int>(i - r * per) * 4;
+    if (tri && c >= kBN * (static_cast<int>(r % cols) / kBN + 1)) continue;
     const float4 v = __ldg(reinterpret_cast<const float4*>(src + r * ld_src + c));
     __nv_bfloat16 h[4], m[4], l[4];
     split3(v.x, h[0], m[0], l[0]);
@@ -595,6 +608,7 @@ struct SelLayout {
   double* expl;     // [Qmax][Ft]
   int32_t* chosen;  // [Qmax]
   uint8_t* mask;    // [Gmax][Ls]
+  int* sched;       // unit counter of the dynamically ordered products
   size_t bytes;
 };
 
@@ -633,6 +647,7 @@ static SelLayout sel_layout(const rf_select_desc* d, void* ws) {
   l.expl = c.take<double>(Q * Ft);
   l.chosen = c.take<int32_t>(Q);
   l.mask = c.take<uint8_t>(Gm * Ls);
+  l.sched = c.take<int>(1);
   l.bytes = c.bytes();
   return l;
 }
@@ -658,14 +673,19 @@ struct SelCtx {
   int32_t* dev_status;
   bool pair;
   int factor_stage = RF_STAGE_SELECT_FACTOR;  // profiler stage of the factorisation's launches
+  // A device int for the dynamic unit order of the products whose units differ in
+  // length (triangle-skipping ones), or nullptr to deal them round-robin: with 76
+  // pairs and 4 tile columns, round-robin gives every pair the same column, so the
+  // longest column sets the launch's time.
+  int* sched = nullptr;
 };
 
 static rf_status split_rows(SelCtx& c, const float* src, long long ld_src, __nv_bfloat16* dst, long long ld_dst,
-                            long long col_off, long long plane_stride, long long rows, int cols) {
+                            long long col_off, long long plane_stride, long long rows, int cols, bool tri = false) {
   const long long total = rows * (cols / 4);
   const unsigned blocks = static_cast<unsigned>(std::min<long long>((total + 255) / 256, 8LL * c.sms));
   ProfScope prof(c.s, RF_STAGE_SELECT_SPLIT);
-  k_split_rows<<<blocks, 256, 0, c.s>>>(src, ld_src, dst, ld_dst, col_off, plane_stride, rows, cols);
+  k_split_rows<<<blocks, 256, 0, c.s>>>(src, ld_src, dst, ld_dst, col_off, plane_stride, rows, cols, tri ? 1 : 0);
   return cuda_check(cudaGetLastError(), "k_split_rows launch");
 }
 
@@ -687,6 +707,7 @@ struct SelGemm {
   long long c_kind = 0, c_b = 0, c_q = 0, c_s = 0, ldc = 0;
   int q_per_kind = 1;
   float* part = nullptr;
+  bool b_tri = false;  // B is an L^-1 (lower triangular in row, K): skip its zero K range
   int stage = RF_STAGE_SELECT_GEMM;  // profiler stage of the launch
 };
 
@@ -724,6 +745,8 @@ static rf_status run_sel_gemm(SelCtx& c, const SelGemm& g) {
   pr.ldc = g.ldc;
   pr.q_per_kind = g.q_per_kind;
   pr.part = g.part;
+  pr.b_tri = g.b_tri ? 1 : 0;
+  pr.sched = g.b_tri ? c.sched : nullptr;
   pr.dev_status = c.dev_status;
   pr.timeout_ns = wait_timeout_ns();
   ProfScope prof(c.s, g.stage);
@@ -774,6 +797,7 @@ static rf_status tri_gemm(SelCtx& c, const __nv_bfloat16* pa, const __nv_bfloat1
   pr.csrc = csrc;
   pr.c_s = c_s;
   pr.ldc = ldc;
+  pr.sched = c.sched;
   pr.dev_status = c.dev_status;
   pr.timeout_ns = wait_timeout_ns();
   ProfScope prof(c.s, stage);
@@ -932,6 +956,7 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
   int sms = 0;
   if ((st = current_device(&sms)) != RF_OK) return st;
   SelCtx c{static_cast<cudaStream_t>(stream), sms, dev_status, use_pair(desc->flags, true)};
+  c.sched = lay.sched;
 
   const int Ls = static_cast<int>(desc->L_src), F = static_cast<int>(desc->F), Ft = static_cast<int>(desc->d_out);
   const int NK = static_cast<int>(desc->n_kinds), T = static_cast<int>(desc->n_targets), K = static_cast<int>(desc->k);
@@ -992,14 +1017,15 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
                            lay.Linv, F, static_cast<long long>(F) * F, F, Q * Ls, static_cast<long long>(F) * F / 4)) !=
           RF_OK)
         return st;
-      if ((st = split_rows(c, lay.Linv, F, lay.Lp, F, 0, lrows * F, lrows, F)) != RF_OK) return st;
+      // L^-1 up to each row's diagonal tile: the products read no further (b_tri)
+      if ((st = split_rows(c, lay.Linv, F, lay.Lp, F, 0, lrows * F, lrows, F, true)) != RF_OK) return st;
       if ((st = split_rows(c, lay.RT, D, lay.RTp, D, 0, rtrows * D, rtrows, static_cast<int>(D))) != RF_OK) return st;
       // colsum(z_s²) for every (q, s): z_sᵀ = R_sᵀ L_s^-ᵀ
       {
         SelGemm g{};
         g.pa = lay.RTp, g.a_rows = rtrows, g.a_kext = D, g.a = op(Ft, 0, 0, 0, F, 0);
         g.pb = lay.Lp, g.b_rows = lrows, g.b_kext = F, g.b = op(static_cast<long long>(Ls) * F, F, 0, 0, 0, 0);
-        g.Q = Q, g.nS = Ls, g.M = Ft, g.N = F, g.K = F;
+        g.Q = Q, g.nS = Ls, g.M = Ft, g.N = F, g.K = F, g.b_tri = true;
         g.part = lay.part;
         if ((st = sel_gemm(c, g)) != RF_OK) return st;
       }
@@ -1015,7 +1041,7 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
         SelGemm g{};
         g.pa = lay.RTp, g.a_rows = rtrows, g.a_kext = D, g.a = op(Ft, 0, 0, 0, 0, F);
         g.pb = lay.Lp, g.b_rows = lrows, g.b_kext = F, g.b = op(static_cast<long long>(Ls) * F, 0, F, 0, 0, 0);
-        g.chosen = lay.chosen, g.Q = Q, g.M = Ft, g.N = F, g.K = F;
+        g.chosen = lay.chosen, g.Q = Q, g.M = Ft, g.N = F, g.K = F, g.b_tri = true;
         g.out = lay.zb, g.o_q = static_cast<long long>(Ft) * F, g.ldo = F;
         if ((st = sel_gemm(c, g)) != RF_OK) return st;
       }
@@ -1041,7 +1067,7 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
         SelGemm g{};
         g.pa = lay.Xp, g.a_rows = wrows, g.a_kext = F, g.a = op(D, 0, 0, 0, 0, 0);
         g.pb = lay.Lp, g.b_rows = lrows, g.b_kext = F, g.b = op(static_cast<long long>(Ls) * F, 0, F, 0, 0, 0);
-        g.chosen = lay.chosen, g.Q = Q, g.M = static_cast<int>(D), g.N = F, g.K = F;
+        g.chosen = lay.chosen, g.Q = Q, g.M = static_cast<int>(D), g.N = F, g.K = F, g.b_tri = true;
         g.out = lay.X, g.o_q = D * F, g.ldo = F;
         if ((st = sel_gemm(c, g)) != RF_OK) return st;
       }
