@@ -80,6 +80,9 @@ struct SelGemmProb {
   // B lower triangular in (row n, column k), an L^-1: tile column nt reads only
   // k < 256 (nt + 1), the rest of its K range being exact zeros
   int b_tri;
+  // unit order: M tiles innermost (for N >> M, so that the units sharing one B tile
+  // run together), else N tiles innermost
+  int m_inner;
   int* sched;  // unit counter (dynamic unit order), or nullptr for round-robin dealing
   int32_t* dev_status;
   uint64_t timeout_ns;
@@ -98,8 +101,12 @@ struct SelGemmProb {
     tma_prefetch_desc(&tmB);
   }
   __device__ int num_units() const { return Q * nS * m_tiles * n_tiles; }
-  // K extent of unit u and its number of kSelChunk-wide chunks (nt = u % n_tiles)
-  __device__ int k_ext(int u) const { return b_tri ? min(K, kBN * (u % n_tiles + 1)) : K; }
+  // K extent of unit u and its number of kSelChunk-wide chunks
+  __device__ int k_ext(int u) const {
+    if (!b_tri) return K;
+    const int nt = m_inner ? (u / m_tiles) % n_tiles : u % n_tiles;
+    return min(K, kBN * (nt + 1));
+  }
   __device__ int chunks(int u) const { return b_tri ? (k_ext(u) + kSelChunk - 1) / kSelChunk : n_chunks; }
   __device__ int num_subtiles(int u) const { return 6 * chunks(u); }
   __device__ int num_kb(int u, int sb) const {
@@ -107,12 +114,28 @@ struct SelGemmProb {
     return (min(kSelChunk, k_ext(u) - c * kSelChunk) + kBK - 1) / kBK;
   }
   __device__ void decode(int u, int& q, int& s, int& mt, int& nt) const {
-    nt = u % n_tiles;
-    u /= n_tiles;
-    mt = u % m_tiles;
-    const int p = u / m_tiles;
-    q = p / nS;
-    s = p - q * nS;
+    if (m_inner) {
+      mt = u % m_tiles;
+      u /= m_tiles;
+      nt = u % n_tiles;
+      u /= n_tiles;
+    } else {
+      nt = u % n_tiles;
+      u /= n_tiles;
+      mt = u % m_tiles;
+      u /= m_tiles;
+    }
+    q = u / nS;
+    s = u - q * nS;
+  }
+  // This thread's row of the β·C term: kCols floats from column n0 = nt·256 + col0.
+  __device__ const float* c_row(int u, int row, int col0, uint32_t rank) const {
+    int q, s, mt, nt;
+    decode(u, q, s, mt, nt);
+    const long long m = static_cast<long long>(mt) * Cfg::kUnitM + rank * kBM + row;
+    const long long n0 = static_cast<long long>(nt) * kBN + col0;
+    const long long bq = chosen != nullptr ? chosen[q] : 0;
+    return csrc + (q / q_per_kind) * c_kind + bq * c_b + q * c_q + s * c_s + m * ldc + n0;
   }
   struct Coords {
     int a_row, a_k, b_row, b_k;
@@ -164,12 +187,7 @@ struct SelGemmProb {
       return;
     }
     float4* o = reinterpret_cast<float4*>(out + q * o_q + s * o_s + m * ldo + n0);
-    const float4* cp = nullptr;
-    if (beta != 0.f) {
-      const long long bq = chosen != nullptr ? chosen[q] : 0;
-      cp = reinterpret_cast<const float4*>(csrc + (q / q_per_kind) * c_kind + bq * c_b + q * c_q + s * c_s + m * ldc +
-                                           n0);
-    }
+    const float4* cp = beta != 0.f ? reinterpret_cast<const float4*>(c_row(u, row, col0, rank)) : nullptr;
 #pragma unroll
     for (int i = 0; i < kCols / 4; ++i) {
       float4 v = make_float4(alpha * es.rs[4 * i], alpha * es.rs[4 * i + 1], alpha * es.rs[4 * i + 2],
@@ -708,6 +726,7 @@ struct SelGemm {
   int q_per_kind = 1;
   float* part = nullptr;
   bool b_tri = false;  // B is an L^-1 (lower triangular in row, K): skip its zero K range
+  bool m_inner = false;  // M tiles innermost in the unit order (N >> M)
   int stage = RF_STAGE_SELECT_GEMM;  // profiler stage of the launch
 };
 
@@ -746,6 +765,7 @@ static rf_status run_sel_gemm(SelCtx& c, const SelGemm& g) {
   pr.q_per_kind = g.q_per_kind;
   pr.part = g.part;
   pr.b_tri = g.b_tri ? 1 : 0;
+  pr.m_inner = g.m_inner ? 1 : 0;
   pr.sched = g.b_tri ? c.sched : nullptr;
   pr.dev_status = c.dev_status;
   pr.timeout_ns = wait_timeout_ns();
@@ -1089,7 +1109,7 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
         SelGemm g{};
         g.pa = lay.zbp, g.a_rows = rtrows, g.a_kext = F, g.a = op(Ft, 0, 0, 0, 0, 0);
         g.pb = lay.Wp, g.b_rows = wrows, g.b_kext = m_max, g.b = op(D, 0, 0, m, 0, 0);
-        g.Q = Q, g.M = Ft, g.N = static_cast<int>(D), g.K = F;
+        g.Q = Q, g.M = Ft, g.N = static_cast<int>(D), g.K = F, g.m_inner = true;
         g.alpha = -1.f, g.beta = 1.f;
         g.out = lay.RT, g.o_q = static_cast<long long>(Ft) * D, g.ldo = D;
         g.csrc = lay.RT, g.c_q = static_cast<long long>(Ft) * D, g.ldc = D;

@@ -202,6 +202,18 @@ def test_select_wide_layers_factor_on_tensor_cores_matches_oracle(flags):
     _check_against_oracle(cfg, ora, sel, r2, cfg.k, cfg.lam, "trace")
 
 
+@KERNELS
+def test_select_three_tile_layers_match_oracle(flags):
+    # F = 768 features per layer (6 x 128 heads): three 256-wide column tiles, so the
+    # products with an L^-1 operand stop at K = 256, 512 and 768 by tile column, and
+    # the Schur blocks (768 is not a multiple of 512) factor on the SIMT recursion
+    cfg = synth.SelectConfig("selection 4->2 layers 6x128 k3", 9, L_src=4, L_tgt=2, k=3, H=6, hd=128, n=4096, R=40,
+                             lam=0.01)
+    gpu, ora = _rows_and_stats(cfg, [0, 1], cfg.n)
+    sel, r2 = _select(cfg, gpu, cfg.k, cfg.lam, rf.RF_ALPHA_TRACE, flags=flags)
+    _check_against_oracle(cfg, ora, sel, r2, cfg.k, cfg.lam, "trace")
+
+
 def test_select_handles_a_target_without_variance():
     # a constant target has TSS = 0 in every head: its scores are 0 and the choice is layer 0 first
     cfg = synth.SELECT_SMALL
