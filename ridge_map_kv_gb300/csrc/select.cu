@@ -29,8 +29,9 @@
 //                            Rᵀ −= z_bᵀ wᵀ
 // Every product is fp32-accurate on the bf16 tensor cores: each fp32 operand is
 // split into three bf16 planes (k_split_rows) and the six plane products that
-// matter at fp32 precision are summed, 1024-wide K chunks in TMEM and in fp32
-// registers across chunks and terms. Operands are K-major rows of the planes;
+// matter at fp32 precision are summed: per 1024-wide K chunk the six terms run as
+// one TMEM accumulation, smallest first, and the chunks add in fp32 registers.
+// Operands are K-major rows of the planes;
 // which rows and columns a batch entry reads is linear in (term, problem, layer
 // slot, chosen layer), the chosen layer read on the device, so no step waits on
 // the host.
@@ -47,7 +48,11 @@ constexpr int kSelChunk = 1024;  // K rows summed in TMEM before the fp32 regist
 constexpr int kSelMaxKinds = 2;
 
 // Six plane products: term t multiplies A plane sel_term_a(t) by B plane sel_term_b(t):
-// hi·hi, mid·hi, hi·mid, lo·hi, mid·mid, hi·lo.
+// hi·hi, mid·hi, hi·mid, lo·hi, mid·mid, hi·lo. A chunk's accumulation takes them in
+// reverse, t = 5 .. 0: the terms of 2^-16 and 2^-8 of the product first, while the
+// accumulator is small, then hi·hi, so the fp32 accumulator's rounding is that of
+// hi·hi's own sum (one accumulator per term, added in registers, took the MMA
+// thread through six epilogue round trips per chunk).
 __device__ __forceinline__ int sel_term_a(int t) { return (0x012010 >> (4 * t)) & 3; }
 __device__ __forceinline__ int sel_term_b(int t) { return (0x210100 >> (4 * t)) & 3; }
 
@@ -108,9 +113,12 @@ struct SelGemmProb {
     return min(K, kBN * (nt + 1));
   }
   __device__ int chunks(int u) const { return b_tri ? (k_ext(u) + kSelChunk - 1) / kSelChunk : n_chunks; }
+  // Sub-tile sb = 6 c + j is term 5 - j of K chunk c; a chunk's six terms chain into
+  // one accumulator, smallest first (see sel_term_a), so the epilogue runs once a chunk.
   __device__ int num_subtiles(int u) const { return 6 * chunks(u); }
+  __device__ bool acc_continues(int, int sb) const { return sb % 6 != 0; }
   __device__ int num_kb(int u, int sb) const {
-    const int c = sb % chunks(u);
+    const int c = sb / 6;
     return (min(kSelChunk, k_ext(u) - c * kSelChunk) + kBK - 1) / kBK;
   }
   __device__ void decode(int u, int& q, int& s, int& mt, int& nt) const {
@@ -143,8 +151,7 @@ struct SelGemmProb {
   __device__ Coords coords(int u, int sb, uint32_t rank) const {
     int q, s, mt, nt;
     decode(u, q, s, mt, nt);
-    const int nch = chunks(u);
-    const int t = sb / nch, c = sb - t * nch;
+    const int c = sb / 6, t = 5 - (sb - 6 * c);
     const long long bq = chosen != nullptr ? chosen[q] : 0;
     Coords r;
     r.a_row = static_cast<int>(sel_term_a(t) * a.plane_rows + q * a.q_rows + s * a.s_rows + bq * a.b_rows +
@@ -166,7 +173,7 @@ struct SelGemmProb {
       tmem_ld32(tacc + ch * 32, v);
       tmem_wait_ld32(v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) es.rs[ch * 32 + i] = sb == 0 ? u2f(v[i]) : es.rs[ch * 32 + i] + u2f(v[i]);
+      for (int i = 0; i < 32; ++i) es.rs[ch * 32 + i] = sb < 6 ? u2f(v[i]) : es.rs[ch * 32 + i] + u2f(v[i]);
     }
   }
   __device__ void epilogue_after(EpiState& es, int u, int sb, int nsub, int row, int col0, uint32_t rank) const {
@@ -287,13 +294,15 @@ struct TriGemmProb {
     k_range(mt, nt, lo, hi);
     return (hi - lo + kTriChunk - 1) / kTriChunk;
   }
+  // Sub-tile sb = 6 c + j is term 5 - j of K chunk c, the six chained into one
+  // accumulation, smallest first (as in SelGemmProb).
   __device__ int num_subtiles(int u) const { return 6 * n_chunks(u); }
+  __device__ bool acc_continues(int, int sb) const { return sb % 6 != 0; }
   __device__ int num_kb(int u, int sb) const {
     int s, mt, nt, lo, hi;
     decode(u, s, mt, nt);
     k_range(mt, nt, lo, hi);
-    const int nch = (hi - lo + kTriChunk - 1) / kTriChunk;
-    const int c = sb % nch;
+    const int c = sb / 6;
     return (min(kTriChunk, hi - lo - c * kTriChunk) + kBK - 1) / kBK;
   }
   struct Coords {
@@ -303,8 +312,7 @@ struct TriGemmProb {
     int s, mt, nt, lo, hi;
     decode(u, s, mt, nt);
     k_range(mt, nt, lo, hi);
-    const int nch = (hi - lo + kTriChunk - 1) / kTriChunk;
-    const int t = sb / nch, c = sb - t * nch;
+    const int c = sb / 6, t = 5 - (sb - 6 * c);
     Coords r;
     r.a_row = static_cast<int>(sel_term_a(t) * plane_rows + static_cast<long long>(s) * h +
                                static_cast<long long>(mt) * Cfg::kUnitM + rank * kBM);
@@ -324,7 +332,7 @@ struct TriGemmProb {
       tmem_ld32(tacc + ch * 32, v);
       tmem_wait_ld32(v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) es.rs[ch * 32 + i] = sb == 0 ? u2f(v[i]) : es.rs[ch * 32 + i] + u2f(v[i]);
+      for (int i = 0; i < 32; ++i) es.rs[ch * 32 + i] = sb < 6 ? u2f(v[i]) : es.rs[ch * 32 + i] + u2f(v[i]);
     }
   }
   __device__ void epilogue_after(EpiState& es, int u, int sb, int nsub, int row, int col0, uint32_t rank) const {

@@ -32,7 +32,10 @@
 // The problem type `Prob` decides the work: how many units there are, how many
 // independent accumulations ("sub-tiles") a unit holds, the K-blocks of each,
 // which TMA boxes a CTA loads for a K-block, and what the epilogue does with a
-// finished 128-row x 256-column fp32 block. The producer asks the problem once
+// finished 128-row x 256-column fp32 block. A problem may chain sub-tiles into one
+// accumulation with `acc_continues(u, sb)`: true when sub-tile sb adds into the
+// accumulator of sub-tile sb - 1, so the MMAs run on without an epilogue between
+// them and the epilogue sees only the chain's last sub-tile. The producer asks the problem once
 // per (unit, sub-tile) for its `Coords` (`coords(u, sb)`), and per K-block only
 // issues the loads from them (`issue_loads(c, kb, ...)`): one thread issues every
 // copy of the CTA, so any per-K-block arithmetic or memory read there would
@@ -107,6 +110,17 @@ template <class P, class = void>
 struct HasSched : std::false_type {};
 template <class P>
 struct HasSched<P, std::void_t<decltype(std::declval<const P&>().sched)>> : std::true_type {};
+// Chained sub-tiles (see above): the problem's `acc_continues`, or none.
+template <class P, class = void>
+struct HasAccChain : std::false_type {};
+template <class P>
+struct HasAccChain<P, std::void_t<decltype(std::declval<const P&>().acc_continues(0, 0))>> : std::true_type {};
+template <class Prob>
+__device__ __forceinline__ bool acc_continues(const Prob& p, int u, int sb) {
+  if constexpr (HasAccChain<Prob>::value) return sb > 0 && p.acc_continues(u, sb);
+  else return false;
+}
+
 template <class Prob>
 __host__ __device__ __forceinline__ int* sched_of(const Prob& p) {
   if constexpr (HasSched<Prob>::value) return p.sched;
@@ -378,10 +392,13 @@ __global__ void __launch_bounds__(gemm_threads<Prob>(), 1) tc_gemm_kernel(const 
            u >= 0;
            u = consumer_next(sh, sched, u, stride, n_units, uslot, uphase, false, false, abort_flag, timeout)) {
         const int nsub = prob.num_subtiles(u);
-        for (int sb = 0; sb < nsub; ++sb, ++it) {
+        for (int sb = 0; sb < nsub; ++sb) {
           const uint32_t acc = it & 1u;
-          if (!mbar_wait(&sh->tmem_empty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, timeout)) goto mma_done;
-          tc_fence_after();
+          const bool cont = acc_continues(prob, u, sb);
+          if (!cont) {
+            if (!mbar_wait(&sh->tmem_empty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, timeout)) goto mma_done;
+            tc_fence_after();
+          }
           const uint32_t d_tmem = tmem_base + acc * kBN;
           const int nkb = prob.num_kb(u, sb);
           for (int kb = 0; kb < nkb; ++kb) {
@@ -390,14 +407,17 @@ __global__ void __launch_bounds__(gemm_threads<Prob>(), 1) tc_gemm_kernel(const 
             const uint64_t soff = static_cast<uint64_t>((stage * Cfg::kStageBytes) >> 4);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-              tc_mma_bf16(d_tmem, adesc[k] + soff, bdesc[k] + soff, idesc, (kb | k) != 0 ? 1u : 0u);
+              tc_mma_bf16(d_tmem, adesc[k] + soff, bdesc[k] + soff, idesc, (cont || (kb | k) != 0) ? 1u : 0u);
             tc_commit(&sh->empty[stage]);
             if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
-          tc_commit(&sh->tmem_full[acc]);
+          if (sb + 1 == nsub || !acc_continues(prob, u, sb + 1)) {
+            tc_commit(&sh->tmem_full[acc]);
+            ++it;
+          }
         }
       }
     mma_done:
@@ -416,7 +436,8 @@ __global__ void __launch_bounds__(gemm_threads<Prob>(), 1) tc_gemm_kernel(const 
     for (int u = consumer_next(sh, sched, first, stride, n_units, uslot, uphase, true, false, abort_flag, timeout);
          u >= 0; u = consumer_next(sh, sched, u, stride, n_units, uslot, uphase, true, false, abort_flag, timeout)) {
       const int nsub = prob.num_subtiles(u);
-      for (int sb = 0; sb < nsub; ++sb, ++it) {
+      for (int sb = 0; sb < nsub; ++sb) {
+        if (sb + 1 < nsub && acc_continues(prob, u, sb + 1)) continue;  // not the end of a chain
         const uint32_t acc = it & 1u;
         bool ok = mbar_wait(&sh->tmem_full[acc], (it >> 1) & 1u, abort_flag, timeout);
         ok = __all_sync(0xffffffffu, ok);
@@ -428,6 +449,7 @@ __global__ void __launch_bounds__(gemm_threads<Prob>(), 1) tc_gemm_kernel(const 
         tc_fence_before();
         mbar_arrive(&sh->tmem_empty[acc]);
         prob.epilogue_after(es, u, sb, nsub, row, col0, 0u);
+        ++it;
       }
     }
   epi_done:;
@@ -573,10 +595,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>()
            u >= 0;
            u = consumer_next(sh, sched, u, n_pairs, n_units, uslot, uphase, false, false, abort_flag, timeout)) {
         const int nsub = prob.num_subtiles(u);
-        for (int sb = 0; sb < nsub; ++sb, ++it) {
+        for (int sb = 0; sb < nsub; ++sb) {
           const uint32_t acc = it & 1u;
-          if (!mbar_wait<true>(&sh->tmem_empty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, timeout)) goto mma_done;
-          tc_fence_after();
+          const bool cont = acc_continues(prob, u, sb);
+          if (!cont) {
+            if (!mbar_wait<true>(&sh->tmem_empty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, timeout)) goto mma_done;
+            tc_fence_after();
+          }
           const uint32_t d_tmem = tmem_base + acc * kBN;
           const int nst = (prob.num_kb(u, sb) + Cfg::kAtoms - 1) / Cfg::kAtoms;
           for (int st = 0; st < nst; ++st) {
@@ -585,14 +610,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>()
             const uint64_t soff = static_cast<uint64_t>((stage * Cfg::kStageBytes) >> 4);
 #pragma unroll
             for (int k = 0; k < kSlices; ++k)
-              tc_mma_bf16_pair(d_tmem, adesc[k] + soff, bdesc[k] + soff, idesc, (st | k) != 0 ? 1u : 0u);
+              tc_mma_bf16_pair(d_tmem, adesc[k] + soff, bdesc[k] + soff, idesc, (cont || (st | k) != 0) ? 1u : 0u);
             tc_commit_pair_multicast(&sh->empty[stage], 0x3);
             if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
-          tc_commit_pair_multicast(&sh->tmem_full[acc], 0x3);
+          if (sb + 1 == nsub || !acc_continues(prob, u, sb + 1)) {
+            tc_commit_pair_multicast(&sh->tmem_full[acc], 0x3);
+            ++it;
+          }
         }
       }
     mma_done:
@@ -610,7 +638,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>()
     for (int u = consumer_next(sh, sched, first, n_pairs, n_units, uslot, uphase, true, rank != 0, abort_flag, timeout);
          u >= 0; u = consumer_next(sh, sched, u, n_pairs, n_units, uslot, uphase, true, rank != 0, abort_flag, timeout)) {
       const int nsub = prob.num_subtiles(u);
-      for (int sb = 0; sb < nsub; ++sb, ++it) {
+      for (int sb = 0; sb < nsub; ++sb) {
+        if (sb + 1 < nsub && acc_continues(prob, u, sb + 1)) continue;  // not the end of a chain
         const uint32_t acc = it & 1u;
         bool ok = mbar_wait(&sh->tmem_full[acc], (it >> 1) & 1u, abort_flag, timeout);
         ok = __all_sync(0xffffffffu, ok);
@@ -623,6 +652,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>()
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sh->tmem_empty[acc]), 0));
         prob.epilogue_after(es, u, sb, nsub, row, col0, rank);
+        ++it;
       }
     }
   epi_done:;
