@@ -809,9 +809,11 @@ __global__ void __launch_bounds__(256) k_split3(const float* __restrict__ src, _
 // out_p = alpha · A_p B + beta · out_p for p < P on the tensor cores, A_p [M][K]
 // and Bᵀ [N][K] given as three bf16 planes each (K-major): planes A [3][P][M][K],
 // B [3][N][K]. Unit: (p, M-tile, N-tile), N fastest so an A strip is reused at
-// once. Sub-tile sb: product term sb / n_chunks over the K chunk sb % n_chunks.
-// Eight epilogue warps keep fp32 running sums of their 128 columns across all
-// sub-tiles and write the tile once at the end.
+// once. Sub-tile sb = 6 c + j: product term 5 - j over the K chunk c; a chunk's terms
+// chain into one TMEM accumulation, smallest first and hi·hi last, so the fp32
+// accumulator's rounding is that of hi·hi's own sum, and terms beyond the planned
+// count have no K-blocks. Eight epilogue warps keep fp32 running sums of their 128
+// columns across the chunks and write the tile once at the end.
 // --------------------------------------------------------------------------
 __constant__ int kTermA[6] = {0, 1, 0, 2, 1, 0};  // hi·hi, mid·hi, hi·mid, lo·hi, mid·mid, hi·lo
 __constant__ int kTermB[6] = {0, 0, 1, 0, 1, 2};
@@ -842,9 +844,11 @@ struct Split3Prob {
     tma_prefetch_desc(&tmB);
   }
   __device__ int num_units() const { return P * m_tiles * n_tiles; }
-  __device__ int num_subtiles(int) const { return (n_terms != nullptr ? *n_terms : 6) * n_chunks; }
+  __device__ int num_subtiles(int) const { return 6 * n_chunks; }
+  __device__ bool acc_continues(int, int sb) const { return sb % 6 != 0; }
   __device__ int num_kb(int, int sb) const {
-    const int c = sb % n_chunks;
+    const int c = sb / 6, t = 5 - (sb - 6 * c);
+    if (n_terms != nullptr && t >= *n_terms) return 0;
     return (min(kSplitChunk, K - c * kSplitChunk) + kBK - 1) / kBK;
   }
   __device__ void decode(int u, int& p, int& mt, int& nt) const {
@@ -859,7 +863,7 @@ struct Split3Prob {
   __device__ Coords coords(int u, int sb, uint32_t rank) const {
     int p, mt, nt;
     decode(u, p, mt, nt);
-    const int t = sb / n_chunks, c = sb - t * n_chunks;
+    const int c = sb / 6, t = 5 - (sb - 6 * c);
     return {(kTermA[t] * P + p) * M + mt * Cfg::kUnitM + static_cast<int>(rank) * kBM,
             kTermB[t] * N + nt * kBN + static_cast<int>(rank) * Cfg::kBRows, c * kSplitChunk};
   }
@@ -874,7 +878,7 @@ struct Split3Prob {
       tmem_ld32(tacc + ch * 32, v);
       tmem_wait_ld32(v);
 #pragma unroll
-      for (int q = 0; q < 32; ++q) es.rs[ch * 32 + q] = sb == 0 ? u2f(v[q]) : es.rs[ch * 32 + q] + u2f(v[q]);
+      for (int q = 0; q < 32; ++q) es.rs[ch * 32 + q] = sb < 6 ? u2f(v[q]) : es.rs[ch * 32 + q] + u2f(v[q]);
     }
   }
   __device__ void epilogue_after(EpiState& es, int u, int sb, int nsub, int row, int col0, uint32_t rank) const {

@@ -35,7 +35,9 @@
 // finished 128-row x 256-column fp32 block. A problem may chain sub-tiles into one
 // accumulation with `acc_continues(u, sb)`: true when sub-tile sb adds into the
 // accumulator of sub-tile sb - 1, so the MMAs run on without an epilogue between
-// them and the epilogue sees only the chain's last sub-tile. The producer asks the problem once
+// them and the epilogue sees only the chain's last sub-tile. Sub-tiles of a chain
+// may have no K-blocks (the chain's first MMA, wherever it falls, starts the sum),
+// but every chain needs at least one. The producer asks the problem once
 // per (unit, sub-tile) for its `Coords` (`coords(u, sb)`), and per K-block only
 // issues the loads from them (`issue_loads(c, kb, ...)`): one thread issues every
 // copy of the CTA, so any per-K-block arithmetic or memory read there would
@@ -388,6 +390,7 @@ __global__ void __launch_bounds__(gemm_threads<Prob>(), 1) tc_gemm_kernel(const 
       int stage = 0;
       uint32_t phase = 0;
       uint32_t it = 0;
+      bool fresh = true;  // no MMA has written the current accumulation yet
       for (int u = consumer_next(sh, sched, first, stride, n_units, uslot, uphase, false, false, abort_flag, timeout);
            u >= 0;
            u = consumer_next(sh, sched, u, stride, n_units, uslot, uphase, false, false, abort_flag, timeout)) {
@@ -400,14 +403,17 @@ __global__ void __launch_bounds__(gemm_threads<Prob>(), 1) tc_gemm_kernel(const 
             tc_fence_after();
           }
           const uint32_t d_tmem = tmem_base + acc * kBN;
+          if (!cont) fresh = true;
           const int nkb = prob.num_kb(u, sb);
           for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&sh->full[stage], phase, abort_flag, timeout)) goto mma_done;
             tc_fence_after();
             const uint64_t soff = static_cast<uint64_t>((stage * Cfg::kStageBytes) >> 4);
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              tc_mma_bf16(d_tmem, adesc[k] + soff, bdesc[k] + soff, idesc, (cont || (kb | k) != 0) ? 1u : 0u);
+            for (int k = 0; k < kBK / 16; ++k) {
+              tc_mma_bf16(d_tmem, adesc[k] + soff, bdesc[k] + soff, idesc, fresh ? 0u : 1u);
+              fresh = false;
+            }
             tc_commit(&sh->empty[stage]);
             if (++stage == Cfg::kStages) {
               stage = 0;
@@ -591,6 +597,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>()
       int stage = 0;
       uint32_t phase = 0;
       uint32_t it = 0;
+      bool fresh = true;  // no MMA has written the current accumulation yet
       for (int u = consumer_next(sh, sched, first, n_pairs, n_units, uslot, uphase, false, false, abort_flag, timeout);
            u >= 0;
            u = consumer_next(sh, sched, u, n_pairs, n_units, uslot, uphase, false, false, abort_flag, timeout)) {
@@ -603,14 +610,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Prob>()
             tc_fence_after();
           }
           const uint32_t d_tmem = tmem_base + acc * kBN;
+          if (!cont) fresh = true;
           const int nst = (prob.num_kb(u, sb) + Cfg::kAtoms - 1) / Cfg::kAtoms;
           for (int st = 0; st < nst; ++st) {
             if (!mbar_wait(&sh->full[stage], phase, abort_flag, timeout)) goto mma_done;
             tc_fence_after();
             const uint64_t soff = static_cast<uint64_t>((stage * Cfg::kStageBytes) >> 4);
 #pragma unroll
-            for (int k = 0; k < kSlices; ++k)
-              tc_mma_bf16_pair(d_tmem, adesc[k] + soff, bdesc[k] + soff, idesc, (cont || (st | k) != 0) ? 1u : 0u);
+            for (int k = 0; k < kSlices; ++k) {
+              tc_mma_bf16_pair(d_tmem, adesc[k] + soff, bdesc[k] + soff, idesc, fresh ? 0u : 1u);
+              fresh = false;
+            }
             tc_commit_pair_multicast(&sh->empty[stage], 0x3);
             if (++stage == Cfg::kStages) {
               stage = 0;
