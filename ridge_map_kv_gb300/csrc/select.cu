@@ -24,7 +24,8 @@
 //                            cores, narrower ones fp32 SIMT, 128-wide leaves in
 //                            shared memory
 //   SelGemm (sum of squares) z_sᵀ = R_sᵀ L_s^-ᵀ, only colsum(z_s²) is kept
-//   k_sel_score              scores, the joint argmax, the tables, e += gain
+//   k_sel_layer_scores       every (target, kind, layer)'s score and its table entry
+//   k_sel_choose             the joint argmax, the choice, e += gain
 //   SelGemm                  z_bᵀ;  H[:, b] − W W_bᵀ;  × L_b^-ᵀ;  Σ_s −= w wᵀ;
 //                            Rᵀ −= z_bᵀ wᵀ
 // Every product is fp32-accurate on the bf16 tensor cores: each fp32 operand is
@@ -46,6 +47,7 @@ namespace rf {
 
 constexpr int kSelChunk = 1024;  // K rows summed in TMEM before the fp32 register sum
 constexpr int kSelMaxKinds = 2;
+enum { kSkipNone = 0, kSkipSlot = 1, kSkipMRows = 2, kSkipNCols = 3 };  // SelGemmProb::skip
 
 // Six plane products: term t multiplies A plane sel_term_a(t) by B plane sel_term_b(t):
 // hi·hi, mid·hi, hi·mid, lo·hi, mid·mid, hi·lo. A chunk's accumulation takes them in
@@ -88,6 +90,11 @@ struct SelGemmProb {
   // unit order: M tiles innermost (for N >> M, so that the units sharing one B tile
   // run together), else N tiles innermost
   int m_inner;
+  // Units of a layer already chosen for the problem's target (mask[(q % mask_g) *
+  // mask_ls + layer] != 0) run nothing: the layer is the batch slot s (kSkipSlot),
+  // the M tile's (kSkipMRows, M = D rows of F per layer) or the N tile's (kSkipNCols).
+  const uint8_t* mask;
+  int skip, mask_g, mask_ls, layer_f;
   int* sched;  // unit counter (dynamic unit order), or nullptr for round-robin dealing
   int32_t* dev_status;
   uint64_t timeout_ns;
@@ -115,11 +122,18 @@ struct SelGemmProb {
   __device__ int chunks(int u) const { return b_tri ? (k_ext(u) + kSelChunk - 1) / kSelChunk : n_chunks; }
   // Sub-tile sb = 6 c + j is term 5 - j of K chunk c; a chunk's six terms chain into
   // one accumulator, smallest first (see sel_term_a), so the epilogue runs once a chunk.
-  __device__ int num_subtiles(int u) const { return 6 * chunks(u); }
+  __device__ int num_subtiles(int u) const { return skipped(u) ? 0 : 6 * chunks(u); }
   __device__ bool acc_continues(int, int sb) const { return sb % 6 != 0; }
   __device__ int num_kb(int u, int sb) const {
     const int c = sb / 6;
     return (min(kSelChunk, k_ext(u) - c * kSelChunk) + kBK - 1) / kBK;
+  }
+  __device__ bool skipped(int u) const {
+    if (skip == kSkipNone) return false;
+    int q, s, mt, nt;
+    decode(u, q, s, mt, nt);
+    const int layer = skip == kSkipSlot ? s : skip == kSkipMRows ? mt * Cfg::kUnitM / layer_f : nt * kBN / layer_f;
+    return mask[(q % mask_g) * mask_ls + layer] != 0;
   }
   __device__ void decode(int u, int& q, int& s, int& mt, int& nt) const {
     if (m_inner) {
@@ -516,50 +530,66 @@ __global__ void __launch_bounds__(256) k_sel_mask_identity(const uint8_t* __rest
   }
 }
 
-// One CTA per target g: for every kind and layer not yet chosen, gain_o = Σ partials
-// of colsum(z_s²); score = mean_h (Σ_{o∈h}(e_o + gain_o)) / Σ_{o∈h} TSS_o (0 for a
-// head without variance); joint = mean over kinds; the first layer with the
-// highest joint score is chosen. Writes the tables, the choice, the mask and e.
-__global__ void __launch_bounds__(256) k_sel_score(const float* __restrict__ part, int n_part, int G, int n_kinds,
-                                                   int Ls, int Ft, int hd, int t0, int n_targets, int k, int j,
-                                                   const double* __restrict__ tss, double* __restrict__ expl,
-                                                   uint8_t* __restrict__ mask, int32_t* __restrict__ chosen,
-                                                   int32_t* __restrict__ sel, float* __restrict__ r2) {
-  extern __shared__ double sh[];  // [n_kinds][Ls] scores
-  const int g = blockIdx.x, t = t0 + g;
+// Scores of every (target g, kind, layer s), one CTA each (grid n_kinds·Ls x G),
+// a warp per head (heads beyond the warps taken in turn): gain_o = Σ partials of
+// colsum(z_s²), score = mean_h (Σ_{o∈h}(e_o + gain_o)) / Σ_{o∈h} TSS_o (0 for a head
+// without variance); a layer already chosen scores 0 and NaN in the table. The heads
+// add in order, so with at most 8 heads the sums are those of one warp taking
+// every head in turn.
+__global__ void __launch_bounds__(256) k_sel_layer_scores(const float* __restrict__ part, int n_part, int G,
+                                                          int n_kinds, int Ls, int Ft, int hd, int t0, int n_targets,
+                                                          int k, int j, const double* __restrict__ tss,
+                                                          const double* __restrict__ expl,
+                                                          const uint8_t* __restrict__ mask, double* __restrict__ scores,
+                                                          float* __restrict__ r2) {
+  __shared__ double hs[8];
+  const int ks = blockIdx.x, g = blockIdx.y, t = t0 + g;
+  const int kind = ks / Ls, s = ks - kind * Ls, q = kind * G + g;
   const int nh = Ft / hd;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  const uint8_t* mk = mask + g * Ls;
-  // scores: one warp per (kind, layer); heads in turn, the warp summing a head's columns
-  for (int ks = warp; ks < n_kinds * Ls; ks += nwarps) {
-    const int kind = ks / Ls, s = ks - kind * Ls;
-    const int q = kind * G + g;
-    double score = 0.0;
-    if (!mk[s]) {
-      const float* pp = part + (static_cast<size_t>(q) * Ls + s) * Ft * n_part;
-      for (int h = 0; h < nh; ++h) {
-        double num = 0.0, den = 0.0;
-        for (int o = h * hd + lane; o < (h + 1) * hd; o += 32) {
-          double gsum = 0.0;
-          for (int i = 0; i < n_part; ++i) gsum += static_cast<double>(pp[static_cast<size_t>(o) * n_part + i]);
-          num += expl[static_cast<size_t>(q) * Ft + o] + gsum;
-          den += tss[static_cast<size_t>(q) * Ft + o];
-        }
-        for (int off = 16; off > 0; off >>= 1) {
-          num += __shfl_xor_sync(0xffffffffu, num, off);
-          den += __shfl_xor_sync(0xffffffffu, den, off);
-        }
-        score += den > 0.0 ? num / den : 0.0;
-      }
-      score /= nh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t r2i = ((static_cast<size_t>(kind) * n_targets + t) * k + j) * Ls + s;
+  if (mask[g * Ls + s]) {
+    if (threadIdx.x == 0) {
+      scores[(static_cast<size_t>(g) * n_kinds + kind) * Ls + s] = 0.0;
+      if (r2 != nullptr) r2[r2i] = nanf("");
     }
-    if (lane == 0) {
-      sh[ks] = score;
-      if (r2 != nullptr)
-        r2[((static_cast<size_t>(kind) * n_targets + t) * k + j) * Ls + s] = mk[s] ? nanf("") : static_cast<float>(score);
-    }
+    return;
   }
+  const float* pp = part + (static_cast<size_t>(q) * Ls + s) * Ft * n_part;
+  double acc = 0.0;
+  for (int h = warp; h < nh; h += 8) {
+    double num = 0.0, den = 0.0;
+    for (int o = h * hd + lane; o < (h + 1) * hd; o += 32) {
+      double gsum = 0.0;
+      for (int i = 0; i < n_part; ++i) gsum += static_cast<double>(pp[static_cast<size_t>(o) * n_part + i]);
+      num += expl[static_cast<size_t>(q) * Ft + o] + gsum;
+      den += tss[static_cast<size_t>(q) * Ft + o];
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+      num += __shfl_xor_sync(0xffffffffu, num, off);
+      den += __shfl_xor_sync(0xffffffffu, den, off);
+    }
+    acc += den > 0.0 ? num / den : 0.0;
+  }
+  if (lane == 0) hs[warp] = acc;
   __syncthreads();
+  if (threadIdx.x == 0) {
+    double score = 0.0;
+    for (int w = 0; w < 8 && w < nh; ++w) score += hs[w];
+    score /= nh;
+    scores[(static_cast<size_t>(g) * n_kinds + kind) * Ls + s] = score;
+    if (r2 != nullptr) r2[r2i] = static_cast<float>(score);
+  }
+}
+
+// One CTA per target g: the first layer not yet chosen with the highest joint
+// score (the mean over kinds) is chosen; writes the choice, the mask and e += gain.
+__global__ void __launch_bounds__(256) k_sel_choose(const double* __restrict__ scores, const float* __restrict__ part,
+                                                    int n_part, int G, int n_kinds, int Ls, int Ft, int t0, int k,
+                                                    int j, double* __restrict__ expl, uint8_t* __restrict__ mask,
+                                                    int32_t* __restrict__ chosen, int32_t* __restrict__ sel) {
+  const int g = blockIdx.x, t = t0 + g;
+  const uint8_t* mk = mask + g * Ls;
   __shared__ int best_s;
   if (threadIdx.x == 0) {
     int best = -1;
@@ -567,7 +597,7 @@ __global__ void __launch_bounds__(256) k_sel_score(const float* __restrict__ par
     for (int s = 0; s < Ls; ++s) {
       if (mk[s]) continue;
       double v = 0.0;
-      for (int kind = 0; kind < n_kinds; ++kind) v += sh[kind * Ls + s];
+      for (int kind = 0; kind < n_kinds; ++kind) v += scores[(static_cast<size_t>(g) * n_kinds + kind) * Ls + s];
       v /= n_kinds;
       if (best < 0 || v > bv) {
         best = s;
@@ -632,6 +662,7 @@ struct SelLayout {
   __nv_bfloat16* Xp;  // [3][Qmax * D][F]
   double* tss;      // [Qmax][Ft]
   double* expl;     // [Qmax][Ft]
+  double* scores;   // [Gmax][n_kinds][Ls] this step's layer scores
   int32_t* chosen;  // [Qmax]
   uint8_t* mask;    // [Gmax][Ls]
   int* sched;       // unit counter of the dynamically ordered products
@@ -671,6 +702,7 @@ static SelLayout sel_layout(const rf_select_desc* d, void* ws) {
   l.Xp = c.take<__nv_bfloat16>(3 * Q * D * F);
   l.tss = c.take<double>(Q * Ft);
   l.expl = c.take<double>(Q * Ft);
+  l.scores = c.take<double>(Gm * NK * Ls);
   l.chosen = c.take<int32_t>(Q);
   l.mask = c.take<uint8_t>(Gm * Ls);
   l.sched = c.take<int>(1);
@@ -735,6 +767,9 @@ struct SelGemm {
   float* part = nullptr;
   bool b_tri = false;  // B is an L^-1 (lower triangular in row, K): skip its zero K range
   bool m_inner = false;  // M tiles innermost in the unit order (N >> M)
+  int skip = kSkipNone;  // which layer index marks a unit of an already chosen layer
+  const uint8_t* mask = nullptr;
+  int mask_g = 1, mask_ls = 1, layer_f = 1;
   int stage = RF_STAGE_SELECT_GEMM;  // profiler stage of the launch
 };
 
@@ -774,7 +809,15 @@ static rf_status run_sel_gemm(SelCtx& c, const SelGemm& g) {
   pr.part = g.part;
   pr.b_tri = g.b_tri ? 1 : 0;
   pr.m_inner = g.m_inner ? 1 : 0;
-  pr.sched = g.b_tri ? c.sched : nullptr;
+  pr.skip = g.mask != nullptr ? g.skip : kSkipNone;
+  pr.mask = g.mask;
+  pr.mask_g = g.mask_g;
+  pr.mask_ls = g.mask_ls;
+  pr.layer_f = g.layer_f;
+  // Dynamic order wherever units differ in length (triangle skipping) or some run
+  // nothing (chosen layers): dealt round-robin, the pairs that skip run ahead of
+  // the ones reading the same operand tiles, and those tiles leave L2 between them.
+  pr.sched = g.b_tri || g.mask != nullptr ? c.sched : nullptr;
   pr.dev_status = c.dev_status;
   pr.timeout_ns = wait_timeout_ns();
   ProfScope prof(c.s, g.stage);
@@ -1012,8 +1055,6 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
       kinds.n[kind] = lay.nn + kind;
     }
   }
-  const size_t score_smem = sizeof(double) * NK * Ls;
-
   for (int t0 = 0; t0 < T; t0 += Gm) {
     const int G = std::min(Gm, T - t0), Q = NK * G;
     {
@@ -1054,14 +1095,17 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
         g.pa = lay.RTp, g.a_rows = rtrows, g.a_kext = D, g.a = op(Ft, 0, 0, 0, F, 0);
         g.pb = lay.Lp, g.b_rows = lrows, g.b_kext = F, g.b = op(static_cast<long long>(Ls) * F, F, 0, 0, 0, 0);
         g.Q = Q, g.nS = Ls, g.M = Ft, g.N = F, g.K = F, g.b_tri = true;
+        g.mask = lay.mask, g.mask_g = G, g.mask_ls = Ls, g.layer_f = F, g.skip = kSkipSlot;
         g.part = lay.part;
         if ((st = sel_gemm(c, g)) != RF_OK) return st;
       }
       {
         ProfScope pf(c.s, RF_STAGE_SELECT_SCORE);
-        k_sel_score<<<G, 256, score_smem, c.s>>>(lay.part, n_part, G, NK, Ls, Ft, hd, t0, T, K, j, lay.tss, lay.expl,
-                                                 lay.mask, lay.chosen, src_layers, r2);
-        if ((st = cuda_check(cudaGetLastError(), "k_sel_score launch")) != RF_OK) return st;
+        k_sel_layer_scores<<<dim3(static_cast<unsigned>(NK * Ls), static_cast<unsigned>(G)), 256, 0, c.s>>>(
+            lay.part, n_part, G, NK, Ls, Ft, hd, t0, T, K, j, lay.tss, lay.expl, lay.mask, lay.scores, r2);
+        k_sel_choose<<<G, 256, 0, c.s>>>(lay.scores, lay.part, n_part, G, NK, Ls, Ft, t0, K, j, lay.expl, lay.mask,
+                                         lay.chosen, src_layers);
+        if ((st = cuda_check(cudaGetLastError(), "score launches")) != RF_OK) return st;
       }
       if (j == K - 1) break;
       // z_bᵀ = R_bᵀ L_b^-ᵀ
@@ -1084,6 +1128,7 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
         g.pa = lay.Wp, g.a_rows = wrows, g.a_kext = m_max, g.a = op(D, 0, 0, 0, 0, 0);
         g.pb = lay.Wp, g.b_rows = wrows, g.b_kext = m_max, g.b = op(D, 0, F, 0, 0, 0);
         g.chosen = lay.chosen, g.Q = Q, g.M = static_cast<int>(D), g.N = F, g.K = static_cast<int>(m);
+        g.mask = lay.mask, g.mask_g = G, g.mask_ls = Ls, g.layer_f = F, g.skip = kSkipMRows;
         g.alpha = -1.f, g.beta = 1.f;
         g.out = lay.X, g.o_q = D * F, g.ldo = F;
         g.csrc = lay.H, g.c_kind = D * D, g.c_b = F, g.ldc = D, g.q_per_kind = G;
@@ -1096,6 +1141,7 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
         g.pa = lay.Xp, g.a_rows = wrows, g.a_kext = F, g.a = op(D, 0, 0, 0, 0, 0);
         g.pb = lay.Lp, g.b_rows = lrows, g.b_kext = F, g.b = op(static_cast<long long>(Ls) * F, 0, F, 0, 0, 0);
         g.chosen = lay.chosen, g.Q = Q, g.M = static_cast<int>(D), g.N = F, g.K = F, g.b_tri = true;
+        g.mask = lay.mask, g.mask_g = G, g.mask_ls = Ls, g.layer_f = F, g.skip = kSkipMRows;
         g.out = lay.X, g.o_q = D * F, g.ldo = F;
         if ((st = sel_gemm(c, g)) != RF_OK) return st;
       }
@@ -1106,6 +1152,7 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
         g.pa = lay.Wp, g.a_rows = wrows, g.a_kext = m_max, g.a = op(D, F, 0, m, 0, 0);
         g.pb = lay.Wp, g.b_rows = wrows, g.b_kext = m_max, g.b = op(D, F, 0, m, 0, 0);
         g.Q = Q, g.nS = Ls, g.M = F, g.N = F, g.K = F;
+        g.mask = lay.mask, g.mask_g = G, g.mask_ls = Ls, g.layer_f = F, g.skip = kSkipSlot;
         g.alpha = -1.f, g.beta = 1.f;
         g.out = lay.Sig, g.o_q = static_cast<long long>(Ls) * F * F, g.o_s = static_cast<long long>(F) * F, g.ldo = F;
         g.csrc = lay.Sig, g.c_q = static_cast<long long>(Ls) * F * F, g.c_s = static_cast<long long>(F) * F,
@@ -1118,6 +1165,7 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
         g.pa = lay.zbp, g.a_rows = rtrows, g.a_kext = F, g.a = op(Ft, 0, 0, 0, 0, 0);
         g.pb = lay.Wp, g.b_rows = wrows, g.b_kext = m_max, g.b = op(D, 0, 0, m, 0, 0);
         g.Q = Q, g.M = Ft, g.N = static_cast<int>(D), g.K = F, g.m_inner = true;
+        g.mask = lay.mask, g.mask_g = G, g.mask_ls = Ls, g.layer_f = F, g.skip = kSkipNCols;
         g.alpha = -1.f, g.beta = 1.f;
         g.out = lay.RT, g.o_q = static_cast<long long>(Ft) * D, g.ldo = D;
         g.csrc = lay.RT, g.c_q = static_cast<long long>(Ft) * D, g.ldc = D;

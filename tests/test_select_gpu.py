@@ -78,7 +78,10 @@ def _select(cfg, stats, k, lam, mode, group=0, flags=0, head_dim=None):
     d = rf.rf_select_desc(L_src=cfg.L_src, F=cfg.F, n_targets=cfg.L_tgt, d_out=cfg.F,
                           head_dim=head_dim or cfg.hd, k=k, n_kinds=nk, group=group, flags=flags)
     wsb = rf.rf_select_workspace_bytes(d)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    # 0xFF bytes are NaN in fp32 and bf16: anything read before the call writes it
+    # (a chosen layer's rows, which the products skip, or the L^-1 planes above the
+    # diagonal tiles) would turn the scores into NaN
+    ws = torch.full((wsb,), 255, dtype=torch.uint8, device=DEV)
     sel = torch.full((cfg.L_tgt, k), -1, dtype=torch.int32, device=DEV)
     r2 = torch.empty((nk, cfg.L_tgt, k, cfg.L_src), dtype=torch.float32, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
