@@ -227,7 +227,8 @@ struct SelGemmProb {
 
 // One split product of the factorisation on square 256 x 256 tiles, for every matrix s
 // of a batch: out_s = alpha · A_s B_sᵀ + beta · C_s with A_s, B_s the h x h blocks of
-// planes [3][batch * h][h] (K-major, matrix s at rows s*h ..). The factors' triangles
+// planes [3][batch * h][h] (K-major, matrix s at rows s*h ..; with kAMN the planes
+// hold A_sᵀ, row k of block s being A_s's column k, read MN-major). The factors' triangles
 // are known, so a unit computes only the output tiles that are read later and only
 // the K-range where both operands can be nonzero (whole 256-wide tiles of zeros
 // skipped, so the sums are those of the full product up to the fp32 chunking):
@@ -243,6 +244,7 @@ enum { kKAll = 0, kKUpToN = 1, kKUpToM = 2, kKFromM = 3, kKFromN = 4 };
 constexpr int kTriChunk = 512;
 
 // CTA pairs only: their 256 x 256 unit is square (a single CTA's is 128 x 256).
+template <bool kAMN_>
 struct TriGemmProb {
   CUtensorMap tmA;
   CUtensorMap tmB;
@@ -256,7 +258,7 @@ struct TriGemmProb {
   int* sched;  // unit counter (dynamic unit order), or nullptr for round-robin dealing
   int32_t* dev_status;
   uint64_t timeout_ns;
-  static constexpr bool kAMN = false;
+  static constexpr bool kAMN = kAMN_;
   static constexpr bool kBMN = false;
   static constexpr bool kPair = true;
   static constexpr int kEpiWarps = 8;
@@ -321,6 +323,7 @@ struct TriGemmProb {
   }
   struct Coords {
     int a_row, b_row, k0;
+    int a_k0;  // kAMN: A's plane row of K offset k0 (a_row is then A's M offset)
   };
   __device__ Coords coords(int u, int sb, uint32_t rank) const {
     int s, mt, nt, lo, hi;
@@ -328,15 +331,18 @@ struct TriGemmProb {
     k_range(mt, nt, lo, hi);
     const int c = sb / 6, t = 5 - (sb - 6 * c);
     Coords r;
-    r.a_row = static_cast<int>(sel_term_a(t) * plane_rows + static_cast<long long>(s) * h +
-                               static_cast<long long>(mt) * Cfg::kUnitM + rank * kBM);
+    const int m0 = mt * Cfg::kUnitM + static_cast<int>(rank) * kBM;
+    const int a_block = static_cast<int>(sel_term_a(t) * plane_rows + static_cast<long long>(s) * h);
+    r.a_row = kAMN ? m0 : a_block + m0;
     r.b_row = static_cast<int>(sel_term_b(t) * plane_rows + static_cast<long long>(s) * h +
                                static_cast<long long>(nt) * kBN + rank * Cfg::kBRows);
     r.k0 = lo + c * kTriChunk;
+    if (kAMN) r.a_k0 = a_block + r.k0;
     return r;
   }
   __device__ void issue_loads(Coords& c, int kb, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
-    load_operand<kBM, false, kPair>(sa, &tmA, bar, c.k0 + kb * kBK, c.a_row);
+    if constexpr (kAMN) load_operand<kBM, true, kPair>(sa, &tmA, bar, c.a_k0 + kb * kBK, c.a_row);
+    else load_operand<kBM, false, kPair>(sa, &tmA, bar, c.k0 + kb * kBK, c.a_row);
     load_operand<Cfg::kBRows, false, kPair>(sb, &tmB, bar, c.k0 + kb * kBK, c.b_row);
   }
   __device__ void epilogue(EpiState& es, int, int sb, int, uint32_t tacc, int, int, uint32_t) const {
@@ -835,11 +841,13 @@ static SelOperand op(long long q_rows, long long s_rows, long long b_rows, long 
 // out_s = alpha · A_s B_sᵀ + beta · C_s for the batch's h x h blocks (planes pa, pb:
 // [3][batch * h][h]) with the factors' triangles skipped (TriGemmProb); on single
 // CTAs, or for h not a multiple of 256, the plain split product over every tile and K.
-static rf_status tri_gemm(SelCtx& c, const __nv_bfloat16* pa, const __nv_bfloat16* pb, int batch, int h,
-                          int tile_mode, int k_mode, float alpha, float beta, float* out, long long o_s,
-                          long long ldo, const float* csrc, long long c_s, long long ldc, int stage) {
+template <bool kAMN>
+static rf_status tri_gemm_t(SelCtx& c, const __nv_bfloat16* pa, const __nv_bfloat16* pb, int batch, int h,
+                            int tile_mode, int k_mode, float alpha, float beta, float* out, long long o_s,
+                            long long ldo, const float* csrc, long long c_s, long long ldc, int stage) {
   const long long rows = static_cast<long long>(batch) * h;
   if (!c.pair || h % kBN != 0) {
+    if (kAMN) return fail(RF_ERR_SHAPE, "MN-major factorisation product needs CTA pairs and h %% 256 == 0");
     SelGemm g{};
     g.pa = pa, g.a_rows = rows, g.a_kext = h, g.a = op(0, h, 0, 0, 0, 0);
     g.pb = pb, g.b_rows = rows, g.b_kext = h, g.b = op(0, h, 0, 0, 0, 0);
@@ -850,9 +858,9 @@ static rf_status tri_gemm(SelCtx& c, const __nv_bfloat16* pa, const __nv_bfloat1
     return sel_gemm(c, g);
   }
   using Cfg = GemmCfg<true>;
-  TriGemmProb pr;
+  TriGemmProb<kAMN> pr;
   rf_status st;
-  if ((st = make_tmap_bf16_2d(&pr.tmA, pa, h, 3 * rows, h, kBK, kBM)) != RF_OK) return st;
+  if ((st = make_tmap_bf16_2d(&pr.tmA, pa, h, 3 * rows, h, kAMN ? 64 : kBK, kAMN ? kBK : kBM)) != RF_OK) return st;
   if ((st = make_tmap_bf16_2d(&pr.tmB, pb, h, 3 * rows, h, kBK, Cfg::kBRows)) != RF_OK) return st;
   pr.plane_rows = rows;
   pr.h = h;
@@ -873,6 +881,12 @@ static rf_status tri_gemm(SelCtx& c, const __nv_bfloat16* pa, const __nv_bfloat1
   pr.timeout_ns = wait_timeout_ns();
   ProfScope prof(c.s, stage);
   return launch_gemm(pr, static_cast<int64_t>(batch) * pr.tiles, c.sms, c.s, "factorisation product launch");
+}
+
+static rf_status tri_gemm(SelCtx& c, const __nv_bfloat16* pa, const __nv_bfloat16* pb, int batch, int h,
+                          int tile_mode, int k_mode, float alpha, float beta, float* out, long long o_s,
+                          long long ldo, const float* csrc, long long c_s, long long ldc, int stage) {
+  return tri_gemm_t<false>(c, pa, pb, batch, h, tile_mode, k_mode, alpha, beta, out, o_s, ldo, csrc, c_s, ldc, stage);
 }
 
 static SelOperand op(long long q_rows, long long s_rows, long long b_rows, long long k0, long long s_k,
@@ -951,11 +965,19 @@ static rf_status sel_factor(SelCtx& c, const FactorScratch& lay, float* A, long 
   if ((st = tri_gemm(c, lay.fpa, lay.fpa, batch, h, kTriLower, kKAll, -1.f, 1.f, A22, sA, lda, A22, sA, lda, fs)) !=
       RF_OK)
     return st;
-  // Tᵀ = W11ᵀ L21ᵀ, kept in A21's storage (W11ᵀ's row m is zero below k = m)
-  if ((st = split_blocks(c, W, ldw, sW, h, h, batch, lay.fpb, true)) != RF_OK) return st;
-  if ((st = tri_gemm(c, lay.fpb, lay.fpa, batch, h, kTriAll, kKFromM, 1.f, 0.f, A21, sA, lda, nullptr, 0, 0, fs)) !=
-      RF_OK)
-    return st;
+  // Tᵀ = W11ᵀ L21ᵀ, kept in A21's storage (W11ᵀ's row m is zero below k = m). On the
+  // triangle-skipping kernel W11ᵀ is read MN-major from W11's planes, still in fpb
+  // from L21's product; otherwise W11 is split again, transposed.
+  if (c.pair && h % kBN == 0) {
+    if ((st = tri_gemm_t<true>(c, lay.fpb, lay.fpa, batch, h, kTriAll, kKFromM, 1.f, 0.f, A21, sA, lda, nullptr, 0,
+                               0, fs)) != RF_OK)
+      return st;
+  } else {
+    if ((st = split_blocks(c, W, ldw, sW, h, h, batch, lay.fpb, true)) != RF_OK) return st;
+    if ((st = tri_gemm(c, lay.fpb, lay.fpa, batch, h, kTriAll, kKFromM, 1.f, 0.f, A21, sA, lda, nullptr, 0, 0, fs)) !=
+        RF_OK)
+      return st;
+  }
   if ((st = sel_factor(c, lay, A22, lda, sA, W22, ldw, sW, h, batch, stmp)) != RF_OK) return st;
   // W21 = −W22 T (W22 lower triangular: k <= m)
   if ((st = split_blocks(c, W22, ldw, sW, h, h, batch, lay.fpa, false)) != RF_OK) return st;
