@@ -1103,19 +1103,23 @@ def run_selection(dev, peak_tflops, flags=0, n_targets=0, n_sources=0):
                                                      status, ws, wsb), 1, stream)
     assert int(status.item()) == 0
     # fp32-accurate products (each is six bf16 plane products on the tensor cores):
-    # per pass of Q problems and step j (m = jF features chosen), the scores of all
-    # L_src candidates (2 D F Ft), and for j < k-1 the new factor column
-    # (2 D F m + 2 D F²), the Schur-block and cross-term updates (2 D F² + 2 Ft F D)
-    # and z_b (2 Ft F²). The scores, z_b and the new column's "× L_b^-ᵀ" multiply by
-    # a lower-triangular L^-1: algorithmically (F+1)/2F of a full product, and the
-    # kernel runs the tiles up to each column tile's diagonal, (T+1)/2T with T = F/256.
+    # per pass of Q problems and step j (m = jF features chosen), the scores of the
+    # L_src - j candidates left (2 D F Ft over those layers), and for j < k-1 z_b
+    # (2 Ft F²) and, over the L_src - j - 1 layers left once b is chosen, the new
+    # factor column (2 D F m + 2 D F²) and the Schur-block and cross-term updates
+    # (2 D F² + 2 Ft F D); the chosen layers' units run nothing. The scores, z_b and
+    # the new column's "× L_b^-ᵀ" multiply by a lower-triangular L^-1: algorithmically
+    # (F+1)/2F of a full product, and the kernel runs the tiles up to each column
+    # tile's diagonal, (T+1)/2T with T = F/256.
     n_prob = 2 * T
+    L = cfg.L_src
     tri_alg, tri_exec = (F + 1) / (2.0 * F), (F // 256 + 1) / (2.0 * (F // 256))
     prod, prod_exec = 0.0, 0.0
     for j in range(cfg.k):
         m = j * F
-        full = 2.0 * D * F * m + 2.0 * D * F * F + 2.0 * F * F * D if j < cfg.k - 1 else 0.0
-        tri = 2.0 * D * F * F + (2.0 * D * F * F + 2.0 * F * F * F if j < cfg.k - 1 else 0.0)
+        left, after = (L - j) / L, (L - j - 1) / L
+        full = (2.0 * D * F * m + 2.0 * D * F * F + 2.0 * F * F * D) * after if j < cfg.k - 1 else 0.0
+        tri = 2.0 * D * F * F * left + ((2.0 * D * F * F * after + 2.0 * F * F * F) if j < cfg.k - 1 else 0.0)
         prod += full + tri_alg * tri
         prod_exec += full + tri_exec * tri
     prod *= n_prob
