@@ -84,6 +84,10 @@ struct SelGemmProb {
   int q_per_kind;
   // sum of squares: part[(p*M + m)*2*n_tiles + 2*nt + half] = Σ (alpha·acc)² over 128 columns
   float* part;
+  // or the result as three bf16 planes (split3 of alpha·acc + beta·C): element
+  // (q, m, n) of plane j at po + j*po_plane + q*po_q + m*po_ld + po_col + n
+  __nv_bfloat16* po;
+  long long po_plane, po_q, po_ld, po_col;
   // B lower triangular in (row n, column k), an L^-1: tile column nt reads only
   // k < 256 (nt + 1), the rest of its K range being exact zeros
   int b_tri;
@@ -205,6 +209,34 @@ struct SelGemmProb {
       }
       const long long p = static_cast<long long>(q) * nS + s;
       part[(p * M + m) * (2 * n_tiles) + 2 * nt + col0 / kCols] = ss;
+      return;
+    }
+    if (po != nullptr) {
+      const float4* cp = beta != 0.f ? reinterpret_cast<const float4*>(c_row(u, row, col0, rank)) : nullptr;
+      __nv_bfloat16* d = po + q * po_q + m * po_ld + po_col + n0;
+#pragma unroll
+      for (int i = 0; i < kCols / 8; ++i) {
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = alpha * es.rs[8 * i + e];
+        if (cp != nullptr) {
+          const float4 c0 = cp[2 * i], c1 = cp[2 * i + 1];
+          v[0] = fmaf(beta, c0.x, v[0]);
+          v[1] = fmaf(beta, c0.y, v[1]);
+          v[2] = fmaf(beta, c0.z, v[2]);
+          v[3] = fmaf(beta, c0.w, v[3]);
+          v[4] = fmaf(beta, c1.x, v[4]);
+          v[5] = fmaf(beta, c1.y, v[5]);
+          v[6] = fmaf(beta, c1.z, v[6]);
+          v[7] = fmaf(beta, c1.w, v[7]);
+        }
+        __align__(16) __nv_bfloat16 hi[8], mi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) split3(v[e], hi[e], mi[e], lo[e]);
+        *reinterpret_cast<uint4*>(d + 8 * i) = *reinterpret_cast<const uint4*>(hi);
+        *reinterpret_cast<uint4*>(d + po_plane + 8 * i) = *reinterpret_cast<const uint4*>(mi);
+        *reinterpret_cast<uint4*>(d + 2 * po_plane + 8 * i) = *reinterpret_cast<const uint4*>(lo);
+      }
       return;
     }
     float4* o = reinterpret_cast<float4*>(out + q * o_q + s * o_s + m * ldo + n0);
@@ -628,17 +660,29 @@ __global__ void __launch_bounds__(256) k_sel_choose(const double* __restrict__ s
 }
 
 // X[q][i][f] = H_kind[i][b_q F + f]: the first block column of the factor's input.
+// Written straight as the three bf16 planes Xp [3][Q*D][F] (plane stride Q*D*F).
 __global__ void __launch_bounds__(256) k_sel_copy_hcols(const float* __restrict__ H, const int32_t* __restrict__ chosen,
-                                                        int G, int Q, long long D, int F, float* __restrict__ X) {
+                                                        int G, int Q, long long D, int F,
+                                                        __nv_bfloat16* __restrict__ Xp) {
   const long long per = D * F / 4;
   const long long total = per * Q;
+  const long long plane = total * 4;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int q = static_cast<int>(i / per);
     const long long e = (i - q * per) * 4;
     const long long r = e / F, c = e - r * F;
     const float* src = H + static_cast<long long>(q / G) * D * D + r * D + static_cast<long long>(chosen[q]) * F + c;
-    *reinterpret_cast<float4*>(X + static_cast<long long>(q) * D * F + e) = *reinterpret_cast<const float4*>(src);
+    const float4 v = *reinterpret_cast<const float4*>(src);
+    __align__(8) __nv_bfloat16 h[4], m[4], l[4];
+    split3(v.x, h[0], m[0], l[0]);
+    split3(v.y, h[1], m[1], l[1]);
+    split3(v.z, h[2], m[2], l[2]);
+    split3(v.w, h[3], m[3], l[3]);
+    __nv_bfloat16* d = Xp + static_cast<long long>(q) * D * F + e;
+    *reinterpret_cast<uint2*>(d) = *reinterpret_cast<const uint2*>(h);
+    *reinterpret_cast<uint2*>(d + plane) = *reinterpret_cast<const uint2*>(m);
+    *reinterpret_cast<uint2*>(d + 2 * plane) = *reinterpret_cast<const uint2*>(l);
   }
 }
 
@@ -664,8 +708,7 @@ struct SelLayout {
   float* part;      // [Qmax * Ls][Ft][2 F / 256]
   float* zb;        // [Qmax][Ft][F]
   __nv_bfloat16* zbp;  // [3][Qmax * Ft][F]
-  float* X;         // [Qmax][D][F]
-  __nv_bfloat16* Xp;  // [3][Qmax * D][F]
+  __nv_bfloat16* Xp;  // [3][Qmax * D][F]  the new block column's planes
   double* tss;      // [Qmax][Ft]
   double* expl;     // [Qmax][Ft]
   double* scores;   // [Gmax][n_kinds][Ls] this step's layer scores
@@ -704,7 +747,6 @@ static SelLayout sel_layout(const rf_select_desc* d, void* ws) {
   l.part = c.take<float>(Q * Ls * Ft * 2 * (F / kBN));
   l.zb = c.take<float>(Q * Ft * F);
   l.zbp = c.take<__nv_bfloat16>(3 * Q * Ft * F);
-  l.X = c.take<float>(Q * D * F);
   l.Xp = c.take<__nv_bfloat16>(3 * Q * D * F);
   l.tss = c.take<double>(Q * Ft);
   l.expl = c.take<double>(Q * Ft);
@@ -771,6 +813,8 @@ struct SelGemm {
   long long c_kind = 0, c_b = 0, c_q = 0, c_s = 0, ldc = 0;
   int q_per_kind = 1;
   float* part = nullptr;
+  __nv_bfloat16* po = nullptr;  // result as bf16 planes instead of `out`
+  long long po_plane = 0, po_q = 0, po_ld = 0, po_col = 0;
   bool b_tri = false;  // B is an L^-1 (lower triangular in row, K): skip its zero K range
   bool m_inner = false;  // M tiles innermost in the unit order (N >> M)
   int skip = kSkipNone;  // which layer index marks a unit of an already chosen layer
@@ -813,6 +857,11 @@ static rf_status run_sel_gemm(SelCtx& c, const SelGemm& g) {
   pr.ldc = g.ldc;
   pr.q_per_kind = g.q_per_kind;
   pr.part = g.part;
+  pr.po = g.po;
+  pr.po_plane = g.po_plane;
+  pr.po_q = g.po_q;
+  pr.po_ld = g.po_ld;
+  pr.po_col = g.po_col;
   pr.b_tri = g.b_tri ? 1 : 0;
   pr.m_inner = g.m_inner ? 1 : 0;
   pr.skip = g.mask != nullptr ? g.skip : kSkipNone;
@@ -1140,10 +1189,10 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
         if ((st = sel_gemm(c, g)) != RF_OK) return st;
       }
       if ((st = split_rows(c, lay.zb, F, lay.zbp, F, 0, rtrows * F, rtrows, F)) != RF_OK) return st;
-      // X = H[:, b] − W W_bᵀ
+      // X = H[:, b] − W W_bᵀ, written as its planes Xp
       if (j == 0) {
         ProfScope pf(c.s, RF_STAGE_SELECT_SCORE);
-        k_sel_copy_hcols<<<eb, 256, 0, c.s>>>(lay.H, lay.chosen, G, Q, D, F, lay.X);
+        k_sel_copy_hcols<<<eb, 256, 0, c.s>>>(lay.H, lay.chosen, G, Q, D, F, lay.Xp);
         if ((st = cuda_check(cudaGetLastError(), "k_sel_copy_hcols launch")) != RF_OK) return st;
       } else {
         SelGemm g{};
@@ -1152,22 +1201,20 @@ extern "C" rf_status rf_select_sources(const rf_select_desc* desc, const rf_cali
         g.chosen = lay.chosen, g.Q = Q, g.M = static_cast<int>(D), g.N = F, g.K = static_cast<int>(m);
         g.mask = lay.mask, g.mask_g = G, g.mask_ls = Ls, g.layer_f = F, g.skip = kSkipMRows;
         g.alpha = -1.f, g.beta = 1.f;
-        g.out = lay.X, g.o_q = D * F, g.ldo = F;
+        g.po = lay.Xp, g.po_plane = wrows * F, g.po_q = D * F, g.po_ld = F, g.po_col = 0;
         g.csrc = lay.H, g.c_kind = D * D, g.c_b = F, g.ldc = D, g.q_per_kind = G;
         if ((st = sel_gemm(c, g)) != RF_OK) return st;
       }
-      if ((st = split_rows(c, lay.X, F, lay.Xp, F, 0, wrows * F, wrows, F)) != RF_OK) return st;
-      // w = X L_b^-ᵀ  (the new block column of every layer), then into the W planes
+      // w = X L_b^-ᵀ  (the new block column of every layer), written into the W planes
       {
         SelGemm g{};
         g.pa = lay.Xp, g.a_rows = wrows, g.a_kext = F, g.a = op(D, 0, 0, 0, 0, 0);
         g.pb = lay.Lp, g.b_rows = lrows, g.b_kext = F, g.b = op(static_cast<long long>(Ls) * F, 0, F, 0, 0, 0);
         g.chosen = lay.chosen, g.Q = Q, g.M = static_cast<int>(D), g.N = F, g.K = F, g.b_tri = true;
         g.mask = lay.mask, g.mask_g = G, g.mask_ls = Ls, g.layer_f = F, g.skip = kSkipMRows;
-        g.out = lay.X, g.o_q = D * F, g.ldo = F;
+        g.po = lay.Wp, g.po_plane = wrows * m_max, g.po_q = D * m_max, g.po_ld = m_max, g.po_col = m;
         if ((st = sel_gemm(c, g)) != RF_OK) return st;
       }
-      if ((st = split_rows(c, lay.X, F, lay.Wp, m_max, m, wrows * m_max, wrows, F)) != RF_OK) return st;
       // Σ_s −= w_s w_sᵀ for every (q, s)
       {
         SelGemm g{};
