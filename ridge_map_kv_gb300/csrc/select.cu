@@ -27,15 +27,15 @@
 //   k_sel_layer_scores       every (target, kind, layer)'s score and its table entry
 //   k_sel_choose             the joint argmax, the choice, e += gain
 //   SelGemm                  z_bᵀ;  H[:, b] − W W_bᵀ;  × L_b^-ᵀ;  Σ_s −= w wᵀ;
-//                            Rᵀ −= z_bᵀ wᵀ
+//                            Rᵀ −= z_bᵀ wᵀ  (the units of chosen layers run nothing)
 // Every product is fp32-accurate on the bf16 tensor cores: each fp32 operand is
-// split into three bf16 planes (k_split_rows) and the six plane products that
-// matter at fp32 precision are summed: per 1024-wide K chunk the six terms run as
-// one TMEM accumulation, smallest first, and the chunks add in fp32 registers.
-// Operands are K-major rows of the planes;
-// which rows and columns a batch entry reads is linear in (term, problem, layer
-// slot, chosen layer), the chosen layer read on the device, so no step waits on
-// the host.
+// split into three bf16 planes (by k_split_rows, or by the epilogue of the product
+// that makes it: the new block column and its × L_b^-ᵀ) and the six plane products
+// that matter at fp32 precision are summed: per 1024-wide K chunk the six terms run
+// as one TMEM accumulation, smallest first, and the chunks add in fp32 registers.
+// Operands are K-major rows of the planes; which rows and columns a batch entry
+// reads is linear in (term, problem, layer slot, chosen layer), the chosen layer
+// read on the device, so no step waits on the host.
 #include <algorithm>
 #include <cmath>
 
