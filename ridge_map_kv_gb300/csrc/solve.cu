@@ -508,28 +508,52 @@ __device__ __forceinline__ double half_of(double v) {
 }
 
 // H = (G + Gᵀ)/2 − n μ_x μ_xᵀ + αI, stored in fp32 and (when H64 is set) fp64.
-// Block (bx, by) writes rows by*32.., columns bx*32.. and reads Gᵀ's matching tile
-// through shared memory, so both reads are row-contiguous. 32 x 8 threads. Per
-// element one fp64 addition and one fma (GB300's fp64 rate is low): the row
-// factors n μ_x[r] are formed once per tile and the halving is an exponent shift.
+// Block (bx, by) with bx <= by takes the tile pair P = G[rows by*32.., columns
+// bx*32..] and Q = G[rows bx*32.., columns by*32..] through shared memory (row-
+// contiguous reads) and writes both H tiles, so every element of G is read once
+// (the diagonal tiles alone: P = Q); blocks with bx > by return at once. 32 x 8
+// threads. Per element one fp64 addition and one fma (GB300's fp64 rate is low):
+// the row factors n μ_x[r] are formed once per tile and the halving is an
+// exponent shift.
 __global__ void __launch_bounds__(256) k_build_h(const double* __restrict__ G, const double* __restrict__ mu_x,
                                                  const double* __restrict__ n, const double* __restrict__ alpha,
                                                  int d_in, double* __restrict__ H64, float* __restrict__ H32) {
-  __shared__ double t[32][33];
-  __shared__ double u[32];
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  for (int j = threadIdx.y; j < 32; j += 8)
-    t[j][threadIdx.x] = G[static_cast<size_t>(c0 + j) * d_in + r0 + threadIdx.x];  // G[c0 + j][r0 + x]
-  if (threadIdx.y == 0) u[threadIdx.x] = *n * mu_x[r0 + threadIdx.x];
-  __syncthreads();
-  const double a = *alpha;
-  const int c = c0 + threadIdx.x;
-  const double mc = mu_x[c];
+  const int bx = blockIdx.x, by = blockIdx.y;
+  if (bx > by) return;
+  __shared__ double p[32][33];  // p[j][x] = G[r0 + j][c0 + x]
+  __shared__ double q[32][33];  // q[j][x] = G[c0 + j][r0 + x]
+  __shared__ double ur[32], uc[32], mr[32], mc[32];
+  const int c0 = bx * 32, r0 = by * 32;
+  const bool diag = bx == by;
   for (int j = threadIdx.y; j < 32; j += 8) {
-    const int r = r0 + j;
+    p[j][threadIdx.x] = G[static_cast<size_t>(r0 + j) * d_in + c0 + threadIdx.x];
+    if (!diag) q[j][threadIdx.x] = G[static_cast<size_t>(c0 + j) * d_in + r0 + threadIdx.x];
+  }
+  if (threadIdx.y == 0) {
+    const double nn = *n, a = mu_x[r0 + threadIdx.x], b = mu_x[c0 + threadIdx.x];
+    mr[threadIdx.x] = a;
+    mc[threadIdx.x] = b;
+    ur[threadIdx.x] = nn * a;
+    uc[threadIdx.x] = nn * b;
+  }
+  __syncthreads();
+  const double al = *alpha;
+  const double (*qq)[33] = diag ? p : q;
+  // H[r0 + j][c0 + x] from G[r0 + j][c0 + x] + G[c0 + x][r0 + j]
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int r = r0 + j, c = c0 + threadIdx.x;
     const size_t e = static_cast<size_t>(r) * d_in + c;
-    double h = fma(-u[j], mc, half_of(G[e] + t[threadIdx.x][j]));
-    if (r == c) h += a;
+    double h = fma(-ur[j], mc[threadIdx.x], half_of(p[j][threadIdx.x] + qq[threadIdx.x][j]));
+    if (r == c) h += al;
+    if (H64 != nullptr) H64[e] = h;
+    H32[e] = f64_to_f32_rn(h);
+  }
+  if (diag) return;
+  // H[c0 + j][r0 + x] from G[c0 + j][r0 + x] + G[r0 + x][c0 + j]
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int r = c0 + j, c = r0 + threadIdx.x;
+    const size_t e = static_cast<size_t>(r) * d_in + c;
+    const double h = fma(-uc[j], mr[threadIdx.x], half_of(q[j][threadIdx.x] + p[threadIdx.x][j]));
     if (H64 != nullptr) H64[e] = h;
     H32[e] = f64_to_f32_rn(h);
   }
